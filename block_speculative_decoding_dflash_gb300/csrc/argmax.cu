@@ -1,0 +1,332 @@
+// Argmax-producing kernels: the split-vocabulary lm_head + softcap + argmax,
+// the target-logit argmax + greedy prefix accept, and the Markov chain step.
+//
+// All three reduce (value, index) pairs first inside a CTA and then across
+// CTAs with the "last CTA done" pattern: every CTA writes its partial, fences,
+// and takes a ticket from an atomic counter; the CTA that draws the last
+// ticket reduces all partials and resets the counter. No CTA ever waits on
+// another. The (larger value, then lower index) rule does not depend on the
+// order partials arrive in, so results are deterministic.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kLmWarps = 8;
+constexpr int kLmNR = 4;       // vocab rows per warp step
+
+// True in every thread of the CTA that drew the last ticket.
+__device__ __forceinline__ bool last_cta(unsigned* counter, unsigned total) {
+  __shared__ bool is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(counter, 1u) == total - 1);
+  __syncthreads();
+  if (is_last) __threadfence();
+  return is_last;
+}
+
+template <typename T, int MT>
+__global__ void __launch_bounds__(kLmWarps * 32) lmhead_kernel(LmHeadArgs a) {
+  extern __shared__ __align__(16) unsigned char lm_smem[];
+  T* xs = reinterpret_cast<T*>(lm_smem);                  // [MT][H]
+  __shared__ float best_v[kLmWarps][MT];
+  __shared__ int best_i[kLmWarps][MT];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  const long long v0 = (long long)a.V * b / a.grid;
+  const long long v1 = (long long)a.V * (b + 1) / a.grid;
+  const T* W = reinterpret_cast<const T*>(a.w);
+  const T* X = reinterpret_cast<const T*>(a.x);
+  const float cap = a.softcap;
+  const float inv_cap = cap > 0.f ? 1.0f / cap : 0.f;
+
+  for (int m0 = 0; m0 < a.R; m0 += MT) {
+    const int mr = min(MT, a.R - m0);
+    for (int e = threadIdx.x * 8; e < MT * a.H; e += blockDim.x * 8) {
+      const int m = e / a.H, k = e % a.H;
+      if (m < mr) {
+        const uint4* src = reinterpret_cast<const uint4*>(X + (size_t)(m0 + m) * a.ldx + k);
+        uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)m * a.H + k);
+        dst[0] = src[0];
+        if (sizeof(T) == 4) dst[1] = src[1];
+      }
+    }
+    __syncthreads();
+    float bv[MT];
+    int bi[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) { bv[m] = -INFINITY; bi[m] = 0x7fffffff; }
+
+    for (long long v = v0 + (long long)warp * kLmNR; v < v1; v += kLmWarps * kLmNR) {
+      const int nr = static_cast<int>(min((long long)kLmNR, v1 - v));
+      float acc[kLmNR][MT];
+#pragma unroll
+      for (int r = 0; r < kLmNR; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+      for (int k = lane * 8; k < a.H; k += 32 * 8) {
+        float w[kLmNR][8];
+#pragma unroll
+        for (int r = 0; r < kLmNR; ++r) {
+          if (r < nr) {
+            load8_stream(W + (size_t)(v + r) * a.H + k, w[r]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w[r][q] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < mr) {
+            float xv[8];
+            load8(xs + (size_t)m * a.H + k, xv);
+#pragma unroll
+            for (int r = 0; r < kLmNR; ++r) {
+              float s = acc[r][m];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) s = fmaf(w[r][q], xv[q], s);
+              acc[r][m] = s;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kLmNR; ++r) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          float z = warp_sum(acc[r][m]);
+          if (r < nr && m < mr) {
+            if (cap > 0.f) z = cap * tanhf(z * inv_cap);
+            const int vi = static_cast<int>(v + r);
+            if (a.logits != nullptr && lane == 0) a.logits[(size_t)(m0 + m) * a.V + vi] = z;
+            if (better(z, vi, bv[m], bi[m])) { bv[m] = z; bi[m] = vi; }
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) { best_v[warp][m] = bv[m]; best_i[warp][m] = bi[m]; }
+    }
+    __syncthreads();
+    if (threadIdx.x < mr) {
+      const int m = threadIdx.x;
+      float v = best_v[0][m];
+      int i = best_i[0][m];
+      for (int w = 1; w < kLmWarps; ++w)
+        if (better(best_v[w][m], best_i[w][m], v, i)) { v = best_v[w][m]; i = best_i[w][m]; }
+      a.part_v[(size_t)b * a.R + m0 + m] = v;
+      a.part_i[(size_t)b * a.R + m0 + m] = i;
+    }
+    __syncthreads();
+  }
+
+  if (last_cta(a.counter, gridDim.x)) {
+    for (int m = threadIdx.x; m < a.R; m += blockDim.x) {
+      float v = -INFINITY;
+      int i = 0x7fffffff;
+      for (int c = 0; c < a.grid; ++c) {
+        const float cv = __ldcg(a.part_v + (size_t)c * a.R + m);
+        const int ci = __ldcg(a.part_i + (size_t)c * a.R + m);
+        if (better(cv, ci, v, i)) { v = cv; i = ci; }
+      }
+      a.ids[m] = i;
+      if (a.ids2) a.ids2[m] = i;
+      a.maxv[m] = v;
+    }
+    if (threadIdx.x == 0) *a.counter = 0u;
+  }
+}
+
+template <typename T, int MT>
+cudaError_t lm_launch(const LmHeadArgs& a, cudaStream_t st) {
+  const size_t smem = (size_t)MT * a.H * sizeof(T);
+  lmhead_kernel<T, MT><<<a.grid, kLmWarps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t lm_dispatch(const LmHeadArgs& a, cudaStream_t st) {
+  if (a.R <= 1) return lm_launch<T, 1>(a, st);
+  if (a.R <= 2) return lm_launch<T, 2>(a, st);
+  if (a.R <= 4) return lm_launch<T, 4>(a, st);
+  if (a.R <= 8) return lm_launch<T, 8>(a, st);
+  return lm_launch<T, 16>(a, st);
+}
+
+template <typename T, int MT>
+cudaError_t lm_attr(int H) {
+  return cudaFuncSetAttribute(lmhead_kernel<T, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)((size_t)MT * H * sizeof(T)));
+}
+
+// ---- verify: target argmax per row + greedy accept ------------------------------------
+constexpr int kVerifyChunk = 8192;
+constexpr int kMaxVerifyRows = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
+  __shared__ float sv[8];
+  __shared__ int si[8];
+  __shared__ int t_s[kMaxVerifyRows];
+  const int i = blockIdx.y, c = blockIdx.x;
+  const T* row = reinterpret_cast<const T*>(a.L) + (size_t)i * a.V;
+  const int v0 = c * kVerifyChunk;
+  const int v1 = min(a.V, v0 + kVerifyChunk);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const float z = to_f(row[v]);
+    if (better(z, v, bv, bi)) { bv = z; bi = v; }
+  }
+  warp_argmax(bv, bi);
+  if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = bv; si[threadIdx.x >> 5] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bv = sv[0];
+    bi = si[0];
+    for (int w = 1; w < 8; ++w)
+      if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+    a.part_v[(size_t)i * a.chunks + c] = bv;
+    a.part_i[(size_t)i * a.chunks + c] = bi;
+  }
+  if (last_cta(a.counter, gridDim.x * gridDim.y)) {
+    for (int r = threadIdx.x; r < a.B; r += blockDim.x) {
+      float v = -INFINITY;
+      int idx = 0x7fffffff;
+      for (int q = 0; q < a.chunks; ++q) {
+        const float cv = __ldcg(a.part_v + (size_t)r * a.chunks + q);
+        const int ci = __ldcg(a.part_i + (size_t)r * a.chunks + q);
+        if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
+      }
+      t_s[r] = idx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      while (acc < a.B - 1 && a.d[acc] == t_s[acc]) ++acc;
+      for (int q = 0; q < a.B; ++q) a.tokens[q] = q < acc ? a.d[q] : (q == acc ? t_s[acc] : -1);
+      *a.n = acc + 1;
+      a.rs->n = acc + 1;
+      a.rs->a = acc;
+      a.rs->bonus = t_s[acc];
+      *a.counter = 0u;
+    }
+  }
+}
+
+// ---- Markov chain step ---------------------------------------------------------------------
+constexpr int kMkThreads = 64;
+constexpr int kMkCols = kMkThreads * 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, int j) {
+  extern __shared__ float w1s[];               // [r]
+  __shared__ float sv[kMkThreads / 32];
+  __shared__ int si[kMkThreads / 32];
+  int prev;
+  if (j == 0) prev = a.anchor_host >= 0 ? a.anchor_host : a.rs->anchor;
+  else prev = a.out[j - 1];
+  if (prev < 0 || prev >= a.V) prev = 0;
+  const T* w1 = reinterpret_cast<const T*>(a.w1) + (size_t)prev * a.r;
+  for (int q = threadIdx.x; q < a.r; q += blockDim.x) w1s[q] = to_f(w1[q]);
+  __syncthreads();
+  const int c = (blockIdx.x * kMkThreads + threadIdx.x) * 8;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if (c < a.V) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const T* w2 = reinterpret_cast<const T*>(a.w2) + c;
+    for (int q = 0; q < a.r; ++q) {
+      float wv[8];
+      load8(w2 + (size_t)q * a.V, wv);
+      const float s = w1s[q];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(s, wv[e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float z = acc[e];
+      if (a.z) z = a.z[(size_t)j * a.ldz + c + e] + z;
+      if (better(z, c + e, bv, bi)) { bv = z; bi = c + e; }
+    }
+  }
+  warp_argmax(bv, bi);
+  if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = bv; si[threadIdx.x >> 5] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bv = sv[0];
+    bi = si[0];
+    for (int w = 1; w < kMkThreads / 32; ++w)
+      if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+    a.part_v[blockIdx.x] = bv;
+    a.part_i[blockIdx.x] = bi;
+  }
+  if (last_cta(a.counter, gridDim.x)) {
+    if (threadIdx.x == 0) {
+      float v = -INFINITY;
+      int idx = 0x7fffffff;
+      for (int q = 0; q < a.grid; ++q) {
+        const float cv = __ldcg(a.part_v + q);
+        const int ci = __ldcg(a.part_i + q);
+        if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
+      }
+      a.out[j] = idx;
+      if (a.out2) a.out2[j] = idx;
+      *a.counter = 0u;
+    }
+  }
+}
+
+}  // namespace
+
+int lmhead_grid(int V) {
+  const int g = (V + 63) / 64;
+  return g < 608 ? g : 608;
+}
+
+int verify_chunks(int V) { return (V + kVerifyChunk - 1) / kVerifyChunk; }
+
+int markov_grid(int V) { return (V + kMkCols - 1) / kMkCols; }
+
+cudaError_t init_lmhead_attrs(int H) {
+  cudaError_t e;
+  if ((e = lm_attr<bf16, 1>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<bf16, 2>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<bf16, 4>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<bf16, 8>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<bf16, 16>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<float, 1>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<float, 2>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<float, 4>(H)) != cudaSuccess) return e;
+  if ((e = lm_attr<float, 8>(H)) != cudaSuccess) return e;
+  return lm_attr<float, 16>(H);
+}
+
+cudaError_t launch_lmhead_argmax(int dtype, const LmHeadArgs& a, cudaStream_t st) {
+  return dtype ? lm_dispatch<bf16>(a, st) : lm_dispatch<float>(a, st);
+}
+
+cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st) {
+  dim3 grid(a.chunks, a.B);
+  if (dtype) verify_kernel<bf16><<<grid, 256, 0, st>>>(a);
+  else verify_kernel<float><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(float) * a.r;
+  for (int j = 0; j < a.gamma; ++j) {
+    if (dtype) markov_step_kernel<bf16><<<a.grid, kMkThreads, smem, st>>>(a, j);
+    else markov_step_kernel<float><<<a.grid, kMkThreads, smem, st>>>(a, j);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace dfl

@@ -1,0 +1,157 @@
+// Host-side launchers of the libdflash kernels (one translation unit per
+// kernel family). Every launcher enqueues on `st` and returns the launch
+// status; none allocates or synchronizes.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dfl {
+
+// ---- linear layers -------------------------------------------------------------
+enum Epi : int {
+  kEpiStore = 0,   // Y = rnd(X W^T)
+  kEpiResid = 1,   // Y = rnd(R + rnd(X W^T)); R may alias Y
+  kEpiSwiglu = 2,  // Y = rnd(silu(rnd(X Wg^T)) * rnd(X Wu^T))
+};
+
+// Up to three weight segments stacked along the output dimension: output
+// columns [seg_end[s-1], seg_end[s]) come from w[s] (its row 0 is column
+// seg_end[s-1]).
+struct LinearArgs {
+  const void* x; int ldx;           // [M, K]
+  const void* w[3]; int seg_end[3]; // [N_s, K] each
+  int nseg;
+  const void* w2;                   // the up weight of kEpiSwiglu ([N, K])
+  const void* r; int ldr;           // residual of kEpiResid
+  void* y; int ldy;                 // [M, N]
+  int M, N, K;
+  int epi;
+};
+// Block rows (any M; 16 rows per weight pass): weight-streaming kernel.
+cudaError_t launch_linear_rows(int dtype, const LinearArgs& a, cudaStream_t st);
+// Many rows (context ingest), kEpiStore only: register-tiled GEMM.
+cudaError_t launch_linear_tiled(int dtype, const LinearArgs& a, cudaStream_t st);
+
+// ---- small per-row kernels -------------------------------------------------------
+// x[r] = E[tok_r] with tok_0 = the device anchor and tok_r = mask for r > 0;
+// also the RoPE table rope[tab_rows][hd/2] = (cos, sin) at ring->offset + r.
+cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab,
+                               RoundState* rs, int mask_id, int rows, void* x,
+                               const RingState* ring, const double* inv_freq,
+                               int half, int tab_rows, float2* rope, cudaStream_t st);
+// RoPE table at positions base + r, base = ring->offset when ring != NULL,
+// else pos0.
+cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,
+                              long long pos0, int rows, float2* rope, cudaStream_t st);
+cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g,
+                           void* y, int ldy, int rows, int H, float eps,
+                           cudaStream_t st);
+// In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
+cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
+                                  int heads, int hd, const void* g, float eps,
+                                  const float2* rope, int neox, cudaStream_t st);
+// kv[rows, 2*nkv*hd] = K heads then V heads: K -> head norm + RoPE -> ring K,
+// V -> ring V, at positions (use_dev ? ring->offset : pos_host) + r.
+// append_only: refuse (and flag) positions at or past base + cap.
+cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows,
+                              int nkv, int hd, const void* kg, float eps,
+                              const float2* rope, int neox, void* ring_k,
+                              void* ring_v, long long cap, int append_only,
+                              RingState* ring, int use_dev, long long pos_host,
+                              cudaStream_t st);
+
+// ---- attention ---------------------------------------------------------------------
+struct AttnArgs {
+  const void* q; int ldq;      // [rows, nq, hd]
+  const void* kb; const void* vb; int ldkv;  // block K/V [rows, nkv, hd]
+  const void* ring_k; const void* ring_v;    // [nkv][cap][hd]
+  long long cap;
+  const RingState* ring;       // offset = position of block row 0
+  int window;                  // <= 0: unbounded
+  int rows, nq, nkv, hd;
+  int max_ctx;                 // most context keys any round can see
+  float* partial;              // scratch [nkv][nsplit][rows*G][hd + 2]
+  void* out; int ldo;          // [rows, nq, hd]
+};
+cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
+size_t attention_scratch_floats(int rows, int nq, int nkv, int hd, int max_ctx);
+cudaError_t init_attention_attrs(int hd);
+
+// ---- lm_head + softcap + argmax ------------------------------------------------------
+struct LmHeadArgs {
+  const void* x; int ldx;      // [R, H] normed rows to read out
+  const void* w;               // [V, H]
+  int R, H, V;
+  float softcap;
+  int* ids;                    // [R] argmax
+  int* ids2;                   // optional second copy of ids (NULL)
+  float* maxv;                 // [R] selected capped logit
+  float* logits;               // optional [R, V] capped fp32 logits (NULL)
+  float* part_v; int* part_i;  // scratch [grid * R]
+  unsigned* counter;           // scratch, zero between launches
+  int grid;
+};
+cudaError_t launch_lmhead_argmax(int dtype, const LmHeadArgs& a, cudaStream_t st);
+int lmhead_grid(int V);
+cudaError_t init_lmhead_attrs(int H);
+
+// ---- verify / commit / Markov / stand-in target ---------------------------------------
+struct VerifyArgs {
+  const void* L;               // [B, V]
+  int B, V;
+  const int* d;                // [B-1]
+  int* tokens;                 // [B]
+  int* n;                      // [1]
+  RoundState* rs;
+  float* part_v; int* part_i;  // scratch [B * chunks]
+  unsigned* counter;
+  int chunks;
+};
+cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st);
+int verify_chunks(int V);
+
+cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
+                          cudaStream_t st);
+// mode 0: append d rows; 1: trim d rows; 2: advance d committed rows.
+cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st);
+cudaError_t launch_ring_reset(RingState* ring, long long base, cudaStream_t st);
+cudaError_t launch_set_anchor(RoundState* rs, int anchor, cudaStream_t st);
+// Copies rows [L, n, nkv, hd] into ring slots at offset + r, then advances.
+cudaError_t launch_ring_append(int dtype, const void* k, const void* v, int L,
+                               int n, int nkv, int hd, void* ring_k, void* ring_v,
+                               long long cap, RingState* ring, cudaStream_t st);
+cudaError_t launch_ring_gather(int dtype, const void* ring_k, const void* ring_v,
+                               int L, long long cap, int nkv, int hd,
+                               long long pos0, int count, void* k_out,
+                               void* v_out, cudaStream_t st);
+
+struct MarkovArgs {
+  const void* w1; const void* w2;  // [V, r], [r, V]
+  int V, r;
+  const RoundState* rs;        // anchor source when anchor_host < 0
+  int anchor_host;
+  const float* z; int ldz;     // optional [gamma, V] fp32
+  int gamma;
+  int* out;                    // [gamma]
+  int* out2;                   // optional second copy
+  float* part_v; int* part_i;  // scratch [grid]
+  unsigned* counter;
+  int grid;
+};
+cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st);
+int markov_grid(int V);
+
+struct SynthArgs {
+  const void* logit_pool; const void* plant; const uint8_t* coins;
+  const void* resid_pool;
+  int n_logit, n_coin, n_resid, block_max, block, V, kin;
+  const int* d;
+  void* logits_out; void* resid_out;
+  const RoundState* rs;
+};
+cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st);
+
+}  // namespace dfl

@@ -1,0 +1,410 @@
+// Per-row kernels of the round: block embedding + RoPE table, RMSNorm,
+// per-head q/k RMSNorm + RoPE, the K/V -> ring write, ring bookkeeping, the
+// commit, and the stand-in target.
+#include "kernels.h"
+
+namespace dfl {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ void copy8(const T* src, T* dst) {
+  if (sizeof(T) == 2) {
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  } else {
+    reinterpret_cast<float4*>(dst)[0] = reinterpret_cast<const float4*>(src)[0];
+    reinterpret_cast<float4*>(dst)[1] = reinterpret_cast<const float4*>(src)[1];
+  }
+}
+
+// (cos, sin) of pos * inv_freq[i]; the angle is formed in fp64 so that large
+// absolute positions keep their precision.
+__device__ __forceinline__ float2 rope_entry(const double* inv_freq, int i, long long pos) {
+  double s, c;
+  sincos(static_cast<double>(pos) * inv_freq[i], &s, &c);
+  return make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+// Block input rows [anchor, mask, ..., mask] from the raw embedding table, and
+// the RoPE table of the block positions p .. p+tab_rows-1.
+template <typename T>
+__global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
+                                   int mask_id, int rows, T* x,
+                                   const RingState* ring, const double* inv_freq,
+                                   int half, int tab_rows, float2* rope) {
+  const int r = blockIdx.x;
+  if (r < rows) {
+    int tok = (r == 0) ? rs->anchor : mask_id;
+    if (tok < 0 || tok >= vocab) {
+      if (threadIdx.x == 0) atomicOr(&rs->error, kErrRange);
+      tok = 0;
+    }
+    const T* src = E + (size_t)tok * H;
+    T* dst = x + (size_t)r * H;
+    for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) copy8(src + i, dst + i);
+  }
+  if (r < tab_rows) {
+    const long long pos = ring->offset + r;
+    for (int i = threadIdx.x; i < half; i += blockDim.x)
+      rope[(size_t)r * half + i] = rope_entry(inv_freq, i, pos);
+  }
+}
+
+__global__ void rope_table_kernel(const double* inv_freq, int half, const RingState* ring,
+                                  long long pos0, int rows, float2* rope) {
+  const int r = blockIdx.x;
+  if (r >= rows) return;
+  const long long base = ring ? ring->offset : pos0;
+  for (int i = threadIdx.x; i < half; i += blockDim.x)
+    rope[(size_t)r * half + i] = rope_entry(inv_freq, i, base + r);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const T* x, int ldx, const T* g,
+                                                     T* y, int ldy, int H, float eps) {
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  const T* xr = x + (size_t)r * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
+    float v[8];
+    load8(xr + i, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / static_cast<float>(H) + eps);
+  T* yr = y + (size_t)r * ldy;
+  for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
+    float v[8], gv[8];
+    load8(xr + i, v);
+    load8(g + i, gv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) yr[i + e] = from_f<T>(v[e] * inv * gv[e]);
+  }
+}
+
+// One warp per (row, head): RMSNorm over hd with gain g[hd], then RoPE with
+// the row's (cos, sin) table; the result is rounded once. src may equal dst.
+template <typename T>
+__device__ __forceinline__ void norm_rope_warp(const T* src, T* dst, int hd,
+                                               const T* g, float eps,
+                                               const float2* rope_row, int neox,
+                                               float* sm) {
+  const int lane = threadIdx.x & 31;
+  float ss = 0.f;
+  for (int d = lane; d < hd; d += 32) {
+    const float v = to_f(src[d]);
+    sm[d] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / static_cast<float>(hd) + eps);
+  __syncwarp();
+  for (int d = lane; d < hd; d += 32) sm[d] = sm[d] * inv * to_f(g[d]);
+  __syncwarp();
+  const int half = hd >> 1;
+  for (int i = lane; i < half; i += 32) {
+    const int ia = neox ? i : 2 * i;
+    const int ib = neox ? i + half : 2 * i + 1;
+    const float2 cs = rope_row[i];
+    const float a = sm[ia], b = sm[ib];
+    dst[ia] = from_f<T>(a * cs.x - b * cs.y);
+    dst[ib] = from_f<T>(a * cs.y + b * cs.x);
+  }
+  __syncwarp();
+}
+
+constexpr int kMaxHd = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(128) head_norm_rope_kernel(T* buf, int ld, int rows,
+                                                             int heads, int hd, const T* g,
+                                                             float eps, const float2* rope,
+                                                             int neox) {
+  __shared__ float sm[4][kMaxHd];
+  const int warp = threadIdx.x >> 5;
+  const int item = blockIdx.x * 4 + warp;
+  if (item >= rows * heads) return;
+  const int r = item / heads, h = item % heads;
+  T* p = buf + (size_t)r * ld + (size_t)h * hd;
+  norm_rope_warp(p, p, hd, g, eps, rope + (size_t)r * (hd >> 1), neox, sm[warp]);
+}
+
+// kv [rows, 2*nkv*hd]: K heads then V heads. K: norm + RoPE into the ring; V:
+// copied into the ring. Ring layout [nkv][cap][hd].
+template <typename T>
+__global__ void __launch_bounds__(128) kv_to_ring_kernel(const T* kv, int ld, int rows,
+                                                         int nkv, int hd, const T* kg,
+                                                         float eps, const float2* rope,
+                                                         int neox, T* ring_k, T* ring_v,
+                                                         long long cap, int append_only,
+                                                         RingState* ring, int use_dev,
+                                                         long long pos_host) {
+  __shared__ float sm[4][kMaxHd];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 4 + warp;
+  if (item >= rows * nkv) return;
+  const int r = item / nkv, h = item % nkv;
+  const long long pos = (use_dev ? ring->offset : pos_host) + r;
+  if (append_only && pos - ring->base >= cap) {
+    if (lane == 0) atomicOr(&ring->error, kErrFull);
+    return;
+  }
+  const long long slot = ring_slot(pos, cap);
+  const T* ksrc = kv + (size_t)r * ld + (size_t)h * hd;
+  const T* vsrc = kv + (size_t)r * ld + (size_t)(nkv + h) * hd;
+  T* kdst = ring_k + ((size_t)h * cap + slot) * hd;
+  T* vdst = ring_v + ((size_t)h * cap + slot) * hd;
+  norm_rope_warp(ksrc, kdst, hd, kg, eps, rope + (size_t)r * (hd >> 1), neox, sm[warp]);
+  for (int d = lane; d < hd; d += 32) vdst[d] = vsrc[d];
+}
+
+// ---- ring bookkeeping ------------------------------------------------------------
+__global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
+  if (mode == 1) {
+    ring->offset -= d;
+    ring->appended = 0;
+  } else {
+    ring->offset += d;
+    if (ring->offset - 1 > ring->hw) ring->hw = ring->offset - 1;
+    ring->appended = (mode == 0) ? ring->appended + d : 0;
+  }
+}
+
+__global__ void ring_reset_kernel(RingState* ring, long long base) {
+  ring->offset = base;
+  ring->base = base;
+  ring->hw = base - 1;
+  ring->appended = 0;
+  ring->error = 0;
+}
+
+__global__ void set_anchor_kernel(RoundState* rs, int anchor) { rs->anchor = anchor; }
+
+// Partial-accept rollback: the block's `block` rows were appended (offset
+// advanced by block); keep the first `keep` (keep < 0: the verify's n).
+__global__ void commit_kernel(RoundState* rs, RingState* ring, int block, int keep) {
+  const int k = keep >= 0 ? keep : rs->n;
+  ring->offset -= (block - k);
+  ring->appended = 0;
+  rs->anchor = rs->bonus;
+  rs->rounds += 1;
+  rs->proposed += block - 1;
+  rs->accepted += rs->a;
+  rs->emitted += rs->a + 1;
+}
+
+template <typename T>
+__global__ void ring_append_kernel(const T* k, const T* v, int L, int n, int nkv,
+                                   int hd, T* ring_k, T* ring_v, long long cap,
+                                   const RingState* ring) {
+  const long long total = (long long)L * n * nkv;
+  for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+    const int h = static_cast<int>(it % nkv);
+    const int j = static_cast<int>((it / nkv) % n);
+    const int l = static_cast<int>(it / ((long long)nkv * n));
+    const long long slot = ring_slot(ring->offset + j, cap);
+    const size_t src = (((size_t)l * n + j) * nkv + h) * hd;
+    const size_t dst = (((size_t)l * nkv + h) * cap + slot) * hd;
+    for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+      ring_k[dst + d] = k[src + d];
+      ring_v[dst + d] = v[src + d];
+    }
+  }
+}
+
+template <typename T>
+__global__ void ring_gather_kernel(const T* ring_k, const T* ring_v, int L,
+                                   long long cap, int nkv, int hd, long long pos0,
+                                   int count, T* k_out, T* v_out) {
+  const long long total = (long long)L * count * nkv;
+  for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+    const int h = static_cast<int>(it % nkv);
+    const int j = static_cast<int>((it / nkv) % count);
+    const int l = static_cast<int>(it / ((long long)nkv * count));
+    const long long slot = ring_slot(pos0 + j, cap);
+    const size_t dst = (((size_t)l * count + j) * nkv + h) * hd;
+    const size_t src = (((size_t)l * nkv + h) * cap + slot) * hd;
+    for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+      k_out[dst + d] = ring_k[src + d];
+      v_out[dst + d] = ring_v[src + d];
+    }
+  }
+}
+
+// ---- stand-in target -------------------------------------------------------------
+template <typename T>
+__global__ void synth_target_kernel(SynthArgs a) {
+  const long long r = a.rs->rounds;
+  const int kl = static_cast<int>(r % a.n_logit);
+  const int kc = static_cast<int>(r % a.n_coin);
+  const int kr = static_cast<int>(r % a.n_resid);
+  const T* L = reinterpret_cast<const T*>(a.logit_pool) + (size_t)kl * a.block_max * a.V;
+  const T* P = reinterpret_cast<const T*>(a.plant) + (size_t)kl * a.block_max;
+  const uint8_t* C = a.coins + (size_t)kc * a.block_max;
+  const T* R = reinterpret_cast<const T*>(a.resid_pool) + (size_t)kr * a.block_max * a.kin;
+  T* Lo = reinterpret_cast<T*>(a.logits_out);
+  T* Ro = reinterpret_cast<T*>(a.resid_out);
+  const long long nl = (long long)a.block * a.V;
+  const long long nr = (long long)a.block * a.kin;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nl + nr; e += stride) {
+    if (e < nl) {
+      const int i = static_cast<int>(e / a.V);
+      const int v = static_cast<int>(e % a.V);
+      T val = L[(size_t)i * a.V + v];
+      if (i < a.block - 1 && C[i] && a.d[i] == v) val = P[i];
+      Lo[e] = val;
+    } else {
+      Ro[e - nl] = R[e - nl];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab, RoundState* rs,
+                               int mask_id, int rows, void* x, const RingState* ring,
+                               const double* inv_freq, int half, int tab_rows, float2* rope,
+                               cudaStream_t st) {
+  const int grid = rows > tab_rows ? rows : tab_rows;
+  if (dtype)
+    embed_block_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)embed, H, vocab, rs, mask_id,
+                                                   rows, (bf16*)x, ring, inv_freq, half,
+                                                   tab_rows, rope);
+  else
+    embed_block_kernel<float><<<grid, 256, 0, st>>>((const float*)embed, H, vocab, rs, mask_id,
+                                                    rows, (float*)x, ring, inv_freq, half,
+                                                    tab_rows, rope);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,
+                              long long pos0, int rows, float2* rope, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  rope_table_kernel<<<rows, 64, 0, st>>>(inv_freq, half, ring, pos0, rows, rope);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g, void* y,
+                           int ldy, int rows, int H, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (dtype)
+    rmsnorm_kernel<bf16><<<rows, 256, 0, st>>>((const bf16*)x, ldx, (const bf16*)g, (bf16*)y,
+                                               ldy, H, eps);
+  else
+    rmsnorm_kernel<float><<<rows, 256, 0, st>>>((const float*)x, ldx, (const float*)g,
+                                                (float*)y, ldy, H, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows, int heads, int hd,
+                                  const void* g, float eps, const float2* rope, int neox,
+                                  cudaStream_t st) {
+  const int items = rows * heads;
+  if (items <= 0) return cudaSuccess;
+  const int grid = (items + 3) / 4;
+  if (dtype)
+    head_norm_rope_kernel<bf16><<<grid, 128, 0, st>>>((bf16*)buf, ld, rows, heads, hd,
+                                                      (const bf16*)g, eps, rope, neox);
+  else
+    head_norm_rope_kernel<float><<<grid, 128, 0, st>>>((float*)buf, ld, rows, heads, hd,
+                                                       (const float*)g, eps, rope, neox);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int nkv, int hd,
+                              const void* kg, float eps, const float2* rope, int neox,
+                              void* ring_k, void* ring_v, long long cap, int append_only,
+                              RingState* ring, int use_dev, long long pos_host,
+                              cudaStream_t st) {
+  const int items = rows * nkv;
+  if (items <= 0) return cudaSuccess;
+  const int grid = (items + 3) / 4;
+  if (dtype)
+    kv_to_ring_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)kv, ld, rows, nkv, hd,
+                                                  (const bf16*)kg, eps, rope, neox,
+                                                  (bf16*)ring_k, (bf16*)ring_v, cap,
+                                                  append_only, ring, use_dev, pos_host);
+  else
+    kv_to_ring_kernel<float><<<grid, 128, 0, st>>>((const float*)kv, ld, rows, nkv, hd,
+                                                   (const float*)kg, eps, rope, neox,
+                                                   (float*)ring_k, (float*)ring_v, cap,
+                                                   append_only, ring, use_dev, pos_host);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
+                          cudaStream_t st) {
+  commit_kernel<<<1, 1, 0, st>>>(rs, ring, block, keep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st) {
+  ring_advance_kernel<<<1, 1, 0, st>>>(ring, d, mode);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_reset(RingState* ring, long long base, cudaStream_t st) {
+  ring_reset_kernel<<<1, 1, 0, st>>>(ring, base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_anchor(RoundState* rs, int anchor, cudaStream_t st) {
+  set_anchor_kernel<<<1, 1, 0, st>>>(rs, anchor);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_append(int dtype, const void* k, const void* v, int L, int n, int nkv,
+                               int hd, void* ring_k, void* ring_v, long long cap,
+                               RingState* ring, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long long items = (long long)L * n * nkv;
+  const int grid = static_cast<int>(items < 4096 ? items : 4096);
+  if (dtype)
+    ring_append_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)k, (const bf16*)v, L, n, nkv,
+                                                   hd, (bf16*)ring_k, (bf16*)ring_v, cap, ring);
+  else
+    ring_append_kernel<float><<<grid, 128, 0, st>>>((const float*)k, (const float*)v, L, n, nkv,
+                                                    hd, (float*)ring_k, (float*)ring_v, cap,
+                                                    ring);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_ring_advance(ring, n, 0, st);
+}
+
+cudaError_t launch_ring_gather(int dtype, const void* ring_k, const void* ring_v, int L,
+                               long long cap, int nkv, int hd, long long pos0, int count,
+                               void* k_out, void* v_out, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  const long long items = (long long)L * count * nkv;
+  const int grid = static_cast<int>(items < 4096 ? items : 4096);
+  if (dtype)
+    ring_gather_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)ring_k, (const bf16*)ring_v, L,
+                                                   cap, nkv, hd, pos0, count, (bf16*)k_out,
+                                                   (bf16*)v_out);
+  else
+    ring_gather_kernel<float><<<grid, 128, 0, st>>>((const float*)ring_k, (const float*)ring_v,
+                                                    L, cap, nkv, hd, pos0, count,
+                                                    (float*)k_out, (float*)v_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st) {
+  const long long total = (long long)a.block * (a.V + a.kin);
+  const long long g = (total + 255) / 256;
+  const int grid = static_cast<int>(g < 2048 ? g : 2048);
+  if (dtype) synth_target_kernel<bf16><<<grid, 256, 0, st>>>(a);
+  else synth_target_kernel<float><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -1,0 +1,335 @@
+/*
+ * dflash.h -- C ABI of libdflash: one DFlash speculative round at batch 1 on
+ * a single GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [Muse]   "Muse Glimmer DFlash assistant drafter on the round loop"
+ *            (mlxcel pull request 1762)
+ *   [Head]   "Load Meta's Muse-Glimmer-30B-assistant DFlash head via a
+ *            draft-adapter registry" (z-lab/dflash pull request 168)
+ *   [DSpark] "LFM2 / LFM2.5 DSpark drafter on the DFlash loop"
+ *            (mlxcel pull request 1751)
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers unless the name ends in _host.
+ *     They are borrowed: the caller owns them and keeps them alive while the
+ *     enqueued work runs. Tensors are dense row-major; linear weights are
+ *     [out_features, in_features]. Element type is the config's dtype
+ *     (fp32 or bf16) unless stated. Every tensor pointer must be 16-byte
+ *     aligned.
+ *   - Every call that takes a context enqueues its GPU work on the context's
+ *     stream and returns without waiting, except the calls marked "syncs".
+ *     The round calls allocate nothing and never synchronize, so a caller may
+ *     capture whole rounds into a CUDA graph (dflash_capture_begin / _end /
+ *     dflash_graph_launch).
+ *   - Every call returns a status (DFLASH_OK == 0) and never aborts or throws
+ *     [Muse "Pre-merge review round", third finding; DSpark "Security fixes":
+ *     a bad checkpoint value must be a request error, not a process abort].
+ *     The context keeps the message of its last error (dflash_last_error).
+ *     Arguments are checked on the host before any GPU work is enqueued.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+enum {
+  DFLASH_OK = 0,
+  DFLASH_EINVAL = 1,  /* null pointer, bad dtype/kind, dimension <= 0, a
+                         dimension product that would wrap an int32, bad
+                         alignment [Muse "Pre-merge review round", third
+                         finding: config dimensions bounded as i32] */
+  DFLASH_ERANGE = 2,  /* token id outside [0, vocab), mask_token_id >= vocab,
+                         block < 2 or block > max_block, Markov shape mismatch
+                         [DSpark "Review fixes": mask id and width bounds,
+                         Markov factor shapes] */
+  DFLASH_EREWIND = 3, /* trim longer than the rows appended since the last
+                         trim: the "short rewind" [Muse "Pre-merge review
+                         round", second finding] */
+  DFLASH_EEMPTY = 4,  /* empty context where a draft needs one, or zero rows
+                         [DSpark "Security fixes": empty prompt / window] */
+  DFLASH_ECUDA = 5,   /* a CUDA call failed; dflash_last_error has its text */
+  DFLASH_ESTATE = 6,  /* call out of order (commit before append, capture
+                         misuse, unknown graph slot) */
+  DFLASH_EFULL = 7    /* an unbounded-window (append-only) cache is out of
+                         rows (config.max_context) */
+};
+
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
+enum { DFLASH_KIND_DFLASH = 0, DFLASH_KIND_DSPARK = 1 };
+
+/* Number of weight pointers per drafter layer in dflash_weights.layers, in
+ * this order: in_norm[H], wq[nq*hd, H], wk[nkv*hd, H], wv[nkv*hd, H],
+ * q_norm[hd], k_norm[hd], wo[H, nq*hd], post_norm[H], wg[I, H], wu[I, H],
+ * wd[H, I]. */
+#define DFLASH_LAYER_TENSORS 11
+
+typedef struct dflash_config {
+  int32_t n_layers;        /* drafter layers (5 on every page) */
+  int32_t hidden;          /* H, a multiple of 8 */
+  int32_t n_q_heads;       /* nq */
+  int32_t n_kv_heads;      /* nkv; nq % nkv == 0 (grouped-query attention) */
+  int32_t head_dim;        /* hd, a multiple of 8, at most 256 */
+  int32_t intermediate;    /* I (SwiGLU), a multiple of 8 */
+  int32_t vocab;           /* V */
+  int32_t window;          /* W of the bidirectional sliding mask |q-k| <= W
+                              [Muse "What changed"]; <= 0: no mask and an
+                              append-only cache [DSpark "Verified against the
+                              issue": mask None, append-only] */
+  int32_t k_target_layers; /* captured target residual streams (5) */
+  int32_t target_hidden;   /* width of each captured stream; k * width is a
+                              multiple of 8 */
+  int32_t mask_token_id;   /* < vocab [DSpark "Review fixes"] */
+  int32_t rope_neox;       /* 1: neox pairs (i, i+hd/2); 0: traditional
+                              pairs (2i, 2i+1) [DSpark "Verified against
+                              the issue": rope_is_neox_style false] */
+  int32_t max_block;       /* largest verify width B any round will use
+                              (2..1024); sizes the ring slack and scratch */
+  int32_t kind;            /* DFLASH_KIND_DFLASH: block of B rows, rows
+                              1..B-1 read out; DFLASH_KIND_DSPARK: block of
+                              B-1 rows, every row read out [DSpark
+                              "Verified against the issue"] */
+  int32_t markov_rank;     /* r of the DSpark Markov head, 0 = none */
+  int32_t markov_add;      /* 0: proposals are argmax(W1[prev].W2); 1:
+                              argmax(z_j + W1[prev].W2) over the lm_head
+                              logits z_j */
+  int32_t dtype;           /* DFLASH_F32 or DFLASH_BF16, for weights, inputs,
+                              activations and the ring; accumulation is fp32 */
+  int32_t max_context;     /* window <= 0 only: rows the append-only cache
+                              holds; ignored for a sliding window */
+  float rope_theta;        /* RoPE base (1e6 on the pages' drafters) */
+  float rms_eps;           /* RMSNorm epsilon */
+  float softcap;           /* c of c*tanh(z/c) on the drafter logits, 0 = off
+                              [Head "How": inherited final_logit_softcapping] */
+} dflash_config;
+
+typedef struct dflash_weights {
+  const void* embed;        /* [V, H] the target's raw embedding table
+                               [Muse "What changed"; "Real-checkpoint
+                               validation" item 5: not the embed_norm lookup] */
+  const void* fc;           /* [H, k*target_hidden] encoder.fc */
+  const void* hidden_norm;  /* [H] encoder.output_norm_enc */
+  const void* final_norm;   /* [H] RMSNorm gain before the lm_head */
+  const void* lm_head;      /* [V, H]; may equal embed (tied, as DSpark) */
+  const void* markov_w1;    /* [V, r] or NULL when markov_rank == 0 */
+  const void* markov_w2;    /* [r, V] or NULL when markov_rank == 0 */
+  const void* const* layers;/* HOST array of n_layers * DFLASH_LAYER_TENSORS
+                               device pointers; copied at create */
+} dflash_weights;
+
+typedef struct dflash_stats {
+  int64_t rounds;     /* draft_rounds */
+  int64_t draft_n;    /* proposals made (block - 1 per round) */
+  int64_t accepted;   /* draft_n_accepted: sum of a */
+  int64_t emitted;    /* tokens emitted by verifies: sum of n = a + 1 */
+} dflash_stats;
+
+typedef struct dflash_round_state {
+  int64_t position;   /* absolute position of the current anchor; equals the
+                         committed context length */
+  int32_t anchor;     /* the current anchor token */
+  int32_t last_n;     /* n of the last verify (accepted + 1) */
+  int32_t last_accepted; /* a of the last verify */
+  int32_t error;      /* device-side error bits: 1 = append-only cache full
+                         (rows skipped), 2 = a token id outside the vocabulary
+                         reached the embedding gather (row 0 used) */
+} dflash_round_state;
+
+typedef struct dflash_ctx dflash_ctx;
+typedef struct ring_cache ring_cache;
+
+/* ---- pure host helpers -------------------------------------------------- */
+
+/* Speculative slack rows for a verify block: max(clamp(8*block, 32, 128),
+ * block) [Muse "Pre-merge review round", second finding]. Returns -1 for
+ * block < 1. */
+int32_t dflash_speculative_slack(int32_t block);
+
+/* Derived round counters. accepted_per_round = accepted / rounds (the Muse
+ * page's "mean accepted"); emitted_per_round = accepted / rounds + 1 (the
+ * DSpark page's "mean accepted length"); acceptance = accepted / draft_n.
+ * Any output pointer may be NULL. EINVAL if stats is NULL or a denominator
+ * is zero. */
+int dflash_stats_ratios(const dflash_stats* stats, double* accepted_per_round,
+                        double* emitted_per_round, double* acceptance);
+
+/* Validates a config without touching the GPU (the same checks as create). */
+int dflash_config_check(const dflash_config* cfg);
+
+/* ---- context lifecycle --------------------------------------------------- */
+
+/* Creates a drafter context on the current CUDA device: validates cfg and the
+ * weight pointers, copies the layer pointer table, allocates the ring
+ * (window + slack(max_block) rows per layer, or max_context rows for an
+ * unbounded window) and all scratch in device memory owned by the context.
+ * stream is a cudaStream_t (NULL: the legacy default stream). On failure *out
+ * is NULL and the status says why (text: dflash_last_error(NULL)). */
+int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w,
+                      void* stream, dflash_ctx** out);
+void dflash_ctx_destroy(dflash_ctx* ctx);
+
+/* Text of the last error on this context (or of the last failed create when
+ * ctx is NULL). Never NULL. */
+const char* dflash_last_error(const dflash_ctx* ctx);
+
+/* ---- the round ------------------------------------------------------------ */
+
+/* Ingests captured residual rows resid [rows, k*target_hidden] at absolute
+ * positions first_pos .. first_pos+rows-1 and sets the next anchor to
+ * `anchor` at position first_pos + rows. Rows older than the window (position
+ * < first_pos + rows - W) are dropped before encoder.fc [Muse "Pre-merge
+ * review round", third finding]; the kept rows go through fc ->
+ * hidden_norm -> per-layer Wk/Wv -> k-norm + RoPE into the ring. Replaces any
+ * earlier context. EEMPTY if rows == 0; ERANGE if anchor is out of range;
+ * EFULL if an append-only cache cannot hold the kept rows. */
+int dflash_ingest_context(dflash_ctx* ctx, const void* resid, int64_t rows,
+                          int64_t first_pos, int32_t anchor);
+
+/* Replaces the device-resident anchor token (the position is unchanged). */
+int dflash_set_anchor(dflash_ctx* ctx, int32_t anchor);
+
+/* Drafts one block of verify width `block` from the device-resident anchor
+ * and position [Muse "What changed"; DSpark "Verified against the issue"]:
+ * embeds [anchor, mask x (rows-1)] from the raw embedding table, runs the
+ * drafter layers (per-head q/k RMSNorm, RoPE at absolute positions,
+ * bidirectional sliding attention over the ring plus the block), the final
+ * norm, the lm_head with softcap and the per-row argmax (no [rows, V] logit
+ * tensor is written), and for a config with a Markov head the chain.
+ * Writes block-1 proposals d_1..d_{block-1} to draft_ids [block-1] (int32).
+ * ERANGE unless 2 <= block <= max_block; EEMPTY if no context was ingested. */
+int dflash_draft_block(dflash_ctx* ctx, int32_t block, int32_t* draft_ids);
+
+/* Greedy exact-match verify [DSpark intro; "Short-conv rollback"]: t_i =
+ * argmax target_logits[i, :] (lowest index on ties) for i < block; a = the
+ * longest prefix with draft_ids[i] == t_i; writes tokens [block] (int32)
+ * = d_1..d_a, t_a, followed by -1 padding, and n [1] (int32) = a + 1.
+ * target_logits is [block, V] in the config dtype. Keeps n, a and the bonus
+ * token t_a on the device for dflash_commit. */
+int dflash_verify_accept(dflash_ctx* ctx, const void* target_logits,
+                         int32_t block, const int32_t* draft_ids,
+                         int32_t* tokens, int32_t* n);
+
+/* Appends the verify block's captured residual rows resid [block,
+ * k*target_hidden] at positions p .. p+block-1 (p = device position) into the
+ * ring through fc -> hidden_norm -> Wk/Wv -> k-norm + RoPE; like
+ * ring_cache_append, the offset advances by block until dflash_commit trims
+ * it. ERANGE unless 1 <= block <= max_block. */
+int dflash_append_block(dflash_ctx* ctx, const void* resid, int32_t block);
+
+/* Partial-accept rollback: keeps the first `keep` appended rows and trims
+ * the other block - keep (KVCache::trim(block - n) [DSpark "Short-conv
+ * rollback"]); keep < 0 takes n from the last verify. The anchor becomes the
+ * verify's bonus token and the counters advance. EINVAL if keep > block;
+ * ESTATE without an append since the last commit. */
+int dflash_commit(dflash_ctx* ctx, int32_t keep);
+
+/* One whole round: draft_block, verify_accept, append_block, commit(-1). */
+int dflash_round(dflash_ctx* ctx, const void* target_logits, const void* resid,
+                 int32_t block, int32_t* draft_ids, int32_t* tokens,
+                 int32_t* n);
+
+/* DSpark Markov chain alone [DSpark "Verified against the issue": seeded
+ * with the anchor, each step's argmax feeds the next step's W1 gather]:
+ * out[j] = argmax_v (z[j, v] + W1[prev] . W2[:, v]) with prev = anchor for
+ * j = 0 and out[j-1] after; z is [gamma, V] fp32 or NULL (then 0).
+ * ERANGE if the context has no Markov head, anchor is out of range or gamma
+ * is outside 1..max_block. */
+int dflash_markov_chain(dflash_ctx* ctx, int32_t anchor, int32_t gamma,
+                        const float* z, int32_t* out);
+
+/* ---- inspection (these sync) ------------------------------------------------- */
+
+/* Copies the final-normed hidden rows of the last draft [rows, H] (rows =
+ * block for DFlash, block - 1 for DSpark) into out (device). */
+int dflash_get_hidden(dflash_ctx* ctx, void* out);
+/* Copies the softcapped maximum logit of each read-out row of the last draft
+ * [block - 1] (fp32, device): the value the argmax selected. */
+int dflash_get_draft_max_logit(dflash_ctx* ctx, float* out);
+/* Copies the lm_head argmax ids of the last draft's read-out rows (before
+ * any Markov chain) [block - 1] (int32, device). */
+int dflash_get_backbone_ids(dflash_ctx* ctx, int32_t* out);
+int dflash_get_state(dflash_ctx* ctx, dflash_round_state* out_host);
+int dflash_get_stats(dflash_ctx* ctx, dflash_stats* out_host);
+int dflash_reset_stats(dflash_ctx* ctx);
+/* The context's ring (borrowed; owned and destroyed by the context). */
+int dflash_ring(dflash_ctx* ctx, ring_cache** out);
+
+/* ---- CUDA graphs of whole rounds -------------------------------------------- */
+
+/* Begins stream capture on the context's stream. Calls made until
+ * dflash_capture_end are recorded, not run. */
+int dflash_capture_begin(dflash_ctx* ctx);
+/* Ends the capture and instantiates it into graph slot `slot` (0..63),
+ * replacing what the slot held. */
+int dflash_capture_end(dflash_ctx* ctx, int32_t slot);
+/* Launches graph slot `slot` on the context's stream. */
+int dflash_graph_launch(dflash_ctx* ctx, int32_t slot);
+/* Waits for the context's stream (syncs). */
+int dflash_sync(dflash_ctx* ctx);
+
+/* ---- stand-in target (benchmark and test harness) ---------------------------- */
+
+/* Fills the round's target inputs the way a target model would, from pools
+ * of synthetic data. r = the context's committed-round counter (device);
+ * logits_out [block, V] = logit_pool[r % n_logit_pool][:block] with
+ * logits_out[i, draft_ids[i]] = plant[r % n_logit_pool][i] wherever
+ * coins[r % n_coin_rows][i] != 0 (i < block - 1); resid_out
+ * [block, k*target_hidden] = resid_pool[r % n_resid_pool][:block].
+ * logit_pool is [n, block_max, V], plant [n, block_max], resid_pool
+ * [n, block_max, k*target_hidden], coins uint8 [n_coin_rows, block_max].
+ * This is not a step of the round: it stands in for the target model. */
+int dflash_synth_target(dflash_ctx* ctx, const void* logit_pool,
+                        const void* plant, const uint8_t* coins,
+                        const void* resid_pool, int32_t n_logit_pool,
+                        int32_t n_coin_rows, int32_t n_resid_pool,
+                        int32_t block_max, int32_t block,
+                        const int32_t* draft_ids, void* logits_out,
+                        void* resid_out);
+
+/* ---- ring KV cache (usable standalone) ---------------------------------------- */
+
+#define DFLASH_RING_UNFLOORED 1 /* test-only: size the slack by the unfloored
+                                   clamp(8*block, 32, 128), to show the window
+                                   corruption the floor prevents */
+
+/* A per-layer ring of K and V rows [kv_heads, head_dim] addressed by absolute
+ * position: position q lives in slot q mod capacity, capacity = window +
+ * slack(max_block) [Muse "What changed": the mask needs absolute key
+ * positions; "Pre-merge review round": the slack past the window]. window
+ * <= 0 makes an append-only cache of max_context rows. stream as in
+ * dflash_ctx_create. */
+int ring_cache_create(int32_t n_layers, int32_t kv_heads, int32_t head_dim,
+                      int32_t window, int32_t max_block, int32_t dtype,
+                      int32_t max_context, void* stream, ring_cache** out);
+int ring_cache_create_ex(int32_t n_layers, int32_t kv_heads, int32_t head_dim,
+                         int32_t window, int32_t max_block, int32_t dtype,
+                         int32_t max_context, int32_t flags, void* stream,
+                         ring_cache** out);
+/* Destroys a standalone ring; a context's ring is destroyed with it. */
+void ring_cache_destroy(ring_cache* rc);
+/* Appends n rows at positions offset .. offset+n-1; k and v are
+ * [n_layers, n, kv_heads, head_dim]. EINVAL if n < 0 or n > capacity; EFULL
+ * if an append-only cache would overflow. */
+int ring_cache_append(ring_cache* rc, const void* k, const void* v, int32_t n);
+/* Rewinds the offset by n_rows without restoring any slot; EREWIND if n_rows
+ * exceeds the rows appended since the last trim or commit. */
+int ring_cache_trim(ring_cache* rc, int32_t n_rows);
+/* Offset (syncs): the next absolute position to be written. */
+int ring_cache_offset(ring_cache* rc, int64_t* offset_host);
+int ring_cache_capacity(const ring_cache* rc, int64_t* capacity_host);
+/* Copies the raw slot contents for positions pos0 .. pos0+count-1 into k_out
+ * and v_out [n_layers, count, kv_heads, head_dim] (device). No validity
+ * check: a slot overwritten since returns what it now holds. */
+int ring_cache_gather(ring_cache* rc, int64_t pos0, int32_t count,
+                      void* k_out, void* v_out);
+const char* ring_cache_last_error(const ring_cache* rc);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */
