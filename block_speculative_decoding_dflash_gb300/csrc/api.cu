@@ -1,0 +1,870 @@
+// libdflash host side: argument checks, the context and ring objects, the
+// order of kernel launches that makes one DFlash round, and CUDA-graph
+// capture of rounds. Nothing here throws across the C ABI and nothing in the
+// round path allocates or synchronizes.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "kernels.h"
+
+using namespace dfl;
+
+namespace {
+
+thread_local std::string g_create_err;
+
+int fail(std::string& err, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  err = buf;
+  return code;
+}
+
+int cuda_fail(std::string& err, cudaError_t e, const char* what) {
+  return fail(err, DFLASH_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define CK(err, call)                                             \
+  do {                                                            \
+    cudaError_t e_ = (call);                                      \
+    if (e_ != cudaSuccess) return cuda_fail((err), e_, #call);    \
+  } while (0)
+
+int slack_rule(int block, bool floor) {
+  int s = 8 * block;
+  if (s < 32) s = 32;
+  if (s > 128) s = 128;
+  return (floor && s < block) ? block : s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kI32Max = std::numeric_limits<int32_t>::max();
+constexpr int kIngestChunk = 2048;
+constexpr int kMaxBlock = 1024;
+
+int check_config(const dflash_config* c, std::string& err) {
+  if (!c) return fail(err, DFLASH_EINVAL, "config is NULL");
+  if (c->n_layers < 1 || c->hidden < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
+      c->head_dim < 1 || c->intermediate < 1 || c->vocab < 2 || c->k_target_layers < 1 ||
+      c->target_hidden < 1)
+    return fail(err, DFLASH_EINVAL, "every dimension must be positive (vocab >= 2)");
+  if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16)
+    return fail(err, DFLASH_EINVAL, "dtype must be DFLASH_F32 or DFLASH_BF16");
+  if (c->kind != DFLASH_KIND_DFLASH && c->kind != DFLASH_KIND_DSPARK)
+    return fail(err, DFLASH_EINVAL, "kind must be DFLASH_KIND_DFLASH or DFLASH_KIND_DSPARK");
+  if (c->rope_neox != 0 && c->rope_neox != 1) return fail(err, DFLASH_EINVAL, "rope_neox must be 0 or 1");
+  if (c->n_q_heads % c->n_kv_heads) return fail(err, DFLASH_EINVAL, "n_q_heads %% n_kv_heads != 0");
+  if (c->hidden % 8 || c->head_dim % 8 || c->intermediate % 8 ||
+      ((int64_t)c->k_target_layers * c->target_hidden) % 8)
+    return fail(err, DFLASH_EINVAL, "hidden, head_dim, intermediate and k*target_hidden must be multiples of 8");
+  if (c->head_dim > 256) return fail(err, DFLASH_EINVAL, "head_dim must be at most 256");
+  if (c->max_block < 2 || c->max_block > kMaxBlock)
+    return fail(err, DFLASH_ERANGE, "max_block %d outside [2, %d]", c->max_block, kMaxBlock);
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab)
+    return fail(err, DFLASH_ERANGE, "mask_token_id %d outside [0, vocab=%d)", c->mask_token_id, c->vocab);
+  if (c->markov_rank < 0 || c->markov_rank > 4096)
+    return fail(err, DFLASH_EINVAL, "markov_rank %d outside [0, 4096]", c->markov_rank);
+  if (c->markov_add != 0 && c->markov_add != 1) return fail(err, DFLASH_EINVAL, "markov_add must be 0 or 1");
+  if (c->markov_rank > 0 && c->vocab % 8)
+    return fail(err, DFLASH_EINVAL, "a Markov head needs vocab to be a multiple of 8");
+  if (c->window <= 0 && c->max_context < 1)
+    return fail(err, DFLASH_EINVAL, "an unbounded window needs max_context >= 1");
+  if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta) || !(c->rms_eps >= 0.f) ||
+      !std::isfinite(c->rms_eps) || !(c->softcap >= 0.f) || !std::isfinite(c->softcap))
+    return fail(err, DFLASH_EINVAL, "rope_theta must be > 0, rms_eps and softcap >= 0, all finite");
+  // Products the kernels index with 32-bit integers.
+  const int64_t prods[] = {
+      (int64_t)c->n_q_heads * c->head_dim,
+      (int64_t)(c->n_q_heads + 2 * (int64_t)c->n_kv_heads) * c->head_dim,
+      (int64_t)c->k_target_layers * c->target_hidden,
+      (int64_t)c->window + slack_rule(c->max_block, true),
+      (int64_t)c->max_block * c->vocab,
+      (int64_t)c->max_block * c->n_q_heads * c->head_dim,
+      (int64_t)c->max_block * ((int64_t)c->k_target_layers * c->target_hidden + c->vocab),
+      (int64_t)c->n_kv_heads * ((int64_t)(c->window > 0 ? c->window : c->max_context) +
+                                c->max_block) * (c->n_q_heads / c->n_kv_heads) * c->max_block,
+  };
+  for (int64_t p : prods)
+    if (p > kI32Max) return fail(err, DFLASH_EINVAL, "a dimension product (%lld) would wrap an int32", (long long)p);
+  return DFLASH_OK;
+}
+
+enum LayerW { kInNorm, kWq, kWk, kWv, kQNorm, kKNorm, kWo, kPostNorm, kWg, kWu, kWd };
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Objects
+// ---------------------------------------------------------------------------
+struct ring_cache {
+  int L = 0, nkv = 0, hd = 0, window = 0, max_block = 0, dtype = 0, flags = 0;
+  long long cap = 0;
+  int append_only = 0;
+  size_t esz = 4;
+  void* k = nullptr;
+  void* v = nullptr;
+  RingState* st = nullptr;
+  cudaStream_t stream = nullptr;
+  bool owned_by_ctx = false;
+  int host_appended = 0;
+  long long pos_hi = 0;     // upper bound of the device offset
+  long long host_base = 0;
+  std::string err;
+};
+
+struct dflash_ctx {
+  dflash_config cfg{};
+  const void* embed = nullptr;
+  const void* fc = nullptr;
+  const void* hidden_norm = nullptr;
+  const void* final_norm = nullptr;
+  const void* lm_head = nullptr;
+  const void* w1 = nullptr;
+  const void* w2 = nullptr;
+  std::vector<const void*> layers;
+  cudaStream_t stream = nullptr;
+  ring_cache* ring = nullptr;
+  int dt = 0;
+  size_t esz = 4;
+  int H = 0, nq = 0, nkv = 0, hd = 0, half = 0, I = 0, V = 0, kin = 0;
+  int qdim = 0, kvdim = 0, qkv_n = 0, rows_max = 0, max_ctx = 0;
+
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  RoundState* rs = nullptr;
+  double* inv_freq = nullptr;
+  void *x = nullptr, *xn = nullptr, *qkv = nullptr, *attn = nullptr, *sbuf = nullptr, *xf = nullptr;
+  float2* rope = nullptr;
+  float* attn_part = nullptr;
+  void *app_f = nullptr, *app_c = nullptr, *app_kv = nullptr;
+  float2* app_rope = nullptr;
+  void *ing_f = nullptr, *ing_c = nullptr, *ing_kv = nullptr;
+  float2* ing_rope = nullptr;
+  int ing_rows = 0;
+  float* lm_pv = nullptr;
+  int* lm_pi = nullptr;
+  int lm_grid = 0;
+  float* vf_pv = nullptr;
+  int* vf_pi = nullptr;
+  int vf_chunks = 0;
+  float* mk_pv = nullptr;
+  int* mk_pi = nullptr;
+  int mk_grid = 0;
+  unsigned* counters = nullptr;  // [0] lm_head, [1] verify, [2] markov
+  float* maxv = nullptr;
+  int* backbone_ids = nullptr;
+  float* zlog = nullptr;
+
+  bool has_context = false;
+  int last_draft_block = 0;
+  int last_verify_block = 0;
+  int appended_block = 0;
+  bool capturing = false;
+  int saved_flags[4] = {0, 0, 0, 0};
+  cudaGraphExec_t graphs[64] = {};
+  std::string err;
+};
+
+namespace {
+
+template <typename P>
+P* carve(char*& cur, size_t bytes) {
+  char* p = cur;
+  cur += (bytes + 255) & ~size_t(255);
+  return reinterpret_cast<P*>(p);
+}
+
+int ring_create_impl(int L, int nkv, int hd, int window, int max_block, int dtype,
+                     int max_context, int flags, cudaStream_t st, ring_cache** out,
+                     std::string& err) {
+  if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (L < 1 || nkv < 1 || hd < 1) return fail(err, DFLASH_EINVAL, "ring dimensions must be positive");
+  if (dtype != DFLASH_F32 && dtype != DFLASH_BF16) return fail(err, DFLASH_EINVAL, "bad dtype");
+  if (max_block < 1 || max_block > kMaxBlock)
+    return fail(err, DFLASH_ERANGE, "max_block %d outside [1, %d]", max_block, kMaxBlock);
+  if (window <= 0 && max_context < 1)
+    return fail(err, DFLASH_EINVAL, "an append-only ring needs max_context >= 1");
+  ring_cache* r = new (std::nothrow) ring_cache();
+  if (!r) return fail(err, DFLASH_ECUDA, "out of host memory");
+  r->L = L; r->nkv = nkv; r->hd = hd; r->window = window; r->max_block = max_block;
+  r->dtype = dtype; r->flags = flags; r->stream = st;
+  r->append_only = window <= 0;
+  r->cap = window > 0 ? (long long)window + slack_rule(max_block, !(flags & DFLASH_RING_UNFLOORED))
+                      : (long long)max_context;
+  r->esz = dtype == DFLASH_BF16 ? 2 : 4;
+  const size_t bytes = (size_t)L * nkv * (size_t)r->cap * hd * r->esz;
+  cudaError_t e;
+  if ((e = cudaMalloc(&r->k, bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&r->v, bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&r->st, sizeof(RingState))) != cudaSuccess ||
+      (e = cudaMemsetAsync(r->k, 0, bytes, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(r->v, 0, bytes, st)) != cudaSuccess ||
+      (e = launch_ring_reset(r->st, 0, st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+    cudaFree(r->k); cudaFree(r->v); cudaFree(r->st);
+    delete r;
+    return cuda_fail(err, e, "ring allocation");
+  }
+  *out = r;
+  return DFLASH_OK;
+}
+
+void ring_free(ring_cache* r) {
+  if (!r) return;
+  cudaFree(r->k);
+  cudaFree(r->v);
+  cudaFree(r->st);
+  delete r;
+}
+
+// Exact device offset (syncs); used only when an append-only bound is close.
+int ring_sync_offset(ring_cache* r, long long* off) {
+  RingState s;
+  CK(r->err, cudaStreamSynchronize(r->stream));
+  CK(r->err, cudaMemcpy(&s, r->st, sizeof s, cudaMemcpyDeviceToHost));
+  *off = s.offset;
+  return DFLASH_OK;
+}
+
+LinearArgs lin_args(const void* x, int ldx, void* y, int ldy, int M, int N, int K) {
+  LinearArgs a{};
+  a.x = x; a.ldx = ldx; a.y = y; a.ldy = ldy; a.M = M; a.N = N; a.K = K;
+  a.nseg = 1; a.seg_end[0] = N; a.epi = kEpiStore;
+  return a;
+}
+
+const void* LW(const dflash_ctx* c, int l, int which) {
+  return c->layers[(size_t)l * DFLASH_LAYER_TENSORS + which];
+}
+
+// Context rows -> ring: fc -> hidden_norm -> per layer [Wk | Wv] -> k-norm +
+// RoPE / copy into ring slots. use_dev: positions from the device offset
+// (block append), else pos_host (ingest).
+int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, void* cn, void* kv,
+                         float2* rope, int use_dev, long long pos_host) {
+  const int dt = c->dt;
+  cudaStream_t st = c->stream;
+  CK(c->err, launch_rope_table(c->inv_freq, c->half, use_dev ? c->ring->st : nullptr, pos_host,
+                               rows, rope, st));
+  LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
+  a.w[0] = c->fc;
+  CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
+  CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    LinearArgs b = lin_args(cn, c->H, kv, 2 * c->kvdim, rows, 2 * c->kvdim, c->H);
+    b.nseg = 2;
+    b.w[0] = LW(c, l, kWk); b.seg_end[0] = c->kvdim;
+    b.w[1] = LW(c, l, kWv); b.seg_end[1] = 2 * c->kvdim;
+    CK(c->err, rows > 32 ? launch_linear_tiled(dt, b, st) : launch_linear_rows(dt, b, st));
+    const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
+    CK(c->err, launch_kv_to_ring(dt, kv, 2 * c->kvdim, rows, c->nkv, c->hd, LW(c, l, kKNorm),
+                                 c->cfg.rms_eps, rope, c->cfg.rope_neox,
+                                 static_cast<char*>(c->ring->k) + lay,
+                                 static_cast<char*>(c->ring->v) + lay, c->ring->cap,
+                                 c->ring->append_only, c->ring->st, use_dev, pos_host, st));
+  }
+  return DFLASH_OK;
+}
+
+int layer_forward(dflash_ctx* c, int l, int rows) {
+  const int dt = c->dt;
+  cudaStream_t st = c->stream;
+  const float eps = c->cfg.rms_eps;
+  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st));
+  LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
+  q.nseg = 3;
+  q.w[0] = LW(c, l, kWq); q.seg_end[0] = c->qdim;
+  q.w[1] = LW(c, l, kWk); q.seg_end[1] = c->qdim + c->kvdim;
+  q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
+  CK(c->err, launch_linear_rows(dt, q, st));
+  CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
+                                   c->rope, c->cfg.rope_neox, st));
+  CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
+                                   c->qkv_n, rows, c->nkv, c->hd, LW(c, l, kKNorm), eps, c->rope,
+                                   c->cfg.rope_neox, st));
+  AttnArgs at{};
+  at.q = c->qkv; at.ldq = c->qkv_n;
+  at.kb = static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz;
+  at.vb = static_cast<char*>(c->qkv) + (size_t)(c->qdim + c->kvdim) * c->esz;
+  at.ldkv = c->qkv_n;
+  const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
+  at.ring_k = static_cast<char*>(c->ring->k) + lay;
+  at.ring_v = static_cast<char*>(c->ring->v) + lay;
+  at.cap = c->ring->cap;
+  at.ring = c->ring->st;
+  at.window = c->cfg.window;
+  at.rows = rows; at.nq = c->nq; at.nkv = c->nkv; at.hd = c->hd;
+  at.max_ctx = c->max_ctx;
+  at.partial = c->attn_part;
+  at.out = c->attn; at.ldo = c->qdim;
+  CK(c->err, launch_attention(dt, at, st));
+  LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
+  o.w[0] = LW(c, l, kWo); o.epi = kEpiResid; o.r = c->x; o.ldr = c->H;
+  CK(c->err, launch_linear_rows(dt, o, st));
+  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st));
+  LinearArgs g = lin_args(c->xn, c->H, c->sbuf, c->I, rows, c->I, c->H);
+  g.w[0] = LW(c, l, kWg); g.w2 = LW(c, l, kWu); g.epi = kEpiSwiglu;
+  CK(c->err, launch_linear_rows(dt, g, st));
+  LinearArgs d = lin_args(c->sbuf, c->I, c->x, c->H, rows, c->H, c->I);
+  d.w[0] = LW(c, l, kWd); d.epi = kEpiResid; d.r = c->x; d.ldr = c->H;
+  CK(c->err, launch_linear_rows(dt, d, st));
+  return DFLASH_OK;
+}
+
+// Append-only rings: make sure `rows` more rows fit (syncs only when the
+// conservative host bound says they might not, and never while capturing).
+int ensure_room(dflash_ctx* c, int rows) {
+  ring_cache* r = c->ring;
+  if (!r->append_only) return DFLASH_OK;
+  if (r->pos_hi + rows - r->host_base <= r->cap) return DFLASH_OK;
+  if (c->capturing)
+    return fail(c->err, DFLASH_EFULL, "append-only cache may be full; cannot check while capturing");
+  long long off;
+  int rc = ring_sync_offset(r, &off);
+  if (rc) { c->err = r->err; return rc; }
+  r->pos_hi = off;
+  if (off + rows - r->host_base > r->cap)
+    return fail(c->err, DFLASH_EFULL, "append-only cache full: %lld + %d rows > %lld",
+                off - r->host_base, rows, r->cap);
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int32_t dflash_speculative_slack(int32_t block) { return block < 1 ? -1 : slack_rule(block, true); }
+
+int dflash_stats_ratios(const dflash_stats* s, double* apr, double* epr, double* acc) {
+  if (!s || s->rounds <= 0 || s->draft_n <= 0) return DFLASH_EINVAL;
+  const double a = static_cast<double>(s->accepted) / static_cast<double>(s->rounds);
+  if (apr) *apr = a;
+  if (epr) *epr = a + 1.0;
+  if (acc) *acc = static_cast<double>(s->accepted) / static_cast<double>(s->draft_n);
+  return DFLASH_OK;
+}
+
+int dflash_config_check(const dflash_config* cfg) { return check_config(cfg, g_create_err); }
+
+const char* dflash_last_error(const dflash_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_create_err.c_str();
+}
+
+void dflash_ctx_destroy(dflash_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->capturing) {
+    cudaGraph_t g = nullptr;
+    cudaStreamEndCapture(ctx->stream, &g);
+    if (g) cudaGraphDestroy(g);
+  }
+  cudaStreamSynchronize(ctx->stream);
+  for (auto& g : ctx->graphs)
+    if (g) cudaGraphExecDestroy(g);
+  ring_free(ctx->ring);
+  cudaFree(ctx->arena);
+  delete ctx;
+}
+
+int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* stream,
+                      dflash_ctx** out) {
+  std::string& err = g_create_err;
+  if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
+  *out = nullptr;
+  int rc = check_config(cfg, err);
+  if (rc) return rc;
+  if (!w || !w->embed || !w->fc || !w->hidden_norm || !w->final_norm || !w->lm_head || !w->layers)
+    return fail(err, DFLASH_EINVAL, "a weight pointer is NULL");
+  const void* tops[] = {w->embed, w->fc, w->hidden_norm, w->final_norm, w->lm_head};
+  for (const void* p : tops)
+    if (!aligned16(p)) return fail(err, DFLASH_EINVAL, "weight pointers must be 16-byte aligned");
+  for (int i = 0; i < cfg->n_layers * DFLASH_LAYER_TENSORS; ++i) {
+    if (!w->layers[i]) return fail(err, DFLASH_EINVAL, "layer weight %d is NULL", i);
+    if (!aligned16(w->layers[i])) return fail(err, DFLASH_EINVAL, "layer weight %d is not 16-byte aligned", i);
+  }
+  if (cfg->markov_rank > 0 && (!w->markov_w1 || !w->markov_w2 || !aligned16(w->markov_w1) ||
+                               !aligned16(w->markov_w2)))
+    return fail(err, DFLASH_ERANGE, "markov_rank > 0 needs aligned markov_w1 [V, r] and markov_w2 [r, V]");
+
+  dflash_ctx* c = new (std::nothrow) dflash_ctx();
+  if (!c) return fail(err, DFLASH_ECUDA, "out of host memory");
+  c->cfg = *cfg;
+  c->embed = w->embed; c->fc = w->fc; c->hidden_norm = w->hidden_norm;
+  c->final_norm = w->final_norm; c->lm_head = w->lm_head;
+  c->w1 = cfg->markov_rank > 0 ? w->markov_w1 : nullptr;
+  c->w2 = cfg->markov_rank > 0 ? w->markov_w2 : nullptr;
+  c->layers.assign(w->layers, w->layers + (size_t)cfg->n_layers * DFLASH_LAYER_TENSORS);
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->dt = cfg->dtype;
+  c->esz = cfg->dtype == DFLASH_BF16 ? 2 : 4;
+  c->H = cfg->hidden; c->nq = cfg->n_q_heads; c->nkv = cfg->n_kv_heads; c->hd = cfg->head_dim;
+  c->half = c->hd / 2; c->I = cfg->intermediate; c->V = cfg->vocab;
+  c->kin = cfg->k_target_layers * cfg->target_hidden;
+  c->qdim = c->nq * c->hd; c->kvdim = c->nkv * c->hd; c->qkv_n = c->qdim + 2 * c->kvdim;
+  c->rows_max = cfg->max_block;
+  c->max_ctx = cfg->window > 0 ? cfg->window : cfg->max_context;
+
+  rc = ring_create_impl(cfg->n_layers, c->nkv, c->hd, cfg->window, cfg->max_block, cfg->dtype,
+                        cfg->max_context, 0, c->stream, &c->ring, err);
+  if (rc) { delete c; return rc; }
+  c->ring->owned_by_ctx = true;
+
+  const size_t E = c->esz, R = c->rows_max;
+  c->ing_rows = c->max_ctx < kIngestChunk ? c->max_ctx : kIngestChunk;
+  c->lm_grid = lmhead_grid(c->V);
+  c->vf_chunks = verify_chunks(c->V);
+  c->mk_grid = markov_grid(c->V);
+  const size_t attn_floats = attention_scratch_floats(c->rows_max, c->nq, c->nkv, c->hd, c->max_ctx);
+  const size_t sizes[] = {
+      sizeof(RoundState), sizeof(double) * c->half,
+      R * c->H * E, R * c->H * E, R * c->qkv_n * E, R * c->qdim * E, R * c->I * E, R * c->H * E,
+      R * c->half * sizeof(float2), attn_floats * sizeof(float),
+      R * c->H * E, R * c->H * E, R * 2 * c->kvdim * E, R * c->half * sizeof(float2),
+      (size_t)c->ing_rows * c->H * E, (size_t)c->ing_rows * c->H * E,
+      (size_t)c->ing_rows * 2 * c->kvdim * E, (size_t)c->ing_rows * c->half * sizeof(float2),
+      (size_t)c->lm_grid * R * 4, (size_t)c->lm_grid * R * 4, R * c->vf_chunks * 4,
+      R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
+      R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0};
+  size_t total = 0;
+  for (size_t s : sizes) total += (s + 255) & ~size_t(255);
+  cudaError_t e = cudaMalloc(&c->arena, total);
+  if (e != cudaSuccess) { ring_free(c->ring); delete c; return cuda_fail(err, e, "scratch allocation"); }
+  c->arena_bytes = total;
+  char* cur = c->arena;
+  int si = 0;
+  c->rs = carve<RoundState>(cur, sizes[si++]);
+  c->inv_freq = carve<double>(cur, sizes[si++]);
+  c->x = carve<char>(cur, sizes[si++]);
+  c->xn = carve<char>(cur, sizes[si++]);
+  c->qkv = carve<char>(cur, sizes[si++]);
+  c->attn = carve<char>(cur, sizes[si++]);
+  c->sbuf = carve<char>(cur, sizes[si++]);
+  c->xf = carve<char>(cur, sizes[si++]);
+  c->rope = carve<float2>(cur, sizes[si++]);
+  c->attn_part = carve<float>(cur, sizes[si++]);
+  c->app_f = carve<char>(cur, sizes[si++]);
+  c->app_c = carve<char>(cur, sizes[si++]);
+  c->app_kv = carve<char>(cur, sizes[si++]);
+  c->app_rope = carve<float2>(cur, sizes[si++]);
+  c->ing_f = carve<char>(cur, sizes[si++]);
+  c->ing_c = carve<char>(cur, sizes[si++]);
+  c->ing_kv = carve<char>(cur, sizes[si++]);
+  c->ing_rope = carve<float2>(cur, sizes[si++]);
+  c->lm_pv = carve<float>(cur, sizes[si++]);
+  c->lm_pi = carve<int>(cur, sizes[si++]);
+  c->vf_pv = carve<float>(cur, sizes[si++]);
+  c->vf_pi = carve<int>(cur, sizes[si++]);
+  c->mk_pv = carve<float>(cur, sizes[si++]);
+  c->mk_pi = carve<int>(cur, sizes[si++]);
+  c->counters = carve<unsigned>(cur, sizes[si++]);
+  c->maxv = carve<float>(cur, sizes[si++]);
+  c->backbone_ids = carve<int>(cur, sizes[si++]);
+  c->zlog = sizes[si] ? carve<float>(cur, sizes[si]) : nullptr;
+  ++si;
+
+  std::vector<double> inv(c->half);
+  for (int i = 0; i < c->half; ++i)
+    inv[i] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / static_cast<double>(c->hd));
+  if ((e = cudaMemsetAsync(c->arena, 0, total, c->stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(c->inv_freq, inv.data(), sizeof(double) * c->half,
+                           cudaMemcpyHostToDevice, c->stream)) != cudaSuccess ||
+      (e = init_lmhead_attrs(c->H)) != cudaSuccess ||
+      (e = init_attention_attrs(c->hd)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
+    dflash_ctx_destroy(c);
+    return cuda_fail(err, e, "context initialisation");
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_t first_pos,
+                          int32_t anchor) {
+  if (!c) return DFLASH_EINVAL;
+  if (rows <= 0) return fail(c->err, DFLASH_EEMPTY, "empty context (rows = %lld)", (long long)rows);
+  if (!resid || !aligned16(resid)) return fail(c->err, DFLASH_EINVAL, "resid is NULL or misaligned");
+  if (first_pos < 0) return fail(c->err, DFLASH_EINVAL, "first_pos must be >= 0");
+  if (anchor < 0 || anchor >= c->V)
+    return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
+  const long long next = first_pos + rows;
+  long long kept_first = first_pos;
+  if (c->cfg.window > 0 && next - c->cfg.window > kept_first) kept_first = next - c->cfg.window;
+  const long long kept = next - kept_first;
+  if (c->ring->append_only && kept > c->ring->cap)
+    return fail(c->err, DFLASH_EFULL, "%lld context rows exceed max_context %lld", kept, c->ring->cap);
+  CK(c->err, launch_ring_reset(c->ring->st, kept_first, c->stream));
+  const char* src = static_cast<const char*>(resid) + (size_t)(kept_first - first_pos) * c->kin * c->esz;
+  for (long long s = 0; s < kept; s += c->ing_rows) {
+    const int n = static_cast<int>(kept - s < c->ing_rows ? kept - s : c->ing_rows);
+    int rc = context_rows_to_ring(c, src + (size_t)s * c->kin * c->esz, n, c->ing_f, c->ing_c,
+                                  c->ing_kv, c->ing_rope, 0, kept_first + s);
+    if (rc) return rc;
+  }
+  CK(c->err, launch_ring_advance(c->ring->st, static_cast<int>(kept), 2, c->stream));
+  CK(c->err, launch_set_anchor(c->rs, anchor, c->stream));
+  c->ring->host_base = kept_first;
+  c->ring->pos_hi = next;
+  c->ring->host_appended = 0;
+  c->has_context = true;
+  c->appended_block = 0;
+  return DFLASH_OK;
+}
+
+int dflash_set_anchor(dflash_ctx* c, int32_t anchor) {
+  if (!c) return DFLASH_EINVAL;
+  if (anchor < 0 || anchor >= c->V)
+    return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
+  CK(c->err, launch_set_anchor(c->rs, anchor, c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
+  if (!c) return DFLASH_EINVAL;
+  if (!draft_ids) return fail(c->err, DFLASH_EINVAL, "draft_ids is NULL");
+  if (block < 2 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
+  if (!c->has_context) return fail(c->err, DFLASH_EEMPTY, "no context ingested");
+  const int dspark = c->cfg.kind == DFLASH_KIND_DSPARK;
+  const int rows = dspark ? block - 1 : block;
+  const int read0 = dspark ? 0 : 1;
+  const int R = block - 1;
+  const int dt = c->dt;
+  cudaStream_t st = c->stream;
+  CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rows, c->x,
+                                c->ring->st, c->inv_freq, c->half, rows, c->rope, st));
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    int rc = layer_forward(c, l, rows);
+    if (rc) return rc;
+  }
+  CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
+                            c->cfg.rms_eps, st));
+  const bool markov = c->cfg.markov_rank > 0;
+  LmHeadArgs lm{};
+  lm.x = static_cast<char*>(c->xf) + (size_t)read0 * c->H * c->esz;
+  lm.ldx = c->H;
+  lm.w = c->lm_head;
+  lm.R = R; lm.H = c->H; lm.V = c->V;
+  lm.softcap = c->cfg.softcap;
+  lm.ids = markov ? c->backbone_ids : draft_ids;
+  lm.ids2 = markov ? nullptr : c->backbone_ids;
+  lm.maxv = c->maxv;
+  lm.logits = (markov && c->cfg.markov_add) ? c->zlog : nullptr;
+  lm.part_v = c->lm_pv; lm.part_i = c->lm_pi;
+  lm.counter = c->counters + 0;
+  lm.grid = c->lm_grid;
+  CK(c->err, launch_lmhead_argmax(dt, lm, st));
+  if (markov) {
+    MarkovArgs mk{};
+    mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
+    mk.rs = c->rs; mk.anchor_host = -1;
+    mk.z = c->cfg.markov_add ? c->zlog : nullptr; mk.ldz = c->V;
+    mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
+    mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2;
+    mk.grid = c->mk_grid;
+    CK(c->err, launch_markov_chain(dt, mk, st));
+  }
+  c->last_draft_block = block;
+  return DFLASH_OK;
+}
+
+int dflash_verify_accept(dflash_ctx* c, const void* target_logits, int32_t block,
+                         const int32_t* draft_ids, int32_t* tokens, int32_t* n) {
+  if (!c) return DFLASH_EINVAL;
+  if (!target_logits || !draft_ids || !tokens || !n)
+    return fail(c->err, DFLASH_EINVAL, "a verify pointer is NULL");
+  if (block < 2 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
+  VerifyArgs v{};
+  v.L = target_logits; v.B = block; v.V = c->V; v.d = draft_ids; v.tokens = tokens; v.n = n;
+  v.rs = c->rs; v.part_v = c->vf_pv; v.part_i = c->vf_pi; v.counter = c->counters + 1;
+  v.chunks = c->vf_chunks;
+  CK(c->err, launch_verify(c->dt, v, c->stream));
+  c->last_verify_block = block;
+  return DFLASH_OK;
+}
+
+int dflash_append_block(dflash_ctx* c, const void* resid, int32_t block) {
+  if (!c) return DFLASH_EINVAL;
+  if (!resid || !aligned16(resid)) return fail(c->err, DFLASH_EINVAL, "resid is NULL or misaligned");
+  if (block < 1 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [1, max_block=%d]", block, c->cfg.max_block);
+  if (!c->has_context) return fail(c->err, DFLASH_EEMPTY, "no context ingested");
+  if (c->appended_block) return fail(c->err, DFLASH_ESTATE, "append without a commit of the previous append");
+  int rc = ensure_room(c, block);
+  if (rc) return rc;
+  rc = context_rows_to_ring(c, resid, block, c->app_f, c->app_c, c->app_kv, c->app_rope, 1, 0);
+  if (rc) return rc;
+  CK(c->err, launch_ring_advance(c->ring->st, block, 0, c->stream));
+  c->appended_block = block;
+  c->ring->host_appended = block;
+  c->ring->pos_hi += block;
+  return DFLASH_OK;
+}
+
+int dflash_commit(dflash_ctx* c, int32_t keep) {
+  if (!c) return DFLASH_EINVAL;
+  if (!c->appended_block) return fail(c->err, DFLASH_ESTATE, "commit without an append");
+  if (keep > c->appended_block)
+    return fail(c->err, DFLASH_EINVAL, "keep %d exceeds the appended block %d", keep, c->appended_block);
+  if (keep < 0 && c->last_verify_block != c->appended_block)
+    return fail(c->err, DFLASH_ESTATE, "commit(-1) needs a verify at the appended width %d", c->appended_block);
+  CK(c->err, launch_commit(c->rs, c->ring->st, c->appended_block, keep, c->stream));
+  if (keep >= 0) c->ring->pos_hi -= c->appended_block - keep;
+  c->appended_block = 0;
+  c->last_verify_block = 0;
+  c->ring->host_appended = 0;
+  return DFLASH_OK;
+}
+
+int dflash_round(dflash_ctx* c, const void* target_logits, const void* resid, int32_t block,
+                 int32_t* draft_ids, int32_t* tokens, int32_t* n) {
+  int rc = dflash_draft_block(c, block, draft_ids);
+  if (!rc) rc = dflash_verify_accept(c, target_logits, block, draft_ids, tokens, n);
+  if (!rc) rc = dflash_append_block(c, resid, block);
+  if (!rc) rc = dflash_commit(c, -1);
+  return rc;
+}
+
+int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const float* z, int32_t* out) {
+  if (!c) return DFLASH_EINVAL;
+  if (!out) return fail(c->err, DFLASH_EINVAL, "out is NULL");
+  if (c->cfg.markov_rank <= 0) return fail(c->err, DFLASH_ERANGE, "the config has no Markov head");
+  if (anchor < 0 || anchor >= c->V)
+    return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
+  if (gamma < 1 || gamma > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "gamma %d outside [1, max_block]", gamma);
+  MarkovArgs mk{};
+  mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
+  mk.rs = c->rs; mk.anchor_host = anchor; mk.z = z; mk.ldz = c->V; mk.gamma = gamma;
+  mk.out = out; mk.out2 = nullptr;
+  mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2; mk.grid = c->mk_grid;
+  CK(c->err, launch_markov_chain(c->dt, mk, c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_get_hidden(dflash_ctx* c, void* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
+  const int rows = c->cfg.kind == DFLASH_KIND_DSPARK ? c->last_draft_block - 1 : c->last_draft_block;
+  CK(c->err, cudaMemcpyAsync(out, c->xf, (size_t)rows * c->H * c->esz, cudaMemcpyDeviceToDevice, c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_get_draft_max_logit(dflash_ctx* c, float* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
+  CK(c->err, cudaMemcpyAsync(out, c->maxv, sizeof(float) * (c->last_draft_block - 1),
+                             cudaMemcpyDeviceToDevice, c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_get_backbone_ids(dflash_ctx* c, int32_t* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
+  CK(c->err, cudaMemcpyAsync(out, c->backbone_ids, sizeof(int) * (c->last_draft_block - 1),
+                             cudaMemcpyDeviceToDevice, c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_get_state(dflash_ctx* c, dflash_round_state* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  RoundState rs;
+  RingState ring;
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  CK(c->err, cudaMemcpy(&rs, c->rs, sizeof rs, cudaMemcpyDeviceToHost));
+  CK(c->err, cudaMemcpy(&ring, c->ring->st, sizeof ring, cudaMemcpyDeviceToHost));
+  out->position = ring.offset;
+  out->anchor = rs.anchor;
+  out->last_n = rs.n;
+  out->last_accepted = rs.a;
+  out->error = rs.error | ring.error;
+  return DFLASH_OK;
+}
+
+int dflash_get_stats(dflash_ctx* c, dflash_stats* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  RoundState rs;
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  CK(c->err, cudaMemcpy(&rs, c->rs, sizeof rs, cudaMemcpyDeviceToHost));
+  out->rounds = rs.rounds;
+  out->draft_n = rs.proposed;
+  out->accepted = rs.accepted;
+  out->emitted = rs.emitted;
+  return DFLASH_OK;
+}
+
+int dflash_reset_stats(dflash_ctx* c) {
+  if (!c) return DFLASH_EINVAL;
+  CK(c->err, cudaMemsetAsync(&c->rs->rounds, 0, 4 * sizeof(long long), c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_ring(dflash_ctx* c, ring_cache** out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  *out = c->ring;
+  return DFLASH_OK;
+}
+
+int dflash_capture_begin(dflash_ctx* c) {
+  if (!c) return DFLASH_EINVAL;
+  if (c->capturing) return fail(c->err, DFLASH_ESTATE, "already capturing");
+  if (!c->stream) return fail(c->err, DFLASH_ESTATE, "the legacy default stream cannot be captured");
+  CK(c->err, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+  c->capturing = true;
+  c->saved_flags[0] = c->last_draft_block;
+  c->saved_flags[1] = c->last_verify_block;
+  c->saved_flags[2] = c->appended_block;
+  c->saved_flags[3] = static_cast<int>(c->ring->pos_hi - c->ring->host_base);
+  return DFLASH_OK;
+}
+
+int dflash_capture_end(dflash_ctx* c, int32_t slot) {
+  if (!c) return DFLASH_EINVAL;
+  if (!c->capturing) return fail(c->err, DFLASH_ESTATE, "not capturing");
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(c->stream, &g);
+  c->capturing = false;
+  c->last_draft_block = c->saved_flags[0];
+  c->last_verify_block = c->saved_flags[1];
+  c->appended_block = c->saved_flags[2];
+  c->ring->pos_hi = c->ring->host_base + c->saved_flags[3];
+  if (e != cudaSuccess) { if (g) cudaGraphDestroy(g); return cuda_fail(c->err, e, "cudaStreamEndCapture"); }
+  if (slot < 0 || slot >= 64) { cudaGraphDestroy(g); return fail(c->err, DFLASH_ERANGE, "slot %d outside [0, 64)", slot); }
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_fail(c->err, e, "cudaGraphInstantiate");
+  if (c->graphs[slot]) cudaGraphExecDestroy(c->graphs[slot]);
+  c->graphs[slot] = ex;
+  return DFLASH_OK;
+}
+
+int dflash_graph_launch(dflash_ctx* c, int32_t slot) {
+  if (!c) return DFLASH_EINVAL;
+  if (slot < 0 || slot >= 64 || !c->graphs[slot]) return fail(c->err, DFLASH_ESTATE, "graph slot %d is empty", slot);
+  CK(c->err, cudaGraphLaunch(c->graphs[slot], c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_sync(dflash_ctx* c) {
+  if (!c) return DFLASH_EINVAL;
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_synth_target(dflash_ctx* c, const void* logit_pool, const void* plant,
+                        const uint8_t* coins, const void* resid_pool, int32_t n_logit_pool,
+                        int32_t n_coin_rows, int32_t n_resid_pool, int32_t block_max, int32_t block,
+                        const int32_t* draft_ids, void* logits_out, void* resid_out) {
+  if (!c) return DFLASH_EINVAL;
+  if (!logit_pool || !plant || !coins || !resid_pool || !draft_ids || !logits_out || !resid_out)
+    return fail(c->err, DFLASH_EINVAL, "a stand-in target pointer is NULL");
+  if (n_logit_pool < 1 || n_coin_rows < 1 || n_resid_pool < 1)
+    return fail(c->err, DFLASH_EINVAL, "pool sizes must be positive");
+  if (block < 2 || block > block_max || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [2, min(block_max, max_block)]", block);
+  SynthArgs a{};
+  a.logit_pool = logit_pool; a.plant = plant; a.coins = coins; a.resid_pool = resid_pool;
+  a.n_logit = n_logit_pool; a.n_coin = n_coin_rows; a.n_resid = n_resid_pool;
+  a.block_max = block_max; a.block = block; a.V = c->V; a.kin = c->kin;
+  a.d = draft_ids; a.logits_out = logits_out; a.resid_out = resid_out; a.rs = c->rs;
+  CK(c->err, launch_synth_target(c->dt, a, c->stream));
+  return DFLASH_OK;
+}
+
+// ---- standalone ring ----------------------------------------------------------------
+int ring_cache_create_ex(int32_t n_layers, int32_t kv_heads, int32_t head_dim, int32_t window,
+                         int32_t max_block, int32_t dtype, int32_t max_context, int32_t flags,
+                         void* stream, ring_cache** out) {
+  return ring_create_impl(n_layers, kv_heads, head_dim, window, max_block, dtype, max_context,
+                          flags, static_cast<cudaStream_t>(stream), out, g_create_err);
+}
+
+int ring_cache_create(int32_t n_layers, int32_t kv_heads, int32_t head_dim, int32_t window,
+                      int32_t max_block, int32_t dtype, int32_t max_context, void* stream,
+                      ring_cache** out) {
+  return ring_cache_create_ex(n_layers, kv_heads, head_dim, window, max_block, dtype, max_context,
+                              0, stream, out);
+}
+
+void ring_cache_destroy(ring_cache* r) {
+  if (!r || r->owned_by_ctx) return;
+  cudaStreamSynchronize(r->stream);
+  ring_free(r);
+}
+
+int ring_cache_append(ring_cache* r, const void* k, const void* v, int32_t n) {
+  if (!r) return DFLASH_EINVAL;
+  if (n < 0 || n > r->cap) return fail(r->err, DFLASH_EINVAL, "n = %d outside [0, capacity=%lld]", n, r->cap);
+  if (n == 0) return DFLASH_OK;
+  if (!k || !v) return fail(r->err, DFLASH_EINVAL, "k or v is NULL");
+  if (r->append_only && r->pos_hi + n - r->host_base > r->cap) {
+    long long off;
+    int rc = ring_sync_offset(r, &off);
+    if (rc) return rc;
+    r->pos_hi = off;
+    if (off + n - r->host_base > r->cap)
+      return fail(r->err, DFLASH_EFULL, "append-only ring full (%lld + %d > %lld)", off - r->host_base, n, r->cap);
+  }
+  CK(r->err, launch_ring_append(r->dtype, k, v, r->L, n, r->nkv, r->hd, r->k, r->v, r->cap, r->st,
+                                r->stream));
+  r->host_appended += n;
+  r->pos_hi += n;
+  return DFLASH_OK;
+}
+
+int ring_cache_trim(ring_cache* r, int32_t m) {
+  if (!r) return DFLASH_EINVAL;
+  if (m < 0) return fail(r->err, DFLASH_EINVAL, "trim of %d rows", m);
+  if (m > r->host_appended)
+    return fail(r->err, DFLASH_EREWIND, "short rewind: trim %d > %d rows appended since the last trim",
+                m, r->host_appended);
+  CK(r->err, launch_ring_advance(r->st, m, 1, r->stream));
+  r->host_appended = 0;
+  r->pos_hi -= m;
+  return DFLASH_OK;
+}
+
+int ring_cache_offset(ring_cache* r, int64_t* off) {
+  if (!r || !off) return DFLASH_EINVAL;
+  long long o;
+  int rc = ring_sync_offset(r, &o);
+  if (rc) return rc;
+  *off = o;
+  return DFLASH_OK;
+}
+
+int ring_cache_capacity(const ring_cache* r, int64_t* cap) {
+  if (!r || !cap) return DFLASH_EINVAL;
+  *cap = r->cap;
+  return DFLASH_OK;
+}
+
+int ring_cache_gather(ring_cache* r, int64_t pos0, int32_t count, void* k_out, void* v_out) {
+  if (!r) return DFLASH_EINVAL;
+  if (!k_out || !v_out || count < 0 || pos0 < 0)
+    return fail(r->err, DFLASH_EINVAL, "bad gather arguments");
+  CK(r->err, launch_ring_gather(r->dtype, r->k, r->v, r->L, r->cap, r->nkv, r->hd, pos0, count,
+                                k_out, v_out, r->stream));
+  return DFLASH_OK;
+}
+
+const char* ring_cache_last_error(const ring_cache* r) { return r ? r->err.c_str() : g_create_err.c_str(); }
+
+}  // extern "C"
