@@ -167,7 +167,9 @@ def to_device(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     else:
         t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
-    return t.to(device)
+    t = t.to(device)
+    torch.cuda.current_stream().synchronize()
+    return t
 
 
 def weights_to_device(w: dict, dtype: str, device="cuda") -> dict:
@@ -267,44 +269,62 @@ class DFlashContext:
         if rc:
             raise DFlashError(rc, last_error(None))
         self.h = h.value
+        self._capturing = False
 
     def _check(self, rc):
         if rc:
             raise DFlashError(rc, lib.dflash_last_error(self.h).decode())
 
+    def _prep(self):
+        """Order the context's stream after the caller's current torch stream,
+        so tensors torch just wrote are ready (skipped while capturing)."""
+        if not self._capturing:
+            self.stream.wait_stream(torch.cuda.current_stream())
+
     def ingest_context(self, resid, rows, first_pos, anchor):
+        self._prep()
         self._check(lib.dflash_ingest_context(self.h, _ptr(resid), rows, first_pos, anchor))
 
     def set_anchor(self, anchor):
+        self._prep()
         self._check(lib.dflash_set_anchor(self.h, anchor))
 
     def draft_block(self, block, draft_ids):
+        self._prep()
         self._check(lib.dflash_draft_block(self.h, block, _ptr(draft_ids)))
 
     def verify_accept(self, logits, block, draft_ids, tokens, n):
+        self._prep()
         self._check(lib.dflash_verify_accept(self.h, _ptr(logits), block, _ptr(draft_ids),
                                              _ptr(tokens), _ptr(n)))
 
     def append_block(self, resid, block):
+        self._prep()
         self._check(lib.dflash_append_block(self.h, _ptr(resid), block))
 
     def commit(self, keep=-1):
+        self._prep()
         self._check(lib.dflash_commit(self.h, keep))
 
     def round(self, logits, resid, block, draft_ids, tokens, n):
+        self._prep()
         self._check(lib.dflash_round(self.h, _ptr(logits), _ptr(resid), block, _ptr(draft_ids),
                                      _ptr(tokens), _ptr(n)))
 
     def markov_chain(self, anchor, gamma, z, out):
+        self._prep()
         self._check(lib.dflash_markov_chain(self.h, anchor, gamma, _ptr(z), _ptr(out)))
 
     def get_hidden(self, out):
+        self._prep()
         self._check(lib.dflash_get_hidden(self.h, _ptr(out)))
 
     def get_draft_max_logit(self, out):
+        self._prep()
         self._check(lib.dflash_get_draft_max_logit(self.h, _ptr(out)))
 
     def get_backbone_ids(self, out):
+        self._prep()
         self._check(lib.dflash_get_backbone_ids(self.h, _ptr(out)))
 
     def state(self) -> dict:
@@ -328,9 +348,12 @@ class DFlashContext:
         return RingCache(handle=h.value, owner=self)
 
     def capture_begin(self):
+        self._prep()
         self._check(lib.dflash_capture_begin(self.h))
+        self._capturing = True
 
     def capture_end(self, slot):
+        self._capturing = False
         self._check(lib.dflash_capture_end(self.h, slot))
 
     def graph_launch(self, slot):
@@ -341,6 +364,7 @@ class DFlashContext:
 
     def synth_target(self, logit_pool, plant, coins, resid_pool, block, draft_ids, logits_out,
                      resid_out):
+        self._prep()
         self._check(lib.dflash_synth_target(
             self.h, _ptr(logit_pool), _ptr(plant), _ptr(coins), _ptr(resid_pool),
             logit_pool.shape[0], coins.shape[0], resid_pool.shape[0], logit_pool.shape[1], block,
