@@ -99,6 +99,9 @@ _sig("dflash_capture_begin", ctypes.c_int, _vp)
 _sig("dflash_capture_end", ctypes.c_int, _vp, _i32)
 _sig("dflash_graph_launch", ctypes.c_int, _vp, _i32)
 _sig("dflash_sync", ctypes.c_int, _vp)
+_sig("dflash_graph_kernel_count", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
+_sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
+_sig("dflash_lm_head_elapsed_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float))
 _sig("dflash_synth_target", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
      _vp, _vp, _vp)
 _sig("ring_cache_create", ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
@@ -361,6 +364,19 @@ class DFlashContext:
 
     def sync(self):
         self._check(lib.dflash_sync(self.h))
+
+    def graph_kernel_count(self, slot) -> int:
+        o = _i64()
+        self._check(lib.dflash_graph_kernel_count(self.h, slot, ctypes.byref(o)))
+        return o.value
+
+    def lm_head_timing(self, enable: bool):
+        self._check(lib.dflash_lm_head_timing(self.h, 1 if enable else 0))
+
+    def lm_head_elapsed_ms(self) -> float:
+        o = ctypes.c_float()
+        self._check(lib.dflash_lm_head_elapsed_ms(self.h, ctypes.byref(o)))
+        return o.value
 
     def synth_target(self, logit_pool, plant, coins, resid_pool, block, draft_ids, logits_out,
                      resid_out):

@@ -8,6 +8,8 @@ No cmake; a rebuild only recompiles sources newer than their object.
 from __future__ import annotations
 
 import os
+import platform
+import struct
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -15,7 +17,7 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(ROOT, "_build")
+BUILD = os.path.join(ROOT, "_build", platform.machine())
 LIB = os.path.join(PKG, "libdflash.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -52,12 +54,29 @@ def _compile(src: str, force: bool) -> str:
     return obj
 
 
+_ELF_MACHINE = {"x86_64": 62, "aarch64": 183}
+
+
+def _lib_matches_host() -> bool:
+    """False if an existing libdflash.so was linked for another CPU."""
+    try:
+        with open(LIB, "rb") as f:
+            head = f.read(20)
+        return struct.unpack("<H", head[18:20])[0] == _ELF_MACHINE.get(platform.machine(), -1)
+    except (OSError, struct.error):
+        return False
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
+    if not _lib_matches_host():
+        force_link = True
+    else:
+        force_link = False
     srcs = sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(s, force), srcs))
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
+    if force or force_link or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         cmd = [nvcc()] + ARCH + ["-shared", "-o", LIB] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -172,6 +172,10 @@ struct dflash_ctx {
   bool capturing = false;
   int saved_flags[4] = {0, 0, 0, 0};
   cudaGraphExec_t graphs[64] = {};
+  long long graph_kernels[64] = {};
+  cudaEvent_t lm_ev[2] = {nullptr, nullptr};
+  bool lm_timing = false;
+  bool lm_recorded = false;
   std::string err;
 };
 
@@ -376,6 +380,8 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
     if (g) cudaGraphExecDestroy(g);
   ring_free(ctx->ring);
   cudaFree(ctx->arena);
+  for (auto& ev : ctx->lm_ev)
+    if (ev) cudaEventDestroy(ev);
   delete ctx;
 }
 
@@ -483,6 +489,8 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
                            cudaMemcpyHostToDevice, c->stream)) != cudaSuccess ||
       (e = init_lmhead_attrs(c->H)) != cudaSuccess ||
       (e = init_attention_attrs(c->hd)) != cudaSuccess ||
+      (e = cudaEventCreate(&c->lm_ev[0])) != cudaSuccess ||
+      (e = cudaEventCreate(&c->lm_ev[1])) != cudaSuccess ||
       (e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
     dflash_ctx_destroy(c);
     return cuda_fail(err, e, "context initialisation");
@@ -565,7 +573,12 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   lm.part_v = c->lm_pv; lm.part_i = c->lm_pi;
   lm.counter = c->counters + 0;
   lm.grid = c->lm_grid;
+  if (c->lm_timing) CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
   CK(c->err, launch_lmhead_argmax(dt, lm, st));
+  if (c->lm_timing) {
+    CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
+    c->lm_recorded = true;
+  }
   if (markov) {
     MarkovArgs mk{};
     mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
@@ -746,12 +759,23 @@ int dflash_capture_end(dflash_ctx* c, int32_t slot) {
   c->ring->pos_hi = c->ring->host_base + c->saved_flags[3];
   if (e != cudaSuccess) { if (g) cudaGraphDestroy(g); return cuda_fail(c->err, e, "cudaStreamEndCapture"); }
   if (slot < 0 || slot >= 64) { cudaGraphDestroy(g); return fail(c->err, DFLASH_ERANGE, "slot %d outside [0, 64)", slot); }
+  size_t nn = 0;
+  long long kernels = 0;
+  if (cudaGraphGetNodes(g, nullptr, &nn) == cudaSuccess && nn) {
+    std::vector<cudaGraphNode_t> nodes(nn);
+    if (cudaGraphGetNodes(g, nodes.data(), &nn) == cudaSuccess)
+      for (size_t i = 0; i < nn; ++i) {
+        cudaGraphNodeType t;
+        if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
+      }
+  }
   cudaGraphExec_t ex = nullptr;
   e = cudaGraphInstantiate(&ex, g, 0);
   cudaGraphDestroy(g);
   if (e != cudaSuccess) return cuda_fail(c->err, e, "cudaGraphInstantiate");
   if (c->graphs[slot]) cudaGraphExecDestroy(c->graphs[slot]);
   c->graphs[slot] = ex;
+  c->graph_kernels[slot] = kernels;
   return DFLASH_OK;
 }
 
@@ -759,6 +783,27 @@ int dflash_graph_launch(dflash_ctx* c, int32_t slot) {
   if (!c) return DFLASH_EINVAL;
   if (slot < 0 || slot >= 64 || !c->graphs[slot]) return fail(c->err, DFLASH_ESTATE, "graph slot %d is empty", slot);
   CK(c->err, cudaGraphLaunch(c->graphs[slot], c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_graph_kernel_count(dflash_ctx* c, int32_t slot, int64_t* out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  if (slot < 0 || slot >= 64 || !c->graphs[slot]) return fail(c->err, DFLASH_ESTATE, "graph slot %d is empty", slot);
+  *out = c->graph_kernels[slot];
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_timing(dflash_ctx* c, int32_t enable) {
+  if (!c) return DFLASH_EINVAL;
+  c->lm_timing = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_elapsed_ms(dflash_ctx* c, float* ms) {
+  if (!c || !ms) return DFLASH_EINVAL;
+  if (!c->lm_recorded) return fail(c->err, DFLASH_ESTATE, "lm_head timing events never recorded");
+  CK(c->err, cudaEventSynchronize(c->lm_ev[1]));
+  CK(c->err, cudaEventElapsedTime(ms, c->lm_ev[0], c->lm_ev[1]));
   return DFLASH_OK;
 }
 

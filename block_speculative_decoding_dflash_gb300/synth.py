@@ -15,7 +15,9 @@ from the fp32 draw by ``torch``'s conversion).
 from __future__ import annotations
 
 import copy
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -62,22 +64,45 @@ def _stream(seed: int, name: str) -> np.random.Generator:
     return np.random.default_rng([int(seed), zlib.crc32(name.encode())])
 
 
+def _f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round finite fp32 values to bfloat16 bit patterns, nearest-even."""
+    u = a.view(np.uint32)
+    return ((u + (np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1)))) >> 16).astype(np.uint16)
+
+
 def to_storage(a: np.ndarray, dtype: str) -> np.ndarray:
     """fp32 array -> storage array (float32, or uint16 bf16 bits)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    if dtype == "f32":
-        return a
-    import torch
-    t = torch.from_numpy(a).to(torch.bfloat16)
-    return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return a if dtype == "f32" else _f32_to_bf16_bits(a)
+
+
+_CHUNK = 1 << 22
 
 
 def normal(seed: int, name: str, shape, std: float, dtype: str) -> np.ndarray:
-    g = _stream(seed, name)
-    a = g.standard_normal(int(np.prod(shape)), dtype=np.float32).reshape(shape)
-    if std != 1.0:
-        a *= np.float32(std)
-    return to_storage(a, dtype)
+    """N(0, std) tensor in storage format. Element i belongs to chunk
+    i // 2^22, and chunk c is drawn from its own PCG64 stream keyed by
+    (seed, name, c), so large tensors are drawn on all cores with values
+    independent of the thread count."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
+    key = zlib.crc32(name.encode())
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = np.random.default_rng([int(seed), key, c])
+        x = g.standard_normal(hi - lo, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        out[lo:hi] = _f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+    chunks = (n + _CHUNK - 1) // _CHUNK
+    if chunks > 1:
+        with ThreadPoolExecutor(max_workers=min(chunks, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(chunks)))
+    else:
+        fill(0)
+    return out.reshape(shape)
 
 
 def ones(shape, dtype: str) -> np.ndarray:

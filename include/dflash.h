@@ -271,6 +271,18 @@ int dflash_capture_end(dflash_ctx* ctx, int32_t slot);
 int dflash_graph_launch(dflash_ctx* ctx, int32_t slot);
 /* Waits for the context's stream (syncs). */
 int dflash_sync(dflash_ctx* ctx);
+/* Number of kernel launches graph slot `slot` holds (its kernel nodes). */
+int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
+
+/* ---- measurement ------------------------------------------------------------- */
+
+/* When enabled, dflash_draft_block brackets its lm_head kernel with two CUDA
+ * events owned by the context, recorded on the context's stream (as event
+ * nodes when the draft is being captured into a graph). */
+int dflash_lm_head_timing(dflash_ctx* ctx, int32_t enable);
+/* Milliseconds between the two events as last recorded (syncs on the end
+ * event). ESTATE if they were never recorded. */
+int dflash_lm_head_elapsed_ms(dflash_ctx* ctx, float* ms_host);
 
 /* ---- stand-in target (benchmark and test harness) ---------------------------- */
 

@@ -21,8 +21,22 @@ from block_speculative_decoding_dflash_gb300 import synth
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
-def f64_weights(w: dict, dtype: str) -> dict:
-    out = {k: O.as_f64(v, dtype) for k, v in w.items() if k != "layers"}
+class LazyRows:
+    """Rows of a stored table converted to fp64 only when indexed (the
+    embedding gather reads a handful of rows of a [V, H] table)."""
+
+    def __init__(self, a, dtype):
+        self.a, self.dtype = a, dtype
+
+    def __getitem__(self, idx):
+        return O.as_f64(self.a[idx], self.dtype)
+
+
+def f64_weights(w: dict, dtype: str, lazy_embed: bool = False) -> dict:
+    out = {k: O.as_f64(v, dtype) for k, v in w.items()
+           if k != "layers" and not (lazy_embed and k == "embed")}
+    if lazy_embed:
+        out["embed"] = LazyRows(w["embed"], dtype)
     out["layers"] = [{k: O.as_f64(v, dtype) for k, v in lw.items()} for lw in w["layers"]]
     return out
 
@@ -61,13 +75,13 @@ def check_ids(got, ref_ids, ref_logits, tol, what):
 class Pair:
     """A GPU context and an oracle session fed the same inputs."""
 
-    def __init__(self, cfg: dict, seed: int = 0, weights=None):
+    def __init__(self, cfg: dict, seed: int = 0, weights=None, w64=None, wd=None):
         self.cfg = cfg
         self.dt = cfg["dtype"]
         self.tol = TOL[self.dt]
         self.w = weights if weights is not None else synth.make_weights(cfg, seed)
-        self.wd = B.weights_to_device(self.w, self.dt)
-        self.w64 = f64_weights(self.w, self.dt)
+        self.wd = wd if wd is not None else B.weights_to_device(self.w, self.dt)
+        self.w64 = w64 if w64 is not None else f64_weights(self.w, self.dt)
         self.ctx = B.DFlashContext(cfg, self.wd)
         self.sess = O.OracleSession(cfg, self.w64)
         self.ties = 0
@@ -132,9 +146,12 @@ class Pair:
         assert t[:nn].tolist() == tokens.tolist() and np.all(t[nn:] == -1)
         return tokens, nn
 
-    def append_commit(self, resid_rows: np.ndarray, block: int, keep: int, tokens, accepted: int):
+    def append_commit(self, resid_rows: np.ndarray, block: int, gpu_keep: int, keep: int, tokens,
+                      accepted: int):
+        """GPU: append + commit(gpu_keep) (-1: the verify's n); oracle: the
+        same rows, keeping ``keep``."""
         self.ctx.append_block(self.to_dev(resid_rows), block)
-        self.ctx.commit(keep)
+        self.ctx.commit(gpu_keep)
         self.sess.append_and_trim(O.as_f64(resid_rows, self.dt), keep)
         self.sess.commit(keep, int(tokens[-1]), block, accepted)
 
@@ -177,7 +194,7 @@ class Pair:
         tokens, nn = self.verify(L, ids_dev, got, block)
         k = nn if keep is None else keep
         self.append_commit(synth.resid_rows(stream, r, block), block, -1 if keep is None else keep,
-                           tokens, nn - 1)
+                           k, tokens, nn - 1)
         return nn, k
 
     def close(self):
