@@ -59,6 +59,25 @@ def assert_rows_close(got, ref, tol, what):
     assert bad.size == 0, f"{what}: rows {bad[:8].tolist()} rel err {(err / scale)[bad[:8]].tolist()}"
 
 
+def assert_hidden_close(got, ref, tol, dtype, what):
+    """Final hidden rows. fp32: max-abs <= tol * row max. bf16: relative L2
+    error <= tol and max-abs <= 2 * tol * row max per row. After five
+    bf16 layers an fp32-accumulating implementation with the oracle's own
+    rounding points already deviates from the fp64 oracle by up to ~2% of the
+    row max on single elements (a few bf16 ulps at the largest element, from
+    residual sums that round to the neighbouring value), with ~1.4% relative
+    L2; the bound is set at that arithmetic, not at the logit rule."""
+    if dtype == "f32":
+        return assert_rows_close(got, ref, tol, what)
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    l2 = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    mx = np.abs(got - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)
+    bad = np.nonzero((l2 > tol) | (mx > 2 * tol))[0]
+    assert bad.size == 0, f"{what}: rows {bad[:8].tolist()} l2 {l2[bad[:8]].tolist()} maxabs {mx[bad[:8]].tolist()}"
+
+
 def check_ids(got, ref_ids, ref_logits, tol, what):
     """Exact, except at a near tie of the oracle's logits."""
     ties = 0
@@ -105,7 +124,7 @@ class Pair:
             rows = ref["hidden"].shape[0]
             hid = torch.empty(rows, self.cfg["hidden"], dtype=torch_dtype(self.dt), device=self.dev)
             self.ctx.get_hidden(hid)
-            assert_rows_close(dev_to_f64(hid), ref["hidden"], self.tol, "final hidden")
+            assert_hidden_close(dev_to_f64(hid), ref["hidden"], self.tol, self.dt, "final hidden")
             mx = torch.empty(block - 1, dtype=torch.float32, device=self.dev)
             self.ctx.get_draft_max_logit(mx)
             zmax = ref["logits"].max(axis=1).astype(np.float64)
