@@ -103,6 +103,10 @@ enum LayerW { kInNorm, kWq, kWk, kWv, kQNorm, kKNorm, kWo, kPostNorm, kWg, kWu, 
 
 }  // namespace
 
+namespace dfl {
+void set_global_error(const char* msg) { g_create_err = msg; }
+}  // namespace dfl
+
 // ---------------------------------------------------------------------------
 // Objects
 // ---------------------------------------------------------------------------

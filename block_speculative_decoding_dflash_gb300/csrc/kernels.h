@@ -112,6 +112,8 @@ struct VerifyArgs {
 };
 cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st);
 int verify_chunks(int V);
+// Text returned by dflash_last_error(NULL).
+void set_global_error(const char* msg);
 
 cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
                           cudaStream_t st);

@@ -284,6 +284,32 @@ int dflash_lm_head_timing(dflash_ctx* ctx, int32_t enable);
  * event). ESTATE if they were never recorded. */
 int dflash_lm_head_elapsed_ms(dflash_ctx* ctx, float* ms_host);
 
+/* ---- verify without allocation ------------------------------------------------ */
+
+/* The greedy verify of dflash_verify_accept for callers that cannot allocate
+ * device memory: no context (creating one allocates), no cudaMalloc, no
+ * cudaFree, no allocating library call. Meant for code whose device memory
+ * all comes from a host framework's own pool, or for a latency-critical loop
+ * that must never pay cudaMalloc's implicit device-wide synchronization. The
+ * pages have no counterpart of this call.
+ *
+ * Same result as dflash_verify_accept: tokens [block] = d_1..d_a, t_a, then
+ * -1 padding, and n [1] = a + 1, for target_logits [block, vocab] of `dtype`
+ * and draft_ids [block - 1], enqueued on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream). Its scratch is one static device array of
+ * about 64 KB that every GPU loading the library holds until the process
+ * exits, so it accepts only 2 <= block <= 64 and 2 <= vocab <= 1048576
+ * (ERANGE beyond, with the reason in dflash_last_error(NULL)). The first call
+ * on a device looks up the array's device address with that device current;
+ * make that first call before any stream capture. All calls share the array:
+ * calls that overlap on the GPU (other streams, other host threads) race.
+ * Returns EINVAL for a NULL pointer or a bad dtype, ECUDA if a CUDA call
+ * fails. */
+int dflash_verify_accept_static(const void* target_logits, int32_t dtype,
+                                int32_t vocab, int32_t block,
+                                const int32_t* draft_ids, int32_t* tokens,
+                                int32_t* n, void* stream);
+
 /* ---- stand-in target (benchmark and test harness) ---------------------------- */
 
 /* Fills the round's target inputs the way a target model would, from pools
