@@ -88,6 +88,8 @@ _sig("dflash_append_block", ctypes.c_int, _vp, _vp, _i32)
 _sig("dflash_commit", ctypes.c_int, _vp, _i32)
 _sig("dflash_round", ctypes.c_int, _vp, _vp, _vp, _i32, _vp, _vp, _vp)
 _sig("dflash_markov_chain", ctypes.c_int, _vp, _i32, _i32, _vp, _vp)
+_sig("dflash_linear", ctypes.c_int, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _i32)
+_sig("dflash_lm_head_argmax", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
 _sig("dflash_get_hidden", ctypes.c_int, _vp, _vp)
 _sig("dflash_get_draft_max_logit", ctypes.c_int, _vp, _vp)
 _sig("dflash_get_backbone_ids", ctypes.c_int, _vp, _vp)
@@ -317,6 +319,14 @@ class DFlashContext:
     def markov_chain(self, anchor, gamma, z, out):
         self._prep()
         self._check(lib.dflash_markov_chain(self.h, anchor, gamma, _ptr(z), _ptr(out)))
+
+    def linear(self, x, M, K, w, N, y, epi=0, w2=None, r=None):
+        self._prep()
+        self._check(lib.dflash_linear(self.h, _ptr(x), M, K, _ptr(w), _ptr(w2), N, _ptr(r), _ptr(y), epi))
+
+    def lm_head_argmax(self, x, rows, ids, maxv):
+        self._prep()
+        self._check(lib.dflash_lm_head_argmax(self.h, _ptr(x), rows, _ptr(ids), _ptr(maxv)))
 
     def get_hidden(self, out):
         self._prep()

@@ -51,6 +51,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int64_t kI32Max = std::numeric_limits<int32_t>::max();
 constexpr int kIngestChunk = 2048;
 constexpr int kMaxBlock = 1024;
+constexpr int kTcGrid = 256;      // upper bound of the tensor-core GEMM grid (SM count)
+constexpr int kTcTiles = 8192;    // split-tile ticket counters
 
 int check_config(const dflash_config* c, std::string& err) {
   if (!c) return fail(err, DFLASH_EINVAL, "config is NULL");
@@ -177,6 +179,20 @@ struct dflash_ctx {
   int saved_flags[4] = {0, 0, 0, 0};
   cudaGraphExec_t graphs[64] = {};
   long long graph_kernels[64] = {};
+  // tensor-core path (bf16 with 128-aligned output dims)
+  bool use_tc = false;
+  int num_sms = 148;
+  int R = 0;                                  // rows of every activation buffer
+  struct LayerMaps { CUtensorMap wq, wk, wv, wo, wg, wu, wd; };
+  std::vector<LayerMaps> lmaps;
+  CUtensorMap fc_map{}, lm_map{};
+  CUtensorMap xn_map[2]{}, attn_map[2]{}, sbuf_map[2]{}, appc_map[2]{}, xf_map[2][2]{};
+  float* tc_part = nullptr;
+  unsigned* tc_tiles = nullptr;
+  int* tc_err = nullptr;
+  float* tc_lm_pv = nullptr;
+  int* tc_lm_pi = nullptr;
+  unsigned* tc_done = nullptr;
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -256,6 +272,35 @@ const void* LW(const dflash_ctx* c, int l, int which) {
   return c->layers[(size_t)l * DFLASH_LAYER_TENSORS + which];
 }
 
+int bn_index(int M) { return M <= 16 ? 0 : 1; }
+int bn_of(int M) { return M <= 16 ? 16 : 32; }
+
+TcGemmArgs tc_args(dflash_ctx* c, int M, int N, int K, int epi) {
+  TcGemmArgs a{};
+  a.M = M; a.N = N; a.K = K; a.epi = epi;
+  a.tiles = (N + 127) / 128;
+  a.kchunks = K / 64;
+  a.partials = c->tc_part;
+  a.tile_ctr = c->tc_tiles;
+  a.err = c->tc_err;
+  return a;
+}
+
+void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMap*, int>> segs) {
+  int i = 0, tiles = 0;
+  for (auto& sg : segs) {
+    a.a_map[i] = *sg.first;
+    tiles += (sg.second + 127) / 128;
+    a.seg_tiles[i] = tiles;
+    ++i;
+  }
+  a.nseg = i;
+}
+
+cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
+  return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
+}
+
 // Context rows -> ring: fc -> hidden_norm -> per layer [Wk | Wv] -> k-norm +
 // RoPE / copy into ring slots. use_dev: positions from the device offset
 // (block append), else pos_host (ingest).
@@ -265,16 +310,34 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
   cudaStream_t st = c->stream;
   CK(c->err, launch_rope_table(c->inv_freq, c->half, use_dev ? c->ring->st : nullptr, pos_host,
                                rows, rope, st));
-  LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
-  a.w[0] = c->fc;
-  CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
+  const bool tc = c->use_tc && rows <= 32 && cn == c->app_c;
+  if (tc) {
+    TcGemmArgs t = tc_args(c, rows, c->H, c->kin, kEpiStore);
+    tc_segments(t, {{&c->fc_map, c->H}});
+    if (!tc_encode_map(&t.b_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, bn_of(rows)))
+      return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the residual rows");
+    t.y = f; t.ldy = c->H;
+    CK(c->err, tc_run(c, t));
+  } else {
+    LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
+    a.w[0] = c->fc;
+    CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
+  }
   CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
-    LinearArgs b = lin_args(cn, c->H, kv, 2 * c->kvdim, rows, 2 * c->kvdim, c->H);
-    b.nseg = 2;
-    b.w[0] = LW(c, l, kWk); b.seg_end[0] = c->kvdim;
-    b.w[1] = LW(c, l, kWv); b.seg_end[1] = 2 * c->kvdim;
-    CK(c->err, rows > 32 ? launch_linear_tiled(dt, b, st) : launch_linear_rows(dt, b, st));
+    if (tc) {
+      TcGemmArgs t = tc_args(c, rows, 2 * c->kvdim, c->H, kEpiStore);
+      tc_segments(t, {{&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
+      t.b_map = c->appc_map[bn_index(rows)];
+      t.y = kv; t.ldy = 2 * c->kvdim;
+      CK(c->err, tc_run(c, t));
+    } else {
+      LinearArgs b = lin_args(cn, c->H, kv, 2 * c->kvdim, rows, 2 * c->kvdim, c->H);
+      b.nseg = 2;
+      b.w[0] = LW(c, l, kWk); b.seg_end[0] = c->kvdim;
+      b.w[1] = LW(c, l, kWv); b.seg_end[1] = 2 * c->kvdim;
+      CK(c->err, rows > 32 ? launch_linear_tiled(dt, b, st) : launch_linear_rows(dt, b, st));
+    }
     const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
     CK(c->err, launch_kv_to_ring(dt, kv, 2 * c->kvdim, rows, c->nkv, c->hd, LW(c, l, kKNorm),
                                  c->cfg.rms_eps, rope, c->cfg.rope_neox,
@@ -290,12 +353,22 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   cudaStream_t st = c->stream;
   const float eps = c->cfg.rms_eps;
   CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st));
-  LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
-  q.nseg = 3;
-  q.w[0] = LW(c, l, kWq); q.seg_end[0] = c->qdim;
-  q.w[1] = LW(c, l, kWk); q.seg_end[1] = c->qdim + c->kvdim;
-  q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
-  CK(c->err, launch_linear_rows(dt, q, st));
+  const bool tc = c->use_tc && rows <= 32;
+  const int bi = bn_index(rows);
+  if (tc) {
+    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, kEpiStore);
+    tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
+    t.b_map = c->xn_map[bi];
+    t.y = c->qkv; t.ldy = c->qkv_n;
+    CK(c->err, tc_run(c, t));
+  } else {
+    LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
+    q.nseg = 3;
+    q.w[0] = LW(c, l, kWq); q.seg_end[0] = c->qdim;
+    q.w[1] = LW(c, l, kWk); q.seg_end[1] = c->qdim + c->kvdim;
+    q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
+    CK(c->err, launch_linear_rows(dt, q, st));
+  }
   CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
                                    c->rope, c->cfg.rope_neox, st));
   CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
@@ -317,16 +390,38 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
   CK(c->err, launch_attention(dt, at, st));
-  LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
-  o.w[0] = LW(c, l, kWo); o.epi = kEpiResid; o.r = c->x; o.ldr = c->H;
-  CK(c->err, launch_linear_rows(dt, o, st));
+  if (tc) {
+    TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
+    tc_segments(t, {{&c->lmaps[l].wo, c->H}});
+    t.b_map = c->attn_map[bi];
+    t.y = c->x; t.ldy = c->H; t.r = c->x; t.ldr = c->H;
+    CK(c->err, tc_run(c, t));
+  } else {
+    LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
+    o.w[0] = LW(c, l, kWo); o.epi = kEpiResid; o.r = c->x; o.ldr = c->H;
+    CK(c->err, launch_linear_rows(dt, o, st));
+  }
   CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st));
-  LinearArgs g = lin_args(c->xn, c->H, c->sbuf, c->I, rows, c->I, c->H);
-  g.w[0] = LW(c, l, kWg); g.w2 = LW(c, l, kWu); g.epi = kEpiSwiglu;
-  CK(c->err, launch_linear_rows(dt, g, st));
-  LinearArgs d = lin_args(c->sbuf, c->I, c->x, c->H, rows, c->H, c->I);
-  d.w[0] = LW(c, l, kWd); d.epi = kEpiResid; d.r = c->x; d.ldr = c->H;
-  CK(c->err, launch_linear_rows(dt, d, st));
+  if (tc) {
+    TcGemmArgs t = tc_args(c, rows, c->I, c->H, kEpiSwiglu);
+    tc_segments(t, {{&c->lmaps[l].wg, c->I}});
+    t.a2_map = c->lmaps[l].wu;
+    t.b_map = c->xn_map[bi];
+    t.y = c->sbuf; t.ldy = c->I;
+    CK(c->err, tc_run(c, t));
+    TcGemmArgs d = tc_args(c, rows, c->H, c->I, kEpiResid);
+    tc_segments(d, {{&c->lmaps[l].wd, c->H}});
+    d.b_map = c->sbuf_map[bi];
+    d.y = c->x; d.ldy = c->H; d.r = c->x; d.ldr = c->H;
+    CK(c->err, tc_run(c, d));
+  } else {
+    LinearArgs g = lin_args(c->xn, c->H, c->sbuf, c->I, rows, c->I, c->H);
+    g.w[0] = LW(c, l, kWg); g.w2 = LW(c, l, kWu); g.epi = kEpiSwiglu;
+    CK(c->err, launch_linear_rows(dt, g, st));
+    LinearArgs d = lin_args(c->sbuf, c->I, c->x, c->H, rows, c->H, c->I);
+    d.w[0] = LW(c, l, kWd); d.epi = kEpiResid; d.r = c->x; d.ldr = c->H;
+    CK(c->err, launch_linear_rows(dt, d, st));
+  }
   return DFLASH_OK;
 }
 
@@ -345,6 +440,46 @@ int ensure_room(dflash_ctx* c, int rows) {
   if (off + rows - r->host_base > r->cap)
     return fail(c->err, DFLASH_EFULL, "append-only cache full: %lld + %d rows > %lld",
                 off - r->host_base, rows, r->cap);
+  return DFLASH_OK;
+}
+
+// Tensor maps of every weight and activation operand of the tensor-core path
+// (bf16 configs whose output dimensions are whole 128-row tiles).
+int setup_tensor_core_path(dflash_ctx* c) {
+  const dflash_config& g = c->cfg;
+  c->use_tc = false;
+  if (g.dtype != DFLASH_BF16) return DFLASH_OK;
+  if (c->H % 128 || c->qdim % 128 || c->kvdim % 128 || c->I % 128 || c->kin % 64) return DFLASH_OK;
+  int dev = 0, sms = 0;
+  CK(c->err, cudaGetDevice(&dev));
+  CK(c->err, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  c->num_sms = sms < kTcGrid ? sms : kTcGrid;
+  const uint64_t H = c->H;
+  auto wmap = [&](CUtensorMap* m, const void* w, uint64_t rows, uint64_t inner) {
+    return tc_encode_map(m, w, inner, rows, inner * 2, 64, 128);
+  };
+  bool ok = wmap(&c->fc_map, c->fc, H, c->kin) && wmap(&c->lm_map, c->lm_head, c->V, H);
+  c->lmaps.resize(g.n_layers);
+  for (int l = 0; l < g.n_layers && ok; ++l) {
+    auto& m = c->lmaps[l];
+    ok = wmap(&m.wq, LW(c, l, kWq), c->qdim, H) && wmap(&m.wk, LW(c, l, kWk), c->kvdim, H) &&
+         wmap(&m.wv, LW(c, l, kWv), c->kvdim, H) && wmap(&m.wo, LW(c, l, kWo), H, c->qdim) &&
+         wmap(&m.wg, LW(c, l, kWg), c->I, H) && wmap(&m.wu, LW(c, l, kWu), c->I, H) &&
+         wmap(&m.wd, LW(c, l, kWd), H, c->I);
+  }
+  for (int b = 0; b < 2 && ok; ++b) {
+    const uint32_t bn = b ? 32 : 16;
+    const uint64_t R = c->R;
+    ok = tc_encode_map(&c->xn_map[b], c->xn, H, R, H * 2, 64, bn) &&
+         tc_encode_map(&c->attn_map[b], c->attn, c->qdim, R, (uint64_t)c->qdim * 2, 64, bn) &&
+         tc_encode_map(&c->sbuf_map[b], c->sbuf, c->I, R, (uint64_t)c->I * 2, 64, bn) &&
+         tc_encode_map(&c->appc_map[b], c->app_c, H, R, H * 2, 64, bn) &&
+         tc_encode_map(&c->xf_map[0][b], c->xf, H, R, H * 2, 64, bn) &&
+         tc_encode_map(&c->xf_map[1][b], static_cast<char*>(c->xf) + H * 2, H, R - 1, H * 2, 64, bn);
+  }
+  if (!ok) return DFLASH_OK;   // no tensor-map encoder: the CUDA-core path serves
+  CK(c->err, init_tc_attrs());
+  c->use_tc = true;
   return DFLASH_OK;
 }
 
@@ -432,7 +567,8 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   if (rc) { delete c; return rc; }
   c->ring->owned_by_ctx = true;
 
-  const size_t E = c->esz, R = c->rows_max;
+  c->R = c->rows_max + 1 > 33 ? c->rows_max + 1 : 33;
+  const size_t E = c->esz, R = c->R;
   c->ing_rows = c->max_ctx < kIngestChunk ? c->max_ctx : kIngestChunk;
   c->lm_grid = lmhead_grid(c->V);
   c->vf_chunks = verify_chunks(c->V);
@@ -447,7 +583,9 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       (size_t)c->ing_rows * 2 * c->kvdim * E, (size_t)c->ing_rows * c->half * sizeof(float2),
       (size_t)c->lm_grid * R * 4, (size_t)c->lm_grid * R * 4, R * c->vf_chunks * 4,
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
-      R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0};
+      R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
+      (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
+      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -484,6 +622,12 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->backbone_ids = carve<int>(cur, sizes[si++]);
   c->zlog = sizes[si] ? carve<float>(cur, sizes[si]) : nullptr;
   ++si;
+  c->tc_part = carve<float>(cur, sizes[si++]);
+  c->tc_tiles = carve<unsigned>(cur, sizes[si++]);
+  c->tc_err = carve<int>(cur, sizes[si++]);
+  c->tc_lm_pv = carve<float>(cur, sizes[si++]);
+  c->tc_lm_pi = carve<int>(cur, sizes[si++]);
+  c->tc_done = carve<unsigned>(cur, sizes[si++]);
 
   std::vector<double> inv(c->half);
   for (int i = 0; i < c->half; ++i)
@@ -499,6 +643,8 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
     dflash_ctx_destroy(c);
     return cuda_fail(err, e, "context initialisation");
   }
+  rc = setup_tensor_core_path(c);
+  if (rc) { std::string m = c->err; dflash_ctx_destroy(c); return fail(err, rc, "%s", m.c_str()); }
   *out = c;
   return DFLASH_OK;
 }
@@ -578,7 +724,17 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   lm.counter = c->counters + 0;
   lm.grid = c->lm_grid;
   if (c->lm_timing) CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
-  CK(c->err, launch_lmhead_argmax(dt, lm, st));
+  if (c->use_tc && R <= 32 && lm.logits == nullptr) {
+    TcGemmArgs t = tc_args(c, R, c->V, c->H, kEpiArgmax);
+    tc_segments(t, {{&c->lm_map, c->V}});
+    t.b_map = c->xf_map[read0][bn_index(R)];
+    t.softcap = c->cfg.softcap;
+    t.ids = lm.ids; t.ids2 = lm.ids2; t.maxv = lm.maxv;
+    t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
+    CK(c->err, tc_run(c, t));
+  } else {
+    CK(c->err, launch_lmhead_argmax(dt, lm, st));
+  }
   if (c->lm_timing) {
     CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
     c->lm_recorded = true;
@@ -655,6 +811,58 @@ int dflash_round(dflash_ctx* c, const void* target_logits, const void* resid, in
   return rc;
 }
 
+int dflash_linear(dflash_ctx* c, const void* x, int32_t M, int32_t K, const void* w, const void* w2,
+                  int32_t N, const void* r, void* y, int32_t epi) {
+  if (!c) return DFLASH_EINVAL;
+  if (!x || !w || !y || (epi == kEpiSwiglu && !w2) || (epi == kEpiResid && !r))
+    return fail(c->err, DFLASH_EINVAL, "a linear operand is NULL");
+  if (epi < 0 || epi > 2) return fail(c->err, DFLASH_EINVAL, "epi must be 0, 1 or 2");
+  if (M < 1 || K < 8 || N < 1 || K % 8) return fail(c->err, DFLASH_EINVAL, "bad linear shape");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (w2 && !aligned16(w2)) || (r && !aligned16(r)))
+    return fail(c->err, DFLASH_EINVAL, "linear operands must be 16-byte aligned");
+  if (c->use_tc && M <= 32 && K % 64 == 0) {
+    TcGemmArgs t = tc_args(c, M, N, K, epi);
+    CUtensorMap wa, wb;
+    bool ok = tc_encode_map(&wa, w, K, N, (uint64_t)K * 2, 64, 128) &&
+              tc_encode_map(&t.b_map, x, K, M, (uint64_t)K * 2, 64, bn_of(M));
+    if (ok && epi == kEpiSwiglu) ok = tc_encode_map(&wb, w2, K, N, (uint64_t)K * 2, 64, 128);
+    if (!ok) return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
+    tc_segments(t, {{&wa, N}});
+    if (epi == kEpiSwiglu) t.a2_map = wb;
+    t.y = y; t.ldy = N; t.r = r; t.ldr = N;
+    CK(c->err, tc_run(c, t));
+  } else {
+    LinearArgs a = lin_args(x, K, y, N, M, N, K);
+    a.w[0] = w; a.w2 = w2; a.r = r; a.ldr = N; a.epi = epi;
+    CK(c->err, launch_linear_rows(c->dt, a, c->stream));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_argmax(dflash_ctx* c, const void* x, int32_t rows, int32_t* ids, float* maxv) {
+  if (!c) return DFLASH_EINVAL;
+  if (!x || !ids || !maxv) return fail(c->err, DFLASH_EINVAL, "an lm_head operand is NULL");
+  if (rows < 1 || rows > c->cfg.max_block) return fail(c->err, DFLASH_ERANGE, "rows outside [1, max_block]");
+  if (!aligned16(x)) return fail(c->err, DFLASH_EINVAL, "x must be 16-byte aligned");
+  if (c->use_tc && rows <= 32) {
+    TcGemmArgs t = tc_args(c, rows, c->V, c->H, kEpiArgmax);
+    tc_segments(t, {{&c->lm_map, c->V}});
+    if (!tc_encode_map(&t.b_map, x, c->H, rows, (uint64_t)c->H * 2, 64, bn_of(rows)))
+      return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
+    t.softcap = c->cfg.softcap;
+    t.ids = ids; t.ids2 = nullptr; t.maxv = maxv;
+    t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
+    CK(c->err, tc_run(c, t));
+  } else {
+    LmHeadArgs lm{};
+    lm.x = x; lm.ldx = c->H; lm.w = c->lm_head; lm.R = rows; lm.H = c->H; lm.V = c->V;
+    lm.softcap = c->cfg.softcap; lm.ids = ids; lm.maxv = maxv;
+    lm.part_v = c->lm_pv; lm.part_i = c->lm_pi; lm.counter = c->counters + 0; lm.grid = c->lm_grid;
+    CK(c->err, launch_lmhead_argmax(c->dt, lm, c->stream));
+  }
+  return DFLASH_OK;
+}
+
 int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const float* z, int32_t* out) {
   if (!c) return DFLASH_EINVAL;
   if (!out) return fail(c->err, DFLASH_EINVAL, "out is NULL");
@@ -710,7 +918,9 @@ int dflash_get_state(dflash_ctx* c, dflash_round_state* out) {
   out->anchor = rs.anchor;
   out->last_n = rs.n;
   out->last_accepted = rs.a;
-  out->error = rs.error | ring.error;
+  int tcerr = 0;
+  if (c->tc_err) CK(c->err, cudaMemcpy(&tcerr, c->tc_err, sizeof tcerr, cudaMemcpyDeviceToHost));
+  out->error = rs.error | ring.error | (tcerr ? 4 : 0);
   return DFLASH_OK;
 }
 

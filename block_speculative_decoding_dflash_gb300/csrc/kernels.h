@@ -3,6 +3,7 @@
 // status; none allocates or synchronizes.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,6 +31,34 @@ struct LinearArgs {
   int M, N, K;
   int epi;
 };
+enum : int { kEpiArgmax = 3 };  // tensor-core GEMM only: softcap + per-row argmax
+
+// Tensor-core weight-streaming GEMM D[n, m] = sum_k W[n, k] X[m, k] (bf16,
+// fp32 accumulate), M <= BN rows of X (BN 16 or 32). Weight rows are stacked
+// segments of whole 128-row tiles (seg_tiles = cumulative tile counts); the
+// last segment may end in a partial tile (rows past N are zero-filled).
+struct TcGemmArgs {
+  CUtensorMap a_map[3];            // weight segments, box {64, 128}
+  CUtensorMap a2_map;              // up weight of kEpiSwiglu, box {64, 128}
+  CUtensorMap b_map;               // X, box {64, BN}
+  int seg_tiles[3];
+  int nseg;
+  int M, N, K, tiles, kchunks, epi;
+  void* y; int ldy;                // output [M, N] (row stride ldy)
+  const void* r; int ldr;          // residual of kEpiResid (may alias y)
+  float* partials;                 // [grid][2][NV*BN][128] fp32 split-tile partials
+  unsigned* tile_ctr;              // [tiles], zero between launches
+  int* err;                        // bounded-wait timeouts are reported here
+  float softcap;                   // kEpiArgmax
+  int* ids; int* ids2; float* maxv;
+  float* part_v; int* part_i;      // [grid * M]
+  unsigned* done_ctr;
+};
+bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+cudaError_t init_tc_attrs();
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st);
+
 // Block rows (any M; 16 rows per weight pass): weight-streaming kernel.
 cudaError_t launch_linear_rows(int dtype, const LinearArgs& a, cudaStream_t st);
 // Many rows (context ingest), kEpiStore only: register-tiled GEMM.

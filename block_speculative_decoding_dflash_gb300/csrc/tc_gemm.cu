@@ -1,0 +1,404 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05 + TMEM,
+// operands staged by TMA), for the decode-shaped linear layers of the round:
+//
+//   D[n, m] = sum_k W[n, k] * X[m, k],   n < N (output features, large),
+//                                        m < M <= BN (block rows, small)
+//
+// W is the MMA's A operand (128-row tiles), X its B operand (BN rows, zero
+// filled past M), so one MMA is 128 x BN x 16 and the accumulator is a
+// 128-lane x BN-column fp32 tile in TMEM.
+//
+// Work split: the (tile, 64-wide K chunk) units of the whole GEMM are cut
+// into gridDim.x contiguous ranges, one per CTA (one CTA per SM), so every
+// SM streams the same number of weight bytes. A tile whose K range spans
+// several CTAs is finished by whichever contributor arrives last: each writes
+// its fp32 partial, takes a ticket, and the last one sums the partials in CTA
+// order (deterministic) and runs the epilogue. Nobody waits on another CTA.
+//
+// Roles: warp 0 issues TMA loads into an S-stage shared-memory ring (the
+// weight tiles of the first S units are requested before the programmatic
+// launch dependency is resolved, so they stream while the previous kernel
+// finishes); warp 1 allocates TMEM and issues tcgen05.mma; warps 2-5 read the
+// accumulators back and run the epilogue (store, residual add, SwiGLU, or
+// softcap + argmax for the lm_head).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dfl {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiBarrier = 1;
+constexpr int kABytes = 128 * 128;     // 128 rows x 64 bf16
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float rnd_bf(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(128) : "memory");
+}
+
+constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+
+template <int BN, int NV, int STAGES>
+struct Cfg {
+  static constexpr int kStage = NV * kABytes + BN * 128;
+  static constexpr uint32_t kTmem = tmem_cols(2 * NV * BN);
+  static constexpr size_t kSmem = (size_t)STAGES * kStage + 1024 + 512;
+};
+
+// CTA owning unit u when U units are split into G contiguous ranges
+// [floor(b*U/G), floor((b+1)*U/G)).
+__device__ __forceinline__ int owner_of(long long u, long long U, int G) {
+  return static_cast<int>((u * G + G - 1) / U);
+}
+
+template <int BN, int EPI, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+  constexpr int NV = (EPI == kEpiSwiglu) ? 2 : 1;
+  using C = Cfg<BN, NV, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * C::kStage);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  __shared__ float best_v[BN];
+  __shared__ int best_i[BN];
+  __shared__ float red_v[4][BN];
+  __shared__ int red_i[4][BN];
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int KC = a.kchunks;
+  const long long U = (long long)a.tiles * KC;
+  const long long u0 = U * b / G, u1 = U * (b + 1) / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&acc_full[s], 1); mbar_init(&acc_empty[s], 128); }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, C::kTmem);
+  if (threadIdx.x < BN) { best_v[threadIdx.x] = -INFINITY; best_i[threadIdx.x] = 0x7fffffff; }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&a.b_map);
+      const uint64_t pol = policy_evict_first();
+      bool ok = true;
+      const long long nunits = u1 - u0;
+      const long long pre = nunits < STAGES ? nunits : STAGES;
+      // Weight tiles of the first stages: they do not depend on earlier kernels.
+      for (long long i = 0; i < nunits && ok; ++i) {
+        const long long u = u0 + i;
+        const int t = static_cast<int>(u / KC), c = static_cast<int>(u % KC);
+        int s = 0;
+        while (s < a.nseg - 1 && t >= a.seg_tiles[s]) ++s;
+        const int row0 = (t - (s ? a.seg_tiles[s - 1] : 0)) * 128;
+        const int st = static_cast<int>(i % STAGES);
+        uint8_t* sa = smem + (size_t)st * C::kStage;
+        if (i >= STAGES) ok = mbar_wait(&empty[st], static_cast<unsigned>((i / STAGES - 1) & 1));
+        if (!ok) break;
+        if (i == pre) pdl_wait();
+        mbar_expect_tx(&full[st], C::kStage);
+        tma_load_2d_hint(sa, &a.a_map[s], c * 64, row0, &full[st], pol);
+        if (NV == 2) tma_load_2d_hint(sa + kABytes, &a.a2_map, c * 64, t * 128, &full[st], pol);
+        if (i >= pre) tma_load_2d(sa + NV * kABytes, &a.b_map, c * 64, 0, &full[st]);
+        if (i == pre - 1) {
+          // The activations of the prefetched stages, once the inputs exist.
+          pdl_wait();
+          for (long long j = 0; j <= i; ++j) {
+            const int cj = static_cast<int>((u0 + j) % KC);
+            const int sj = static_cast<int>(j % STAGES);
+            tma_load_2d(smem + (size_t)sj * C::kStage + NV * kABytes, &a.b_map, cj * 64, 0, &full[sj]);
+          }
+        }
+      }
+      if (!ok) atomicOr(a.err, 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, BN);
+      bool ok = true;
+      long long i = 0;
+      int seg = 0;
+      for (long long u = u0; u < u1 && ok; ++seg) {
+        const int c0 = static_cast<int>(u % KC);
+        const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
+        const int buf = seg & 1;
+        if (seg >= 2) ok = mbar_wait(&acc_empty[buf], static_cast<unsigned>((seg / 2 - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * NV * BN;
+        for (int c = c0; c < c1; ++c, ++i) {
+          const int st = static_cast<int>(i % STAGES);
+          ok = mbar_wait(&full[st], static_cast<unsigned>((i / STAGES) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)st * C::kStage);
+          const uint32_t sb = sa + NV * kABytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = smem_desc_sw128(sb + kk * 32);
+            const uint32_t acc = (c > c0 || kk > 0) ? 1u : 0u;
+            tc_mma_bf16(d, smem_desc_sw128(sa + kk * 32), bd, idesc, acc);
+            if (NV == 2) tc_mma_bf16(d + BN, smem_desc_sw128(sa + kABytes + kk * 32), bd, idesc, acc);
+          }
+          tc_commit(&empty[st]);
+        }
+        tc_commit(&acc_full[buf]);
+        u += c1 - c0;
+      }
+      if (!ok) atomicOr(a.err, 2);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    pdl_wait();
+    const int q = warp & 3;                       // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;                // accumulator row = output feature in tile
+    const int first_tile = static_cast<int>(u0 / KC);
+    bool ok = true;
+    int seg = 0;
+    for (long long u = u0; u < u1 && ok; ++seg) {
+      const int t = static_cast<int>(u / KC);
+      const int c0 = static_cast<int>(u % KC);
+      const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
+      const int buf = seg & 1;
+      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float acc[NV][BN];
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < BN / 16; ++j)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * NV * BN + v * BN + j * 16,
+                    &acc[v][j * 16]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      u += c1 - c0;
+
+      bool finish = (c0 == 0 && c1 == KC);
+      if (!finish) {
+        // Split tile: publish this CTA's partial, take a ticket.
+        const int slot = (t == first_tile) ? 0 : 1;
+        float* mine = a.partials + ((size_t)b * 2 + slot) * NV * BN * 128;
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int m = 0; m < BN; ++m) mine[(v * BN + m) * 128 + row] = acc[v][m];
+        __threadfence();
+        epi_sync();
+        const int bf = owner_of((long long)t * KC, U, G);
+        const int bl = owner_of((long long)t * KC + KC - 1, U, G);
+        if (threadIdx.x == 64) {
+          const unsigned ticket = atomicAdd(&a.tile_ctr[t], 1u);
+          s_last = (ticket == static_cast<unsigned>(bl - bf));
+        }
+        epi_sync();
+        finish = s_last != 0;
+        if (finish) {
+          __threadfence();
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
+          for (int bb = bf; bb <= bl; ++bb) {
+            const int first_bb = static_cast<int>((U * bb / G) / KC);
+            const int sl = (t == first_bb) ? 0 : 1;
+            const float* p = a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+              for (int m = 0; m < BN; ++m) acc[v][m] += __ldcg(p + (v * BN + m) * 128 + row);
+          }
+          if (threadIdx.x == 64) a.tile_ctr[t] = 0u;
+        }
+      }
+      if (!finish) continue;
+
+      // ---- final epilogue of tile t ----
+      const int n = t * 128 + row;
+      const bool valid = n < a.N;
+      if (EPI == kEpiArgmax) {
+        const float cap = a.softcap;
+#pragma unroll
+        for (int m = 0; m < BN; ++m) {
+          float z = acc[0][m];
+          if (cap > 0.f) z = cap * tanhf(z / cap);
+          float bv = (valid && m < a.M) ? z : -INFINITY;
+          int bi = valid ? n : 0x7fffffff;
+          warp_argmax(bv, bi);
+          if (lane == 0) { red_v[q][m] = bv; red_i[q][m] = bi; }
+        }
+        epi_sync();
+        if (threadIdx.x >= 64 && threadIdx.x < 64 + BN) {
+          const int m = threadIdx.x - 64;
+          float bv = best_v[m];
+          int bi = best_i[m];
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            if (better(red_v[w][m], red_i[w][m], bv, bi)) { bv = red_v[w][m]; bi = red_i[w][m]; }
+          best_v[m] = bv;
+          best_i[m] = bi;
+        }
+        epi_sync();
+      } else if (valid) {
+        bf16* Y = reinterpret_cast<bf16*>(a.y);
+#pragma unroll
+        for (int m = 0; m < BN; ++m) {
+          if (m < a.M) {
+            float out;
+            if (EPI == kEpiStore) {
+              out = acc[0][m];
+            } else if (EPI == kEpiResid) {
+              out = __bfloat162float(reinterpret_cast<const bf16*>(a.r)[(size_t)m * a.ldr + n]) +
+                    rnd_bf(acc[0][m]);
+            } else {
+              out = silu_f(rnd_bf(acc[0][m])) * rnd_bf(acc[NV - 1][m]);
+            }
+            Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(out);
+          }
+        }
+      }
+    }
+    if (!ok) atomicOr(a.err, 4);
+
+    if (EPI == kEpiArgmax) {
+      // Per-CTA best of every row, then the last CTA to finish reduces them.
+      epi_sync();
+      if (threadIdx.x >= 64 && threadIdx.x < 64 + BN && threadIdx.x - 64 < a.M) {
+        const int m = threadIdx.x - 64;
+        a.part_v[(size_t)b * a.M + m] = best_v[m];
+        a.part_i[(size_t)b * a.M + m] = best_i[m];
+      }
+      __threadfence();
+      epi_sync();
+      if (threadIdx.x == 64) s_last = (atomicAdd(a.done_ctr, 1u) == static_cast<unsigned>(G - 1));
+      epi_sync();
+      if (s_last) {
+        __threadfence();
+        if (threadIdx.x >= 64 && threadIdx.x - 64 < a.M) {
+          const int m = threadIdx.x - 64;
+          float v = -INFINITY;
+          int idx = 0x7fffffff;
+          for (int c = 0; c < G; ++c) {
+            const float cv = __ldcg(a.part_v + (size_t)c * a.M + m);
+            const int ci = __ldcg(a.part_i + (size_t)c * a.M + m);
+            if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
+          }
+          a.ids[m] = idx;
+          if (a.ids2) a.ids2[m] = idx;
+          a.maxv[m] = v;
+        }
+        if (threadIdx.x == 64) *a.done_ctr = 0u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmem);
+  }
+}
+
+template <int BN, int EPI>
+constexpr int stages_for() { return EPI == kEpiSwiglu ? 6 : 8; }
+
+template <int BN, int EPI>
+cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
+  constexpr int S = stages_for<BN, EPI>();
+  constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<BN, NV, S>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI, S>, a);
+}
+
+template <int BN, int EPI>
+cudaError_t attr_tc() {
+  constexpr int S = stages_for<BN, EPI>();
+  constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<BN, NV, S>::kSmem);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t init_tc_attrs() {
+  cudaError_t e;
+  if ((e = attr_tc<16, kEpiStore>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiResid>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiSwiglu>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiArgmax>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiStore>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiResid>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
+  return attr_tc<32, kEpiArgmax>();
+}
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st) {
+  const long long U = (long long)a.tiles * a.kchunks;
+  if (grid > U) grid = static_cast<int>(U);
+  if (bn == 16) {
+    switch (a.epi) {
+      case kEpiStore: return launch_tc<16, kEpiStore>(a, grid, pdl, st);
+      case kEpiResid: return launch_tc<16, kEpiResid>(a, grid, pdl, st);
+      case kEpiSwiglu: return launch_tc<16, kEpiSwiglu>(a, grid, pdl, st);
+      default: return launch_tc<16, kEpiArgmax>(a, grid, pdl, st);
+    }
+  }
+  switch (a.epi) {
+    case kEpiStore: return launch_tc<32, kEpiStore>(a, grid, pdl, st);
+    case kEpiResid: return launch_tc<32, kEpiResid>(a, grid, pdl, st);
+    case kEpiSwiglu: return launch_tc<32, kEpiSwiglu>(a, grid, pdl, st);
+    default: return launch_tc<32, kEpiArgmax>(a, grid, pdl, st);
+  }
+}
+
+}  // namespace dfl

@@ -242,6 +242,24 @@ int dflash_round(dflash_ctx* ctx, const void* target_logits, const void* resid,
 int dflash_markov_chain(dflash_ctx* ctx, int32_t anchor, int32_t gamma,
                         const float* z, int32_t* out);
 
+/* ---- single ops of the round (same kernels, same stream) --------------------- */
+
+/* One linear layer of the drafter on the context's stream and scratch:
+ * y[m, n] = rnd(sum_k x[m, k] w[n, k]) (epi 0), rnd(r[m, n] + rnd(...))
+ * (epi 1, r may alias y), or rnd(silu(rnd(x.w^T)) * rnd(x.w2^T)) (epi 2,
+ * the SwiGLU of Qwen-shaped MLPs [Head "Why"]); x [M, K], w and w2 [N, K],
+ * r and y [M, N], all dense in the config dtype, accumulation fp32. bf16
+ * with M <= 32 and K % 64 == 0 runs on the tensor cores. */
+int dflash_linear(dflash_ctx* ctx, const void* x, int32_t M, int32_t K,
+                  const void* w, const void* w2, int32_t N, const void* r,
+                  void* y, int32_t epi);
+/* The fused lm_head of dflash_draft_block on given rows: for x [rows, H]
+ * (normed hidden rows), ids[m] = argmax_v c*tanh((x[m].lm_head[v])/c) (c =
+ * softcap, 0 = no cap; lowest index on ties) and maxv[m] the selected value
+ * (fp32). No [rows, V] logit tensor is written. 1 <= rows <= max_block. */
+int dflash_lm_head_argmax(dflash_ctx* ctx, const void* x, int32_t rows,
+                          int32_t* ids, float* maxv);
+
 /* ---- inspection (these sync) ------------------------------------------------- */
 
 /* Copies the final-normed hidden rows of the last draft [rows, H] (rows =
