@@ -193,6 +193,7 @@ struct dflash_ctx {
   float* tc_lm_pv = nullptr;
   int* tc_lm_pi = nullptr;
   unsigned* tc_done = nullptr;
+  unsigned* attn_ctr = nullptr;
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -389,6 +390,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.max_ctx = c->max_ctx;
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
+  at.head_ctr = c->attn_ctr;
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
@@ -585,7 +587,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
-      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64};
+      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)c->nkv * 4};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -628,6 +630,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->tc_lm_pv = carve<float>(cur, sizes[si++]);
   c->tc_lm_pi = carve<int>(cur, sizes[si++]);
   c->tc_done = carve<unsigned>(cur, sizes[si++]);
+  c->attn_ctr = carve<unsigned>(cur, sizes[si++]);
 
   std::vector<double> inv(c->half);
   for (int i = 0; i < c->half; ++i)

@@ -8,6 +8,8 @@
 // keys; one CTA per (split, kv head) scores all rows*G queries of that kv
 // head against its keys (each K/V byte is read once) and writes an
 // online-softmax partial (max, sum, o[hd]); a combine kernel merges them.
+// This CUDA-core version serves fp32 and head dims other than 128; bf16 with
+// head_dim 128 goes to the tensor-core version in attention_mma.cu.
 #include <math.h>
 
 #include "kernels.h"
@@ -161,8 +163,10 @@ size_t attention_scratch_floats(int rows, int nq, int nkv, int hd, int max_ctx) 
 }
 
 cudaError_t init_attention_attrs(int hd) {
+  cudaError_t e = init_attention_mma_attrs();
+  if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(partial_smem(hd));
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<bf16>,
+  e = cudaFuncSetAttribute(attn_partial_kernel<bf16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(attn_partial_kernel<float>,
@@ -170,6 +174,7 @@ cudaError_t init_attention_attrs(int hd) {
 }
 
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st) {
+  if (attention_mma_ok(dtype, a.hd) && a.head_ctr) return launch_attention_mma(a, a.head_ctr, st);
   const int nsplit = num_splits(a.rows, a.max_ctx);
   const size_t smem = partial_smem(a.hd);
   dim3 grid(nsplit, a.nkv);

@@ -1,0 +1,290 @@
+// Bidirectional sliding-window GQA attention of the drafter block, bf16,
+// head_dim 128, on tensor cores (mma.sync m16n8k16, fp32 accumulate).
+//
+// One CTA per (split of kKeys = 128 keys, kv head g); its 8 warps each own 16
+// keys. For every 16-query tile (queries = block rows x the G query heads of
+// g): S = Q K^T for the warp's keys (mask |q - k| <= W by absolute
+// positions), the warp's online-softmax partial (max, sum, P V), a merge of
+// the 8 warps in shared memory in warp order, and the CTA's partial written
+// to global scratch. The CTA that takes the last ticket of head g merges the
+// splits in split order and writes the bf16 output: no separate combine
+// launch, no CTA ever waits on another, and the result is deterministic.
+//
+// Keys are addressed by absolute position (ring slot = position mod cap), the
+// context keys [kstart, p) followed by the block's own rows.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kHd = 128;
+constexpr int kKeys = 128;
+constexpr int kWarps = 8;
+constexpr int kPad = 8;                    // bf16 elements of row padding
+constexpr int kRowB = (kHd + kPad) * 2;    // 272-byte rows: conflict-free ldmatrix
+
+struct MmaSmem {
+  bf16 k[kKeys][kHd + kPad];
+  bf16 v[kKeys][kHd + kPad];
+  bf16 q[16][kHd + kPad];
+  float o[kWarps][16][kHd];                // per-warp unnormalised P V
+  float m[kWarps][16];
+  float l[kWarps][16];
+  int last;
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit,
+                                                               unsigned* head_ctr) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
+  const int s = blockIdx.x, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.nq / a.nkv;
+  const int Qn = a.rows * G;
+  const long long p = a.ring->offset;
+  long long kstart = a.ring->base;
+  if (a.window > 0 && p - a.window > kstart) kstart = p - a.window;
+  const int nctx = static_cast<int>(p - kstart);
+  const int nk = nctx + a.rows;
+  const int j0 = s * kKeys;
+  const size_t pstride = (size_t)kHd + 2;
+  float* part = a.partial + ((size_t)g * nsplit + s) * Qn * pstride;
+  const bf16* rk = reinterpret_cast<const bf16*>(a.ring_k) + (size_t)g * a.cap * kHd;
+  const bf16* rv = reinterpret_cast<const bf16*>(a.ring_v) + (size_t)g * a.cap * kHd;
+  const bf16* kb = reinterpret_cast<const bf16*>(a.kb);
+  const bf16* vb = reinterpret_cast<const bf16*>(a.vb);
+  const bf16* qg = reinterpret_cast<const bf16*>(a.q);
+
+  if (j0 < nk) {
+    // K and V tiles: 128 keys x 16 chunks of 16 bytes each.
+    for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
+      const int j = e >> 4, ch = e & 15;
+      const int kj = j0 + j;
+      const bf16* ks = kb;
+      const bf16* vs = vb;
+      bool valid = kj < nk;
+      if (kj < nctx) {
+        const long long slot = ring_slot(kstart + kj, a.cap);
+        ks = rk + slot * kHd + ch * 8;
+        vs = rv + slot * kHd + ch * 8;
+      } else if (valid) {
+        const size_t off = (size_t)(kj - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
+        ks = kb + off;
+        vs = vb + off;
+      }
+      cp_async16(&S.k[j][ch * 8], ks, valid);
+      cp_async16(&S.v[j][ch * 8], vs, valid);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  const int grp = lane >> 2, tig = lane & 3;
+  const float scale = rsqrtf(static_cast<float>(kHd));
+  for (int qt = 0; qt * 16 < Qn; ++qt) {
+    // this tile's 16 queries
+    for (int e = threadIdx.x; e < 16 * (kHd / 8); e += blockDim.x) {
+      const int r = e >> 4, ch = e & 15;
+      const int qi = qt * 16 + r;
+      const bool valid = qi < Qn;
+      const bf16* src = qg;
+      if (valid) src = qg + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
+      cp_async16(&S.q[r][ch * 8], src, valid);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    float m_row[2] = {-INFINITY, -INFINITY}, l_row[2] = {0.f, 0.f};
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    if (j0 < nk) {
+      // S = Q K^T over the warp's 16 keys (two 8-key n-tiles).
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < kHd / 16; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        const int mi = lane >> 3;
+        ldsm_x4(&S.q[(lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
+        ldsm_x4(&S.k[warp * 16 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
+        mma16816(sc[0], a0, a1, a2, a3, b0, b1);
+        mma16816(sc[1], a0, a1, a2, a3, b2, b3);
+      }
+      // mask, scale, per-row max over the warp's keys
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int qi = qt * 16 + grp + hr * 8;
+        const long long qpos = p + (qi < Qn ? qi / G : 0);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int kj = j0 + warp * 16 + nt * 8 + tig * 2 + c;
+            bool vis = qi < Qn && kj < nk;
+            if (vis && a.window > 0) {
+              const long long kpos = kj < nctx ? kstart + kj : p + (kj - nctx);
+              const long long d = qpos > kpos ? qpos - kpos : kpos - qpos;
+              vis = d <= a.window;
+            }
+            float& v = sc[nt][hr * 2 + c];
+            v = vis ? v * scale : -INFINITY;
+            m_row[hr] = fmaxf(m_row[hr], v);
+          }
+        m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 1));
+        m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 2));
+      }
+      // P = exp(S - m) (bf16 for the MMA), row sums, O = P V
+      uint32_t pa[4];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        float pv[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const float v = sc[nt][hr * 2 + c];
+            pv[nt][c] = (m_row[hr] == -INFINITY || v == -INFINITY) ? 0.f : expf(v - m_row[hr]);
+            l_row[hr] += pv[nt][c];
+          }
+        pa[hr] = pack_bf16(pv[0][0], pv[0][1]);        // keys 0..7 of this row
+        pa[2 + hr] = pack_bf16(pv[1][0], pv[1][1]);    // keys 8..15
+        l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 1);
+        l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 2);
+      }
+#pragma unroll
+      for (int dt = 0; dt < kHd / 16; ++dt) {
+        uint32_t b0, b1, b2, b3;
+        const int mi = lane >> 3;
+        ldsm_x4_t(&S.v[warp * 16 + (mi & 1) * 8 + (lane & 7)][dt * 16 + (mi >> 1) * 8], b0, b1, b2, b3);
+        mma16816(o[dt * 2], pa[0], pa[1], pa[2], pa[3], b0, b1);
+        mma16816(o[dt * 2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      }
+    }
+    // publish the warp's partial, then merge the 8 warps in warp order
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        S.o[warp][grp + hr * 8][nt * 8 + tig * 2] = o[nt][hr * 2];
+        S.o[warp][grp + hr * 8][nt * 8 + tig * 2 + 1] = o[nt][hr * 2 + 1];
+      }
+    if (tig == 0) {
+      S.m[warp][grp] = m_row[0]; S.m[warp][grp + 8] = m_row[1];
+      S.l[warp][grp] = l_row[0]; S.l[warp][grp + 8] = l_row[1];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 16 * kHd; e += blockDim.x) {
+      const int r = e / kHd, d = e % kHd;
+      const int qi = qt * 16 + r;
+      if (qi >= Qn) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, S.m[w][r]);
+      float O = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = S.m[w][r];
+          if (mw == -INFINITY) continue;
+          const float f = expf(mw - M);
+          O += f * S.o[w][r][d];
+          L += f * S.l[w][r];
+        }
+      }
+      float* out = part + (size_t)qi * pstride;
+      out[d] = O;
+      if (d == 0) { out[kHd] = M; out[kHd + 1] = L; }
+    }
+    __syncthreads();
+  }
+
+  // the last CTA of head g merges the splits
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) S.last = (atomicAdd(&head_ctr[g], 1u) == static_cast<unsigned>(nsplit - 1));
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
+  const float* base = a.partial + (size_t)g * nsplit * Qn * pstride;
+  bf16* outp = reinterpret_cast<bf16*>(a.out);
+  for (int e = threadIdx.x; e < Qn * (kHd / 4); e += blockDim.x) {
+    const int qi = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd));
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float L = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float* pr = base + ((size_t)sp * Qn + qi) * pstride;
+      const float ms = __ldcg(pr + kHd);
+      if (ms == -INFINITY) continue;
+      const float f = expf(ms - M);
+      L += f * __ldcg(pr + kHd + 1);
+      const float4 ov = __ldcg(reinterpret_cast<const float4*>(pr + d4));
+      acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
+    }
+    const int r = qi / G, h = g * G + qi % G;
+    bf16* dst = outp + (size_t)r * a.ldo + (size_t)h * kHd + d4;
+    const float inv = 1.0f / L;
+    dst[0] = __float2bfloat16_rn(acc[0] * inv);
+    dst[1] = __float2bfloat16_rn(acc[1] * inv);
+    dst[2] = __float2bfloat16_rn(acc[2] * inv);
+    dst[3] = __float2bfloat16_rn(acc[3] * inv);
+  }
+  if (threadIdx.x == 0) head_ctr[g] = 0u;
+}
+
+}  // namespace
+
+int attention_mma_splits(int rows, int max_ctx) { return (max_ctx + rows + kKeys - 1) / kKeys; }
+
+bool attention_mma_ok(int dtype, int hd) { return dtype == 1 && hd == kHd; }
+
+cudaError_t init_attention_mma_attrs() {
+  return cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(MmaSmem));
+}
+
+cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st) {
+  const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
+  dim3 grid(nsplit, a.nkv);
+  attn_mma_kernel<<<grid, kWarps * 32, sizeof(MmaSmem), st>>>(a, nsplit, head_ctr);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

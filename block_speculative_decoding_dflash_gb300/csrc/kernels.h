@@ -104,8 +104,13 @@ struct AttnArgs {
   int max_ctx;                 // most context keys any round can see
   float* partial;              // scratch [nkv][nsplit][rows*G][hd + 2]
   void* out; int ldo;          // [rows, nq, hd]
+  unsigned* head_ctr;          // [nkv] tickets, zero between launches (tensor-core path)
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
+// bf16, head_dim 128: tensor-core attention with the split merge fused in.
+bool attention_mma_ok(int dtype, int hd);
+cudaError_t init_attention_mma_attrs();
+cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st);
 size_t attention_scratch_floats(int rows, int nq, int nkv, int hd, int max_ctx);
 cudaError_t init_attention_attrs(int hd);
 
