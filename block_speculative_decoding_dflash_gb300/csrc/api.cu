@@ -575,7 +575,9 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->lm_grid = lmhead_grid(c->V);
   c->vf_chunks = verify_chunks(c->V);
   c->mk_grid = markov_grid(c->V);
-  const size_t attn_floats = attention_scratch_floats(c->rows_max, c->nq, c->nkv, c->hd, c->max_ctx);
+  size_t attn_floats = attention_scratch_floats(c->rows_max, c->nq, c->nkv, c->hd, c->max_ctx);
+  const size_t attn_mma_floats = attention_mma_scratch_floats(c->rows_max, c->nq, c->nkv, c->max_ctx);
+  if (attn_mma_floats > attn_floats) attn_floats = attn_mma_floats;
   const size_t sizes[] = {
       sizeof(RoundState), sizeof(double) * c->half,
       R * c->H * E, R * c->H * E, R * c->qkv_n * E, R * c->qdim * E, R * c->I * E, R * c->H * E,

@@ -24,6 +24,9 @@ constexpr int kKeys = 128;
 constexpr int kWarps = 8;
 constexpr int kPad = 8;                    // bf16 elements of row padding
 constexpr int kRowB = (kHd + kPad) * 2;    // 272-byte rows: conflict-free ldmatrix
+// Per-query partial: o[hd], max, sum, 2 floats of padding (528 bytes, a
+// multiple of 16, so the merge can read o with float4 loads).
+constexpr int kPartStride = kHd + 4;
 
 struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   const int nctx = static_cast<int>(p - kstart);
   const int nk = nctx + a.rows;
   const int j0 = s * kKeys;
-  const size_t pstride = (size_t)kHd + 2;
+  const size_t pstride = kPartStride;     // 16-byte aligned rows for float4 reads
   float* part = a.partial + ((size_t)g * nsplit + s) * Qn * pstride;
   const bf16* rk = reinterpret_cast<const bf16*>(a.ring_k) + (size_t)g * a.cap * kHd;
   const bf16* rv = reinterpret_cast<const bf16*>(a.ring_v) + (size_t)g * a.cap * kHd;
@@ -272,6 +275,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
 }  // namespace
 
 int attention_mma_splits(int rows, int max_ctx) { return (max_ctx + rows + kKeys - 1) / kKeys; }
+
+size_t attention_mma_scratch_floats(int rows, int nq, int nkv, int max_ctx) {
+  return (size_t)nkv * attention_mma_splits(rows, max_ctx) * rows * (nq / nkv) * kPartStride;
+}
 
 bool attention_mma_ok(int dtype, int hd) { return dtype == 1 && hd == kHd; }
 

@@ -109,6 +109,7 @@ struct AttnArgs {
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.
 bool attention_mma_ok(int dtype, int hd);
+size_t attention_mma_scratch_floats(int rows, int nq, int nkv, int max_ctx);
 cudaError_t init_attention_mma_attrs();
 cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st);
 size_t attention_scratch_floats(int rows, int nq, int nkv, int hd, int max_ctx);
