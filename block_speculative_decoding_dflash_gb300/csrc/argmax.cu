@@ -10,6 +10,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dfl {
 namespace {
@@ -30,6 +31,7 @@ __device__ __forceinline__ bool last_cta(unsigned* counter, unsigned total) {
 
 template <typename T, int MT>
 __global__ void __launch_bounds__(kLmWarps * 32) lmhead_kernel(LmHeadArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char lm_smem[];
   T* xs = reinterpret_cast<T*>(lm_smem);                  // [MT][H]
   __shared__ float best_v[kLmWarps][MT];
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kLmWarps * 32) lmhead_kernel(LmHeadArgs a) {
 template <typename T, int MT>
 cudaError_t lm_launch(const LmHeadArgs& a, cudaStream_t st) {
   const size_t smem = (size_t)MT * a.H * sizeof(T);
-  lmhead_kernel<T, MT><<<a.grid, kLmWarps * 32, smem, st>>>(a);
+  launch_pdl(lmhead_kernel<T, MT>, dim3(a.grid), dim3(kLmWarps * 32), smem, st, a);
   return cudaGetLastError();
 }
 
@@ -170,6 +172,7 @@ constexpr int kMaxVerifyRows = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
+  pdl_enter();
   __shared__ float sv[8];
   __shared__ int si[8];
   __shared__ int t_s[kMaxVerifyRows];
@@ -225,6 +228,7 @@ constexpr int kMkCols = kMkThreads * 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, int j) {
+  pdl_enter();
   extern __shared__ float w1s[];               // [r]
   __shared__ float sv[kMkThreads / 32];
   __shared__ int si[kMkThreads / 32];
@@ -313,16 +317,16 @@ cudaError_t launch_lmhead_argmax(int dtype, const LmHeadArgs& a, cudaStream_t st
 
 cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st) {
   dim3 grid(a.chunks, a.B);
-  if (dtype) verify_kernel<bf16><<<grid, 256, 0, st>>>(a);
-  else verify_kernel<float><<<grid, 256, 0, st>>>(a);
+  if (dtype) launch_pdl(verify_kernel<bf16>, dim3(grid), dim3(256), 0, st, a);
+  else launch_pdl(verify_kernel<float>, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(float) * a.r;
   for (int j = 0; j < a.gamma; ++j) {
-    if (dtype) markov_step_kernel<bf16><<<a.grid, kMkThreads, smem, st>>>(a, j);
-    else markov_step_kernel<float><<<a.grid, kMkThreads, smem, st>>>(a, j);
+    if (dtype) launch_pdl(markov_step_kernel<bf16>, dim3(a.grid), dim3(kMkThreads), smem, st, a, j);
+    else launch_pdl(markov_step_kernel<float>, dim3(a.grid), dim3(kMkThreads), smem, st, a, j);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -13,6 +13,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dfl {
 namespace {
@@ -22,6 +23,7 @@ constexpr int kWarps = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(AttnArgs a, int nsplit) {
+  pdl_enter();
   extern __shared__ float smem[];
   const int hd = a.hd, hdp = hd + 1;
   float* Ks = smem;                       // [kKS][hd+1]
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(AttnArgs a, i
 
 template <typename T>
 __global__ void attn_combine_kernel(AttnArgs a, int nsplit) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
   const int Qn = a.rows * G;
@@ -178,14 +181,14 @@ cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st) {
   const int nsplit = num_splits(a.rows, a.max_ctx);
   const size_t smem = partial_smem(a.hd);
   dim3 grid(nsplit, a.nkv);
-  if (dtype) attn_partial_kernel<bf16><<<grid, kWarps * 32, smem, st>>>(a, nsplit);
-  else attn_partial_kernel<float><<<grid, kWarps * 32, smem, st>>>(a, nsplit);
+  if (dtype) launch_pdl(attn_partial_kernel<bf16>, dim3(grid), dim3(kWarps * 32), smem, st, a, nsplit);
+  else launch_pdl(attn_partial_kernel<float>, dim3(grid), dim3(kWarps * 32), smem, st, a, nsplit);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int items = a.nkv * a.rows * (a.nq / a.nkv);
   const int cgrid = (items + 3) / 4;
-  if (dtype) attn_combine_kernel<bf16><<<cgrid, 128, 0, st>>>(a, nsplit);
-  else attn_combine_kernel<float><<<cgrid, 128, 0, st>>>(a, nsplit);
+  if (dtype) launch_pdl(attn_combine_kernel<bf16>, dim3(cgrid), dim3(128), 0, st, a, nsplit);
+  else launch_pdl(attn_combine_kernel<float>, dim3(cgrid), dim3(128), 0, st, a, nsplit);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dfl {
 namespace {
@@ -73,6 +74,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit,
                                                                unsigned* head_ctr) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
   const int s = blockIdx.x, g = blockIdx.y;
@@ -246,28 +248,60 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   __threadfence();
   const float* base = a.partial + (size_t)g * nsplit * Qn * pstride;
   bf16* outp = reinterpret_cast<bf16*>(a.out);
-  for (int e = threadIdx.x; e < Qn * (kHd / 4); e += blockDim.x) {
-    const int qi = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd));
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float L = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* pr = base + ((size_t)sp * Qn + qi) * pstride;
-      const float ms = __ldcg(pr + kHd);
-      if (ms == -INFINITY) continue;
-      const float f = expf(ms - M);
-      L += f * __ldcg(pr + kHd + 1);
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(pr + d4));
-      acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
+  // Split weights exp(m_s - M) and 1/L per query, computed once (the K/V tile
+  // area of shared memory is free now): all (split, query) maxima and sums
+  // are loaded in parallel first.
+  float* wsm = reinterpret_cast<float*>(&S.k[0][0]);          // [nsplit][16] weights
+  float* linv = reinterpret_cast<float*>(&S.v[0][0]);         // [16] 1 / L
+  for (int q0 = 0; q0 < Qn; q0 += 16) {
+    const int nq = Qn - q0 < 16 ? Qn - q0 : 16;
+    for (int e = threadIdx.x; e < nsplit * nq; e += blockDim.x) {
+      const int sp = e / nq, qi = q0 + e % nq;
+      wsm[sp * 16 + (qi - q0)] = __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd);
     }
-    const int r = qi / G, h = g * G + qi % G;
-    bf16* dst = outp + (size_t)r * a.ldo + (size_t)h * kHd + d4;
-    const float inv = 1.0f / L;
-    dst[0] = __float2bfloat16_rn(acc[0] * inv);
-    dst[1] = __float2bfloat16_rn(acc[1] * inv);
-    dst[2] = __float2bfloat16_rn(acc[2] * inv);
-    dst[3] = __float2bfloat16_rn(acc[3] * inv);
+    __syncthreads();
+    if (threadIdx.x < nq) {
+      const int r = threadIdx.x, qi = q0 + r;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wsm[sp * 16 + r]);
+      float L = 0.f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float ms = wsm[sp * 16 + r];
+        const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+        wsm[sp * 16 + r] = f;
+        if (f != 0.f) L += f * __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd + 1);
+      }
+      linv[r] = 1.0f / L;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nq * (kHd / 4); e += blockDim.x) {
+      const int r = e / (kHd / 4), qi = q0 + r, d4 = (e % (kHd / 4)) * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      int sp = 0;
+      for (; sp + 4 <= nsplit; sp += 4) {
+        float4 ov[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          ov[u] = __ldcg(reinterpret_cast<const float4*>(base + ((size_t)(sp + u) * Qn + qi) * pstride + d4));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float f = wsm[(sp + u) * 16 + r];
+          acc[0] += f * ov[u].x; acc[1] += f * ov[u].y; acc[2] += f * ov[u].z; acc[3] += f * ov[u].w;
+        }
+      }
+      for (; sp < nsplit; ++sp) {
+        const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + ((size_t)sp * Qn + qi) * pstride + d4));
+        const float f = wsm[sp * 16 + r];
+        acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
+      }
+      const float inv = linv[r];
+      bf16* dst = outp + (size_t)(qi / G) * a.ldo + (size_t)(g * G + qi % G) * kHd + d4;
+      dst[0] = __float2bfloat16_rn(acc[0] * inv);
+      dst[1] = __float2bfloat16_rn(acc[1] * inv);
+      dst[2] = __float2bfloat16_rn(acc[2] * inv);
+      dst[3] = __float2bfloat16_rn(acc[3] * inv);
+    }
+    __syncthreads();
   }
   if (threadIdx.x == 0) head_ctr[g] = 0u;
 }
@@ -290,7 +324,7 @@ cudaError_t init_attention_mma_attrs() {
 cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st) {
   const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
   dim3 grid(nsplit, a.nkv);
-  attn_mma_kernel<<<grid, kWarps * 32, sizeof(MmaSmem), st>>>(a, nsplit, head_ctr);
+  launch_pdl(attn_mma_kernel, dim3(grid), dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit, head_ctr);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@
 // Both accumulate in fp32 and round once to the storage type at the
 // epilogue (plus the residual / SwiGLU rounding points).
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dfl {
 namespace {
@@ -24,6 +25,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <typename T, int MT, int EPI>
 __global__ void __launch_bounds__(kRowsWarps * 32)
 linear_rows_kernel(LinearArgs a) {
+  pdl_enter();
   constexpr int NR = kRowsNR;
   constexpr int NV = (EPI == kEpiSwiglu) ? 2 : 1;
   __shared__ float red[kRowsWarps][NV * NR * MT];
@@ -119,11 +121,11 @@ template <typename T, int EPI>
 cudaError_t rows_dispatch(const LinearArgs& a, cudaStream_t st) {
   dim3 grid((a.N + kRowsNR - 1) / kRowsNR), block(kRowsWarps * 32);
   const int mt = a.M;
-  if (mt <= 1) linear_rows_kernel<T, 1, EPI><<<grid, block, 0, st>>>(a);
-  else if (mt <= 2) linear_rows_kernel<T, 2, EPI><<<grid, block, 0, st>>>(a);
-  else if (mt <= 4) linear_rows_kernel<T, 4, EPI><<<grid, block, 0, st>>>(a);
-  else if (mt <= 8) linear_rows_kernel<T, 8, EPI><<<grid, block, 0, st>>>(a);
-  else linear_rows_kernel<T, 16, EPI><<<grid, block, 0, st>>>(a);
+  if (mt <= 1) launch_pdl(linear_rows_kernel<T, 1, EPI>, dim3(grid), dim3(block), 0, st, a);
+  else if (mt <= 2) launch_pdl(linear_rows_kernel<T, 2, EPI>, dim3(grid), dim3(block), 0, st, a);
+  else if (mt <= 4) launch_pdl(linear_rows_kernel<T, 4, EPI>, dim3(grid), dim3(block), 0, st, a);
+  else if (mt <= 8) launch_pdl(linear_rows_kernel<T, 8, EPI>, dim3(grid), dim3(block), 0, st, a);
+  else launch_pdl(linear_rows_kernel<T, 16, EPI>, dim3(grid), dim3(block), 0, st, a);
   return cudaGetLastError();
 }
 
@@ -143,6 +145,7 @@ constexpr int TB = 64, TK = 16;
 
 template <typename T>
 __global__ void __launch_bounds__(256) linear_tiled_kernel(LinearArgs a) {
+  pdl_enter();
   __shared__ float As[TK][TB + 4];
   __shared__ float Bs[TK][TB + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -200,8 +203,8 @@ cudaError_t launch_linear_rows(int dtype, const LinearArgs& a, cudaStream_t st) 
 cudaError_t launch_linear_tiled(int dtype, const LinearArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.N <= 0) return cudaSuccess;
   dim3 grid((a.N + TB - 1) / TB, (a.M + TB - 1) / TB);
-  if (dtype) linear_tiled_kernel<bf16><<<grid, 256, 0, st>>>(a);
-  else linear_tiled_kernel<float><<<grid, 256, 0, st>>>(a);
+  if (dtype) launch_pdl(linear_tiled_kernel<bf16>, dim3(grid), dim3(256), 0, st, a);
+  else launch_pdl(linear_tiled_kernel<float>, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError();
 }
 

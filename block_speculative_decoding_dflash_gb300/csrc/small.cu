@@ -2,6 +2,7 @@
 // per-head q/k RMSNorm + RoPE, the K/V -> ring write, ring bookkeeping, the
 // commit, and the stand-in target.
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dfl {
 namespace {
@@ -31,6 +32,7 @@ __global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
                                    int mask_id, int rows, T* x,
                                    const RingState* ring, const double* inv_freq,
                                    int half, int tab_rows, float2* rope) {
+  pdl_enter();
   const int r = blockIdx.x;
   if (r < rows) {
     int tok = (r == 0) ? rs->anchor : mask_id;
@@ -51,6 +53,7 @@ __global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
 
 __global__ void rope_table_kernel(const double* inv_freq, int half, const RingState* ring,
                                   long long pos0, int rows, float2* rope) {
+  pdl_enter();
   const int r = blockIdx.x;
   if (r >= rows) return;
   const long long base = ring ? ring->offset : pos0;
@@ -61,6 +64,7 @@ __global__ void rope_table_kernel(const double* inv_freq, int half, const RingSt
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* x, int ldx, const T* g,
                                                      T* y, int ldy, int H, float eps) {
+  pdl_enter();
   __shared__ float red[8];
   const int r = blockIdx.x;
   const T* xr = x + (size_t)r * ldx;
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(128) head_norm_rope_kernel(T* buf, int ld, int
                                                              int heads, int hd, const T* g,
                                                              float eps, const float2* rope,
                                                              int neox) {
+  pdl_enter();
   __shared__ float sm[4][kMaxHd];
   const int warp = threadIdx.x >> 5;
   const int item = blockIdx.x * 4 + warp;
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(128) kv_to_ring_kernel(const T* kv, int ld, in
                                                          long long cap, int append_only,
                                                          RingState* ring, int use_dev,
                                                          long long pos_host) {
+  pdl_enter();
   __shared__ float sm[4][kMaxHd];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * 4 + warp;
@@ -169,6 +175,7 @@ __global__ void __launch_bounds__(128) kv_to_ring_kernel(const T* kv, int ld, in
 
 // ---- ring bookkeeping ------------------------------------------------------------
 __global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
+  pdl_enter();
   if (mode == 1) {
     ring->offset -= d;
     ring->appended = 0;
@@ -180,6 +187,7 @@ __global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
 }
 
 __global__ void ring_reset_kernel(RingState* ring, long long base) {
+  pdl_enter();
   ring->offset = base;
   ring->base = base;
   ring->hw = base - 1;
@@ -187,11 +195,13 @@ __global__ void ring_reset_kernel(RingState* ring, long long base) {
   ring->error = 0;
 }
 
-__global__ void set_anchor_kernel(RoundState* rs, int anchor) { rs->anchor = anchor; }
+__global__ void set_anchor_kernel(RoundState* rs, int anchor) {
+  pdl_enter(); rs->anchor = anchor; }
 
 // Partial-accept rollback: the block's `block` rows were appended (offset
 // advanced by block); keep the first `keep` (keep < 0: the verify's n).
 __global__ void commit_kernel(RoundState* rs, RingState* ring, int block, int keep) {
+  pdl_enter();
   const int k = keep >= 0 ? keep : rs->n;
   ring->offset -= (block - k);
   ring->appended = 0;
@@ -206,6 +216,7 @@ template <typename T>
 __global__ void ring_append_kernel(const T* k, const T* v, int L, int n, int nkv,
                                    int hd, T* ring_k, T* ring_v, long long cap,
                                    const RingState* ring) {
+  pdl_enter();
   const long long total = (long long)L * n * nkv;
   for (long long it = blockIdx.x; it < total; it += gridDim.x) {
     const int h = static_cast<int>(it % nkv);
@@ -225,6 +236,7 @@ template <typename T>
 __global__ void ring_gather_kernel(const T* ring_k, const T* ring_v, int L,
                                    long long cap, int nkv, int hd, long long pos0,
                                    int count, T* k_out, T* v_out) {
+  pdl_enter();
   const long long total = (long long)L * count * nkv;
   for (long long it = blockIdx.x; it < total; it += gridDim.x) {
     const int h = static_cast<int>(it % nkv);
@@ -243,6 +255,7 @@ __global__ void ring_gather_kernel(const T* ring_k, const T* ring_v, int L,
 // ---- stand-in target -------------------------------------------------------------
 template <typename T>
 __global__ void synth_target_kernel(SynthArgs a) {
+  pdl_enter();
   const long long r = a.rs->rounds;
   const int kl = static_cast<int>(r % a.n_logit);
   const int kc = static_cast<int>(r % a.n_coin);
@@ -277,11 +290,11 @@ cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab, R
                                cudaStream_t st) {
   const int grid = rows > tab_rows ? rows : tab_rows;
   if (dtype)
-    embed_block_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)embed, H, vocab, rs, mask_id,
+    launch_pdl(embed_block_kernel<bf16>, dim3(grid), dim3(256), 0, st, (const bf16*)embed, H, vocab, rs, mask_id,
                                                    rows, (bf16*)x, ring, inv_freq, half,
                                                    tab_rows, rope);
   else
-    embed_block_kernel<float><<<grid, 256, 0, st>>>((const float*)embed, H, vocab, rs, mask_id,
+    launch_pdl(embed_block_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)embed, H, vocab, rs, mask_id,
                                                     rows, (float*)x, ring, inv_freq, half,
                                                     tab_rows, rope);
   return cudaGetLastError();
@@ -290,7 +303,7 @@ cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab, R
 cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,
                               long long pos0, int rows, float2* rope, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  rope_table_kernel<<<rows, 64, 0, st>>>(inv_freq, half, ring, pos0, rows, rope);
+  launch_pdl(rope_table_kernel, dim3(rows), dim3(64), 0, st, inv_freq, half, ring, pos0, rows, rope);
   return cudaGetLastError();
 }
 
@@ -298,10 +311,10 @@ cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g, voi
                            int ldy, int rows, int H, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (dtype)
-    rmsnorm_kernel<bf16><<<rows, 256, 0, st>>>((const bf16*)x, ldx, (const bf16*)g, (bf16*)y,
+    launch_pdl(rmsnorm_kernel<bf16>, dim3(rows), dim3(256), 0, st, (const bf16*)x, ldx, (const bf16*)g, (bf16*)y,
                                                ldy, H, eps);
   else
-    rmsnorm_kernel<float><<<rows, 256, 0, st>>>((const float*)x, ldx, (const float*)g,
+    launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, st, (const float*)x, ldx, (const float*)g,
                                                 (float*)y, ldy, H, eps);
   return cudaGetLastError();
 }
@@ -313,10 +326,10 @@ cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows, int he
   if (items <= 0) return cudaSuccess;
   const int grid = (items + 3) / 4;
   if (dtype)
-    head_norm_rope_kernel<bf16><<<grid, 128, 0, st>>>((bf16*)buf, ld, rows, heads, hd,
+    launch_pdl(head_norm_rope_kernel<bf16>, dim3(grid), dim3(128), 0, st, (bf16*)buf, ld, rows, heads, hd,
                                                       (const bf16*)g, eps, rope, neox);
   else
-    head_norm_rope_kernel<float><<<grid, 128, 0, st>>>((float*)buf, ld, rows, heads, hd,
+    launch_pdl(head_norm_rope_kernel<float>, dim3(grid), dim3(128), 0, st, (float*)buf, ld, rows, heads, hd,
                                                        (const float*)g, eps, rope, neox);
   return cudaGetLastError();
 }
@@ -330,12 +343,12 @@ cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int n
   if (items <= 0) return cudaSuccess;
   const int grid = (items + 3) / 4;
   if (dtype)
-    kv_to_ring_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)kv, ld, rows, nkv, hd,
+    launch_pdl(kv_to_ring_kernel<bf16>, dim3(grid), dim3(128), 0, st, (const bf16*)kv, ld, rows, nkv, hd,
                                                   (const bf16*)kg, eps, rope, neox,
                                                   (bf16*)ring_k, (bf16*)ring_v, cap,
                                                   append_only, ring, use_dev, pos_host);
   else
-    kv_to_ring_kernel<float><<<grid, 128, 0, st>>>((const float*)kv, ld, rows, nkv, hd,
+    launch_pdl(kv_to_ring_kernel<float>, dim3(grid), dim3(128), 0, st, (const float*)kv, ld, rows, nkv, hd,
                                                    (const float*)kg, eps, rope, neox,
                                                    (float*)ring_k, (float*)ring_v, cap,
                                                    append_only, ring, use_dev, pos_host);
@@ -344,22 +357,22 @@ cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int n
 
 cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
                           cudaStream_t st) {
-  commit_kernel<<<1, 1, 0, st>>>(rs, ring, block, keep);
+  launch_pdl(commit_kernel, dim3(1), dim3(1), 0, st, rs, ring, block, keep);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st) {
-  ring_advance_kernel<<<1, 1, 0, st>>>(ring, d, mode);
+  launch_pdl(ring_advance_kernel, dim3(1), dim3(1), 0, st, ring, d, mode);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ring_reset(RingState* ring, long long base, cudaStream_t st) {
-  ring_reset_kernel<<<1, 1, 0, st>>>(ring, base);
+  launch_pdl(ring_reset_kernel, dim3(1), dim3(1), 0, st, ring, base);
   return cudaGetLastError();
 }
 
 cudaError_t launch_set_anchor(RoundState* rs, int anchor, cudaStream_t st) {
-  set_anchor_kernel<<<1, 1, 0, st>>>(rs, anchor);
+  launch_pdl(set_anchor_kernel, dim3(1), dim3(1), 0, st, rs, anchor);
   return cudaGetLastError();
 }
 
@@ -370,10 +383,10 @@ cudaError_t launch_ring_append(int dtype, const void* k, const void* v, int L, i
   const long long items = (long long)L * n * nkv;
   const int grid = static_cast<int>(items < 4096 ? items : 4096);
   if (dtype)
-    ring_append_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)k, (const bf16*)v, L, n, nkv,
+    launch_pdl(ring_append_kernel<bf16>, dim3(grid), dim3(128), 0, st, (const bf16*)k, (const bf16*)v, L, n, nkv,
                                                    hd, (bf16*)ring_k, (bf16*)ring_v, cap, ring);
   else
-    ring_append_kernel<float><<<grid, 128, 0, st>>>((const float*)k, (const float*)v, L, n, nkv,
+    launch_pdl(ring_append_kernel<float>, dim3(grid), dim3(128), 0, st, (const float*)k, (const float*)v, L, n, nkv,
                                                     hd, (float*)ring_k, (float*)ring_v, cap,
                                                     ring);
   cudaError_t e = cudaGetLastError();
@@ -388,11 +401,11 @@ cudaError_t launch_ring_gather(int dtype, const void* ring_k, const void* ring_v
   const long long items = (long long)L * count * nkv;
   const int grid = static_cast<int>(items < 4096 ? items : 4096);
   if (dtype)
-    ring_gather_kernel<bf16><<<grid, 128, 0, st>>>((const bf16*)ring_k, (const bf16*)ring_v, L,
+    launch_pdl(ring_gather_kernel<bf16>, dim3(grid), dim3(128), 0, st, (const bf16*)ring_k, (const bf16*)ring_v, L,
                                                    cap, nkv, hd, pos0, count, (bf16*)k_out,
                                                    (bf16*)v_out);
   else
-    ring_gather_kernel<float><<<grid, 128, 0, st>>>((const float*)ring_k, (const float*)ring_v,
+    launch_pdl(ring_gather_kernel<float>, dim3(grid), dim3(128), 0, st, (const float*)ring_k, (const float*)ring_v,
                                                     L, cap, nkv, hd, pos0, count,
                                                     (float*)k_out, (float*)v_out);
   return cudaGetLastError();
@@ -402,8 +415,8 @@ cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st) 
   const long long total = (long long)a.block * (a.V + a.kin);
   const long long g = (total + 255) / 256;
   const int grid = static_cast<int>(g < 2048 ? g : 2048);
-  if (dtype) synth_target_kernel<bf16><<<grid, 256, 0, st>>>(a);
-  else synth_target_kernel<float><<<grid, 256, 0, st>>>(a);
+  if (dtype) launch_pdl(synth_target_kernel<bf16>, dim3(grid), dim3(256), 0, st, a);
+  else launch_pdl(synth_target_kernel<float>, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError();
 }
 

@@ -197,11 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!finish) {
         // Split tile: publish this CTA's partial, take a ticket.
         const int slot = (t == first_tile) ? 0 : 1;
-        float* mine = a.partials + ((size_t)b * 2 + slot) * NV * BN * 128;
+        // row-contiguous [128][NV*BN] so each thread moves its values as float4
+        float4* mine = reinterpret_cast<float4*>(a.partials + ((size_t)b * 2 + slot) * NV * BN * 128 +
+                                                 (size_t)row * NV * BN);
 #pragma unroll
         for (int v = 0; v < NV; ++v)
 #pragma unroll
-          for (int m = 0; m < BN; ++m) mine[(v * BN + m) * 128 + row] = acc[v][m];
+          for (int m = 0; m < BN; m += 4)
+            mine[(v * BN + m) / 4] = make_float4(acc[v][m], acc[v][m + 1], acc[v][m + 2], acc[v][m + 3]);
         __threadfence();
         epi_sync();
         const int bf = owner_of((long long)t * KC, U, G);
@@ -221,11 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int bb = bf; bb <= bl; ++bb) {
             const int first_bb = static_cast<int>((U * bb / G) / KC);
             const int sl = (t == first_bb) ? 0 : 1;
-            const float* p = a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128;
+            const float4* p = reinterpret_cast<const float4*>(
+                a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128 + (size_t)row * NV * BN);
+            float4 pv[NV * BN / 4];
 #pragma unroll
-            for (int v = 0; v < NV; ++v)
+            for (int j = 0; j < NV * BN / 4; ++j) pv[j] = __ldcg(p + j);
 #pragma unroll
-              for (int m = 0; m < BN; ++m) acc[v][m] += __ldcg(p + (v * BN + m) * 128 + row);
+            for (int j = 0; j < NV * BN / 4; ++j) {
+              float* dst = &acc[(4 * j) / BN][(4 * j) % BN];
+              dst[0] += pv[j].x; dst[1] += pv[j].y; dst[2] += pv[j].z; dst[3] += pv[j].w;
+            }
           }
           if (threadIdx.x == 64) a.tile_ctr[t] = 0u;
         }
