@@ -353,6 +353,11 @@ def run_ours(args, world, rank, local):
     lm_t = [t for _, t in lm]
     achieved = sum(lm_bytes) / (sum(lm_t) / 1e3) / 1e9 if lm_t else None
     widths = [w for r in results for w in r["widths"]]
+    per_width = {}
+    for r in results:
+        for (w, tokens, wms, _adopted) in r["controller"]:
+            per_width.setdefault(w, []).append(wms / args.window)
+    round_us = {str(w): round(1e3 * statistics.mean(v), 1) for w, v in sorted(per_width.items())}
 
     e2e = None
     if not args.no_e2e:
@@ -390,6 +395,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2: ~1.5 GB of weights streamed per round"},
             "draft_tok_s": round(proposals / (ms_max / 1e3), 1),
+            "round_us_by_width": round_us,
             "accepted_per_round": round(accepted / nrounds, 4),
             "emitted_per_round": round(accepted / nrounds + 1, 4),
             "roofline": {"kernel": "lmhead_argmax (split-vocab lm_head + softcap + argmax)",

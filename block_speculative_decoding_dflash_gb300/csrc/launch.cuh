@@ -13,10 +13,11 @@
 
 namespace dfl {
 
-// Wait for the preceding grid, then let the following grid be scheduled.
+// Let the following grid be scheduled (it can take free SM resources and
+// start streaming its weights), then wait for the preceding grid.
 __device__ __forceinline__ void pdl_enter() {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
 }
 
 template <typename... KArgs, typename... Args>

@@ -57,7 +57,7 @@ __device__ __forceinline__ int owner_of(long long u, long long U, int G) {
 }
 
 template <int BN, int EPI, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   constexpr int NV = (EPI == kEpiSwiglu) ? 2 : 1;
   using C = Cfg<BN, NV, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -326,8 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
 }
 
+// The decode-layer GEMMs are short: keep two CTAs per SM (about 73 / 103 KB of
+// shared memory each) so the next GEMM's CTAs fit beside the running one and
+// stream their first weight tiles early. The lm_head is long: a deep ring.
 template <int BN, int EPI>
-constexpr int stages_for() { return EPI == kEpiSwiglu ? 6 : 8; }
+constexpr int stages_for() { return EPI == kEpiArgmax ? 8 : EPI == kEpiSwiglu ? 3 : 4; }
 
 template <int BN, int EPI>
 cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
