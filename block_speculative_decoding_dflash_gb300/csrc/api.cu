@@ -194,6 +194,7 @@ struct dflash_ctx {
   int* tc_lm_pi = nullptr;
   unsigned* tc_done = nullptr;
   unsigned* attn_ctr = nullptr;
+  const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -325,6 +326,39 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
     CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
   }
   CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
+  if (tc && c->hd == 128) {
+    // One GEMM per group of up to five layers over [Wk_l | Wv_l ...]; its
+    // epilogue norms, rotates and writes K and V straight into the ring.
+    const int L = c->cfg.n_layers;
+    for (int l0 = 0; l0 < L; l0 += kTcMaxSeg / 2) {
+      const int nl = L - l0 < kTcMaxSeg / 2 ? L - l0 : kTcMaxSeg / 2;
+      TcGemmArgs t = tc_args(c, rows, nl * 2 * c->kvdim, c->H, kEpiKVRing);
+      t.nseg = 2 * nl;
+      int tiles = 0;
+      for (int j = 0; j < nl; ++j) {
+        t.a_map[2 * j] = c->lmaps[l0 + j].wk;
+        t.a_map[2 * j + 1] = c->lmaps[l0 + j].wv;
+        tiles += c->kvdim / 128;
+        t.seg_tiles[2 * j] = tiles;
+        tiles += c->kvdim / 128;
+        t.seg_tiles[2 * j + 1] = tiles;
+      }
+      t.b_map = c->appc_map[bn_index(rows)];
+      const size_t lay = (size_t)l0 * c->nkv * c->ring->cap * c->hd * c->esz;
+      t.ring_k = static_cast<char*>(c->ring->k) + lay;
+      t.ring_v = static_cast<char*>(c->ring->v) + lay;
+      t.cap = c->ring->cap;
+      t.ring = c->ring->st;
+      t.rope = rope;
+      t.kgain = c->kgain_dev + l0;
+      t.nkv = c->nkv;
+      t.neox = c->cfg.rope_neox;
+      t.append_only = c->ring->append_only;
+      t.eps = c->cfg.rms_eps;
+      CK(c->err, tc_run(c, t));
+    }
+    return DFLASH_OK;
+  }
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     if (tc) {
       TcGemmArgs t = tc_args(c, rows, 2 * c->kvdim, c->H, kEpiStore);
@@ -589,7 +623,8 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
-      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)c->nkv * 4};
+      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)c->nkv * 4,
+      (size_t)cfg->n_layers * sizeof(void*)};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -633,12 +668,17 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->tc_lm_pi = carve<int>(cur, sizes[si++]);
   c->tc_done = carve<unsigned>(cur, sizes[si++]);
   c->attn_ctr = carve<unsigned>(cur, sizes[si++]);
+  c->kgain_dev = carve<const void*>(cur, sizes[si++]);
 
+  std::vector<const void*> kg(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) kg[l] = c->layers[(size_t)l * DFLASH_LAYER_TENSORS + 5];
   std::vector<double> inv(c->half);
   for (int i = 0; i < c->half; ++i)
     inv[i] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / static_cast<double>(c->hd));
   if ((e = cudaMemsetAsync(c->arena, 0, total, c->stream)) != cudaSuccess ||
       (e = cudaMemcpyAsync(c->inv_freq, inv.data(), sizeof(double) * c->half,
+                           cudaMemcpyHostToDevice, c->stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(c->kgain_dev, kg.data(), sizeof(void*) * kg.size(),
                            cudaMemcpyHostToDevice, c->stream)) != cudaSuccess ||
       (e = init_lmhead_attrs(c->H)) != cudaSuccess ||
       (e = init_attention_attrs(c->hd)) != cudaSuccess ||

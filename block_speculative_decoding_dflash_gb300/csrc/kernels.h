@@ -31,17 +31,21 @@ struct LinearArgs {
   int M, N, K;
   int epi;
 };
-enum : int { kEpiArgmax = 3 };  // tensor-core GEMM only: softcap + per-row argmax
+enum : int {
+  kEpiArgmax = 3,   // tensor-core GEMM only: softcap + per-row argmax
+  kEpiKVRing = 4,   // tensor-core GEMM only: K head-norm + RoPE / V, into ring slots
+};
+constexpr int kTcMaxSeg = 10;
 
 // Tensor-core weight-streaming GEMM D[n, m] = sum_k W[n, k] X[m, k] (bf16,
 // fp32 accumulate), M <= BN rows of X (BN 16 or 32). Weight rows are stacked
 // segments of whole 128-row tiles (seg_tiles = cumulative tile counts); the
 // last segment may end in a partial tile (rows past N are zero-filled).
 struct TcGemmArgs {
-  CUtensorMap a_map[3];            // weight segments, box {64, 128}
+  CUtensorMap a_map[kTcMaxSeg];    // weight segments, box {64, 128}
   CUtensorMap a2_map;              // up weight of kEpiSwiglu, box {64, 128}
   CUtensorMap b_map;               // X, box {64, BN}
-  int seg_tiles[3];
+  int seg_tiles[kTcMaxSeg];
   int nseg;
   int M, N, K, tiles, kchunks, epi;
   void* y; int ldy;                // output [M, N] (row stride ldy)
@@ -53,6 +57,16 @@ struct TcGemmArgs {
   int* ids; int* ids2; float* maxv;
   float* part_v; int* part_i;      // [grid * M]
   unsigned* done_ctr;
+  // kEpiKVRing: the weight rows are [K_0 | V_0 | K_1 | V_1 | ...], one
+  // 128-row tile per kv head (head_dim 128); row m goes to position
+  // ring->offset + m.
+  void* ring_k; void* ring_v;      // [L][nkv][cap][128]
+  long long cap;
+  RingState* ring;
+  const float2* rope;              // [M][64] (cos, sin)
+  const void* const* kgain;        // [L] k_norm gains, device array of pointers
+  int nkv, neox, append_only;
+  float eps;
 };
 bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);

@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   __shared__ float red_v[4][BN];
   __shared__ int red_i[4][BN];
   __shared__ int s_last;
+  __shared__ float kv_ss[4][BN];
+  __shared__ float kv_x[(EPI == kEpiKVRing) ? 128 * BN : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
@@ -221,18 +223,31 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           for (int v = 0; v < NV; ++v)
 #pragma unroll
             for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
-          for (int bb = bf; bb <= bl; ++bb) {
-            const int first_bb = static_cast<int>((U * bb / G) / KC);
-            const int sl = (t == first_bb) ? 0 : 1;
-            const float4* p = reinterpret_cast<const float4*>(
-                a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128 + (size_t)row * NV * BN);
-            float4 pv[NV * BN / 4];
+          // Sum the contributors' partials in CTA order, issuing the loads of
+          // kBatch contributors before adding them (L2 latency, not bandwidth,
+          // bounds this loop).
+          constexpr int kBatch = NV * BN <= 16 ? 4 : NV * BN <= 32 ? 2 : 1;
+          for (int b0 = bf; b0 <= bl; b0 += kBatch) {
+            float4 pv[kBatch][NV * BN / 4];
 #pragma unroll
-            for (int j = 0; j < NV * BN / 4; ++j) pv[j] = __ldcg(p + j);
+            for (int q = 0; q < kBatch; ++q) {
+              const int bb = b0 + q;
+              if (bb > bl) break;
+              const int first_bb = static_cast<int>((U * bb / G) / KC);
+              const int sl = (t == first_bb) ? 0 : 1;
+              const float4* p = reinterpret_cast<const float4*>(
+                  a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128 + (size_t)row * NV * BN);
 #pragma unroll
-            for (int j = 0; j < NV * BN / 4; ++j) {
-              float* dst = &acc[(4 * j) / BN][(4 * j) % BN];
-              dst[0] += pv[j].x; dst[1] += pv[j].y; dst[2] += pv[j].z; dst[3] += pv[j].w;
+              for (int j = 0; j < NV * BN / 4; ++j) pv[q][j] = __ldcg(p + j);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              if (b0 + q > bl) break;
+#pragma unroll
+              for (int j = 0; j < NV * BN / 4; ++j) {
+                float* dst = &acc[(4 * j) / BN][(4 * j) % BN];
+                dst[0] += pv[q][j].x; dst[1] += pv[q][j].y; dst[2] += pv[q][j].z; dst[3] += pv[q][j].w;
+              }
             }
           }
           if (threadIdx.x == 64) a.tile_ctr[t] = 0u;
@@ -266,6 +281,70 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           best_i[m] = bi;
         }
         epi_sync();
+      } else if (EPI == kEpiKVRing) {
+        // tile t = kv head h of layer l, K or V (hd = 128 = one tile)
+        const int seg = t / a.nkv, h = t % a.nkv;
+        const int layer = seg >> 1;
+        const bool isv = seg & 1;
+        const long long off0 = a.ring->offset;
+        const size_t head_base = (((size_t)layer * a.nkv + h) * a.cap) * 128;
+        bf16* dst = reinterpret_cast<bf16*>(isv ? a.ring_v : a.ring_k) + head_base;
+        float val[BN];
+#pragma unroll
+        for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
+        if (!isv) {
+          // per-head RMSNorm over the 128 rows of the tile (one per thread)
+#pragma unroll
+          for (int m = 0; m < BN; ++m) {
+            const float ss = warp_sum(val[m] * val[m]);
+            if (lane == 0) kv_ss[q][m] = ss;
+          }
+          epi_sync();
+          const float g = __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[layer])[row]);
+#pragma unroll
+          for (int m = 0; m < BN; ++m) {
+            const float ss = kv_ss[0][m] + kv_ss[1][m] + kv_ss[2][m] + kv_ss[3][m];
+            val[m] = val[m] * rsqrtf(ss / 128.0f + a.eps) * g;
+          }
+          // RoPE on the normed values: pair (i, i + 64) or (2i, 2i + 1)
+          if (a.neox) {
+#pragma unroll
+            for (int m = 0; m < BN; ++m) kv_x[row * BN + m] = val[m];
+            epi_sync();
+            const int i = row & 63;
+            const bool lo = row < 64;
+            const int partner = lo ? row + 64 : row - 64;
+#pragma unroll
+            for (int m = 0; m < BN; ++m) {
+              if (m >= a.M) break;
+              const float2 cs = a.rope[m * 64 + i];
+              const float other = kv_x[partner * BN + m];
+              val[m] = lo ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
+            }
+            epi_sync();
+          } else {
+            const int i = row >> 1;
+            const bool ev = (row & 1) == 0;
+#pragma unroll
+            for (int m = 0; m < BN; ++m) {
+              const float other = __shfl_xor_sync(0xffffffffu, val[m], 1);
+              if (m < a.M) {
+                const float2 cs = a.rope[m * 64 + i];
+                val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < BN; ++m) {
+          if (m >= a.M) break;
+          const long long pos = off0 + m;
+          if (a.append_only && pos - a.ring->base >= a.cap) {
+            if (row == 0) atomicOr(&a.ring->error, kErrFull);
+            continue;
+          }
+          dst[(size_t)ring_slot(pos, a.cap) * 128 + row] = __float2bfloat16_rn(val[m]);
+        }
       } else if (valid) {
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
@@ -390,17 +469,26 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiStore>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiResid>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiKVRing>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiKVRing>()) != cudaSuccess) return e;
   return attr_tc<32, kEpiArgmax>();
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st) {
+  // At least kMinUnits (64-wide K chunks of a 128-row tile, 16 KB of weights
+  // each) per CTA: a short GEMM then splits a tile over a few CTAs rather than
+  // a dozen, whose partial sums the last one would have to gather.
+  constexpr long long kMinUnits = 8;
   const long long U = (long long)a.tiles * a.kchunks;
-  if (grid > U) grid = static_cast<int>(U);
+  const long long want = (U + kMinUnits - 1) / kMinUnits;
+  if (grid > want) grid = static_cast<int>(want);
+  if (grid < 1) grid = 1;
   if (bn == 16) {
     switch (a.epi) {
       case kEpiStore: return launch_tc<16, kEpiStore>(a, grid, pdl, st);
       case kEpiResid: return launch_tc<16, kEpiResid>(a, grid, pdl, st);
       case kEpiSwiglu: return launch_tc<16, kEpiSwiglu>(a, grid, pdl, st);
+      case kEpiKVRing: return launch_tc<16, kEpiKVRing>(a, grid, pdl, st);
       default: return launch_tc<16, kEpiArgmax>(a, grid, pdl, st);
     }
   }
@@ -408,6 +496,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
     case kEpiStore: return launch_tc<32, kEpiStore>(a, grid, pdl, st);
     case kEpiResid: return launch_tc<32, kEpiResid>(a, grid, pdl, st);
     case kEpiSwiglu: return launch_tc<32, kEpiSwiglu>(a, grid, pdl, st);
+    case kEpiKVRing: return launch_tc<32, kEpiKVRing>(a, grid, pdl, st);
     default: return launch_tc<32, kEpiArgmax>(a, grid, pdl, st);
   }
 }
