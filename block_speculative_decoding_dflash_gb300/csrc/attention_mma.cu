@@ -6,9 +6,9 @@
 // g): S = Q K^T for the warp's keys (mask |q - k| <= W by absolute
 // positions), the warp's online-softmax partial (max, sum, P V), a merge of
 // the 8 warps in shared memory in warp order, and the CTA's partial written
-// to global scratch. The CTA that takes the last ticket of head g merges the
-// splits in split order and writes the bf16 output: no separate combine
-// launch, no CTA ever waits on another, and the result is deterministic.
+// to global scratch. A combine kernel (one warp per (query, head)) merges the
+// splits in split order and writes the bf16 output; nothing waits on another
+// CTA and the result is deterministic.
 //
 // Keys are addressed by absolute position (ring slot = position mod cap), the
 // context keys [kstart, p) followed by the block's own rows.
@@ -36,7 +36,9 @@ struct MmaSmem {
   float o[kWarps][16][kHd];                // per-warp unnormalised P V
   float m[kWarps][16];
   float l[kWarps][16];
-  int last;
+  float f[kWarps][16];                     // exp(m_w - M) per (warp, row)
+  float L[16];                             // merged sum per row
+  float M[16];                             // merged max per row
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -72,8 +74,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit,
-                                                               unsigned* head_ctr) {
+__global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
@@ -214,96 +215,90 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       S.l[warp][grp] = l_row[0]; S.l[warp][grp + 8] = l_row[1];
     }
     __syncthreads();
+    // per-row merge weights of the 8 warps: one thread per (row, warp)
+    if (threadIdx.x < 16 * kWarps) {
+      const int r = threadIdx.x >> 3, w = threadIdx.x & 7;
+      float M = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < kWarps; ++x) M = fmaxf(M, S.m[x][r]);
+      const float mw = S.m[w][r];
+      const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : expf(mw - M);
+      S.f[w][r] = f;
+      float lw = f * S.l[w][r];
+#pragma unroll
+      for (int o2 = 4; o2 > 0; o2 >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o2);
+      if (w == 0) { S.L[r] = lw; S.M[r] = M; }
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < 16 * kHd; e += blockDim.x) {
       const int r = e / kHd, d = e % kHd;
       const int qi = qt * 16 + r;
       if (qi >= Qn) continue;
-      float M = -INFINITY;
+      float O = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, S.m[w][r]);
-      float O = 0.f, L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float mw = S.m[w][r];
-          if (mw == -INFINITY) continue;
-          const float f = expf(mw - M);
-          O += f * S.o[w][r][d];
-          L += f * S.l[w][r];
-        }
-      }
+      for (int w = 0; w < kWarps; ++w) O = fmaf(S.f[w][r], S.o[w][r][d], O);
       float* out = part + (size_t)qi * pstride;
       out[d] = O;
-      if (d == 0) { out[kHd] = M; out[kHd + 1] = L; }
+      if (d == 0) { out[kHd] = S.M[r]; out[kHd + 1] = S.L[r]; }
     }
     __syncthreads();
   }
+}
 
-  // the last CTA of head g merges the splits
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) S.last = (atomicAdd(&head_ctr[g], 1u) == static_cast<unsigned>(nsplit - 1));
-  __syncthreads();
-  if (!S.last) return;
-  __threadfence();
-  const float* base = a.partial + (size_t)g * nsplit * Qn * pstride;
-  bf16* outp = reinterpret_cast<bf16*>(a.out);
-  // Split weights exp(m_s - M) and 1/L per query, computed once (the K/V tile
-  // area of shared memory is free now): all (split, query) maxima and sums
-  // are loaded in parallel first.
-  float* wsm = reinterpret_cast<float*>(&S.k[0][0]);          // [nsplit][16] weights
-  float* linv = reinterpret_cast<float*>(&S.v[0][0]);         // [16] 1 / L
-  for (int q0 = 0; q0 < Qn; q0 += 16) {
-    const int nq = Qn - q0 < 16 ? Qn - q0 : 16;
-    for (int e = threadIdx.x; e < nsplit * nq; e += blockDim.x) {
-      const int sp = e / nq, qi = q0 + e % nq;
-      wsm[sp * 16 + (qi - q0)] = __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd);
-    }
-    __syncthreads();
-    if (threadIdx.x < nq) {
-      const int r = threadIdx.x, qi = q0 + r;
-      float M = -INFINITY;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wsm[sp * 16 + r]);
-      float L = 0.f;
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const float ms = wsm[sp * 16 + r];
-        const float f = ms == -INFINITY ? 0.f : expf(ms - M);
-        wsm[sp * 16 + r] = f;
-        if (f != 0.f) L += f * __ldcg(base + ((size_t)sp * Qn + qi) * pstride + kHd + 1);
-      }
-      linv[r] = 1.0f / L;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < nq * (kHd / 4); e += blockDim.x) {
-      const int r = e / (kHd / 4), qi = q0 + r, d4 = (e % (kHd / 4)) * 4;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      int sp = 0;
-      for (; sp + 4 <= nsplit; sp += 4) {
-        float4 ov[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          ov[u] = __ldcg(reinterpret_cast<const float4*>(base + ((size_t)(sp + u) * Qn + qi) * pstride + d4));
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float f = wsm[(sp + u) * 16 + r];
-          acc[0] += f * ov[u].x; acc[1] += f * ov[u].y; acc[2] += f * ov[u].z; acc[3] += f * ov[u].w;
-        }
-      }
-      for (; sp < nsplit; ++sp) {
-        const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + ((size_t)sp * Qn + qi) * pstride + d4));
-        const float f = wsm[sp * 16 + r];
-        acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
-      }
-      const float inv = linv[r];
-      bf16* dst = outp + (size_t)(qi / G) * a.ldo + (size_t)(g * G + qi % G) * kHd + d4;
-      dst[0] = __float2bfloat16_rn(acc[0] * inv);
-      dst[1] = __float2bfloat16_rn(acc[1] * inv);
-      dst[2] = __float2bfloat16_rn(acc[2] * inv);
-      dst[3] = __float2bfloat16_rn(acc[3] * inv);
-    }
-    __syncthreads();
+// One warp per (query, kv head): merge the splits' partials in split order.
+__global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int nsplit) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.nq / a.nkv;
+  const int Qn = a.rows * G;
+  const int item = blockIdx.x * 4 + warp;
+  if (item >= a.nkv * Qn) return;
+  const int g = item / Qn, qi = item % Qn;
+  const size_t pstride = kPartStride;
+  const float* base = a.partial + (size_t)g * nsplit * Qn * pstride + (size_t)qi * pstride;
+  const size_t sstride = (size_t)Qn * pstride;
+  // split maxima and sums, 32 splits per load round
+  float M = -INFINITY;
+  for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(base + sp * sstride + kHd));
+  M = warp_max(M);
+  float L = 0.f;
+  for (int sp = lane; sp < nsplit; sp += 32) {
+    const float ms = __ldcg(base + sp * sstride + kHd);
+    if (ms != -INFINITY) L += expf(ms - M) * __ldcg(base + sp * sstride + kHd + 1);
   }
-  if (threadIdx.x == 0) head_ctr[g] = 0u;
+  L = warp_sum(L);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int d4 = lane * 4;
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int sp_l = s0 + lane;
+    const float ms_l = sp_l < nsplit ? __ldcg(base + sp_l * sstride + kHd) : -INFINITY;
+    const float f_l = ms_l == -INFINITY ? 0.f : expf(ms_l - M);
+    const int n = nsplit - s0 < 32 ? nsplit - s0 : 32;
+    int j = 0;
+    for (; j + 8 <= n; j += 8) {
+      float4 ov[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j + u) * sstride + d4));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float f = __shfl_sync(0xffffffffu, f_l, j + u);
+        acc[0] += f * ov[u].x; acc[1] += f * ov[u].y; acc[2] += f * ov[u].z; acc[3] += f * ov[u].w;
+      }
+    }
+    for (; j < n; ++j) {
+      const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + d4));
+      const float f = __shfl_sync(0xffffffffu, f_l, j);
+      acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
+    }
+  }
+  const float inv = 1.0f / L;
+  bf16* dst = reinterpret_cast<bf16*>(a.out) + (size_t)(qi / G) * a.ldo +
+              (size_t)(g * G + qi % G) * kHd + d4;
+  dst[0] = __float2bfloat16_rn(acc[0] * inv);
+  dst[1] = __float2bfloat16_rn(acc[1] * inv);
+  dst[2] = __float2bfloat16_rn(acc[2] * inv);
+  dst[3] = __float2bfloat16_rn(acc[3] * inv);
 }
 
 }  // namespace
@@ -321,11 +316,13 @@ cudaError_t init_attention_mma_attrs() {
                               (int)sizeof(MmaSmem));
 }
 
-cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st) {
+cudaError_t launch_attention_mma(const AttnArgs& a, unsigned*, cudaStream_t st) {
   const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
   dim3 grid(nsplit, a.nkv);
-  launch_pdl(attn_mma_kernel, dim3(grid), dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit, head_ctr);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_mma_kernel, grid, dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit);
+  if (e != cudaSuccess) return e;
+  const int items = a.nkv * a.rows * (a.nq / a.nkv);
+  return launch_pdl(attn_mma_combine_kernel, dim3((items + 3) / 4), dim3(128), 0, st, a, nsplit);
 }
 
 }  // namespace dfl
