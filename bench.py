@@ -231,7 +231,10 @@ class Job:
             with torch.cuda.stream(s):
                 self.resid.copy_(self.h_resid, non_blocking=True)
         c.reset_stats()
+        i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        i0.record(s)
         c.graph_launch(self.SLOT_INGEST)
+        i1.record(s)
         launches += self.kcount[self.SLOT_INGEST]
         ctl = ThroughputController(4, 16, window=a.window, challenge_every=a.challenge_every)
         done, lm_ms, emitted_prev, proposals = 0, [], 0, 0
@@ -269,7 +272,7 @@ class Job:
             done += nr
         st = c.stats()
         return {"stats": st, "lm_ms": lm_ms, "launches": launches, "widths": widths_used,
-                "controller": ctl.history}
+                "controller": ctl.history, "ingest_ms": i0.elapsed_time(i1)}
 
     def e2e_bytes_per_step(self, widths):
         V, kin = self.cfg["vocab"], self.cfg["k_target_layers"] * self.cfg["target_hidden"]
@@ -359,6 +362,17 @@ def run_ours(args, world, rank, local):
             per_width.setdefault(w, []).append(wms / args.window)
     round_us = {str(w): round(1e3 * statistics.mean(v), 1) for w, v in sorted(per_width.items())}
 
+    # context ingest: fc over the kept rows plus every layer's K|V projection
+    cfg = job.cfg
+    kin = cfg["k_target_layers"] * cfg["target_hidden"]
+    rows = cfg["context_rows"]
+    ingest_flop = 2 * rows * cfg["hidden"] * kin + \
+        cfg["n_layers"] * 2 * rows * cfg["hidden"] * 2 * cfg["n_kv_heads"] * cfg["head_dim"]
+    ingest_ms = statistics.median(r["ingest_ms"] for r in results)
+    ingest_tf = ingest_flop / (ingest_ms / 1e3) / 1e12
+    ingest = {"kernels": "tc_gemm_wide_kernel (fc, K|V) + rmsnorm + kv_to_ring", "gflop": round(ingest_flop / 1e9, 1),
+              "ms": round(ingest_ms, 4), "tflops": round(ingest_tf, 1),
+              "peak_tflops": peaks.get("bf16_tflops"), "frac": round(ingest_tf / peaks.get("bf16_tflops", 1900.0), 4)}
     e2e = None
     if not args.no_e2e:
         for _ in range(1):
@@ -404,6 +418,7 @@ def run_ours(args, world, rank, local):
                          "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
                          "traffic": None, "launches_timed": len(lm_t),
                          "mean_ms": round(sum(lm_t) / len(lm_t), 4) if lm_t else None},
+            "context_ingest": ingest,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "setup_s": round(job.setup_s, 1),
         }

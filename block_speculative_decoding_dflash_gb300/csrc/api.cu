@@ -186,6 +186,9 @@ struct dflash_ctx {
   struct LayerMaps { CUtensorMap wq, wk, wv, wo, wg, wu, wd; };
   std::vector<LayerMaps> lmaps;
   CUtensorMap fc_map{}, lm_map{};
+  struct WideMaps { CUtensorMap wk, wv; };
+  std::vector<WideMaps> lmaps_wide;          // box {64, 256} for the ingest GEMM
+  CUtensorMap fcw_map{};
   CUtensorMap xn_map[2]{}, attn_map[2]{}, sbuf_map[2]{}, appc_map[2]{}, xf_map[2][2]{};
   float* tc_part = nullptr;
   unsigned* tc_tiles = nullptr;
@@ -383,6 +386,51 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
   return DFLASH_OK;
 }
 
+// Context rows on the tensor cores (many rows): fc -> hidden_norm -> all
+// layers' [Wk | Wv] in launches of up to five layers -> ring writes.
+int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void* cn, void* kv,
+                      float2* rope, long long pos_host) {
+  const int dt = c->dt;
+  cudaStream_t st = c->stream;
+  CK(c->err, launch_rope_table(c->inv_freq, c->half, nullptr, pos_host, rows, rope, st));
+  TcWideArgs a{};
+  a.M = rows; a.K = c->kin; a.N = c->H; a.nseg = 1; a.seg_rows[0] = c->H;
+  a.w_map[0] = c->fcw_map;
+  a.y = f; a.ldy = c->H; a.err = c->tc_err;
+  if (!tc_encode_map(&a.x_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, 128))
+    return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the context rows");
+  CK(c->err, launch_tc_wide(a, c->num_sms, st));
+  CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
+  const int L = c->cfg.n_layers;
+  const int ldkv = L * 2 * c->kvdim;
+  for (int l0 = 0; l0 < L; l0 += kTcMaxSeg / 2) {
+    const int nl = L - l0 < kTcMaxSeg / 2 ? L - l0 : kTcMaxSeg / 2;
+    TcWideArgs b{};
+    b.M = rows; b.K = c->H; b.N = nl * 2 * c->kvdim; b.nseg = 2 * nl;
+    for (int j = 0; j < nl; ++j) {
+      b.w_map[2 * j] = c->lmaps_wide[l0 + j].wk;
+      b.w_map[2 * j + 1] = c->lmaps_wide[l0 + j].wv;
+      b.seg_rows[2 * j] = (2 * j + 1) * c->kvdim;
+      b.seg_rows[2 * j + 1] = (2 * j + 2) * c->kvdim;
+    }
+    b.y = static_cast<char*>(kv) + (size_t)l0 * 2 * c->kvdim * c->esz;
+    b.ldy = ldkv;
+    b.err = c->tc_err;
+    if (!tc_encode_map(&b.x_map, cn, c->H, rows, (uint64_t)c->H * 2, 64, 128))
+      return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the normed context rows");
+    CK(c->err, launch_tc_wide(b, c->num_sms, st));
+  }
+  for (int l = 0; l < L; ++l) {
+    const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
+    CK(c->err, launch_kv_to_ring(dt, static_cast<char*>(kv) + (size_t)l * 2 * c->kvdim * c->esz, ldkv,
+                                 rows, c->nkv, c->hd, LW(c, l, kKNorm), c->cfg.rms_eps, rope,
+                                 c->cfg.rope_neox, static_cast<char*>(c->ring->k) + lay,
+                                 static_cast<char*>(c->ring->v) + lay, c->ring->cap,
+                                 c->ring->append_only, c->ring->st, 0, pos_host, st));
+  }
+  return DFLASH_OK;
+}
+
 int layer_forward(dflash_ctx* c, int l, int rows) {
   const int dt = c->dt;
   cudaStream_t st = c->stream;
@@ -503,6 +551,14 @@ int setup_tensor_core_path(dflash_ctx* c) {
          wmap(&m.wg, LW(c, l, kWg), c->I, H) && wmap(&m.wu, LW(c, l, kWu), c->I, H) &&
          wmap(&m.wd, LW(c, l, kWd), H, c->I);
   }
+  auto wide = [&](CUtensorMap* m, const void* w, uint64_t rows, uint64_t inner) {
+    return tc_encode_map(m, w, inner, rows, inner * 2, 64, 256);
+  };
+  ok = ok && wide(&c->fcw_map, c->fc, H, c->kin);
+  c->lmaps_wide.resize(g.n_layers);
+  for (int l = 0; l < g.n_layers && ok; ++l)
+    ok = wide(&c->lmaps_wide[l].wk, LW(c, l, kWk), c->kvdim, H) &&
+         wide(&c->lmaps_wide[l].wv, LW(c, l, kWv), c->kvdim, H);
   for (int b = 0; b < 2 && ok; ++b) {
     const uint32_t bn = b ? 32 : 16;
     const uint64_t R = c->R;
@@ -618,7 +674,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * c->half * sizeof(float2), attn_floats * sizeof(float),
       R * c->H * E, R * c->H * E, R * 2 * c->kvdim * E, R * c->half * sizeof(float2),
       (size_t)c->ing_rows * c->H * E, (size_t)c->ing_rows * c->H * E,
-      (size_t)c->ing_rows * 2 * c->kvdim * E, (size_t)c->ing_rows * c->half * sizeof(float2),
+      (size_t)c->ing_rows * 2 * c->kvdim * E * cfg->n_layers, (size_t)c->ing_rows * c->half * sizeof(float2),
       (size_t)c->lm_grid * R * 4, (size_t)c->lm_grid * R * 4, R * c->vf_chunks * 4,
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
@@ -710,10 +766,14 @@ int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_
     return fail(c->err, DFLASH_EFULL, "%lld context rows exceed max_context %lld", kept, c->ring->cap);
   CK(c->err, launch_ring_reset(c->ring->st, kept_first, c->stream));
   const char* src = static_cast<const char*>(resid) + (size_t)(kept_first - first_pos) * c->kin * c->esz;
+  const bool wide = c->use_tc && c->H % 256 == 0 && c->kvdim % 256 == 0;
   for (long long s = 0; s < kept; s += c->ing_rows) {
     const int n = static_cast<int>(kept - s < c->ing_rows ? kept - s : c->ing_rows);
-    int rc = context_rows_to_ring(c, src + (size_t)s * c->kin * c->esz, n, c->ing_f, c->ing_c,
-                                  c->ing_kv, c->ing_rope, 0, kept_first + s);
+    const void* rows_ptr = src + (size_t)s * c->kin * c->esz;
+    int rc = (wide && n > 32)
+                 ? context_rows_wide(c, rows_ptr, n, c->ing_f, c->ing_c, c->ing_kv, c->ing_rope, kept_first + s)
+                 : context_rows_to_ring(c, rows_ptr, n, c->ing_f, c->ing_c, c->ing_kv, c->ing_rope, 0,
+                                        kept_first + s);
     if (rc) return rc;
   }
   CK(c->err, launch_ring_advance(c->ring->st, static_cast<int>(kept), 2, c->stream));
@@ -865,7 +925,15 @@ int dflash_linear(dflash_ctx* c, const void* x, int32_t M, int32_t K, const void
   if (M < 1 || K < 8 || N < 1 || K % 8) return fail(c->err, DFLASH_EINVAL, "bad linear shape");
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (w2 && !aligned16(w2)) || (r && !aligned16(r)))
     return fail(c->err, DFLASH_EINVAL, "linear operands must be 16-byte aligned");
-  if (c->use_tc && M <= 32 && K % 64 == 0) {
+  if (c->use_tc && M > 32 && K % 64 == 0 && N % 256 == 0 && epi == kEpiStore) {
+    TcWideArgs a{};
+    a.M = M; a.N = N; a.K = K; a.nseg = 1; a.seg_rows[0] = N;
+    a.y = y; a.ldy = N; a.err = c->tc_err;
+    if (!tc_encode_map(&a.x_map, x, K, M, (uint64_t)K * 2, 64, 128) ||
+        !tc_encode_map(&a.w_map[0], w, K, N, (uint64_t)K * 2, 64, 256))
+      return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
+    CK(c->err, launch_tc_wide(a, c->num_sms, c->stream));
+  } else if (c->use_tc && M <= 32 && K % 64 == 0) {
     TcGemmArgs t = tc_args(c, M, N, K, epi);
     CUtensorMap wa, wb;
     bool ok = tc_encode_map(&wa, w, K, N, (uint64_t)K * 2, 64, 128) &&
@@ -879,7 +947,8 @@ int dflash_linear(dflash_ctx* c, const void* x, int32_t M, int32_t K, const void
   } else {
     LinearArgs a = lin_args(x, K, y, N, M, N, K);
     a.w[0] = w; a.w2 = w2; a.r = r; a.ldr = N; a.epi = epi;
-    CK(c->err, launch_linear_rows(c->dt, a, c->stream));
+    CK(c->err, (M > 32 && epi == kEpiStore) ? launch_linear_tiled(c->dt, a, c->stream)
+                                            : launch_linear_rows(c->dt, a, c->stream));
   }
   return DFLASH_OK;
 }

@@ -68,6 +68,20 @@ struct TcGemmArgs {
   int nkv, neox, append_only;
   float eps;
 };
+// Many-row tensor-core GEMM (context ingest): Y[m, n] = rnd(X W^T), X [M, K]
+// (box {64, 128}), W stacked segments of rows (box {64, 256}; segment row
+// counts multiples of 256), bf16 out with row stride ldy.
+struct TcWideArgs {
+  CUtensorMap x_map;
+  CUtensorMap w_map[kTcMaxSeg];
+  int seg_rows[kTcMaxSeg];         // cumulative row ends of the segments
+  int nseg;
+  int M, N, K;
+  void* y; int ldy;
+  int* err;
+};
+cudaError_t launch_tc_wide(const TcWideArgs& a, int grid, cudaStream_t st);
+
 bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 cudaError_t init_tc_attrs();

@@ -436,6 +436,138 @@ cudaError_t attr_tc() {
                               (int)Cfg<BN, NV, S>::kSmem);
 }
 
+// ---------------------------------------------------------------------------
+// Many-row GEMM (context ingest): Y[m, n] = rnd(sum_k X[m, k] W[n, k]) with
+// X the A operand (128-row tiles) and W the B operand (256-row tiles), one
+// 128 x 256 x 16 MMA per K step, fp32 accumulators in TMEM (two 256-column
+// buffers = the whole TMEM), full K per tile, persistent CTAs striding over
+// the (m-tile, n-tile) grid. Same warp roles as above.
+// ---------------------------------------------------------------------------
+constexpr int kWideN = 256;
+constexpr int kWideStages = 4;
+constexpr int kWideStage = kABytes + kWideN * 128;          // 48 KB
+constexpr size_t kWideSmem = (size_t)kWideStages * kWideStage + 1024 + 512;
+
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_wide_kernel(const __grid_constant__ TcWideArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kWideStages * kWideStage);
+  uint64_t* empty = full + kWideStages;
+  uint64_t* acc_full = empty + kWideStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (a.M + 127) / 128, nt = (a.N + kWideN - 1) / kWideN;
+  const int T = mt * nt, KC = a.K / 64;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWideStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&acc_full[s], 1); mbar_init(&acc_empty[s], 128); }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      pdl_wait();
+      bool ok = true;
+      long long i = 0;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        const int m0 = (t % mt) * 128, n0 = (t / mt) * kWideN;
+        int s = 0;
+        while (s < a.nseg - 1 && n0 >= a.seg_rows[s]) ++s;
+        const int nrow0 = n0 - (s ? a.seg_rows[s - 1] : 0);
+        for (int c = 0; c < KC && ok; ++c, ++i) {
+          const int st = static_cast<int>(i % kWideStages);
+          if (i >= kWideStages) ok = mbar_wait(&empty[st], static_cast<unsigned>((i / kWideStages - 1) & 1));
+          if (!ok) break;
+          uint8_t* sa = smem + (size_t)st * kWideStage;
+          mbar_expect_tx(&full[st], kWideStage);
+          tma_load_2d(sa, &a.x_map, c * 64, m0, &full[st]);
+          tma_load_2d(sa + kABytes, &a.w_map[s], c * 64, nrow0, &full[st]);
+        }
+      }
+      if (!ok) atomicOr(a.err, 8);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, kWideN);
+      bool ok = true;
+      long long i = 0;
+      int seg = 0;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x, ++seg) {
+        const int buf = seg & 1;
+        if (seg >= 2) ok = mbar_wait(&acc_empty[buf], static_cast<unsigned>((seg / 2 - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kWideN;
+        for (int c = 0; c < KC; ++c, ++i) {
+          const int st = static_cast<int>(i % kWideStages);
+          ok = mbar_wait(&full[st], static_cast<unsigned>((i / kWideStages) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)st * kWideStage);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sa + kABytes + kk * 32), idesc,
+                        (c > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);
+        }
+        tc_commit(&acc_full[buf]);
+      }
+      if (!ok) atomicOr(a.err, 16);
+    }
+  } else {
+    pdl_wait();
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    bool ok = true;
+    int seg = 0;
+    bf16* Y = reinterpret_cast<bf16*>(a.y);
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x, ++seg) {
+      const int m0 = (t % mt) * 128, n0 = (t / mt) * kWideN;
+      const int buf = seg & 1;
+      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const int m = m0 + row;
+      for (int j = 0; j < kWideN / 16; ++j) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kWideN + j * 16, v);
+        tmem_ld_wait();
+        const int n = n0 + j * 16;
+        if (m < a.M && n < a.N) {
+          uint4 pk[2];
+          uint32_t* w32 = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w32[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(Y + (size_t)m * a.ldy + n);
+          dst[0] = pk[0];
+          dst[1] = pk[1];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+    }
+    if (!ok) atomicOr(a.err, 32);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -471,7 +603,25 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
   if ((e = attr_tc<16, kEpiKVRing>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiKVRing>()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kWideSmem)) != cudaSuccess) return e;
   return attr_tc<32, kEpiArgmax>();
+}
+
+cudaError_t launch_tc_wide(const TcWideArgs& a, int grid, cudaStream_t st) {
+  const int T = ((a.M + 127) / 128) * ((a.N + kWideN - 1) / kWideN);
+  if (grid > T) grid = T;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kWideSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_wide_kernel, a);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st) {

@@ -249,7 +249,9 @@ int dflash_markov_chain(dflash_ctx* ctx, int32_t anchor, int32_t gamma,
  * (epi 1, r may alias y), or rnd(silu(rnd(x.w^T)) * rnd(x.w2^T)) (epi 2,
  * the SwiGLU of Qwen-shaped MLPs [Head "Why"]); x [M, K], w and w2 [N, K],
  * r and y [M, N], all dense in the config dtype, accumulation fp32. bf16
- * with M <= 32 and K % 64 == 0 runs on the tensor cores. */
+ * with K % 64 == 0 runs on the tensor cores: M <= 32 as a weight-streaming
+ * GEMM, M > 32 (epi 0, N % 256 == 0) as the many-row GEMM of the context
+ * ingest. */
 int dflash_linear(dflash_ctx* ctx, const void* x, int32_t M, int32_t K,
                   const void* w, const void* w2, int32_t N, const void* r,
                   void* y, int32_t epi);

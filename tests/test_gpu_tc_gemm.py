@@ -66,6 +66,23 @@ def test_linear_matches_torch(B, M, N, K, epi):
     ctx.close()
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 10240), (300, 2048, 2048), (128, 256, 64),
+                                   (2048, 10240, 2048), (33, 512, 4096)])
+def test_many_row_linear_matches_torch(B, M, N, K):
+    """The context-ingest GEMM (128 x 256 x 16 tensor-core tiles)."""
+    ctx, _ = _ctx(B, 4096)
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    y = torch.full((M, N), 7.0, device="cuda", dtype=torch.bfloat16)
+    ctx.linear(x, M, K, w, N, y, epi=0)
+    ctx.sync()
+    ref = (x.float() @ w.float().T).to(torch.bfloat16)
+    _close(y, ref, f"many-row linear M={M} N={N} K={K}")
+    assert ctx.state()["error"] == 0
+    ctx.close()
+
+
 def test_linear_residual_in_place(B):
     ctx, _ = _ctx(B, 4096)
     M, N, K = 16, 2048, 4096
