@@ -438,11 +438,15 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st));
   const bool tc = c->use_tc && rows <= 32;
   const int bi = bn_index(rows);
+  const bool fused_qk = tc && c->hd == 128;
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, kEpiStore);
+    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, fused_qk ? kEpiQKV : kEpiStore);
     tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
     t.b_map = c->xn_map[bi];
     t.y = c->qkv; t.ldy = c->qkv_n;
+    t.nq_tiles = c->nq; t.nkv = c->nkv;
+    t.qn = LW(c, l, kQNorm); t.kn = LW(c, l, kKNorm);
+    t.rope = c->rope; t.neox = c->cfg.rope_neox; t.eps = eps;
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
@@ -452,11 +456,13 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
     CK(c->err, launch_linear_rows(dt, q, st));
   }
-  CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
-                                   c->rope, c->cfg.rope_neox, st));
-  CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
-                                   c->qkv_n, rows, c->nkv, c->hd, LW(c, l, kKNorm), eps, c->rope,
-                                   c->cfg.rope_neox, st));
+  if (!fused_qk) {
+    CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
+                                     c->rope, c->cfg.rope_neox, st));
+    CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
+                                     c->qkv_n, rows, c->nkv, c->hd, LW(c, l, kKNorm), eps, c->rope,
+                                     c->cfg.rope_neox, st));
+  }
   AttnArgs at{};
   at.q = c->qkv; at.ldq = c->qkv_n;
   at.kb = static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz;

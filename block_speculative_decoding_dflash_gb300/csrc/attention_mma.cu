@@ -28,11 +28,12 @@ constexpr int kRowB = (kHd + kPad) * 2;    // 272-byte rows: conflict-free ldmat
 // Per-query partial: o[hd], max, sum, 2 floats of padding (528 bytes, a
 // multiple of 16, so the merge can read o with float4 loads).
 constexpr int kPartStride = kHd + 4;
+constexpr int kQChunk = 64;
 
 struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
   bf16 v[kKeys][kHd + kPad];
-  bf16 q[16][kHd + kPad];
+  bf16 q[kQChunk][kHd + kPad];            // up to 64 query rows, loaded with K/V
   float o[kWarps][16][kHd];                // per-warp unnormalised P V
   float m[kWarps][16];
   float l[kWarps][16];
@@ -96,6 +97,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   const bf16* vb = reinterpret_cast<const bf16*>(a.vb);
   const bf16* qg = reinterpret_cast<const bf16*>(a.q);
 
+  auto load_q = [&](int q0) {
+    for (int e = threadIdx.x; e < kQChunk * (kHd / 8); e += blockDim.x) {
+      const int r = e >> 4, ch = e & 15;
+      const int qi = q0 + r;
+      const bool valid = qi < Qn;
+      const bf16* src = qg;
+      if (valid) src = qg + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
+      cp_async16(&S.q[r][ch * 8], src, valid);
+    }
+  };
   if (j0 < nk) {
     // K and V tiles: 128 keys x 16 chunks of 16 bytes each.
     for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
@@ -117,24 +128,19 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       cp_async16(&S.v[j][ch * 8], vs, valid);
     }
   }
+  load_q(0);
   cp_async_wait_all();
   __syncthreads();
 
   const int grp = lane >> 2, tig = lane & 3;
   const float scale = rsqrtf(static_cast<float>(kHd));
   for (int qt = 0; qt * 16 < Qn; ++qt) {
-    // this tile's 16 queries
-    for (int e = threadIdx.x; e < 16 * (kHd / 8); e += blockDim.x) {
-      const int r = e >> 4, ch = e & 15;
-      const int qi = qt * 16 + r;
-      const bool valid = qi < Qn;
-      const bf16* src = qg;
-      if (valid) src = qg + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
-      cp_async16(&S.q[r][ch * 8], src, valid);
+    const int qr = (qt * 16) % kQChunk;           // row of this tile in the Q chunk
+    if (qt > 0 && qr == 0) {                      // next chunk of 64 queries
+      load_q(qt * 16);
+      cp_async_wait_all();
+      __syncthreads();
     }
-    cp_async_wait_all();
-    __syncthreads();
-
     float m_row[2] = {-INFINITY, -INFINITY}, l_row[2] = {0.f, 0.f};
     float o[16][4];
 #pragma unroll
@@ -147,7 +153,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       for (int ks = 0; ks < kHd / 16; ++ks) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         const int mi = lane >> 3;
-        ldsm_x4(&S.q[(lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
+        ldsm_x4(&S.q[qr + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
         ldsm_x4(&S.k[warp * 16 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
         mma16816(sc[0], a0, a1, a2, a3, b0, b1);
         mma16816(sc[1], a0, a1, a2, a3, b2, b3);

@@ -34,6 +34,7 @@ struct LinearArgs {
 enum : int {
   kEpiArgmax = 3,   // tensor-core GEMM only: softcap + per-row argmax
   kEpiKVRing = 4,   // tensor-core GEMM only: K head-norm + RoPE / V, into ring slots
+  kEpiQKV = 5,      // tensor-core GEMM only: q/k head-norm + RoPE, v plain, stored
 };
 constexpr int kTcMaxSeg = 10;
 
@@ -67,6 +68,9 @@ struct TcGemmArgs {
   const void* const* kgain;        // [L] k_norm gains, device array of pointers
   int nkv, neox, append_only;
   float eps;
+  // kEpiQKV: rows [Q heads | K heads | V heads], q_norm / k_norm gains [128]
+  int nq_tiles;
+  const void* qn; const void* kn;
 };
 // Many-row tensor-core GEMM (context ingest): Y[m, n] = rnd(X W^T), X [M, K]
 // (box {64, 128}), W stacked segments of rows (box {64, 256}; segment row

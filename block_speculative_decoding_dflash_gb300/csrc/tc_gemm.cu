@@ -41,6 +41,55 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(128) : "memory");
 }
 
+// Per-head RMSNorm over a 128-row tile (head_dim 128: one dim per epilogue
+// thread) followed by RoPE, for every block row m < M of the tile's BN
+// columns; the value is normalised in fp32 and rotated before the single
+// rounding the caller applies. All 128 epilogue threads must call it.
+template <int BN>
+__device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const float2* rope, int M,
+                                                    int neox, float eps, int row, int lane, int q,
+                                                    float (*ss_sm)[BN], float* x_sm) {
+#pragma unroll
+  for (int m = 0; m < BN; ++m) {
+    const float ss = warp_sum(val[m] * val[m]);
+    if (lane == 0) ss_sm[q][m] = ss;
+  }
+  epi_sync();
+#pragma unroll
+  for (int m = 0; m < BN; ++m) {
+    const float ss = ss_sm[0][m] + ss_sm[1][m] + ss_sm[2][m] + ss_sm[3][m];
+    val[m] = val[m] * rsqrtf(ss / 128.0f + eps) * g;
+  }
+  if (neox) {
+#pragma unroll
+    for (int m = 0; m < BN; ++m) x_sm[row * BN + m] = val[m];
+    epi_sync();
+    const int i = row & 63;
+    const bool lo = row < 64;
+    const int partner = lo ? row + 64 : row - 64;
+#pragma unroll
+    for (int m = 0; m < BN; ++m) {
+      if (m < M) {
+        const float2 cs = rope[m * 64 + i];
+        const float other = x_sm[partner * BN + m];
+        val[m] = lo ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
+      }
+    }
+    epi_sync();
+  } else {
+    const int i = row >> 1;
+    const bool ev = (row & 1) == 0;
+#pragma unroll
+    for (int m = 0; m < BN; ++m) {
+      const float other = __shfl_xor_sync(0xffffffffu, val[m], 1);
+      if (m < M) {
+        const float2 cs = rope[m * 64 + i];
+        val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
+      }
+    }
+  }
+}
+
 constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
 
 template <int BN, int NV, int STAGES>
@@ -74,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   __shared__ int red_i[4][BN];
   __shared__ int s_last;
   __shared__ float kv_ss[4][BN];
-  __shared__ float kv_x[(EPI == kEpiKVRing) ? 128 * BN : 1];
+  __shared__ float kv_x[(EPI == kEpiKVRing || EPI == kEpiQKV) ? 128 * BN : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
@@ -281,6 +330,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           best_i[m] = bi;
         }
         epi_sync();
+      } else if (EPI == kEpiQKV) {
+        // tiles: query heads, then key heads, then value heads (hd 128 each)
+        float val[BN];
+#pragma unroll
+        for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
+        const bool isq = t < a.nq_tiles;
+        const bool isk = !isq && t < a.nq_tiles + a.nkv;
+        if (isq || isk) {
+          const float g = __bfloat162float(reinterpret_cast<const bf16*>(isq ? a.qn : a.kn)[row]);
+          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x);
+        }
+        bf16* Y = reinterpret_cast<bf16*>(a.y);
+#pragma unroll
+        for (int m = 0; m < BN; ++m)
+          if (m < a.M && valid) Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(val[m]);
       } else if (EPI == kEpiKVRing) {
         // tile t = kv head h of layer l, K or V (hd = 128 = one tile)
         const int seg = t / a.nkv, h = t % a.nkv;
@@ -293,47 +357,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 #pragma unroll
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
         if (!isv) {
-          // per-head RMSNorm over the 128 rows of the tile (one per thread)
-#pragma unroll
-          for (int m = 0; m < BN; ++m) {
-            const float ss = warp_sum(val[m] * val[m]);
-            if (lane == 0) kv_ss[q][m] = ss;
-          }
-          epi_sync();
           const float g = __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[layer])[row]);
-#pragma unroll
-          for (int m = 0; m < BN; ++m) {
-            const float ss = kv_ss[0][m] + kv_ss[1][m] + kv_ss[2][m] + kv_ss[3][m];
-            val[m] = val[m] * rsqrtf(ss / 128.0f + a.eps) * g;
-          }
-          // RoPE on the normed values: pair (i, i + 64) or (2i, 2i + 1)
-          if (a.neox) {
-#pragma unroll
-            for (int m = 0; m < BN; ++m) kv_x[row * BN + m] = val[m];
-            epi_sync();
-            const int i = row & 63;
-            const bool lo = row < 64;
-            const int partner = lo ? row + 64 : row - 64;
-#pragma unroll
-            for (int m = 0; m < BN; ++m) {
-              if (m >= a.M) break;
-              const float2 cs = a.rope[m * 64 + i];
-              const float other = kv_x[partner * BN + m];
-              val[m] = lo ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
-            }
-            epi_sync();
-          } else {
-            const int i = row >> 1;
-            const bool ev = (row & 1) == 0;
-#pragma unroll
-            for (int m = 0; m < BN; ++m) {
-              const float other = __shfl_xor_sync(0xffffffffu, val[m], 1);
-              if (m < a.M) {
-                const float2 cs = a.rope[m * 64 + i];
-                val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
-              }
-            }
-          }
+          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x);
         }
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
@@ -409,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 // shared memory each) so the next GEMM's CTAs fit beside the running one and
 // stream their first weight tiles early. The lm_head is long: a deep ring.
 template <int BN, int EPI>
-constexpr int stages_for() { return EPI == kEpiArgmax ? 8 : EPI == kEpiSwiglu ? 3 : 4; }
+constexpr int stages_for() { return EPI == kEpiArgmax ? 12 : EPI == kEpiSwiglu ? 3 : 4; }
 
 template <int BN, int EPI>
 cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
@@ -602,6 +627,8 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiResid>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
   if ((e = attr_tc<16, kEpiKVRing>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiQKV>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiQKV>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiKVRing>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
@@ -639,6 +666,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
       case kEpiResid: return launch_tc<16, kEpiResid>(a, grid, pdl, st);
       case kEpiSwiglu: return launch_tc<16, kEpiSwiglu>(a, grid, pdl, st);
       case kEpiKVRing: return launch_tc<16, kEpiKVRing>(a, grid, pdl, st);
+      case kEpiQKV: return launch_tc<16, kEpiQKV>(a, grid, pdl, st);
       default: return launch_tc<16, kEpiArgmax>(a, grid, pdl, st);
     }
   }
@@ -647,6 +675,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
     case kEpiResid: return launch_tc<32, kEpiResid>(a, grid, pdl, st);
     case kEpiSwiglu: return launch_tc<32, kEpiSwiglu>(a, grid, pdl, st);
     case kEpiKVRing: return launch_tc<32, kEpiKVRing>(a, grid, pdl, st);
+    case kEpiQKV: return launch_tc<32, kEpiQKV>(a, grid, pdl, st);
     default: return launch_tc<32, kEpiArgmax>(a, grid, pdl, st);
   }
 }
