@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 // shared memory each) so the next GEMM's CTAs fit beside the running one and
 // stream their first weight tiles early. The lm_head is long: a deep ring.
 template <int BN, int EPI>
-constexpr int stages_for() { return EPI == kEpiArgmax ? 12 : EPI == kEpiSwiglu ? 3 : 4; }
+constexpr int stages_for() { return EPI == kEpiArgmax ? (BN == 16 ? 12 : 10) : EPI == kEpiSwiglu ? 3 : 4; }
 
 template <int BN, int EPI>
 cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
