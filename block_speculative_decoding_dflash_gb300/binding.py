@@ -63,6 +63,7 @@ class RoundStateC(ctypes.Structure):
 
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE = 1, 2
 
 
 def _sig(name, res, *args):
@@ -102,6 +103,8 @@ _sig("dflash_capture_end", ctypes.c_int, _vp, _i32)
 _sig("dflash_graph_launch", ctypes.c_int, _vp, _i32)
 _sig("dflash_sync", ctypes.c_int, _vp)
 _sig("dflash_graph_kernel_count", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
+_sig("dflash_set_option", ctypes.c_int, _vp, _i32, _i64)
+_sig("dflash_get_option", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
 _sig("dflash_lm_head_elapsed_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float))
 _sig("dflash_synth_target", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -379,6 +382,16 @@ class DFlashContext:
         o = _i64()
         self._check(lib.dflash_graph_kernel_count(self.h, slot, ctypes.byref(o)))
         return o.value
+
+    def set_fused_draft(self, enable: bool):
+        """Draft with the persistent single-launch kernel where the config
+        allows it (the default), or with one kernel per operation."""
+        self._check(lib.dflash_set_option(self.h, OPT_FUSED_DRAFT, 1 if enable else 0))
+
+    def fused_draft_available(self) -> bool:
+        o = _i64()
+        self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT_AVAILABLE, ctypes.byref(o)))
+        return bool(o.value)
 
     def lm_head_timing(self, enable: bool):
         self._check(lib.dflash_lm_head_timing(self.h, 1 if enable else 0))

@@ -152,6 +152,7 @@ struct dflash_ctx {
   void *x = nullptr, *xn = nullptr, *qkv = nullptr, *attn = nullptr, *sbuf = nullptr, *xf = nullptr;
   float2* rope = nullptr;
   float* attn_part = nullptr;
+  size_t attn_part_floats = 0;
   void *app_f = nullptr, *app_c = nullptr, *app_kv = nullptr;
   float2* app_rope = nullptr;
   void *ing_f = nullptr, *ing_c = nullptr, *ing_kv = nullptr;
@@ -198,6 +199,15 @@ struct dflash_ctx {
   unsigned* tc_done = nullptr;
   unsigned* attn_ctr = nullptr;
   const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
+  // persistent draft kernel (bf16, head_dim 128, up to 16 block rows)
+  bool draft_fused_ok = false;                 // the config and device allow it
+  bool draft_fused_on = true;                  // DFLASH_OPT_FUSED_DRAFT
+  MegaPhase* mega_phases = nullptr;            // device phase list
+  int mega_nphase = 0;
+  CUtensorMap* mega_maps = nullptr;            // device tensor-map table
+  unsigned* mega_done = nullptr;               // [nphase] counters + abort flag
+  int mega_grid = 0;
+  int mega_nsplit = 0;
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -533,6 +543,104 @@ int ensure_room(dflash_ctx* c, int rows) {
   return DFLASH_OK;
 }
 
+// Phase list and tensor-map table of the persistent draft kernel, when the
+// config fits it: head_dim 128, hidden <= 2048 (the normalised operand lives
+// in shared memory), block <= 16 rows with at most 64 queries per kv head,
+// and every CTA resident at once (one per SM).
+int setup_draft_kernel(dflash_ctx* c) {
+  const dflash_config& g = c->cfg;
+  const int G = c->nq / c->nkv;
+  if (c->hd != 128 || c->H > 2048 || c->H % 256 || c->nq % c->nkv || 16 * G > 64) return DFLASH_OK;
+  int dev = 0, sms = 0;
+  CK(c->err, cudaGetDevice(&dev));
+  CK(c->err, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (sms > kTcGrid) return DFLASH_OK;
+  CK(c->err, init_draft_kernel_attrs());
+  if (draft_kernel_blocks_per_sm() < 1) return DFLASH_OK;
+  const int nsplit = (c->max_ctx + 16 + 127) / 128;
+  if ((size_t)c->nkv * nsplit * 16 * G * (128 + 4) > c->attn_part_floats) return DFLASH_OK;
+
+  // map table: per layer wq wk wv wo wg wu wd, then lm_head, attn rows, SwiGLU rows
+  std::vector<CUtensorMap> maps;
+  for (int l = 0; l < g.n_layers; ++l) {
+    const auto& m = c->lmaps[l];
+    for (const CUtensorMap* t : {&m.wq, &m.wk, &m.wv, &m.wo, &m.wg, &m.wu, &m.wd}) maps.push_back(*t);
+  }
+  const int lm_idx = (int)maps.size();
+  maps.push_back(c->lm_map);
+  const int attn_idx = (int)maps.size();
+  maps.push_back(c->attn_map[0]);
+  const int sbuf_idx = (int)maps.size();
+  maps.push_back(c->sbuf_map[0]);
+
+  auto gemm = [&](int epi, int norm, int N, int K) {
+    MegaPhase p{};
+    p.kind = kPhGemm; p.epi = epi; p.norm = norm;
+    p.N = N; p.K = K; p.tiles = (N + 127) / 128; p.kchunks = K / 64;
+    p.nseg = 1;
+    p.seg_tiles[0] = p.tiles;
+    return p;
+  };
+  std::vector<MegaPhase> ph;
+  MegaPhase e{};
+  e.kind = kPhEmbed;
+  ph.push_back(e);
+  for (int l = 0; l < g.n_layers; ++l) {
+    const int w0 = l * 7;
+    MegaPhase q = gemm(kEpiQKV, 1, c->qkv_n, c->H);
+    q.nseg = 3;
+    q.a_map[0] = w0 + 0; q.a_map[1] = w0 + 1; q.a_map[2] = w0 + 2;
+    q.seg_tiles[0] = c->qdim / 128;
+    q.seg_tiles[1] = (c->qdim + c->kvdim) / 128;
+    q.seg_tiles[2] = c->qkv_n / 128;
+    q.y = c->qkv; q.ldy = c->qkv_n;
+    q.gain = LW(c, l, kInNorm); q.qn = LW(c, l, kQNorm); q.kn = LW(c, l, kKNorm);
+    q.nq_tiles = c->nq;
+    ph.push_back(q);
+    MegaPhase at{};
+    at.kind = kPhAttn; at.layer = l;
+    ph.push_back(at);
+    MegaPhase cb{};
+    cb.kind = kPhComb; cb.layer = l;
+    ph.push_back(cb);
+    MegaPhase o = gemm(kEpiResid, 0, c->H, c->qdim);
+    o.a_map[0] = w0 + 3; o.b_map = attn_idx;
+    o.y = c->x; o.ldy = c->H;
+    ph.push_back(o);
+    MegaPhase gu = gemm(kEpiSwiglu, 1, c->I, c->H);
+    gu.a_map[0] = w0 + 4; gu.a2_map = w0 + 5;
+    gu.y = c->sbuf; gu.ldy = c->I;
+    gu.gain = LW(c, l, kPostNorm);
+    ph.push_back(gu);
+    MegaPhase d = gemm(kEpiResid, 0, c->H, c->I);
+    d.a_map[0] = w0 + 6; d.b_map = sbuf_idx;
+    d.y = c->x; d.ldy = c->H;
+    ph.push_back(d);
+  }
+  MegaPhase lm = gemm(kEpiArgmax, 1, c->V, c->H);
+  lm.lm = 1; lm.a_map[0] = lm_idx; lm.gain = c->final_norm;
+  ph.push_back(lm);
+
+  CK(c->err, cudaMalloc(&c->mega_maps, maps.size() * sizeof(CUtensorMap)));
+  CK(c->err, cudaMalloc(&c->mega_phases, ph.size() * sizeof(MegaPhase)));
+  CK(c->err, cudaMalloc(&c->mega_done, (ph.size() + 1) * sizeof(unsigned)));
+  CK(c->err, cudaMemcpyAsync(c->mega_maps, maps.data(), maps.size() * sizeof(CUtensorMap),
+                             cudaMemcpyHostToDevice, c->stream));
+  CK(c->err, cudaMemcpyAsync(c->mega_phases, ph.data(), ph.size() * sizeof(MegaPhase),
+                             cudaMemcpyHostToDevice, c->stream));
+  CK(c->err, cudaMemsetAsync(c->mega_done, 0, (ph.size() + 1) * sizeof(unsigned), c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  c->mega_nphase = (int)ph.size();
+  c->mega_grid = sms;
+  c->mega_nsplit = nsplit;
+  c->draft_fused_ok = true;
+  return DFLASH_OK;
+}
+
+bool draft_fused(const dflash_ctx* c, int rows, int lm_rows, bool logits) {
+  return c->draft_fused_ok && c->draft_fused_on && rows <= 16 && lm_rows >= 1 && !logits;
+}
+
 // Tensor maps of every weight and activation operand of the tensor-core path
 // (bf16 configs whose output dimensions are whole 128-row tiles).
 int setup_tensor_core_path(dflash_ctx* c) {
@@ -578,7 +686,7 @@ int setup_tensor_core_path(dflash_ctx* c) {
   if (!ok) return DFLASH_OK;   // no tensor-map encoder: the CUDA-core path serves
   CK(c->err, init_tc_attrs());
   c->use_tc = true;
-  return DFLASH_OK;
+  return setup_draft_kernel(c);
 }
 
 }  // namespace
@@ -617,6 +725,9 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
     if (g) cudaGraphExecDestroy(g);
   ring_free(ctx->ring);
   cudaFree(ctx->arena);
+  cudaFree(ctx->mega_maps);
+  cudaFree(ctx->mega_phases);
+  cudaFree(ctx->mega_done);
   for (auto& ev : ctx->lm_ev)
     if (ev) cudaEventDestroy(ev);
   delete ctx;
@@ -703,6 +814,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->sbuf = carve<char>(cur, sizes[si++]);
   c->xf = carve<char>(cur, sizes[si++]);
   c->rope = carve<float2>(cur, sizes[si++]);
+  c->attn_part_floats = attn_floats;
   c->attn_part = carve<float>(cur, sizes[si++]);
   c->app_f = carve<char>(cur, sizes[si++]);
   c->app_c = carve<char>(cur, sizes[si++]);
@@ -800,6 +912,19 @@ int dflash_set_anchor(dflash_ctx* c, int32_t anchor) {
   return DFLASH_OK;
 }
 
+// DSpark: the rank-r Markov chain proposes the draft from the anchor, adding
+// the backbone's logits when configured.
+cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
+  MarkovArgs mk{};
+  mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
+  mk.rs = c->rs; mk.anchor_host = -1;
+  mk.z = c->cfg.markov_add ? c->zlog : nullptr; mk.ldz = c->V;
+  mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
+  mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2;
+  mk.grid = c->mk_grid;
+  return launch_markov_chain(c->dt, mk, c->stream);
+}
+
 int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   if (!c) return DFLASH_EINVAL;
   if (!draft_ids) return fail(c->err, DFLASH_EINVAL, "draft_ids is NULL");
@@ -812,6 +937,39 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   const int R = block - 1;
   const int dt = c->dt;
   cudaStream_t st = c->stream;
+  const bool markov = c->cfg.markov_rank > 0;
+  const bool want_logits = markov && c->cfg.markov_add;
+  if (draft_fused(c, rows, R, want_logits)) {
+    if (c->lm_timing)
+      CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
+    MegaArgs m{};
+    m.phases = c->mega_phases; m.nphase = c->mega_nphase;
+    m.maps = c->mega_maps;
+    m.M = rows; m.Mlm = R; m.read0 = read0;
+    m.H = c->H; m.V = c->V; m.nq = c->nq; m.nkv = c->nkv; m.qkv_n = c->qkv_n; m.half = c->half;
+    m.embed = c->embed; m.rs = c->rs; m.mask_id = c->cfg.mask_token_id;
+    m.inv_freq = c->inv_freq; m.rope = c->rope;
+    m.x = c->x; m.qkv = c->qkv; m.attn = c->attn; m.xf = c->xf;
+    m.ring = c->ring->st; m.ring_k = c->ring->k; m.ring_v = c->ring->v; m.cap = c->ring->cap;
+    m.window = c->cfg.window;
+    m.attn_part = c->attn_part; m.nsplit = c->mega_nsplit;
+    m.partials = c->tc_part; m.tile_ctr = c->tc_tiles; m.err = c->tc_err;
+    m.done = c->mega_done; m.abort_flag = c->mega_done + c->mega_nphase;
+    m.softcap = c->cfg.softcap;
+    m.ids = markov ? c->backbone_ids : draft_ids;
+    m.ids2 = markov ? nullptr : c->backbone_ids;
+    m.maxv = c->maxv;
+    m.part_v = c->tc_lm_pv; m.part_i = c->tc_lm_pi;
+    m.eps = c->cfg.rms_eps; m.neox = c->cfg.rope_neox;
+    CK(c->err, launch_draft_kernel(m, c->mega_grid, st));
+    if (c->lm_timing) {
+      CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
+      c->lm_recorded = true;
+    }
+    if (markov) CK(c->err, draft_markov(c, R, draft_ids));
+    c->last_draft_block = block;
+    return DFLASH_OK;
+  }
   CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rows, c->x,
                                 c->ring->st, c->inv_freq, c->half, rows, c->rope, st));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
@@ -820,7 +978,6 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   }
   CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
                             c->cfg.rms_eps, st));
-  const bool markov = c->cfg.markov_rank > 0;
   LmHeadArgs lm{};
   lm.x = static_cast<char*>(c->xf) + (size_t)read0 * c->H * c->esz;
   lm.ldx = c->H;
@@ -850,16 +1007,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
     c->lm_recorded = true;
   }
-  if (markov) {
-    MarkovArgs mk{};
-    mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
-    mk.rs = c->rs; mk.anchor_host = -1;
-    mk.z = c->cfg.markov_add ? c->zlog : nullptr; mk.ldz = c->V;
-    mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
-    mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2;
-    mk.grid = c->mk_grid;
-    CK(c->err, launch_markov_chain(dt, mk, st));
-  }
+  if (markov) CK(c->err, draft_markov(c, R, draft_ids));
   c->last_draft_block = block;
   return DFLASH_OK;
 }
@@ -1125,6 +1273,24 @@ int dflash_graph_kernel_count(dflash_ctx* c, int32_t slot, int64_t* out) {
   if (slot < 0 || slot >= 64 || !c->graphs[slot]) return fail(c->err, DFLASH_ESTATE, "graph slot %d is empty", slot);
   *out = c->graph_kernels[slot];
   return DFLASH_OK;
+}
+
+int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
+  if (!c) return DFLASH_EINVAL;
+  if (option == DFLASH_OPT_FUSED_DRAFT) {
+    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
+    c->draft_fused_on = value != 0;
+    return DFLASH_OK;
+  }
+  return fail(c->err, DFLASH_EINVAL, "unknown or read-only option %d", option);
+}
+
+int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
+  if (!c) return DFLASH_EINVAL;
+  if (!value) return fail(c->err, DFLASH_EINVAL, "value is NULL");
+  if (option == DFLASH_OPT_FUSED_DRAFT) { *value = c->draft_fused_on ? 1 : 0; return DFLASH_OK; }
+  if (option == DFLASH_OPT_FUSED_DRAFT_AVAILABLE) { *value = c->draft_fused_ok ? 1 : 0; return DFLASH_OK; }
+  return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 
 int dflash_lm_head_timing(dflash_ctx* c, int32_t enable) {

@@ -14,6 +14,7 @@
 // context keys [kstart, p) followed by the block's own rows.
 #include <math.h>
 
+#include "attn_common.cuh"
 #include "kernels.h"
 #include "mma_sync.cuh"
 #include "launch.cuh"
@@ -21,14 +22,12 @@
 namespace dfl {
 namespace {
 
-constexpr int kHd = 128;
-constexpr int kKeys = 128;
+constexpr int kHd = kAttnHd;
+constexpr int kKeys = kAttnKeys;
 constexpr int kWarps = 8;
 constexpr int kPad = 8;                    // bf16 elements of row padding
 constexpr int kRowB = (kHd + kPad) * 2;    // 272-byte rows: conflict-free ldmatrix
-// Per-query partial: o[hd], max, sum, 2 floats of padding (528 bytes, a
-// multiple of 16, so the merge can read o with float4 loads).
-constexpr int kPartStride = kHd + 4;
+constexpr int kPartStride = kAttnPartStride;
 constexpr int kQChunk = 64;
 
 struct MmaSmem {
@@ -227,52 +226,8 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
   const int Qn = a.rows * G;
   const int item = blockIdx.x * 4 + warp;
   if (item >= a.nkv * Qn) return;
-  const int g = item / Qn, qi = item % Qn;
-  const size_t pstride = kPartStride;
-  const float* base = a.partial + (size_t)g * nsplit * Qn * pstride + (size_t)qi * pstride;
-  const size_t sstride = (size_t)Qn * pstride;
-  // split maxima and sums, 32 splits per load round
-  float M = -INFINITY;
-  for (int sp = lane; sp < nsplit; sp += 32) M = fmaxf(M, __ldcg(base + sp * sstride + kHd));
-  M = warp_max(M);
-  float L = 0.f;
-  for (int sp = lane; sp < nsplit; sp += 32) {
-    const float ms = __ldcg(base + sp * sstride + kHd);
-    if (ms != -INFINITY) L += expf(ms - M) * __ldcg(base + sp * sstride + kHd + 1);
-  }
-  L = warp_sum(L);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const int d4 = lane * 4;
-  for (int s0 = 0; s0 < nsplit; s0 += 32) {
-    const int sp_l = s0 + lane;
-    const float ms_l = sp_l < nsplit ? __ldcg(base + sp_l * sstride + kHd) : -INFINITY;
-    const float f_l = ms_l == -INFINITY ? 0.f : expf(ms_l - M);
-    const int n = nsplit - s0 < 32 ? nsplit - s0 : 32;
-    int j = 0;
-    for (; j + 8 <= n; j += 8) {
-      float4 ov[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        ov[u] = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j + u) * sstride + d4));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float f = __shfl_sync(0xffffffffu, f_l, j + u);
-        acc[0] += f * ov[u].x; acc[1] += f * ov[u].y; acc[2] += f * ov[u].z; acc[3] += f * ov[u].w;
-      }
-    }
-    for (; j < n; ++j) {
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + d4));
-      const float f = __shfl_sync(0xffffffffu, f_l, j);
-      acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
-    }
-  }
-  const float inv = 1.0f / L;
-  bf16* dst = reinterpret_cast<bf16*>(a.out) + (size_t)(qi / G) * a.ldo +
-              (size_t)(g * G + qi % G) * kHd + d4;
-  dst[0] = __float2bfloat16_rn(acc[0] * inv);
-  dst[1] = __float2bfloat16_rn(acc[1] * inv);
-  dst[2] = __float2bfloat16_rn(acc[2] * inv);
-  dst[3] = __float2bfloat16_rn(acc[3] * inv);
+  attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
+                    reinterpret_cast<bf16*>(a.out), a.ldo, lane);
 }
 
 }  // namespace

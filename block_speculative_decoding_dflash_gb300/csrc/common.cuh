@@ -122,4 +122,12 @@ __device__ __forceinline__ long long ring_slot(long long pos, long long cap) {
   return pos % cap;
 }
 
+// (cos, sin) of pos * inv_freq[i]; the angle is formed in fp64 so that large
+// absolute positions keep their precision.
+__device__ __forceinline__ float2 rope_entry(const double* inv_freq, int i, long long pos) {
+  double s, c;
+  sincos(static_cast<double>(pos) * inv_freq[i], &s, &c);
+  return make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
 }  // namespace dfl

@@ -91,6 +91,49 @@ bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
 cudaError_t init_tc_attrs();
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st);
 
+// ---- persistent draft kernel ------------------------------------------------------
+// One cooperative launch runs the drafter block forward as a list of phases.
+enum : int { kPhEmbed = 0, kPhGemm = 1, kPhAttn = 2, kPhComb = 3 };
+struct MegaPhase {
+  int kind;
+  int epi;                 // kPhGemm: kEpiQKV, kEpiResid (y += ...), kEpiSwiglu, kEpiArgmax
+  int norm;                // kPhGemm: 1 = operand is rmsnorm(x rows) * gain, built in shared memory
+  int lm;                  // kPhGemm: the lm_head (argmax over block columns read0 ..; CTA 0
+                           // also stores the normalised rows to MegaArgs::xf)
+  int layer;               // kPhAttn: ring layer
+  int nseg;
+  int a_map[3];            // weight segment maps (index into MegaArgs::maps), box {64, 128}
+  int seg_tiles[3];        // cumulative 128-row tiles of the segments
+  int a2_map;              // kEpiSwiglu: up weight map
+  int b_map;               // norm == 0: activation map, box {64, 16}
+  int N, K, tiles, kchunks;
+  void* y; int ldy;        // output rows [M][ldy]; kEpiResid adds into it
+  const void* gain;        // norm == 1: RMSNorm gain [K]
+  const void* qn; const void* kn;  // kEpiQKV: q_norm / k_norm gains [128]
+  int nq_tiles;            // kEpiQKV: query tiles before the key tiles
+};
+struct MegaArgs {
+  const MegaPhase* phases; int nphase;
+  const CUtensorMap* maps;           // device array, 64-byte aligned
+  int M, Mlm, read0;                 // block rows; lm_head rows = block rows read0 .. M-1
+  int H, V, nq, nkv, qkv_n, half;
+  const void* embed; RoundState* rs; int mask_id;
+  const double* inv_freq; float2* rope;   // rope: [M][half], written by the embed phase
+  void* x; void* qkv; void* attn;    // [R][H], [R][qkv_n], [R][nq*128]
+  void* xf;                          // [R][H] final normalised rows
+  RingState* ring; void* ring_k; void* ring_v; long long cap; int window;
+  float* attn_part; int nsplit;      // split partials, layout stride nsplit
+  float* partials; unsigned* tile_ctr; int* err;
+  unsigned* done;                    // [nphase] phase counters, zero between launches
+  unsigned* abort_flag;              // raised by a CTA that gave up a wait
+  float softcap; int* ids; int* ids2; float* maxv; float* part_v; int* part_i;
+  float eps; int neox;
+};
+size_t draft_kernel_smem();
+cudaError_t init_draft_kernel_attrs();
+int draft_kernel_blocks_per_sm();
+cudaError_t launch_draft_kernel(const MegaArgs& a, int grid, cudaStream_t st);
+
 // Block rows (any M; 16 rows per weight pass): weight-streaming kernel.
 cudaError_t launch_linear_rows(int dtype, const LinearArgs& a, cudaStream_t st);
 // Many rows (context ingest), kEpiStore only: register-tiled GEMM.

@@ -17,14 +17,6 @@ __device__ __forceinline__ void copy8(const T* src, T* dst) {
   }
 }
 
-// (cos, sin) of pos * inv_freq[i]; the angle is formed in fp64 so that large
-// absolute positions keep their precision.
-__device__ __forceinline__ float2 rope_entry(const double* inv_freq, int i, long long pos) {
-  double s, c;
-  sincos(static_cast<double>(pos) * inv_freq[i], &s, &c);
-  return make_float2(static_cast<float>(c), static_cast<float>(s));
-}
-
 // Block input rows [anchor, mask, ..., mask] from the raw embedding table, and
 // the RoPE table of the block positions p .. p+tab_rows-1.
 template <typename T>

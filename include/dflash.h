@@ -294,11 +294,28 @@ int dflash_sync(dflash_ctx* ctx);
 /* Number of kernel launches graph slot `slot` holds (its kernel nodes). */
 int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
 
+/* ---- options ------------------------------------------------------------------ */
+
+/* DFLASH_OPT_FUSED_DRAFT: 1 (the default) runs dflash_draft_block as one
+ * persistent cooperative kernel (one CTA per SM) when the context allows it:
+ * bf16 weights, head_dim 128, hidden <= 2048, at most 16 block rows with at
+ * most 64 queries per kv head, no markov_add, every CTA resident at once.
+ * 0 runs one kernel per operation. Both give the same draft up to fp32
+ * summation order (same rounding points). */
+#define DFLASH_OPT_FUSED_DRAFT 1
+/* DFLASH_OPT_FUSED_DRAFT_AVAILABLE (read only): 1 if the context can use the
+ * persistent draft kernel at all (it still falls back for wider blocks). */
+#define DFLASH_OPT_FUSED_DRAFT_AVAILABLE 2
+/* EINVAL for an unknown option or value. Takes effect from the next call. */
+int dflash_set_option(dflash_ctx* ctx, int32_t option, int64_t value);
+int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
+
 /* ---- measurement ------------------------------------------------------------- */
 
-/* When enabled, dflash_draft_block brackets its lm_head kernel with two CUDA
- * events owned by the context, recorded on the context's stream (as event
- * nodes when the draft is being captured into a graph). */
+/* When enabled, dflash_draft_block brackets its lm_head kernel (the whole
+ * draft kernel, when the persistent one runs) with two CUDA events owned by
+ * the context, recorded on the context's stream (as event nodes when the
+ * draft is being captured into a graph). */
 int dflash_lm_head_timing(dflash_ctx* ctx, int32_t enable);
 /* Milliseconds between the two events as last recorded (syncs on the end
  * event). ESTATE if they were never recorded. */
