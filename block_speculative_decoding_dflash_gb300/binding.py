@@ -63,7 +63,7 @@ class RoundStateC(ctypes.Structure):
 
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE = 1, 2
+OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE, OPT_DRAFT_TRACE = 1, 2, 3
 
 
 def _sig(name, res, *args):
@@ -105,6 +105,7 @@ _sig("dflash_sync", ctypes.c_int, _vp)
 _sig("dflash_graph_kernel_count", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_set_option", ctypes.c_int, _vp, _i32, _i64)
 _sig("dflash_get_option", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
+_sig("dflash_draft_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
 _sig("dflash_lm_head_elapsed_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float))
 _sig("dflash_synth_target", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -392,6 +393,21 @@ class DFlashContext:
         o = _i64()
         self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT_AVAILABLE, ctypes.byref(o)))
         return bool(o.value)
+
+    def draft_trace(self, enable: bool):
+        """Stamp each CTA's phase completions in every draft-kernel launch."""
+        self._check(lib.dflash_set_option(self.h, OPT_DRAFT_TRACE, 1 if enable else 0))
+
+    def draft_trace_read(self) -> np.ndarray:
+        """[phases, CTAs, 12] globaltimer stamps (ns) of the last traced launch."""
+        r, c = _i32(), _i32()
+        rc = lib.dflash_draft_trace(self.h, None, 0, ctypes.byref(r), ctypes.byref(c))
+        if rc not in (0, ERANGE):
+            self._check(rc)
+        out = np.zeros((r.value, c.value, 12), dtype=np.uint64)
+        self._check(lib.dflash_draft_trace(self.h, out.ctypes.data, out.size, ctypes.byref(r),
+                                           ctypes.byref(c)))
+        return out
 
     def lm_head_timing(self, enable: bool):
         self._check(lib.dflash_lm_head_timing(self.h, 1 if enable else 0))

@@ -201,13 +201,15 @@ struct dflash_ctx {
   const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
   // persistent draft kernel (bf16, head_dim 128, up to 16 block rows)
   bool draft_fused_ok = false;                 // the config and device allow it
-  bool draft_fused_on = true;                  // DFLASH_OPT_FUSED_DRAFT
+  bool draft_fused_on = false;                 // DFLASH_OPT_FUSED_DRAFT
   MegaPhase* mega_phases = nullptr;            // device phase list
   int mega_nphase = 0;
   CUtensorMap* mega_maps = nullptr;            // device tensor-map table
   unsigned* mega_done = nullptr;               // [nphase] counters + abort flag
   int mega_grid = 0;
   int mega_nsplit = 0;
+  unsigned long long* mega_trace = nullptr;    // DFLASH_OPT_DRAFT_TRACE stamps
+  bool mega_trace_on = false;
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -551,6 +553,7 @@ int setup_draft_kernel(dflash_ctx* c) {
   const dflash_config& g = c->cfg;
   const int G = c->nq / c->nkv;
   if (c->hd != 128 || c->H > 2048 || c->H % 256 || c->nq % c->nkv || 16 * G > 64) return DFLASH_OK;
+  if (2 + 6 * g.n_layers > kMegaMaxPhases) return DFLASH_OK;
   int dev = 0, sms = 0;
   CK(c->err, cudaGetDevice(&dev));
   CK(c->err, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -623,12 +626,12 @@ int setup_draft_kernel(dflash_ctx* c) {
 
   CK(c->err, cudaMalloc(&c->mega_maps, maps.size() * sizeof(CUtensorMap)));
   CK(c->err, cudaMalloc(&c->mega_phases, ph.size() * sizeof(MegaPhase)));
-  CK(c->err, cudaMalloc(&c->mega_done, (ph.size() + 1) * sizeof(unsigned)));
+  CK(c->err, cudaMalloc(&c->mega_done, (ph.size() + 1) * kMegaDoneStride * sizeof(unsigned)));
   CK(c->err, cudaMemcpyAsync(c->mega_maps, maps.data(), maps.size() * sizeof(CUtensorMap),
                              cudaMemcpyHostToDevice, c->stream));
   CK(c->err, cudaMemcpyAsync(c->mega_phases, ph.data(), ph.size() * sizeof(MegaPhase),
                              cudaMemcpyHostToDevice, c->stream));
-  CK(c->err, cudaMemsetAsync(c->mega_done, 0, (ph.size() + 1) * sizeof(unsigned), c->stream));
+  CK(c->err, cudaMemsetAsync(c->mega_done, 0, (ph.size() + 1) * kMegaDoneStride * sizeof(unsigned), c->stream));
   CK(c->err, cudaStreamSynchronize(c->stream));
   c->mega_nphase = (int)ph.size();
   c->mega_grid = sms;
@@ -728,6 +731,7 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   cudaFree(ctx->mega_maps);
   cudaFree(ctx->mega_phases);
   cudaFree(ctx->mega_done);
+  cudaFree(ctx->mega_trace);
   for (auto& ev : ctx->lm_ev)
     if (ev) cudaEventDestroy(ev);
   delete ctx;
@@ -954,13 +958,14 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     m.window = c->cfg.window;
     m.attn_part = c->attn_part; m.nsplit = c->mega_nsplit;
     m.partials = c->tc_part; m.tile_ctr = c->tc_tiles; m.err = c->tc_err;
-    m.done = c->mega_done; m.abort_flag = c->mega_done + c->mega_nphase;
+    m.done = c->mega_done; m.abort_flag = c->mega_done + (size_t)c->mega_nphase * kMegaDoneStride;
     m.softcap = c->cfg.softcap;
     m.ids = markov ? c->backbone_ids : draft_ids;
     m.ids2 = markov ? nullptr : c->backbone_ids;
     m.maxv = c->maxv;
     m.part_v = c->tc_lm_pv; m.part_i = c->tc_lm_pi;
     m.eps = c->cfg.rms_eps; m.neox = c->cfg.rope_neox;
+    m.trace = c->mega_trace_on ? c->mega_trace : nullptr;
     CK(c->err, launch_draft_kernel(m, c->mega_grid, st));
     if (c->lm_timing) {
       CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
@@ -1282,7 +1287,32 @@ int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
     c->draft_fused_on = value != 0;
     return DFLASH_OK;
   }
+  if (option == DFLASH_OPT_DRAFT_TRACE) {
+    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
+    if (value && !c->draft_fused_ok) return fail(c->err, DFLASH_ESTATE, "no persistent draft kernel");
+    if (value && !c->mega_trace) {
+      const size_t n = (size_t)c->mega_nphase * c->mega_grid * kMegaTraceSlots;
+      CK(c->err, cudaMalloc(&c->mega_trace, n * sizeof(unsigned long long)));
+      CK(c->err, cudaMemsetAsync(c->mega_trace, 0, n * sizeof(unsigned long long), c->stream));
+    }
+    c->mega_trace_on = value != 0;
+    return DFLASH_OK;
+  }
   return fail(c->err, DFLASH_EINVAL, "unknown or read-only option %d", option);
+}
+
+int dflash_draft_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t* rows, int32_t* cols) {
+  if (!c) return DFLASH_EINVAL;
+  if (!rows || !cols) return fail(c->err, DFLASH_EINVAL, "rows or cols is NULL");
+  if (!c->mega_trace) return fail(c->err, DFLASH_ESTATE, "draft tracing was never enabled");
+  *rows = c->mega_nphase;
+  *cols = c->mega_grid;
+  const int64_t n = (int64_t)(*rows) * (*cols) * kMegaTraceSlots;
+  if (!out || capacity < n)
+    return fail(c->err, DFLASH_ERANGE, "capacity %lld < %lld stamps", (long long)capacity, (long long)n);
+  CK(c->err, cudaMemcpyAsync(out, c->mega_trace, n * sizeof(uint64_t), cudaMemcpyDeviceToHost, c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  return DFLASH_OK;
 }
 
 int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
@@ -1290,6 +1320,7 @@ int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
   if (!value) return fail(c->err, DFLASH_EINVAL, "value is NULL");
   if (option == DFLASH_OPT_FUSED_DRAFT) { *value = c->draft_fused_on ? 1 : 0; return DFLASH_OK; }
   if (option == DFLASH_OPT_FUSED_DRAFT_AVAILABLE) { *value = c->draft_fused_ok ? 1 : 0; return DFLASH_OK; }
+  if (option == DFLASH_OPT_DRAFT_TRACE) { *value = c->mega_trace_on ? 1 : 0; return DFLASH_OK; }
   return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 

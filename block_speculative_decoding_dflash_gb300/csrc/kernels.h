@@ -124,11 +124,23 @@ struct MegaArgs {
   RingState* ring; void* ring_k; void* ring_v; long long cap; int window;
   float* attn_part; int nsplit;      // split partials, layout stride nsplit
   float* partials; unsigned* tile_ctr; int* err;
-  unsigned* done;                    // [nphase] phase counters, zero between launches
+  unsigned* done;                    // [nphase][kMegaDoneStride] phase counters (one per
+                                     // 128-byte line), zero between launches
   unsigned* abort_flag;              // raised by a CTA that gave up a wait
   float softcap; int* ids; int* ids2; float* maxv; float* part_v; int* part_i;
   float eps; int neox;
+  // optional: [nphase][grid][kMegaTraceSlots] globaltimer stamps per phase
+  // and CTA: 0 workers start the phase, 1 normalised operand built /
+  // attention done, 2 first accumulator ready, 3 phase counted done, 4 the
+  // MMA issuer reaches the phase, 5 last MMA committed, 6 first weight tile
+  // requested, 7 first activation tile requested, 8 normalised operand's
+  // loads landed, 9 its row sums done, 10 first attention split's loads
+  // landed, 11 unused
+  unsigned long long* trace;
 };
+constexpr int kMegaDoneStride = 32;
+constexpr int kMegaTraceSlots = 12;
+constexpr int kMegaMaxPhases = 64;       // 2 + 6 per layer: up to 10 layers
 size_t draft_kernel_smem();
 cudaError_t init_draft_kernel_attrs();
 int draft_kernel_blocks_per_sm();

@@ -296,19 +296,40 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
 
 /* ---- options ------------------------------------------------------------------ */
 
-/* DFLASH_OPT_FUSED_DRAFT: 1 (the default) runs dflash_draft_block as one
- * persistent cooperative kernel (one CTA per SM) when the context allows it:
+/* DFLASH_OPT_FUSED_DRAFT: 1 runs dflash_draft_block as one persistent
+ * cooperative kernel (one CTA per SM) when the context allows it:
  * bf16 weights, head_dim 128, hidden <= 2048, at most 16 block rows with at
  * most 64 queries per kv head, no markov_add, every CTA resident at once.
- * 0 runs one kernel per operation. Both give the same draft up to fp32
- * summation order (same rounding points). */
+ * 0 (the default) runs one kernel per operation. Both give the same draft
+ * up to fp32 summation order (same rounding points). */
 #define DFLASH_OPT_FUSED_DRAFT 1
 /* DFLASH_OPT_FUSED_DRAFT_AVAILABLE (read only): 1 if the context can use the
  * persistent draft kernel at all (it still falls back for wider blocks). */
 #define DFLASH_OPT_FUSED_DRAFT_AVAILABLE 2
+/* DFLASH_OPT_DRAFT_TRACE: 1 makes every persistent draft kernel launch stamp
+ * the GPU's global timer (ns) at twelve events of every phase on every CTA
+ * (allocates phases x CTAs x 96 bytes on first use; 0 stops it). The stamps
+ * of the last launch are read with dflash_draft_trace. */
+#define DFLASH_OPT_DRAFT_TRACE 3
 /* EINVAL for an unknown option or value. Takes effect from the next call. */
 int dflash_set_option(dflash_ctx* ctx, int32_t option, int64_t value);
 int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
+/* Copies the stamps of the last traced draft-kernel launch into out_host as
+ * [rows][cols][12] (rows = phases, cols = CTAs). Per phase and CTA: 0 the
+ * workers start the phase, 1 the normalised operand is built (GEMM phases
+ * with an RMSNorm input) or the attention splits are done, 2 the first
+ * accumulator is ready, 3 the CTA counts the phase done, 4 the MMA issuer
+ * reaches the phase, 5 the last MMA is committed, 6 the first weight tile is
+ * requested, 7 the first activation tile is requested, 8 the normalised
+ * operand's loads have landed, 9 its row sums are done, 10 the first
+ * attention split's loads have landed, 11 unused; events that do not occur
+ * keep their old value (zero at first). Syncs the context's stream. ERANGE
+ * if out_host is NULL or capacity < rows * cols * 12 (rows and cols are still
+ * set, so a call with capacity 0 asks for the size), ESTATE if tracing was
+ * never enabled. The phase order is: embedding, then per layer QKV,
+ * attention, split merge, O, gate/up, down, then the lm_head. */
+int dflash_draft_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity,
+                       int32_t* rows, int32_t* cols);
 
 /* ---- measurement ------------------------------------------------------------- */
 

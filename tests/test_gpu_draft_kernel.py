@@ -1,9 +1,8 @@
 """The persistent draft kernel (the whole drafter block forward in one
 cooperative launch) against the one-kernel-per-operation path on the same
 context, against a plain PyTorch fp32 lm_head + softcap + argmax of its own
-final hidden rows, and under graph replay. Its parity with the oracle is
-covered by the Muse- and DSpark-shaped round tests, which draft through it
-by default for blocks of at most 16 rows."""
+final hidden rows, under graph replay, and against the oracle through full
+rounds (Muse- and DSpark-shaped)."""
 
 import numpy as np
 import pytest
@@ -98,6 +97,7 @@ def test_fused_repeat_and_graph_replay(B):
     """Phase counters rearm between launches: 40 back-to-back drafts and
     graph replays of two widths give the first draft's ids every time."""
     cfg, ctx, wd = _ctx(B, "muse", n_layers=1, ctx_rows=512)
+    ctx.set_fused_draft(True)
     ref = {blk: _draft(ctx, cfg, blk)[0] for blk in (4, 16)}
     ids = {blk: torch.empty(blk - 1, dtype=torch.int32, device="cuda") for blk in (4, 16)}
     for i in range(40):
@@ -126,3 +126,27 @@ def test_fused_availability(B):
     ctx = B.DFlashContext(tiny, B.weights_to_device(w, "f32"))
     assert not ctx.fused_draft_available()       # fp32 drafter: one kernel per operation
     ctx.close()
+
+
+@pytest.mark.parametrize("name", ["muse", "dspark"])
+def test_fused_rounds_match_oracle(B, name):
+    """Full rounds drafted by the persistent kernel, checked against the
+    oracle round by round (hidden rows, max logits, ids, state, ring)."""
+    import gpu_harness as Hh
+    over = {"n_layers": 2}
+    if name == "dspark":
+        over["max_context"] = 1024 + 4 * 10
+    cfg = synth.config(name, **over)
+    w = synth.make_weights(cfg, 0)
+    pair = Hh.Pair(cfg, weights=w, w64=Hh.f64_weights(w, "bf16", lazy_embed=True))
+    pair.ctx.set_fused_draft(True)
+    assert pair.ctx.fused_draft_available()
+    ctx_rows = 1024
+    pair.ingest(synth.make_context(cfg, ctx_rows, seed=5), 0, anchor=321)
+    blocks = (4, 16, 5, 16) if name == "muse" else (8, 10, 8)
+    stream = synth.make_target_stream(cfg, len(blocks), max(blocks), seed=5, logit_pool=2, resid_pool=4)
+    for r, blk in enumerate(blocks):
+        pair.round(stream, r, blk)
+        pair.check_state()
+    pair.check_ring(max_rows=32)
+    pair.close()
