@@ -34,18 +34,24 @@ namespace {
 
 constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
 
-template <int BN, int NV, int STAGES>
+// A stage holds P consecutive K chunks of one tile (P = 2: each weight row
+// is read as 256 contiguous bytes per stage instead of 128, which lets HBM
+// stream at ~95% of its copy rate instead of ~65%): the P weight sub-tiles
+// (NV each: gate, up), then the P activation sub-tiles.
+template <int BN, int NV, int STAGES, int P>
 struct Cfg {
-  static constexpr int kStage = NV * kABytes + BN * 128;
+  static constexpr int kSub = NV * kABytes;
+  static constexpr int kBOff = P * kSub;
+  static constexpr int kStage = P * (kSub + BN * 128);
   static constexpr uint32_t kTmem = tmem_cols(2 * NV * BN);
   static constexpr size_t kSmem = (size_t)STAGES * kStage + 1024 + 512;
 };
 
 
-template <int BN, int EPI, int STAGES>
+template <int BN, int EPI, int STAGES, int P>
 __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   constexpr int NV = (EPI == kEpiSwiglu) ? 2 : 1;
-  using C = Cfg<BN, NV, STAGES>;
+  using C = Cfg<BN, NV, STAGES, P>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
@@ -87,33 +93,55 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       tma_prefetch_desc(&a.b_map);
       const uint64_t pol = policy_evict_first();
       bool ok = true;
-      const long long nunits = u1 - u0;
-      const long long pre = nunits < STAGES ? nunits : STAGES;
-      // Weight tiles of the first stages: they do not depend on earlier kernels.
-      for (long long i = 0; i < nunits && ok; ++i) {
-        const long long u = u0 + i;
+      // Stage i covers units [u, u + nc): nc = P while the next unit is in the
+      // same tile and in this CTA's range (the MMA issuer pairs the same way).
+      auto issue_a = [&](int st, long long u, int nc) {
         const int t = static_cast<int>(u / KC), c = static_cast<int>(u % KC);
         int s = 0;
         while (s < a.nseg - 1 && t >= a.seg_tiles[s]) ++s;
         const int row0 = (t - (s ? a.seg_tiles[s - 1] : 0)) * 128;
-        const int st = static_cast<int>(i % STAGES);
         uint8_t* sa = smem + (size_t)st * C::kStage;
-        if (i >= STAGES) ok = mbar_wait(&empty[st], static_cast<unsigned>((i / STAGES - 1) & 1));
-        if (!ok) break;
-        if (i == pre) pdl_wait();
-        mbar_expect_tx(&full[st], C::kStage);
-        tma_load_2d_hint(sa, &a.a_map[s], c * 64, row0, &full[st], pol);
-        if (NV == 2) tma_load_2d_hint(sa + kABytes, &a.a2_map, c * 64, t * 128, &full[st], pol);
-        if (i >= pre) tma_load_2d(sa + NV * kABytes, &a.b_map, c * 64, 0, &full[st]);
-        if (i == pre - 1) {
-          // The activations of the prefetched stages, once the inputs exist.
-          pdl_wait();
-          for (long long j = 0; j <= i; ++j) {
-            const int cj = static_cast<int>((u0 + j) % KC);
-            const int sj = static_cast<int>(j % STAGES);
-            tma_load_2d(smem + (size_t)sj * C::kStage + NV * kABytes, &a.b_map, cj * 64, 0, &full[sj]);
-          }
+        mbar_expect_tx(&full[st], nc * (C::kSub + BN * 128));
+        for (int k = 0; k < nc; ++k) {
+          tma_load_2d_hint(sa + k * C::kSub, &a.a_map[s], (c + k) * 64, row0, &full[st], pol);
+          if (NV == 2) tma_load_2d_hint(sa + k * C::kSub + kABytes, &a.a2_map, (c + k) * 64, t * 128, &full[st], pol);
         }
+      };
+      auto issue_b = [&](int st, long long u, int nc) {
+        const int c = static_cast<int>(u % KC);
+        uint8_t* sb = smem + (size_t)st * C::kStage + C::kBOff;
+        for (int k = 0; k < nc; ++k) tma_load_2d(sb + k * BN * 128, &a.b_map, (c + k) * 64, 0, &full[st]);
+      };
+      auto width = [&](long long u) {
+        return (P == 2 && u + 1 < u1 && (u % KC) + 1 < KC) ? 2 : 1;
+      };
+      // The weight tiles of the first stages do not depend on earlier
+      // kernels: request them before the programmatic launch dependency
+      // resolves, and their activations once it has.
+      long long u = u0;
+      int pre = 0;
+      for (; pre < STAGES && u < u1; ++pre) {
+        const int nc = width(u);
+        issue_a(pre, u, nc);
+        u += nc;
+      }
+      pdl_wait();
+      {
+        long long v = u0;
+        for (int j = 0; j < pre; ++j) {
+          const int nc = width(v);
+          issue_b(j, v, nc);
+          v += nc;
+        }
+      }
+      for (long long i = pre; u < u1 && ok; ++i) {
+        const int st = static_cast<int>(i % STAGES);
+        ok = mbar_wait(&empty[st], static_cast<unsigned>((i / STAGES - 1) & 1));
+        if (!ok) break;
+        const int nc = width(u);
+        issue_a(st, u, nc);
+        issue_b(st, u, nc);
+        u += nc;
       }
       if (!ok) atomicOr(a.err, 1);
     }
@@ -132,22 +160,28 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * NV * BN;
-        for (int c = c0; c < c1; ++c, ++i) {
+        for (int c = c0; c < c1; ++i) {
+          const int nc = (P == 2 && c + 1 < c1) ? 2 : 1;
           const int st = static_cast<int>(i % STAGES);
           ok = mbar_wait(&full[st], static_cast<unsigned>((i / STAGES) & 1));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)st * C::kStage);
-          const uint32_t sb = sa + NV * kABytes;
+          const uint32_t s0 = smem_u32(smem + (size_t)st * C::kStage);
+          for (int k = 0; k < nc; ++k) {
+            const uint32_t sa = s0 + k * C::kSub;
+            const uint32_t sb = s0 + C::kBOff + k * BN * 128;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = smem_desc_sw128(sb + kk * 32);
-            const uint32_t acc = (c > c0 || kk > 0) ? 1u : 0u;
-            tc_mma_bf16(d, smem_desc_sw128(sa + kk * 32), bd, idesc, acc);
-            if (NV == 2) tc_mma_bf16(d + BN, smem_desc_sw128(sa + kABytes + kk * 32), bd, idesc, acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = smem_desc_sw128(sb + kk * 32);
+              const uint32_t acc = (c + k > c0 || kk > 0) ? 1u : 0u;
+              tc_mma_bf16(d, smem_desc_sw128(sa + kk * 32), bd, idesc, acc);
+              if (NV == 2) tc_mma_bf16(d + BN, smem_desc_sw128(sa + kABytes + kk * 32), bd, idesc, acc);
+            }
           }
           tc_commit(&empty[st]);
+          c += nc;
         }
+        if (!ok) break;
         tc_commit(&acc_full[buf]);
         u += c1 - c0;
       }
@@ -369,33 +403,40 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 
 // The decode-layer GEMMs are short: keep two CTAs per SM (about 73 / 103 KB of
 // shared memory each) so the next GEMM's CTAs fit beside the running one and
-// stream their first weight tiles early. The lm_head is long: a deep ring.
+// stream their first weight tiles early. The lm_head is long: a deep ring of
+// paired-chunk stages.
 template <int BN, int EPI>
-constexpr int stages_for() { return EPI == kEpiArgmax ? (BN == 16 ? 12 : 10) : EPI == kEpiSwiglu ? 3 : 4; }
+constexpr int stages_for() {
+  return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : EPI == kEpiSwiglu ? (BN == 16 ? 3 : 2) : (BN == 16 ? 3 : 2);
+}
+template <int BN, int EPI>
+constexpr int pairs_for() { return 2; }
 
 template <int BN, int EPI>
 cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
   constexpr int S = stages_for<BN, EPI>();
+  constexpr int P = pairs_for<BN, EPI>();
   constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<BN, NV, S>::kSmem;
+  cfg.dynamicSmemBytes = Cfg<BN, NV, S, P>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI, S>, a);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI, S, P>, a);
 }
 
 template <int BN, int EPI>
 cudaError_t attr_tc() {
   constexpr int S = stages_for<BN, EPI>();
+  constexpr int P = pairs_for<BN, EPI>();
   constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
-  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<BN, NV, S>::kSmem);
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<BN, NV, S, P>::kSmem);
 }
 
 // ---------------------------------------------------------------------------
