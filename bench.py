@@ -5,8 +5,8 @@ One step = one whole Muse-assistant-shaped job: ingest 2048 captured context
 rows (window 2048), then 512 rounds (draft, stand-in target, verify, ring
 append, partial-accept trim) with the verify width starting at 4 and
 widening to 16 when a measurement window pays for it. Metric: rounds/s
-(whole job, all GPUs); draft tokens/s and the lm_head kernel's HBM roofline
-fraction ride along. Inputs are synthetic (seeded), weights random-init bf16.
+(whole job, all GPUs); draft tokens/s and the HBM roofline fraction of the
+draft kernel (the whole drafter forward + lm_head argmax) ride along. Inputs are synthetic (seeded), weights random-init bf16.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -285,6 +285,18 @@ def lm_head_bytes(cfg, rows):
     return cfg["vocab"] * cfg["hidden"] * 2 + rows * cfg["hidden"] * 2 + rows * 8
 
 
+def draft_bytes(cfg, rows, nctx):
+    """Algorithmic HBM bytes of one persistent draft-kernel launch: every
+    drafter weight once (5 layers of Wq Wk Wv Wo Wg Wu Wd, the lm_head), the
+    window's K and V of every layer, the block's embedding rows, and the
+    argmax outputs."""
+    H, I, hd = cfg["hidden"], cfg["intermediate"], cfg["head_dim"]
+    qdim, kvdim = cfg["n_q_heads"] * hd, cfg["n_kv_heads"] * hd
+    layer = (H * (qdim + 2 * kvdim) + qdim * H + 3 * H * I + 4 * H) * 2
+    kv = 2 * nctx * kvdim * 2
+    return cfg["n_layers"] * (layer + kv) + lm_head_bytes(cfg, rows - 1) + rows * H * 2
+
+
 def cpu_baseline(job, n_rounds):
     """The oracle as it stands, on the host cores: ingest + n_rounds rounds at
     width 4, extrapolated to the 512-round job."""
@@ -352,7 +364,16 @@ def run_ours(args, world, rank, local):
     launches = sum(r["launches"] for r in results)
     lm = [x for r in results for x in r["lm_ms"]]
     peaks, which = measured_peaks()
-    lm_bytes = [lm_head_bytes(job.cfg, w - 1) for w, _ in lm]
+    fused = job.ctx.fused_draft_available() and job.ctx.fused_draft_enabled()
+    if fused:
+        lm_bytes = [draft_bytes(job.cfg, w, job.cfg["window"]) for w, _ in lm]
+        kname = ("draft_kernel (persistent cooperative drafter block forward: 5 layers + "
+                 "lm_head + softcap + argmax)")
+        unit_desc = "all drafter weights + the window's K/V per launch"
+    else:
+        lm_bytes = [lm_head_bytes(job.cfg, w - 1) for w, _ in lm]
+        kname = "lmhead_argmax (split-vocab lm_head + softcap + argmax)"
+        unit_desc = "lm_head weights per launch"
     lm_t = [t for _, t in lm]
     achieved = sum(lm_bytes) / (sum(lm_t) / 1e3) / 1e9 if lm_t else None
     widths = [w for r in results for w in r["widths"]]
@@ -412,7 +433,9 @@ def run_ours(args, world, rank, local):
             "round_us_by_width": round_us,
             "accepted_per_round": round(accepted / nrounds, 4),
             "emitted_per_round": round(accepted / nrounds + 1, 4),
-            "roofline": {"kernel": "lmhead_argmax (split-vocab lm_head + softcap + argmax)",
+            "roofline": {"kernel": kname, "bytes": unit_desc,
+                         "bytes_per_launch": {str(w): draft_bytes(job.cfg, w, job.cfg["window"]) if fused
+                                              else lm_head_bytes(job.cfg, w - 1) for w in (4, 16)},
                          "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
                          "peak": peaks["hbm_gbs"], "peak_source": which, "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,

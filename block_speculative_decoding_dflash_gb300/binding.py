@@ -389,6 +389,11 @@ class DFlashContext:
         allows it (the default), or with one kernel per operation."""
         self._check(lib.dflash_set_option(self.h, OPT_FUSED_DRAFT, 1 if enable else 0))
 
+    def fused_draft_enabled(self) -> bool:
+        o = _i64()
+        self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT, ctypes.byref(o)))
+        return bool(o.value)
+
     def fused_draft_available(self) -> bool:
         o = _i64()
         self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT_AVAILABLE, ctypes.byref(o)))

@@ -493,13 +493,8 @@ __device__ __noinline__ int gemm_epilogue(const MegaArgs& a, const MegaPhase& ph
     bool finish = (c0 == 0 && c1 == KC);
     if (!finish) {
       const int slot = (t == first_tile) ? 0 : 1;
-      float4* mine = reinterpret_cast<float4*>(partials + ((size_t)b * 2 + slot) * NV * BN * 128 +
-                                               (size_t)row * NV * BN);
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int m = 0; m < BN; m += 4)
-          mine[(v * BN + m) / 4] = make_float4(acc[v][m], acc[v][m + 1], acc[v][m + 2], acc[v][m + 3]);
+      const int mq = (Mr + 3) / 4;
+      put_partial<NV, BN>(partials, b, slot, row, mq, acc);
       epi_sync();
       const int bf = owner_of((long long)t * KC, rg.U, G);
       const int bl = owner_of((long long)t * KC + KC - 1, rg.U, G);
@@ -512,34 +507,9 @@ __device__ __noinline__ int gemm_epilogue(const MegaArgs& a, const MegaPhase& ph
       finish = E.flag != 0;
       if (finish) {
         __threadfence();
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-          for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
-        constexpr int kBatch = NV == 1 ? 4 : 2;
-        for (int b0 = bf; b0 <= bl; b0 += kBatch) {
-          float4 pv[kBatch][NV * BN / 4];
-#pragma unroll
-          for (int qq = 0; qq < kBatch; ++qq) {
-            const int bb = b0 + qq;
-            if (bb > bl) break;
-            const int first_bb = static_cast<int>((rg.U * bb / G) / KC);
-            const int sl = (t == first_bb) ? 0 : 1;
-            const float4* p = reinterpret_cast<const float4*>(
-                partials + ((size_t)bb * 2 + sl) * NV * BN * 128 + (size_t)row * NV * BN);
-#pragma unroll
-            for (int j = 0; j < NV * BN / 4; ++j) pv[qq][j] = __ldcg(p + j);
-          }
-#pragma unroll
-          for (int qq = 0; qq < kBatch; ++qq) {
-            if (b0 + qq > bl) break;
-#pragma unroll
-            for (int j = 0; j < NV * BN / 4; ++j) {
-              float* dst = &acc[(4 * j) / BN][(4 * j) % BN];
-              dst[0] += pv[qq][j].x; dst[1] += pv[qq][j].y; dst[2] += pv[qq][j].z; dst[3] += pv[qq][j].w;
-            }
-          }
-        }
+        auto slot_of = [&](int bb) { return t == static_cast<int>((rg.U * bb / G) / KC) ? 0 : 1; };
+        if (mq == 1) sum_partials<NV, BN, 1, 4 / NV>(acc, partials, row, bf, bl, mq, slot_of);
+        else sum_partials<NV, BN, BN / 4, (NV == 1 ? 4 : 2)>(acc, partials, row, bf, bl, mq, slot_of);
         if (wt == 0) tile_ctr[t] = 0u;
       }
     }

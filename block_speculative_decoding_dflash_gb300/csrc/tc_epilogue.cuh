@@ -66,6 +66,63 @@ __device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const f
   }
 }
 
+// Split-tile partials: CTA b's fp32 partial of a tile sits in slot 0 (its
+// first tile) or 1 (its last) of partials[b][2][128][NV * BN], row-major, so
+// a thread moves its row's values as float4. Only the first mq float4 groups
+// of each NV block (the block rows m < M) are written and read.
+template <int NV, int BN>
+__device__ __forceinline__ void put_partial(float* partials, int b, int slot, int row, int mq,
+                                            const float (&acc)[NV][BN]) {
+  float4* mine = reinterpret_cast<float4*>(partials + ((size_t)b * 2 + slot) * NV * BN * 128 +
+                                           (size_t)row * NV * BN);
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int j = 0; j < BN / 4; ++j)
+      if (j < mq)
+        mine[v * (BN / 4) + j] = make_float4(acc[v][4 * j], acc[v][4 * j + 1], acc[v][4 * j + 2], acc[v][4 * j + 3]);
+}
+
+// acc = sum of the partials of CTAs bf..bl in CTA order (deterministic),
+// issuing the loads of KB contributors before adding them: L2 latency, not
+// bandwidth, bounds this loop, so fewer groups per contributor (MQC) allow a
+// deeper batch. slot_of(bb) gives contributor bb's slot for this tile.
+template <int NV, int BN, int MQC, int KB, class SlotOf>
+__device__ __forceinline__ void sum_partials(float (&acc)[NV][BN], const float* partials, int row, int bf,
+                                             int bl, int mq, SlotOf slot_of) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
+  for (int b0 = bf; b0 <= bl; b0 += KB) {
+    float4 pv[KB][NV * MQC];
+#pragma unroll
+    for (int q = 0; q < KB; ++q) {
+      const int bb = b0 + q;
+      if (bb > bl) break;
+      const float4* p = reinterpret_cast<const float4*>(
+          partials + ((size_t)bb * 2 + slot_of(bb)) * NV * BN * 128 + (size_t)row * NV * BN);
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < MQC; ++j)
+          pv[q][v * MQC + j] = j < mq ? __ldcg(p + v * (BN / 4) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < KB; ++q) {
+      if (b0 + q > bl) break;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < MQC; ++j) {
+          float* dst = &acc[v][4 * j];
+          const float4 x = pv[q][v * MQC + j];
+          dst[0] += x.x; dst[1] += x.y; dst[2] += x.z; dst[3] += x.w;
+        }
+    }
+  }
+}
+
 // CTA owning unit u when U units are split into G contiguous ranges
 // [floor(b*U/G), floor((b+1)*U/G)).
 __device__ __forceinline__ int owner_of(long long u, long long U, int G) {

@@ -219,14 +219,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       if (!finish) {
         // Split tile: publish this CTA's partial, take a ticket.
         const int slot = (t == first_tile) ? 0 : 1;
-        // row-contiguous [128][NV*BN] so each thread moves its values as float4
-        float4* mine = reinterpret_cast<float4*>(a.partials + ((size_t)b * 2 + slot) * NV * BN * 128 +
-                                                 (size_t)row * NV * BN);
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-          for (int m = 0; m < BN; m += 4)
-            mine[(v * BN + m) / 4] = make_float4(acc[v][m], acc[v][m + 1], acc[v][m + 2], acc[v][m + 3]);
+        const int mq = (a.M + 3) / 4;
+        put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
         __threadfence();
         epi_sync();
         const int bf = owner_of((long long)t * KC, U, G);
@@ -239,37 +233,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         finish = s_last != 0;
         if (finish) {
           __threadfence();
-#pragma unroll
-          for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
-          // Sum the contributors' partials in CTA order, issuing the loads of
-          // kBatch contributors before adding them (L2 latency, not bandwidth,
-          // bounds this loop).
-          constexpr int kBatch = NV * BN <= 16 ? 4 : NV * BN <= 32 ? 2 : 1;
-          for (int b0 = bf; b0 <= bl; b0 += kBatch) {
-            float4 pv[kBatch][NV * BN / 4];
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-              const int bb = b0 + q;
-              if (bb > bl) break;
-              const int first_bb = static_cast<int>((U * bb / G) / KC);
-              const int sl = (t == first_bb) ? 0 : 1;
-              const float4* p = reinterpret_cast<const float4*>(
-                  a.partials + ((size_t)bb * 2 + sl) * NV * BN * 128 + (size_t)row * NV * BN);
-#pragma unroll
-              for (int j = 0; j < NV * BN / 4; ++j) pv[q][j] = __ldcg(p + j);
-            }
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-              if (b0 + q > bl) break;
-#pragma unroll
-              for (int j = 0; j < NV * BN / 4; ++j) {
-                float* dst = &acc[(4 * j) / BN][(4 * j) % BN];
-                dst[0] += pv[q][j].x; dst[1] += pv[q][j].y; dst[2] += pv[q][j].z; dst[3] += pv[q][j].w;
-              }
-            }
-          }
+          auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
+          if (mq == 1) sum_partials<NV, BN, 1, 8 / NV>(acc, a.partials, row, bf, bl, mq, slot_of);
+          else sum_partials<NV, BN, BN / 4, (NV * BN <= 16 ? 4 : NV * BN <= 32 ? 2 : 1)>(acc, a.partials, row, bf, bl, mq, slot_of);
           if (threadIdx.x == 64) a.tile_ctr[t] = 0u;
         }
       }
