@@ -37,6 +37,7 @@ enum : int {
   kEpiQKV = 5,      // tensor-core GEMM only: q/k head-norm + RoPE, v plain, stored
 };
 constexpr int kTcMaxSeg = 10;
+constexpr int kTileDepart = 4096;  // tiles per GEMM at most; departures follow arrivals
 
 // Tensor-core weight-streaming GEMM D[n, m] = sum_k W[n, k] X[m, k] (bf16,
 // fp32 accumulate), M <= BN rows of X (BN 16 or 32). Weight rows are stacked
@@ -52,7 +53,8 @@ struct TcGemmArgs {
   void* y; int ldy;                // output [M, N] (row stride ldy)
   const void* r; int ldr;          // residual of kEpiResid (may alias y)
   float* partials;                 // [grid][2][NV*BN][128] fp32 split-tile partials
-  unsigned* tile_ctr;              // [tiles], zero between launches
+  unsigned* tile_ctr;              // [kTileDepart + tiles]: arrivals, then departures per
+                                   // split tile; zero between launches
   int* err;                        // bounded-wait timeouts are reported here
   float softcap;                   // kEpiArgmax
   int* ids; int* ids2; float* maxv;

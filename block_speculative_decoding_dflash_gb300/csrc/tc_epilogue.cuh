@@ -123,6 +123,55 @@ __device__ __forceinline__ void sum_partials(float (&acc)[NV][BN], const float* 
   }
 }
 
+// acc[v][4g .. 4g+3] = the sum of float4 group g of the partials of CTAs
+// bf..bl in CTA order, KB contributors' loads in flight at a time (the other
+// columns of acc are left zero).
+template <int NV, int BN, int KB, class SlotOf>
+__device__ __forceinline__ void sum_group(float (&acc)[NV][BN], const float* partials, int row, int g,
+                                          int bf, int bl, SlotOf slot_of) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int m = 0; m < BN; ++m) acc[v][m] = 0.f;
+  float4 sum[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) sum[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b0 = bf; b0 <= bl; b0 += KB) {
+    float4 pv[KB][NV];
+#pragma unroll
+    for (int qq = 0; qq < KB; ++qq) {
+      const int bb = b0 + qq;
+      if (bb > bl) break;
+      const float4* p = reinterpret_cast<const float4*>(
+          partials + ((size_t)bb * 2 + slot_of(bb)) * NV * BN * 128 + (size_t)row * NV * BN);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) pv[qq][v] = __ldcg(p + v * (BN / 4) + g);
+    }
+#pragma unroll
+    for (int qq = 0; qq < KB; ++qq) {
+      if (b0 + qq > bl) break;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        sum[v].x += pv[qq][v].x; sum[v].y += pv[qq][v].y; sum[v].z += pv[qq][v].z; sum[v].w += pv[qq][v].w;
+      }
+    }
+  }
+  // g is warp-uniform; the static selection below keeps acc in registers
+#pragma unroll
+  for (int j = 0; j < BN / 4; ++j)
+    if (j == g) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        acc[v][4 * j] = sum[v].x; acc[v][4 * j + 1] = sum[v].y;
+        acc[v][4 * j + 2] = sum[v].z; acc[v][4 * j + 3] = sum[v].w;
+      }
+    }
+}
+
+__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned* p) {
+  return *reinterpret_cast<const volatile unsigned*>(p);
+}
+
 // CTA owning unit u when U units are split into G contiguous ranges
 // [floor(b*U/G), floor((b+1)*U/G)).
 __device__ __forceinline__ int owner_of(long long u, long long U, int G) {

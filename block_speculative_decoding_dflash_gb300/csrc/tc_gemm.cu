@@ -193,70 +193,28 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     const int q = warp & 3;                       // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;                // accumulator row = output feature in tile
     const int first_tile = static_cast<int>(u0 / KC);
+    const int mq = (a.M + 3) / 4;                 // float4 groups of block rows
     bool ok = true;
     int seg = 0;
-    for (long long u = u0; u < u1 && ok; ++seg) {
-      const int t = static_cast<int>(u / KC);
-      const int c0 = static_cast<int>(u % KC);
-      const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
-      const int buf = seg & 1;
-      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      float acc[NV][BN];
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int j = 0; j < BN / 16; ++j)
-          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * NV * BN + v * BN + j * 16,
-                    &acc[v][j * 16]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
-      u += c1 - c0;
 
-      bool finish = (c0 == 0 && c1 == KC);
-      if (!finish) {
-        // Split tile: publish this CTA's partial, take a ticket.
-        const int slot = (t == first_tile) ? 0 : 1;
-        const int mq = (a.M + 3) / 4;
-        put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
-        __threadfence();
-        epi_sync();
-        const int bf = owner_of((long long)t * KC, U, G);
-        const int bl = owner_of((long long)t * KC + KC - 1, U, G);
-        if (threadIdx.x == 64) {
-          const unsigned ticket = atomicAdd(&a.tile_ctr[t], 1u);
-          s_last = (ticket == static_cast<unsigned>(bl - bf));
-        }
-        epi_sync();
-        finish = s_last != 0;
-        if (finish) {
-          __threadfence();
-          auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
-          if (mq == 1) sum_partials<NV, BN, 1, 8 / NV>(acc, a.partials, row, bf, bl, mq, slot_of);
-          else sum_partials<NV, BN, BN / 4, (NV * BN <= 16 ? 4 : NV * BN <= 32 ? 2 : 1)>(acc, a.partials, row, bf, bl, mq, slot_of);
-          if (threadIdx.x == 64) a.tile_ctr[t] = 0u;
-        }
-      }
-      if (!finish) continue;
-
-      // ---- final epilogue of tile t ----
+    // Final epilogue of tile t for block rows [m0, m1).
+    auto finish_tile = [&](float (&acc)[NV][BN], int t, int m0, int m1) {
       const int n = t * 128 + row;
       const bool valid = n < a.N;
       if (EPI == kEpiArgmax) {
         const float cap = a.softcap;
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
+          if (m < m0 || m >= m1) continue;        // uniform: only this call's columns
           float z = acc[0][m];
           if (cap > 0.f) z = cap * tanhf(z / cap);
-          float bv = (valid && m < a.M) ? z : -INFINITY;
+          float bv = valid ? z : -INFINITY;
           int bi = valid ? n : 0x7fffffff;
           warp_argmax(bv, bi);
           if (lane == 0) { red_v[q][m] = bv; red_i[q][m] = bi; }
         }
         epi_sync();
-        if (threadIdx.x >= 64 && threadIdx.x < 64 + BN) {
+        if (threadIdx.x >= 64 + m0 && threadIdx.x < 64 + m1) {
           const int m = threadIdx.x - 64;
           float bv = best_v[m];
           int bi = best_i[m];
@@ -281,12 +239,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
         for (int m = 0; m < BN; ++m)
-          if (m < a.M && valid) Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(val[m]);
+          if (m >= m0 && m < m1 && valid) Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(val[m]);
       } else if (EPI == kEpiKVRing) {
         // tile t = kv head h of layer l, K or V (hd = 128 = one tile)
-        const int seg = t / a.nkv, h = t % a.nkv;
-        const int layer = seg >> 1;
-        const bool isv = seg & 1;
+        const int sg = t / a.nkv, h = t % a.nkv;
+        const int layer = sg >> 1;
+        const bool isv = sg & 1;
         const long long off0 = a.ring->offset;
         const size_t head_base = (((size_t)layer * a.nkv + h) * a.cap) * 128;
         bf16* dst = reinterpret_cast<bf16*>(isv ? a.ring_v : a.ring_k) + head_base;
@@ -299,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         }
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
-          if (m >= a.M) break;
+          if (m < m0 || m >= m1) continue;
           const long long pos = off0 + m;
           if (a.append_only && pos - a.ring->base >= a.cap) {
             if (row == 0) atomicOr(&a.ring->error, kErrFull);
@@ -311,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
-          if (m < a.M) {
+          if (m >= m0 && m < m1) {
             float out;
             if (EPI == kEpiStore) {
               out = acc[0][m];
@@ -324,6 +282,99 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
             Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(out);
           }
         }
+      }
+    };
+
+    // Whole tiles are finished at once. A tile split across CTAs is finished
+    // cooperatively: every contributor publishes its fp32 partial and arrives
+    // on the tile's counter; once all of this CTA's tiles are published it
+    // waits for the other contributors of its split tiles and reduces one
+    // float4 group of block rows each (contributor k of n takes groups k,
+    // k + n, ...), summing the partials in CTA order. (The lm_head's split
+    // tiles have two contributors; the later one finishes those alone.)
+    int split_first = -1, split_last = -1;        // split tiles published (slot 0, slot 1)
+    unsigned* const arrive = a.tile_ctr;
+    unsigned* const depart = a.tile_ctr + kTileDepart;
+    for (long long u = u0; u < u1 && ok; ++seg) {
+      const int t = static_cast<int>(u / KC);
+      const int c0 = static_cast<int>(u % KC);
+      const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
+      const int buf = seg & 1;
+      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float acc[NV][BN];
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int j = 0; j < BN / 16; ++j)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * NV * BN + v * BN + j * 16,
+                    &acc[v][j * 16]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      u += c1 - c0;
+      if (c0 == 0 && c1 == KC) {
+        finish_tile(acc, t, 0, a.M);
+      } else if (EPI == kEpiArgmax) {
+        // lm_head: a split tile has two contributors (each CTA streams many
+        // tiles); the later one reads the other's partial and finishes it.
+        const int slot = (t == first_tile) ? 0 : 1;
+        put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
+        epi_sync();
+        const int bf = owner_of((long long)t * KC, U, G);
+        const int bl = owner_of((long long)t * KC + KC - 1, U, G);
+        if (threadIdx.x == 64) {
+          __threadfence();
+          s_last = (atomicAdd(&arrive[t], 1u) == static_cast<unsigned>(bl - bf));
+        }
+        epi_sync();
+        if (s_last) {
+          __threadfence();
+          auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
+          if (mq == 1) sum_partials<NV, BN, 1, 8 / NV>(acc, a.partials, row, bf, bl, mq, slot_of);
+          else sum_partials<NV, BN, BN / 4, 4>(acc, a.partials, row, bf, bl, mq, slot_of);
+          if (threadIdx.x == 64) arrive[t] = 0u;
+          finish_tile(acc, t, 0, a.M);
+        }
+      } else {
+        const int slot = (t == first_tile) ? 0 : 1;
+        put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
+        if (slot == 0) split_first = t; else split_last = t;
+        epi_sync();
+        if (threadIdx.x == 64) {
+          __threadfence();
+          atomicAdd(&arrive[t], 1u);
+        }
+      }
+    }
+    for (int slot = 0; slot < 2 && ok; ++slot) {
+      const int t = slot == 0 ? split_first : split_last;
+      if (t < 0) continue;
+      const int bf = owner_of((long long)t * KC, U, G);
+      const int bl = owner_of((long long)t * KC + KC - 1, U, G);
+      const int nc = bl - bf + 1, k = b - bf;
+      if (k < mq) {
+        if (threadIdx.x == 64) {
+          unsigned spins = 0;
+          while (ld_volatile_u32(&arrive[t]) < static_cast<unsigned>(nc)) {
+            if (++spins > (1u << 24)) { atomicOr(a.err, 8); break; }
+            __nanosleep(64);
+          }
+          __threadfence();
+        }
+        epi_sync();
+        auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
+        for (int g = k; g < mq; g += nc) {
+          float acc[NV][BN];
+          sum_group<NV, BN, 8 / NV>(acc, a.partials, row, g, bf, bl, slot_of);
+          finish_tile(acc, t, 4 * g, 4 * g + 4 < a.M ? 4 * g + 4 : a.M);
+        }
+        epi_sync();
+      }
+      if (threadIdx.x == 64 && atomicAdd(&depart[t], 1u) == static_cast<unsigned>(nc - 1)) {
+        arrive[t] = 0u;                           // every contributor is past its wait
+        depart[t] = 0u;
       }
     }
     if (!ok) atomicOr(a.err, 4);
@@ -598,8 +649,9 @@ cudaError_t launch_tc_wide(const TcWideArgs& a, int grid, cudaStream_t st) {
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st) {
   // At least kMinUnits (64-wide K chunks of a 128-row tile, 16 KB of weights
   // each) per CTA: a short GEMM then splits a tile over a few CTAs rather than
-  // a dozen, whose partial sums the last one would have to gather.
+  // a dozen.
   constexpr long long kMinUnits = 8;
+  if (a.tiles > kTileDepart) return cudaErrorInvalidValue;     // split-tile counters
   const long long U = (long long)a.tiles * a.kchunks;
   const long long want = (U + kMinUnits - 1) / kMinUnits;
   if (grid > want) grid = static_cast<int>(want);
