@@ -491,6 +491,8 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
   at.head_ctr = c->attn_ctr;
+  at.err = c->tc_err;
+  at.sms = c->num_sms;
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
@@ -800,7 +802,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
-      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)c->nkv * 4,
+      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)2 * c->nkv * 4,
       (size_t)cfg->n_layers * sizeof(void*)};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);

@@ -193,7 +193,11 @@ struct AttnArgs {
   int max_ctx;                 // most context keys any round can see
   float* partial;              // scratch [nkv][nsplit][rows*G][hd + 2]
   void* out; int ldo;          // [rows, nq, hd]
-  unsigned* head_ctr;          // [nkv] tickets, zero between launches (tensor-core path)
+  unsigned* head_ctr;          // [2 * nkv] arrivals then departures per kv head, zero
+                               // between launches (tensor-core path)
+  int* err;                    // bounded-wait timeouts are reported here (bit 16)
+  int sms;                     // SMs: the split merge joins the attention kernel when the
+                               // grid fits one CTA per SM
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.
