@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 // paired-chunk stages.
 template <int BN, int EPI>
 constexpr int stages_for() {
-  return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : EPI == kEpiSwiglu ? (BN == 16 ? 3 : 2) : (BN == 16 ? 3 : 2);
+  return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : EPI == kEpiSwiglu ? (BN == 16 ? 3 : 2) : (BN == 16 ? 4 : 2);
 }
 template <int BN, int EPI>
 constexpr int pairs_for() { return 2; }
