@@ -515,10 +515,11 @@ cudaError_t launch_attention_mma(const AttnArgs& a, unsigned*, cudaStream_t st) 
   const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
   dim3 grid(nsplit, a.nkv);
   const int Qn = a.rows * (a.nq / a.nkv);
-  if (Qn <= kTileQ) {
-    // Merging inside the kernel pays from two query tiles on (measured: -12 us
-    // per draft at 64 queries per kv head, +5 us at 16).
-    const int merge = (Qn > 16 && a.head_ctr && a.err && nsplit * a.nkv <= a.sms) ? 1 : 0;
+  // The 87 KB tile kernel with the split merge folded in pays from two query
+  // tiles on (A/B on one GB300: -12 us per draft at 64 queries per kv head);
+  // at one tile the 8-warp key split with its separate merge is faster (-6 us).
+  if (Qn > 16 && Qn <= kTileQ) {
+    const int merge = (a.head_ctr && a.err && nsplit * a.nkv <= a.sms) ? 1 : 0;
     cudaError_t e = launch_pdl(attn_tile_kernel, grid, dim3(kWarps * 32), sizeof(TileSmem), st, a, nsplit, merge);
     if (e != cudaSuccess || merge) return e;
   } else {
