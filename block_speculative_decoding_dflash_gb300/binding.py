@@ -107,6 +107,8 @@ _sig("dflash_set_option", ctypes.c_int, _vp, _i32, _i64)
 _sig("dflash_get_option", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_draft_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
+_sig("dflash_ingest_gemm_timing", ctypes.c_int, _vp, _i32)
+_sig("dflash_ingest_gemm_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float))
 _sig("dflash_lm_head_elapsed_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float))
 _sig("dflash_synth_target", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
      _vp, _vp, _vp)
@@ -416,6 +418,15 @@ class DFlashContext:
 
     def lm_head_timing(self, enable: bool):
         self._check(lib.dflash_lm_head_timing(self.h, 1 if enable else 0))
+
+    def ingest_gemm_timing(self, enable: bool):
+        self._check(lib.dflash_ingest_gemm_timing(self.h, 1 if enable else 0))
+
+    def ingest_gemm_ms(self):
+        """(fc GEMM ms, K|V GEMM ms) of the last timed ingest chunk."""
+        a, b = ctypes.c_float(), ctypes.c_float()
+        self._check(lib.dflash_ingest_gemm_ms(self.h, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
 
     def lm_head_elapsed_ms(self) -> float:
         o = ctypes.c_float()

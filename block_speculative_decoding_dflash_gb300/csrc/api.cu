@@ -213,6 +213,9 @@ struct dflash_ctx {
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
+  cudaEvent_t ing_ev[4] = {nullptr, nullptr, nullptr, nullptr};   // fc GEMM, K/V GEMM brackets
+  bool ing_timing = false;
+  bool ing_recorded = false;
   std::string err;
 };
 
@@ -411,10 +414,17 @@ int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void*
   a.y = f; a.ldy = c->H; a.err = c->tc_err;
   if (!tc_encode_map(&a.x_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, 128))
     return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the context rows");
+  const unsigned evf = c->capturing ? cudaEventRecordExternal : 0;
+  if (c->ing_timing) CK(c->err, cudaEventRecordWithFlags(c->ing_ev[0], st, evf));
   CK(c->err, launch_tc_wide(a, c->num_sms, st));
+  if (c->ing_timing) CK(c->err, cudaEventRecordWithFlags(c->ing_ev[1], st, evf));
   CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
+  if (c->ing_timing) CK(c->err, cudaEventRecordWithFlags(c->ing_ev[2], st, evf));
   const int L = c->cfg.n_layers;
   const int ldkv = L * 2 * c->kvdim;
+  // head_dim 128 with whole 256-column tiles per K or V: the wide GEMM's
+  // epilogue does the k-norm + RoPE and the ring stores itself.
+  const bool to_ring = c->hd == 128 && c->kvdim % 256 == 0;
   for (int l0 = 0; l0 < L; l0 += kTcMaxSeg / 2) {
     const int nl = L - l0 < kTcMaxSeg / 2 ? L - l0 : kTcMaxSeg / 2;
     TcWideArgs b{};
@@ -428,11 +438,21 @@ int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void*
     b.y = static_cast<char*>(kv) + (size_t)l0 * 2 * c->kvdim * c->esz;
     b.ldy = ldkv;
     b.err = c->tc_err;
+    if (to_ring) {
+      b.ring_k = c->ring->k; b.ring_v = c->ring->v; b.cap = c->ring->cap; b.pos0 = pos_host;
+      b.ring = c->ring->st; b.rope = rope; b.kgain = c->kgain_dev;
+      b.nkv = c->nkv; b.kvdim = c->kvdim; b.l0 = l0; b.append_only = c->ring->append_only;
+      b.neox = c->cfg.rope_neox; b.eps = c->cfg.rms_eps;
+    }
     if (!tc_encode_map(&b.x_map, cn, c->H, rows, (uint64_t)c->H * 2, 64, 128))
       return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the normed context rows");
     CK(c->err, launch_tc_wide(b, c->num_sms, st));
   }
-  for (int l = 0; l < L; ++l) {
+  if (c->ing_timing) {
+    CK(c->err, cudaEventRecordWithFlags(c->ing_ev[3], st, evf));
+    c->ing_recorded = true;
+  }
+  for (int l = 0; l < L && !to_ring; ++l) {
     const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
     CK(c->err, launch_kv_to_ring(dt, static_cast<char*>(kv) + (size_t)l * 2 * c->kvdim * c->esz, ldkv,
                                  rows, c->nkv, c->hd, LW(c, l, kKNorm), c->cfg.rms_eps, rope,
@@ -734,6 +754,8 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   cudaFree(ctx->mega_phases);
   cudaFree(ctx->mega_done);
   cudaFree(ctx->mega_trace);
+  for (auto& ev : ctx->ing_ev)
+    if (ev) cudaEventDestroy(ev);
   for (auto& ev : ctx->lm_ev)
     if (ev) cudaEventDestroy(ev);
   delete ctx;
@@ -864,6 +886,10 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       (e = init_attention_attrs(c->hd)) != cudaSuccess ||
       (e = cudaEventCreate(&c->lm_ev[0])) != cudaSuccess ||
       (e = cudaEventCreate(&c->lm_ev[1])) != cudaSuccess ||
+      (e = cudaEventCreate(&c->ing_ev[0])) != cudaSuccess ||
+      (e = cudaEventCreate(&c->ing_ev[1])) != cudaSuccess ||
+      (e = cudaEventCreate(&c->ing_ev[2])) != cudaSuccess ||
+      (e = cudaEventCreate(&c->ing_ev[3])) != cudaSuccess ||
       (e = cudaStreamSynchronize(c->stream)) != cudaSuccess) {
     dflash_ctx_destroy(c);
     return cuda_fail(err, e, "context initialisation");
@@ -1337,6 +1363,21 @@ int dflash_lm_head_elapsed_ms(dflash_ctx* c, float* ms) {
   if (!c->lm_recorded) return fail(c->err, DFLASH_ESTATE, "lm_head timing events never recorded");
   CK(c->err, cudaEventSynchronize(c->lm_ev[1]));
   CK(c->err, cudaEventElapsedTime(ms, c->lm_ev[0], c->lm_ev[1]));
+  return DFLASH_OK;
+}
+
+int dflash_ingest_gemm_timing(dflash_ctx* c, int32_t enable) {
+  if (!c) return DFLASH_EINVAL;
+  c->ing_timing = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_ingest_gemm_ms(dflash_ctx* c, float* fc_ms, float* kv_ms) {
+  if (!c || !fc_ms || !kv_ms) return DFLASH_EINVAL;
+  if (!c->ing_recorded) return fail(c->err, DFLASH_ESTATE, "ingest GEMM timing events never recorded");
+  CK(c->err, cudaEventSynchronize(c->ing_ev[3]));
+  CK(c->err, cudaEventElapsedTime(fc_ms, c->ing_ev[0], c->ing_ev[1]));
+  CK(c->err, cudaEventElapsedTime(kv_ms, c->ing_ev[2], c->ing_ev[3]));
   return DFLASH_OK;
 }
 

@@ -85,6 +85,17 @@ struct TcWideArgs {
   int M, N, K;
   void* y; int ldy;
   int* err;
+  // K/V into the ring instead of y (ring_k != NULL): the columns are layers
+  // l0, l0+1, ... of [K heads | V heads] (kvdim each, kvdim % 256 == 0,
+  // head_dim 128); row m is position pos0 + m; K heads get the per-head
+  // RMSNorm (kgain[layer]) and RoPE (rope[m][64]) before the ring store.
+  void* ring_k; void* ring_v;      // [L][nkv][cap][128]
+  long long cap, pos0;
+  RingState* ring;
+  const float2* rope;
+  const void* const* kgain;
+  int nkv, kvdim, l0, append_only, neox;
+  float eps;
 };
 cudaError_t launch_tc_wide(const TcWideArgs& a, int grid, cudaStream_t st);
 

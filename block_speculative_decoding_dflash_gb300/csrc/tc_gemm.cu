@@ -557,6 +557,106 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_wide_kernel(const __grid_
       if (!ok) break;
       tc_fence_after();
       const int m = m0 + row;
+      if (a.ring_k) {
+        // Two whole heads of one layer's K or V: the thread holds its row's
+        // 128 values of each head, so the head norm and RoPE are thread-local.
+        const int per_layer = 2 * a.kvdim;
+        const int cin = n0 % per_layer;
+        const bool isv = cin >= a.kvdim;
+        const int layer = a.l0 + n0 / per_layer;
+        const int hbase = (cin % a.kvdim) / 128;
+        const long long pos = a.pos0 + m;
+        bool store = m < a.M;
+        if (store && a.append_only && pos - a.ring->base >= a.cap) {
+          atomicOr(&a.ring->error, kErrFull);
+          store = false;
+        }
+        const long long slot = ring_slot(pos, a.cap);
+        const bf16* g = reinterpret_cast<const bf16*>(a.kgain[layer]);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kWideN;
+        auto put16 = [&](bf16* dst, const float* v) {
+          uint4 pk[2];
+          uint32_t* w32 = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w32[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          reinterpret_cast<uint4*>(dst)[0] = pk[0];
+          reinterpret_cast<uint4*>(dst)[1] = pk[1];
+        };
+        for (int hh = 0; hh < kWideN / 128; ++hh) {
+          const uint32_t th = tl + hh * 128;
+          bf16* dst = reinterpret_cast<bf16*>(isv ? a.ring_v : a.ring_k) +
+                      (((size_t)layer * a.nkv + hbase + hh) * a.cap + slot) * 128;
+          if (isv) {
+            for (int j = 0; j < 8; ++j) {
+              float v[16];
+              tmem_ld16(th + j * 16, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = rnd_bf(v[e]);
+              if (store) put16(dst + j * 16, v);
+            }
+            continue;
+          }
+          // K head: the values rounded as stored, their 1/rms, then per piece
+          // the gain and RoPE (neox pairs dims i and i + 64: pieces j, j + 4).
+          float ss = 0.f;
+          for (int j = 0; j < 8; ++j) {
+            float v[16];
+            tmem_ld16(th + j * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) { const float r = rnd_bf(v[e]); ss = fmaf(r, r, ss); }
+          }
+          const float inv = rsqrtf(ss / 128.0f + a.eps);
+          const float2* rr = a.rope + (size_t)(m < a.M ? m : 0) * 64;
+          auto scale = [&](float* v, int d0) {
+            float gv[16];
+            load8(g + d0, gv);
+            load8(g + d0 + 8, gv + 8);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = rnd_bf(v[e]) * inv * gv[e];
+          };
+          if (a.neox) {
+            for (int j = 0; j < 4; ++j) {
+              float lo[16], hi[16];
+              tmem_ld16(th + j * 16, lo);
+              tmem_ld16(th + (j + 4) * 16, hi);
+              tmem_ld_wait();
+              scale(lo, j * 16);
+              scale(hi, (j + 4) * 16);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float2 cs = rr[j * 16 + e];
+                const float x0 = lo[e], x1 = hi[e];
+                lo[e] = x0 * cs.x - x1 * cs.y;
+                hi[e] = x0 * cs.y + x1 * cs.x;
+              }
+              if (store) { put16(dst + j * 16, lo); put16(dst + (j + 4) * 16, hi); }
+            }
+          } else {
+            for (int j = 0; j < 8; ++j) {
+              float v[16];
+              tmem_ld16(th + j * 16, v);
+              tmem_ld_wait();
+              scale(v, j * 16);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float2 cs = rr[j * 8 + e];
+                const float x0 = v[2 * e], x1 = v[2 * e + 1];
+                v[2 * e] = x0 * cs.x - x1 * cs.y;
+                v[2 * e + 1] = x0 * cs.y + x1 * cs.x;
+              }
+              if (store) put16(dst + j * 16, v);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
       for (int j = 0; j < kWideN / 16; ++j) {
         float v[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kWideN + j * 16, v);

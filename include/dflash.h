@@ -342,6 +342,15 @@ int dflash_lm_head_timing(dflash_ctx* ctx, int32_t enable);
  * event). ESTATE if they were never recorded. */
 int dflash_lm_head_elapsed_ms(dflash_ctx* ctx, float* ms_host);
 
+/* When enabled, dflash_ingest_context brackets the tensor-core context GEMMs
+ * of each ingest chunk (encoder.fc over the chunk's rows; the K|V projections
+ * of every layer) with context-owned CUDA events (event nodes when captured).
+ * Applies to the 128 x 256 tensor-core ingest path only. */
+int dflash_ingest_gemm_timing(dflash_ctx* ctx, int32_t enable);
+/* Milliseconds of the fc GEMM and of the K|V GEMM(s) of the last recorded
+ * chunk (syncs on the last event). ESTATE if never recorded. */
+int dflash_ingest_gemm_ms(dflash_ctx* ctx, float* fc_ms_host, float* kv_ms_host);
+
 /* ---- verify without allocation ------------------------------------------------ */
 
 /* The greedy verify of dflash_verify_accept for callers that cannot allocate
