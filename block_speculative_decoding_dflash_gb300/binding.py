@@ -63,7 +63,7 @@ class RoundStateC(ctypes.Structure):
 
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE, OPT_DRAFT_TRACE = 1, 2, 3
+OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE, OPT_DRAFT_TRACE, OPT_KERNEL_TRACE = 1, 2, 3, 4
 
 
 def _sig(name, res, *args):
@@ -106,6 +106,7 @@ _sig("dflash_graph_kernel_count", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_set_option", ctypes.c_int, _vp, _i32, _i64)
 _sig("dflash_get_option", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_draft_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
+_sig("dflash_kernel_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.c_char_p, _i64)
 _sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
 _sig("dflash_ingest_gemm_timing", ctypes.c_int, _vp, _i32)
 _sig("dflash_ingest_gemm_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float))
@@ -415,6 +416,20 @@ class DFlashContext:
         self._check(lib.dflash_draft_trace(self.h, out.ctypes.data, out.size, ctypes.byref(r),
                                            ctypes.byref(c)))
         return out
+
+    def kernel_trace(self, enable: bool):
+        """Stamp each launch of the per-operation draft (see kernel_trace_read)."""
+        self._check(lib.dflash_set_option(self.h, OPT_KERNEL_TRACE, 1 if enable else 0))
+
+    def kernel_trace_read(self):
+        """[(name, entry_ns, wait_return_ns, exit_ns)] of the last traced draft."""
+        n = _i32()
+        buf = np.zeros(3 * 256, dtype=np.uint64)
+        names = ctypes.create_string_buffer(1 << 14)
+        self._check(lib.dflash_kernel_trace(self.h, buf.ctypes.data, buf.size, ctypes.byref(n), names,
+                                            len(names)))
+        labels = names.value.decode().split("\n")
+        return [(labels[i], int(buf[3 * i]), int(buf[3 * i + 1]), int(buf[3 * i + 2])) for i in range(n.value)]
 
     def lm_head_timing(self, enable: bool):
         self._check(lib.dflash_lm_head_timing(self.h, 1 if enable else 0))

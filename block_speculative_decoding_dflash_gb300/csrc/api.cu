@@ -213,6 +213,10 @@ struct dflash_ctx {
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
+  unsigned long long* ktr = nullptr;           // DFLASH_OPT_KERNEL_TRACE: [3][kKTraceSlots]
+  bool ktr_on = false;
+  int ktr_n = 0;
+  std::vector<std::string> ktr_names;
   cudaEvent_t ing_ev[4] = {nullptr, nullptr, nullptr, nullptr};   // fc GEMM, K/V GEMM brackets
   bool ing_timing = false;
   bool ing_recorded = false;
@@ -304,6 +308,15 @@ TcGemmArgs tc_args(dflash_ctx* c, int M, int N, int K, int epi) {
   a.tile_ctr = c->tc_tiles;
   a.err = c->tc_err;
   return a;
+}
+
+// Next slot(s) of the per-launch kernel trace, or none when tracing is off.
+KTrace ktrace_slot(dflash_ctx* c, const std::string& name, int nslots = 1) {
+  if (!c->ktr_on || !c->ktr || c->ktr_n + nslots > kKTraceSlots) return KTrace{nullptr, 0};
+  const KTrace t{c->ktr, c->ktr_n};
+  for (int i = 0; i < nslots; ++i) c->ktr_names.push_back(i ? name + "." + std::to_string(i) : name);
+  c->ktr_n += nslots;
+  return t;
 }
 
 void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMap*, int>> segs) {
@@ -467,7 +480,9 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   const int dt = c->dt;
   cudaStream_t st = c->stream;
   const float eps = c->cfg.rms_eps;
-  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st));
+  const std::string ln = "L" + std::to_string(l) + ".";
+  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st,
+                            ktrace_slot(c, ln + "in_norm")));
   const bool tc = c->use_tc && rows <= 32;
   const int bi = bn_index(rows);
   const bool fused_qk = tc && c->hd == 128;
@@ -479,6 +494,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     t.nq_tiles = c->nq; t.nkv = c->nkv;
     t.qn = LW(c, l, kQNorm); t.kn = LW(c, l, kKNorm);
     t.rope = c->rope; t.neox = c->cfg.rope_neox; t.eps = eps;
+    t.trace = ktrace_slot(c, ln + "qkv");
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
@@ -513,30 +529,35 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.head_ctr = c->attn_ctr;
   at.err = c->tc_err;
   at.sms = c->num_sms;
+  at.trace = ktrace_slot(c, ln + "attn", 3);
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
     tc_segments(t, {{&c->lmaps[l].wo, c->H}});
     t.b_map = c->attn_map[bi];
     t.y = c->x; t.ldy = c->H; t.r = c->x; t.ldr = c->H;
+    t.trace = ktrace_slot(c, ln + "o");
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
     o.w[0] = LW(c, l, kWo); o.epi = kEpiResid; o.r = c->x; o.ldr = c->H;
     CK(c->err, launch_linear_rows(dt, o, st));
   }
-  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st));
+  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st,
+                            ktrace_slot(c, ln + "post_norm")));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->I, c->H, kEpiSwiglu);
     tc_segments(t, {{&c->lmaps[l].wg, c->I}});
     t.a2_map = c->lmaps[l].wu;
     t.b_map = c->xn_map[bi];
     t.y = c->sbuf; t.ldy = c->I;
+    t.trace = ktrace_slot(c, ln + "gate_up");
     CK(c->err, tc_run(c, t));
     TcGemmArgs d = tc_args(c, rows, c->H, c->I, kEpiResid);
     tc_segments(d, {{&c->lmaps[l].wd, c->H}});
     d.b_map = c->sbuf_map[bi];
     d.y = c->x; d.ldy = c->H; d.r = c->x; d.ldr = c->H;
+    d.trace = ktrace_slot(c, ln + "down");
     CK(c->err, tc_run(c, d));
   } else {
     LinearArgs g = lin_args(c->xn, c->H, c->sbuf, c->I, rows, c->I, c->H);
@@ -754,6 +775,7 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   cudaFree(ctx->mega_phases);
   cudaFree(ctx->mega_done);
   cudaFree(ctx->mega_trace);
+  cudaFree(ctx->ktr);
   for (auto& ev : ctx->ing_ev)
     if (ev) cudaEventDestroy(ev);
   for (auto& ev : ctx->lm_ev)
@@ -1003,6 +1025,12 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     c->last_draft_block = block;
     return DFLASH_OK;
   }
+  if (c->ktr_on && c->ktr) {
+    c->ktr_n = 0;
+    c->ktr_names.clear();
+    CK(c->err, cudaMemsetAsync(c->ktr, 0xFF, sizeof(unsigned long long) * kKTraceSlots, st));
+    CK(c->err, cudaMemsetAsync(c->ktr + kKTraceSlots, 0, 2 * sizeof(unsigned long long) * kKTraceSlots, st));
+  }
   CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rows, c->x,
                                 c->ring->st, c->inv_freq, c->half, rows, c->rope, st));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
@@ -1010,7 +1038,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     if (rc) return rc;
   }
   CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
-                            c->cfg.rms_eps, st));
+                            c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
   LmHeadArgs lm{};
   lm.x = static_cast<char*>(c->xf) + (size_t)read0 * c->H * c->esz;
   lm.ldx = c->H;
@@ -1032,6 +1060,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     t.softcap = c->cfg.softcap;
     t.ids = lm.ids; t.ids2 = lm.ids2; t.maxv = lm.maxv;
     t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
+    t.trace = ktrace_slot(c, "lm_head");
     CK(c->err, tc_run(c, t));
   } else {
     CK(c->err, launch_lmhead_argmax(dt, lm, st));
@@ -1315,6 +1344,12 @@ int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
     c->draft_fused_on = value != 0;
     return DFLASH_OK;
   }
+  if (option == DFLASH_OPT_KERNEL_TRACE) {
+    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
+    if (value && !c->ktr) CK(c->err, cudaMalloc(&c->ktr, 3 * sizeof(unsigned long long) * kKTraceSlots));
+    c->ktr_on = value != 0;
+    return DFLASH_OK;
+  }
   if (option == DFLASH_OPT_DRAFT_TRACE) {
     if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
     if (value && !c->draft_fused_ok) return fail(c->err, DFLASH_ESTATE, "no persistent draft kernel");
@@ -1327,6 +1362,26 @@ int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
     return DFLASH_OK;
   }
   return fail(c->err, DFLASH_EINVAL, "unknown or read-only option %d", option);
+}
+
+int dflash_kernel_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t* count, char* names,
+                        int64_t names_cap) {
+  if (!c) return DFLASH_EINVAL;
+  if (!count) return fail(c->err, DFLASH_EINVAL, "count is NULL");
+  if (!c->ktr) return fail(c->err, DFLASH_ESTATE, "kernel tracing was never enabled");
+  *count = c->ktr_n;
+  std::string joined;
+  for (const auto& nm : c->ktr_names) joined += nm + "\n";
+  if (!out || capacity < 3LL * c->ktr_n || !names || names_cap < (int64_t)joined.size() + 1)
+    return fail(c->err, DFLASH_ERANGE, "need %d stamps and %zu name bytes", 3 * c->ktr_n, joined.size() + 1);
+  std::vector<unsigned long long> h(3 * kKTraceSlots);
+  CK(c->err, cudaMemcpyAsync(h.data(), c->ktr, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost,
+                             c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
+  for (int i = 0; i < c->ktr_n; ++i)
+    for (int k = 0; k < 3; ++k) out[3 * i + k] = h[(size_t)k * kKTraceSlots + i];
+  std::memcpy(names, joined.c_str(), joined.size() + 1);
+  return DFLASH_OK;
 }
 
 int dflash_draft_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t* rows, int32_t* cols) {
@@ -1348,6 +1403,7 @@ int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
   if (!value) return fail(c->err, DFLASH_EINVAL, "value is NULL");
   if (option == DFLASH_OPT_FUSED_DRAFT) { *value = c->draft_fused_on ? 1 : 0; return DFLASH_OK; }
   if (option == DFLASH_OPT_FUSED_DRAFT_AVAILABLE) { *value = c->draft_fused_ok ? 1 : 0; return DFLASH_OK; }
+  if (option == DFLASH_OPT_KERNEL_TRACE) { *value = c->ktr_on ? 1 : 0; return DFLASH_OK; }
   if (option == DFLASH_OPT_DRAFT_TRACE) { *value = c->mega_trace_on ? 1 : 0; return DFLASH_OK; }
   return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }

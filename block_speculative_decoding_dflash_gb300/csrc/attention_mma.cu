@@ -43,7 +43,9 @@ struct MmaSmem {
 };
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
   const int s = blockIdx.x, g = blockIdx.y;
@@ -216,6 +218,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
     }
     __syncthreads();
   }
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 2);
 }
 
 // ---------------------------------------------------------------------------
@@ -228,6 +231,14 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
 // their weights.
 // ---------------------------------------------------------------------------
 constexpr int kTileQ = 64;
+
+// Phase stamps of the tile kernel in the two trace slots after its own
+// (latest CTA; allotted only when the split merge is folded in): slot + 1 gets
+// [1] loads landed, [2] per-warp attention done; slot + 2 gets [1] partials
+// written, [2] the head's splits all present.
+__device__ __forceinline__ void attn_phase(const KTrace& t, int slot_off, int k) {
+  if (t.p && threadIdx.x == 0) ktrace_mark(KTrace{t.p, t.slot + slot_off}, k);
+}
 
 // The split merge inside the attention kernel, for grids of at most one CTA
 // per SM (all resident, so waiting on the other splits of a head cannot
@@ -252,6 +263,7 @@ __device__ __noinline__ void merge_splits(const AttnArgs& a, int nsplit, int s, 
         __nanosleep(64);
       }
       __threadfence();
+      if (a.trace.p) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 2);
     }
     s_ok = ok;
   }
@@ -288,7 +300,9 @@ struct TileSmem {
 static_assert(sizeof(TileSmem) <= 90 * 1024, "attention tile too large to share an SM with a GEMM CTA");
 
 __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int nsplit, int merge) {
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TileSmem& S = *reinterpret_cast<TileSmem*>(smem_raw);
   const int s = blockIdx.x, g = blockIdx.y;
@@ -319,6 +333,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
       part[e] = d == kHd ? -INFINITY : 0.f;
     }
     if (merge) merge_splits(a, nsplit, s, g, G, Qn);
+    if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
     return;
   }
   for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
@@ -350,6 +365,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
   }
   cp_async_wait_all();
   __syncthreads();
+  if (merge) attn_phase(a.trace, 1, 1);
 
   const int kg = nqt == 1 ? 8 : nqt == 2 ? 4 : 2;   // key groups per query tile
   const int span = kKeys / kg;                        // keys per warp
@@ -370,17 +386,22 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
       qok[hr] = qi < Qn;
       qrel[hr] = qok[hr] ? qi / G : 0;
     }
+    // the warp's 16 queries as MMA A fragments, loaded once for all its keys
+    uint32_t qa[kHd / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < kHd / 16; ++ks)
+      ldsm_x4(&S.q[qt * 16 + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], qa[ks][0], qa[ks][1],
+              qa[ks][2], qa[ks][3]);
     for (int kb0 = gk * span; kb0 < (gk + 1) * span; kb0 += 16) {
       const int kj0 = j0 + kb0;
       if (kj0 >= nk) break;
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int ks = 0; ks < kHd / 16; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(&S.q[qt * 16 + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
+        uint32_t b0, b1, b2, b3;
         ldsm_x4(&S.kv.k[kb0 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
-        mma16816(sc[0], a0, a1, a2, a3, b0, b1);
-        mma16816(sc[1], a0, a1, a2, a3, b2, b3);
+        mma16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
       }
       float mb[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -436,6 +457,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
     }
   }
   __syncthreads();                                    // K and V are no longer read
+  if (merge) attn_phase(a.trace, 1, 2);
   if (busy) {
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt)
@@ -478,19 +500,28 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
     *reinterpret_cast<float4*>(out + d4) = acc;
     if (d4 == 0) { out[kHd] = S.mg.M[qi]; out[kHd + 1] = S.mg.L[qi]; }
   }
-  if (merge) merge_splits(a, nsplit, s, g, G, Qn);
+  if (merge) {
+    __syncthreads();
+    attn_phase(a.trace, 2, 1);
+    merge_splits(a, nsplit, s, g, G, Qn);
+  }
+  if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
 }
 
 // One warp per (query, kv head): merge the splits' partials in split order.
 __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int nsplit) {
+  const KTrace tr{a.trace.p, a.trace.slot + 1};
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
   const int Qn = a.rows * G;
   const int item = blockIdx.x * 4 + warp;
-  if (item >= a.nkv * Qn) return;
-  attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
-                    reinterpret_cast<bf16*>(a.out), a.ldo, lane);
+  if (item < a.nkv * Qn)
+    attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
+                      reinterpret_cast<bf16*>(a.out), a.ldo, lane);
+  if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
 }
 
 }  // namespace

@@ -22,46 +22,44 @@ __host__ __device__ __forceinline__ int attn_splits(long long n) {
 }
 
 // One warp merges the first ns splits (layout stride nsplit) of query qi of kv
-// head g, in split order, and writes the normalised bf16 output row.
+// head g, in split order, and writes the normalised bf16 output row. Each
+// lane owns 4 output dims; the splits' maxima, sums and output slices of a
+// batch of up to 32 splits are requested together, so a merge of up to 32
+// splits is one round trip to L2.
 __device__ __forceinline__ void attn_combine_warp(const float* partial, int nsplit, int ns, int Qn,
                                                   int G, int g, int qi, bf16* out, int ldo,
                                                   int lane) {
+  constexpr int kB = 32;
   const size_t pstride = kAttnPartStride;
   const float* base = partial + (size_t)g * nsplit * Qn * pstride + (size_t)qi * pstride;
   const size_t sstride = (size_t)Qn * pstride;
-  float M = -INFINITY;
-  for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, __ldcg(base + sp * sstride + kAttnHd));
-  M = warp_max(M);
-  float L = 0.f;
-  for (int sp = lane; sp < ns; sp += 32) {
-    const float ms = __ldcg(base + sp * sstride + kAttnHd);
-    if (ms != -INFINITY) L += expf(ms - M) * __ldcg(base + sp * sstride + kAttnHd + 1);
-  }
-  L = warp_sum(L);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const int d4 = lane * 4;
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    const int sp_l = s0 + lane;
-    const float ms_l = sp_l < ns ? __ldcg(base + sp_l * sstride + kAttnHd) : -INFINITY;
-    const float f_l = ms_l == -INFINITY ? 0.f : expf(ms_l - M);
-    const int n = ns - s0 < 32 ? ns - s0 : 32;
-    int j = 0;
-    for (; j + 8 <= n; j += 8) {
-      float4 ov[8];
+  float M = -INFINITY, L = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0; s0 < ns; s0 += kB) {
+    const int n = ns - s0 < kB ? ns - s0 : kB;
+    // lane j < n holds split s0 + j's (max, sum); every lane its dims of all n
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml = __ldcg(reinterpret_cast<const float2*>(base + (s0 + lane) * sstride + kAttnHd));
+    float4 ov[kB];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        ov[u] = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j + u) * sstride + d4));
+    for (int j = 0; j < kB; ++j)
+      ov[j] = j < n ? __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + d4))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float Mb = warp_max(ml.x);
+    const float Mn = fmaxf(M, Mb);
+    // rescale what was merged so far to the new maximum
+    const float r = (M == -INFINITY) ? 0.f : expf(M - Mn);
+    L *= r;
+    acc[0] *= r; acc[1] *= r; acc[2] *= r; acc[3] *= r;
+    const float f_l = ml.x == -INFINITY ? 0.f : expf(ml.x - Mn);
+    L += warp_sum(f_l * ml.y);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float f = __shfl_sync(0xffffffffu, f_l, j + u);
-        acc[0] += f * ov[u].x; acc[1] += f * ov[u].y; acc[2] += f * ov[u].z; acc[3] += f * ov[u].w;
-      }
-    }
-    for (; j < n; ++j) {
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(base + (s0 + j) * sstride + d4));
+    for (int j = 0; j < kB; ++j) {
       const float f = __shfl_sync(0xffffffffu, f_l, j);
-      acc[0] += f * ov.x; acc[1] += f * ov.y; acc[2] += f * ov.z; acc[3] += f * ov.w;
+      acc[0] += f * ov[j].x; acc[1] += f * ov[j].y; acc[2] += f * ov[j].z; acc[3] += f * ov[j].w;
     }
+    M = Mn;
   }
   const float inv = 1.0f / L;
   bf16* dst = out + (size_t)(qi / G) * ldo + (size_t)(g * G + qi % G) * kAttnHd + d4;

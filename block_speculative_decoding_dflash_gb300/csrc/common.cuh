@@ -122,6 +122,27 @@ __device__ __forceinline__ long long ring_slot(long long pos, long long cap) {
   return pos % cap;
 }
 
+// Optional per-launch timeline (globaltimer, ns): a launch owns slot `slot` of
+// three arrays: [0] earliest CTA entry (min), [1] latest return from the
+// programmatic-dependency wait (max), [2] latest CTA exit (max).
+struct KTrace {
+  unsigned long long* p;   // [3][kTraceSlots] or NULL
+  int slot;
+};
+constexpr int kKTraceSlots = 256;
+__device__ __forceinline__ unsigned long long ktrace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Call from one thread per CTA.
+__device__ __forceinline__ void ktrace_mark(const KTrace& t, int k) {
+  if (!t.p) return;
+  unsigned long long* a = t.p + (size_t)k * kKTraceSlots + t.slot;
+  if (k == 0) atomicMin(a, ktrace_now());
+  else atomicMax(a, ktrace_now());
+}
+
 // (cos, sin) of pos * inv_freq[i]; the angle is formed in fp64 so that large
 // absolute positions keep their precision.
 __device__ __forceinline__ float2 rope_entry(const double* inv_freq, int i, long long pos) {

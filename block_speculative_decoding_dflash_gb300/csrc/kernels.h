@@ -73,6 +73,7 @@ struct TcGemmArgs {
   // kEpiQKV: rows [Q heads | K heads | V heads], q_norm / k_norm gains [128]
   int nq_tiles;
   const void* qn; const void* kn;
+  KTrace trace;
 };
 // Many-row tensor-core GEMM (context ingest): Y[m, n] = rnd(X W^T), X [M, K]
 // (box {64, 128}), W stacked segments of rows (box {64, 256}; segment row
@@ -177,7 +178,7 @@ cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState*
                               long long pos0, int rows, float2* rope, cudaStream_t st);
 cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g,
                            void* y, int ldy, int rows, int H, float eps,
-                           cudaStream_t st);
+                           cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
 // In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
 cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
                                   int heads, int hd, const void* g, float eps,
@@ -209,6 +210,7 @@ struct AttnArgs {
   int* err;                    // bounded-wait timeouts are reported here (bit 16)
   int sms;                     // SMs: the split merge joins the attention kernel when the
                                // grid fits one CTA per SM
+  KTrace trace;                // attention kernel; the separate merge kernel uses slot + 1
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.

@@ -55,8 +55,10 @@ __global__ void rope_table_kernel(const double* inv_freq, int half, const RingSt
 
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* x, int ldx, const T* g,
-                                                     T* y, int ldy, int H, float eps) {
+                                                     T* y, int ldy, int H, float eps, KTrace tr) {
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
   __shared__ float red[8];
   const int r = blockIdx.x;
   const T* xr = x + (size_t)r * ldx;
@@ -84,6 +86,10 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* x, int ldx, const
     load8(g + i, gv);
 #pragma unroll
     for (int e = 0; e < 8; ++e) yr[i + e] = from_f<T>(v[e] * inv * gv[e]);
+  }
+  if (tr.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(tr, 2);
   }
 }
 
@@ -300,14 +306,14 @@ cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState*
 }
 
 cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g, void* y,
-                           int ldy, int rows, int H, float eps, cudaStream_t st) {
+                           int ldy, int rows, int H, float eps, cudaStream_t st, KTrace tr) {
   if (rows <= 0) return cudaSuccess;
   if (dtype)
     launch_pdl(rmsnorm_kernel<bf16>, dim3(rows), dim3(256), 0, st, (const bf16*)x, ldx, (const bf16*)g, (bf16*)y,
-                                               ldy, H, eps);
+                                               ldy, H, eps, tr);
   else
     launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, st, (const float*)x, ldx, (const float*)g,
-                                                (float*)y, ldy, H, eps);
+                                                (float*)y, ldy, H, eps, tr);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     pdl_wait();
+    if (threadIdx.x == 64) ktrace_mark(a.trace, 1);
     const int q = warp & 3;                       // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;                // accumulator row = output feature in tile
     const int first_tile = static_cast<int>(u0 / KC);
@@ -412,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 2);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmem);

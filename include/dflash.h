@@ -311,6 +311,12 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
  * (allocates phases x CTAs x 96 bytes on first use; 0 stops it). The stamps
  * of the last launch are read with dflash_draft_trace. */
 #define DFLASH_OPT_DRAFT_TRACE 3
+/* DFLASH_OPT_KERNEL_TRACE: 1 makes dflash_draft_block on the one-kernel-per-
+ * operation path stamp the GPU's global timer (ns) for each traced launch:
+ * earliest CTA entry, latest return from the wait on the preceding kernel,
+ * latest CTA exit (allocates 6 KB on first use; 0 stops it). Read with
+ * dflash_kernel_trace. */
+#define DFLASH_OPT_KERNEL_TRACE 4
 /* EINVAL for an unknown option or value. Takes effect from the next call. */
 int dflash_set_option(dflash_ctx* ctx, int32_t option, int64_t value);
 int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
@@ -330,6 +336,13 @@ int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
  * attention, split merge, O, gate/up, down, then the lm_head. */
 int dflash_draft_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity,
                        int32_t* rows, int32_t* cols);
+/* The kernel trace of the last traced dflash_draft_block: count launches,
+ * out_host [count][3] stamps (entry, wait return, exit) and names_host their
+ * newline-separated names (e.g. "L0.qkv"). Syncs the context's stream.
+ * ERANGE if out_host / names_host are NULL or too small (count is still
+ * set); ESTATE if tracing was never enabled. */
+int dflash_kernel_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity, int32_t* count,
+                        char* names_host, int64_t names_capacity);
 
 /* ---- measurement ------------------------------------------------------------- */
 
