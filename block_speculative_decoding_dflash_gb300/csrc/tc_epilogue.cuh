@@ -18,34 +18,40 @@ __device__ __forceinline__ void epi_sync() {
 }
 
 // Per-head RMSNorm over a 128-row tile (head_dim 128: one dim per epilogue
-// thread) followed by RoPE, for every block row m < M of the tile's BN
-// columns; the value is normalised in fp32 and rotated before the single
-// rounding the caller applies. All 128 epilogue threads must call it.
+// thread) followed by RoPE, for the block rows m in [m0, m1) of the tile's
+// BN columns (m1 <= M; the bounds are the same for all threads); the value is
+// normalised in fp32 and rotated before the single rounding the caller
+// applies. All 128 epilogue threads must call it.
 template <int BN>
 __device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const float2* rope, int M,
                                                     int neox, float eps, int row, int lane, int q,
-                                                    float (*ss_sm)[BN], float* x_sm) {
+                                                    float (*ss_sm)[BN], float* x_sm, int m0 = 0,
+                                                    int m1 = BN) {
+  if (m1 > M) m1 = M;
 #pragma unroll
   for (int m = 0; m < BN; ++m) {
+    if (m < m0 || m >= m1) continue;
     const float ss = warp_sum(val[m] * val[m]);
     if (lane == 0) ss_sm[q][m] = ss;
   }
   epi_sync();
 #pragma unroll
   for (int m = 0; m < BN; ++m) {
+    if (m < m0 || m >= m1) continue;
     const float ss = ss_sm[0][m] + ss_sm[1][m] + ss_sm[2][m] + ss_sm[3][m];
     val[m] = val[m] * rsqrtf(ss / 128.0f + eps) * g;
   }
   if (neox) {
 #pragma unroll
-    for (int m = 0; m < BN; ++m) x_sm[row * BN + m] = val[m];
+    for (int m = 0; m < BN; ++m)
+      if (m >= m0 && m < m1) x_sm[row * BN + m] = val[m];
     epi_sync();
     const int i = row & 63;
     const bool lo = row < 64;
     const int partner = lo ? row + 64 : row - 64;
 #pragma unroll
     for (int m = 0; m < BN; ++m) {
-      if (m < M) {
+      if (m >= m0 && m < m1) {
         const float2 cs = rope[m * 64 + i];
         const float other = x_sm[partner * BN + m];
         val[m] = lo ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
@@ -57,8 +63,9 @@ __device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const f
     const bool ev = (row & 1) == 0;
 #pragma unroll
     for (int m = 0; m < BN; ++m) {
+      if (m < m0 || m >= m1) continue;
       const float other = __shfl_xor_sync(0xffffffffu, val[m], 1);
-      if (m < M) {
+      {
         const float2 cs = rope[m * 64 + i];
         val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
       }

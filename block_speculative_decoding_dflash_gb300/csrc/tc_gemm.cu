@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         const bool isk = !isq && t < a.nq_tiles + a.nkv;
         if (isq || isk) {
           const float g = __bfloat162float(reinterpret_cast<const bf16*>(isq ? a.qn : a.kn)[row]);
-          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x);
+          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
         }
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
         if (!isv) {
           const float g = __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[layer])[row]);
-          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x);
+          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
         }
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
