@@ -350,13 +350,15 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
     if (!tc_encode_map(&t.b_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, bn_of(rows)))
       return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the residual rows");
     t.y = f; t.ldy = c->H;
+    if (use_dev) t.trace = ktrace_slot(c, "append.fc");
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
     a.w[0] = c->fc;
     CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
   }
-  CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st));
+  CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st,
+                            use_dev ? ktrace_slot(c, "append.hidden_norm") : KTrace{nullptr, 0}));
   if (tc && c->hd == 128) {
     // One GEMM per group of up to five layers over [Wk_l | Wv_l ...]; its
     // epilogue norms, rotates and writes K and V straight into the ring.
@@ -386,6 +388,7 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
       t.neox = c->cfg.rope_neox;
       t.append_only = c->ring->append_only;
       t.eps = c->cfg.rms_eps;
+      if (use_dev) t.trace = ktrace_slot(c, "append.kv");
       CK(c->err, tc_run(c, t));
     }
     return DFLASH_OK;

@@ -199,8 +199,22 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     bool ok = true;
     int seg = 0;
 
-    // Final epilogue of tile t for block rows [m0, m1).
-    auto finish_tile = [&](float (&acc)[NV][BN], int t, int m0, int m1) {
+    // Per-tile values the epilogue needs, requested early: the ring offset
+    // and base (K/V into the ring) and, per tile, this row's head-norm gain.
+    long long ring_off = 0, ring_base = 0;
+    if (EPI == kEpiKVRing) { ring_off = a.ring->offset; ring_base = a.ring->base; }
+    auto gain_of = [&](int t) -> float {
+      if (EPI == kEpiQKV) {
+        if (t < a.nq_tiles) return __bfloat162float(reinterpret_cast<const bf16*>(a.qn)[row]);
+        if (t < a.nq_tiles + a.nkv) return __bfloat162float(reinterpret_cast<const bf16*>(a.kn)[row]);
+      } else if (EPI == kEpiKVRing) {
+        const int sg = t / a.nkv;
+        if (!(sg & 1)) return __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[sg >> 1])[row]);
+      }
+      return 0.f;
+    };
+    // Final epilogue of tile t for block rows [m0, m1); gv = gain_of(t).
+    auto finish_tile = [&](float (&acc)[NV][BN], int t, int m0, int m1, float gv) {
       const int n = t * 128 + row;
       const bool valid = n < a.N;
       if (EPI == kEpiArgmax) {
@@ -234,10 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
         const bool isq = t < a.nq_tiles;
         const bool isk = !isq && t < a.nq_tiles + a.nkv;
-        if (isq || isk) {
-          const float g = __bfloat162float(reinterpret_cast<const bf16*>(isq ? a.qn : a.kn)[row]);
-          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
-        }
+        if (isq || isk) head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
         for (int m = 0; m < BN; ++m)
@@ -247,21 +258,18 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         const int sg = t / a.nkv, h = t % a.nkv;
         const int layer = sg >> 1;
         const bool isv = sg & 1;
-        const long long off0 = a.ring->offset;
+        const long long off0 = ring_off;
         const size_t head_base = (((size_t)layer * a.nkv + h) * a.cap) * 128;
         bf16* dst = reinterpret_cast<bf16*>(isv ? a.ring_v : a.ring_k) + head_base;
         float val[BN];
 #pragma unroll
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
-        if (!isv) {
-          const float g = __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[layer])[row]);
-          head_norm_rope_tile<BN>(val, g, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
-        }
+        if (!isv) head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
           if (m < m0 || m >= m1) continue;
           const long long pos = off0 + m;
-          if (a.append_only && pos - a.ring->base >= a.cap) {
+          if (a.append_only && pos - ring_base >= a.cap) {
             if (row == 0) atomicOr(&a.ring->error, kErrFull);
             continue;
           }
@@ -295,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     // k + n, ...), summing the partials in CTA order. (The lm_head's split
     // tiles have two contributors; the later one finishes those alone.)
     int split_first = -1, split_last = -1;        // split tiles published (slot 0, slot 1)
+    float gv_first = 0.f, gv_last = 0.f;          // and their rows' gains
     unsigned* const arrive = a.tile_ctr;
     unsigned* const depart = a.tile_ctr + kTileDepart;
     for (long long u = u0; u < u1 && ok; ++seg) {
@@ -302,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       const int c0 = static_cast<int>(u % KC);
       const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
       const int buf = seg & 1;
+      const float gv = gain_of(t);
       ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
       if (!ok) break;
       tc_fence_after();
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       mbar_arrive(&acc_empty[buf]);
       u += c1 - c0;
       if (c0 == 0 && c1 == KC) {
-        finish_tile(acc, t, 0, a.M);
+        finish_tile(acc, t, 0, a.M, gv);
       } else if (EPI == kEpiArgmax) {
         // lm_head: a split tile has two contributors (each CTA streams many
         // tiles); the later one reads the other's partial and finishes it.
@@ -337,12 +347,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           if (mq == 1) sum_partials<NV, BN, 1, 8 / NV>(acc, a.partials, row, bf, bl, mq, slot_of);
           else sum_partials<NV, BN, BN / 4, 4>(acc, a.partials, row, bf, bl, mq, slot_of);
           if (threadIdx.x == 64) arrive[t] = 0u;
-          finish_tile(acc, t, 0, a.M);
+          finish_tile(acc, t, 0, a.M, gv);
         }
       } else {
         const int slot = (t == first_tile) ? 0 : 1;
         put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
-        if (slot == 0) split_first = t; else split_last = t;
+        if (slot == 0) { split_first = t; gv_first = gv; } else { split_last = t; gv_last = gv; }
         epi_sync();
         if (threadIdx.x == 64) {
           __threadfence();
@@ -370,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         for (int g = k; g < mq; g += nc) {
           float acc[NV][BN];
           sum_group<NV, BN, 8 / NV>(acc, a.partials, row, g, bf, bl, slot_of);
-          finish_tile(acc, t, 4 * g, 4 * g + 4 < a.M ? 4 * g + 4 : a.M);
+          finish_tile(acc, t, 4 * g, 4 * g + 4 < a.M ? 4 * g + 4 : a.M, slot == 0 ? gv_first : gv_last);
         }
         epi_sync();
       }

@@ -312,7 +312,8 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
  * of the last launch are read with dflash_draft_trace. */
 #define DFLASH_OPT_DRAFT_TRACE 3
 /* DFLASH_OPT_KERNEL_TRACE: 1 makes dflash_draft_block on the one-kernel-per-
- * operation path stamp the GPU's global timer (ns) for each traced launch:
+ * operation path (and the dflash_append_block that follows it) stamp the
+ * GPU's global timer (ns) for each traced launch:
  * earliest CTA entry, latest return from the wait on the preceding kernel,
  * latest CTA exit (allocates 6 KB on first use; 0 stops it). Read with
  * dflash_kernel_trace. */
