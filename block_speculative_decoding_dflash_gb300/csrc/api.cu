@@ -350,7 +350,7 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
     if (!tc_encode_map(&t.b_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, bn_of(rows)))
       return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the residual rows");
     t.y = f; t.ldy = c->H;
-    if (use_dev) t.trace = ktrace_slot(c, "append.fc");
+    if (use_dev) t.trace = ktrace_slot(c, "append.fc", 4);
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
@@ -388,7 +388,7 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
       t.neox = c->cfg.rope_neox;
       t.append_only = c->ring->append_only;
       t.eps = c->cfg.rms_eps;
-      if (use_dev) t.trace = ktrace_slot(c, "append.kv");
+      if (use_dev) t.trace = ktrace_slot(c, "append.kv", 4);
       CK(c->err, tc_run(c, t));
     }
     return DFLASH_OK;
@@ -497,7 +497,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     t.nq_tiles = c->nq; t.nkv = c->nkv;
     t.qn = LW(c, l, kQNorm); t.kn = LW(c, l, kKNorm);
     t.rope = c->rope; t.neox = c->cfg.rope_neox; t.eps = eps;
-    t.trace = ktrace_slot(c, ln + "qkv");
+    t.trace = ktrace_slot(c, ln + "qkv", 4);
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs q = lin_args(c->xn, c->H, c->qkv, c->qkv_n, rows, c->qkv_n, c->H);
@@ -532,14 +532,14 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.head_ctr = c->attn_ctr;
   at.err = c->tc_err;
   at.sms = c->num_sms;
-  at.trace = ktrace_slot(c, ln + "attn", 3);
+  at.trace = ktrace_slot(c, ln + "attn", 4);
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
     tc_segments(t, {{&c->lmaps[l].wo, c->H}});
     t.b_map = c->attn_map[bi];
     t.y = c->x; t.ldy = c->H; t.r = c->x; t.ldr = c->H;
-    t.trace = ktrace_slot(c, ln + "o");
+    t.trace = ktrace_slot(c, ln + "o", 4);
     CK(c->err, tc_run(c, t));
   } else {
     LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
@@ -554,13 +554,13 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     t.a2_map = c->lmaps[l].wu;
     t.b_map = c->xn_map[bi];
     t.y = c->sbuf; t.ldy = c->I;
-    t.trace = ktrace_slot(c, ln + "gate_up");
+    t.trace = ktrace_slot(c, ln + "gate_up", 4);
     CK(c->err, tc_run(c, t));
     TcGemmArgs d = tc_args(c, rows, c->H, c->I, kEpiResid);
     tc_segments(d, {{&c->lmaps[l].wd, c->H}});
     d.b_map = c->sbuf_map[bi];
     d.y = c->x; d.ldy = c->H; d.r = c->x; d.ldr = c->H;
-    d.trace = ktrace_slot(c, ln + "down");
+    d.trace = ktrace_slot(c, ln + "down", 4);
     CK(c->err, tc_run(c, d));
   } else {
     LinearArgs g = lin_args(c->xn, c->H, c->sbuf, c->I, rows, c->I, c->H);
@@ -1063,7 +1063,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     t.softcap = c->cfg.softcap;
     t.ids = lm.ids; t.ids2 = lm.ids2; t.maxv = lm.maxv;
     t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
-    t.trace = ktrace_slot(c, "lm_head");
+    t.trace = ktrace_slot(c, "lm_head", 4);
     CK(c->err, tc_run(c, t));
   } else {
     CK(c->err, launch_lmhead_argmax(dt, lm, st));

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   const int nctx = static_cast<int>(p - kstart);
   const int nk = nctx + a.rows;
   const int j0 = s * kKeys;
+  const int cap = static_cast<int>(a.cap);
+  const int slot0 = static_cast<int>(ring_slot(kstart, a.cap));
   const size_t pstride = kPartStride;     // 16-byte aligned rows for float4 reads
   float* part = a.partial + ((size_t)g * nsplit + s) * Qn * pstride;
   const bf16* rk = reinterpret_cast<const bf16*>(a.ring_k) + (size_t)g * a.cap * kHd;
@@ -85,9 +87,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       const bf16* vs = vb;
       bool valid = kj < nk;
       if (kj < nctx) {
-        const long long slot = ring_slot(kstart + kj, a.cap);
-        ks = rk + slot * kHd + ch * 8;
-        vs = rv + slot * kHd + ch * 8;
+        int slot = slot0 + kj;                     // = ring_slot(kstart + kj, cap)
+        if (slot >= cap) slot -= cap;
+        ks = rk + (size_t)slot * kHd + ch * 8;
+        vs = rv + (size_t)slot * kHd + ch * 8;
       } else if (valid) {
         const size_t off = (size_t)(kj - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
         ks = kb + off;

@@ -507,9 +507,9 @@ __device__ __noinline__ int gemm_epilogue(const MegaArgs& a, const MegaPhase& ph
       finish = E.flag != 0;
       if (finish) {
         __threadfence();
-        auto slot_of = [&](int bb) { return t == static_cast<int>((rg.U * bb / G) / KC) ? 0 : 1; };
-        if (mq == 1) sum_partials<NV, BN, 1, 4 / NV>(acc, partials, row, bf, bl, mq, slot_of);
-        else sum_partials<NV, BN, BN / 4, (NV == 1 ? 4 : 2)>(acc, partials, row, bf, bl, mq, slot_of);
+        const int s_bf = t == static_cast<int>((rg.U * bf / G) / KC) ? 0 : 1;
+        if (mq == 1) sum_partials<NV, BN, 1, 4 / NV>(acc, partials, row, bf, bl, mq, s_bf);
+        else sum_partials<NV, BN, BN / 4, (NV == 1 ? 4 : 2)>(acc, partials, row, bf, bl, mq, s_bf);
         if (wt == 0) tile_ctr[t] = 0u;
       }
     }

@@ -17,16 +17,30 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(128) : "memory");
 }
 
-// Per-head RMSNorm over a 128-row tile (head_dim 128: one dim per epilogue
-// thread) followed by RoPE, for the block rows m in [m0, m1) of the tile's
-// BN columns (m1 <= M; the bounds are the same for all threads); the value is
-// normalised in fp32 and rotated before the single rounding the caller
-// applies. All 128 epilogue threads must call it.
+// This thread's RoPE entries for block rows [m0, m1): the (cos, sin) of its
+// rotation pair (row & 63 in the half-split layout, row / 2 in the
+// interleaved one) at each row's position; rope[m * 64 + i]. They do not
+// depend on the tile, so an epilogue can load them once.
 template <int BN>
-__device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const float2* rope, int M,
-                                                    int neox, float eps, int row, int lane, int q,
-                                                    float (*ss_sm)[BN], float* x_sm, int m0 = 0,
-                                                    int m1 = BN) {
+__device__ __forceinline__ void rope_entries(float2 (&cs)[BN], const float2* rope, int M, int neox,
+                                             int row, int m0 = 0, int m1 = BN) {
+  const int i = neox ? (row & 63) : (row >> 1);
+#pragma unroll
+  for (int m = 0; m < BN; ++m)
+    cs[m] = (m >= m0 && m < m1 && m < M) ? rope[m * 64 + i] : make_float2(1.f, 0.f);
+}
+
+// Per-head RMSNorm over a 128-row tile (head_dim 128: one dim per epilogue
+// thread) followed by RoPE with the entries cs_at(m) (rope_entries), for the
+// block rows m in [m0, m1) of the tile's BN columns (m1 <= M; the bounds are
+// the same for all threads); the value is normalised in fp32 and rotated
+// before the single rounding the caller applies. All 128 epilogue threads
+// must call it.
+template <int BN, class CsAt>
+__device__ __forceinline__ void head_norm_rope_cs(float* val, float g, CsAt cs_at, int M, int neox,
+                                                  float eps, int row, int lane, int q,
+                                                  float (*ss_sm)[BN], float* x_sm, int m0 = 0,
+                                                  int m1 = BN) {
   if (m1 > M) m1 = M;
 #pragma unroll
   for (int m = 0; m < BN; ++m) {
@@ -46,30 +60,46 @@ __device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const f
     for (int m = 0; m < BN; ++m)
       if (m >= m0 && m < m1) x_sm[row * BN + m] = val[m];
     epi_sync();
-    const int i = row & 63;
     const bool lo = row < 64;
     const int partner = lo ? row + 64 : row - 64;
 #pragma unroll
     for (int m = 0; m < BN; ++m) {
       if (m >= m0 && m < m1) {
-        const float2 cs = rope[m * 64 + i];
         const float other = x_sm[partner * BN + m];
+        const float2 cs = cs_at(m);
         val[m] = lo ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
       }
     }
     epi_sync();
   } else {
-    const int i = row >> 1;
     const bool ev = (row & 1) == 0;
 #pragma unroll
     for (int m = 0; m < BN; ++m) {
       if (m < m0 || m >= m1) continue;
       const float other = __shfl_xor_sync(0xffffffffu, val[m], 1);
-      {
-        const float2 cs = rope[m * 64 + i];
-        val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
-      }
+      const float2 cs = cs_at(m);
+      val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
     }
+  }
+}
+
+// The same with the entries read from the table: up to 16 block rows they
+// are loaded first (the loads overlap the norm's reduction), beyond that
+// where they are used, to save registers.
+template <int BN>
+__device__ __forceinline__ void head_norm_rope_tile(float* val, float g, const float2* rope, int M,
+                                                    int neox, float eps, int row, int lane, int q,
+                                                    float (*ss_sm)[BN], float* x_sm, int m0 = 0,
+                                                    int m1 = BN) {
+  if (BN <= 16) {
+    float2 cs[BN];
+    rope_entries<BN>(cs, rope, M, neox, row, m0, m1);
+    head_norm_rope_cs<BN>(val, g, [&](int m) { return cs[m]; }, M, neox, eps, row, lane, q, ss_sm, x_sm,
+                          m0, m1);
+  } else {
+    const int i = neox ? (row & 63) : (row >> 1);
+    head_norm_rope_cs<BN>(val, g, [&](int m) { return rope[m * 64 + i]; }, M, neox, eps, row, lane, q,
+                          ss_sm, x_sm, m0, m1);
   }
 }
 
@@ -93,10 +123,11 @@ __device__ __forceinline__ void put_partial(float* partials, int b, int slot, in
 // acc = sum of the partials of CTAs bf..bl in CTA order (deterministic),
 // issuing the loads of KB contributors before adding them: L2 latency, not
 // bandwidth, bounds this loop, so fewer groups per contributor (MQC) allow a
-// deeper batch. slot_of(bb) gives contributor bb's slot for this tile.
-template <int NV, int BN, int MQC, int KB, class SlotOf>
+// deeper batch. The tile is the first one of every contributor after bf
+// (slot 0); s_bf is bf's slot for it.
+template <int NV, int BN, int MQC, int KB>
 __device__ __forceinline__ void sum_partials(float (&acc)[NV][BN], const float* partials, int row, int bf,
-                                             int bl, int mq, SlotOf slot_of) {
+                                             int bl, int mq, int s_bf) {
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -108,7 +139,7 @@ __device__ __forceinline__ void sum_partials(float (&acc)[NV][BN], const float* 
       const int bb = b0 + q;
       if (bb > bl) break;
       const float4* p = reinterpret_cast<const float4*>(
-          partials + ((size_t)bb * 2 + slot_of(bb)) * NV * BN * 128 + (size_t)row * NV * BN);
+          partials + ((size_t)bb * 2 + (bb == bf ? s_bf : 0)) * NV * BN * 128 + (size_t)row * NV * BN);
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -133,9 +164,9 @@ __device__ __forceinline__ void sum_partials(float (&acc)[NV][BN], const float* 
 // acc[v][4g .. 4g+3] = the sum of float4 group g of the partials of CTAs
 // bf..bl in CTA order, KB contributors' loads in flight at a time (the other
 // columns of acc are left zero).
-template <int NV, int BN, int KB, class SlotOf>
+template <int NV, int BN, int KB>
 __device__ __forceinline__ void sum_group(float (&acc)[NV][BN], const float* partials, int row, int g,
-                                          int bf, int bl, SlotOf slot_of) {
+                                          int bf, int bl, int s_bf) {
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -150,7 +181,7 @@ __device__ __forceinline__ void sum_group(float (&acc)[NV][BN], const float* par
       const int bb = b0 + qq;
       if (bb > bl) break;
       const float4* p = reinterpret_cast<const float4*>(
-          partials + ((size_t)bb * 2 + slot_of(bb)) * NV * BN * 128 + (size_t)row * NV * BN);
+          partials + ((size_t)bb * 2 + (bb == bf ? s_bf : 0)) * NV * BN * 128 + (size_t)row * NV * BN);
 #pragma unroll
       for (int v = 0; v < NV; ++v) pv[qq][v] = __ldcg(p + v * (BN / 4) + g);
     }
@@ -175,13 +206,22 @@ __device__ __forceinline__ void sum_group(float (&acc)[NV][BN], const float* par
     }
 }
 
-__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned* p) {
-  return *reinterpret_cast<const volatile unsigned*>(p);
+// Load with acquire semantics at GPU scope: reads after it see what the
+// writer published before its release (fence + atomic).
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // CTA owning unit u when U units are split into G contiguous ranges
 // [floor(b*U/G), floor((b+1)*U/G)).
 __device__ __forceinline__ int owner_of(long long u, long long U, int G) {
+  return static_cast<int>((u * G + G - 1) / U);
+}
+// The same in 32-bit arithmetic, for U * G < 2^32 (a 64-bit division is a
+// long software sequence on the GPU).
+__device__ __forceinline__ int owner_of_u32(unsigned u, unsigned U, unsigned G) {
   return static_cast<int>((u * G + G - 1) / U);
 }
 

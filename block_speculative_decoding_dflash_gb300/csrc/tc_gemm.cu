@@ -70,9 +70,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
-  const int KC = a.kchunks;
-  const long long U = (long long)a.tiles * KC;
-  const long long u0 = U * b / G, u1 = U * (b + 1) / G;
+  // Units (tile, 64-wide K chunk) in 32-bit arithmetic: the host checks
+  // that tiles * kchunks * grid fits.
+  const unsigned KC = a.kchunks;
+  const unsigned U = static_cast<unsigned>(a.tiles) * KC;
+  const unsigned u0 = U * b / G, u1 = U * (b + 1) / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       bool ok = true;
       // Stage i covers units [u, u + nc): nc = P while the next unit is in the
       // same tile and in this CTA's range (the MMA issuer pairs the same way).
-      auto issue_a = [&](int st, long long u, int nc) {
+      auto issue_a = [&](int st, unsigned u, int nc) {
         const int t = static_cast<int>(u / KC), c = static_cast<int>(u % KC);
         int s = 0;
         while (s < a.nseg - 1 && t >= a.seg_tiles[s]) ++s;
@@ -108,18 +110,18 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           if (NV == 2) tma_load_2d_hint(sa + k * C::kSub + kABytes, &a.a2_map, (c + k) * 64, t * 128, &full[st], pol);
         }
       };
-      auto issue_b = [&](int st, long long u, int nc) {
+      auto issue_b = [&](int st, unsigned u, int nc) {
         const int c = static_cast<int>(u % KC);
         uint8_t* sb = smem + (size_t)st * C::kStage + C::kBOff;
         for (int k = 0; k < nc; ++k) tma_load_2d(sb + k * BN * 128, &a.b_map, (c + k) * 64, 0, &full[st]);
       };
-      auto width = [&](long long u) {
+      auto width = [&](unsigned u) {
         return (P == 2 && u + 1 < u1 && (u % KC) + 1 < KC) ? 2 : 1;
       };
       // The weight tiles of the first stages do not depend on earlier
       // kernels: request them before the programmatic launch dependency
       // resolves, and their activations once it has.
-      long long u = u0;
+      unsigned u = u0;
       int pre = 0;
       for (; pre < STAGES && u < u1; ++pre) {
         const int nc = width(u);
@@ -128,14 +130,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       }
       pdl_wait();
       {
-        long long v = u0;
+        unsigned v = u0;
         for (int j = 0; j < pre; ++j) {
           const int nc = width(v);
           issue_b(j, v, nc);
           v += nc;
         }
       }
-      for (long long i = pre; u < u1 && ok; ++i) {
+      for (unsigned i = pre; u < u1 && ok; ++i) {
         const int st = static_cast<int>(i % STAGES);
         ok = mbar_wait(&empty[st], static_cast<unsigned>((i / STAGES - 1) & 1));
         if (!ok) break;
@@ -151,9 +153,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(128, BN);
       bool ok = true;
-      long long i = 0;
+      unsigned i = 0;
       int seg = 0;
-      for (long long u = u0; u < u1 && ok; ++seg) {
+      for (unsigned u = u0; u < u1 && ok; ++seg) {
         const int c0 = static_cast<int>(u % KC);
         const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
         const int buf = seg & 1;
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         tc_commit(&acc_full[buf]);
         u += c1 - c0;
       }
+      if (a.trace.p) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 1}, 1);   // last MMA issued
       if (!ok) atomicOr(a.err, 2);
     }
   } else {
@@ -202,7 +205,17 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     // Per-tile values the epilogue needs, requested early: the ring offset
     // and base (K/V into the ring) and, per tile, this row's head-norm gain.
     long long ring_off = 0, ring_base = 0;
-    if (EPI == kEpiKVRing) { ring_off = a.ring->offset; ring_base = a.ring->base; }
+    int ring_s0 = 0;                              // ring slot of ring_off
+    if (EPI == kEpiKVRing) {
+      ring_off = a.ring->offset;
+      ring_base = a.ring->base;
+      ring_s0 = static_cast<int>(ring_slot(ring_off, a.cap));
+    }
+    // This thread's RoPE entries, the same for every tile (kept in registers
+    // for 16 block rows; 32 would crowd out the epilogue's other values).
+    constexpr bool kHoistRope = (EPI == kEpiQKV || EPI == kEpiKVRing) && BN == 16;
+    float2 rope_cs[BN];
+    if (kHoistRope) rope_entries<BN>(rope_cs, a.rope, a.M, a.neox, row);
     auto gain_of = [&](int t) -> float {
       if (EPI == kEpiQKV) {
         if (t < a.nq_tiles) return __bfloat162float(reinterpret_cast<const bf16*>(a.qn)[row]);
@@ -214,7 +227,20 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       return 0.f;
     };
     // Final epilogue of tile t for block rows [m0, m1); gv = gain_of(t).
-    auto finish_tile = [&](float (&acc)[NV][BN], int t, int m0, int m1, float gv) {
+    // Residuals of tile t's row for the block rows (kEpiResid), requested
+    // ahead of the accumulator so the finish has no dependent load.
+    // (Kept for 16 block rows; at 32 the registers are better spent elsewhere
+    // and the finish loads them.)
+    constexpr bool kHoistResid = EPI == kEpiResid && BN == 16;
+    auto resid_at = [&](int m, int n) {
+      return __bfloat162float(reinterpret_cast<const bf16*>(a.r)[(size_t)m * a.ldr + n]);
+    };
+    auto resid_of = [&](int t, float (&res)[BN]) {
+      const int n = t * 128 + row;
+#pragma unroll
+      for (int m = 0; m < BN; ++m) res[m] = (kHoistResid && m < a.M && n < a.N) ? resid_at(m, n) : 0.f;
+    };
+    auto finish_tile = [&](float (&acc)[NV][BN], int t, int m0, int m1, float gv, const float (&res)[BN]) {
       const int n = t * 128 + row;
       const bool valid = n < a.N;
       if (EPI == kEpiArgmax) {
@@ -248,7 +274,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
         const bool isq = t < a.nq_tiles;
         const bool isk = !isq && t < a.nq_tiles + a.nkv;
-        if (isq || isk) head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+        if (isq || isk) {
+          if (kHoistRope) head_norm_rope_cs<BN>(val, gv, [&](int m) { return rope_cs[m]; }, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+          else head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+        }
         bf16* Y = reinterpret_cast<bf16*>(a.y);
 #pragma unroll
         for (int m = 0; m < BN; ++m)
@@ -264,7 +293,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         float val[BN];
 #pragma unroll
         for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
-        if (!isv) head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+        if (!isv) {
+          if (kHoistRope) head_norm_rope_cs<BN>(val, gv, [&](int m) { return rope_cs[m]; }, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+          else head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
+        }
 #pragma unroll
         for (int m = 0; m < BN; ++m) {
           if (m < m0 || m >= m1) continue;
@@ -273,7 +305,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
             if (row == 0) atomicOr(&a.ring->error, kErrFull);
             continue;
           }
-          dst[(size_t)ring_slot(pos, a.cap) * 128 + row] = __float2bfloat16_rn(val[m]);
+          int slot = ring_s0 + m;                 // = ring_slot(pos, cap)
+          while (slot >= a.cap) slot -= static_cast<int>(a.cap);
+          dst[(size_t)slot * 128 + row] = __float2bfloat16_rn(val[m]);
         }
       } else if (valid) {
         bf16* Y = reinterpret_cast<bf16*>(a.y);
@@ -284,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
             if (EPI == kEpiStore) {
               out = acc[0][m];
             } else if (EPI == kEpiResid) {
-              out = __bfloat162float(reinterpret_cast<const bf16*>(a.r)[(size_t)m * a.ldr + n]) +
-                    rnd_bf(acc[0][m]);
+              out = (kHoistResid ? res[m] : resid_at(m, n)) + rnd_bf(acc[0][m]);
             } else {
               out = silu_f(rnd_bf(acc[0][m])) * rnd_bf(acc[NV - 1][m]);
             }
@@ -304,14 +337,19 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     // tiles have two contributors; the later one finishes those alone.)
     int split_first = -1, split_last = -1;        // split tiles published (slot 0, slot 1)
     float gv_first = 0.f, gv_last = 0.f;          // and their rows' gains
+    float res_first[BN], res_last[BN];            // and residuals
+#pragma unroll
+    for (int m = 0; m < BN; ++m) res_first[m] = res_last[m] = 0.f;
     unsigned* const arrive = a.tile_ctr;
     unsigned* const depart = a.tile_ctr + kTileDepart;
-    for (long long u = u0; u < u1 && ok; ++seg) {
+    for (unsigned u = u0; u < u1 && ok; ++seg) {
       const int t = static_cast<int>(u / KC);
       const int c0 = static_cast<int>(u % KC);
       const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
       const int buf = seg & 1;
       const float gv = gain_of(t);
+      float res[BN];
+      resid_of(t, res);
       ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
       if (!ok) break;
       tc_fence_after();
@@ -327,15 +365,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       mbar_arrive(&acc_empty[buf]);
       u += c1 - c0;
       if (c0 == 0 && c1 == KC) {
-        finish_tile(acc, t, 0, a.M, gv);
+        finish_tile(acc, t, 0, a.M, gv, res);
       } else if (EPI == kEpiArgmax) {
         // lm_head: a split tile has two contributors (each CTA streams many
         // tiles); the later one reads the other's partial and finishes it.
         const int slot = (t == first_tile) ? 0 : 1;
         put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
         epi_sync();
-        const int bf = owner_of((long long)t * KC, U, G);
-        const int bl = owner_of((long long)t * KC + KC - 1, U, G);
+        const int bf = owner_of_u32(t * KC, U, G);
+        const int bl = owner_of_u32(t * KC + KC - 1, U, G);
         if (threadIdx.x == 64) {
           __threadfence();
           s_last = (atomicAdd(&arrive[t], 1u) == static_cast<unsigned>(bl - bf));
@@ -343,16 +381,24 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         epi_sync();
         if (s_last) {
           __threadfence();
-          auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
-          if (mq == 1) sum_partials<NV, BN, 1, 8 / NV>(acc, a.partials, row, bf, bl, mq, slot_of);
-          else sum_partials<NV, BN, BN / 4, 4>(acc, a.partials, row, bf, bl, mq, slot_of);
+          const int s_bf = U * bf / G == t * KC ? 0 : 1;
+          if (mq == 1) sum_partials<NV, BN, 1, 2>(acc, a.partials, row, bf, bl, mq, s_bf);
+          else sum_partials<NV, BN, BN / 4, 2>(acc, a.partials, row, bf, bl, mq, s_bf);
           if (threadIdx.x == 64) arrive[t] = 0u;
-          finish_tile(acc, t, 0, a.M, gv);
+          finish_tile(acc, t, 0, a.M, gv, res);
         }
       } else {
         const int slot = (t == first_tile) ? 0 : 1;
         put_partial<NV, BN>(a.partials, b, slot, row, mq, acc);
-        if (slot == 0) { split_first = t; gv_first = gv; } else { split_last = t; gv_last = gv; }
+        if (slot == 0) {
+          split_first = t; gv_first = gv;
+#pragma unroll
+          for (int m = 0; m < BN; ++m) res_first[m] = res[m];
+        } else {
+          split_last = t; gv_last = gv;
+#pragma unroll
+          for (int m = 0; m < BN; ++m) res_last[m] = res[m];
+        }
         epi_sync();
         if (threadIdx.x == 64) {
           __threadfence();
@@ -360,35 +406,72 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         }
       }
     }
-    for (int slot = 0; slot < 2 && ok; ++slot) {
+    if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 1}, 2);  // tiles published
+    // Wait for the other contributors of both split tiles before reducing
+    // either, so the two waits overlap.
+    // Contributors whose partial loads are in flight at once: the long-K
+    // GEMMs (residual, store) split a tile over about ten CTAs, the others
+    // over two to four and need the registers for their epilogue.
+    constexpr int kSumBatch = (EPI == kEpiResid || EPI == kEpiStore) ? (NV == 1 ? 16 : 4) : (NV == 1 ? 8 : 4);
+    int bfs[2], bls[2];
+    bool work[2];
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
       const int t = slot == 0 ? split_first : split_last;
-      if (t < 0) continue;
-      const int bf = owner_of((long long)t * KC, U, G);
-      const int bl = owner_of((long long)t * KC + KC - 1, U, G);
-      const int nc = bl - bf + 1, k = b - bf;
-      if (k < mq) {
-        if (threadIdx.x == 64) {
-          unsigned spins = 0;
-          while (ld_volatile_u32(&arrive[t]) < static_cast<unsigned>(nc)) {
-            if (++spins > (1u << 24)) { atomicOr(a.err, 8); break; }
-            __nanosleep(64);
-          }
-          __threadfence();
+      bfs[slot] = t < 0 ? 0 : owner_of_u32(t * KC, U, G);
+      bls[slot] = t < 0 ? -1 : owner_of_u32(t * KC + KC - 1, U, G);
+      work[slot] = t >= 0 && b - bfs[slot] < mq;
+    }
+    if (threadIdx.x == 64 && ok) {
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        if (!work[slot]) continue;
+        const int t = slot == 0 ? split_first : split_last;
+        const unsigned nc = static_cast<unsigned>(bls[slot] - bfs[slot] + 1);
+        unsigned spins = 0;
+        while (ld_acquire_u32(&arrive[t]) < nc) {
+          if (++spins > (1u << 24)) { atomicOr(a.err, 8); break; }
+          __nanosleep(64);
         }
-        epi_sync();
-        auto slot_of = [&](int bb) { return t == static_cast<int>((U * bb / G) / KC) ? 0 : 1; };
-        for (int g = k; g < mq; g += nc) {
-          float acc[NV][BN];
-          sum_group<NV, BN, 8 / NV>(acc, a.partials, row, g, bf, bl, slot_of);
-          finish_tile(acc, t, 4 * g, 4 * g + 4 < a.M ? 4 * g + 4 : a.M, slot == 0 ? gv_first : gv_last);
-        }
-        epi_sync();
       }
-      if (threadIdx.x == 64 && atomicAdd(&depart[t], 1u) == static_cast<unsigned>(nc - 1)) {
-        arrive[t] = 0u;                           // every contributor is past its wait
-        depart[t] = 0u;
+      if (a.trace.p && (work[0] || work[1])) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 1);  // present
+      // This CTA no longer reads the arrive counters; the last contributor of
+      // a tile to get here clears both of its counters for the next launch.
+      unsigned d[2] = {0u, 0u};
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int t = slot == 0 ? split_first : split_last;
+        if (t >= 0) d[slot] = atomicAdd(&depart[t], 1u);
+      }
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int t = slot == 0 ? split_first : split_last;
+        if (t >= 0 && d[slot] == static_cast<unsigned>(bls[slot] - bfs[slot])) {
+          arrive[t] = 0u;
+          depart[t] = 0u;
+        }
       }
     }
+    if (ok && (work[0] || work[1])) {
+      epi_sync();
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        if (!work[slot]) continue;
+        const int t = slot == 0 ? split_first : split_last;
+        const int bf = bfs[slot], bl = bls[slot];
+        const int nc = bl - bf + 1;
+        const int s_bf = U * bf / G == t * KC ? 0 : 1;
+        for (int g = b - bf; g < mq; g += nc) {
+          float acc[NV][BN];
+          sum_group<NV, BN, kSumBatch>(acc, a.partials, row, g, bf, bl, s_bf);
+          finish_tile(acc, t, 4 * g, 4 * g + 4 < a.M ? 4 * g + 4 : a.M, slot == 0 ? gv_first : gv_last,
+                      slot == 0 ? res_first : res_last);
+        }
+      }
+      if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 3}, 1);  // summed
+      epi_sync();
+    }
+    if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 2);  // finished
     if (!ok) atomicOr(a.err, 4);
 
     if (EPI == kEpiArgmax) {
@@ -769,6 +852,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
   const long long want = (U + kMinUnits - 1) / kMinUnits;
   if (grid > want) grid = static_cast<int>(want);
   if (grid < 1) grid = 1;
+  if (U * grid >= (1ll << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
   if (bn == 16) {
     switch (a.epi) {
       case kEpiStore: return launch_tc<16, kEpiStore>(a, grid, pdl, st);
