@@ -80,6 +80,7 @@ __device__ __forceinline__ void head_norm_rope_cs(float* val, float g, CsAt cs_a
       const float2 cs = cs_at(m);
       val[m] = ev ? val[m] * cs.x - other * cs.y : other * cs.y + val[m] * cs.x;
     }
+    epi_sync();                                   // ss_sm is free for the next call
   }
 }
 

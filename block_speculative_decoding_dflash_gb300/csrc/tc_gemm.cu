@@ -407,8 +407,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       }
     }
     if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 1}, 2);  // tiles published
-    // Wait for the other contributors of both split tiles before reducing
-    // either, so the two waits overlap.
     // Contributors whose partial loads are in flight at once: the long-K
     // GEMMs (residual, store) split a tile over about ten CTAs, the others
     // over two to four and need the registers for their epilogue.
@@ -422,6 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       bls[slot] = t < 0 ? -1 : owner_of_u32(t * KC + KC - 1, U, G);
       work[slot] = t >= 0 && b - bfs[slot] < mq;
     }
+    // Wait for the other contributors of both split tiles before reducing
+    // either, so the two waits overlap.
     if (threadIdx.x == 64 && ok) {
 #pragma unroll
       for (int slot = 0; slot < 2; ++slot) {
@@ -435,21 +435,17 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         }
       }
       if (a.trace.p && (work[0] || work[1])) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 1);  // present
-      // This CTA no longer reads the arrive counters; the last contributor of
-      // a tile to get here clears both of its counters for the next launch.
-      unsigned d[2] = {0u, 0u};
+    }
+    // This CTA no longer reads the arrive counters: depart. The last
+    // contributor of a tile to depart clears both of its counters for the
+    // next launch; the results are looked at only after the reduction, so the
+    // atomics' round trip overlaps it.
+    unsigned dep[2] = {0u, 0u};
+    if (threadIdx.x == 64 && ok) {
 #pragma unroll
       for (int slot = 0; slot < 2; ++slot) {
         const int t = slot == 0 ? split_first : split_last;
-        if (t >= 0) d[slot] = atomicAdd(&depart[t], 1u);
-      }
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const int t = slot == 0 ? split_first : split_last;
-        if (t >= 0 && d[slot] == static_cast<unsigned>(bls[slot] - bfs[slot])) {
-          arrive[t] = 0u;
-          depart[t] = 0u;
-        }
+        if (t >= 0) dep[slot] = atomicAdd(&depart[t], 1u);
       }
     }
     if (ok && (work[0] || work[1])) {
@@ -469,7 +465,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         }
       }
       if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 3}, 1);  // summed
-      epi_sync();
+    }
+    if (threadIdx.x == 64 && ok) {
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int t = slot == 0 ? split_first : split_last;
+        if (t >= 0 && dep[slot] == static_cast<unsigned>(bls[slot] - bfs[slot])) {
+          arrive[t] = 0u;
+          depart[t] = 0u;
+        }
+      }
     }
     if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 2);  // finished
     if (!ok) atomicOr(a.err, 4);
