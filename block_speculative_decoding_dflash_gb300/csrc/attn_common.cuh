@@ -9,6 +9,8 @@
 #pragma once
 
 #include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
 
 namespace dfl {
 
@@ -19,6 +21,29 @@ constexpr int kAttnPartStride = kAttnHd + 4;
 // Splits covering n keys.
 __host__ __device__ __forceinline__ int attn_splits(long long n) {
   return static_cast<int>((n + kAttnKeys - 1) / kAttnKeys);
+}
+
+// Before a kernel waits on the ones still running: asks L2 for the context
+// keys (thread 0) and values (thread 1) of key split s of kv head g. The ring
+// state read here may be older than the one the kernel then uses (a round
+// old at worst, always a valid state, so the range stays inside the ring);
+// that only costs the hint.
+__device__ __forceinline__ void attn_prefetch_context(const AttnArgs& a, int s, int g) {
+  if (threadIdx.x >= 2) return;
+  const volatile RingState* rs = a.ring;
+  const long long p = rs->offset;
+  long long kstart = rs->base;
+  if (a.window > 0 && p - a.window > kstart) kstart = p - a.window;
+  const long long j0 = (long long)s * kAttnKeys;
+  long long n = p - kstart - j0;
+  if (n <= 0 || a.cap <= 0) return;
+  if (n > kAttnKeys) n = kAttnKeys;
+  const long long slot = ring_slot(kstart + j0, a.cap);
+  const long long first = n < a.cap - slot ? n : a.cap - slot;
+  const char* base = static_cast<const char*>(threadIdx.x == 0 ? a.ring_k : a.ring_v) +
+                     (size_t)g * a.cap * kAttnHd * 2;
+  l2_prefetch_bulk(base + (size_t)slot * kAttnHd * 2, static_cast<uint32_t>(first * kAttnHd * 2));
+  if (n > first) l2_prefetch_bulk(base, static_cast<uint32_t>((n - first) * kAttnHd * 2));
 }
 
 // One warp merges the first ns splits (layout stride nsplit) of query qi of kv
