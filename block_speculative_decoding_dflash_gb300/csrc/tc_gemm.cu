@@ -492,19 +492,44 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       if (threadIdx.x == 64) s_last = (atomicAdd(a.done_ctr, 1u) == static_cast<unsigned>(G - 1));
       epi_sync();
       if (s_last) {
+        // All 128 epilogue threads: column m = e % BN, CTAs c = e / BN + k *
+        // (128 / BN), eight of them requested per round trip; then the
+        // 128 / BN candidates of a column are reduced through shared memory.
+        // (The (value, index) order makes the result independent of the
+        // reduction order.)
         __threadfence();
-        if (threadIdx.x >= 64 && threadIdx.x - 64 < a.M) {
-          const int m = threadIdx.x - 64;
-          float v = -INFINITY;
-          int idx = 0x7fffffff;
-          for (int c = 0; c < G; ++c) {
-            const float cv = __ldcg(a.part_v + (size_t)c * a.M + m);
-            const int ci = __ldcg(a.part_i + (size_t)c * a.M + m);
-            if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
+        constexpr int kSub = 128 / BN;
+        const int e = threadIdx.x - 64, m = e % BN, sub = e / BN;
+        float v = -INFINITY;
+        int idx = 0x7fffffff;
+        if (m < a.M) {
+          for (int c0 = sub; c0 < G; c0 += 8 * kSub) {
+            float cv[8];
+            int ci[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c = c0 + j * kSub;
+              cv[j] = c < G ? __ldcg(a.part_v + (size_t)c * a.M + m) : -INFINITY;
+              ci[j] = c < G ? __ldcg(a.part_i + (size_t)c * a.M + m) : 0x7fffffff;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (better(cv[j], ci[j], v, idx)) { v = cv[j]; idx = ci[j]; }
           }
-          a.ids[m] = idx;
-          if (a.ids2) a.ids2[m] = idx;
-          a.maxv[m] = v;
+        }
+        // kSub candidates per column; thread m combines them.
+        __shared__ float fin_v[128];
+        __shared__ int fin_i[128];
+        fin_v[e] = v;
+        fin_i[e] = idx;
+        epi_sync();
+        if (e < BN && e < a.M) {
+#pragma unroll
+          for (int k = 1; k < kSub; ++k)
+            if (better(fin_v[k * BN + e], fin_i[k * BN + e], v, idx)) { v = fin_v[k * BN + e]; idx = fin_i[k * BN + e]; }
+          a.ids[e] = idx;
+          if (a.ids2) a.ids2[e] = idx;
+          a.maxv[e] = v;
         }
         if (threadIdx.x == 64) *a.done_ctr = 0u;
       }
