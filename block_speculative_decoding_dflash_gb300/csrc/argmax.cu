@@ -182,9 +182,29 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
   const int v1 = min(a.V, v0 + kVerifyChunk);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
-  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    const float z = to_f(row[v]);
-    if (better(z, v, bv, bi)) { bv = z; bi = v; }
+  // 8 consecutive logits per load (16 bytes for bf16) when the row is
+  // 16-byte aligned; the chunk's 1024 groups are all requested up front.
+  if ((a.V & 7) == 0 && (reinterpret_cast<uintptr_t>(a.L) & 15) == 0 && sizeof(T) == 2) {
+    float z[4][8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = v0 + (threadIdx.x + k * 256) * 8;
+      if (v < v1) load8(row + v, z[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = v0 + (threadIdx.x + k * 256) * 8;
+      if (v < v1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (better(z[k][e], v + e, bv, bi)) { bv = z[k][e]; bi = v + e; }
+      }
+    }
+  } else {
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+      const float z = to_f(row[v]);
+      if (better(z, v, bv, bi)) { bv = z; bi = v; }
+    }
   }
   warp_argmax(bv, bi);
   if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = bv; si[threadIdx.x >> 5] = bi; }
@@ -198,15 +218,18 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
     a.part_i[(size_t)i * a.chunks + c] = bi;
   }
   if (last_cta(a.counter, gridDim.x * gridDim.y)) {
-    for (int r = threadIdx.x; r < a.B; r += blockDim.x) {
+    // warp w reduces rows w, w + 8, ...: lane q takes chunks q, q + 32, ...
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = warp; r < a.B; r += 8) {
       float v = -INFINITY;
       int idx = 0x7fffffff;
-      for (int q = 0; q < a.chunks; ++q) {
+      for (int q = lane; q < a.chunks; q += 32) {
         const float cv = __ldcg(a.part_v + (size_t)r * a.chunks + q);
         const int ci = __ldcg(a.part_i + (size_t)r * a.chunks + q);
         if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
       }
-      t_s[r] = idx;
+      warp_argmax(v, idx);
+      if (lane == 0) t_s[r] = idx;
     }
     __syncthreads();
     if (threadIdx.x == 0) {

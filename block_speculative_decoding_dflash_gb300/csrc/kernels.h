@@ -294,6 +294,7 @@ struct SynthArgs {
   const int* d;
   void* logits_out; void* resid_out;
   const RoundState* rs;
+  int vec;                     // set by the launcher: rows allow 16-byte copies
 };
 cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st);
 

@@ -258,24 +258,41 @@ __global__ void synth_target_kernel(SynthArgs a) {
   const int kl = static_cast<int>(r % a.n_logit);
   const int kc = static_cast<int>(r % a.n_coin);
   const int kr = static_cast<int>(r % a.n_resid);
-  const T* L = reinterpret_cast<const T*>(a.logit_pool) + (size_t)kl * a.block_max * a.V;
-  const T* P = reinterpret_cast<const T*>(a.plant) + (size_t)kl * a.block_max;
-  const uint8_t* C = a.coins + (size_t)kc * a.block_max;
-  const T* R = reinterpret_cast<const T*>(a.resid_pool) + (size_t)kr * a.block_max * a.kin;
-  T* Lo = reinterpret_cast<T*>(a.logits_out);
-  T* Ro = reinterpret_cast<T*>(a.resid_out);
-  const long long nl = (long long)a.block * a.V;
-  const long long nr = (long long)a.block * a.kin;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nl + nr; e += stride) {
-    if (e < nl) {
-      const int i = static_cast<int>(e / a.V);
-      const int v = static_cast<int>(e % a.V);
-      T val = L[(size_t)i * a.V + v];
-      if (i < a.block - 1 && C[i] && a.d[i] == v) val = P[i];
-      Lo[e] = val;
+  // block row i = blockIdx.y; this thread's 8 consecutive elements of the
+  // row's logits and of its residual row (16-byte copies when both rows are
+  // 16-byte aligned, element by element otherwise)
+  const int i = blockIdx.y;
+  const int v = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  const T* L = reinterpret_cast<const T*>(a.logit_pool) + ((size_t)kl * a.block_max + i) * a.V;
+  const T* R = reinterpret_cast<const T*>(a.resid_pool) + ((size_t)kr * a.block_max + i) * a.kin;
+  T* Lo = reinterpret_cast<T*>(a.logits_out) + (size_t)i * a.V;
+  T* Ro = reinterpret_cast<T*>(a.resid_out) + (size_t)i * a.kin;
+  const bool plant = i < a.block - 1 && a.coins[(size_t)kc * a.block_max + i];
+  const int di = plant ? a.d[i] : -1;
+  const T pv = plant ? reinterpret_cast<const T*>(a.plant)[(size_t)kl * a.block_max + i] : T{};
+  const bool vec = a.vec != 0;
+  if (v < a.V) {
+    if (vec && v + 8 <= a.V) {
+      uint4 u[sizeof(T) / 2];
+#pragma unroll
+      for (int k = 0; k < (int)(sizeof(T) / 2); ++k) u[k] = reinterpret_cast<const uint4*>(L + v)[k];
+      T* ue = reinterpret_cast<T*>(u);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (v + e == di) ue[e] = pv;
+#pragma unroll
+      for (int k = 0; k < (int)(sizeof(T) / 2); ++k) reinterpret_cast<uint4*>(Lo + v)[k] = u[k];
     } else {
-      Ro[e - nl] = R[e - nl];
+      for (int e = v; e < v + 8 && e < a.V; ++e) Lo[e] = e == di ? pv : L[e];
+    }
+  }
+  if (v < a.kin) {
+    if (vec && v + 8 <= a.kin) {
+#pragma unroll
+      for (int k = 0; k < (int)(sizeof(T) / 2); ++k)
+        reinterpret_cast<uint4*>(Ro + v)[k] = reinterpret_cast<const uint4*>(R + v)[k];
+    } else {
+      for (int e = v; e < v + 8 && e < a.kin; ++e) Ro[e] = R[e];
     }
   }
 }
@@ -410,11 +427,16 @@ cudaError_t launch_ring_gather(int dtype, const void* ring_k, const void* ring_v
 }
 
 cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st) {
-  const long long total = (long long)a.block * (a.V + a.kin);
-  const long long g = (total + 255) / 256;
-  const int grid = static_cast<int>(g < 2048 ? g : 2048);
-  if (dtype) launch_pdl(synth_target_kernel<bf16>, dim3(grid), dim3(256), 0, st, a);
-  else launch_pdl(synth_target_kernel<float>, dim3(grid), dim3(256), 0, st, a);
+  if (a.block <= 0) return cudaSuccess;
+  SynthArgs b = a;
+  const size_t esz = dtype ? 2 : 4;
+  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  b.vec = (a.V * esz) % 16 == 0 && (a.kin * esz) % 16 == 0 && al16(a.logit_pool) && al16(a.resid_pool) &&
+          al16(a.logits_out) && al16(a.resid_out);
+  const int n = a.V > a.kin ? a.V : a.kin;
+  const dim3 grid((n + 8 * 256 - 1) / (8 * 256), a.block);
+  if (dtype) launch_pdl(synth_target_kernel<bf16>, grid, dim3(256), 0, st, b);
+  else launch_pdl(synth_target_kernel<float>, grid, dim3(256), 0, st, b);
   return cudaGetLastError();
 }
 

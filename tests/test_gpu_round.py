@@ -362,3 +362,38 @@ def test_ring_floor_at_block_129(B, H, flags, corrupt):
         diff = (before_k != after_k).any(dim=-1).view(-1).nonzero().view(-1).tolist()
         assert diff == [0]                          # the oldest window row, overwritten by block row 128
     ring.close()
+
+
+# ---------------------------------------------------------------------------
+# stand-in target: the block's logits with the planted draft tokens, and the
+# captured residual rows, exactly as the host reference builds them
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,V,block", [("bf16", 1024, 4), ("bf16", 1001, 16), ("f32", 1024, 16),
+                                           ("f32", 999, 4)])
+def test_synth_target_matches_host(B, H, dtype, V, block):
+    cfg = synth.config("tiny", dtype=dtype, vocab=V, mask_token_id=V - 1, n_layers=1, max_block=16)
+    pair = H.Pair(cfg)
+    stream = synth.make_target_stream(cfg, 4, 16, seed=V + block, logit_pool=2, resid_pool=2, p_plant=0.8)
+    as_t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                      else np.ascontiguousarray(a)).cuda()
+    pools = {k: as_t(stream[k]) for k in ("logits", "plant", "coins", "resid")}
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kin = cfg["k_target_layers"] * cfg["target_hidden"]
+    d = np.random.default_rng(V).integers(0, V, block - 1).astype(np.int32)
+    ids = torch.from_numpy(d).cuda()
+    Lb = torch.zeros(block, V, dtype=tdt, device="cuda")
+    Rb = torch.zeros(block, kin, dtype=tdt, device="cuda")
+    pair.ctx.synth_target(pools["logits"].view(tdt) if dtype == "bf16" else pools["logits"],
+                          pools["plant"].view(tdt) if dtype == "bf16" else pools["plant"],
+                          pools["coins"], pools["resid"].view(tdt) if dtype == "bf16" else pools["resid"],
+                          block, ids, Lb, Rb)
+    pair.ctx.sync()
+    r = pair.ctx.stats()["rounds"]
+    want_l = synth.planted_logits(stream, r, block, d)
+    want_r = stream["resid"][r % stream["resid_pool"], :block]
+    got_l = Lb.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else Lb.cpu().numpy()
+    got_r = Rb.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else Rb.cpu().numpy()
+    assert np.array_equal(got_l, want_l)
+    assert np.array_equal(got_r, want_r)
+    pair.close()
