@@ -144,7 +144,7 @@ class ClockSampler:
 class Job:
     """Device-resident inputs, graphs and the round loop of one Muse job."""
 
-    SLOT_INGEST, SLOT_TIMED, SLOT_E2E = 1, 20, 40
+    SLOT_INGEST, SLOT_TIMED, SLOT_E2E, SLOT_E2E_B = 1, 20, 40, 41   # graph slots (< 64) + width
 
     def __init__(self, args, device):
         import torch
@@ -175,11 +175,16 @@ class Job:
         self.n = torch.zeros(1, dtype=torch.int32, device=device)
         self.Lb = torch.zeros(16, V, dtype=torch.bfloat16, device=device)
         self.Rb = torch.zeros(16, kin, dtype=torch.bfloat16, device=device)
-        # e2e staging (pool of one entry, refilled from pinned host memory per round)
-        self.st_L = torch.zeros(1, 16, V, dtype=torch.bfloat16, device=device)
-        self.st_P = torch.zeros(1, 16, dtype=torch.bfloat16, device=device)
-        self.st_C = torch.zeros(1, 16, dtype=torch.uint8, device=device)
-        self.st_R = torch.zeros(1, 16, kin, dtype=torch.bfloat16, device=device)
+        # e2e staging: two pools of one entry each, refilled from pinned host
+        # memory on a copy stream, round r into pool r % 2, so that round r + 1's
+        # inputs cross while round r computes
+        self.st = [(torch.zeros(1, 16, V, dtype=torch.bfloat16, device=device),
+                    torch.zeros(1, 16, dtype=torch.bfloat16, device=device),
+                    torch.zeros(1, 16, dtype=torch.uint8, device=device),
+                    torch.zeros(1, 16, kin, dtype=torch.bfloat16, device=device)) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.freed = [torch.cuda.Event() for _ in range(2)]
         pin = lambda a: torch.from_numpy(i16(a)).pin_memory()
         self.h_L = pin(self.ts["logits"]).view(torch.bfloat16)
         self.h_P = pin(self.ts["plant"]).view(torch.bfloat16)
@@ -203,12 +208,12 @@ class Job:
         c = self.ctx
         c.ingest_context(self.resid, self.cfg["context_rows"], 0, 5)
         dev_pools = (self.pool_L, self.pool_P, self.pool_C, self.pool_R)
-        st_pools = (self.st_L, self.st_P, self.st_C, self.st_R)
         for w in self.widths:
             self.bw = w
             self._round(dev_pools)                 # eager warm-up of this width
             for slot, timing, pools in ((w, False, dev_pools), (self.SLOT_TIMED + w, True, dev_pools),
-                                        (self.SLOT_E2E + w, False, st_pools)):
+                                        (self.SLOT_E2E + w, False, self.st[0]),
+                                        (self.SLOT_E2E_B + w, False, self.st[1])):
                 c.lm_head_timing(timing)
                 c.capture_begin()
                 self._round(pools)
@@ -221,7 +226,8 @@ class Job:
         c.ingest_gemm_timing(False)
         c.sync()
         self.kcount = {s: c.graph_kernel_count(s) for s in
-                       [self.SLOT_INGEST] + [x + w for w in self.widths for x in (0, self.SLOT_TIMED, self.SLOT_E2E)]}
+                       [self.SLOT_INGEST] + [x + w for w in self.widths
+                                             for x in (0, self.SLOT_TIMED, self.SLOT_E2E, self.SLOT_E2E_B)]}
 
     def run(self, e2e=False):
         """One job. Returns dict of counters; the caller brackets timing."""
@@ -232,6 +238,8 @@ class Job:
         if e2e:
             with torch.cuda.stream(s):
                 self.resid.copy_(self.h_resid, non_blocking=True)
+            for ev in self.freed:
+                ev.record(s)
         c.reset_stats()
         i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         i0.record(s)
@@ -250,17 +258,24 @@ class Job:
             for i in range(nr):
                 r = done + i
                 if e2e:
-                    with torch.cuda.stream(s):
-                        self.st_L[0, :w].copy_(self.h_L[r % 8, :w], non_blocking=True)
-                        self.st_P[0].copy_(self.h_P[r % 8], non_blocking=True)
-                        self.st_C[0].copy_(self.h_C[r], non_blocking=True)
-                        self.st_R[0, :w].copy_(self.h_R[r % 64, :w], non_blocking=True)
-                    slot = self.SLOT_E2E + w
+                    k = r % 2
+                    stL, stP, stC, stR = self.st[k]
+                    cs = self.copy_stream
+                    cs.wait_event(self.freed[k])   # the round that last read pool k is done
+                    with torch.cuda.stream(cs):
+                        stL[0, :w].copy_(self.h_L[r % 8, :w], non_blocking=True)
+                        stP[0].copy_(self.h_P[r % 8], non_blocking=True)
+                        stC[0].copy_(self.h_C[r], non_blocking=True)
+                        stR[0, :w].copy_(self.h_R[r % 64, :w], non_blocking=True)
+                        self.copied[k].record(cs)
+                    s.wait_event(self.copied[k])
+                    slot = (self.SLOT_E2E if k == 0 else self.SLOT_E2E_B) + w
                 else:
                     slot = self.SLOT_TIMED + w if i == 0 else w
                 c.graph_launch(slot)
                 launches += self.kcount[slot]
                 if e2e:
+                    self.freed[r % 2].record(s)
                     with torch.cuda.stream(s):
                         self.h_out[r, :16].copy_(self.tok, non_blocking=True)
                         self.h_out[r, 16:].copy_(self.n, non_blocking=True)
