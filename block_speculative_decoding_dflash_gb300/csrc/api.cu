@@ -197,7 +197,6 @@ struct dflash_ctx {
   float* tc_lm_pv = nullptr;
   int* tc_lm_pi = nullptr;
   unsigned* tc_done = nullptr;
-  unsigned* attn_ctr = nullptr;
   const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
   // persistent draft kernel (bf16, head_dim 128, up to 16 block rows)
   bool draft_fused_ok = false;                 // the config and device allow it
@@ -529,9 +528,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.max_ctx = c->max_ctx;
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
-  at.head_ctr = c->attn_ctr;
   at.err = c->tc_err;
-  at.sms = c->num_sms;
   at.trace = ktrace_slot(c, ln + "attn", 4);
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
@@ -849,7 +846,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
-      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64, (size_t)2 * c->nkv * 4,
+      (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64,
       (size_t)cfg->n_layers * sizeof(void*)};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
@@ -894,7 +891,6 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->tc_lm_pv = carve<float>(cur, sizes[si++]);
   c->tc_lm_pi = carve<int>(cur, sizes[si++]);
   c->tc_done = carve<unsigned>(cur, sizes[si++]);
-  c->attn_ctr = carve<unsigned>(cur, sizes[si++]);
   c->kgain_dev = carve<const void*>(cur, sizes[si++]);
 
   std::vector<const void*> kg(cfg->n_layers);

@@ -177,7 +177,7 @@ cudaError_t init_attention_attrs(int hd) {
 }
 
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st) {
-  if (attention_mma_ok(dtype, a.hd) && a.head_ctr) return launch_attention_mma(a, a.head_ctr, st);
+  if (attention_mma_ok(dtype, a.hd)) return launch_attention_mma(a, st);
   const int nsplit = num_splits(a.rows, a.max_ctx);
   const size_t smem = partial_smem(a.hd);
   dim3 grid(nsplit, a.nkv);

@@ -1,14 +1,15 @@
 // Bidirectional sliding-window GQA attention of the drafter block, bf16,
-// head_dim 128, on tensor cores (mma.sync m16n8k16, fp32 accumulate).
+// head_dim 128, on tensor cores, one CTA per (split of kKeys = 128 keys, kv
+// head g); the queries of g are the block rows x its G query heads.
 //
-// One CTA per (split of kKeys = 128 keys, kv head g); its 8 warps each own 16
-// keys. For every 16-query tile (queries = block rows x the G query heads of
-// g): S = Q K^T for the warp's keys (mask |q - k| <= W by absolute
-// positions), the warp's online-softmax partial (max, sum, P V), a merge of
-// the 8 warps in shared memory in warp order, and the CTA's partial written
-// to global scratch. A combine kernel (one warp per (query, head)) merges the
-// splits in split order and writes the bf16 output; nothing waits on another
-// CTA and the result is deterministic.
+// One 16-query tile (attn_mma_kernel, mma.sync m16n8k16, fp32 accumulate):
+// the 8 warps each own 16 keys: S = Q K^T for the warp's keys (mask |q - k|
+// <= W by absolute positions), the warp's online-softmax partial (max, sum,
+// P V), a merge of the 8 warps in shared memory in warp order, and the CTA's
+// partial written to global scratch. Two to four tiles: attn_tc_kernel
+// (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
+// merges the splits in split order and writes the bf16 output; nothing waits
+// on another CTA and the result is deterministic.
 //
 // Keys are addressed by absolute position (ring slot = position mod cap), the
 // context keys [kstart, p) followed by the block's own rows.
@@ -25,8 +26,7 @@ namespace {
 constexpr int kHd = kAttnHd;
 constexpr int kKeys = kAttnKeys;
 constexpr int kWarps = 8;
-constexpr int kPad = 8;                    // bf16 elements of row padding
-constexpr int kRowB = (kHd + kPad) * 2;    // 272-byte rows: conflict-free ldmatrix
+constexpr int kPad = 8;                    // bf16 elements of row padding (conflict-free ldmatrix)
 constexpr int kPartStride = kAttnPartStride;
 constexpr int kQChunk = 64;
 
@@ -227,90 +227,68 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   if (threadIdx.x == 0) ktrace_mark(a.trace, 2);
 }
 
-// ---------------------------------------------------------------------------
-// Up to 64 queries per kv head (block rows x query heads per kv head): the 8
-// warps split (16-query tile) x (key group) — 1 tile x 8 groups of 16 keys,
-// 2 x 4 of 32, or 4 x 2 of 64 — and each runs an online softmax over its keys.
-// Once every warp is done with K and V their shared memory holds the warps'
-// partials, which are merged per query in group order and written out. 87 KB
-// of shared memory, so the next GEMM's CTAs fit beside it and start streaming
-// their weights.
-// ---------------------------------------------------------------------------
-constexpr int kTileQ = 64;
-
-// Phase stamps of the tile kernel in the two trace slots after its own
-// (latest CTA; allotted only when the split merge is folded in): slot + 1 gets
-// [1] loads landed, [2] per-warp attention done; slot + 2 gets [1] partials
-// written, [2] the head's splits all present.
-__device__ __forceinline__ void attn_phase(const KTrace& t, int slot_off, int k) {
-  if (t.p && threadIdx.x == 0) ktrace_mark(KTrace{t.p, t.slot + slot_off}, k);
+// One warp per (query, kv head): merge the splits' partials in split order.
+__global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int nsplit) {
+  const KTrace tr{a.trace.p, a.trace.slot + 1};
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
+  pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.nq / a.nkv;
+  const int Qn = a.rows * G;
+  const int item = blockIdx.x * 4 + warp;
+  if (item < a.nkv * Qn)
+    attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
+                      reinterpret_cast<bf16*>(a.out), a.ldo, lane);
+  if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
 }
 
-// The split merge inside the attention kernel, for grids of at most one CTA
-// per SM (all resident, so waiting on the other splits of a head cannot
-// block them): split s of kv head g arrives on the head's counter after
-// writing its partial, waits for the head's other splits (bounded), then its
-// warps merge queries s, s + nsplit, ... of that head (in split order, as the
-// standalone merge kernel does). The last split to leave rearms the counters.
-__device__ __noinline__ void merge_splits(const AttnArgs& a, int nsplit, int s, int g, int G, int Qn) {
-  unsigned* arrive = a.head_ctr + g;
-  unsigned* depart = a.head_ctr + a.nkv + g;
-  __shared__ int s_ok;
-  __syncthreads();
-  const bool mine = s < Qn;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(arrive, 1u);
-    int ok = 1;
-    if (mine) {
-      unsigned spins = 0;
-      while (*reinterpret_cast<volatile unsigned*>(arrive) < static_cast<unsigned>(nsplit)) {
-        if (++spins > (1u << 24)) { atomicOr(a.err, 16); ok = 0; break; }
-        __nanosleep(64);
-      }
-      __threadfence();
-      if (a.trace.p) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 2);
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  if (mine && s_ok) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int qi = s + nsplit * warp; qi < Qn; qi += nsplit * kWarps)
-      attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, g, qi, reinterpret_cast<bf16*>(a.out), a.ldo, lane);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(depart, 1u) == static_cast<unsigned>(nsplit - 1)) {
-    *arrive = 0u;                     // every split of the head is past its wait
-    *depart = 0u;
-  }
+constexpr int kTileQ = 64;                 // queries per kv head of the tensor-core kernel
+
+// ---------------------------------------------------------------------------
+// Up to 64 queries per kv head on the 5th-generation tensor cores. Per key
+// split: S = Q K^T and then O = P V, each one 128 x 128 x 128 product issued
+// as eight tcgen05.mma (kind::f16, fp32 accumulators in TMEM). Operands are
+// K-major shared-memory tiles in the 128-byte swizzled layout: Q and K as
+// loaded, V transposed in shared memory (keys along K), P written by the
+// softmax threads into Q's place once S is done.
+//
+// The 64 queries fill operand rows 0-63 and again 64-127, so that all eight
+// warps can read S back (a warp reads the TMEM lanes of its quarter): row R
+// holds query R mod 64, and its P row carries only the keys of its half
+// (R < 64: keys 0-63, else 64-127; zeros elsewhere), so O = P V leaves two
+// partial products per query, added when O is read back. Each thread takes
+// 32 keys of one row for the softmax (the row's maximum and sum combine four
+// threads through shared memory). Same partial format as the kernel above;
+// the separate merge kernel combines the splits (folding the merge into this
+// kernel, with every split of a head waiting for the others, measured 12 us
+// per draft slower at 16 block rows: it keeps the 131 KB CTAs resident while
+// the next GEMM's CTAs wait for their shared memory).
+// ---------------------------------------------------------------------------
+constexpr int kTcTileB = 128 * 128;                  // one 128-row x 64-column bf16 tile
+constexpr int kTcQ = 0, kTcK = 2 * kTcTileB, kTcVt = 4 * kTcTileB, kTcVs = 6 * kTcTileB;
+constexpr int kTcVsRow = kHd * 2 + 16;               // padded staging rows of V
+constexpr int kTcBars = kTcVs + kKeys * kTcVsRow;
+constexpr size_t kTcAttnSmem = (size_t)kTcBars + 64 + 1024;
+constexpr int kTcOStride = kHd + 4;                  // O staging rows (floats), over K and V^T
+static_assert(kTileQ * kTcOStride * 4 <= 4 * kTcTileB, "O staging must fit in the K and V^T tiles");
+
+// Byte offset of element (row, col) of a 128-row x 128-column bf16 operand
+// stored as two K-major 64-column tiles with 16-byte granules swizzled by row.
+__device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
+  return (col >> 6) * kTcTileB + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2;
 }
 
-struct TileSmem {
-  union {
-    struct {
-      bf16 k[kKeys][kHd + kPad];
-      bf16 v[kKeys][kHd + kPad];
-    } kv;
-    struct {
-      float o[kWarps][16][kHd];
-      float m[kWarps][16];
-      float l[kWarps][16];
-      float f[kTileQ][kWarps];
-      float M[kTileQ];
-      float L[kTileQ];
-    } mg;
-  };
-  bf16 q[kTileQ][kHd + kPad];
-};
-static_assert(sizeof(TileSmem) <= 90 * 1024, "attention tile too large to share an SM with a GEMM CTA");
-
-__global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int nsplit, int merge) {
+__global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
   if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  TileSmem& S = *reinterpret_cast<TileSmem*>(smem_raw);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kTcBars);     // [0] S ready, [1] O ready
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 2);
+  __shared__ float red_m[4][kTileQ], red_l[4][kTileQ];
   const int s = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
@@ -338,10 +316,18 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
       const int d = e % kPartStride;
       part[e] = d == kHd ? -INFINITY : 0.f;
     }
-    if (merge) merge_splits(a, nsplit, s, g, G, Qn);
     if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
     return;
   }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_holder, 256);
+
+  // K into its tile, V into padded staging rows (keys past nk zero-filled),
+  // each query into rows r and r + 64
   for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
     const int j = e >> 4, ch = e & 15;
     const int kj = j0 + j;
@@ -358,176 +344,153 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tile_kernel(AttnArgs a, int 
       ks = kb + off;
       vs = vb + off;
     }
-    cp_async16(&S.kv.k[j][ch * 8], ks, valid);
-    cp_async16(&S.kv.v[j][ch * 8], vs, valid);
+    cp_async16(sm + kTcK + tc_sw128(j, ch * 8), ks, valid);
+    cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, vs, valid);
   }
-  const int nqt = (Qn + 15) / 16;
-  for (int e = threadIdx.x; e < nqt * 16 * (kHd / 8); e += blockDim.x) {
-    const int r = e >> 4, ch = e & 15;
-    const bool valid = r < Qn;
-    const bf16* src = qg;
-    if (valid) src = qg + (size_t)(r / G) * ldq + (size_t)(r % G) * kHd + ch * 8;
-    cp_async16(&S.q[r][ch * 8], src, valid);
+  for (int e = threadIdx.x; e < 2 * kTileQ * (kHd / 8); e += blockDim.x) {
+    const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
+    const bool valid = qr < Qn;
+    const bf16* src = valid ? qg + (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : qg;
+    cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), src, valid);
   }
   cp_async_wait_all();
+  fence_proxy_async_shared();
+  tc_fence_before();
   __syncthreads();
-  if (merge) attn_phase(a.trace, 1, 1);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  constexpr uint32_t idesc = idesc_bf16(128, 128);
+  const uint32_t sbase = smem_u32(sm);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_bf16(tmem, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
+                    smem_desc_sw128(sbase + kTcK + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
+    tc_commit(&bar[0]);
+  }
+  // V^T while S is computed: the lanes of a warp take consecutive keys of one
+  // 8-dim granule, so each of its stores fills part of one row (fenced for
+  // the tensor cores with P below)
+  for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
+    const int j = e & (kKeys - 1), ch = e >> 7;
+    const uint4 u = *reinterpret_cast<const uint4*>(sm + kTcVs + j * kTcVsRow + ch * 16);
+    const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) *reinterpret_cast<bf16*>(sm + kTcVt + tc_sw128(ch * 8 + t, j)) = h[t];
+  }
 
-  const int kg = nqt == 1 ? 8 : nqt == 2 ? 4 : 2;   // key groups per query tile
-  const int span = kKeys / kg;                        // keys per warp
-  const int qt = warp / kg, gk = warp % kg;
-  const bool busy = qt < nqt;
-  const int grp = lane >> 2, tig = lane & 3, mi = lane >> 3;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float o[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  if (busy) {
-    const float scale = rsqrtf(static_cast<float>(kHd));
-    int qrel[2];
-    bool qok[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int qi = qt * 16 + grp + hr * 8;
-      qok[hr] = qi < Qn;
-      qrel[hr] = qok[hr] ? qi / G : 0;
-    }
-    // the warp's 16 queries as MMA A fragments, loaded once for all its keys
-    uint32_t qa[kHd / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < kHd / 16; ++ks)
-      ldsm_x4(&S.q[qt * 16 + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], qa[ks][0], qa[ks][1],
-              qa[ks][2], qa[ks][3]);
-    for (int kb0 = gk * span; kb0 < (gk + 1) * span; kb0 += 16) {
-      const int kj0 = j0 + kb0;
-      if (kj0 >= nk) break;
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < kHd / 16; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(&S.kv.k[kb0 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
-        mma16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-      }
-      float mb[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int kj = kj0 + nt * 8 + tig * 2 + c;
-            bool vis = qok[hr] && kj < nk;
-            if (window > 0) {
-              const int d = qrel[hr] - (kj - nctx);          // positions relative to the block
-              vis = vis && (d < 0 ? -d : d) <= window;
-            }
-            float& v = sc[nt][hr * 2 + c];
-            v = vis ? v * scale : -INFINITY;
-            mb[hr] = fmaxf(mb[hr], v);
-          }
-        mb[hr] = fmaxf(mb[hr], __shfl_xor_sync(0xffffffffu, mb[hr], 1));
-        mb[hr] = fmaxf(mb[hr], __shfl_xor_sync(0xffffffffu, mb[hr], 2));
-      }
-      uint32_t pa[4];
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const float m_new = fmaxf(m_run[hr], mb[hr]);
-        const float alpha = m_run[hr] == -INFINITY ? 0.f : expf(m_run[hr] - m_new);
-        float pv[2][2];
-        float ls = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const float v = sc[nt][hr * 2 + c];
-            pv[nt][c] = (m_new == -INFINITY || v == -INFINITY) ? 0.f : expf(v - m_new);
-            ls += pv[nt][c];
-          }
-        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-        l_run[hr] = l_run[hr] * alpha + ls;
-        m_run[hr] = m_new;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) { o[nt][hr * 2] *= alpha; o[nt][hr * 2 + 1] *= alpha; }
-        pa[hr] = pack_bf16(pv[0][0], pv[0][1]);
-        pa[2 + hr] = pack_bf16(pv[1][0], pv[1][1]);
-      }
-#pragma unroll
-      for (int dt = 0; dt < kHd / 16; ++dt) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(&S.kv.v[kb0 + (mi & 1) * 8 + (lane & 7)][dt * 16 + (mi >> 1) * 8], b0, b1, b2, b3);
-        mma16816(o[dt * 2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-        mma16816(o[dt * 2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-      }
-    }
+  // thread: operand row R (TMEM lane), query qi = R mod 64, keys kc0 .. kc0 + 31
+  const int quad = warp & 3, half = warp >> 2;
+  const int R = quad * 32 + lane, qi = R & (kTileQ - 1), rh = R >> 6;
+  const int grp = rh * 2 + half;                       // which quarter of the keys
+  const int kc0 = grp * 32;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  // visible keys of this query: kpos = kstart + kj within the window of its
+  // position, kj < nk (0 <= lo, hi < nk)
+  int lo = 0, hi = nk - 1;
+  if (qi >= Qn) {
+    lo = 1; hi = 0;
+  } else if (window > 0) {
+    const long long rel = p + qi / G - kstart;           // query position - kstart
+    if (rel - window > lo) lo = static_cast<int>(rel - window);
+    if (rel + window < hi) hi = static_cast<int>(rel + window);
   }
-  __syncthreads();                                    // K and V are no longer read
-  if (merge) attn_phase(a.trace, 1, 2);
-  if (busy) {
+  const float sl2 = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;   // scale * log2(e)
+  bool ok = mbar_wait(&bar[0], 0);
+  tc_fence_after();
+  float sv[32];
+  tmem_ld16(trow + kc0, &sv[0]);
+  tmem_ld16(trow + kc0 + 16, &sv[16]);
+  tmem_ld_wait();
+  float mrow = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
+  for (int c = 0; c < 32; ++c) {
+    const int kj = j0 + kc0 + c;
+    sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sl2 : -INFINITY;
+    mrow = fmaxf(mrow, sv[c]);
+  }
+  red_m[grp][qi] = mrow;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
+  float l = 0.f;
+  uint32_t pk[16];
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr)
-        *reinterpret_cast<float2*>(&S.mg.o[warp][grp + hr * 8][nt * 8 + tig * 2]) =
-            make_float2(o[nt][hr * 2], o[nt][hr * 2 + 1]);
-    if (tig == 0) {
-      S.mg.m[warp][grp] = m_run[0]; S.mg.m[warp][grp + 8] = m_run[1];
-      S.mg.l[warp][grp] = l_run[0]; S.mg.l[warp][grp + 8] = l_run[1];
-    }
+  for (int c = 0; c < 32; c += 2) {
+    const float p0 = (M == -INFINITY || sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - M);
+    const float p1 = (M == -INFINITY || sv[c + 1] == -INFINITY) ? 0.f : exp2f(sv[c + 1] - M);
+    l += p0 + p1;
+    pk[c >> 1] = pack_bf16(p0, p1);
+  }
+  red_l[grp][qi] = l;
+  // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
+  // over the same granules of the other tile
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    const int gg = half * 4 + gi;
+    *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + R * 128 + ((gg ^ (R & 7)) << 4)) =
+        make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
+    *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + R * 128 + ((gg ^ (R & 7)) << 4)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
+                    smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
+    tc_commit(&bar[1]);
+  }
+  // O: rows R and R + 64 hold the two halves of query qi's sum; each thread
+  // reads 64 dims of its row, the low rows store them, the high rows add
+  ok = mbar_wait(&bar[1], 0) && ok;
+  tc_fence_after();
+  float ov[64];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
+  tmem_ld_wait();
+  float* ost = reinterpret_cast<float*>(sm + kTcK) + qi * kTcOStride + half * 64;
+  if (rh == 0) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      *reinterpret_cast<float4*>(ost + 4 * i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
   }
   __syncthreads();
-  // merge weights: one thread per query
-  if (threadIdx.x < Qn) {
-    const int qi = threadIdx.x, t = qi >> 4, r = qi & 15;
-    float M = -INFINITY;
-    for (int x = 0; x < kg; ++x) M = fmaxf(M, S.mg.m[t * kg + x][r]);
-    float L = 0.f;
-    for (int x = 0; x < kg; ++x) {
-      const float mw = S.mg.m[t * kg + x][r];
-      const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : expf(mw - M);
-      S.mg.f[qi][x] = f;
-      L += f * S.mg.l[t * kg + x][r];
+  if (rh == 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float4 x = *reinterpret_cast<float4*>(ost + 4 * i);
+      x.x += ov[4 * i]; x.y += ov[4 * i + 1]; x.z += ov[4 * i + 2]; x.w += ov[4 * i + 3];
+      *reinterpret_cast<float4*>(ost + 4 * i) = x;
     }
-    S.mg.M[qi] = M;
-    S.mg.L[qi] = L;
   }
+  if (!ok && lane == 0) atomicOr(a.err, 32);
+  tc_fence_before();
   __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+  // the split's partial, one query row per warp pass (coalesced)
+  const float* osm = reinterpret_cast<const float*>(sm + kTcK);
   for (int e = threadIdx.x; e < Qn * (kHd / 4); e += blockDim.x) {
-    const int qi = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-    const int t = qi >> 4, r = qi & 15;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x = 0; x < kg; ++x) {
-      const float f = S.mg.f[qi][x];
-      const float4 ov = *reinterpret_cast<const float4*>(&S.mg.o[t * kg + x][r][d4]);
-      acc.x += f * ov.x; acc.y += f * ov.y; acc.z += f * ov.z; acc.w += f * ov.w;
+    const int q = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+    float* out = part + (size_t)q * kPartStride;
+    *reinterpret_cast<float4*>(out + d4) = *reinterpret_cast<const float4*>(osm + q * kTcOStride + d4);
+    if (d4 == 0) {
+      // the row's maximum in natural-log units, as the merge expects
+      const float Mq = fmaxf(fmaxf(red_m[0][q], red_m[1][q]), fmaxf(red_m[2][q], red_m[3][q]));
+      out[kHd] = Mq == -INFINITY ? -INFINITY : Mq * 0.6931471805599453f;
+      out[kHd + 1] = (red_l[0][q] + red_l[1][q]) + (red_l[2][q] + red_l[3][q]);
     }
-    float* out = part + (size_t)qi * kPartStride;
-    *reinterpret_cast<float4*>(out + d4) = acc;
-    if (d4 == 0) { out[kHd] = S.mg.M[qi]; out[kHd + 1] = S.mg.L[qi]; }
-  }
-  if (merge) {
-    __syncthreads();
-    attn_phase(a.trace, 2, 1);
-    merge_splits(a, nsplit, s, g, G, Qn);
   }
   if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
-}
-
-// One warp per (query, kv head): merge the splits' partials in split order.
-__global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int nsplit) {
-  const KTrace tr{a.trace.p, a.trace.slot + 1};
-  if (threadIdx.x == 0) ktrace_mark(tr, 0);
-  pdl_enter();
-  if (threadIdx.x == 0) ktrace_mark(tr, 1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = a.nq / a.nkv;
-  const int Qn = a.rows * G;
-  const int item = blockIdx.x * 4 + warp;
-  if (item < a.nkv * Qn)
-    attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
-                      reinterpret_cast<bf16*>(a.out), a.ldo, lane);
-  if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
 }
 
 }  // namespace
@@ -541,24 +504,24 @@ size_t attention_mma_scratch_floats(int rows, int nq, int nkv, int max_ctx) {
 bool attention_mma_ok(int dtype, int hd) { return dtype == 1 && hd == kHd; }
 
 cudaError_t init_attention_mma_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(TileSmem));
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kTcAttnSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)sizeof(MmaSmem));
 }
 
-cudaError_t launch_attention_mma(const AttnArgs& a, unsigned*, cudaStream_t st) {
+cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
   const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
   dim3 grid(nsplit, a.nkv);
   const int Qn = a.rows * (a.nq / a.nkv);
-  // The 87 KB tile kernel with the split merge folded in pays from two query
-  // tiles on (A/B on one GB300: -12 us per draft at 64 queries per kv head);
-  // at one tile the 8-warp key split with its separate merge is faster (-6 us).
+  // Two to four 16-query tiles per kv head: the tensor-core kernel (A/B on
+  // one GB300 at 64 queries per kv head: 16 us per draft faster than an
+  // mma.sync kernel with the split merge folded in). One tile: the 8-warp key
+  // split on mma.sync.
   if (Qn > 16 && Qn <= kTileQ) {
-    const int merge = (a.head_ctr && a.err && nsplit * a.nkv <= a.sms) ? 1 : 0;
-    cudaError_t e = launch_pdl(attn_tile_kernel, grid, dim3(kWarps * 32), sizeof(TileSmem), st, a, nsplit, merge);
-    if (e != cudaSuccess || merge) return e;
+    cudaError_t e = launch_pdl(attn_tc_kernel, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = launch_pdl(attn_mma_kernel, grid, dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit);
     if (e != cudaSuccess) return e;

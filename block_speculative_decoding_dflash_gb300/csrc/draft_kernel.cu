@@ -80,9 +80,6 @@ __device__ __forceinline__ unsigned long long gtimer() {
 __device__ __forceinline__ unsigned ld_volatile(const unsigned* p) {
   return *reinterpret_cast<const volatile unsigned*>(p);
 }
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Trace stamp k of phase p on this CTA (tracing on only).
 __device__ __forceinline__ void stamp(unsigned long long* trace, int p, int k) {

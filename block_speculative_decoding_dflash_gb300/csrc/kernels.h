@@ -205,11 +205,7 @@ struct AttnArgs {
   int max_ctx;                 // most context keys any round can see
   float* partial;              // scratch [nkv][nsplit][rows*G][hd + 2]
   void* out; int ldo;          // [rows, nq, hd]
-  unsigned* head_ctr;          // [2 * nkv] arrivals then departures per kv head, zero
-                               // between launches (tensor-core path)
-  int* err;                    // bounded-wait timeouts are reported here (bit 16)
-  int sms;                     // SMs: the split merge joins the attention kernel when the
-                               // grid fits one CTA per SM
+  int* err;                    // bounded-wait timeouts are reported here (bit 32)
   KTrace trace;                // attention kernel; the separate merge kernel uses slot + 1
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
@@ -217,7 +213,7 @@ cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 bool attention_mma_ok(int dtype, int hd);
 size_t attention_mma_scratch_floats(int rows, int nq, int nkv, int max_ctx);
 cudaError_t init_attention_mma_attrs();
-cudaError_t launch_attention_mma(const AttnArgs& a, unsigned* head_ctr, cudaStream_t st);
+cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st);
 size_t attention_scratch_floats(int rows, int nq, int nkv, int hd, int max_ctx);
 cudaError_t init_attention_attrs(int hd);
 

@@ -67,6 +67,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tcgen05.mma operands, TMA stores).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Asks L2 to fetch `bytes` (a multiple of 16) from global address p (16-byte
 // aligned); a hint only, with no completion to wait for.
 __device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
