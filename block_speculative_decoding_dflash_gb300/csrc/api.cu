@@ -487,7 +487,12 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
                             ktrace_slot(c, ln + "in_norm")));
   const bool tc = c->use_tc && rows <= 32;
   const int bi = bn_index(rows);
-  const bool fused_qk = tc && c->hd == 128;
+  // q/k head norm + RoPE: applied by the tensor-core attention kernels as they
+  // load q and the block's k rows (the QKV GEMM then just stores, and its
+  // split tiles finish sooner); else in the QKV GEMM's epilogue, else by
+  // their own kernel
+  const bool attn_norm = tc && attention_mma_ok(dt, c->hd);
+  const bool fused_qk = tc && c->hd == 128 && !attn_norm;
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, fused_qk ? kEpiQKV : kEpiStore);
     tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
@@ -506,7 +511,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
     CK(c->err, launch_linear_rows(dt, q, st));
   }
-  if (!fused_qk) {
+  if (!fused_qk && !attn_norm) {
     CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
                                      c->rope, c->cfg.rope_neox, st));
     CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
@@ -530,6 +535,10 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.out = c->attn; at.ldo = c->qdim;
   at.err = c->tc_err;
   at.trace = ktrace_slot(c, ln + "attn", 4);
+  if (attn_norm) {
+    at.qn = LW(c, l, kQNorm); at.kn = LW(c, l, kKNorm);
+    at.rope = c->rope; at.neox = c->cfg.rope_neox; at.eps = eps;
+  }
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);

@@ -103,9 +103,34 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       cp_async16(&S.v[j][ch * 8], vs, valid);
     }
   }
+  // Raw projections (a.qn set): per-head RMSNorm + RoPE of the loaded query
+  // rows and of the block's own keys in this split, four threads a row.
+  auto norm_q = [&](int q0) {
+    const int r = threadIdx.x >> 2, t = threadIdx.x & 3;
+    const int qi = q0 + r;
+    if (r >= kQChunk || qi >= Qn) return;
+    qk_norm_rope_quad([&](int d) { return __bfloat162float(S.q[r][d]); },
+                      [&](int d, float v) { S.q[r][d] = __float2bfloat16_rn(v); },
+                      reinterpret_cast<const bf16*>(a.qn), a.eps, a.rope + (size_t)(qi / G) * (kHd / 2),
+                      a.neox, t);
+  };
+  const bool norm = a.qn != nullptr;
   load_q(0);
   cp_async_wait_all();
   __syncthreads();
+  if (norm) {
+    norm_q(0);
+    const int kb0 = nctx > j0 ? nctx - j0 : 0;
+    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
+    for (int e = threadIdx.x; e < (kb1 - kb0) * 4; e += blockDim.x) {
+      const int j = kb0 + (e >> 2);
+      qk_norm_rope_quad([&](int d) { return __bfloat162float(S.k[j][d]); },
+                        [&](int d, float v) { S.k[j][d] = __float2bfloat16_rn(v); },
+                        reinterpret_cast<const bf16*>(a.kn), a.eps,
+                        a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, e & 3);
+    }
+    __syncthreads();
+  }
 
   const int grp = lane >> 2, tig = lane & 3;
   const float scale = rsqrtf(static_cast<float>(kHd));
@@ -115,6 +140,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       load_q(qt * 16);
       cp_async_wait_all();
       __syncthreads();
+      if (norm) {
+        norm_q(qt * 16);
+        __syncthreads();
+      }
     }
     float m_row[2] = {-INFINITY, -INFINITY}, l_row[2] = {0.f, 0.f};
     float o[16][4];
@@ -347,13 +376,45 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     cp_async16(sm + kTcK + tc_sw128(j, ch * 8), ks, valid);
     cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, vs, valid);
   }
-  for (int e = threadIdx.x; e < 2 * kTileQ * (kHd / 8); e += blockDim.x) {
+  // raw projections: each query into row r only, then normalised into r and r + 64
+  const bool norm = a.qn != nullptr;
+  for (int e = threadIdx.x; e < (norm ? 1 : 2) * kTileQ * (kHd / 8); e += blockDim.x) {
     const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
     const bool valid = qr < Qn;
     const bf16* src = valid ? qg + (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : qg;
     cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), src, valid);
   }
   cp_async_wait_all();
+  if (norm) {
+    __syncthreads();
+    // per-head RMSNorm + RoPE of the queries (four threads a row) and of the
+    // block's own keys in this split (the ring's keys are stored normalised)
+    const int t = threadIdx.x & 3;
+    {
+      const int r = threadIdx.x >> 2;
+      if (r < Qn) {
+        bf16* q0 = reinterpret_cast<bf16*>(sm + kTcQ);
+        qk_norm_rope_quad(
+            [&](int d) { return __bfloat162float(q0[tc_sw128(r, d) >> 1]); },
+            [&](int d, float v) {
+              const bf16 b = __float2bfloat16_rn(v);
+              q0[tc_sw128(r, d) >> 1] = b;
+              q0[tc_sw128(r + kTileQ, d) >> 1] = b;
+            },
+            reinterpret_cast<const bf16*>(a.qn), a.eps, a.rope + (size_t)(r / G) * (kHd / 2), a.neox, t);
+      }
+    }
+    const int kb0 = nctx > j0 ? nctx - j0 : 0;           // first block key of this split
+    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
+    for (int e = threadIdx.x; e < (kb1 - kb0) * 4; e += blockDim.x) {
+      const int j = kb0 + (e >> 2);
+      bf16* k0 = reinterpret_cast<bf16*>(sm + kTcK);
+      qk_norm_rope_quad([&](int d) { return __bfloat162float(k0[tc_sw128(j, d) >> 1]); },
+                        [&](int d, float v) { k0[tc_sw128(j, d) >> 1] = __float2bfloat16_rn(v); },
+                        reinterpret_cast<const bf16*>(a.kn), a.eps,
+                        a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, t);
+    }
+  }
   fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();

@@ -207,6 +207,13 @@ struct AttnArgs {
   void* out; int ldo;          // [rows, nq, hd]
   int* err;                    // bounded-wait timeouts are reported here (bit 32)
   KTrace trace;                // attention kernel; the separate merge kernel uses slot + 1
+  // When qn is set (tensor-core path only), q and the block's k rows are the
+  // raw projections: the kernel applies the per-head RMSNorm (gains qn / kn,
+  // [hd]) and RoPE (rope[m * hd/2 + i] for block row m) as it loads them.
+  const void* qn; const void* kn;
+  const float2* rope;
+  int neox;
+  float eps;
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.
