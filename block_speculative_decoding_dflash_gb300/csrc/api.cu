@@ -488,19 +488,14 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   const bool tc = c->use_tc && rows <= 32;
   const int bi = bn_index(rows);
   // q/k head norm + RoPE: applied by the tensor-core attention kernels as they
-  // load q and the block's k rows (the QKV GEMM then just stores, and its
-  // split tiles finish sooner); else in the QKV GEMM's epilogue, else by
-  // their own kernel
+  // load q and the block's k rows (the QKV GEMM then just stores, so its
+  // split tiles finish sooner), else by their own kernel
   const bool attn_norm = tc && attention_mma_ok(dt, c->hd);
-  const bool fused_qk = tc && c->hd == 128 && !attn_norm;
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, fused_qk ? kEpiQKV : kEpiStore);
+    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, kEpiStore);
     tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
     t.b_map = c->xn_map[bi];
     t.y = c->qkv; t.ldy = c->qkv_n;
-    t.nq_tiles = c->nq; t.nkv = c->nkv;
-    t.qn = LW(c, l, kQNorm); t.kn = LW(c, l, kKNorm);
-    t.rope = c->rope; t.neox = c->cfg.rope_neox; t.eps = eps;
     t.trace = ktrace_slot(c, ln + "qkv", 4);
     CK(c->err, tc_run(c, t));
   } else {
@@ -511,7 +506,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
     CK(c->err, launch_linear_rows(dt, q, st));
   }
-  if (!fused_qk && !attn_norm) {
+  if (!attn_norm) {
     CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
                                      c->rope, c->cfg.rope_neox, st));
     CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,

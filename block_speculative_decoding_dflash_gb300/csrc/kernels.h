@@ -34,7 +34,7 @@ struct LinearArgs {
 enum : int {
   kEpiArgmax = 3,   // tensor-core GEMM only: softcap + per-row argmax
   kEpiKVRing = 4,   // tensor-core GEMM only: K head-norm + RoPE / V, into ring slots
-  kEpiQKV = 5,      // tensor-core GEMM only: q/k head-norm + RoPE, v plain, stored
+  kEpiQKV = 5,      // persistent draft kernel only: q/k head-norm + RoPE, v plain, stored
 };
 constexpr int kTcMaxSeg = 10;
 constexpr int kTileDepart = 4096;  // tiles per GEMM at most; departures follow arrivals
@@ -70,9 +70,6 @@ struct TcGemmArgs {
   const void* const* kgain;        // [L] k_norm gains, device array of pointers
   int nkv, neox, append_only;
   float eps;
-  // kEpiQKV: rows [Q heads | K heads | V heads], q_norm / k_norm gains [128]
-  int nq_tiles;
-  const void* qn; const void* kn;
   KTrace trace;
 };
 // Many-row tensor-core GEMM (context ingest): Y[m, n] = rnd(X W^T), X [M, K]

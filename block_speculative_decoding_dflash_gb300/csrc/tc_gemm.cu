@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   __shared__ int red_i[4][BN];
   __shared__ int s_last;
   __shared__ float kv_ss[4][BN];
-  __shared__ float kv_x[(EPI == kEpiKVRing || EPI == kEpiQKV) ? 128 * BN : 1];
+  __shared__ float kv_x[EPI == kEpiKVRing ? 128 * BN : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
@@ -213,14 +213,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     }
     // This thread's RoPE entries, the same for every tile (kept in registers
     // for 16 block rows; 32 would crowd out the epilogue's other values).
-    constexpr bool kHoistRope = (EPI == kEpiQKV || EPI == kEpiKVRing) && BN == 16;
+    constexpr bool kHoistRope = EPI == kEpiKVRing && BN == 16;
     float2 rope_cs[BN];
     if (kHoistRope) rope_entries<BN>(rope_cs, a.rope, a.M, a.neox, row);
     auto gain_of = [&](int t) -> float {
-      if (EPI == kEpiQKV) {
-        if (t < a.nq_tiles) return __bfloat162float(reinterpret_cast<const bf16*>(a.qn)[row]);
-        if (t < a.nq_tiles + a.nkv) return __bfloat162float(reinterpret_cast<const bf16*>(a.kn)[row]);
-      } else if (EPI == kEpiKVRing) {
+      if (EPI == kEpiKVRing) {
         const int sg = t / a.nkv;
         if (!(sg & 1)) return __bfloat162float(reinterpret_cast<const bf16*>(a.kgain[sg >> 1])[row]);
       }
@@ -267,21 +264,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
           best_i[m] = bi;
         }
         epi_sync();
-      } else if (EPI == kEpiQKV) {
-        // tiles: query heads, then key heads, then value heads (hd 128 each)
-        float val[BN];
-#pragma unroll
-        for (int m = 0; m < BN; ++m) val[m] = rnd_bf(acc[0][m]);
-        const bool isq = t < a.nq_tiles;
-        const bool isk = !isq && t < a.nq_tiles + a.nkv;
-        if (isq || isk) {
-          if (kHoistRope) head_norm_rope_cs<BN>(val, gv, [&](int m) { return rope_cs[m]; }, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
-          else head_norm_rope_tile<BN>(val, gv, a.rope, a.M, a.neox, a.eps, row, lane, q, kv_ss, kv_x, m0, m1);
-        }
-        bf16* Y = reinterpret_cast<bf16*>(a.y);
-#pragma unroll
-        for (int m = 0; m < BN; ++m)
-          if (m >= m0 && m < m1 && valid) Y[(size_t)m * a.ldy + n] = __float2bfloat16_rn(val[m]);
       } else if (EPI == kEpiKVRing) {
         // tile t = kv head h of layer l, K or V (hd = 128 = one tile)
         const int sg = t / a.nkv, h = t % a.nkv;
@@ -848,8 +830,6 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiResid>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
   if ((e = attr_tc<16, kEpiKVRing>()) != cudaSuccess) return e;
-  if ((e = attr_tc<16, kEpiQKV>()) != cudaSuccess) return e;
-  if ((e = attr_tc<32, kEpiQKV>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiKVRing>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
@@ -889,7 +869,6 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
       case kEpiResid: return launch_tc<16, kEpiResid>(a, grid, pdl, st);
       case kEpiSwiglu: return launch_tc<16, kEpiSwiglu>(a, grid, pdl, st);
       case kEpiKVRing: return launch_tc<16, kEpiKVRing>(a, grid, pdl, st);
-      case kEpiQKV: return launch_tc<16, kEpiQKV>(a, grid, pdl, st);
       default: return launch_tc<16, kEpiArgmax>(a, grid, pdl, st);
     }
   }
@@ -898,7 +877,6 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
     case kEpiResid: return launch_tc<32, kEpiResid>(a, grid, pdl, st);
     case kEpiSwiglu: return launch_tc<32, kEpiSwiglu>(a, grid, pdl, st);
     case kEpiKVRing: return launch_tc<32, kEpiKVRing>(a, grid, pdl, st);
-    case kEpiQKV: return launch_tc<32, kEpiQKV>(a, grid, pdl, st);
     default: return launch_tc<32, kEpiArgmax>(a, grid, pdl, st);
   }
 }
