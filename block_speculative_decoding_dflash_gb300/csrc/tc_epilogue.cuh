@@ -207,14 +207,6 @@ __device__ __forceinline__ void sum_group(float (&acc)[NV][BN], const float* par
     }
 }
 
-// Load with acquire semantics at GPU scope: reads after it see what the
-// writer published before its release (fence + atomic).
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // CTA owning unit u when U units are split into G contiguous ranges
 // [floor(b*U/G), floor((b+1)*U/G)).
 __device__ __forceinline__ int owner_of(long long u, long long U, int G) {

@@ -11,16 +11,21 @@
 // Work split: the (tile, 64-wide K chunk) units of the whole GEMM are cut
 // into gridDim.x contiguous ranges, one per CTA (one CTA per SM), so every
 // SM streams the same number of weight bytes. A tile whose K range spans
-// several CTAs is finished by whichever contributor arrives last: each writes
-// its fp32 partial, takes a ticket, and the last one sums the partials in CTA
-// order (deterministic) and runs the epilogue. Nobody waits on another CTA.
+// several CTAs is finished cooperatively: each contributor writes its fp32
+// partial and arrives on the tile's counter; once all of a CTA's own tiles
+// are published, contributor k of n waits (bounded) for the others and
+// reduces float4 groups k, k + n, ... of the block rows, summing the partials
+// in CTA order (deterministic). Every CTA of the grid is resident (one per
+// SM), so these waits cannot block one another. The lm_head's split tiles
+// (two contributors) are finished by the later one, which knows it is last
+// from a ticket.
 //
 // Roles: warp 0 issues TMA loads into an S-stage shared-memory ring (the
 // weight tiles of the first S units are requested before the programmatic
 // launch dependency is resolved, so they stream while the previous kernel
 // finishes); warp 1 allocates TMEM and issues tcgen05.mma; warps 2-5 read the
-// accumulators back and run the epilogue (store, residual add, SwiGLU, or
-// softcap + argmax for the lm_head).
+// accumulators back and run the epilogue (store, residual add, SwiGLU, K/V
+// with k-norm + RoPE into ring slots, or softcap + argmax for the lm_head).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         const int t = slot == 0 ? split_first : split_last;
         const unsigned nc = static_cast<unsigned>(bls[slot] - bfs[slot] + 1);
         unsigned spins = 0;
-        while (ld_acquire_u32(&arrive[t]) < nc) {
+        while (ld_acquire(&arrive[t]) < nc) {
           if (++spins > (1u << 24)) { atomicOr(a.err, 8); break; }
           __nanosleep(64);
         }
