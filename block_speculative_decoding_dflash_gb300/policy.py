@@ -25,6 +25,14 @@ class ThroughputController:
         self.since_challenge = 0
         self.history = []          # (width, tokens, ms, adopted)
 
+    def probed_verify_widths(self) -> tuple:
+        """Every width a run can settle on: the warm-up depth and the
+        ceiling ("Pre-merge review round", the exactness-gate finding: a check
+        made at one width says nothing about another, so anything that must
+        hold at the widths the loop runs at has to be checked at all of
+        these)."""
+        return tuple(sorted({self.depth, self.ceiling}))
+
     def other(self) -> int:
         return self.ceiling if self.current == self.depth else self.depth
 

@@ -44,3 +44,14 @@ def test_rejects_bad_parameters():
         ThroughputController(1, 16)
     with pytest.raises(ValueError):
         ThroughputController(8, 4)
+
+
+def test_probed_widths_cover_the_warm_up_depth_and_the_ceiling():
+    assert ThroughputController(4, 16).probed_verify_widths() == (4, 16)
+    assert ThroughputController(8, 8).probed_verify_widths() == (8,)
+    c = ThroughputController(4, 16, window=2, challenge_every=1)
+    # whatever the controller adopts stays inside the probed set
+    for rate in (1.0, 2.0, 2.0, 3.0, 3.0, 1.0):
+        w = c.next_width()
+        c.observe(w, int(rate * 10), 10.0)
+        assert w in c.probed_verify_widths() and c.current in c.probed_verify_widths()
