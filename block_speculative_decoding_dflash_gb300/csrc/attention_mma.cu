@@ -44,8 +44,8 @@ struct MmaSmem {
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
-  // (Measured: 3 us per draft faster at 4 block rows; at 16, where the query
-  // tile kernel runs, the hint's traffic costs the QKV GEMM about as much.)
+  // (Measured: 3 us per draft faster at 4 block rows; the tensor-core kernel
+  // used at 16 gained nothing from the same hint and does not issue it.)
   attn_prefetch_context(a, blockIdx.x, blockIdx.y);
   pdl_enter();
   if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
