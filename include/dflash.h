@@ -337,9 +337,15 @@ int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
  * attention, split merge, O, gate/up, down, then the lm_head. */
 int dflash_draft_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity,
                        int32_t* rows, int32_t* cols);
-/* The kernel trace of the last traced dflash_draft_block: count launches,
+/* The kernel trace of the last traced dflash_draft_block: count entries,
  * out_host [count][3] stamps (entry, wait return, exit) and names_host their
- * newline-separated names (e.g. "L0.qkv"). Syncs the context's stream.
+ * newline-separated names (e.g. "L0.qkv"). A weight-streaming GEMM "X" adds
+ * entries for phases of its latest CTA: "X.1" [1] last MMA issued, [2] own
+ * tiles published; "X.2" [1] split-tile contributors present, [2] finished;
+ * "X.3" [1] split groups reduced. An attention "L<l>.attn" adds "L<l>.attn.1",
+ * its split-merge kernel (entry, wait return, exit). Unused stamps read as
+ * their reset value (all ones for [0], zero otherwise). Syncs the context's
+ * stream.
  * ERANGE if out_host / names_host are NULL or too small (count is still
  * set); ESTATE if tracing was never enabled. */
 int dflash_kernel_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity, int32_t* count,
