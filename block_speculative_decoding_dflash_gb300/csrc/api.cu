@@ -529,7 +529,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
   at.err = c->tc_err;
-  at.trace = ktrace_slot(c, ln + "attn", 4);
+  at.trace = ktrace_slot(c, ln + "attn", 2);
   if (attn_norm) {
     at.qn = LW(c, l, kQNorm); at.kn = LW(c, l, kKNorm);
     at.rope = c->rope; at.neox = c->cfg.rope_neox; at.eps = eps;
