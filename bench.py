@@ -388,16 +388,9 @@ def run_ours(args, world, rank, local):
     launches = sum(r["launches"] for r in results)
     lm = [x for r in results for x in r["lm_ms"]]
     peaks, which = measured_peaks()
-    fused = job.ctx.fused_draft_available() and job.ctx.fused_draft_enabled()
-    if fused:
-        lm_bytes = [draft_bytes(job.cfg, w, job.cfg["window"]) for w, _ in lm]
-        kname = ("draft_kernel (persistent cooperative drafter block forward: 5 layers + "
-                 "lm_head + softcap + argmax)")
-        unit_desc = "all drafter weights + the window's K/V per launch"
-    else:
-        lm_bytes = [lm_head_bytes(job.cfg, w - 1) for w, _ in lm]
-        kname = "tc_gemm_kernel<16, 3, 6, 2> (lm_head + softcap + argmax, tcgen05, paired K chunks)"
-        unit_desc = "lm_head weights per launch"
+    lm_bytes = [lm_head_bytes(job.cfg, w - 1) for w, _ in lm]
+    kname = "tc_gemm_kernel<16, 3, 6, 2> (lm_head + softcap + argmax, tcgen05, paired K chunks)"
+    unit_desc = "lm_head weights per launch"
     lm_t = [t for _, t in lm]
     achieved = sum(lm_bytes) / (sum(lm_t) / 1e3) / 1e9 if lm_t else None
     widths = [w for r in results for w in r["widths"]]
@@ -469,12 +462,11 @@ def run_ours(args, world, rank, local):
             "accepted_per_round": round(accepted / nrounds, 4),
             "emitted_per_round": round(accepted / nrounds + 1, 4),
             "roofline": {"kernel": kname, "bytes": unit_desc,
-                         "bytes_per_launch": {str(w): draft_bytes(job.cfg, w, job.cfg["window"]) if fused
-                                              else lm_head_bytes(job.cfg, w - 1) for w in (4, 16)},
+                         "bytes_per_launch": {str(w): lm_head_bytes(job.cfg, w - 1) for w in (4, 16)},
                          "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
                          "peak": peaks["hbm_gbs"], "peak_source": which, "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
-                         "traffic": None if fused else LMHEAD_TRAFFIC, "launches_timed": len(lm_t),
+                         "traffic": LMHEAD_TRAFFIC, "launches_timed": len(lm_t),
                          "mean_ms": round(sum(lm_t) / len(lm_t), 4) if lm_t else None},
             "context_ingest": ingest,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,

@@ -63,7 +63,7 @@ class RoundStateC(ctypes.Structure):
 
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-OPT_FUSED_DRAFT, OPT_FUSED_DRAFT_AVAILABLE, OPT_DRAFT_TRACE, OPT_KERNEL_TRACE = 1, 2, 3, 4
+OPT_KERNEL_TRACE = 4
 
 
 def _sig(name, res, *args):
@@ -83,7 +83,8 @@ _sig("dflash_ctx_destroy", None, _vp)
 _sig("dflash_last_error", ctypes.c_char_p, _vp)
 _sig("dflash_ingest_context", ctypes.c_int, _vp, _vp, _i64, _i64, _i32)
 _sig("dflash_set_anchor", ctypes.c_int, _vp, _i32)
-_sig("dflash_draft_block", ctypes.c_int, _vp, _i32, _vp)
+_sig("dflash_draft_block", ctypes.c_int, _vp, _i32, _i64, _i32, _vp)
+_sig("dflash_sync_round", ctypes.c_int, _vp, _vp, _vp)
 _sig("dflash_verify_accept", ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp)
 _sig("dflash_append_block", ctypes.c_int, _vp, _vp, _i32)
 _sig("dflash_commit", ctypes.c_int, _vp, _i32)
@@ -105,7 +106,6 @@ _sig("dflash_sync", ctypes.c_int, _vp)
 _sig("dflash_graph_kernel_count", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
 _sig("dflash_set_option", ctypes.c_int, _vp, _i32, _i64)
 _sig("dflash_get_option", ctypes.c_int, _vp, _i32, ctypes.POINTER(_i64))
-_sig("dflash_draft_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _sig("dflash_kernel_trace", ctypes.c_int, _vp, _vp, _i64, ctypes.POINTER(_i32), ctypes.c_char_p, _i64)
 _sig("dflash_lm_head_timing", ctypes.c_int, _vp, _i32)
 _sig("dflash_ingest_gemm_timing", ctypes.c_int, _vp, _i32)
@@ -301,9 +301,18 @@ class DFlashContext:
         self._prep()
         self._check(lib.dflash_set_anchor(self.h, anchor))
 
-    def draft_block(self, block, draft_ids):
+    def draft_block(self, block, draft_ids, anchor=-1, anchor_pos=-1):
+        """anchor / anchor_pos < 0: the device-resident anchor and no
+        position check (the CUDA-graph round path)."""
         self._prep()
-        self._check(lib.dflash_draft_block(self.h, block, _ptr(draft_ids)))
+        self._check(lib.dflash_draft_block(self.h, anchor, anchor_pos, block, _ptr(draft_ids)))
+
+    def sync_round(self, block):
+        """Waits for the stream; returns (tokens[:n], n) of the last verify."""
+        tok = np.zeros(block, dtype=np.int32)
+        n = np.zeros(1, dtype=np.int32)
+        self._check(lib.dflash_sync_round(self.h, tok.ctypes.data, n.ctypes.data))
+        return tok[: int(n[0])], int(n[0])
 
     def verify_accept(self, logits, block, draft_ids, tokens, n):
         self._prep()
@@ -386,36 +395,6 @@ class DFlashContext:
         o = _i64()
         self._check(lib.dflash_graph_kernel_count(self.h, slot, ctypes.byref(o)))
         return o.value
-
-    def set_fused_draft(self, enable: bool):
-        """Draft with the persistent single-launch kernel where the config
-        allows it (the default), or with one kernel per operation."""
-        self._check(lib.dflash_set_option(self.h, OPT_FUSED_DRAFT, 1 if enable else 0))
-
-    def fused_draft_enabled(self) -> bool:
-        o = _i64()
-        self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT, ctypes.byref(o)))
-        return bool(o.value)
-
-    def fused_draft_available(self) -> bool:
-        o = _i64()
-        self._check(lib.dflash_get_option(self.h, OPT_FUSED_DRAFT_AVAILABLE, ctypes.byref(o)))
-        return bool(o.value)
-
-    def draft_trace(self, enable: bool):
-        """Stamp each CTA's phase completions in every draft-kernel launch."""
-        self._check(lib.dflash_set_option(self.h, OPT_DRAFT_TRACE, 1 if enable else 0))
-
-    def draft_trace_read(self) -> np.ndarray:
-        """[phases, CTAs, 12] globaltimer stamps (ns) of the last traced launch."""
-        r, c = _i32(), _i32()
-        rc = lib.dflash_draft_trace(self.h, None, 0, ctypes.byref(r), ctypes.byref(c))
-        if rc not in (0, ERANGE):
-            self._check(rc)
-        out = np.zeros((r.value, c.value, 12), dtype=np.uint64)
-        self._check(lib.dflash_draft_trace(self.h, out.ctypes.data, out.size, ctypes.byref(r),
-                                           ctypes.byref(c)))
-        return out
 
     def kernel_trace(self, enable: bool):
         """Stamp each launch of the per-operation draft (see kernel_trace_read)."""

@@ -175,6 +175,9 @@ struct dflash_ctx {
   bool has_context = false;
   int last_draft_block = 0;
   int last_verify_block = 0;
+  int32_t* last_tokens = nullptr;              // the last verify's outputs (dflash_sync_round)
+  int32_t* last_n = nullptr;
+  int last_tokens_block = 0;
   int appended_block = 0;
   bool capturing = false;
   int saved_flags[4] = {0, 0, 0, 0};
@@ -198,17 +201,6 @@ struct dflash_ctx {
   int* tc_lm_pi = nullptr;
   unsigned* tc_done = nullptr;
   const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
-  // persistent draft kernel (bf16, head_dim 128, up to 16 block rows)
-  bool draft_fused_ok = false;                 // the config and device allow it
-  bool draft_fused_on = false;                 // DFLASH_OPT_FUSED_DRAFT
-  MegaPhase* mega_phases = nullptr;            // device phase list
-  int mega_nphase = 0;
-  CUtensorMap* mega_maps = nullptr;            // device tensor-map table
-  unsigned* mega_done = nullptr;               // [nphase] counters + abort flag
-  int mega_grid = 0;
-  int mega_nsplit = 0;
-  unsigned long long* mega_trace = nullptr;    // DFLASH_OPT_DRAFT_TRACE stamps
-  bool mega_trace_on = false;
   cudaEvent_t lm_ev[2] = {nullptr, nullptr};
   bool lm_timing = false;
   bool lm_recorded = false;
@@ -592,105 +584,6 @@ int ensure_room(dflash_ctx* c, int rows) {
   return DFLASH_OK;
 }
 
-// Phase list and tensor-map table of the persistent draft kernel, when the
-// config fits it: head_dim 128, hidden <= 2048 (the normalised operand lives
-// in shared memory), block <= 16 rows with at most 64 queries per kv head,
-// and every CTA resident at once (one per SM).
-int setup_draft_kernel(dflash_ctx* c) {
-  const dflash_config& g = c->cfg;
-  const int G = c->nq / c->nkv;
-  if (c->hd != 128 || c->H > 2048 || c->H % 256 || c->nq % c->nkv || 16 * G > 64) return DFLASH_OK;
-  if (2 + 6 * g.n_layers > kMegaMaxPhases) return DFLASH_OK;
-  int dev = 0, sms = 0;
-  CK(c->err, cudaGetDevice(&dev));
-  CK(c->err, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  if (sms > kTcGrid) return DFLASH_OK;
-  CK(c->err, init_draft_kernel_attrs());
-  if (draft_kernel_blocks_per_sm() < 1) return DFLASH_OK;
-  const int nsplit = (c->max_ctx + 16 + 127) / 128;
-  if ((size_t)c->nkv * nsplit * 16 * G * (128 + 4) > c->attn_part_floats) return DFLASH_OK;
-
-  // map table: per layer wq wk wv wo wg wu wd, then lm_head, attn rows, SwiGLU rows
-  std::vector<CUtensorMap> maps;
-  for (int l = 0; l < g.n_layers; ++l) {
-    const auto& m = c->lmaps[l];
-    for (const CUtensorMap* t : {&m.wq, &m.wk, &m.wv, &m.wo, &m.wg, &m.wu, &m.wd}) maps.push_back(*t);
-  }
-  const int lm_idx = (int)maps.size();
-  maps.push_back(c->lm_map);
-  const int attn_idx = (int)maps.size();
-  maps.push_back(c->attn_map[0]);
-  const int sbuf_idx = (int)maps.size();
-  maps.push_back(c->sbuf_map[0]);
-
-  auto gemm = [&](int epi, int norm, int N, int K) {
-    MegaPhase p{};
-    p.kind = kPhGemm; p.epi = epi; p.norm = norm;
-    p.N = N; p.K = K; p.tiles = (N + 127) / 128; p.kchunks = K / 64;
-    p.nseg = 1;
-    p.seg_tiles[0] = p.tiles;
-    return p;
-  };
-  std::vector<MegaPhase> ph;
-  MegaPhase e{};
-  e.kind = kPhEmbed;
-  ph.push_back(e);
-  for (int l = 0; l < g.n_layers; ++l) {
-    const int w0 = l * 7;
-    MegaPhase q = gemm(kEpiQKV, 1, c->qkv_n, c->H);
-    q.nseg = 3;
-    q.a_map[0] = w0 + 0; q.a_map[1] = w0 + 1; q.a_map[2] = w0 + 2;
-    q.seg_tiles[0] = c->qdim / 128;
-    q.seg_tiles[1] = (c->qdim + c->kvdim) / 128;
-    q.seg_tiles[2] = c->qkv_n / 128;
-    q.y = c->qkv; q.ldy = c->qkv_n;
-    q.gain = LW(c, l, kInNorm); q.qn = LW(c, l, kQNorm); q.kn = LW(c, l, kKNorm);
-    q.nq_tiles = c->nq;
-    ph.push_back(q);
-    MegaPhase at{};
-    at.kind = kPhAttn; at.layer = l;
-    ph.push_back(at);
-    MegaPhase cb{};
-    cb.kind = kPhComb; cb.layer = l;
-    ph.push_back(cb);
-    MegaPhase o = gemm(kEpiResid, 0, c->H, c->qdim);
-    o.a_map[0] = w0 + 3; o.b_map = attn_idx;
-    o.y = c->x; o.ldy = c->H;
-    ph.push_back(o);
-    MegaPhase gu = gemm(kEpiSwiglu, 1, c->I, c->H);
-    gu.a_map[0] = w0 + 4; gu.a2_map = w0 + 5;
-    gu.y = c->sbuf; gu.ldy = c->I;
-    gu.gain = LW(c, l, kPostNorm);
-    ph.push_back(gu);
-    MegaPhase d = gemm(kEpiResid, 0, c->H, c->I);
-    d.a_map[0] = w0 + 6; d.b_map = sbuf_idx;
-    d.y = c->x; d.ldy = c->H;
-    ph.push_back(d);
-  }
-  MegaPhase lm = gemm(kEpiArgmax, 1, c->V, c->H);
-  lm.lm = 1; lm.a_map[0] = lm_idx; lm.gain = c->final_norm;
-  ph.push_back(lm);
-
-  CK(c->err, cudaMalloc(&c->mega_maps, maps.size() * sizeof(CUtensorMap)));
-  CK(c->err, cudaMalloc(&c->mega_phases, ph.size() * sizeof(MegaPhase)));
-  CK(c->err, cudaMalloc(&c->mega_done, (ph.size() + 1) * kMegaDoneStride * sizeof(unsigned)));
-  CK(c->err, cudaMemcpyAsync(c->mega_maps, maps.data(), maps.size() * sizeof(CUtensorMap),
-                             cudaMemcpyHostToDevice, c->stream));
-  CK(c->err, cudaMemcpyAsync(c->mega_phases, ph.data(), ph.size() * sizeof(MegaPhase),
-                             cudaMemcpyHostToDevice, c->stream));
-  CK(c->err, cudaMemsetAsync(c->mega_done, 0, (ph.size() + 1) * kMegaDoneStride * sizeof(unsigned), c->stream));
-  CK(c->err, cudaStreamSynchronize(c->stream));
-  c->mega_nphase = (int)ph.size();
-  c->mega_grid = sms;
-  c->mega_nsplit = nsplit;
-  c->draft_fused_ok = true;
-  return DFLASH_OK;
-}
-
-bool draft_fused(const dflash_ctx* c, int rows, int lm_rows, bool logits) {
-  return c->draft_fused_ok && c->draft_fused_on && rows <= 16 && lm_rows >= 1 && !logits;
-}
-
 // Tensor maps of every weight and activation operand of the tensor-core path
 // (bf16 configs whose output dimensions are whole 128-row tiles).
 int setup_tensor_core_path(dflash_ctx* c) {
@@ -736,7 +629,7 @@ int setup_tensor_core_path(dflash_ctx* c) {
   if (!ok) return DFLASH_OK;   // no tensor-map encoder: the CUDA-core path serves
   CK(c->err, init_tc_attrs());
   c->use_tc = true;
-  return setup_draft_kernel(c);
+  return DFLASH_OK;
 }
 
 }  // namespace
@@ -775,10 +668,6 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
     if (g) cudaGraphExecDestroy(g);
   ring_free(ctx->ring);
   cudaFree(ctx->arena);
-  cudaFree(ctx->mega_maps);
-  cudaFree(ctx->mega_phases);
-  cudaFree(ctx->mega_done);
-  cudaFree(ctx->mega_trace);
   cudaFree(ctx->ktr);
   for (auto& ev : ctx->ing_ev)
     if (ev) cudaEventDestroy(ev);
@@ -982,11 +871,14 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
   return launch_markov_chain(c->dt, mk, c->stream);
 }
 
-int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
+int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_t block,
+                       int32_t* draft_ids) {
   if (!c) return DFLASH_EINVAL;
   if (!draft_ids) return fail(c->err, DFLASH_EINVAL, "draft_ids is NULL");
   if (block < 2 || block > c->cfg.max_block)
     return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
+  if (anchor >= c->V)
+    return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
   if (!c->has_context) return fail(c->err, DFLASH_EEMPTY, "no context ingested");
   const int dspark = c->cfg.kind == DFLASH_KIND_DSPARK;
   const int rows = dspark ? block - 1 : block;
@@ -995,39 +887,6 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
   const int dt = c->dt;
   cudaStream_t st = c->stream;
   const bool markov = c->cfg.markov_rank > 0;
-  const bool want_logits = markov && c->cfg.markov_add;
-  if (draft_fused(c, rows, R, want_logits)) {
-    if (c->lm_timing)
-      CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
-    MegaArgs m{};
-    m.phases = c->mega_phases; m.nphase = c->mega_nphase;
-    m.maps = c->mega_maps;
-    m.M = rows; m.Mlm = R; m.read0 = read0;
-    m.H = c->H; m.V = c->V; m.nq = c->nq; m.nkv = c->nkv; m.qkv_n = c->qkv_n; m.half = c->half;
-    m.embed = c->embed; m.rs = c->rs; m.mask_id = c->cfg.mask_token_id;
-    m.inv_freq = c->inv_freq; m.rope = c->rope;
-    m.x = c->x; m.qkv = c->qkv; m.attn = c->attn; m.xf = c->xf;
-    m.ring = c->ring->st; m.ring_k = c->ring->k; m.ring_v = c->ring->v; m.cap = c->ring->cap;
-    m.window = c->cfg.window;
-    m.attn_part = c->attn_part; m.nsplit = c->mega_nsplit;
-    m.partials = c->tc_part; m.tile_ctr = c->tc_tiles; m.err = c->tc_err;
-    m.done = c->mega_done; m.abort_flag = c->mega_done + (size_t)c->mega_nphase * kMegaDoneStride;
-    m.softcap = c->cfg.softcap;
-    m.ids = markov ? c->backbone_ids : draft_ids;
-    m.ids2 = markov ? nullptr : c->backbone_ids;
-    m.maxv = c->maxv;
-    m.part_v = c->tc_lm_pv; m.part_i = c->tc_lm_pi;
-    m.eps = c->cfg.rms_eps; m.neox = c->cfg.rope_neox;
-    m.trace = c->mega_trace_on ? c->mega_trace : nullptr;
-    CK(c->err, launch_draft_kernel(m, c->mega_grid, st));
-    if (c->lm_timing) {
-      CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
-      c->lm_recorded = true;
-    }
-    if (markov) CK(c->err, draft_markov(c, R, draft_ids));
-    c->last_draft_block = block;
-    return DFLASH_OK;
-  }
   if (c->ktr_on && c->ktr) {
     c->ktr_n = 0;
     c->ktr_names.clear();
@@ -1035,7 +894,8 @@ int dflash_draft_block(dflash_ctx* c, int32_t block, int32_t* draft_ids) {
     CK(c->err, cudaMemsetAsync(c->ktr + kKTraceSlots, 0, 2 * sizeof(unsigned long long) * kKTraceSlots, st));
   }
   CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rows, c->x,
-                                c->ring->st, c->inv_freq, c->half, rows, c->rope, st));
+                                c->ring->st, c->inv_freq, c->half, rows, c->rope,
+                                anchor < 0 ? -1 : anchor, anchor_pos < 0 ? -1 : anchor_pos, st));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     int rc = layer_forward(c, l, rows);
     if (rc) return rc;
@@ -1090,6 +950,21 @@ int dflash_verify_accept(dflash_ctx* c, const void* target_logits, int32_t block
   v.chunks = c->vf_chunks;
   CK(c->err, launch_verify(c->dt, v, c->stream));
   c->last_verify_block = block;
+  c->last_tokens = tokens;
+  c->last_n = n;
+  c->last_tokens_block = block;
+  return DFLASH_OK;
+}
+
+int dflash_sync_round(dflash_ctx* c, int32_t* tokens_host, int32_t* n_host) {
+  if (!c) return DFLASH_EINVAL;
+  if (!tokens_host || !n_host) return fail(c->err, DFLASH_EINVAL, "tokens_host or n_host is NULL");
+  if (c->capturing) return fail(c->err, DFLASH_ESTATE, "dflash_sync_round while capturing");
+  if (!c->last_tokens || !c->last_n) return fail(c->err, DFLASH_ESTATE, "no verify yet");
+  CK(c->err, cudaMemcpyAsync(n_host, c->last_n, sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream));
+  CK(c->err, cudaMemcpyAsync(tokens_host, c->last_tokens, sizeof(int32_t) * c->last_tokens_block,
+                             cudaMemcpyDeviceToHost, c->stream));
+  CK(c->err, cudaStreamSynchronize(c->stream));
   return DFLASH_OK;
 }
 
@@ -1128,7 +1003,7 @@ int dflash_commit(dflash_ctx* c, int32_t keep) {
 
 int dflash_round(dflash_ctx* c, const void* target_logits, const void* resid, int32_t block,
                  int32_t* draft_ids, int32_t* tokens, int32_t* n) {
-  int rc = dflash_draft_block(c, block, draft_ids);
+  int rc = dflash_draft_block(c, -1, -1, block, draft_ids);
   if (!rc) rc = dflash_verify_accept(c, target_logits, block, draft_ids, tokens, n);
   if (!rc) rc = dflash_append_block(c, resid, block);
   if (!rc) rc = dflash_commit(c, -1);
@@ -1342,29 +1217,13 @@ int dflash_graph_kernel_count(dflash_ctx* c, int32_t slot, int64_t* out) {
 
 int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
   if (!c) return DFLASH_EINVAL;
-  if (option == DFLASH_OPT_FUSED_DRAFT) {
-    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
-    c->draft_fused_on = value != 0;
-    return DFLASH_OK;
-  }
   if (option == DFLASH_OPT_KERNEL_TRACE) {
     if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
     if (value && !c->ktr) CK(c->err, cudaMalloc(&c->ktr, 3 * sizeof(unsigned long long) * kKTraceSlots));
     c->ktr_on = value != 0;
     return DFLASH_OK;
   }
-  if (option == DFLASH_OPT_DRAFT_TRACE) {
-    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
-    if (value && !c->draft_fused_ok) return fail(c->err, DFLASH_ESTATE, "no persistent draft kernel");
-    if (value && !c->mega_trace) {
-      const size_t n = (size_t)c->mega_nphase * c->mega_grid * kMegaTraceSlots;
-      CK(c->err, cudaMalloc(&c->mega_trace, n * sizeof(unsigned long long)));
-      CK(c->err, cudaMemsetAsync(c->mega_trace, 0, n * sizeof(unsigned long long), c->stream));
-    }
-    c->mega_trace_on = value != 0;
-    return DFLASH_OK;
-  }
-  return fail(c->err, DFLASH_EINVAL, "unknown or read-only option %d", option);
+  return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 
 int dflash_kernel_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t* count, char* names,
@@ -1387,27 +1246,10 @@ int dflash_kernel_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t*
   return DFLASH_OK;
 }
 
-int dflash_draft_trace(dflash_ctx* c, uint64_t* out, int64_t capacity, int32_t* rows, int32_t* cols) {
-  if (!c) return DFLASH_EINVAL;
-  if (!rows || !cols) return fail(c->err, DFLASH_EINVAL, "rows or cols is NULL");
-  if (!c->mega_trace) return fail(c->err, DFLASH_ESTATE, "draft tracing was never enabled");
-  *rows = c->mega_nphase;
-  *cols = c->mega_grid;
-  const int64_t n = (int64_t)(*rows) * (*cols) * kMegaTraceSlots;
-  if (!out || capacity < n)
-    return fail(c->err, DFLASH_ERANGE, "capacity %lld < %lld stamps", (long long)capacity, (long long)n);
-  CK(c->err, cudaMemcpyAsync(out, c->mega_trace, n * sizeof(uint64_t), cudaMemcpyDeviceToHost, c->stream));
-  CK(c->err, cudaStreamSynchronize(c->stream));
-  return DFLASH_OK;
-}
-
 int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
   if (!c) return DFLASH_EINVAL;
   if (!value) return fail(c->err, DFLASH_EINVAL, "value is NULL");
-  if (option == DFLASH_OPT_FUSED_DRAFT) { *value = c->draft_fused_on ? 1 : 0; return DFLASH_OK; }
-  if (option == DFLASH_OPT_FUSED_DRAFT_AVAILABLE) { *value = c->draft_fused_ok ? 1 : 0; return DFLASH_OK; }
   if (option == DFLASH_OPT_KERNEL_TRACE) { *value = c->ktr_on ? 1 : 0; return DFLASH_OK; }
-  if (option == DFLASH_OPT_DRAFT_TRACE) { *value = c->mega_trace_on ? 1 : 0; return DFLASH_OK; }
   return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 
@@ -1513,6 +1355,13 @@ int ring_cache_trim(ring_cache* r, int32_t m) {
   if (m > r->host_appended)
     return fail(r->err, DFLASH_EREWIND, "short rewind: trim %d > %d rows appended since the last trim",
                 m, r->host_appended);
+  // A sliding ring keeps the rows behind the offset only for `slack` slots
+  // past the window: rows appended beyond that have already overwritten
+  // window rows that a rewind would make visible again.
+  if (!r->append_only && m > r->cap - r->window)
+    return fail(r->err, DFLASH_EREWIND,
+                "trim %d > slack %lld: the window rows it would expose were overwritten", m,
+                r->cap - r->window);
   CK(r->err, launch_ring_advance(r->st, m, 1, r->stream));
   r->host_appended = 0;
   r->pos_hi -= m;

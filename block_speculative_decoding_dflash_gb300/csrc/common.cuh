@@ -39,6 +39,8 @@ struct RoundState {
 enum : int {
   kErrFull = 1,        // append-only ring overflow (rows skipped)
   kErrRange = 2,       // a token id outside the vocabulary reached a gather
+  kErrPos = 8,         // a draft's host-given anchor position was not the
+                       // committed context length
 };
 
 // ---------------------------------------------------------------------------

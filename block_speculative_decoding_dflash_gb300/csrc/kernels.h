@@ -34,7 +34,6 @@ struct LinearArgs {
 enum : int {
   kEpiArgmax = 3,   // tensor-core GEMM only: softcap + per-row argmax
   kEpiKVRing = 4,   // tensor-core GEMM only: K head-norm + RoPE / V, into ring slots
-  kEpiQKV = 5,      // persistent draft kernel only: q/k head-norm + RoPE, v plain, stored
 };
 constexpr int kTcMaxSeg = 10;
 constexpr int kTileDepart = 4096;  // tiles per GEMM at most; departures follow arrivals
@@ -102,73 +101,21 @@ bool tc_encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
 cudaError_t init_tc_attrs();
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cudaStream_t st);
 
-// ---- persistent draft kernel ------------------------------------------------------
-// One cooperative launch runs the drafter block forward as a list of phases.
-enum : int { kPhEmbed = 0, kPhGemm = 1, kPhAttn = 2, kPhComb = 3 };
-struct MegaPhase {
-  int kind;
-  int epi;                 // kPhGemm: kEpiQKV, kEpiResid (y += ...), kEpiSwiglu, kEpiArgmax
-  int norm;                // kPhGemm: 1 = operand is rmsnorm(x rows) * gain, built in shared memory
-  int lm;                  // kPhGemm: the lm_head (argmax over block columns read0 ..; CTA 0
-                           // also stores the normalised rows to MegaArgs::xf)
-  int layer;               // kPhAttn: ring layer
-  int nseg;
-  int a_map[3];            // weight segment maps (index into MegaArgs::maps), box {64, 128}
-  int seg_tiles[3];        // cumulative 128-row tiles of the segments
-  int a2_map;              // kEpiSwiglu: up weight map
-  int b_map;               // norm == 0: activation map, box {64, 16}
-  int N, K, tiles, kchunks;
-  void* y; int ldy;        // output rows [M][ldy]; kEpiResid adds into it
-  const void* gain;        // norm == 1: RMSNorm gain [K]
-  const void* qn; const void* kn;  // kEpiQKV: q_norm / k_norm gains [128]
-  int nq_tiles;            // kEpiQKV: query tiles before the key tiles
-};
-struct MegaArgs {
-  const MegaPhase* phases; int nphase;
-  const CUtensorMap* maps;           // device array, 64-byte aligned
-  int M, Mlm, read0;                 // block rows; lm_head rows = block rows read0 .. M-1
-  int H, V, nq, nkv, qkv_n, half;
-  const void* embed; RoundState* rs; int mask_id;
-  const double* inv_freq; float2* rope;   // rope: [M][half], written by the embed phase
-  void* x; void* qkv; void* attn;    // [R][H], [R][qkv_n], [R][nq*128]
-  void* xf;                          // [R][H] final normalised rows
-  RingState* ring; void* ring_k; void* ring_v; long long cap; int window;
-  float* attn_part; int nsplit;      // split partials, layout stride nsplit
-  float* partials; unsigned* tile_ctr; int* err;
-  unsigned* done;                    // [nphase][kMegaDoneStride] phase counters (one per
-                                     // 128-byte line), zero between launches
-  unsigned* abort_flag;              // raised by a CTA that gave up a wait
-  float softcap; int* ids; int* ids2; float* maxv; float* part_v; int* part_i;
-  float eps; int neox;
-  // optional: [nphase][grid][kMegaTraceSlots] globaltimer stamps per phase
-  // and CTA: 0 workers start the phase, 1 normalised operand built /
-  // attention done, 2 first accumulator ready, 3 phase counted done, 4 the
-  // MMA issuer reaches the phase, 5 last MMA committed, 6 first weight tile
-  // requested, 7 first activation tile requested, 8 normalised operand's
-  // loads landed, 9 its row sums done, 10 first attention split's loads
-  // landed, 11 unused
-  unsigned long long* trace;
-};
-constexpr int kMegaDoneStride = 32;
-constexpr int kMegaTraceSlots = 12;
-constexpr int kMegaMaxPhases = 64;       // 2 + 6 per layer: up to 10 layers
-size_t draft_kernel_smem();
-cudaError_t init_draft_kernel_attrs();
-int draft_kernel_blocks_per_sm();
-cudaError_t launch_draft_kernel(const MegaArgs& a, int grid, cudaStream_t st);
-
 // Block rows (any M; 16 rows per weight pass): weight-streaming kernel.
 cudaError_t launch_linear_rows(int dtype, const LinearArgs& a, cudaStream_t st);
 // Many rows (context ingest), kEpiStore only: register-tiled GEMM.
 cudaError_t launch_linear_tiled(int dtype, const LinearArgs& a, cudaStream_t st);
 
 // ---- small per-row kernels -------------------------------------------------------
-// x[r] = E[tok_r] with tok_0 = the device anchor and tok_r = mask for r > 0;
-// also the RoPE table rope[tab_rows][hd/2] = (cos, sin) at ring->offset + r.
+// x[r] = E[tok_r] with tok_0 = the anchor and tok_r = mask for r > 0; also
+// the RoPE table rope[tab_rows][hd/2] = (cos, sin) at ring->offset + r. The
+// anchor is anchor_host when >= 0 (also stored as the device anchor), else
+// the device anchor; expect_pos >= 0 is compared with ring->offset (kErrPos).
 cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab,
                                RoundState* rs, int mask_id, int rows, void* x,
                                const RingState* ring, const double* inv_freq,
-                               int half, int tab_rows, float2* rope, cudaStream_t st);
+                               int half, int tab_rows, float2* rope, int anchor_host,
+                               long long expect_pos, cudaStream_t st);
 // RoPE table at positions base + r, base = ring->offset when ring != NULL,
 // else pos0.
 cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,

@@ -33,17 +33,25 @@ std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices] = {};
 
 // Device address of the scratch on the current device. The symbol's name in
-// host code is only a host-side stand-in, so the address is looked up once
-// per device with that device current.
-int scratch_address(void** out) {
+// host code is only a host-side stand-in, so the address is looked up with
+// that device current. It is looked up again on every call made outside a
+// stream capture (a device reset reloads the module, which can move the
+// array); a call on a capturing stream uses the address found last.
+int scratch_address(cudaStream_t st, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     dfl::set_global_error("dflash_verify_accept_static: no usable current CUDA device");
     return DFLASH_ECUDA;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) {
+    dfl::set_global_error(cudaGetErrorString(e));
+    return DFLASH_ECUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_dev[dev]) {
+  if (!g_scratch_dev[dev] || cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_verify_scratch);
     if (e != cudaSuccess || !p) {
@@ -74,15 +82,15 @@ extern "C" int dflash_verify_accept_static(const void* target_logits, int32_t dt
                           "(the size of its static scratch)");
     return DFLASH_ERANGE;
   }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* base = nullptr;
-  int rc = scratch_address(&base);
+  int rc = scratch_address(st, &base);
   if (rc) return rc;
   auto* bytes = static_cast<unsigned char*>(base);
   unsigned* counter = reinterpret_cast<unsigned*>(bytes);
   dfl::RoundState* rs = reinterpret_cast<dfl::RoundState*>(bytes + 64);
   float* part_v = reinterpret_cast<float*>(bytes + kHeader);
   int* part_i = reinterpret_cast<int*>(bytes + kHeader + kPartials * sizeof(float));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The ticket counter must start at zero: clear it in case an earlier call
   // was cut short. Calls that overlap on the GPU share this array and race.
   cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), st);

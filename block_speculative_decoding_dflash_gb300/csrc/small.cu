@@ -23,11 +23,19 @@ template <typename T>
 __global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
                                    int mask_id, int rows, T* x,
                                    const RingState* ring, const double* inv_freq,
-                                   int half, int tab_rows, float2* rope) {
+                                   int half, int tab_rows, float2* rope,
+                                   int anchor_host, long long expect_pos) {
   pdl_enter();
   const int r = blockIdx.x;
+  if (r == 0 && threadIdx.x == 0) {
+    // A host-given anchor replaces the device-resident one (the Markov chain
+    // that may follow seeds from it); a host-given position is checked
+    // against the committed context length, which stays authoritative.
+    if (anchor_host >= 0) rs->anchor = anchor_host;
+    if (expect_pos >= 0 && ring->offset != expect_pos) atomicOr(&rs->error, kErrPos);
+  }
   if (r < rows) {
-    int tok = (r == 0) ? rs->anchor : mask_id;
+    int tok = (r == 0) ? (anchor_host >= 0 ? anchor_host : rs->anchor) : mask_id;
     if (tok < 0 || tok >= vocab) {
       if (threadIdx.x == 0) atomicOr(&rs->error, kErrRange);
       tok = 0;
@@ -302,16 +310,16 @@ __global__ void synth_target_kernel(SynthArgs a) {
 cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab, RoundState* rs,
                                int mask_id, int rows, void* x, const RingState* ring,
                                const double* inv_freq, int half, int tab_rows, float2* rope,
-                               cudaStream_t st) {
+                               int anchor_host, long long expect_pos, cudaStream_t st) {
   const int grid = rows > tab_rows ? rows : tab_rows;
   if (dtype)
     launch_pdl(embed_block_kernel<bf16>, dim3(grid), dim3(256), 0, st, (const bf16*)embed, H, vocab, rs, mask_id,
                                                    rows, (bf16*)x, ring, inv_freq, half,
-                                                   tab_rows, rope);
+                                                   tab_rows, rope, anchor_host, expect_pos);
   else
     launch_pdl(embed_block_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)embed, H, vocab, rs, mask_id,
                                                     rows, (float*)x, ring, inv_freq, half,
-                                                    tab_rows, rope);
+                                                    tab_rows, rope, anchor_host, expect_pos);
   return cudaGetLastError();
 }
 

@@ -137,7 +137,9 @@ typedef struct dflash_round_state {
   int32_t last_accepted; /* a of the last verify */
   int32_t error;      /* device-side error bits: 1 = append-only cache full
                          (rows skipped), 2 = a token id outside the vocabulary
-                         reached the embedding gather (row 0 used) */
+                         reached the embedding gather (row 0 used), 4 = a
+                         bounded wait in a tensor-core kernel gave up, 8 = a
+                         draft's anchor_pos was not the committed length */
 } dflash_round_state;
 
 typedef struct dflash_ctx dflash_ctx;
@@ -193,16 +195,28 @@ int dflash_ingest_context(dflash_ctx* ctx, const void* resid, int64_t rows,
 /* Replaces the device-resident anchor token (the position is unchanged). */
 int dflash_set_anchor(dflash_ctx* ctx, int32_t anchor);
 
-/* Drafts one block of verify width `block` from the device-resident anchor
- * and position [Muse "What changed"; DSpark "Verified against the issue"]:
- * embeds [anchor, mask x (rows-1)] from the raw embedding table, runs the
- * drafter layers (per-head q/k RMSNorm, RoPE at absolute positions,
+/* Drafts one block of verify width `block` from the anchor token at absolute
+ * position anchor_pos [Muse "What changed"; DSpark "Verified against the
+ * issue"]: embeds [anchor, mask x (rows-1)] from the raw embedding table,
+ * runs the drafter layers (per-head q/k RMSNorm, RoPE at absolute positions,
  * bidirectional sliding attention over the ring plus the block), the final
  * norm, the lm_head with softcap and the per-row argmax (no [rows, V] logit
  * tensor is written), and for a config with a Markov head the chain.
  * Writes block-1 proposals d_1..d_{block-1} to draft_ids [block-1] (int32).
- * ERANGE unless 2 <= block <= max_block; EEMPTY if no context was ingested. */
-int dflash_draft_block(dflash_ctx* ctx, int32_t block, int32_t* draft_ids);
+ *
+ * anchor < 0 takes the device-resident anchor (set by dflash_ingest_context,
+ * dflash_set_anchor or the last dflash_commit: the bonus token t_a), which
+ * is what lets whole rounds run from a CUDA graph with nothing passed from
+ * the host; anchor >= 0 replaces it. The position is always the committed
+ * context length held on the device (the ring offset): every row of the
+ * ring is addressed by it, so it cannot be set per call. anchor_pos < 0
+ * skips the check; anchor_pos >= 0 is compared with it on the device and a
+ * mismatch sets error bit 8 of dflash_round_state (the draft still runs at
+ * the committed position).
+ * ERANGE unless 2 <= block <= max_block and anchor < vocab; EEMPTY if no
+ * context was ingested. */
+int dflash_draft_block(dflash_ctx* ctx, int32_t anchor, int64_t anchor_pos, int32_t block,
+                       int32_t* draft_ids);
 
 /* Greedy exact-match verify [DSpark intro; "Short-conv rollback"]: t_i =
  * argmax target_logits[i, :] (lowest index on ties) for i < block; a = the
@@ -228,7 +242,16 @@ int dflash_append_block(dflash_ctx* ctx, const void* resid, int32_t block);
  * ESTATE without an append since the last commit. */
 int dflash_commit(dflash_ctx* ctx, int32_t keep);
 
-/* One whole round: draft_block, verify_accept, append_block, commit(-1). */
+/* The one host synchronization of a round: waits for the context's stream
+ * and copies what the last dflash_verify_accept wrote (to its tokens and n
+ * device buffers) into host memory: n_host [1] = a + 1 and tokens_host
+ * [block] = d_1..d_a, t_a, then -1 padding (block = that verify's width)
+ * [DSpark "Implementation Review Summary": one materialisation of the
+ * argmax per round]. Syncs. ESTATE before any verify or while capturing. */
+int dflash_sync_round(dflash_ctx* ctx, int32_t* tokens_host, int32_t* n_host);
+
+/* One whole round: draft_block (device anchor), verify_accept, append_block,
+ * commit(-1). */
 int dflash_round(dflash_ctx* ctx, const void* target_logits, const void* resid,
                  int32_t block, int32_t* draft_ids, int32_t* tokens,
                  int32_t* n);
@@ -296,21 +319,6 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
 
 /* ---- options ------------------------------------------------------------------ */
 
-/* DFLASH_OPT_FUSED_DRAFT: 1 runs dflash_draft_block as one persistent
- * cooperative kernel (one CTA per SM) when the context allows it:
- * bf16 weights, head_dim 128, hidden <= 2048, at most 16 block rows with at
- * most 64 queries per kv head, no markov_add, every CTA resident at once.
- * 0 (the default) runs one kernel per operation. Both give the same draft
- * up to fp32 summation order (same rounding points). */
-#define DFLASH_OPT_FUSED_DRAFT 1
-/* DFLASH_OPT_FUSED_DRAFT_AVAILABLE (read only): 1 if the context can use the
- * persistent draft kernel at all (it still falls back for wider blocks). */
-#define DFLASH_OPT_FUSED_DRAFT_AVAILABLE 2
-/* DFLASH_OPT_DRAFT_TRACE: 1 makes every persistent draft kernel launch stamp
- * the GPU's global timer (ns) at twelve events of every phase on every CTA
- * (allocates phases x CTAs x 96 bytes on first use; 0 stops it). The stamps
- * of the last launch are read with dflash_draft_trace. */
-#define DFLASH_OPT_DRAFT_TRACE 3
 /* DFLASH_OPT_KERNEL_TRACE: 1 makes dflash_draft_block on the one-kernel-per-
  * operation path (and the dflash_append_block that follows it) stamp the
  * GPU's global timer (ns) for each traced launch:
@@ -321,22 +329,6 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
 /* EINVAL for an unknown option or value. Takes effect from the next call. */
 int dflash_set_option(dflash_ctx* ctx, int32_t option, int64_t value);
 int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);
-/* Copies the stamps of the last traced draft-kernel launch into out_host as
- * [rows][cols][12] (rows = phases, cols = CTAs). Per phase and CTA: 0 the
- * workers start the phase, 1 the normalised operand is built (GEMM phases
- * with an RMSNorm input) or the attention splits are done, 2 the first
- * accumulator is ready, 3 the CTA counts the phase done, 4 the MMA issuer
- * reaches the phase, 5 the last MMA is committed, 6 the first weight tile is
- * requested, 7 the first activation tile is requested, 8 the normalised
- * operand's loads have landed, 9 its row sums are done, 10 the first
- * attention split's loads have landed, 11 unused; events that do not occur
- * keep their old value (zero at first). Syncs the context's stream. ERANGE
- * if out_host is NULL or capacity < rows * cols * 12 (rows and cols are still
- * set, so a call with capacity 0 asks for the size), ESTATE if tracing was
- * never enabled. The phase order is: embedding, then per layer QKV,
- * attention, split merge, O, gate/up, down, then the lm_head. */
-int dflash_draft_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity,
-                       int32_t* rows, int32_t* cols);
 /* The kernel trace of the last traced dflash_draft_block: count entries,
  * out_host [count][3] stamps (entry, wait return, exit) and names_host their
  * newline-separated names (e.g. "L0.qkv"). A weight-streaming GEMM "X" adds
@@ -353,9 +345,8 @@ int dflash_kernel_trace(dflash_ctx* ctx, uint64_t* out_host, int64_t capacity, i
 
 /* ---- measurement ------------------------------------------------------------- */
 
-/* When enabled, dflash_draft_block brackets its lm_head kernel (the whole
- * draft kernel, when the persistent one runs) with two CUDA events owned by
- * the context, recorded on the context's stream (as event nodes when the
+/* When enabled, dflash_draft_block brackets its lm_head kernel with two CUDA
+ * events owned by the context, recorded on the context's stream (as event nodes when the
  * draft is being captured into a graph). */
 int dflash_lm_head_timing(dflash_ctx* ctx, int32_t enable);
 /* Milliseconds between the two events as last recorded (syncs on the end
@@ -386,9 +377,12 @@ int dflash_ingest_gemm_ms(dflash_ctx* ctx, float* fc_ms_host, float* kv_ms_host)
  * the legacy default stream). Its scratch is one static device array of
  * about 64 KB that every GPU loading the library holds until the process
  * exits, so it accepts only 2 <= block <= 64 and 2 <= vocab <= 1048576
- * (ERANGE beyond, with the reason in dflash_last_error(NULL)). The first call
- * on a device looks up the array's device address with that device current;
- * make that first call before any stream capture. All calls share the array:
+ * (ERANGE beyond, with the reason in dflash_last_error(NULL)). Each call
+ * made outside a stream capture looks up the array's device address with the
+ * current device (so a device reset, which reloads the library's device code,
+ * is followed); a call on a capturing stream reuses the address its device's
+ * last call found, so make the first call on a device before any stream
+ * capture. All calls share the array:
  * calls that overlap on the GPU (other streams, other host threads) race.
  * Returns EINVAL for a NULL pointer or a bad dtype, ECUDA if a CUDA call
  * fails. */
@@ -442,7 +436,11 @@ void ring_cache_destroy(ring_cache* rc);
  * if an append-only cache would overflow. */
 int ring_cache_append(ring_cache* rc, const void* k, const void* v, int32_t n);
 /* Rewinds the offset by n_rows without restoring any slot; EREWIND if n_rows
- * exceeds the rows appended since the last trim or commit. */
+ * exceeds the rows appended since the last trim or commit, or (sliding ring)
+ * exceeds the slack, capacity - window: rows appended past the slack have
+ * overwritten window rows that the rewind would make visible again [Muse
+ * "Pre-merge review round", second finding: trim must restore exactly the
+ * window seen before the append]. */
 int ring_cache_trim(ring_cache* rc, int32_t n_rows);
 /* Offset (syncs): the next absolute position to be written. */
 int ring_cache_offset(ring_cache* rc, int64_t* offset_host);

@@ -23,7 +23,7 @@ Sources, cited by page title and section:
   -- the greedy exact-match verify rule, n = accepted + 1 and trim(block - n),
   the DSpark block input and read-out rows, the Markov chain, traditional RoPE.
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open:
 
  R1  RMSNorm is x / sqrt(mean(x^2) + eps) * g with a plain gain (Qwen shape).
  R2  q/k norm is an RMSNorm over head_dim with one gain vector shared by all

@@ -94,7 +94,8 @@ def test_create_rejects_null_weights_before_cuda(B):
 
 
 def test_null_context_calls_return_einval(B):
-    assert B.lib.dflash_draft_block(None, 4, None) == B.EINVAL
+    assert B.lib.dflash_draft_block(None, -1, -1, 4, None) == B.EINVAL
+    assert B.lib.dflash_sync_round(None, None, None) == B.EINVAL
     assert B.lib.dflash_commit(None, -1) == B.EINVAL
     assert B.lib.ring_cache_trim(None, 1) == B.EINVAL
     B.lib.dflash_ctx_destroy(None)

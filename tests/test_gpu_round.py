@@ -216,6 +216,47 @@ def test_graph_round_equals_eager_round(B, H):
     assert results[0] == results[1]
 
 
+def test_host_driven_rounds_with_explicit_anchor_and_sync(B, H):
+    """The round as the pages' loop drives it: the host passes the anchor and
+    its position to the draft, and reads the verify's tokens and n back once
+    per round (dflash_sync_round). The oracle runs the same rounds."""
+    cfg = synth.config("tiny")
+    pair = H.Pair(cfg, seed=3)
+    pair.ingest(synth.make_context(cfg, 32, seed=3), 0, anchor=5)
+    stream = synth.make_target_stream(cfg, 6, 4, seed=3)
+    ids = torch.zeros(3, dtype=torch.int32, device="cuda")
+    tok = torch.zeros(4, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    anchor, pos = 5, 32
+    for r in range(6):
+        if r == 3:
+            anchor = 11                                 # the host may replace the anchor
+            pair.sess.anchor = anchor
+        pair.ctx.draft_block(4, ids, anchor=anchor, anchor_pos=pos)
+        ref = pair.sess.draft(4)
+        got = ids.cpu().numpy().astype(np.int64)
+        H.check_ids(got, ref["backbone_ids"], ref["logits"], pair.tol, "draft ids")
+        L = synth.planted_logits(stream, r, 4, got)
+        pair.ctx.verify_accept(pair.to_dev(L), 4, ids, tok, n)
+        pair.ctx.append_block(pair.to_dev(synth.resid_rows(stream, r, 4)), 4)
+        pair.ctx.commit(-1)
+        tokens_h, n_h = pair.ctx.sync_round(4)
+        want, nn, _ = O.verify_accept(O.as_f64(L, "f32"), got)
+        assert n_h == nn and tokens_h.tolist() == want.tolist()
+        pair.sess.append_and_trim(O.as_f64(synth.resid_rows(stream, r, 4), "f32"), nn)
+        pair.sess.commit(nn, int(want[-1]), 4, nn - 1)
+        anchor, pos = int(tokens_h[-1]), pos + n_h
+        pair.check_state()
+    # a position that is not the committed length is flagged, not obeyed
+    pair.ctx.draft_block(4, ids, anchor=anchor, anchor_pos=pos + 1)
+    st = pair.ctx.state()
+    assert st["error"] & 8 and st["position"] == pos
+    with pytest.raises(B.DFlashError) as e:
+        pair.ctx.draft_block(4, ids, anchor=cfg["vocab"])
+    assert e.value.code == B.ERANGE
+    pair.close()
+
+
 def test_synth_target_kernel_matches_host(B, H):
     cfg = synth.config("tiny")
     pair = H.Pair(cfg)
@@ -332,6 +373,29 @@ def test_ring_wraparound_matches_history(B, H):
     with pytest.raises(B.DFlashError) as e:
         ring.trim(1)
     assert e.value.code == B.EREWIND
+    ring.close()
+
+
+def test_ring_trim_past_slack_is_a_short_rewind(B, H):
+    """Muse page, "Pre-merge review round", second finding: a trim must bring
+    back exactly the window seen before the append. Appending more rows than
+    the slack between trims overwrites window rows, so rewinding past the
+    slack is refused (EREWIND) and the offset stays put."""
+    L, nkv, hd, W, Bmax = 1, 1, 8, 24, 4
+    ring = B.RingCache(L, nkv, hd, W, Bmax, "f32")
+    slack = ring.capacity() - W
+    assert slack == O.speculative_slack(Bmax) == 32
+    rows = torch.zeros(L, slack + 1, nkv, hd, device="cuda")
+    ring.append(rows[:, :W].contiguous(), rows[:, :W].contiguous(), W)
+    ring.trim(0)
+    ring.append(rows, rows, slack + 1)
+    before = ring.offset()
+    with pytest.raises(B.DFlashError) as e:
+        ring.trim(slack + 1)
+    assert e.value.code == B.EREWIND
+    assert ring.offset() == before
+    ring.trim(slack)                                # the slack itself may be rewound
+    assert ring.offset() == before - slack
     ring.close()
 
 
