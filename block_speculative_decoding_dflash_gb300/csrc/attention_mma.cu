@@ -5,7 +5,7 @@
 // One 16-query tile (attn_mma_kernel, mma.sync m16n8k16, fp32 accumulate):
 // the 8 warps each own 16 keys: S = Q K^T for the warp's keys (mask |q - k|
 // <= W by absolute positions), the warp's online-softmax partial (max, sum,
-// P V), a merge of the 8 warps in shared memory in warp order, and the CTA's
+// P V, with P as a high and a low bf16 part), a merge of the 8 warps in shared memory in warp order, and the CTA's
 // partial written to global scratch. Two to four tiles: attn_tc_kernel
 // (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
 // merges the splits in split order and writes the bf16 output; nothing waits
@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
         m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 1));
         m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 2));
       }
-      // P = exp(S - m) (bf16 for the MMA), row sums, O = P V
-      uint32_t pa[4];
+      // P = exp(S - m) as a high and a low bf16 part, row sums, O = P V
+      uint32_t pa[4], pl[4];
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         float pv[2][2];
@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
           }
         pa[hr] = pack_bf16(pv[0][0], pv[0][1]);        // keys 0..7 of this row
         pa[2 + hr] = pack_bf16(pv[1][0], pv[1][1]);    // keys 8..15
+        pl[hr] = pack_bf16_residue(pv[0][0], pv[0][1]);
+        pl[2 + hr] = pack_bf16_residue(pv[1][0], pv[1][1]);
         l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 1);
         l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 2);
       }
@@ -210,6 +212,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
         ldsm_x4_t(&S.v[warp * 16 + (mi & 1) * 8 + (lane & 7)][dt * 16 + (mi >> 1) * 8], b0, b1, b2, b3);
         mma16816(o[dt * 2], pa[0], pa[1], pa[2], pa[3], b0, b1);
         mma16816(o[dt * 2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+        mma16816(o[dt * 2], pl[0], pl[1], pl[2], pl[3], b0, b1);
+        mma16816(o[dt * 2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
       }
     }
     // publish the warp's partial, then merge the 8 warps in warp order
@@ -276,8 +280,9 @@ constexpr int kTileQ = 64;                 // queries per kv head of the tensor-
 
 // ---------------------------------------------------------------------------
 // Up to 64 queries per kv head on the 5th-generation tensor cores. Per key
-// split: S = Q K^T and then O = P V, each one 128 x 128 x 128 product issued
-// as eight tcgen05.mma (kind::f16, fp32 accumulators in TMEM). Operands are
+// split: S = Q K^T and then O = P V, 128 x 128 x 128 products issued as
+// tcgen05.mma (kind::f16, fp32 accumulators in TMEM); P V is two products,
+// of P's high and low bf16 parts, so P keeps about 16 significant bits. Operands are
 // K-major shared-memory tiles in the 128-byte swizzled layout: Q and K as
 // loaded, V transposed in shared memory (keys along K), P written by the
 // softmax threads into Q's place once S is done.
@@ -476,24 +481,29 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   __syncthreads();
   const float M = fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
   float l = 0.f;
-  uint32_t pk[16];
+  uint32_t pk[16], pr[16];
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const float p0 = (M == -INFINITY || sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - M);
     const float p1 = (M == -INFINITY || sv[c + 1] == -INFINITY) ? 0.f : exp2f(sv[c + 1] - M);
     l += p0 + p1;
     pk[c >> 1] = pack_bf16(p0, p1);
+    pr[c >> 1] = pack_bf16_residue(p0, p1);
   }
   red_l[grp][qi] = l;
   // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
-  // over the same granules of the other tile
+  // over the same granules of the other tile; the high bf16 part in Q's
+  // tiles, the low part in K's (K is no longer read once S is done)
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     const int gg = half * 4 + gi;
-    *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + R * 128 + ((gg ^ (R & 7)) << 4)) =
+    const int at = R * 128 + ((gg ^ (R & 7)) << 4);
+    *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + at) =
         make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
-    *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + R * 128 + ((gg ^ (R & 7)) << 4)) =
-        make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(sm + kTcK + rh * kTcTileB + at) =
+        make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
+    *reinterpret_cast<uint4*>(sm + kTcK + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_shared();
   tc_fence_before();
@@ -506,6 +516,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       for (int kk = 0; kk < 4; ++kk)
         tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
                     smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcK + kc * kTcTileB + kk * 32),
+                    smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, 1u);
     tc_commit(&bar[1]);
   }
   // O: rows R and R + 64 hold the two halves of query qi's sum; each thread

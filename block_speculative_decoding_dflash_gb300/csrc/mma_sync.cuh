@@ -38,5 +38,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// The rounding residues x - bf16(x) of two values, packed as bf16: with
+// pack_bf16 they split fp32 attention probabilities into a high and a low
+// bf16 part whose sum keeps about 16 significant bits, so that P V on bf16
+// tensor cores (two products) loses no more than the fp32 softmax itself.
+__device__ __forceinline__ uint32_t pack_bf16_residue(float lo, float hi) {
+  const float rl = lo - __bfloat162float(__float2bfloat16_rn(lo));
+  const float rh = hi - __bfloat162float(__float2bfloat16_rn(hi));
+  return pack_bf16(rl, rh);
+}
 
 }  // namespace dfl

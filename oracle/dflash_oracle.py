@@ -47,13 +47,20 @@ Readings of points the pages leave open:
      q/k-norm + RoPE output, attention output, residual sums, the SwiGLU
      product; logits stay fp32.
 
-Parity status: the slack rule, the ring restore, accept = prefix + 1, the
-mask, attention, RoPE, RMSNorm, linear, window drop, softcap, argmax ties,
-verify and the Markov feedback are pinned by ``tests/test_oracle_pins.py``.
-The composition of a drafter layer (readings R1, R2, R4, R6, R12) is checked
-only by invariants (identity layers, translation invariance, window bound,
-bidirectionality); the pages print no numbers for it, so that composition is
-"parity unpinned" beyond those invariants.
+Parity status: every function here has a named pin. The slack rule, the ring
+restore, accept = prefix + 1, the mask, attention, RoPE, RMSNorm, linear,
+window drop, softcap, argmax ties, bf16 rounding, verify and the Markov
+feedback are pinned by ``tests/test_oracle_pins.py`` (page values, torch
+fp64 routines, closed forms, brute force). The composition is pinned by
+``tests/test_oracle_composition.py`` with closed forms on constructed
+weights: the drafter layer (uniform attention gives x + Wo . mean of the
+visible values; a gate/up fixture gives the MLP's output by hand; the MLP's
+input depends on Wo), the context path (one-hot fc / Wk / Wv give each K and
+V row by hand, RoPE at the absolute position, no input norm), the draft's
+read-out rows through the final norm, lm_head and softcap, and the session's
+history against the ring model. The pages print no numbers for the layer
+layout itself (readings R1, R2, R4, R6, R12): those pins fix the reading
+taken, not a value from the pages.
 """
 
 from __future__ import annotations

@@ -18,7 +18,7 @@ import oracle as O
 from block_speculative_decoding_dflash_gb300 import binding as B
 from block_speculative_decoding_dflash_gb300 import synth
 
-TOL = {"f32": 1e-4, "bf16": 2e-2}
+from tolerances import BF16_HIDDEN_L2, BF16_HIDDEN_MAXABS_RATIO, TOL
 
 
 class LazyRows:
@@ -61,12 +61,10 @@ def assert_rows_close(got, ref, tol, what):
 
 def assert_hidden_close(got, ref, tol, dtype, what):
     """Final hidden rows. fp32: max-abs <= tol * row max. bf16: relative L2
-    error <= tol and max-abs <= 2 * tol * row max per row. After five
-    bf16 layers an fp32-accumulating implementation with the oracle's own
-    rounding points already deviates from the fp64 oracle by up to ~2% of the
-    row max on single elements (a few bf16 ulps at the largest element, from
-    residual sums that round to the neighbouring value), with ~1.4% relative
-    L2; the bound is set at that arithmetic, not at the logit rule."""
+    error <= BF16_HIDDEN_L2 and max-abs <= BF16_HIDDEN_MAXABS_RATIO *
+    BF16_HIDDEN_L2 of the row's largest magnitude, the rule derived in
+    test_bf16_tolerance.py (an fp32 implementation with the oracle's rounding
+    points already sits at about 1.5% relative L2 after five bf16 layers)."""
     if dtype == "f32":
         return assert_rows_close(got, ref, tol, what)
     got = np.asarray(got, dtype=np.float64)
@@ -74,7 +72,7 @@ def assert_hidden_close(got, ref, tol, dtype, what):
     assert got.shape == ref.shape
     l2 = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
     mx = np.abs(got - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)
-    bad = np.nonzero((l2 > tol) | (mx > 2 * tol))[0]
+    bad = np.nonzero((l2 > BF16_HIDDEN_L2) | (mx > BF16_HIDDEN_MAXABS_RATIO * BF16_HIDDEN_L2))[0]
     assert bad.size == 0, f"{what}: rows {bad[:8].tolist()} l2 {l2[bad[:8]].tolist()} maxabs {mx[bad[:8]].tolist()}"
 
 

@@ -416,15 +416,22 @@ def test_ring_floor_at_block_129(B, H, flags, corrupt):
     ring.gather(p - W, W, before_k, before_v)
     blk = torch.full((L, Bk, nkv, hd), -7.0, dtype=torch.bfloat16, device="cuda")
     ring.append(blk, blk, Bk)
-    ring.trim(Bk)
     after_k = torch.empty_like(before_k)
     after_v = torch.empty_like(before_k)
+    # the slots of the window seen before the append
     ring.gather(p - W, W, after_k, after_v)
     same = torch.equal(before_k, after_k)
     assert same != corrupt
     if corrupt:
         diff = (before_k != after_k).any(dim=-1).view(-1).nonzero().view(-1).tolist()
         assert diff == [0]                          # the oldest window row, overwritten by block row 128
+        # a rewind would expose it: trim refuses to go past the slack
+        with pytest.raises(B.DFlashError) as e:
+            ring.trim(Bk)
+        assert e.value.code == B.EREWIND
+    else:
+        ring.trim(Bk)
+        assert ring.offset() == p
     ring.close()
 
 
