@@ -5,8 +5,13 @@ One step = one whole Muse-assistant-shaped job: ingest 2048 captured context
 rows (window 2048), then 512 rounds (draft, stand-in target, verify, ring
 append, partial-accept trim) with the verify width starting at 4 and
 widening to 16 when a measurement window pays for it. Metric: rounds/s
-(whole job, all GPUs); draft tokens/s and the HBM roofline fraction of the
-draft kernel (the whole drafter forward + lm_head argmax) ride along. Inputs are synthetic (seeded), weights random-init bf16.
+(whole job, all GPUs). Riding along: draft tokens/s; the HBM roofline
+fraction of the lm_head kernel (the round's largest) and of the whole round
+per width; a per-kernel-class breakdown from one traced round per width; the
+end-to-end rate with host inputs; the CPU oracle on the host cores; and the
+other shapes of the workload list (DSpark drafter, long-context slab stress,
+block-width sweep), each through captured round graphs. Inputs are synthetic
+(seeded), weights random-init bf16.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -45,6 +50,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-rounds", type=int, default=3)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the DSpark, slab-stress and width-sweep measurements")
+    ap.add_argument("--no-breakdown", action="store_true", help="skip the per-kernel trace")
+    ap.add_argument("--config-rounds", type=int, default=64,
+                    help="timed rounds per point of the DSpark / width-sweep measurements")
     return ap.parse_args()
 
 
@@ -231,7 +241,7 @@ class Job:
 
     def run(self, e2e=False):
         """One job. Returns dict of counters; the caller brackets timing."""
-        from block_speculative_decoding_dflash_gb300.policy import ThroughputController
+        from block_speculative_decoding_dflash_gb300.policy import ThroughputController, resolve_widths
         torch, c, a = self.torch, self.ctx, self.args
         s = self.stream
         launches = 0
@@ -247,7 +257,9 @@ class Job:
         i1.record(s)
         launches += self.kcount[self.SLOT_INGEST]
         gemm_ms = c.ingest_gemm_ms()
-        ctl = ThroughputController(4, 16, window=a.window, challenge_every=a.challenge_every)
+        # the Muse assistant declares a depth of 4 under the requested 16 rows
+        depth, ceiling = resolve_widths(16, configured_depth=4)
+        ctl = ThroughputController(depth, ceiling, window=a.window, challenge_every=a.challenge_every)
         done, lm_ms, emitted_prev, proposals = 0, [], 0, 0
         widths_used = []
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -321,9 +333,242 @@ def draft_bytes(cfg, rows, nctx):
     return cfg["n_layers"] * (layer + kv) + lm_head_bytes(cfg, rows - 1) + rows * H * 2
 
 
-def cpu_baseline(job, n_rounds):
+def round_bytes(cfg, block, nctx):
+    """Algorithmic HBM bytes of one round at verify width `block` with `nctx`
+    visible context rows: every drafter weight once (5 layers of Wq Wk Wv Wo
+    Wg Wu Wd and their norm gains, the lm_head), the window's K and V of every
+    layer, the block's embedding rows, the target's block logits, the captured
+    residual rows and encoder.fc plus every layer's Wk and Wv for the append,
+    and the ring rows it writes."""
+    H, I, hd, L = cfg["hidden"], cfg["intermediate"], cfg["head_dim"], cfg["n_layers"]
+    V, kin = cfg["vocab"], cfg["k_target_layers"] * cfg["target_hidden"]
+    qdim, kvdim = cfg["n_q_heads"] * hd, cfg["n_kv_heads"] * hd
+    rows = block - 1 if cfg.get("kind") == "dspark" else block
+    layer_w = (H * (qdim + 2 * kvdim) + qdim * H + 3 * H * I + 2 * H + 2 * hd) * 2
+    draft = L * (layer_w + 2 * nctx * kvdim * 2) + 2 * H * 2 + V * H * 2 + (H * 2 if rows else 0)
+    if cfg.get("markov_rank", 0):
+        r = cfg["markov_rank"]
+        draft += r * V * 2 + (block - 1) * r * 2
+    verify = block * V * 2
+    append = block * kin * 2 + H * kin * 2 + 2 * H * 2 + L * 2 * kvdim * H * 2 + L * 2 * block * kvdim * 2
+    return draft + verify + append
+
+
+# bytes each traced kernel class must move per launch (Muse shape)
+def _class_bytes(cfg, block):
+    H, I, hd, L = cfg["hidden"], cfg["intermediate"], cfg["head_dim"], cfg["n_layers"]
+    qdim, kvdim = cfg["n_q_heads"] * hd, cfg["n_kv_heads"] * hd
+    kin = cfg["k_target_layers"] * cfg["target_hidden"]
+    nctx = cfg["window"] if cfg["window"] > 0 else cfg["context_rows"]
+    return {"qkv": H * (qdim + 2 * kvdim) * 2, "attn": 2 * nctx * kvdim * 2, "o": qdim * H * 2,
+            "gate_up": 2 * H * I * 2, "down": I * H * 2, "lm_head": cfg["vocab"] * H * 2,
+            "append.fc": H * kin * 2 + block * kin * 2, "append.kv": L * 2 * kvdim * H * 2}
+
+
+def kernel_breakdown(job, peak):
+    """One traced round per width (captured like the timed rounds): for every
+    kernel of the round the time from the release of its programmatic
+    dependency to its last CTA's exit (weights a kernel requested before the
+    release stream during its predecessor), summed per class, with the class's
+    algorithmic bytes over that time."""
+    c, out = job.ctx, {}
+    pools = (job.pool_L, job.pool_P, job.pool_C, job.pool_R)
+    for w in job.widths:
+        job.bw = w
+        c.kernel_trace(True)
+        c.capture_begin()
+        job._round(pools)
+        c.capture_end(60)
+        c.kernel_trace(False)
+        for _ in range(4):
+            c.graph_launch(60)
+        c.sync()
+        tr = c.kernel_trace_read()
+        main = [t for t in tr if not any(t[0].endswith(x) for x in (".1", ".2", ".3"))]
+        t0 = min(t[1] for t in main)
+        t1 = max(t[3] for t in main)
+        by = {}
+        for name, _entry, wait_ret, exit_ in main:
+            cls = name.split(".", 1)[1] if name.startswith("L") else name
+            by.setdefault(cls, []).append((exit_ - wait_ret) / 1e3)
+        nb = _class_bytes(job.cfg, w)
+        cl = {}
+        for cls, us in sorted(by.items()):
+            mean = statistics.mean(us)
+            e = {"launches": len(us), "us_per_launch": round(mean, 2), "us_per_round": round(sum(us), 1)}
+            if cls in nb:
+                gbs = nb[cls] / (mean * 1e-6) / 1e9
+                e.update({"bytes": nb[cls], "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)})
+            cl[cls] = e
+        out[str(w)] = {"traced_span_us": round((t1 - t0) / 1e3, 1), "classes": cl}
+    return {"how": "kernel trace (globaltimer) of one captured round per width: per launch, "
+                   "dependency release to last CTA exit", "by_width": out}
+
+
+def _pools(B, ts, device):
+    import torch
+    i16 = lambda a: np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)
+    tt = lambda a: torch.from_numpy(i16(a)).to(device)
+    bf = ts["logits"].dtype == np.uint16
+    v = (lambda t: t.view(torch.bfloat16)) if bf else (lambda t: t)
+    return (v(tt(ts["logits"])), v(tt(ts["plant"])), tt(ts["coins"]), v(tt(ts["resid"])))
+
+
+class _Rounds:
+    """Round buffers and graphs of one side measurement."""
+
+    def __init__(self, ctx, cfg, bmax, device):
+        import torch
+        V, kin = cfg["vocab"], cfg["k_target_layers"] * cfg["target_hidden"]
+        tdt = torch.bfloat16
+        self.ctx, self.torch = ctx, torch
+        self.ids = torch.zeros(bmax, dtype=torch.int32, device=device)
+        self.tok = torch.zeros(bmax, dtype=torch.int32, device=device)
+        self.n = torch.zeros(1, dtype=torch.int32, device=device)
+        self.Lb = torch.zeros(bmax, V, dtype=tdt, device=device)
+        self.Rb = torch.zeros(bmax, kin, dtype=tdt, device=device)
+
+    def round(self, pools, w, keep=-1):
+        c = self.ctx
+        c.draft_block(w, self.ids)
+        c.synth_target(*pools, w, self.ids, self.Lb, self.Rb)
+        c.verify_accept(self.Lb, w, self.ids, self.tok, self.n)
+        c.append_block(self.Rb, w)
+        c.commit(keep)
+
+    def capture(self, slot, pools, w, keep=-1):
+        self.ctx.capture_begin()
+        self.round(pools, w, keep)
+        self.ctx.capture_end(slot)
+
+    def timed(self, slots, s):
+        """Launches the graph slots in order; returns elapsed ms."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for sl in slots:
+            self.ctx.graph_launch(sl)
+        e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
+
+def side_configs(job, args, peak, device):
+    """The other shapes the workload list names, each timed with CUDA events
+    on the context's stream through captured round graphs: the DSpark drafter
+    (widths 8 and 10, rank-256 Markov chain, append-only cache), the
+    long-context slab stress (16384-row slab, window drop, width 16, keep ~
+    U{0..16}) and the Muse block-width sweep (widths 4..129 x planting
+    probability 0.3 / 0.7 / 0.95)."""
+    import torch
+    B, synth = job.B, job.synth
+    R = args.config_rounds
+    out = {}
+    # -- DSpark ------------------------------------------------------------------------
+    t0 = time.time()
+    dcfg = synth.config("dspark", max_context=1024 + 3 * (R + 8) * 10)
+    dw = B.weights_to_device(synth.make_weights(dcfg, 0), "bf16", device)
+    ctx = B.DFlashContext(dcfg, dw)
+    ctx.ingest_context(B.to_device(synth.make_context(dcfg, 1024, seed=4), "bf16", device), 1024, 0, 999)
+    ts = synth.make_target_stream(dcfg, 2 * (R + 8) + 8, 10, seed=4, logit_pool=8, resid_pool=16)
+    pools = _pools(B, ts, device)
+    rb = _Rounds(ctx, dcfg, 10, device)
+    res = {}
+    for w in (8, 10):
+        rb.round(pools, w)
+        rb.capture(w, pools, w)
+        for _ in range(4):
+            ctx.graph_launch(w)
+        st0 = ctx.stats()
+        ms = rb.timed([w] * R, ctx.stream)
+        st1 = ctx.stats()
+        nctx = 1024 + (st1["emitted"])
+        us = ms * 1e3 / R
+        res[str(w)] = {"rounds_per_s": round(R / (ms / 1e3), 1),
+                       "draft_tok_s": round(R * (w - 1) / (ms / 1e3), 1),
+                       "accepted_per_round": round((st1["accepted"] - st0["accepted"]) / R, 3),
+                       "round_us": round(us, 1),
+                       "round_frac": round(round_bytes(dcfg, w, nctx) / (us * 1e-6) / 1e9 / peak, 3)}
+    out["dspark"] = {"workload": "dspark_bf16_ctx1024_vocab65536_markov256_block8and10",
+                     "rounds_timed_per_width": R, "by_width": res,
+                     "note": "tied lm_head; proposals are the Markov chain argmax(W1[prev] W2)",
+                     "setup_s": round(time.time() - t0, 1)}
+    ctx.close()
+    del dw
+    # -- slab stress ----------------------------------------------------------------------
+    t0 = time.time()
+    cfg = job.cfg
+    ctx = B.DFlashContext(cfg, job.wd)
+    slab = B.to_device(synth.make_context(cfg, 16384, seed=3, name="slab"), "bf16", device)
+    ctx.ingest_context(slab, 16384, 0, 4321)
+    ctx.sync()
+    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    i0.record(ctx.stream)
+    ctx.ingest_context(slab, 16384, 0, 4321)
+    i1.record(ctx.stream)
+    i1.synchronize()
+    ingest_ms = i0.elapsed_time(i1)
+    nr = 256
+    ts = synth.make_target_stream(cfg, nr + 64, 16, seed=3, logit_pool=4, resid_pool=32)
+    pools = _pools(B, ts, device)
+    keeps = np.random.default_rng(33).integers(0, 17, nr)
+    rb = _Rounds(ctx, cfg, 16, device)
+    for k in range(17):
+        rb.round(pools, 16, k)
+        rb.capture(k, pools, 16, k)
+    st0 = ctx.stats()
+    ms = rb.timed([int(k) for k in keeps], ctx.stream)
+    st1 = ctx.stats()
+    us = ms * 1e3 / nr
+    out["slab_stress"] = {"workload": "muse_bf16_slab16384_w2048_block16_keepU0to16_256rounds",
+                          "ingest_ms": round(ingest_ms, 3),
+                          "ingest_note": "16384-row slab: the 14336 rows older than the window are "
+                                         "dropped before encoder.fc, 2048 kept",
+                          "rounds_per_s": round(nr / (ms / 1e3), 1),
+                          "draft_tok_s": round(nr * 15 / (ms / 1e3), 1), "round_us": round(us, 1),
+                          "round_frac": round(round_bytes(cfg, 16, 2048) / (us * 1e-6) / 1e9 / peak, 3),
+                          "rounds": st1["rounds"] - st0["rounds"],
+                          "setup_s": round(time.time() - t0, 1)}
+    ctx.close()
+    del slab
+    # -- block-width sweep ----------------------------------------------------------------
+    t0 = time.time()
+    scfg = dict(cfg, max_block=129)
+    ctx = B.DFlashContext(scfg, job.wd)
+    ctx.ingest_context(job.resid, 2048, 0, 77)
+    rb = _Rounds(ctx, scfg, 129, device)
+    sweep = {}
+    for pi, p in enumerate((0.3, 0.7, 0.95)):
+        ts = synth.make_target_stream(scfg, 8 * (R + 8), 129, seed=20 + pi, logit_pool=4, resid_pool=8,
+                                      p_plant=p)
+        pools = _pools(B, ts, device)
+        for slot, w in enumerate((4, 5, 8, 16, 32, 129)):
+            rb.round(pools, w)
+            rb.capture(slot, pools, w)
+            for _ in range(4):
+                ctx.graph_launch(slot)
+            st0 = ctx.stats()
+            ms = rb.timed([slot] * R, ctx.stream)
+            st1 = ctx.stats()
+            us = ms * 1e3 / R
+            sweep.setdefault(str(w), {})[str(p)] = {
+                "rounds_per_s": round(R / (ms / 1e3), 1),
+                "draft_tok_s": round(R * (w - 1) / (ms / 1e3), 1),
+                "accepted_per_round": round((st1["accepted"] - st0["accepted"]) / R, 3),
+                "round_us": round(us, 1),
+                "round_frac": round(round_bytes(scfg, w, 2048) / (us * 1e-6) / 1e9 / peak, 3)}
+        del pools
+    out["width_sweep"] = {"workload": "muse_bf16_ctx2048_vocab202048_block4to129_p0.3_0.7_0.95",
+                          "rounds_timed_per_point": R, "by_width_then_p": sweep,
+                          "setup_s": round(time.time() - t0, 1)}
+    ctx.close()
+    return out
+
+
+def cpu_baseline(job, n_rounds, mix):
     """The oracle as it stands, on the host cores: ingest + n_rounds rounds at
-    width 4, extrapolated to the 512-round job."""
+    each verify width, weighted by the width mix of the GPU job (mix: width ->
+    share of its rounds) and extrapolated to the 512-round job."""
     import oracle as O
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     cfg, w = job.cfg, job.w
@@ -342,21 +587,26 @@ def cpu_baseline(job, n_rounds):
     sess.ingest(O.as_f64(job.resid_host, "bf16"), 0, 5)
     t_ingest = time.time() - t0
     ts = job.ts
-    t0 = time.time()
     from block_speculative_decoding_dflash_gb300 import synth
-    for r in range(n_rounds):
-        d = sess.draft(4)
-        L = synth.planted_logits(ts, r, 4, d["draft_ids"])
-        tokens, n, _ = sess.verify(O.as_f64(L, "bf16"), d["draft_ids"])
-        sess.append_and_trim(O.as_f64(synth.resid_rows(ts, r, 4), "bf16"), n)
-        sess.commit(n, int(tokens[-1]), 4, n - 1)
-    t_round = (time.time() - t0) / n_rounds
+    per_width, r = {}, 0
+    for w in sorted(mix):
+        t0 = time.time()
+        for _ in range(n_rounds):
+            d = sess.draft(w)
+            L = synth.planted_logits(ts, r, w, d["draft_ids"])
+            tokens, n, _ = sess.verify(O.as_f64(L, "bf16"), d["draft_ids"])
+            sess.append_and_trim(O.as_f64(synth.resid_rows(ts, r, w), "bf16"), n)
+            sess.commit(n, int(tokens[-1]), w, n - 1)
+            r += 1
+        per_width[w] = (time.time() - t0) / n_rounds
+    t_round = sum(mix[w] * per_width[w] for w in mix)
     job_s = t_ingest + job.args.rounds * t_round
     cores = len(os.sched_getaffinity(0))
+    widths = ", ".join(f"width {w}: {per_width[w]:.2f} s/round x {mix[w]:.2f} of the rounds" for w in sorted(mix))
     return {"value": job.args.rounds / job_s, "unit": "rounds/s", "cores": cores, "kind": "oracle",
-            "sample": f"ingest of 2048 context rows ({t_ingest:.2f} s) + {n_rounds} rounds at width 4 "
-                      f"({t_round:.2f} s/round), extrapolated to the {job.args.rounds}-round job; "
-                      f"fp64 weight conversion ({setup:.1f} s) untimed"}
+            "sample": f"ingest of 2048 context rows ({t_ingest:.2f} s) + {n_rounds} rounds at each width "
+                      f"({widths}), weighted by the GPU job's width mix and extrapolated to the "
+                      f"{job.args.rounds}-round job; fp64 weight conversion ({setup:.1f} s) untimed"}
 
 
 def run_ours(args, world, rank, local):
@@ -442,9 +692,24 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "host_wall_s": round(wall, 3)}
 
+    # the round against its HBM roofline, per width: every byte a round must
+    # move (round_bytes) over the mean round time the controller measured
+    peak = peaks["hbm_gbs"]
+    round_roof = {}
+    for w, us in round_us.items():
+        nb = round_bytes(cfg, int(w), cfg["window"])
+        gbs = nb / (us * 1e-6) / 1e9
+        round_roof[w] = {"bytes": nb, "us": us, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    nw = len(widths)
+    mix = {w: widths.count(w) / nw for w in set(widths)}
+    job_bytes = sum(round_bytes(cfg, w, cfg["window"]) for w in widths) / args.steps
+    job_gbs = job_bytes / (ms_max / args.steps / 1e3) / 1e9 / world
+    breakdown = None if args.no_breakdown else kernel_breakdown(job, peak)
+    configs = None if args.no_configs else side_configs(job, args, peak, device)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(job, args.cpu_rounds)
+        cpu = cpu_baseline(job, args.cpu_rounds, mix)
 
     if rank == 0:
         line = {
@@ -467,7 +732,15 @@ def run_ours(args, world, rank, local):
                          "peak": peaks["hbm_gbs"], "peak_source": which, "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
                          "traffic": LMHEAD_TRAFFIC, "launches_timed": len(lm_t),
-                         "mean_ms": round(sum(lm_t) / len(lm_t), 4) if lm_t else None},
+                         "mean_ms": round(sum(lm_t) / len(lm_t), 4) if lm_t else None,
+                         "round": {"by_width": round_roof,
+                                   "job": {"gbs": round(job_gbs, 1), "frac": round(job_gbs / peak, 4)},
+                                   "bytes": "every drafter weight once, the window's K and V of every "
+                                            "layer, the block logits, residual rows, encoder.fc and "
+                                            "every layer's Wk, Wv for the append, the ring rows "
+                                            "written (round_bytes in bench.py)"}},
+            "kernels": breakdown,
+            "configs": configs,
             "context_ingest": ingest,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "setup_s": round(job.setup_s, 1),

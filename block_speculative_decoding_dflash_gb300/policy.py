@@ -1,44 +1,89 @@
 """Verify-width policy of the round loop (host side, no kernel).
 
-"Muse Glimmer DFlash assistant drafter on the round loop", "What changed"
-(round loop bullet) and "Real-checkpoint validation" item 5: the Muse
-assistant starts at its declared depth of 4 rows and widens to the requested
-ceiling (16) only when a measurement window pays for it in tokens per
-millisecond. This controller does that with two widths: it runs windows of
-``window`` rounds at the current width, and every ``challenge_every`` windows
-runs one window at the other width; the other width is adopted when its
-tokens/ms beats the current width's last window.
+"Muse Glimmer DFlash assistant drafter on the round loop":
+
+* "What changed", round-loop bullet: the round loop reads the drafter's
+  declared depth (``configured_block_size``) and whether it insists on the
+  requested width (``prefer_requested_block_size``). A drafter that declares a
+  depth below the requested width without insisting on it runs a block
+  throughput controller between the two; a drafter with no depth (Qwen 3.5
+  DFlash) or one that prefers the requested width (DSpark) keeps a fixed
+  width. ``resolve_widths`` is that rule.
+* "Real-checkpoint validation", item 5: the Muse assistant starts at 4 rows
+  under the 16-row ceiling and widens only when a measurement window pays for
+  it in tokens per millisecond. ``ThroughputController`` runs windows at the
+  current width and periodically one challenge window at each other probed
+  width, adopting a challenger whose tokens/ms beats the current width's last
+  window.
+* "Pre-merge review round", first finding: a check made at one width is no
+  evidence about another (the width selects different kernels), so a gate
+  that must hold wherever the loop runs has to pass at every width the run
+  can settle on (``probed_verify_widths``), and its decline names the width
+  that failed. ``ExactnessGate`` is that gate; the probe itself is supplied by
+  the caller. Its verdicts are cached per (model identity, width), so two
+  checkpoints of the same shape are not confused (the third LOW finding).
 """
 
 from __future__ import annotations
 
+from dataclasses import dataclass, field
+from typing import Callable, Optional
+
+
+def resolve_widths(requested: int, configured_depth: Optional[int] = None,
+                   prefer_requested: bool = False) -> tuple:
+    """(depth, ceiling) the round loop runs between; depth == ceiling means a
+    fixed width. The depth applies only when it is below the requested width
+    and the drafter does not insist on the requested width."""
+    if requested < 2:
+        raise ValueError("the verify width must be at least 2")
+    if configured_depth is None or prefer_requested or configured_depth >= requested:
+        return requested, requested
+    if configured_depth < 2:
+        raise ValueError("a declared depth must be at least 2")
+    return configured_depth, requested
+
 
 class ThroughputController:
+    """Measurement windows over a ladder of verify widths.
+
+    The run starts at ``depth``. Windows of ``window`` rounds run at the
+    current width; after every ``challenge_every`` windows at the current
+    width, one window runs at the next challenger (the other probed widths in
+    turn, nearest first). A challenger is adopted when its tokens/ms beats the
+    current width's last window. ``widths`` defaults to (depth, ceiling)."""
+
     def __init__(self, depth: int = 4, ceiling: int = 16, window: int = 32,
-                 challenge_every: int = 4):
+                 challenge_every: int = 4, widths: Optional[tuple] = None):
         if depth < 2 or ceiling < depth or window < 1 or challenge_every < 1:
             raise ValueError("bad controller parameters")
-        self.depth, self.ceiling = depth, ceiling
+        ws = tuple(sorted(set(widths if widths is not None else (depth, ceiling))))
+        if ws[0] != depth or ws[-1] != ceiling or any(w < 2 for w in ws):
+            raise ValueError("the width ladder must run from the depth to the ceiling")
+        self.depth, self.ceiling, self.ladder = depth, ceiling, ws
         self.window, self.challenge_every = window, challenge_every
         self.current = depth
         self.rate = {}
         self.since_challenge = 0
+        self._turn = 0
         self.history = []          # (width, tokens, ms, adopted)
 
     def probed_verify_widths(self) -> tuple:
-        """Every width a run can settle on: the warm-up depth and the
-        ceiling ("Pre-merge review round", the exactness-gate finding: a check
-        made at one width says nothing about another, so anything that must
-        hold at the widths the loop runs at has to be checked at all of
-        these)."""
-        return tuple(sorted({self.depth, self.ceiling}))
+        """Every width a run can settle on: the warm-up depth, the ceiling and
+        any width between them on the ladder."""
+        return self.ladder
+
+    def challengers(self) -> list:
+        """The other probed widths, nearest to the current width first."""
+        return sorted((w for w in self.ladder if w != self.current),
+                      key=lambda w: (abs(w - self.current), w))
 
     def other(self) -> int:
-        return self.ceiling if self.current == self.depth else self.depth
+        return self.challengers()[self._turn % max(1, len(self.ladder) - 1)]
 
     def next_width(self) -> int:
         """Width of the next measurement window."""
-        if self.depth == self.ceiling:
+        if len(self.ladder) == 1:
             return self.current
         if self.since_challenge >= self.challenge_every and self.current in self.rate:
             return self.other()
@@ -46,15 +91,60 @@ class ThroughputController:
 
     def observe(self, width: int, tokens: int, ms: float) -> None:
         """Feed the emitted tokens and elapsed ms of one finished window."""
+        if width not in self.ladder:
+            raise ValueError(f"width {width} is not on the probed ladder {self.ladder}")
         rate = tokens / ms if ms > 0 else 0.0
         adopted = False
+        self.rate[width] = rate
         if width == self.current:
-            self.rate[width] = rate
             self.since_challenge += 1
         else:
-            self.rate[width] = rate
+            self._turn += 1
             if rate > self.rate.get(self.current, float("inf")):
                 self.current = width
                 adopted = True
+                self._turn = 0
             self.since_challenge = 0
         self.history.append((width, tokens, ms, adopted))
+
+    def tokens_per_ms(self) -> dict:
+        return dict(self.rate)
+
+
+@dataclass
+class GateVerdict:
+    allowed: bool
+    failed_width: Optional[int] = None
+    detail: str = ""
+
+    def message(self, requested: int) -> str:
+        if self.allowed:
+            return f"speculative dispatch allowed at every probed width (requested {requested})"
+        return (f"speculative dispatch declined: the exactness probe did not pass at "
+                f"block_size={self.failed_width} (requested {requested}); {self.detail}")
+
+
+@dataclass
+class ExactnessGate:
+    """Allows speculative dispatch only if ``probe(width)`` passes at every
+    probed width. ``probe`` returns (passed, detail). Verdicts are cached per
+    (model identity, width)."""
+
+    probe: Callable[[int], tuple]
+    model_key: tuple
+    cache: dict = field(default_factory=dict)
+    calls: int = 0
+
+    def check(self, width: int) -> tuple:
+        key = self.model_key + (width,)
+        if key not in self.cache:
+            self.calls += 1
+            self.cache[key] = self.probe(width)
+        return self.cache[key]
+
+    def allows_every_width(self, widths) -> GateVerdict:
+        for w in sorted(widths):
+            ok, detail = self.check(w)
+            if not ok:
+                return GateVerdict(False, w, detail)
+        return GateVerdict(True)

@@ -72,8 +72,9 @@ def test_muse_slab_stress_wraparound(H, muse):
     """16384-row slab, rows older than W dropped before fc; block 16, slack
     128; 256 rounds keeping n ~ U{0..16} rows, so append and trim cross the
     ring boundary. The ring content does not depend on the drafts, so the
-    oracle tracks every round's ring and the drafts are checked on the
-    first rounds."""
+    oracle tracks every round's ring; the drafts are checked on the first
+    rounds and then on one round in 32, long after the ring has wrapped
+    (the oracle takes the GPU's anchor there: teacher forcing)."""
     from block_speculative_decoding_dflash_gb300 import binding as B
     pair = _pair(H, muse)
     cfg = pair.cfg
@@ -96,10 +97,19 @@ def test_muse_slab_stress_wraparound(H, muse):
     n = torch.zeros(1, dtype=torch.int32, device="cuda")
     Lb = torch.zeros(16, cfg["vocab"], dtype=torch.bfloat16, device="cuda")
     Rb = torch.zeros(16, 10240, dtype=torch.bfloat16, device="cuda")
+    checked = 0
     for r in range(3, rounds):
-        ctx.draft_block(16, ids)
-        ctx.synth_target(pools["logits"], pools["plant"], pools["coins"], pools["resid"], 16, ids, Lb, Rb)
-        ctx.verify_accept(Lb, 16, ids, tok, n)
+        d = ids
+        if r % 32 == 0:
+            st = ctx.state()
+            assert st["position"] == pair.sess.pos and st["error"] == 0
+            pair.sess.anchor = st["anchor"]
+            d, _, _ = pair.draft(16)               # compared with the oracle's draft
+            checked += 1
+        else:
+            ctx.draft_block(16, d)
+        ctx.synth_target(pools["logits"], pools["plant"], pools["coins"], pools["resid"], 16, d, Lb, Rb)
+        ctx.verify_accept(Lb, 16, d, tok, n)
         ctx.append_block(Rb, 16)
         ctx.commit(int(keeps[r]))
         rows = stream["resid"][r % stream["resid_pool"], :16]
@@ -111,6 +121,7 @@ def test_muse_slab_stress_wraparound(H, muse):
             assert st["position"] == pair.sess.pos and st["error"] == 0
             pair.check_ring(max_rows=32)
     assert pair.sess.pos == 16384 + int(keeps.sum())
+    assert checked == 7
     pair.close()
 
 
