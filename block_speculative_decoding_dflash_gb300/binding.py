@@ -85,6 +85,10 @@ _sig("dflash_ingest_context", ctypes.c_int, _vp, _vp, _i64, _i64, _i32)
 _sig("dflash_set_anchor", ctypes.c_int, _vp, _i32)
 _sig("dflash_draft_block", ctypes.c_int, _vp, _i32, _i64, _i32, _vp)
 _sig("dflash_sync_round", ctypes.c_int, _vp, _vp, _vp)
+_sig("dflash_verify_sampled", ctypes.c_int, _vp, _vp, _i32, _vp, _vp, ctypes.c_float, ctypes.c_float,
+     _vp, _vp, _vp)
+_sig("dflash_short_conv_block", ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp)
+_sig("dflash_short_conv_rollback", ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp)
 _sig("dflash_verify_accept", ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp)
 _sig("dflash_append_block", ctypes.c_int, _vp, _vp, _i32)
 _sig("dflash_commit", ctypes.c_int, _vp, _i32)
@@ -307,6 +311,14 @@ class DFlashContext:
         self._prep()
         self._check(lib.dflash_draft_block(self.h, anchor, anchor_pos, block, _ptr(draft_ids)))
 
+    def verify_sampled(self, logits, block, draft_ids, uniforms, temperature, tokens, n,
+                       softcap=None, p_draft=None):
+        self._prep()
+        cap = self.cfg.get("softcap", 0.0) if softcap is None else softcap
+        self._check(lib.dflash_verify_sampled(self.h, _ptr(logits), block, _ptr(draft_ids), _ptr(uniforms),
+                                              float(temperature), float(cap), _ptr(tokens), _ptr(n),
+                                              _ptr(p_draft) if p_draft is not None else None))
+
     def sync_round(self, block):
         """Waits for the stream; returns (tokens[:n], n) of the last verify."""
         tok = np.zeros(block, dtype=np.int32)
@@ -445,3 +457,25 @@ class DFlashContext:
             self.close()
         except Exception:
             pass
+
+
+def short_conv_block(state, bx, w, layers, lcache, channels, block, dtype, y, state_after=None,
+                     stream=None):
+    """dflash_short_conv_block on the current torch stream (or `stream`)."""
+    st = (stream or torch.cuda.current_stream()).cuda_stream
+    rc = lib.dflash_short_conv_block(_ptr(state) if state is not None else None, _ptr(bx), _ptr(w), layers,
+                                     lcache, channels, block, BF16 if dtype == "bf16" else F32, _ptr(y),
+                                     _ptr(state_after) if state_after is not None else None, st)
+    if rc:
+        raise DFlashError(rc, last_error(None))
+
+
+def short_conv_rollback(prev_state, bx, n_dev, layers, lcache, channels, block, dtype, state_out,
+                        stream=None):
+    """dflash_short_conv_rollback on the current torch stream (or `stream`)."""
+    st = (stream or torch.cuda.current_stream()).cuda_stream
+    rc = lib.dflash_short_conv_rollback(_ptr(prev_state) if prev_state is not None else None, _ptr(bx),
+                                        _ptr(n_dev), layers, lcache, channels, block,
+                                        BF16 if dtype == "bf16" else F32, _ptr(state_out), st)
+    if rc:
+        raise DFlashError(rc, last_error(None))

@@ -171,6 +171,10 @@ struct dflash_ctx {
   float* maxv = nullptr;
   int* backbone_ids = nullptr;
   float* zlog = nullptr;
+  int* samp_acc = nullptr;                     // sampled verify: per-row accept, bonus candidate,
+  int* samp_cand = nullptr;                    // p(d), ticket
+  float* samp_pd = nullptr;
+  unsigned* samp_ctr = nullptr;
 
   bool has_context = false;
   int last_draft_block = 0;
@@ -740,7 +744,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
       (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64,
-      (size_t)cfg->n_layers * sizeof(void*)};
+      (size_t)cfg->n_layers * sizeof(void*), R * 4, R * 4, R * 4, 64};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -785,6 +789,10 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->tc_lm_pi = carve<int>(cur, sizes[si++]);
   c->tc_done = carve<unsigned>(cur, sizes[si++]);
   c->kgain_dev = carve<const void*>(cur, sizes[si++]);
+  c->samp_acc = carve<int>(cur, sizes[si++]);
+  c->samp_cand = carve<int>(cur, sizes[si++]);
+  c->samp_pd = carve<float>(cur, sizes[si++]);
+  c->samp_ctr = carve<unsigned>(cur, sizes[si++]);
 
   std::vector<const void*> kg(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) kg[l] = c->layers[(size_t)l * DFLASH_LAYER_TENSORS + 5];
@@ -949,6 +957,29 @@ int dflash_verify_accept(dflash_ctx* c, const void* target_logits, int32_t block
   v.rs = c->rs; v.part_v = c->vf_pv; v.part_i = c->vf_pi; v.counter = c->counters + 1;
   v.chunks = c->vf_chunks;
   CK(c->err, launch_verify(c->dt, v, c->stream));
+  c->last_verify_block = block;
+  c->last_tokens = tokens;
+  c->last_n = n;
+  c->last_tokens_block = block;
+  return DFLASH_OK;
+}
+
+int dflash_verify_sampled(dflash_ctx* c, const void* target_logits, int32_t block,
+                          const int32_t* draft_ids, const float* uniforms, float temperature,
+                          float softcap, int32_t* tokens, int32_t* n, float* p_draft) {
+  if (!c) return DFLASH_EINVAL;
+  if (!target_logits || !draft_ids || !uniforms || !tokens || !n)
+    return fail(c->err, DFLASH_EINVAL, "a sampled-verify pointer is NULL");
+  if (block < 2 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !(softcap >= 0.f) || !std::isfinite(softcap))
+    return fail(c->err, DFLASH_EINVAL, "temperature must be > 0 and softcap >= 0, both finite");
+  SampledVerifyArgs a{};
+  a.L = target_logits; a.B = block; a.V = c->V; a.d = draft_ids; a.u = uniforms;
+  a.temperature = temperature; a.softcap = softcap; a.tokens = tokens; a.n = n; a.rs = c->rs;
+  a.acc = c->samp_acc; a.cand = c->samp_cand; a.pd = p_draft ? p_draft : c->samp_pd;
+  a.counter = c->samp_ctr;
+  CK(c->err, launch_verify_sampled(c->dt, a, c->stream));
   c->last_verify_block = block;
   c->last_tokens = tokens;
   c->last_n = n;
@@ -1305,6 +1336,55 @@ int dflash_synth_target(dflash_ctx* c, const void* logit_pool, const void* plant
   a.block_max = block_max; a.block = block; a.V = c->V; a.kin = c->kin;
   a.d = draft_ids; a.logits_out = logits_out; a.resid_out = resid_out; a.rs = c->rs;
   CK(c->err, launch_synth_target(c->dt, a, c->stream));
+  return DFLASH_OK;
+}
+
+// ---- LFM2 short convolution ----------------------------------------------------------
+namespace {
+int short_conv_check(int32_t layers, int32_t lcache, int32_t channels, int32_t block, int32_t dtype) {
+  if (layers < 1 || channels < 1 || block < 1 || dtype < 0 || dtype > 1) {
+    g_create_err = "short conv: dimensions must be positive and dtype DFLASH_F32 or DFLASH_BF16";
+    return DFLASH_EINVAL;
+  }
+  if (lcache < 2 || lcache > kShortConvMaxL) {
+    g_create_err = "short conv: lcache outside [2, 16]";
+    return DFLASH_ERANGE;
+  }
+  if ((int64_t)layers * channels * (block > lcache ? block : lcache) > kI32Max) {
+    g_create_err = "short conv: a dimension product would wrap an int32";
+    return DFLASH_EINVAL;
+  }
+  return DFLASH_OK;
+}
+}  // namespace
+
+int dflash_short_conv_block(const void* state, const void* bx, const void* w, int32_t layers,
+                            int32_t lcache, int32_t channels, int32_t block, int32_t dtype, void* y,
+                            void* state_after, void* stream) {
+  int rc = short_conv_check(layers, lcache, channels, block, dtype);
+  if (rc) return rc;
+  if (!bx || !w || !y) {
+    g_create_err = "short conv: bx, w and y must not be NULL";
+    return DFLASH_EINVAL;
+  }
+  cudaError_t e = launch_short_conv(dtype, state, bx, w, layers, lcache, channels, block, y, state_after,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(g_create_err, e, "short conv");
+  return DFLASH_OK;
+}
+
+int dflash_short_conv_rollback(const void* prev_state, const void* bx, const int32_t* n_dev,
+                               int32_t layers, int32_t lcache, int32_t channels, int32_t block,
+                               int32_t dtype, void* state_out, void* stream) {
+  int rc = short_conv_check(layers, lcache, channels, block, dtype);
+  if (rc) return rc;
+  if (!bx || !n_dev || !state_out) {
+    g_create_err = "short conv rollback: bx, n_dev and state_out must not be NULL";
+    return DFLASH_EINVAL;
+  }
+  cudaError_t e = launch_short_conv_rollback(dtype, prev_state, bx, n_dev, layers, lcache, channels, block,
+                                             state_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(g_create_err, e, "short conv rollback");
   return DFLASH_OK;
 }
 

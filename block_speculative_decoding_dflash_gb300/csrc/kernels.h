@@ -218,6 +218,27 @@ cudaError_t launch_ring_gather(int dtype, const void* ring_k, const void* ring_v
                                long long pos0, int count, void* k_out,
                                void* v_out, cudaStream_t st);
 
+// Speculative-sampling verify at temperature T > 0 (one CTA per row).
+struct SampledVerifyArgs {
+  const void* L;               // [B, V]
+  int B, V;
+  const int* d;                // [B-1]
+  const float* u;              // [B] uniforms in [0, 1): B-1 accept tests, the bonus draw
+  float temperature, softcap;
+  int* tokens;                 // [B]
+  int* n;                      // [1]
+  RoundState* rs;              // may be NULL
+  int* acc; int* cand;         // scratch [B]
+  float* pd;                   // [B] p_i(d_{i+1}) (0 for the last row)
+  unsigned* counter;           // zero between launches
+};
+cudaError_t launch_verify_sampled(int dtype, const SampledVerifyArgs& a, cudaStream_t st);
+constexpr int kShortConvMaxL = 16;
+cudaError_t launch_short_conv(int dtype, const void* state, const void* bx, const void* w, int layers,
+                              int lc, int C, int block, void* y, void* state_after, cudaStream_t st);
+cudaError_t launch_short_conv_rollback(int dtype, const void* prev, const void* bx, const int* n_dev,
+                                       int layers, int lc, int C, int block, void* out, cudaStream_t st);
+
 struct MarkovArgs {
   const void* w1; const void* w2;  // [V, r], [r, V]
   int V, r;

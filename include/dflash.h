@@ -250,6 +250,27 @@ int dflash_commit(dflash_ctx* ctx, int32_t keep);
  * argmax per round]. Syncs. ESTATE before any verify or while capturing. */
 int dflash_sync_round(dflash_ctx* ctx, int32_t* tokens_host, int32_t* n_host);
 
+/* Speculative-sampling verify at temperature T > 0, the counterpart of
+ * dflash_verify_accept for sampled decoding ["Load Meta's
+ * Muse-Glimmer-30B-assistant DFlash head", "Measured": the sampled-acceptance
+ * run at T = 1]. The drafter proposes its argmaxes, so its proposal
+ * distribution is a point mass on d_{i+1} and the speculative-sampling rule
+ * min(1, p/q) accepts d_{i+1} iff uniforms[i] < p_i(d_{i+1}), with p_i =
+ * softmax(c * tanh(target_logits[i] / c) / temperature) (c = softcap, 0 =
+ * no cap). a = the accepted prefix; the bonus token is drawn by inverse CDF
+ * in vocabulary order with uniforms[block - 1], from p_a without d_{a+1}
+ * after a rejection (the residual max(p - q, 0)), from p_{block-1} after a
+ * full accept. The emitted tokens then follow the target distribution
+ * exactly. Writes tokens [block] = d_1..d_a, bonus, then -1 padding, n [1] =
+ * a + 1 and, when p_draft is not NULL, p_draft [block] = p_i(d_{i+1}) (0 for
+ * the last row). uniforms [block] fp32 in [0, 1) are caller-drawn (device).
+ * Keeps n, a and the bonus on the device for dflash_commit like the greedy
+ * verify. Top-k / top-p filtering is not applied. ERANGE unless 2 <= block
+ * <= max_block; EINVAL for a NULL pointer, temperature <= 0 or softcap < 0. */
+int dflash_verify_sampled(dflash_ctx* ctx, const void* target_logits, int32_t block,
+                          const int32_t* draft_ids, const float* uniforms, float temperature,
+                          float softcap, int32_t* tokens, int32_t* n, float* p_draft);
+
 /* One whole round: draft_block (device anchor), verify_accept, append_block,
  * commit(-1). */
 int dflash_round(dflash_ctx* ctx, const void* target_logits, const void* resid,
@@ -409,6 +430,35 @@ int dflash_synth_target(dflash_ctx* ctx, const void* logit_pool,
                         int32_t block_max, int32_t block,
                         const int32_t* draft_ids, void* logits_out,
                         void* resid_out);
+
+/* ---- LFM2 short convolution and its rollback ---------------------------------- */
+
+/* The causal depthwise short convolution of an LFM2 conv layer over a verify
+ * block ["LFM2 / LFM2.5 DSpark drafter on the DFlash loop", "Short-conv
+ * rollback"], for `layers` layers at once: with x = concat(state [lcache-1,
+ * C] (NULL: zeros), bx [block, C]) per layer, y[t, c] = sum_k w[c, k] *
+ * x[t + k, c] for t < block (fp32 accumulation, stored in dtype), and
+ * state_after (may be NULL, may alias state) = the last lcache - 1 rows of x.
+ * Layouts: state/state_after [layers, lcache-1, C], bx and y [layers, block,
+ * C], w [layers, C, lcache]; all device memory, dense. Enqueued on `stream`
+ * (a cudaStream_t; NULL: the legacy default stream); no context, no
+ * allocation. EINVAL for NULL bx/w/y or a bad size or dtype, ERANGE for
+ * lcache outside [2, 16]; the reason is in dflash_last_error(NULL). */
+int dflash_short_conv_block(const void* state, const void* bx, const void* w, int32_t layers,
+                            int32_t lcache, int32_t channels, int32_t block, int32_t dtype, void* y,
+                            void* state_after, void* stream);
+
+/* Partial-accept rollback of short-conv states (same page and section): a
+ * conv state cannot be trimmed like a KV cache, so the committed state is
+ * recomputed as the last lcache - 1 rows of concat(prev_state (NULL: zeros),
+ * bx[:n]), n = *n_dev read on the device (the verify's n = a + 1, clamped to
+ * [0, block]), so a captured round needs no host read. prev_state is the
+ * state before the block, bx the block's gated conv input; state_out [layers,
+ * lcache-1, C] may alias prev_state. Bit-exact copies. Same conventions and
+ * errors as dflash_short_conv_block. */
+int dflash_short_conv_rollback(const void* prev_state, const void* bx, const int32_t* n_dev,
+                               int32_t layers, int32_t lcache, int32_t channels, int32_t block,
+                               int32_t dtype, void* state_out, void* stream);
 
 /* ---- ring KV cache (usable standalone) ---------------------------------------- */
 

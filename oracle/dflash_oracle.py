@@ -46,6 +46,11 @@ Readings of points the pages leave open:
  R12 Rounding points (storage type): GEMM outputs, norm outputs, the fused
      q/k-norm + RoPE output, attention output, residual sums, the SwiGLU
      product; logits stay fp32.
+ R13 Sampled verify (T > 0): the drafter proposes its argmaxes, so its
+     proposal distribution is a point mass and the standard speculative-
+     sampling rule accepts d with probability p(d); the bonus after a
+     rejection comes from p with d removed; uniforms are inputs and the
+     inverse CDF runs in vocabulary order.
 
 Parity status: every function here has a named pin. The slack rule, the ring
 restore, accept = prefix + 1, the mask, attention, RoPE, RMSNorm, linear,
@@ -76,7 +81,8 @@ __all__ = [
     "visible_mask", "attention", "linear", "silu", "softcap", "argmax_lowest",
     "window_drop", "context_kv", "block_tokens", "drafter_layer",
     "lm_head_argmax", "draft_block", "markov_chain",
-    "verify_accept", "RingModel", "OracleSession", "stats_ratios",
+    "verify_accept", "sampled_probs", "verify_sampled", "short_conv_block",
+    "short_conv_rollback", "RingModel", "OracleSession", "stats_ratios",
 ]
 
 
@@ -486,6 +492,77 @@ def verify_accept(target_logits: np.ndarray, draft_ids: np.ndarray):
         a += 1
     tokens = np.concatenate([np.asarray(draft_ids[:a], dtype=np.int64), t[a:a + 1]])
     return tokens, a + 1, t
+
+
+def sampled_probs(logits: np.ndarray, temperature: float, cap: float) -> np.ndarray:
+    """Target token probabilities of one verify row at temperature T > 0 on
+    softcapped logits: softmax(c * tanh(L / c) / T) (reading R10 for the cap,
+    c = 0 meaning none), formed in fp64 from the fp32 capped logits.
+
+    "Load Meta's Muse-Glimmer-30B-assistant DFlash head", "Measured": the
+    sampled-acceptance run at T = 1; "How": the head inherits the tanh cap.
+    """
+    z = softcap(np.asarray(logits, dtype=np.float32), cap).astype(np.float64) / temperature
+    z = z - z.max()
+    e = np.exp(z)
+    return e / e.sum()
+
+
+def verify_sampled(target_logits: np.ndarray, draft_ids: np.ndarray, u: np.ndarray,
+                   temperature: float, cap: float):
+    """Speculative-sampling verify for a drafter whose proposals are its
+    argmaxes, i.e. whose proposal distribution q is a point mass on d_{i+1}
+    (reading R13). Row i accepts d_{i+1} with probability min(1, p_i(d)/q(d))
+    = p_i(d_{i+1}): accepted iff u[i] < p_i(d_{i+1}). a is the accepted
+    prefix. The bonus token is drawn by inverse CDF with u[block - 1] in
+    vocabulary order: after a rejection at row a from the residual
+    max(p_a - q, 0) renormalised (p_a with d_{a+1} removed), after a full
+    accept from p_{block-1}. Returns (tokens d_1..d_a + bonus, n = a + 1, a).
+    ``u`` holds block values in [0, 1): the random numbers are inputs.
+    """
+    b = target_logits.shape[0]
+    a = 0
+    while a < b - 1:
+        p = sampled_probs(target_logits[a], temperature, cap)
+        if u[a] < p[int(draft_ids[a])]:
+            a += 1
+        else:
+            break
+    p = sampled_probs(target_logits[a], temperature, cap)
+    if a < b - 1:
+        p = p.copy()
+        p[int(draft_ids[a])] = 0.0
+    c = np.cumsum(p)
+    t = u[b - 1] * c[-1]
+    bonus = int(np.searchsorted(c, t, side="right"))
+    bonus = min(bonus, int(np.nonzero(p > 0)[0][-1]))
+    tokens = np.concatenate([np.asarray(draft_ids[:a], dtype=np.int64), [bonus]])
+    return tokens, a + 1, a
+
+
+def short_conv_block(state, bx, w):
+    """LFM2 short convolution over a block (DSpark page, "Short-conv
+    rollback"): a causal depthwise convolution of kernel length L over the
+    gated input Bx. With the L - 1 rows of state before the block (zeros when
+    there are none), y[t, c] = sum_k w[c, k] * x[t + k, c] over x = concat(
+    state, bx), t < block; the state after the block is the last L - 1 rows of
+    x. state [L-1, C] or None, bx [block, C], w [C, L]."""
+    lc = w.shape[1]
+    if state is None:
+        state = np.zeros((lc - 1, bx.shape[1]))
+    x = np.concatenate([state, bx], axis=0)
+    y = np.stack([np.sum(w * x[t:t + lc].T, axis=1) for t in range(bx.shape[0])])
+    return y, x[x.shape[0] - (lc - 1):]
+
+
+def short_conv_rollback(prev_state, bx, n, lcache):
+    """Partial-accept rollback of a short-conv state (DSpark page, "Short-conv
+    rollback"): a conv state cannot be trimmed, so the committed state is
+    recomputed as the last L - 1 rows of concat(prev_state or zeros, bx[:n])."""
+    if prev_state is None:
+        prev_state = np.zeros((lcache - 1, bx.shape[1]))
+    x = np.concatenate([prev_state, bx[:n]], axis=0)
+    return x[x.shape[0] - (lcache - 1):]
 
 
 def stats_ratios(rounds: int, proposed: int, accepted: int) -> dict:
