@@ -589,20 +589,21 @@ def cpu_baseline(job, n_rounds, mix):
     ts = job.ts
     from block_speculative_decoding_dflash_gb300 import synth
     per_width, r = {}, 0
-    for w in sorted(mix):
+    for bw in sorted(mix):
         t0 = time.time()
         for _ in range(n_rounds):
-            d = sess.draft(w)
-            L = synth.planted_logits(ts, r, w, d["draft_ids"])
+            d = sess.draft(bw)
+            L = synth.planted_logits(ts, r, bw, d["draft_ids"])
             tokens, n, _ = sess.verify(O.as_f64(L, "bf16"), d["draft_ids"])
-            sess.append_and_trim(O.as_f64(synth.resid_rows(ts, r, w), "bf16"), n)
-            sess.commit(n, int(tokens[-1]), w, n - 1)
+            sess.append_and_trim(O.as_f64(synth.resid_rows(ts, r, bw), "bf16"), n)
+            sess.commit(n, int(tokens[-1]), bw, n - 1)
             r += 1
-        per_width[w] = (time.time() - t0) / n_rounds
-    t_round = sum(mix[w] * per_width[w] for w in mix)
+        per_width[bw] = (time.time() - t0) / n_rounds
+    t_round = sum(mix[bw] * per_width[bw] for bw in mix)
     job_s = t_ingest + job.args.rounds * t_round
     cores = len(os.sched_getaffinity(0))
-    widths = ", ".join(f"width {w}: {per_width[w]:.2f} s/round x {mix[w]:.2f} of the rounds" for w in sorted(mix))
+    widths = ", ".join(f"width {bw}: {per_width[bw]:.2f} s/round x {mix[bw]:.2f} of the rounds"
+                       for bw in sorted(mix))
     return {"value": job.args.rounds / job_s, "unit": "rounds/s", "cores": cores, "kind": "oracle",
             "sample": f"ingest of 2048 context rows ({t_ingest:.2f} s) + {n_rounds} rounds at each width "
                       f"({widths}), weighted by the GPU job's width mix and extrapolated to the "

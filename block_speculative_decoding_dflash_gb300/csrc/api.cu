@@ -171,6 +171,10 @@ struct dflash_ctx {
   float* maxv = nullptr;
   int* backbone_ids = nullptr;
   float* zlog = nullptr;
+  float* acc = nullptr;                        // [R][H] fp32 sums of the kEpiRed GEMMs, zero between uses
+  float* qkv_acc = nullptr;                    // [R][qkv_n] fp32 sums of the QKV GEMM, zero between uses
+  float* gu_acc = nullptr;                     // [R][2 I] fp32 gate / up sums, zero between uses
+  float* kv_acc = nullptr;                     // [R][L 2 kvdim] fp32 sums of the append's K/V GEMM
   int* samp_acc = nullptr;                     // sampled verify: per-row accept, bonus candidate,
   int* samp_cand = nullptr;                    // p(d), ticket
   float* samp_pd = nullptr;
@@ -201,7 +205,7 @@ struct dflash_ctx {
   float* tc_part = nullptr;
   unsigned* tc_tiles = nullptr;
   int* tc_err = nullptr;
-  float* tc_lm_pv = nullptr;
+  unsigned long long* tc_best = nullptr;       // lm_head: packed per-row argmax keys
   int* tc_lm_pi = nullptr;
   unsigned* tc_done = nullptr;
   const void** kgain_dev = nullptr;            // [n_layers] k_norm gain pointers
@@ -340,27 +344,35 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
                                rows, rope, st));
   const bool tc = c->use_tc && rows <= 32 && cn == c->app_c;
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->H, c->kin, kEpiStore);
+    // encoder.fc adds its fp32 sums into c->acc; hidden_norm rounds them
+    // (f = rnd(acc)) and normalises
+    TcGemmArgs t = tc_args(c, rows, c->H, c->kin, kEpiRed);
     tc_segments(t, {{&c->fc_map, c->H}});
     if (!tc_encode_map(&t.b_map, resid, c->kin, rows, (uint64_t)c->kin * 2, 64, bn_of(rows)))
       return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the residual rows");
-    t.y = f; t.ldy = c->H;
+    t.acc = c->acc; t.ldacc = c->H;
     if (use_dev) t.trace = ktrace_slot(c, "append.fc", 4);
     CK(c->err, tc_run(c, t));
+    CK(c->err, launch_resid_rmsnorm(nullptr, 0, c->acc, c->H, c->hidden_norm, cn, c->H, rows, c->H,
+                                    c->cfg.rms_eps, st,
+                                    use_dev ? ktrace_slot(c, "append.hidden_norm") : KTrace{nullptr, 0}));
   } else {
     LinearArgs a = lin_args(resid, c->kin, f, c->H, rows, c->H, c->kin);
     a.w[0] = c->fc;
     CK(c->err, rows > 32 ? launch_linear_tiled(dt, a, st) : launch_linear_rows(dt, a, st));
+    CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st,
+                              use_dev ? ktrace_slot(c, "append.hidden_norm") : KTrace{nullptr, 0}));
   }
-  CK(c->err, launch_rmsnorm(dt, f, c->H, c->hidden_norm, cn, c->H, rows, c->H, c->cfg.rms_eps, st,
-                            use_dev ? ktrace_slot(c, "append.hidden_norm") : KTrace{nullptr, 0}));
   if (tc && c->hd == 128) {
-    // One GEMM per group of up to five layers over [Wk_l | Wv_l ...]; its
-    // epilogue norms, rotates and writes K and V straight into the ring.
+    // One GEMM per group of up to five layers over [Wk_l | Wv_l ...] adds its
+    // fp32 sums into c->kv_acc; one finishing kernel then norms, rotates and
+    // writes K and V of every layer into the ring.
     const int L = c->cfg.n_layers;
     for (int l0 = 0; l0 < L; l0 += kTcMaxSeg / 2) {
       const int nl = L - l0 < kTcMaxSeg / 2 ? L - l0 : kTcMaxSeg / 2;
-      TcGemmArgs t = tc_args(c, rows, nl * 2 * c->kvdim, c->H, kEpiKVRing);
+      TcGemmArgs t = tc_args(c, rows, nl * 2 * c->kvdim, c->H, kEpiRed);
+      t.acc = c->kv_acc + (size_t)l0 * 2 * c->kvdim;
+      t.ldacc = L * 2 * c->kvdim;
       t.nseg = 2 * nl;
       int tiles = 0;
       for (int j = 0; j < nl; ++j) {
@@ -386,6 +398,10 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
       if (use_dev) t.trace = ktrace_slot(c, "append.kv", 4);
       CK(c->err, tc_run(c, t));
     }
+    CK(c->err, launch_kv_acc_to_ring(c->kv_acc, L * 2 * c->kvdim, rows, L, c->nkv, c->kgain_dev,
+                                     c->cfg.rms_eps, rope, c->cfg.rope_neox, c->ring->k, c->ring->v,
+                                     c->ring->cap, c->ring->append_only, c->ring->st, st,
+                                     use_dev ? ktrace_slot(c, "append.kv_ring") : KTrace{nullptr, 0}));
     return DFLASH_OK;
   }
   for (int l = 0; l < c->cfg.n_layers; ++l) {
@@ -479,19 +495,30 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   cudaStream_t st = c->stream;
   const float eps = c->cfg.rms_eps;
   const std::string ln = "L" + std::to_string(l) + ".";
-  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st,
-                            ktrace_slot(c, ln + "in_norm")));
   const bool tc = c->use_tc && rows <= 32;
+  // The residual GEMMs (O, down) of the tensor-core path add their fp32 sums
+  // into c->acc and leave the residual add to the RMSNorm that follows them:
+  // x = rnd(x + rnd(acc)), then the norm of x.
+  if (tc && l > 0)
+    CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H,
+                                    eps, st, ktrace_slot(c, ln + "in_norm")));
+  else
+    CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st,
+                              ktrace_slot(c, ln + "in_norm")));
   const int bi = bn_index(rows);
   // q/k head norm + RoPE: applied by the tensor-core attention kernels as they
   // load q and the block's k rows (the QKV GEMM then just stores, so its
   // split tiles finish sooner), else by their own kernel
   const bool attn_norm = tc && attention_mma_ok(dt, c->hd);
+  // With the tensor-core attention the QKV GEMM adds its fp32 sums into
+  // c->qkv_acc and the attention rounds them as it loads q, k and v.
+  const bool qkv_red = tc && attn_norm;
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, kEpiStore);
+    TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, qkv_red ? kEpiRed : kEpiStore);
     tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
     t.b_map = c->xn_map[bi];
     t.y = c->qkv; t.ldy = c->qkv_n;
+    t.acc = c->qkv_acc; t.ldacc = c->qkv_n;
     t.trace = ktrace_slot(c, ln + "qkv", 4);
     CK(c->err, tc_run(c, t));
   } else {
@@ -514,6 +541,14 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.kb = static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz;
   at.vb = static_cast<char*>(c->qkv) + (size_t)(c->qdim + c->kvdim) * c->esz;
   at.ldkv = c->qkv_n;
+  if (qkv_red) {
+    at.q = c->qkv_acc;
+    at.kb = c->qkv_acc + c->qdim;
+    at.vb = c->qkv_acc + c->qdim + c->kvdim;
+    at.qkv_f32 = 1;
+    at.zero_acc = c->qkv_acc;
+    at.zero_n = rows * c->qkv_n;
+  }
   const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
   at.ring_k = static_cast<char*>(c->ring->k) + lay;
   at.ring_v = static_cast<char*>(c->ring->v) + lay;
@@ -532,31 +567,37 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   }
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiResid);
+    TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiRed);
     tc_segments(t, {{&c->lmaps[l].wo, c->H}});
     t.b_map = c->attn_map[bi];
-    t.y = c->x; t.ldy = c->H; t.r = c->x; t.ldr = c->H;
+    t.acc = c->acc; t.ldacc = c->H;
     t.trace = ktrace_slot(c, ln + "o", 4);
     CK(c->err, tc_run(c, t));
+    CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H,
+                                    eps, st, ktrace_slot(c, ln + "post_norm")));
   } else {
     LinearArgs o = lin_args(c->attn, c->qdim, c->x, c->H, rows, c->H, c->qdim);
     o.w[0] = LW(c, l, kWo); o.epi = kEpiResid; o.r = c->x; o.ldr = c->H;
     CK(c->err, launch_linear_rows(dt, o, st));
+    CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st,
+                              ktrace_slot(c, ln + "post_norm")));
   }
-  CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kPostNorm), c->xn, c->H, rows, c->H, eps, st,
-                            ktrace_slot(c, ln + "post_norm")));
   if (tc) {
-    TcGemmArgs t = tc_args(c, rows, c->I, c->H, kEpiSwiglu);
+    // gate and up add their fp32 sums into c->gu_acc; the SwiGLU finish
+    // rounds them and writes the down GEMM's operand
+    TcGemmArgs t = tc_args(c, rows, c->I, c->H, kEpiRedPair);
     tc_segments(t, {{&c->lmaps[l].wg, c->I}});
     t.a2_map = c->lmaps[l].wu;
     t.b_map = c->xn_map[bi];
-    t.y = c->sbuf; t.ldy = c->I;
+    t.acc = c->gu_acc; t.ldacc = 2 * c->I;
     t.trace = ktrace_slot(c, ln + "gate_up", 4);
     CK(c->err, tc_run(c, t));
-    TcGemmArgs d = tc_args(c, rows, c->H, c->I, kEpiResid);
+    CK(c->err, launch_swiglu_finish(c->gu_acc, 2 * c->I, c->sbuf, c->I, rows, c->I, st,
+                                    ktrace_slot(c, ln + "swiglu")));
+    TcGemmArgs d = tc_args(c, rows, c->H, c->I, kEpiRed);
     tc_segments(d, {{&c->lmaps[l].wd, c->H}});
     d.b_map = c->sbuf_map[bi];
-    d.y = c->x; d.ldy = c->H; d.r = c->x; d.ldr = c->H;
+    d.acc = c->acc; d.ldacc = c->H;
     d.trace = ktrace_slot(c, ln + "down", 4);
     CK(c->err, tc_run(c, d));
   } else {
@@ -740,11 +781,12 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       (size_t)c->ing_rows * c->H * E, (size_t)c->ing_rows * c->H * E,
       (size_t)c->ing_rows * 2 * c->kvdim * E * cfg->n_layers, (size_t)c->ing_rows * c->half * sizeof(float2),
       (size_t)c->lm_grid * R * 4, (size_t)c->lm_grid * R * 4, R * c->vf_chunks * 4,
-      R * c->vf_chunks * 4, (size_t)c->mk_grid * 4, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
+      R * c->vf_chunks * 4, R * 8, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
       (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64,
-      (size_t)cfg->n_layers * sizeof(void*), R * 4, R * 4, R * 4, 64};
+      (size_t)cfg->n_layers * sizeof(void*), R * 4, R * 4, R * 4, 64, R * c->H * 4, R * c->qkv_n * 4, R * 2 * c->I * 4,
+      R * (size_t)cfg->n_layers * 2 * c->kvdim * 4};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -785,7 +827,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->tc_part = carve<float>(cur, sizes[si++]);
   c->tc_tiles = carve<unsigned>(cur, sizes[si++]);
   c->tc_err = carve<int>(cur, sizes[si++]);
-  c->tc_lm_pv = carve<float>(cur, sizes[si++]);
+  c->tc_best = carve<unsigned long long>(cur, sizes[si++]);
   c->tc_lm_pi = carve<int>(cur, sizes[si++]);
   c->tc_done = carve<unsigned>(cur, sizes[si++]);
   c->kgain_dev = carve<const void*>(cur, sizes[si++]);
@@ -793,6 +835,10 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->samp_cand = carve<int>(cur, sizes[si++]);
   c->samp_pd = carve<float>(cur, sizes[si++]);
   c->samp_ctr = carve<unsigned>(cur, sizes[si++]);
+  c->acc = carve<float>(cur, sizes[si++]);
+  c->qkv_acc = carve<float>(cur, sizes[si++]);
+  c->gu_acc = carve<float>(cur, sizes[si++]);
+  c->kv_acc = carve<float>(cur, sizes[si++]);
 
   std::vector<const void*> kg(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) kg[l] = c->layers[(size_t)l * DFLASH_LAYER_TENSORS + 5];
@@ -874,7 +920,7 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
   mk.rs = c->rs; mk.anchor_host = -1;
   mk.z = c->cfg.markov_add ? c->zlog : nullptr; mk.ldz = c->V;
   mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
-  mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2;
+  mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2;
   mk.grid = c->mk_grid;
   return launch_markov_chain(c->dt, mk, c->stream);
 }
@@ -908,8 +954,12 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     int rc = layer_forward(c, l, rows);
     if (rc) return rc;
   }
-  CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
-                            c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
+  if (c->use_tc && rows <= 32)   // the last down GEMM's sums are still in c->acc
+    CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, c->final_norm, c->xf, c->H, rows, c->H,
+                                    c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
+  else
+    CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
+                              c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
   LmHeadArgs lm{};
   lm.x = static_cast<char*>(c->xf) + (size_t)read0 * c->H * c->esz;
   lm.ldx = c->H;
@@ -930,7 +980,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     t.b_map = c->xf_map[read0][bn_index(R)];
     t.softcap = c->cfg.softcap;
     t.ids = lm.ids; t.ids2 = lm.ids2; t.maxv = lm.maxv;
-    t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
+    t.best_key = c->tc_best; t.done_ctr = c->tc_done; t.whole_tiles = t.M > 8;
     t.trace = ktrace_slot(c, "lm_head", 4);
     CK(c->err, tc_run(c, t));
   } else {
@@ -1090,7 +1140,7 @@ int dflash_lm_head_argmax(dflash_ctx* c, const void* x, int32_t rows, int32_t* i
       return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
     t.softcap = c->cfg.softcap;
     t.ids = ids; t.ids2 = nullptr; t.maxv = maxv;
-    t.part_v = c->tc_lm_pv; t.part_i = c->tc_lm_pi; t.done_ctr = c->tc_done;
+    t.best_key = c->tc_best; t.done_ctr = c->tc_done; t.whole_tiles = t.M > 8;
     CK(c->err, tc_run(c, t));
   } else {
     LmHeadArgs lm{};
@@ -1114,7 +1164,7 @@ int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const floa
   mk.w1 = c->w1; mk.w2 = c->w2; mk.V = c->V; mk.r = c->cfg.markov_rank;
   mk.rs = c->rs; mk.anchor_host = anchor; mk.z = z; mk.ldz = c->V; mk.gamma = gamma;
   mk.out = out; mk.out2 = nullptr;
-  mk.part_v = c->mk_pv; mk.part_i = c->mk_pi; mk.counter = c->counters + 2; mk.grid = c->mk_grid;
+  mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2; mk.grid = c->mk_grid;
   CK(c->err, launch_markov_chain(c->dt, mk, c->stream));
   return DFLASH_OK;
 }

@@ -246,13 +246,29 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
 }
 
 // ---- Markov chain step ---------------------------------------------------------------------
-constexpr int kMkThreads = 64;
-constexpr int kMkCols = kMkThreads * 8;
+// One launch per chain step (step j needs step j-1's argmax). A CTA takes
+// kMkCols vocabulary columns: its 256 threads are 64 groups of 8 columns x 4
+// quarters of the rank, so each thread issues r/4 independent 16-byte loads
+// of W2 (33.6 MB for the DSpark head, resident in L2 after the first step),
+// then the quarters are summed in shared memory. Each CTA folds its best
+// (value, column) into one 64-bit key per step with an atomic maximum (the
+// order-preserving value bits above the inverted column); the last CTA
+// decodes it into out[j] and clears it.
+constexpr int kMkThreads = 256;
+constexpr int kMkQuarters = 4;
+constexpr int kMkCols = (kMkThreads / kMkQuarters) * 8;
+
+__device__ __forceinline__ unsigned long long mk_key(float v, int i) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, int j) {
   pdl_enter();
   extern __shared__ float w1s[];               // [r]
+  __shared__ float part[kMkQuarters][kMkThreads / kMkQuarters][8];
   __shared__ float sv[kMkThreads / 32];
   __shared__ int si[kMkThreads / 32];
   int prev;
@@ -262,22 +278,31 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
   const T* w1 = reinterpret_cast<const T*>(a.w1) + (size_t)prev * a.r;
   for (int q = threadIdx.x; q < a.r; q += blockDim.x) w1s[q] = to_f(w1[q]);
   __syncthreads();
-  const int c = (blockIdx.x * kMkThreads + threadIdx.x) * 8;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
+  const int grp = threadIdx.x % (kMkThreads / kMkQuarters), qt = threadIdx.x / (kMkThreads / kMkQuarters);
+  const int c = blockIdx.x * kMkCols + grp * 8;
+  const int rq = (a.r + kMkQuarters - 1) / kMkQuarters;
+  const int q0 = qt * rq, q1 = min(a.r, q0 + rq);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (c < a.V) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const T* w2 = reinterpret_cast<const T*>(a.w2) + c;
-    for (int q = 0; q < a.r; ++q) {
+#pragma unroll 8
+    for (int q = q0; q < q1; ++q) {
       float wv[8];
       load8(w2 + (size_t)q * a.V, wv);
       const float s = w1s[q];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = fmaf(s, wv[e], acc[e]);
     }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[qt][grp][e] = acc[e];
+  __syncthreads();
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if (qt == 0 && c < a.V) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float z = acc[e];
+      float z = (part[0][grp][e] + part[1][grp][e]) + (part[2][grp][e] + part[3][grp][e]);
       if (a.z) z = a.z[(size_t)j * a.ldz + c + e] + z;
       if (better(z, c + e, bv, bi)) { bv = z; bi = c + e; }
     }
@@ -290,22 +315,14 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
     bi = si[0];
     for (int w = 1; w < kMkThreads / 32; ++w)
       if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
-    a.part_v[blockIdx.x] = bv;
-    a.part_i[blockIdx.x] = bi;
+    atomicMax(a.key + j, mk_key(bv, bi));
   }
-  if (last_cta(a.counter, gridDim.x)) {
-    if (threadIdx.x == 0) {
-      float v = -INFINITY;
-      int idx = 0x7fffffff;
-      for (int q = 0; q < a.grid; ++q) {
-        const float cv = __ldcg(a.part_v + q);
-        const int ci = __ldcg(a.part_i + q);
-        if (better(cv, ci, v, idx)) { v = cv; idx = ci; }
-      }
-      a.out[j] = idx;
-      if (a.out2) a.out2[j] = idx;
-      *a.counter = 0u;
-    }
+  if (last_cta(a.counter, gridDim.x) && threadIdx.x == 0) {
+    const unsigned long long key = atomicExch(a.key + j, 0ull);
+    const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+    a.out[j] = idx;
+    if (a.out2) a.out2[j] = idx;
+    *a.counter = 0u;
   }
 }
 

@@ -30,6 +30,18 @@ constexpr int kPad = 8;                    // bf16 elements of row padding (conf
 constexpr int kPartStride = kAttnPartStride;
 constexpr int kQChunk = 64;
 
+// 8 consecutive fp32 sums of a kEpiRed GEMM, rounded to bf16, into 16 bytes
+// of shared memory (zeros when !valid).
+__device__ __forceinline__ void f32x8_to_smem(void* dst, const float* src, bool valid) {
+  uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+    pk = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+  }
+  *reinterpret_cast<uint4*>(dst) = pk;
+}
+
 struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
   bf16 v[kKeys][kHd + kPad];
@@ -71,14 +83,15 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   const bf16* vb = reinterpret_cast<const bf16*>(a.vb);
   const bf16* qg = reinterpret_cast<const bf16*>(a.q);
 
+  const float* qf = reinterpret_cast<const float*>(a.q);
   auto load_q = [&](int q0) {
     for (int e = threadIdx.x; e < kQChunk * (kHd / 8); e += blockDim.x) {
       const int r = e >> 4, ch = e & 15;
       const int qi = q0 + r;
       const bool valid = qi < Qn;
-      const bf16* src = qg;
-      if (valid) src = qg + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
-      cp_async16(&S.q[r][ch * 8], src, valid);
+      const size_t off = valid ? (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8 : 0;
+      if (a.qkv_f32) f32x8_to_smem(&S.q[r][ch * 8], qf + off, valid);
+      else cp_async16(&S.q[r][ch * 8], qg + off, valid);
     }
   };
   if (j0 < nk) {
@@ -96,6 +109,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
         vs = rv + (size_t)slot * kHd + ch * 8;
       } else if (valid) {
         const size_t off = (size_t)(kj - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
+        if (a.qkv_f32) {
+          f32x8_to_smem(&S.k[j][ch * 8], reinterpret_cast<const float*>(a.kb) + off, true);
+          f32x8_to_smem(&S.v[j][ch * 8], reinterpret_cast<const float*>(a.vb) + off, true);
+          continue;
+        }
         ks = kb + off;
         vs = vb + off;
       }
@@ -273,6 +291,10 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
   if (item < a.nkv * Qn)
     attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
                       reinterpret_cast<bf16*>(a.out), a.ldo, lane);
+  // every attention CTA is done with the QKV GEMM's fp32 sums: clear them
+  if (a.zero_acc)
+    for (int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4; e < a.zero_n; e += gridDim.x * blockDim.x * 4)
+      *reinterpret_cast<float4*>(a.zero_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
 }
 
@@ -375,6 +397,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       vs = rv + (size_t)slot * kHd + ch * 8;
     } else if (valid) {
       const size_t off = (size_t)(kj - nctx) * ldkv + ch * 8;
+      if (a.qkv_f32) {
+        f32x8_to_smem(sm + kTcK + tc_sw128(j, ch * 8), reinterpret_cast<const float*>(a.kb) + g * kHd + off, true);
+        f32x8_to_smem(sm + kTcVs + j * kTcVsRow + ch * 16, reinterpret_cast<const float*>(a.vb) + g * kHd + off,
+                      true);
+        continue;
+      }
       ks = kb + off;
       vs = vb + off;
     }
@@ -386,8 +414,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   for (int e = threadIdx.x; e < (norm ? 1 : 2) * kTileQ * (kHd / 8); e += blockDim.x) {
     const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
     const bool valid = qr < Qn;
-    const bf16* src = valid ? qg + (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : qg;
-    cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), src, valid);
+    const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
+    if (a.qkv_f32)
+      f32x8_to_smem(sm + kTcQ + tc_sw128(r, ch * 8), reinterpret_cast<const float*>(a.q) + (size_t)g * G * kHd + off,
+                    valid);
+    else
+      cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
   }
   cp_async_wait_all();
   if (norm) {

@@ -34,6 +34,10 @@ struct LinearArgs {
 enum : int {
   kEpiArgmax = 3,   // tensor-core GEMM only: softcap + per-row argmax
   kEpiKVRing = 4,   // tensor-core GEMM only: K head-norm + RoPE / V, into ring slots
+  kEpiRed = 5,      // tensor-core GEMM only: fp32 sums added into acc (zeroed), no finish;
+                    // launch_resid_rmsnorm finishes them
+  kEpiRedPair = 6,  // as kEpiRed for the two weights of a SwiGLU (gate sums at acc[m][n],
+                    // up sums at acc[m][N + n]); launch_swiglu_finish finishes them
 };
 constexpr int kTcMaxSeg = 10;
 constexpr int kTileDepart = 4096;  // tiles per GEMM at most; departures follow arrivals
@@ -51,13 +55,15 @@ struct TcGemmArgs {
   int M, N, K, tiles, kchunks, epi;
   void* y; int ldy;                // output [M, N] (row stride ldy)
   const void* r; int ldr;          // residual of kEpiResid (may alias y)
+  float* acc; int ldacc;           // kEpiRed: [M][ldacc] fp32, zero before the launch
   float* partials;                 // [grid][2][NV*BN][128] fp32 split-tile partials
   unsigned* tile_ctr;              // [kTileDepart + tiles]: arrivals, then departures per
                                    // split tile; zero between launches
   int* err;                        // bounded-wait timeouts are reported here
   float softcap;                   // kEpiArgmax
   int* ids; int* ids2; float* maxv;
-  float* part_v; int* part_i;      // [grid * M]
+  unsigned long long* best_key;     // kEpiArgmax: [M] packed (value, index) maxima, zero between launches
+  int whole_tiles;                 // kEpiArgmax: whole tiles per CTA (no split-tile finish)
   unsigned* done_ctr;
   // kEpiKVRing: the weight rows are [K_0 | V_0 | K_1 | V_1 | ...], one
   // 128-row tile per kv head (head_dim 128); row m goes to position
@@ -123,6 +129,26 @@ cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState*
 cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g,
                            void* y, int ldy, int rows, int H, float eps,
                            cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
+// bf16: finishes a split-K GEMM that added its fp32 sums into acc [rows,
+// ldacc] (kEpiRed): h = rnd(x + rnd(acc)) (rnd(acc) when x is NULL) written
+// back into x (when not NULL), acc cleared, y = rnd(rmsnorm(h) * g). H % 8 ==
+// 0, H <= 8192.
+cudaError_t launch_resid_rmsnorm(void* x, int ldx, float* acc, int ldacc, const void* g, void* y,
+                                 int ldy, int rows, int H, float eps, cudaStream_t st,
+                                 KTrace trace = KTrace{nullptr, 0});
+// bf16: finishes a kEpiRedPair gate/up GEMM: s[m][k] = rnd(silu(rnd(g)) *
+// rnd(u)) with g = acc[m][k], u = acc[m][I + k] (row stride ldacc), acc
+// cleared. I % 8 == 0, I <= 8192.
+cudaError_t launch_swiglu_finish(float* acc, int ldacc, void* s, int lds, int rows, int I,
+                                 cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
+// bf16, head_dim 128: finishes the append's K/V GEMM (kEpiRed over the
+// [K_l | V_l] column blocks of L layers, acc row stride ldacc): rounds, k-norm
+// (gain kgain[l]) + RoPE (rope[r][64]) for K, stores K and V of row r at
+// position ring->offset + r, clears the sums.
+cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nkv,
+                                  const void* const* kgain, float eps, const float2* rope, int neox,
+                                  void* ring_k, void* ring_v, long long cap, int append_only,
+                                  RingState* ring, cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
 // In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
 cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
                                   int heads, int hd, const void* g, float eps,
@@ -158,6 +184,12 @@ struct AttnArgs {
   const float2* rope;
   int neox;
   float eps;
+  // Tensor-core kernels only: q, kb and vb point into the fp32 sums of a
+  // kEpiRed QKV GEMM ([rows][ldq] floats, ldkv == ldq); each value is rounded
+  // to bf16 as it is loaded (the GEMM's output rounding). The split-merge
+  // kernel then clears those sums: zero_acc [zero_n] floats.
+  int qkv_f32;
+  float* zero_acc; int zero_n;
 };
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.
@@ -248,7 +280,7 @@ struct MarkovArgs {
   int gamma;
   int* out;                    // [gamma]
   int* out2;                   // optional second copy
-  float* part_v; int* part_i;  // scratch [grid]
+  unsigned long long* key;     // scratch [gamma] packed per-step maxima, zero between launches
   unsigned* counter;
   int grid;
 };

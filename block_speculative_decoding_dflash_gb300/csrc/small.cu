@@ -101,6 +101,139 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* x, int ldx, const
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The finish of a split-K GEMM whose CTAs added their fp32 partial sums into
+// acc (bf16 path): per row, h = rnd(x + rnd(acc)) (or rnd(acc) when x is
+// NULL), stored back into x, acc cleared for the next GEMM, then y =
+// rnd(h / rms(h) * g). One CTA per row; each thread keeps its 8-element
+// groups in registers between the passes (H <= 256 * 8 * kResidGroups).
+constexpr int kResidGroups = 4;
+__global__ void __launch_bounds__(256) resid_rmsnorm_kernel(bf16* x, int ldx, float* acc, int ldacc,
+                                                           const bf16* g, bf16* y, int ldy, int H,
+                                                           float eps, KTrace tr) {
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
+  // the gains are weights, written by no earlier kernel: load them before
+  // waiting for the GEMM whose sums this kernel finishes
+  float gv[kResidGroups][8];
+#pragma unroll
+  for (int q = 0; q < kResidGroups; ++q) {
+    const int i = (threadIdx.x + q * blockDim.x) * 8;
+    if (i < H) load8(g + i, gv[q]);
+  }
+  pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  bf16* xr = x ? x + (size_t)r * ldx : nullptr;
+  float* ar = acc + (size_t)r * ldacc;
+  float h[kResidGroups][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < kResidGroups; ++q) {
+    const int i = (threadIdx.x + q * blockDim.x) * 8;
+    if (i >= H) break;
+    float xv[8];
+    if (xr) load8(xr + i, xv);
+    const float4 a0 = __ldcg(reinterpret_cast<const float4*>(ar + i));
+    const float4 a1 = __ldcg(reinterpret_cast<const float4*>(ar + i + 4));
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    uint4 pk;
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float o0 = __bfloat162float(__float2bfloat16_rn(av[e]));
+      const float o1 = __bfloat162float(__float2bfloat16_rn(av[e + 1]));
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(xr ? xv[e] + o0 : o0, xr ? xv[e + 1] + o1 : o1);
+      h[q][e] = __low2float(b2);
+      h[q][e + 1] = __high2float(b2);
+      w32[e >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+      ss = fmaf(h[q][e], h[q][e], ss);
+      ss = fmaf(h[q][e + 1], h[q][e + 1], ss);
+    }
+    if (xr) *reinterpret_cast<uint4*>(xr + i) = pk;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(ar + i)[0] = z;
+    reinterpret_cast<float4*>(ar + i)[1] = z;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / static_cast<float>(H) + eps);
+  bf16* yr = y + (size_t)r * ldy;
+#pragma unroll
+  for (int q = 0; q < kResidGroups; ++q) {
+    const int i = (threadIdx.x + q * blockDim.x) * 8;
+    if (i >= H) break;
+    uint4 pk;
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const __nv_bfloat162 b2 =
+          __floats2bfloat162_rn(h[q][e] * inv * gv[q][e], h[q][e + 1] * inv * gv[q][e + 1]);
+      w32[e >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(yr + i) = pk;
+  }
+  if (tr.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(tr, 2);
+  }
+}
+
+// SwiGLU finish of a kEpiRedPair GEMM: blockIdx.y is the row, each thread
+// one group of 8 columns.
+__global__ void __launch_bounds__(256) swiglu_finish_kernel(float* acc, int ldacc, bf16* sout, int lds,
+                                                           int I, KTrace tr) {
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
+  pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
+  float* ar = acc + (size_t)blockIdx.y * ldacc;
+  bf16* sr = sout + (size_t)blockIdx.y * lds;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i < I) {
+    const float4 g0 = __ldcg(reinterpret_cast<const float4*>(ar + i));
+    const float4 g1 = __ldcg(reinterpret_cast<const float4*>(ar + i + 4));
+    const float4 u0 = __ldcg(reinterpret_cast<const float4*>(ar + I + i));
+    const float4 u1 = __ldcg(reinterpret_cast<const float4*>(ar + I + i + 4));
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint4 pk;
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float o[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float gr = __bfloat162float(__float2bfloat16_rn(g[e + k]));
+        const float ur = __bfloat162float(__float2bfloat16_rn(u[e + k]));
+        o[k] = gr / (1.0f + expf(-gr)) * ur;
+      }
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[0], o[1]);
+      w32[e >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(sr + i) = pk;
+    reinterpret_cast<float4*>(ar + i)[0] = z;
+    reinterpret_cast<float4*>(ar + i)[1] = z;
+    reinterpret_cast<float4*>(ar + I + i)[0] = z;
+    reinterpret_cast<float4*>(ar + I + i)[1] = z;
+  }
+  if (tr.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(tr, 2);
+  }
+}
+
 // One warp per (row, head): RMSNorm over hd with gain g[hd], then RoPE with
 // the row's (cos, sin) table; the result is rounded once. src may equal dst.
 template <typename T>
@@ -177,6 +310,67 @@ __global__ void __launch_bounds__(128) kv_to_ring_kernel(const T* kv, int ld, in
   T* vdst = ring_v + ((size_t)h * cap + slot) * hd;
   norm_rope_warp(ksrc, kdst, hd, kg, eps, rope + (size_t)r * (hd >> 1), neox, sm[warp]);
   for (int d = lane; d < hd; d += 32) vdst[d] = vsrc[d];
+}
+
+// Finish of the append's K/V GEMM (kEpiRed, head_dim 128): the fp32 sums of
+// block row r for layer l are acc[r][l * 2 kvdim + (K heads | V heads)];
+// each K head is rounded (the GEMM's output rounding), RMS-normalised with
+// the layer's k-norm gain and rotated at position ring->offset + r, each V
+// head rounded, both stored into the ring slot; the sums are cleared. One
+// warp per (row, layer, kv head), four dims a lane.
+__global__ void __launch_bounds__(128) kv_acc_to_ring_kernel(float* acc, int ldacc, int rows, int L,
+                                                            int nkv, const void* const* kgain, float eps,
+                                                            const float2* rope, int neox, bf16* ring_k,
+                                                            bf16* ring_v, long long cap, int append_only,
+                                                            RingState* ring) {
+  pdl_enter();
+  __shared__ float sm[4][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 4 + warp;
+  if (item >= rows * L * nkv) return;
+  const int r = item / (L * nkv), l = (item / nkv) % L, h = item % nkv;
+  const int kvdim = nkv * 128;
+  float* kacc = acc + (size_t)r * ldacc + (size_t)l * 2 * kvdim + h * 128;
+  float* vacc = kacc + kvdim;
+  const float4 k4 = __ldcg(reinterpret_cast<const float4*>(kacc) + lane);
+  const float4 v4 = __ldcg(reinterpret_cast<const float4*>(vacc) + lane);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  reinterpret_cast<float4*>(kacc)[lane] = z;
+  reinterpret_cast<float4*>(vacc)[lane] = z;
+  const long long pos = ring->offset + r;
+  if (append_only && pos - ring->base >= cap) {
+    if (lane == 0) atomicOr(&ring->error, kErrFull);
+    return;
+  }
+  const long long slot = ring_slot(pos, cap);
+  const size_t head = (((size_t)l * nkv + h) * cap + slot) * 128;
+  // V: rounded and stored
+  {
+    uint2 pk;
+    pk.x = pack_bf2(v4.x, v4.y);
+    pk.y = pack_bf2(v4.z, v4.w);
+    reinterpret_cast<uint2*>(ring_v + head)[lane] = pk;
+  }
+  // K: rounded, head RMSNorm, gain, RoPE, rounded once more
+  const float kv[4] = {rnd<bf16>(k4.x), rnd<bf16>(k4.y), rnd<bf16>(k4.z), rnd<bf16>(k4.w)};
+  float ss = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / 128.0f + eps);
+  const bf16* g = reinterpret_cast<const bf16*>(kgain[l]);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sm[warp][lane * 4 + e] = kv[e] * inv * __bfloat162float(g[lane * 4 + e]);
+  __syncwarp();
+  const float2* rr = rope + (size_t)r * 64;
+  bf16* kd = ring_k + head;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = lane + 32 * q;                         // rotation pair i of 64
+    const int ia = neox ? i : 2 * i, ib = neox ? i + 64 : 2 * i + 1;
+    const float2 cs = rr[i];
+    const float a = sm[warp][ia], b = sm[warp][ib];
+    kd[ia] = __float2bfloat16_rn(a * cs.x - b * cs.y);
+    kd[ib] = __float2bfloat16_rn(a * cs.y + b * cs.x);
+  }
 }
 
 // ---- ring bookkeeping ------------------------------------------------------------
@@ -330,6 +524,25 @@ cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState*
   return cudaGetLastError();
 }
 
+cudaError_t launch_resid_rmsnorm(void* x, int ldx, float* acc, int ldacc, const void* g, void* y,
+                                 int ldy, int rows, int H, float eps, cudaStream_t st, KTrace tr) {
+  if (rows <= 0) return cudaSuccess;
+  if (H % 8 || H > 256 * 8 * kResidGroups || ldacc % 4 || (x && ldx % 8) || ldy % 8)
+    return cudaErrorInvalidValue;
+  launch_pdl(resid_rmsnorm_kernel, dim3(rows), dim3(256), 0, st, (bf16*)x, ldx, acc, ldacc,
+             (const bf16*)g, (bf16*)y, ldy, H, eps, tr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_finish(float* acc, int ldacc, void* sout, int lds, int rows, int I,
+                                 cudaStream_t st, KTrace tr) {
+  if (rows <= 0) return cudaSuccess;
+  if (I % 8 || ldacc % 4 || lds % 8) return cudaErrorInvalidValue;
+  launch_pdl(swiglu_finish_kernel, dim3((I / 8 + 255) / 256, rows), dim3(256), 0, st, acc, ldacc,
+             (bf16*)sout, lds, I, tr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g, void* y,
                            int ldy, int rows, int H, float eps, cudaStream_t st, KTrace tr) {
   if (rows <= 0) return cudaSuccess;
@@ -375,6 +588,19 @@ cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int n
                                                    (const float*)kg, eps, rope, neox,
                                                    (float*)ring_k, (float*)ring_v, cap,
                                                    append_only, ring, use_dev, pos_host);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nkv,
+                                  const void* const* kgain, float eps, const float2* rope, int neox,
+                                  void* ring_k, void* ring_v, long long cap, int append_only,
+                                  RingState* ring, cudaStream_t st, KTrace tr) {
+  (void)tr;
+  const int items = rows * L * nkv;
+  if (items <= 0) return cudaSuccess;
+  if (ldacc % 4) return cudaErrorInvalidValue;
+  launch_pdl(kv_acc_to_ring_kernel, dim3((items + 3) / 4), dim3(128), 0, st, acc, ldacc, rows, L, nkv, kgain,
+             eps, rope, neox, (bf16*)ring_k, (bf16*)ring_v, cap, append_only, ring);
   return cudaGetLastError();
 }
 

@@ -55,7 +55,7 @@ struct Cfg {
 
 template <int BN, int EPI, int STAGES, int P>
 __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
-  constexpr int NV = (EPI == kEpiSwiglu) ? 2 : 1;
+  constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
   using C = Cfg<BN, NV, STAGES, P>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -79,7 +79,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   // that tiles * kchunks * grid fits.
   const unsigned KC = a.kchunks;
   const unsigned U = static_cast<unsigned>(a.tiles) * KC;
-  const unsigned u0 = U * b / G, u1 = U * (b + 1) / G;
+  // With a.whole_tiles (the lm_head at more than 8 rows) every CTA takes
+  // whole tiles (10 or 11 of the 1579 at the Muse shape): no split tile to
+  // finish at the end of its range, whose argmax epilogue grows with the
+  // rows, against a ~3% imbalance; otherwise the units are cut evenly.
+  const unsigned tb0 = static_cast<unsigned>(a.tiles) * b / G, tb1 = static_cast<unsigned>(a.tiles) * (b + 1) / G;
+  const bool whole = EPI == kEpiArgmax && a.whole_tiles;
+  const unsigned u0 = whole ? tb0 * KC : U * b / G;
+  const unsigned u1 = whole ? tb1 * KC : U * (b + 1) / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -351,6 +358,22 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
       u += c1 - c0;
+      if (EPI == kEpiRed || EPI == kEpiRedPair) {
+        // add this CTA's K range of the tile into the fp32 sums (the second
+        // weight's at column offset N); the kernel that reads them (after the
+        // programmatic dependency) finishes them
+        const int n = t * 128 + row;
+        if (n < a.N) {
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            float* dst = a.acc + (size_t)v * a.N + n;
+#pragma unroll
+            for (int m = 0; m < BN; ++m)
+              if (m < a.M) atomicAdd(dst + (size_t)m * a.ldacc, acc[v][m]);
+          }
+        }
+        continue;
+      }
       if (c0 == 0 && c1 == KC) {
         finish_tile(acc, t, 0, a.M, gv, res);
       } else if (EPI == kEpiArgmax) {
@@ -467,58 +490,35 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
     if (!ok) atomicOr(a.err, 4);
 
     if (EPI == kEpiArgmax) {
-      // Per-CTA best of every row, then the last CTA to finish reduces them.
+      // Per-CTA best of every row folded into one 64-bit key per row with an
+      // atomic maximum: the value's order-preserving bits above the inverted
+      // index, so the larger value wins and equal values keep the lower
+      // index (-0 is taken as +0). The last CTA to finish decodes the keys and
+      // clears them for the next launch.
       epi_sync();
       if (threadIdx.x >= 64 && threadIdx.x < 64 + BN && threadIdx.x - 64 < a.M) {
         const int m = threadIdx.x - 64;
-        a.part_v[(size_t)b * a.M + m] = best_v[m];
-        a.part_i[(size_t)b * a.M + m] = best_i[m];
+        const uint32_t u = __float_as_uint(best_v[m] + 0.0f);
+        const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        const unsigned long long key =
+            (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(best_i[m]));
+        atomicMax(a.best_key + m, key);
       }
       __threadfence();
       epi_sync();
       if (threadIdx.x == 64) s_last = (atomicAdd(a.done_ctr, 1u) == static_cast<unsigned>(G - 1));
       epi_sync();
-      if (s_last) {
-        // All 128 epilogue threads: column m = e % BN, CTAs c = e / BN + k *
-        // (128 / BN), eight of them requested per round trip; then the
-        // 128 / BN candidates of a column are reduced through shared memory.
-        // (The (value, index) order makes the result independent of the
-        // reduction order.)
+      if (s_last && threadIdx.x >= 64 && threadIdx.x < 64 + BN && threadIdx.x - 64 < a.M) {
         __threadfence();
-        constexpr int kSub = 128 / BN;
-        const int e = threadIdx.x - 64, m = e % BN, sub = e / BN;
-        float v = -INFINITY;
-        int idx = 0x7fffffff;
-        if (m < a.M) {
-          for (int c0 = sub; c0 < G; c0 += 8 * kSub) {
-            float cv[8];
-            int ci[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int c = c0 + j * kSub;
-              cv[j] = c < G ? __ldcg(a.part_v + (size_t)c * a.M + m) : -INFINITY;
-              ci[j] = c < G ? __ldcg(a.part_i + (size_t)c * a.M + m) : 0x7fffffff;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (better(cv[j], ci[j], v, idx)) { v = cv[j]; idx = ci[j]; }
-          }
-        }
-        // kSub candidates per column; thread m combines them.
-        __shared__ float fin_v[128];
-        __shared__ int fin_i[128];
-        fin_v[e] = v;
-        fin_i[e] = idx;
-        epi_sync();
-        if (e < BN && e < a.M) {
-#pragma unroll
-          for (int k = 1; k < kSub; ++k)
-            if (better(fin_v[k * BN + e], fin_i[k * BN + e], v, idx)) { v = fin_v[k * BN + e]; idx = fin_i[k * BN + e]; }
-          a.ids[e] = idx;
-          if (a.ids2) a.ids2[e] = idx;
-          a.maxv[e] = v;
-        }
-        if (threadIdx.x == 64) *a.done_ctr = 0u;
+        const int m = threadIdx.x - 64;
+        const unsigned long long key = atomicExch(a.best_key + m, 0ull);
+        const uint32_t ord = static_cast<uint32_t>(key >> 32);
+        const uint32_t u = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+        const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+        a.ids[m] = idx;
+        if (a.ids2) a.ids2[m] = idx;
+        a.maxv[m] = __uint_as_float(u);
+        if (m == 0) *a.done_ctr = 0u;
       }
     }
   }
@@ -531,13 +531,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   }
 }
 
-// The decode-layer GEMMs are short: keep two CTAs per SM (about 73 / 103 KB of
-// shared memory each) so the next GEMM's CTAs fit beside the running one and
-// stream their first weight tiles early. The lm_head is long: a deep ring of
-// paired-chunk stages.
+// Ring depth in paired-chunk stages: the decode-layer GEMMs take four (three
+// for the two-weight SwiGLU stages), which at up to 16 block rows holds most
+// of a CTA's weight range, requested before the programmatic dependency
+// resolves; the lm_head is long and takes a deeper ring.
 template <int BN, int EPI>
 constexpr int stages_for() {
-  return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : EPI == kEpiSwiglu ? (BN == 16 ? 3 : 2) : (BN == 16 ? 4 : 2);
+  return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 3 : 4;
 }
 template <int BN, int EPI>
 constexpr int pairs_for() { return 2; }
@@ -546,7 +546,7 @@ template <int BN, int EPI>
 cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) {
   constexpr int S = stages_for<BN, EPI>();
   constexpr int P = pairs_for<BN, EPI>();
-  constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
+  constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -564,7 +564,7 @@ template <int BN, int EPI>
 cudaError_t attr_tc() {
   constexpr int S = stages_for<BN, EPI>();
   constexpr int P = pairs_for<BN, EPI>();
-  constexpr int NV = EPI == kEpiSwiglu ? 2 : 1;
+  constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
   return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)Cfg<BN, NV, S, P>::kSmem);
 }
@@ -836,6 +836,10 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiSwiglu>()) != cudaSuccess) return e;
   if ((e = attr_tc<16, kEpiKVRing>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiKVRing>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiRed>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiRed>()) != cudaSuccess) return e;
+  if ((e = attr_tc<16, kEpiRedPair>()) != cudaSuccess) return e;
+  if ((e = attr_tc<32, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
   return attr_tc<32, kEpiArgmax>();
@@ -874,6 +878,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
       case kEpiResid: return launch_tc<16, kEpiResid>(a, grid, pdl, st);
       case kEpiSwiglu: return launch_tc<16, kEpiSwiglu>(a, grid, pdl, st);
       case kEpiKVRing: return launch_tc<16, kEpiKVRing>(a, grid, pdl, st);
+      case kEpiRed: return launch_tc<16, kEpiRed>(a, grid, pdl, st);
+      case kEpiRedPair: return launch_tc<16, kEpiRedPair>(a, grid, pdl, st);
       default: return launch_tc<16, kEpiArgmax>(a, grid, pdl, st);
     }
   }
@@ -882,6 +888,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
     case kEpiResid: return launch_tc<32, kEpiResid>(a, grid, pdl, st);
     case kEpiSwiglu: return launch_tc<32, kEpiSwiglu>(a, grid, pdl, st);
     case kEpiKVRing: return launch_tc<32, kEpiKVRing>(a, grid, pdl, st);
+    case kEpiRed: return launch_tc<32, kEpiRed>(a, grid, pdl, st);
+    case kEpiRedPair: return launch_tc<32, kEpiRedPair>(a, grid, pdl, st);
     default: return launch_tc<32, kEpiArgmax>(a, grid, pdl, st);
   }
 }

@@ -60,5 +60,4 @@ def test_muse_graph_rounds_match_oracle(H):
         check.check_state()
         if r % 5 == 4:
             check.check_ring(max_rows=32)
-    assert check.ties <= 2
     c.close()
