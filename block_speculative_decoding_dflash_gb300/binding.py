@@ -85,6 +85,13 @@ _sig("dflash_ingest_context", ctypes.c_int, _vp, _vp, _i64, _i64, _i32)
 _sig("dflash_set_anchor", ctypes.c_int, _vp, _i32)
 _sig("dflash_draft_block", ctypes.c_int, _vp, _i32, _i64, _i32, _vp)
 _sig("dflash_sync_round", ctypes.c_int, _vp, _vp, _vp)
+_sig("dflash_ctx_create_batched", ctypes.c_int, ctypes.POINTER(Config), ctypes.POINTER(Weights), _i32, _vp,
+     ctypes.POINTER(_vp))
+_sig("dflash_batch_size", ctypes.c_int, _vp)
+_sig("dflash_ingest_context_seq", ctypes.c_int, _vp, _i32, _vp, _i64, _i64, _i32)
+_sig("dflash_get_state_seq", ctypes.c_int, _vp, _i32, ctypes.POINTER(RoundStateC))
+_sig("dflash_get_stats_seq", ctypes.c_int, _vp, _i32, ctypes.POINTER(Stats))
+_sig("dflash_ring_seq", ctypes.c_int, _vp, _i32, ctypes.POINTER(_vp))
 _sig("dflash_verify_sampled", ctypes.c_int, _vp, _vp, _i32, _vp, _vp, ctypes.c_float, ctypes.c_float,
      _vp, _vp, _vp)
 _sig("dflash_short_conv_block", ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp)
@@ -261,8 +268,11 @@ class DFlashContext:
     """One drafter context (C: dflash_ctx). Holds references to the weight
     tensors it borrows."""
 
-    def __init__(self, cfg: dict, weights: dict, stream: torch.cuda.Stream | None = None):
+    def __init__(self, cfg: dict, weights: dict, stream: torch.cuda.Stream | None = None, n_seq: int = 1):
+        """n_seq > 1: a batch of sequences drafted, verified and committed
+        together (dflash_ctx_create_batched)."""
         self.cfg = dict(cfg)
+        self.n_seq = n_seq
         self.ccfg = make_config(cfg)
         self.weights = weights
         self.stream = stream or torch.cuda.Stream()
@@ -280,8 +290,8 @@ class DFlashContext:
         w.markov_w2 = weights["markov_w2"].data_ptr() if "markov_w2" in weights else None
         w.layers = ctypes.cast(self._layers, ctypes.POINTER(ctypes.c_void_p))
         h = _vp()
-        rc = lib.dflash_ctx_create(ctypes.byref(self.ccfg), ctypes.byref(w),
-                                   self.stream.cuda_stream, ctypes.byref(h))
+        rc = lib.dflash_ctx_create_batched(ctypes.byref(self.ccfg), ctypes.byref(w), n_seq,
+                                           self.stream.cuda_stream, ctypes.byref(h))
         if rc:
             raise DFlashError(rc, last_error(None))
         self.h = h.value
@@ -320,11 +330,13 @@ class DFlashContext:
                                               _ptr(p_draft) if p_draft is not None else None))
 
     def sync_round(self, block):
-        """Waits for the stream; returns (tokens[:n], n) of the last verify."""
-        tok = np.zeros(block, dtype=np.int32)
-        n = np.zeros(1, dtype=np.int32)
+        """Waits for the stream; returns (tokens[:n], n) of the last verify
+        (a list of them, one per sequence, for a batch)."""
+        tok = np.zeros((self.n_seq, block), dtype=np.int32)
+        n = np.zeros(self.n_seq, dtype=np.int32)
         self._check(lib.dflash_sync_round(self.h, tok.ctypes.data, n.ctypes.data))
-        return tok[: int(n[0])], int(n[0])
+        out = [(tok[s, : int(n[s])], int(n[s])) for s in range(self.n_seq)]
+        return out[0] if self.n_seq == 1 else out
 
     def verify_accept(self, logits, block, draft_ids, tokens, n):
         self._prep()
@@ -368,24 +380,28 @@ class DFlashContext:
         self._prep()
         self._check(lib.dflash_get_backbone_ids(self.h, _ptr(out)))
 
-    def state(self) -> dict:
+    def ingest_context_seq(self, seq, resid, rows, first_pos, anchor):
+        self._prep()
+        self._check(lib.dflash_ingest_context_seq(self.h, seq, _ptr(resid), rows, first_pos, anchor))
+
+    def state(self, seq: int = 0) -> dict:
         s = RoundStateC()
-        self._check(lib.dflash_get_state(self.h, ctypes.byref(s)))
+        self._check(lib.dflash_get_state_seq(self.h, seq, ctypes.byref(s)))
         return {"position": s.position, "anchor": s.anchor, "last_n": s.last_n,
                 "last_accepted": s.last_accepted, "error": s.error}
 
-    def stats(self) -> dict:
+    def stats(self, seq: int = 0) -> dict:
         s = Stats()
-        self._check(lib.dflash_get_stats(self.h, ctypes.byref(s)))
+        self._check(lib.dflash_get_stats_seq(self.h, seq, ctypes.byref(s)))
         return {"rounds": s.rounds, "draft_n": s.draft_n, "accepted": s.accepted,
                 "emitted": s.emitted}
 
     def reset_stats(self):
         self._check(lib.dflash_reset_stats(self.h))
 
-    def ring(self) -> RingCache:
+    def ring(self, seq: int = 0) -> RingCache:
         h = _vp()
-        self._check(lib.dflash_ring(self.h, ctypes.byref(h)))
+        self._check(lib.dflash_ring_seq(self.h, seq, ctypes.byref(h)))
         return RingCache(handle=h.value, owner=self)
 
     def capture_begin(self):

@@ -122,6 +122,8 @@ struct ring_cache {
   RingState* st = nullptr;
   cudaStream_t stream = nullptr;
   bool owned_by_ctx = false;
+  bool view = false;        // a batch sequence's view into its context's ring storage
+  int nseq = 1;             // sequences whose rings this storage holds (a context's batch)
   int host_appended = 0;
   long long pos_hi = 0;     // upper bound of the device offset
   long long host_base = 0;
@@ -171,6 +173,15 @@ struct dflash_ctx {
   float* maxv = nullptr;
   int* backbone_ids = nullptr;
   float* zlog = nullptr;
+  // batch: nseq sequences per round, each with its own ring (views[s]),
+  // round state (rs[s]) and verify ticket; an ingest writes sequence seq_cur
+  int nseq = 1;
+  int seq_cur = 0;
+  std::vector<ring_cache*> views;
+  std::vector<char> seq_ctx;
+  int* ids_all = nullptr;                      // [R] read-out ids of every block row (batch)
+  float* maxv_all = nullptr;                   // [R]
+  unsigned* vf_ctr = nullptr;                  // [nseq] verify tickets
   float* acc = nullptr;                        // [R][H] fp32 sums of the kEpiRed GEMMs, zero between uses
   float* qkv_acc = nullptr;                    // [R][qkv_n] fp32 sums of the QKV GEMM, zero between uses
   float* gu_acc = nullptr;                     // [R][2 I] fp32 gate / up sums, zero between uses
@@ -233,7 +244,7 @@ P* carve(char*& cur, size_t bytes) {
 
 int ring_create_impl(int L, int nkv, int hd, int window, int max_block, int dtype,
                      int max_context, int flags, cudaStream_t st, ring_cache** out,
-                     std::string& err) {
+                     std::string& err, int nseq = 1) {
   if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
   *out = nullptr;
   if (L < 1 || nkv < 1 || hd < 1) return fail(err, DFLASH_EINVAL, "ring dimensions must be positive");
@@ -250,15 +261,20 @@ int ring_create_impl(int L, int nkv, int hd, int window, int max_block, int dtyp
   r->cap = window > 0 ? (long long)window + slack_rule(max_block, !(flags & DFLASH_RING_UNFLOORED))
                       : (long long)max_context;
   r->esz = dtype == DFLASH_BF16 ? 2 : 4;
-  const size_t bytes = (size_t)L * nkv * (size_t)r->cap * hd * r->esz;
+  r->nseq = nseq;
+  const size_t bytes = (size_t)nseq * L * nkv * (size_t)r->cap * hd * r->esz;
   cudaError_t e;
   if ((e = cudaMalloc(&r->k, bytes)) != cudaSuccess ||
       (e = cudaMalloc(&r->v, bytes)) != cudaSuccess ||
-      (e = cudaMalloc(&r->st, sizeof(RingState))) != cudaSuccess ||
+      (e = cudaMalloc(&r->st, sizeof(RingState) * nseq)) != cudaSuccess ||
       (e = cudaMemsetAsync(r->k, 0, bytes, st)) != cudaSuccess ||
-      (e = cudaMemsetAsync(r->v, 0, bytes, st)) != cudaSuccess ||
-      (e = launch_ring_reset(r->st, 0, st)) != cudaSuccess ||
-      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+      (e = cudaMemsetAsync(r->v, 0, bytes, st)) != cudaSuccess) {
+    cudaFree(r->k); cudaFree(r->v); cudaFree(r->st);
+    delete r;
+    return cuda_fail(err, e, "ring allocation");
+  }
+  for (int q = 0; q < nseq && e == cudaSuccess; ++q) e = launch_ring_reset(r->st + q, 0, st);
+  if (e != cudaSuccess || (e = cudaStreamSynchronize(st)) != cudaSuccess) {
     cudaFree(r->k); cudaFree(r->v); cudaFree(r->st);
     delete r;
     return cuda_fail(err, e, "ring allocation");
@@ -269,6 +285,7 @@ int ring_create_impl(int L, int nkv, int hd, int window, int max_block, int dtyp
 
 void ring_free(ring_cache* r) {
   if (!r) return;
+  if (r->view) { delete r; return; }
   cudaFree(r->k);
   cudaFree(r->v);
   cudaFree(r->st);
@@ -294,6 +311,11 @@ LinearArgs lin_args(const void* x, int ldx, void* y, int ldy, int M, int N, int 
 const void* LW(const dflash_ctx* c, int l, int which) {
   return c->layers[(size_t)l * DFLASH_LAYER_TENSORS + which];
 }
+
+// Ring elements of one sequence (all layers) and sequence s's K / V base.
+size_t seq_kv_elems(const dflash_ctx* c) { return (size_t)c->cfg.n_layers * c->nkv * c->ring->cap * c->hd; }
+char* ring_k_of(const dflash_ctx* c, int s) { return static_cast<char*>(c->ring->k) + s * seq_kv_elems(c) * c->esz; }
+char* ring_v_of(const dflash_ctx* c, int s) { return static_cast<char*>(c->ring->v) + s * seq_kv_elems(c) * c->esz; }
 
 int bn_index(int M) { return M <= 16 ? 0 : 1; }
 int bn_of(int M) { return M <= 16 ? 16 : 32; }
@@ -340,8 +362,13 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
                          float2* rope, int use_dev, long long pos_host) {
   const int dt = c->dt;
   cudaStream_t st = c->stream;
-  CK(c->err, launch_rope_table(c->inv_freq, c->half, use_dev ? c->ring->st : nullptr, pos_host,
-                               rows, rope, st));
+  // an append (use_dev) writes every sequence of the batch, rows / nseq rows
+  // each; an ingest writes sequence seq_cur
+  const int ns = use_dev ? c->nseq : 1;
+  const int rps = rows / ns;
+  const int sq = use_dev ? 0 : c->seq_cur;
+  RingState* rst = c->ring->st + sq;
+  CK(c->err, launch_rope_table(c->inv_freq, c->half, use_dev ? rst : nullptr, pos_host, rps, rope, st, ns));
   const bool tc = c->use_tc && rows <= 32 && cn == c->app_c;
   if (tc) {
     // encoder.fc adds its fp32 sums into c->acc; hidden_norm rounds them
@@ -399,9 +426,10 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
       CK(c->err, tc_run(c, t));
     }
     CK(c->err, launch_kv_acc_to_ring(c->kv_acc, L * 2 * c->kvdim, rows, L, c->nkv, c->kgain_dev,
-                                     c->cfg.rms_eps, rope, c->cfg.rope_neox, c->ring->k, c->ring->v,
-                                     c->ring->cap, c->ring->append_only, c->ring->st, st,
-                                     use_dev ? ktrace_slot(c, "append.kv_ring") : KTrace{nullptr, 0}));
+                                     c->cfg.rms_eps, rope, c->cfg.rope_neox, ring_k_of(c, sq), ring_v_of(c, sq),
+                                     c->ring->cap, c->ring->append_only, rst, st,
+                                     use_dev ? ktrace_slot(c, "append.kv_ring") : KTrace{nullptr, 0}, rps,
+                                     (long long)seq_kv_elems(c)));
     return DFLASH_OK;
   }
   for (int l = 0; l < c->cfg.n_layers; ++l) {
@@ -420,10 +448,9 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
     }
     const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
     CK(c->err, launch_kv_to_ring(dt, kv, 2 * c->kvdim, rows, c->nkv, c->hd, LW(c, l, kKNorm),
-                                 c->cfg.rms_eps, rope, c->cfg.rope_neox,
-                                 static_cast<char*>(c->ring->k) + lay,
-                                 static_cast<char*>(c->ring->v) + lay, c->ring->cap,
-                                 c->ring->append_only, c->ring->st, use_dev, pos_host, st));
+                                 c->cfg.rms_eps, rope, c->cfg.rope_neox, ring_k_of(c, sq) + lay,
+                                 ring_v_of(c, sq) + lay, c->ring->cap, c->ring->append_only, rst, use_dev,
+                                 pos_host, st, rps, (long long)seq_kv_elems(c)));
   }
   return DFLASH_OK;
 }
@@ -466,8 +493,8 @@ int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void*
     b.ldy = ldkv;
     b.err = c->tc_err;
     if (to_ring) {
-      b.ring_k = c->ring->k; b.ring_v = c->ring->v; b.cap = c->ring->cap; b.pos0 = pos_host;
-      b.ring = c->ring->st; b.rope = rope; b.kgain = c->kgain_dev;
+      b.ring_k = ring_k_of(c, c->seq_cur); b.ring_v = ring_v_of(c, c->seq_cur); b.cap = c->ring->cap;
+      b.pos0 = pos_host; b.ring = c->ring->st + c->seq_cur; b.rope = rope; b.kgain = c->kgain_dev;
       b.nkv = c->nkv; b.kvdim = c->kvdim; b.l0 = l0; b.append_only = c->ring->append_only;
       b.neox = c->cfg.rope_neox; b.eps = c->cfg.rms_eps;
     }
@@ -483,9 +510,9 @@ int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void*
     const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
     CK(c->err, launch_kv_to_ring(dt, static_cast<char*>(kv) + (size_t)l * 2 * c->kvdim * c->esz, ldkv,
                                  rows, c->nkv, c->hd, LW(c, l, kKNorm), c->cfg.rms_eps, rope,
-                                 c->cfg.rope_neox, static_cast<char*>(c->ring->k) + lay,
-                                 static_cast<char*>(c->ring->v) + lay, c->ring->cap,
-                                 c->ring->append_only, c->ring->st, 0, pos_host, st));
+                                 c->cfg.rope_neox, ring_k_of(c, c->seq_cur) + lay,
+                                 ring_v_of(c, c->seq_cur) + lay, c->ring->cap, c->ring->append_only,
+                                 c->ring->st + c->seq_cur, 0, pos_host, st, rows, 0));
   }
   return DFLASH_OK;
 }
@@ -555,7 +582,8 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.cap = c->ring->cap;
   at.ring = c->ring->st;
   at.window = c->cfg.window;
-  at.rows = rows; at.nq = c->nq; at.nkv = c->nkv; at.hd = c->hd;
+  at.rows = rows / c->nseq; at.nq = c->nq; at.nkv = c->nkv; at.hd = c->hd;
+  at.nseq = c->nseq; at.seq_kv = (long long)seq_kv_elems(c);
   at.max_ctx = c->max_ctx;
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
@@ -711,6 +739,7 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   cudaStreamSynchronize(ctx->stream);
   for (auto& g : ctx->graphs)
     if (g) cudaGraphExecDestroy(g);
+  for (ring_cache* v : ctx->views) ring_free(v);
   ring_free(ctx->ring);
   cudaFree(ctx->arena);
   cudaFree(ctx->ktr);
@@ -721,13 +750,25 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   delete ctx;
 }
 
-int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* stream,
-                      dflash_ctx** out) {
+int dflash_ctx_create_batched(const dflash_config* cfg, const dflash_weights* w, int32_t n_seq,
+                              void* stream, dflash_ctx** out) {
   std::string& err = g_create_err;
   if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
   *out = nullptr;
   int rc = check_config(cfg, err);
   if (rc) return rc;
+  if (n_seq < 1 || n_seq > 64) return fail(err, DFLASH_ERANGE, "n_seq %d outside [1, 64]", n_seq);
+  if (n_seq > 1 && (cfg->window <= 0 || cfg->markov_rank > 0))
+    return fail(err, DFLASH_EINVAL, "a batch needs a sliding window and no Markov head");
+  if ((int64_t)n_seq * cfg->max_block > kMaxBlock)
+    return fail(err, DFLASH_ERANGE, "n_seq * max_block = %lld exceeds %d rows",
+                (long long)n_seq * cfg->max_block, kMaxBlock);
+  {
+    dflash_config wide = *cfg;
+    wide.max_block = n_seq * cfg->max_block;     // the products the batch's row count reaches
+    rc = check_config(&wide, err);
+    if (rc) return rc;
+  }
   if (!w || !w->embed || !w->fc || !w->hidden_norm || !w->final_norm || !w->lm_head || !w->layers)
     return fail(err, DFLASH_EINVAL, "a weight pointer is NULL");
   const void* tops[] = {w->embed, w->fc, w->hidden_norm, w->final_norm, w->lm_head};
@@ -756,13 +797,25 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->half = c->hd / 2; c->I = cfg->intermediate; c->V = cfg->vocab;
   c->kin = cfg->k_target_layers * cfg->target_hidden;
   c->qdim = c->nq * c->hd; c->kvdim = c->nkv * c->hd; c->qkv_n = c->qdim + 2 * c->kvdim;
-  c->rows_max = cfg->max_block;
+  c->nseq = n_seq;
+  c->rows_max = n_seq * cfg->max_block;
   c->max_ctx = cfg->window > 0 ? cfg->window : cfg->max_context;
 
   rc = ring_create_impl(cfg->n_layers, c->nkv, c->hd, cfg->window, cfg->max_block, cfg->dtype,
-                        cfg->max_context, 0, c->stream, &c->ring, err);
+                        cfg->max_context, 0, c->stream, &c->ring, err, n_seq);
   if (rc) { delete c; return rc; }
   c->ring->owned_by_ctx = true;
+  c->seq_ctx.assign(n_seq, 0);
+  for (int q = 0; q < n_seq; ++q) {
+    ring_cache* v = new (std::nothrow) ring_cache(*c->ring);
+    if (!v) { ring_free(c->ring); delete c; return fail(err, DFLASH_ECUDA, "out of host memory"); }
+    v->view = true;
+    v->nseq = 1;
+    v->k = static_cast<char*>(c->ring->k) + (size_t)q * c->ring->L * c->nkv * c->ring->cap * c->hd * c->esz;
+    v->v = static_cast<char*>(c->ring->v) + (size_t)q * c->ring->L * c->nkv * c->ring->cap * c->hd * c->esz;
+    v->st = c->ring->st + q;
+    c->views.push_back(v);
+  }
 
   c->R = c->rows_max + 1 > 33 ? c->rows_max + 1 : 33;
   const size_t E = c->esz, R = c->R;
@@ -774,7 +827,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   const size_t attn_mma_floats = attention_mma_scratch_floats(c->rows_max, c->nq, c->nkv, c->max_ctx);
   if (attn_mma_floats > attn_floats) attn_floats = attn_mma_floats;
   const size_t sizes[] = {
-      sizeof(RoundState), sizeof(double) * c->half,
+      sizeof(RoundState) * n_seq, sizeof(double) * c->half,
       R * c->H * E, R * c->H * E, R * c->qkv_n * E, R * c->qdim * E, R * c->I * E, R * c->H * E,
       R * c->half * sizeof(float2), attn_floats * sizeof(float),
       R * c->H * E, R * c->H * E, R * 2 * c->kvdim * E, R * c->half * sizeof(float2),
@@ -786,7 +839,7 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
       (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64,
       (size_t)cfg->n_layers * sizeof(void*), R * 4, R * 4, R * 4, 64, R * c->H * 4, R * c->qkv_n * 4, R * 2 * c->I * 4,
-      R * (size_t)cfg->n_layers * 2 * c->kvdim * 4};
+      R * (size_t)cfg->n_layers * 2 * c->kvdim * 4, R * 4, R * 4, sizeof(unsigned) * n_seq};
   size_t total = 0;
   for (size_t s : sizes) total += (s + 255) & ~size_t(255);
   cudaError_t e = cudaMalloc(&c->arena, total);
@@ -839,6 +892,9 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   c->qkv_acc = carve<float>(cur, sizes[si++]);
   c->gu_acc = carve<float>(cur, sizes[si++]);
   c->kv_acc = carve<float>(cur, sizes[si++]);
+  c->ids_all = carve<int>(cur, sizes[si++]);
+  c->maxv_all = carve<float>(cur, sizes[si++]);
+  c->vf_ctr = carve<unsigned>(cur, sizes[si++]);
 
   std::vector<const void*> kg(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) kg[l] = c->layers[(size_t)l * DFLASH_LAYER_TENSORS + 5];
@@ -868,9 +924,21 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* s
   return DFLASH_OK;
 }
 
+int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w, void* stream,
+                      dflash_ctx** out) {
+  return dflash_ctx_create_batched(cfg, w, 1, stream, out);
+}
+
 int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_t first_pos,
                           int32_t anchor) {
+  return dflash_ingest_context_seq(c, 0, resid, rows, first_pos, anchor);
+}
+
+int dflash_ingest_context_seq(dflash_ctx* c, int32_t seq, const void* resid, int64_t rows, int64_t first_pos,
+                              int32_t anchor) {
   if (!c) return DFLASH_EINVAL;
+  if (seq < 0 || seq >= c->nseq) return fail(c->err, DFLASH_ERANGE, "seq %d outside [0, %d)", seq, c->nseq);
+  c->seq_cur = seq;
   if (rows <= 0) return fail(c->err, DFLASH_EEMPTY, "empty context (rows = %lld)", (long long)rows);
   if (!resid || !aligned16(resid)) return fail(c->err, DFLASH_EINVAL, "resid is NULL or misaligned");
   if (first_pos < 0) return fail(c->err, DFLASH_EINVAL, "first_pos must be >= 0");
@@ -882,7 +950,7 @@ int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_
   const long long kept = next - kept_first;
   if (c->ring->append_only && kept > c->ring->cap)
     return fail(c->err, DFLASH_EFULL, "%lld context rows exceed max_context %lld", kept, c->ring->cap);
-  CK(c->err, launch_ring_reset(c->ring->st, kept_first, c->stream));
+  CK(c->err, launch_ring_reset(c->ring->st + seq, kept_first, c->stream));
   const char* src = static_cast<const char*>(resid) + (size_t)(kept_first - first_pos) * c->kin * c->esz;
   const bool wide = c->use_tc && c->H % 256 == 0 && c->kvdim % 256 == 0;
   for (long long s = 0; s < kept; s += c->ing_rows) {
@@ -894,12 +962,14 @@ int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_
                                         kept_first + s);
     if (rc) return rc;
   }
-  CK(c->err, launch_ring_advance(c->ring->st, static_cast<int>(kept), 2, c->stream));
-  CK(c->err, launch_set_anchor(c->rs, anchor, c->stream));
+  CK(c->err, launch_ring_advance(c->ring->st + seq, static_cast<int>(kept), 2, c->stream));
+  CK(c->err, launch_set_anchor(c->rs + seq, anchor, c->stream));
   c->ring->host_base = kept_first;
   c->ring->pos_hi = next;
   c->ring->host_appended = 0;
+  c->seq_ctx[seq] = 1;
   c->has_context = true;
+  for (char h : c->seq_ctx) c->has_context = c->has_context && h;
   c->appended_block = 0;
   return DFLASH_OK;
 }
@@ -933,9 +1003,12 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
   if (anchor >= c->V)
     return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
+  if (c->nseq > 1 && (anchor >= 0 || anchor_pos >= 0))
+    return fail(c->err, DFLASH_EINVAL, "a batch drafts from its device-resident anchors (pass -1, -1)");
   if (!c->has_context) return fail(c->err, DFLASH_EEMPTY, "no context ingested");
   const int dspark = c->cfg.kind == DFLASH_KIND_DSPARK;
-  const int rows = dspark ? block - 1 : block;
+  const int rps = dspark ? block - 1 : block;      // block rows of one sequence
+  const int rows = rps * c->nseq;                  // rows of the whole batch
   const int read0 = dspark ? 0 : 1;
   const int R = block - 1;
   const int dt = c->dt;
@@ -947,9 +1020,9 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     CK(c->err, cudaMemsetAsync(c->ktr, 0xFF, sizeof(unsigned long long) * kKTraceSlots, st));
     CK(c->err, cudaMemsetAsync(c->ktr + kKTraceSlots, 0, 2 * sizeof(unsigned long long) * kKTraceSlots, st));
   }
-  CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rows, c->x,
-                                c->ring->st, c->inv_freq, c->half, rows, c->rope,
-                                anchor < 0 ? -1 : anchor, anchor_pos < 0 ? -1 : anchor_pos, st));
+  CK(c->err, launch_embed_block(dt, c->embed, c->H, c->V, c->rs, c->cfg.mask_token_id, rps, c->x,
+                                c->ring->st, c->inv_freq, c->half, rps, c->rope,
+                                anchor < 0 ? -1 : anchor, anchor_pos < 0 ? -1 : anchor_pos, st, c->nseq));
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     int rc = layer_forward(c, l, rows);
     if (rc) return rc;
@@ -960,24 +1033,29 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
   else
     CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H,
                               c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
+  // One sequence: the read-out rows read0 .. are contiguous and the argmax
+  // writes the proposals directly. A batch: the argmax runs over every block
+  // row and the read-out rows of each sequence are picked out afterwards.
+  const bool batch = c->nseq > 1;
+  const int lm_rows = batch ? rows : R;
   LmHeadArgs lm{};
-  lm.x = static_cast<char*>(c->xf) + (size_t)read0 * c->H * c->esz;
+  lm.x = static_cast<char*>(c->xf) + (size_t)(batch ? 0 : read0) * c->H * c->esz;
   lm.ldx = c->H;
   lm.w = c->lm_head;
-  lm.R = R; lm.H = c->H; lm.V = c->V;
+  lm.R = lm_rows; lm.H = c->H; lm.V = c->V;
   lm.softcap = c->cfg.softcap;
-  lm.ids = markov ? c->backbone_ids : draft_ids;
-  lm.ids2 = markov ? nullptr : c->backbone_ids;
-  lm.maxv = c->maxv;
+  lm.ids = batch ? c->ids_all : (markov ? c->backbone_ids : draft_ids);
+  lm.ids2 = (batch || markov) ? nullptr : c->backbone_ids;
+  lm.maxv = batch ? c->maxv_all : c->maxv;
   lm.logits = (markov && c->cfg.markov_add) ? c->zlog : nullptr;
   lm.part_v = c->lm_pv; lm.part_i = c->lm_pi;
   lm.counter = c->counters + 0;
   lm.grid = c->lm_grid;
   if (c->lm_timing) CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
-  if (c->use_tc && R <= 32 && lm.logits == nullptr) {
-    TcGemmArgs t = tc_args(c, R, c->V, c->H, kEpiArgmax);
+  if (c->use_tc && lm_rows <= 32 && lm.logits == nullptr) {
+    TcGemmArgs t = tc_args(c, lm_rows, c->V, c->H, kEpiArgmax);
     tc_segments(t, {{&c->lm_map, c->V}});
-    t.b_map = c->xf_map[read0][bn_index(R)];
+    t.b_map = c->xf_map[batch ? 0 : read0][bn_index(lm_rows)];
     t.softcap = c->cfg.softcap;
     t.ids = lm.ids; t.ids2 = lm.ids2; t.maxv = lm.maxv;
     t.best_key = c->tc_best; t.done_ctr = c->tc_done; t.whole_tiles = t.M > 8;
@@ -990,6 +1068,9 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     CK(c->err, cudaEventRecordWithFlags(c->lm_ev[1], st, c->capturing ? cudaEventRecordExternal : 0));
     c->lm_recorded = true;
   }
+  if (batch)
+    CK(c->err, launch_split_ids(c->ids_all, c->maxv_all, rps, read0, c->nseq, draft_ids, c->backbone_ids,
+                                c->maxv, st));
   if (markov) CK(c->err, draft_markov(c, R, draft_ids));
   c->last_draft_block = block;
   return DFLASH_OK;
@@ -1004,7 +1085,8 @@ int dflash_verify_accept(dflash_ctx* c, const void* target_logits, int32_t block
     return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
   VerifyArgs v{};
   v.L = target_logits; v.B = block; v.V = c->V; v.d = draft_ids; v.tokens = tokens; v.n = n;
-  v.rs = c->rs; v.part_v = c->vf_pv; v.part_i = c->vf_pi; v.counter = c->counters + 1;
+  v.rs = c->rs; v.part_v = c->vf_pv; v.part_i = c->vf_pi; v.counter = c->vf_ctr;
+  v.nseq = c->nseq;
   v.chunks = c->vf_chunks;
   CK(c->err, launch_verify(c->dt, v, c->stream));
   c->last_verify_block = block;
@@ -1024,6 +1106,7 @@ int dflash_verify_sampled(dflash_ctx* c, const void* target_logits, int32_t bloc
     return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
   if (!(temperature > 0.f) || !std::isfinite(temperature) || !(softcap >= 0.f) || !std::isfinite(softcap))
     return fail(c->err, DFLASH_EINVAL, "temperature must be > 0 and softcap >= 0, both finite");
+  if (c->nseq > 1) return fail(c->err, DFLASH_EINVAL, "the sampled verify takes one sequence");
   SampledVerifyArgs a{};
   a.L = target_logits; a.B = block; a.V = c->V; a.d = draft_ids; a.u = uniforms;
   a.temperature = temperature; a.softcap = softcap; a.tokens = tokens; a.n = n; a.rs = c->rs;
@@ -1042,8 +1125,8 @@ int dflash_sync_round(dflash_ctx* c, int32_t* tokens_host, int32_t* n_host) {
   if (!tokens_host || !n_host) return fail(c->err, DFLASH_EINVAL, "tokens_host or n_host is NULL");
   if (c->capturing) return fail(c->err, DFLASH_ESTATE, "dflash_sync_round while capturing");
   if (!c->last_tokens || !c->last_n) return fail(c->err, DFLASH_ESTATE, "no verify yet");
-  CK(c->err, cudaMemcpyAsync(n_host, c->last_n, sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream));
-  CK(c->err, cudaMemcpyAsync(tokens_host, c->last_tokens, sizeof(int32_t) * c->last_tokens_block,
+  CK(c->err, cudaMemcpyAsync(n_host, c->last_n, sizeof(int32_t) * c->nseq, cudaMemcpyDeviceToHost, c->stream));
+  CK(c->err, cudaMemcpyAsync(tokens_host, c->last_tokens, sizeof(int32_t) * c->last_tokens_block * c->nseq,
                              cudaMemcpyDeviceToHost, c->stream));
   CK(c->err, cudaStreamSynchronize(c->stream));
   return DFLASH_OK;
@@ -1058,9 +1141,9 @@ int dflash_append_block(dflash_ctx* c, const void* resid, int32_t block) {
   if (c->appended_block) return fail(c->err, DFLASH_ESTATE, "append without a commit of the previous append");
   int rc = ensure_room(c, block);
   if (rc) return rc;
-  rc = context_rows_to_ring(c, resid, block, c->app_f, c->app_c, c->app_kv, c->app_rope, 1, 0);
+  rc = context_rows_to_ring(c, resid, block * c->nseq, c->app_f, c->app_c, c->app_kv, c->app_rope, 1, 0);
   if (rc) return rc;
-  CK(c->err, launch_ring_advance(c->ring->st, block, 0, c->stream));
+  CK(c->err, launch_ring_advance(c->ring->st, block, 0, c->stream, c->nseq));
   c->appended_block = block;
   c->ring->host_appended = block;
   c->ring->pos_hi += block;
@@ -1074,7 +1157,7 @@ int dflash_commit(dflash_ctx* c, int32_t keep) {
     return fail(c->err, DFLASH_EINVAL, "keep %d exceeds the appended block %d", keep, c->appended_block);
   if (keep < 0 && c->last_verify_block != c->appended_block)
     return fail(c->err, DFLASH_ESTATE, "commit(-1) needs a verify at the appended width %d", c->appended_block);
-  CK(c->err, launch_commit(c->rs, c->ring->st, c->appended_block, keep, c->stream));
+  CK(c->err, launch_commit(c->rs, c->ring->st, c->appended_block, keep, c->stream, c->nseq));
   if (keep >= 0) c->ring->pos_hi -= c->appended_block - keep;
   c->appended_block = 0;
   c->last_verify_block = 0;
@@ -1156,6 +1239,7 @@ int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const floa
   if (!c) return DFLASH_EINVAL;
   if (!out) return fail(c->err, DFLASH_EINVAL, "out is NULL");
   if (c->cfg.markov_rank <= 0) return fail(c->err, DFLASH_ERANGE, "the config has no Markov head");
+  if (c->nseq > 1) return fail(c->err, DFLASH_EINVAL, "the Markov chain takes one sequence");
   if (anchor < 0 || anchor >= c->V)
     return fail(c->err, DFLASH_ERANGE, "anchor %d outside [0, vocab=%d)", anchor, c->V);
   if (gamma < 1 || gamma > c->cfg.max_block)
@@ -1172,7 +1256,7 @@ int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const floa
 int dflash_get_hidden(dflash_ctx* c, void* out) {
   if (!c || !out) return DFLASH_EINVAL;
   if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
-  const int rows = c->cfg.kind == DFLASH_KIND_DSPARK ? c->last_draft_block - 1 : c->last_draft_block;
+  const int rows = (c->cfg.kind == DFLASH_KIND_DSPARK ? c->last_draft_block - 1 : c->last_draft_block) * c->nseq;
   CK(c->err, cudaMemcpyAsync(out, c->xf, (size_t)rows * c->H * c->esz, cudaMemcpyDeviceToDevice, c->stream));
   CK(c->err, cudaStreamSynchronize(c->stream));
   return DFLASH_OK;
@@ -1181,7 +1265,7 @@ int dflash_get_hidden(dflash_ctx* c, void* out) {
 int dflash_get_draft_max_logit(dflash_ctx* c, float* out) {
   if (!c || !out) return DFLASH_EINVAL;
   if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
-  CK(c->err, cudaMemcpyAsync(out, c->maxv, sizeof(float) * (c->last_draft_block - 1),
+  CK(c->err, cudaMemcpyAsync(out, c->maxv, sizeof(float) * (c->last_draft_block - 1) * c->nseq,
                              cudaMemcpyDeviceToDevice, c->stream));
   CK(c->err, cudaStreamSynchronize(c->stream));
   return DFLASH_OK;
@@ -1190,19 +1274,22 @@ int dflash_get_draft_max_logit(dflash_ctx* c, float* out) {
 int dflash_get_backbone_ids(dflash_ctx* c, int32_t* out) {
   if (!c || !out) return DFLASH_EINVAL;
   if (!c->last_draft_block) return fail(c->err, DFLASH_ESTATE, "no draft yet");
-  CK(c->err, cudaMemcpyAsync(out, c->backbone_ids, sizeof(int) * (c->last_draft_block - 1),
+  CK(c->err, cudaMemcpyAsync(out, c->backbone_ids, sizeof(int) * (c->last_draft_block - 1) * c->nseq,
                              cudaMemcpyDeviceToDevice, c->stream));
   CK(c->err, cudaStreamSynchronize(c->stream));
   return DFLASH_OK;
 }
 
-int dflash_get_state(dflash_ctx* c, dflash_round_state* out) {
+int dflash_get_state(dflash_ctx* c, dflash_round_state* out) { return dflash_get_state_seq(c, 0, out); }
+
+int dflash_get_state_seq(dflash_ctx* c, int32_t seq, dflash_round_state* out) {
   if (!c || !out) return DFLASH_EINVAL;
+  if (seq < 0 || seq >= c->nseq) return fail(c->err, DFLASH_ERANGE, "seq %d outside [0, %d)", seq, c->nseq);
   RoundState rs;
   RingState ring;
   CK(c->err, cudaStreamSynchronize(c->stream));
-  CK(c->err, cudaMemcpy(&rs, c->rs, sizeof rs, cudaMemcpyDeviceToHost));
-  CK(c->err, cudaMemcpy(&ring, c->ring->st, sizeof ring, cudaMemcpyDeviceToHost));
+  CK(c->err, cudaMemcpy(&rs, c->rs + seq, sizeof rs, cudaMemcpyDeviceToHost));
+  CK(c->err, cudaMemcpy(&ring, c->ring->st + seq, sizeof ring, cudaMemcpyDeviceToHost));
   out->position = ring.offset;
   out->anchor = rs.anchor;
   out->last_n = rs.n;
@@ -1213,11 +1300,14 @@ int dflash_get_state(dflash_ctx* c, dflash_round_state* out) {
   return DFLASH_OK;
 }
 
-int dflash_get_stats(dflash_ctx* c, dflash_stats* out) {
+int dflash_get_stats(dflash_ctx* c, dflash_stats* out) { return dflash_get_stats_seq(c, 0, out); }
+
+int dflash_get_stats_seq(dflash_ctx* c, int32_t seq, dflash_stats* out) {
   if (!c || !out) return DFLASH_EINVAL;
+  if (seq < 0 || seq >= c->nseq) return fail(c->err, DFLASH_ERANGE, "seq %d outside [0, %d)", seq, c->nseq);
   RoundState rs;
   CK(c->err, cudaStreamSynchronize(c->stream));
-  CK(c->err, cudaMemcpy(&rs, c->rs, sizeof rs, cudaMemcpyDeviceToHost));
+  CK(c->err, cudaMemcpy(&rs, c->rs + seq, sizeof rs, cudaMemcpyDeviceToHost));
   out->rounds = rs.rounds;
   out->draft_n = rs.proposed;
   out->accepted = rs.accepted;
@@ -1227,15 +1317,21 @@ int dflash_get_stats(dflash_ctx* c, dflash_stats* out) {
 
 int dflash_reset_stats(dflash_ctx* c) {
   if (!c) return DFLASH_EINVAL;
-  CK(c->err, cudaMemsetAsync(&c->rs->rounds, 0, 4 * sizeof(long long), c->stream));
+  for (int q = 0; q < c->nseq; ++q)
+    CK(c->err, cudaMemsetAsync(&c->rs[q].rounds, 0, 4 * sizeof(long long), c->stream));
   return DFLASH_OK;
 }
 
-int dflash_ring(dflash_ctx* c, ring_cache** out) {
+int dflash_ring(dflash_ctx* c, ring_cache** out) { return dflash_ring_seq(c, 0, out); }
+
+int dflash_ring_seq(dflash_ctx* c, int32_t seq, ring_cache** out) {
   if (!c || !out) return DFLASH_EINVAL;
-  *out = c->ring;
+  if (seq < 0 || seq >= c->nseq) return fail(c->err, DFLASH_ERANGE, "seq %d outside [0, %d)", seq, c->nseq);
+  *out = c->nseq == 1 ? c->ring : c->views[seq];
   return DFLASH_OK;
 }
+
+int dflash_batch_size(const dflash_ctx* c) { return c ? c->nseq : 0; }
 
 int dflash_capture_begin(dflash_ctx* c) {
   if (!c) return DFLASH_EINVAL;
@@ -1385,6 +1481,7 @@ int dflash_synth_target(dflash_ctx* c, const void* logit_pool, const void* plant
   a.n_logit = n_logit_pool; a.n_coin = n_coin_rows; a.n_resid = n_resid_pool;
   a.block_max = block_max; a.block = block; a.V = c->V; a.kin = c->kin;
   a.d = draft_ids; a.logits_out = logits_out; a.resid_out = resid_out; a.rs = c->rs;
+  a.nseq = c->nseq;
   CK(c->err, launch_synth_target(c->dt, a, c->stream));
   return DFLASH_OK;
 }

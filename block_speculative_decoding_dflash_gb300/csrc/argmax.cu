@@ -176,6 +176,19 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
   __shared__ float sv[8];
   __shared__ int si[8];
   __shared__ int t_s[kMaxVerifyRows];
+  // sequence blockIdx.z of a batch: its own logits, drafts, outputs, state,
+  // partials and ticket
+  {
+    const int sq = blockIdx.z;
+    a.L = static_cast<const char*>(a.L) + (size_t)sq * a.B * a.V * sizeof(T);
+    a.d += (size_t)sq * (a.B - 1);
+    a.tokens += (size_t)sq * a.B;
+    a.n += sq;
+    a.rs += sq;
+    a.part_v += (size_t)sq * a.B * a.chunks;
+    a.part_i += (size_t)sq * a.B * a.chunks;
+    a.counter += sq;
+  }
   const int i = blockIdx.y, c = blockIdx.x;
   const T* row = reinterpret_cast<const T*>(a.L) + (size_t)i * a.V;
   const int v0 = c * kVerifyChunk;
@@ -328,6 +341,28 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
 
 }  // namespace
 
+// Batch read-out: ids of every block row [nseq][rows] -> draft ids [nseq]
+// [rows - read0] (and the same for a second copy and the maxima).
+__global__ void split_ids_kernel(const int* ids_all, const float* maxv_all, int rows, int read0, int nseq,
+                                 int* ids, int* ids2, float* maxv) {
+  pdl_enter();
+  const int per = rows - read0;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= nseq * per) return;
+  const int src = (e / per) * rows + read0 + e % per;
+  ids[e] = ids_all[src];
+  if (ids2) ids2[e] = ids_all[src];
+  if (maxv) maxv[e] = maxv_all[src];
+}
+
+cudaError_t launch_split_ids(const int* ids_all, const float* maxv_all, int rows, int read0, int nseq, int* ids,
+                             int* ids2, float* maxv, cudaStream_t st) {
+  const int n = nseq * (rows - read0);
+  launch_pdl(split_ids_kernel, dim3((n + 127) / 128), dim3(128), 0, st, ids_all, maxv_all, rows, read0, nseq, ids,
+             ids2, maxv);
+  return cudaGetLastError();
+}
+
 int lmhead_grid(int V) {
   const int g = (V + 63) / 64;
   return g < 608 ? g : 608;
@@ -356,7 +391,7 @@ cudaError_t launch_lmhead_argmax(int dtype, const LmHeadArgs& a, cudaStream_t st
 }
 
 cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st) {
-  dim3 grid(a.chunks, a.B);
+  dim3 grid(a.chunks, a.B, a.nseq > 1 ? a.nseq : 1);
   if (dtype) launch_pdl(verify_kernel<bf16>, dim3(grid), dim3(256), 0, st, a);
   else launch_pdl(verify_kernel<float>, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError();

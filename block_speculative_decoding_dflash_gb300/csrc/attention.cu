@@ -24,6 +24,7 @@ constexpr int kWarps = 8;
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(AttnArgs a, int nsplit) {
   pdl_enter();
+  attn_select_seq(a, blockIdx.z, nsplit, sizeof(T), sizeof(T), a.hd + 2);
   extern __shared__ float smem[];
   const int hd = a.hd, hdp = hd + 1;
   float* Ks = smem;                       // [kKS][hd+1]
@@ -128,8 +129,10 @@ __global__ void attn_combine_kernel(AttnArgs a, int nsplit) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
   const int Qn = a.rows * G;
-  const int item = blockIdx.x * (blockDim.x >> 5) + warp;   // over nkv * Qn
-  if (item >= a.nkv * Qn) return;
+  int item = blockIdx.x * (blockDim.x >> 5) + warp;         // over nseq * nkv * Qn
+  if (item >= (a.nseq > 1 ? a.nseq : 1) * a.nkv * Qn) return;
+  attn_select_seq(a, item / (a.nkv * Qn), nsplit, sizeof(T), sizeof(T), a.hd + 2);
+  item %= a.nkv * Qn;
   const int g = item / Qn, qi = item % Qn;
   const int r = qi / G, h = g * G + qi % G;
   const int hd = a.hd;
@@ -180,12 +183,13 @@ cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st) {
   if (attention_mma_ok(dtype, a.hd)) return launch_attention_mma(a, st);
   const int nsplit = num_splits(a.rows, a.max_ctx);
   const size_t smem = partial_smem(a.hd);
-  dim3 grid(nsplit, a.nkv);
+  const int ns = a.nseq > 1 ? a.nseq : 1;
+  dim3 grid(nsplit, a.nkv, ns);
   if (dtype) launch_pdl(attn_partial_kernel<bf16>, dim3(grid), dim3(kWarps * 32), smem, st, a, nsplit);
   else launch_pdl(attn_partial_kernel<float>, dim3(grid), dim3(kWarps * 32), smem, st, a, nsplit);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int items = a.nkv * a.rows * (a.nq / a.nkv);
+  const int items = ns * a.nkv * a.rows * (a.nq / a.nkv);
   const int cgrid = (items + 3) / 4;
   if (dtype) launch_pdl(attn_combine_kernel<bf16>, dim3(cgrid), dim3(128), 0, st, a, nsplit);
   else launch_pdl(attn_combine_kernel<float>, dim3(cgrid), dim3(128), 0, st, a, nsplit);

@@ -2,12 +2,13 @@
 // head_dim 128, on tensor cores, one CTA per (split of kKeys = 128 keys, kv
 // head g); the queries of g are the block rows x its G query heads.
 //
-// One 16-query tile (attn_mma_kernel, mma.sync m16n8k16, fp32 accumulate):
-// the 8 warps each own 16 keys: S = Q K^T for the warp's keys (mask |q - k|
-// <= W by absolute positions), the warp's online-softmax partial (max, sum,
-// P V, with P as a high and a low bf16 part), a merge of the 8 warps in shared memory in warp order, and the CTA's
-// partial written to global scratch. Two to four tiles: attn_tc_kernel
-// (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
+// One 16-query tile at a time (attn_mma_kernel, mma.sync m16n8k16, fp32
+// accumulate): each of the 8 warps scores the tile against 16 keys (S = Q
+// K^T, mask |q - k| <= W by absolute positions) into shared memory; each warp
+// then takes two query rows' softmax over the split (P as a high and a low
+// bf16 part); each warp finally computes P V for 16 of the 128 output dims
+// over all the split's keys and writes them to the CTA's partial. Two to
+// four tiles: attn_tc_kernel (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
 // merges the splits in split order and writes the bf16 output; nothing waits
 // on another CTA and the result is deterministic.
 //
@@ -46,15 +47,15 @@ struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
   bf16 v[kKeys][kHd + kPad];
   bf16 q[kQChunk][kHd + kPad];            // up to 64 query rows, loaded with K/V
-  float o[kWarps][16][kHd];                // per-warp unnormalised P V
-  float m[kWarps][16];
-  float l[kWarps][16];
-  float f[kWarps][16];                     // exp(m_w - M) per (warp, row)
-  float L[16];                             // merged sum per row
-  float M[16];                             // merged max per row
+  float s[16][kKeys + 4];                  // scaled, masked scores of one query tile
+  bf16 ph[16][kKeys + kPad];               // P = exp(S - M): high bf16 part
+  bf16 pl[16][kKeys + kPad];               //                 low bf16 part
+  float rm[16];                            // per query row: maximum score
+  float rl[16];                            //                sum of P
 };
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
+  attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   // (Measured: 3 us per draft faster at 4 block rows; the tensor-core kernel
   // used at 16 gained nothing from the same hint and does not issue it.)
@@ -163,24 +164,22 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
         __syncthreads();
       }
     }
-    float m_row[2] = {-INFINITY, -INFINITY}, l_row[2] = {0.f, 0.f};
-    float o[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-
-    if (j0 < nk) {
-      // S = Q K^T over the warp's 16 keys (two 8-key n-tiles).
+    // S = Q K^T: warp w scores the 16 queries of this tile against its 16
+    // keys (two 8-key n-tiles), masks |q - k| <= W by absolute positions and
+    // scales; the scores go to shared memory.
+    {
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (j0 < nk) {
 #pragma unroll
-      for (int ks = 0; ks < kHd / 16; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        const int mi = lane >> 3;
-        ldsm_x4(&S.q[qr + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
-        ldsm_x4(&S.k[warp * 16 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
-        mma16816(sc[0], a0, a1, a2, a3, b0, b1);
-        mma16816(sc[1], a0, a1, a2, a3, b2, b3);
+        for (int ks = 0; ks < kHd / 16; ++ks) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          const int mi = lane >> 3;
+          ldsm_x4(&S.q[qr + (lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], a0, a1, a2, a3);
+          ldsm_x4(&S.k[warp * 16 + (mi >> 1) * 8 + (lane & 7)][ks * 16 + (mi & 1) * 8], b0, b1, b2, b3);
+          mma16816(sc[0], a0, a1, a2, a3, b0, b1);
+          mma16816(sc[1], a0, a1, a2, a3, b2, b3);
+        }
       }
-      // mask, scale, per-row max over the warp's keys
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int qi = qt * 16 + grp + hr * 8;
@@ -189,91 +188,70 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int kj = j0 + warp * 16 + nt * 8 + tig * 2 + c;
+            const int kk = warp * 16 + nt * 8 + tig * 2 + c;
+            const int kj = j0 + kk;
             bool vis = qi < Qn && kj < nk;
             if (vis && a.window > 0) {
               const long long kpos = kj < nctx ? kstart + kj : p + (kj - nctx);
               const long long d = qpos > kpos ? qpos - kpos : kpos - qpos;
               vis = d <= a.window;
             }
-            float& v = sc[nt][hr * 2 + c];
-            v = vis ? v * scale : -INFINITY;
-            m_row[hr] = fmaxf(m_row[hr], v);
+            S.s[grp + hr * 8][kk] = vis ? sc[nt][hr * 2 + c] * scale : -INFINITY;
           }
-        m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 1));
-        m_row[hr] = fmaxf(m_row[hr], __shfl_xor_sync(0xffffffffu, m_row[hr], 2));
       }
-      // P = exp(S - m) as a high and a low bf16 part, row sums, O = P V
-      uint32_t pa[4], pl[4];
+    }
+    __syncthreads();
+    // Softmax rows: warp w takes query rows 2w and 2w + 1, four keys a lane;
+    // P is kept as a high and a low bf16 part (about 16 significant bits).
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        float pv[2][2];
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = warp * 2 + rr;
+      const float4 v4 = *reinterpret_cast<const float4*>(&S.s[r][lane * 4]);
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      mx = warp_max(mx);
+      float pe[4], l = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const float v = sc[nt][hr * 2 + c];
-            pv[nt][c] = (m_row[hr] == -INFINITY || v == -INFINITY) ? 0.f : expf(v - m_row[hr]);
-            l_row[hr] += pv[nt][c];
-          }
-        pa[hr] = pack_bf16(pv[0][0], pv[0][1]);        // keys 0..7 of this row
-        pa[2 + hr] = pack_bf16(pv[1][0], pv[1][1]);    // keys 8..15
-        pl[hr] = pack_bf16_residue(pv[0][0], pv[0][1]);
-        pl[2 + hr] = pack_bf16_residue(pv[1][0], pv[1][1]);
-        l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 1);
-        l_row[hr] += __shfl_xor_sync(0xffffffffu, l_row[hr], 2);
+      for (int e = 0; e < 4; ++e) {
+        pe[e] = (mx == -INFINITY || v[e] == -INFINITY) ? 0.f : expf(v[e] - mx);
+        l += pe[e];
       }
+      l = warp_sum(l);
+      *reinterpret_cast<uint2*>(&S.ph[r][lane * 4]) = make_uint2(pack_bf16(pe[0], pe[1]), pack_bf16(pe[2], pe[3]));
+      *reinterpret_cast<uint2*>(&S.pl[r][lane * 4]) =
+          make_uint2(pack_bf16_residue(pe[0], pe[1]), pack_bf16_residue(pe[2], pe[3]));
+      if (lane == 0) { S.rm[r] = mx; S.rl[r] = l; }
+    }
+    __syncthreads();
+    // O = P V: warp w owns output dims 16w .. 16w + 15 over all keys of the
+    // split (eight 16-key steps, high and low parts of P)
+    float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (j0 < nk) {
 #pragma unroll
-      for (int dt = 0; dt < kHd / 16; ++dt) {
-        uint32_t b0, b1, b2, b3;
+      for (int ks = 0; ks < kKeys / 16; ++ks) {
+        uint32_t h0, h1, h2, h3, l0, l1, l2, l3, b0, b1, b2, b3;
         const int mi = lane >> 3;
-        ldsm_x4_t(&S.v[warp * 16 + (mi & 1) * 8 + (lane & 7)][dt * 16 + (mi >> 1) * 8], b0, b1, b2, b3);
-        mma16816(o[dt * 2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-        mma16816(o[dt * 2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-        mma16816(o[dt * 2], pl[0], pl[1], pl[2], pl[3], b0, b1);
-        mma16816(o[dt * 2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+        ldsm_x4(&S.ph[(lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], h0, h1, h2, h3);
+        ldsm_x4(&S.pl[(lane & 7) + (mi & 1) * 8][ks * 16 + (mi >> 1) * 8], l0, l1, l2, l3);
+        ldsm_x4_t(&S.v[ks * 16 + (mi & 1) * 8 + (lane & 7)][warp * 16 + (mi >> 1) * 8], b0, b1, b2, b3);
+        mma16816(o[0], h0, h1, h2, h3, b0, b1);
+        mma16816(o[1], h0, h1, h2, h3, b2, b3);
+        mma16816(o[0], l0, l1, l2, l3, b0, b1);
+        mma16816(o[1], l0, l1, l2, l3, b2, b3);
       }
     }
-    // publish the warp's partial, then merge the 8 warps in warp order
+    // the split's partial: unnormalised O, then the row's maximum and sum
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        S.o[warp][grp + hr * 8][nt * 8 + tig * 2] = o[nt][hr * 2];
-        S.o[warp][grp + hr * 8][nt * 8 + tig * 2 + 1] = o[nt][hr * 2 + 1];
-      }
-    if (tig == 0) {
-      S.m[warp][grp] = m_row[0]; S.m[warp][grp + 8] = m_row[1];
-      S.l[warp][grp] = l_row[0]; S.l[warp][grp + 8] = l_row[1];
-    }
-    __syncthreads();
-    // per-row merge weights of the 8 warps: one thread per (row, warp)
-    if (threadIdx.x < 16 * kWarps) {
-      const int r = threadIdx.x >> 3, w = threadIdx.x & 7;
-      float M = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < kWarps; ++x) M = fmaxf(M, S.m[x][r]);
-      const float mw = S.m[w][r];
-      const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : expf(mw - M);
-      S.f[w][r] = f;
-      float lw = f * S.l[w][r];
-#pragma unroll
-      for (int o2 = 4; o2 > 0; o2 >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o2);
-      if (w == 0) { S.L[r] = lw; S.M[r] = M; }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < 16 * kHd; e += blockDim.x) {
-      const int r = e / kHd, d = e % kHd;
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = grp + hr * 8;
       const int qi = qt * 16 + r;
       if (qi >= Qn) continue;
-      float O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) O = fmaf(S.f[w][r], S.o[w][r][d], O);
       float* out = part + (size_t)qi * pstride;
-      out[d] = O;
-      if (d == 0) { out[kHd] = S.M[r]; out[kHd + 1] = S.L[r]; }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        *reinterpret_cast<float2*>(out + warp * 16 + nt * 8 + tig * 2) = make_float2(o[nt][hr * 2], o[nt][hr * 2 + 1]);
+      if (warp == 0 && tig == 0) { out[kHd] = S.rm[r]; out[kHd + 1] = S.rl[r]; }
     }
-    __syncthreads();
   }
   if (threadIdx.x == 0) ktrace_mark(a.trace, 2);
 }
@@ -287,14 +265,20 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
   const int Qn = a.rows * G;
+  const int ns = a.nseq > 1 ? a.nseq : 1;
   const int item = blockIdx.x * 4 + warp;
-  if (item < a.nkv * Qn)
-    attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, item / Qn, item % Qn,
+  float* zero_acc = a.zero_acc;
+  const int zero_n = a.zero_n;
+  if (item < ns * a.nkv * Qn) {
+    attn_select_seq(a, item / (a.nkv * Qn), nsplit, 2, 2, kPartStride);
+    const int it = item % (a.nkv * Qn);
+    attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, it / Qn, it % Qn,
                       reinterpret_cast<bf16*>(a.out), a.ldo, lane);
+  }
   // every attention CTA is done with the QKV GEMM's fp32 sums: clear them
-  if (a.zero_acc)
-    for (int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4; e < a.zero_n; e += gridDim.x * blockDim.x * 4)
-      *reinterpret_cast<float4*>(a.zero_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (zero_acc)
+    for (int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4; e < zero_n; e += gridDim.x * blockDim.x * 4)
+      *reinterpret_cast<float4*>(zero_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
 }
 
@@ -336,6 +320,7 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
 }
 
 __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
+  attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
   if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
@@ -622,7 +607,8 @@ cudaError_t init_attention_mma_attrs() {
 
 cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
   const int nsplit = attention_mma_splits(a.rows, a.max_ctx);
-  dim3 grid(nsplit, a.nkv);
+  const int ns = a.nseq > 1 ? a.nseq : 1;
+  dim3 grid(nsplit, a.nkv, ns);
   const int Qn = a.rows * (a.nq / a.nkv);
   // Two to four 16-query tiles per kv head: the tensor-core kernel (A/B on
   // one GB300 at 64 queries per kv head: 16 us per draft faster than an
@@ -635,7 +621,7 @@ cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
     cudaError_t e = launch_pdl(attn_mma_kernel, grid, dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit);
     if (e != cudaSuccess) return e;
   }
-  const int items = a.nkv * a.rows * (a.nq / a.nkv);
+  const int items = ns * a.nkv * a.rows * (a.nq / a.nkv);
   return launch_pdl(attn_mma_combine_kernel, dim3((items + 3) / 4), dim3(128), 0, st, a, nsplit);
 }
 

@@ -121,11 +121,11 @@ cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab,
                                RoundState* rs, int mask_id, int rows, void* x,
                                const RingState* ring, const double* inv_freq,
                                int half, int tab_rows, float2* rope, int anchor_host,
-                               long long expect_pos, cudaStream_t st);
+                               long long expect_pos, cudaStream_t st, int nseq = 1);
 // RoPE table at positions base + r, base = ring->offset when ring != NULL,
 // else pos0.
 cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,
-                              long long pos0, int rows, float2* rope, cudaStream_t st);
+                              long long pos0, int rows, float2* rope, cudaStream_t st, int nseq = 1);
 cudaError_t launch_rmsnorm(int dtype, const void* x, int ldx, const void* g,
                            void* y, int ldy, int rows, int H, float eps,
                            cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
@@ -144,24 +144,28 @@ cudaError_t launch_swiglu_finish(float* acc, int ldacc, void* s, int lds, int ro
 // bf16, head_dim 128: finishes the append's K/V GEMM (kEpiRed over the
 // [K_l | V_l] column blocks of L layers, acc row stride ldacc): rounds, k-norm
 // (gain kgain[l]) + RoPE (rope[r][64]) for K, stores K and V of row r at
-// position ring->offset + r, clears the sums.
+// position ring[s].offset + r % rows_per_seq of sequence s = r / rows_per_seq
+// (its ring rows seq_kv elements after sequence s - 1's), clears the sums.
 cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nkv,
                                   const void* const* kgain, float eps, const float2* rope, int neox,
                                   void* ring_k, void* ring_v, long long cap, int append_only,
-                                  RingState* ring, cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
+                                  RingState* ring, cudaStream_t st, KTrace trace, int rows_per_seq,
+                                  long long seq_kv);
 // In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
 cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
                                   int heads, int hd, const void* g, float eps,
                                   const float2* rope, int neox, cudaStream_t st);
 // kv[rows, 2*nkv*hd] = K heads then V heads: K -> head norm + RoPE -> ring K,
-// V -> ring V, at positions (use_dev ? ring->offset : pos_host) + r.
+// V -> ring V, at positions (use_dev ? ring->offset : pos_host) + r; row r
+// belongs to sequence r / rows_per_seq (its ring state ring[s], its rows
+// seq_kv elements on).
 // append_only: refuse (and flag) positions at or past base + cap.
 cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows,
                               int nkv, int hd, const void* kg, float eps,
                               const float2* rope, int neox, void* ring_k,
                               void* ring_v, long long cap, int append_only,
                               RingState* ring, int use_dev, long long pos_host,
-                              cudaStream_t st);
+                              cudaStream_t st, int rows_per_seq, long long seq_kv);
 
 // ---- attention ---------------------------------------------------------------------
 struct AttnArgs {
@@ -190,7 +194,30 @@ struct AttnArgs {
   // kernel then clears those sums: zero_acc [zero_n] floats.
   int qkv_f32;
   float* zero_acc; int zero_n;
+  // Batch of nseq sequences (0 or 1: one): sequence s (blockIdx.z) has its
+  // own ring state ring[s], ring rows seq_kv elements after sequence s - 1's,
+  // its rows s * rows .. of q, kb, vb, out and the RoPE table, and its own
+  // partials.
+  int nseq;
+  long long seq_kv;
 };
+// Points a's per-sequence operands at sequence s: q, kb, vb hold elements of
+// qkv_esz bytes, the ring and out of esz bytes; partial rows are part_stride
+// floats per query.
+__device__ __forceinline__ void attn_select_seq(AttnArgs& a, int s, int nsplit, int qkv_esz, int esz,
+                                                int part_stride) {
+  if (s == 0) return;
+  const int Qn = a.rows * (a.nq / a.nkv);
+  a.ring += s;
+  a.q = static_cast<const char*>(a.q) + (size_t)s * a.rows * a.ldq * qkv_esz;
+  a.kb = static_cast<const char*>(a.kb) + (size_t)s * a.rows * a.ldkv * qkv_esz;
+  a.vb = static_cast<const char*>(a.vb) + (size_t)s * a.rows * a.ldkv * qkv_esz;
+  a.ring_k = static_cast<const char*>(a.ring_k) + (size_t)s * a.seq_kv * esz;
+  a.ring_v = static_cast<const char*>(a.ring_v) + (size_t)s * a.seq_kv * esz;
+  a.out = static_cast<char*>(a.out) + (size_t)s * a.rows * a.ldo * esz;
+  if (a.rope) a.rope += (size_t)s * a.rows * (a.hd / 2);
+  a.partial += (size_t)s * a.nkv * nsplit * Qn * part_stride;
+}
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);
 // bf16, head_dim 128: tensor-core attention with the split merge fused in.
 bool attention_mma_ok(int dtype, int hd);
@@ -229,16 +256,23 @@ struct VerifyArgs {
   float* part_v; int* part_i;  // scratch [B * chunks]
   unsigned* counter;
   int chunks;
+  int nseq;                    // batch (0 or 1: one): sequence s at L + s [B, V], d + s [B-1],
+                               // tokens + s [B], n + s, rs + s, partials + s [B * chunks],
+                               // counter + s
 };
 cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st);
+// Batch read-out: ids [nseq][rows - read0] = ids_all[s * rows + read0 + i]
+// (and a second copy ids2, and maxv from maxv_all, when not NULL).
+cudaError_t launch_split_ids(const int* ids_all, const float* maxv_all, int rows, int read0, int nseq, int* ids,
+                             int* ids2, float* maxv, cudaStream_t st);
 int verify_chunks(int V);
 // Text returned by dflash_last_error(NULL).
 void set_global_error(const char* msg);
 
 cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
-                          cudaStream_t st);
+                          cudaStream_t st, int nseq = 1);
 // mode 0: append d rows; 1: trim d rows; 2: advance d committed rows.
-cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st);
+cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st, int nseq = 1);
 cudaError_t launch_ring_reset(RingState* ring, long long base, cudaStream_t st);
 cudaError_t launch_set_anchor(RoundState* rs, int anchor, cudaStream_t st);
 // Copies rows [L, n, nkv, hd] into ring slots at offset + r, then advances.
@@ -295,6 +329,8 @@ struct SynthArgs {
   void* logits_out; void* resid_out;
   const RoundState* rs;
   int vec;                     // set by the launcher: rows allow 16-byte copies
+  int nseq;                    // batch: sequence s uses rs[s], d + s (block-1), outputs + s block
+                               // rows, and pool entry (round * nseq + s)
 };
 cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st);
 

@@ -24,9 +24,15 @@ __global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
                                    int mask_id, int rows, T* x,
                                    const RingState* ring, const double* inv_freq,
                                    int half, int tab_rows, float2* rope,
-                                   int anchor_host, long long expect_pos) {
+                                   int anchor_host, long long expect_pos, int nseq) {
   pdl_enter();
-  const int r = blockIdx.x;
+  // sequence s of a batch takes rows s * rows .. and table rows s * tab_rows ..
+  const int per = gridDim.x / nseq;
+  const int sq = blockIdx.x / per, r = blockIdx.x % per;
+  rs += sq;
+  ring += sq;
+  x += (size_t)sq * rows * H;
+  rope += (size_t)sq * tab_rows * half;
   if (r == 0 && threadIdx.x == 0) {
     // A host-given anchor replaces the device-resident one (the Markov chain
     // that may follow seeds from it); a host-given position is checked
@@ -54,11 +60,11 @@ __global__ void embed_block_kernel(const T* E, int H, int vocab, RoundState* rs,
 __global__ void rope_table_kernel(const double* inv_freq, int half, const RingState* ring,
                                   long long pos0, int rows, float2* rope) {
   pdl_enter();
-  const int r = blockIdx.x;
-  if (r >= rows) return;
-  const long long base = ring ? ring->offset : pos0;
+  // table row blockIdx.x is row r of sequence s (rows per sequence)
+  const int sq = blockIdx.x / rows, r = blockIdx.x % rows;
+  const long long base = ring ? ring[sq].offset : pos0;
   for (int i = threadIdx.x; i < half; i += blockDim.x)
-    rope[(size_t)r * half + i] = rope_entry(inv_freq, i, base + r);
+    rope[(size_t)blockIdx.x * half + i] = rope_entry(inv_freq, i, base + r);
 }
 
 template <typename T>
@@ -291,14 +297,19 @@ __global__ void __launch_bounds__(128) kv_to_ring_kernel(const T* kv, int ld, in
                                                          int neox, T* ring_k, T* ring_v,
                                                          long long cap, int append_only,
                                                          RingState* ring, int use_dev,
-                                                         long long pos_host) {
+                                                         long long pos_host, int rows_per_seq,
+                                                         long long seq_kv) {
   pdl_enter();
   __shared__ float sm[4][kMaxHd];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x * 4 + warp;
   if (item >= rows * nkv) return;
   const int r = item / nkv, h = item % nkv;
-  const long long pos = (use_dev ? ring->offset : pos_host) + r;
+  const int sq = r / rows_per_seq;
+  ring += sq;
+  ring_k += (size_t)sq * seq_kv;
+  ring_v += (size_t)sq * seq_kv;
+  const long long pos = (use_dev ? ring->offset : pos_host) + r % rows_per_seq;
   if (append_only && pos - ring->base >= cap) {
     if (lane == 0) atomicOr(&ring->error, kErrFull);
     return;
@@ -322,7 +333,8 @@ __global__ void __launch_bounds__(128) kv_acc_to_ring_kernel(float* acc, int lda
                                                             int nkv, const void* const* kgain, float eps,
                                                             const float2* rope, int neox, bf16* ring_k,
                                                             bf16* ring_v, long long cap, int append_only,
-                                                            RingState* ring) {
+                                                            RingState* ring, int rows_per_seq,
+                                                            long long seq_kv) {
   pdl_enter();
   __shared__ float sm[4][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -337,7 +349,12 @@ __global__ void __launch_bounds__(128) kv_acc_to_ring_kernel(float* acc, int lda
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   reinterpret_cast<float4*>(kacc)[lane] = z;
   reinterpret_cast<float4*>(vacc)[lane] = z;
-  const long long pos = ring->offset + r;
+  // row r of the batch is row r % rows_per_seq of sequence r / rows_per_seq
+  const int sq = r / rows_per_seq;
+  ring += sq;
+  ring_k += (size_t)sq * seq_kv;
+  ring_v += (size_t)sq * seq_kv;
+  const long long pos = ring->offset + r % rows_per_seq;
   if (append_only && pos - ring->base >= cap) {
     if (lane == 0) atomicOr(&ring->error, kErrFull);
     return;
@@ -376,6 +393,7 @@ __global__ void __launch_bounds__(128) kv_acc_to_ring_kernel(float* acc, int lda
 // ---- ring bookkeeping ------------------------------------------------------------
 __global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
   pdl_enter();
+  ring += threadIdx.x;                         // one thread per sequence
   if (mode == 1) {
     ring->offset -= d;
     ring->appended = 0;
@@ -402,6 +420,8 @@ __global__ void set_anchor_kernel(RoundState* rs, int anchor) {
 // advanced by block); keep the first `keep` (keep < 0: the verify's n).
 __global__ void commit_kernel(RoundState* rs, RingState* ring, int block, int keep) {
   pdl_enter();
+  rs += threadIdx.x;                           // one thread per sequence
+  ring += threadIdx.x;
   const int k = keep >= 0 ? keep : rs->n;
   ring->offset -= (block - k);
   ring->appended = 0;
@@ -456,10 +476,15 @@ __global__ void ring_gather_kernel(const T* ring_k, const T* ring_v, int L,
 template <typename T>
 __global__ void synth_target_kernel(SynthArgs a) {
   pdl_enter();
-  const long long r = a.rs->rounds;
+  // sequence blockIdx.z of a batch draws pool entry r * nseq + s
+  const int sq = blockIdx.z;
+  const long long r = a.rs[sq].rounds * a.nseq + sq;
   const int kl = static_cast<int>(r % a.n_logit);
   const int kc = static_cast<int>(r % a.n_coin);
   const int kr = static_cast<int>(r % a.n_resid);
+  a.d += (size_t)sq * (a.block - 1);
+  a.logits_out = static_cast<char*>(a.logits_out) + (size_t)sq * a.block * a.V * sizeof(T);
+  a.resid_out = static_cast<char*>(a.resid_out) + (size_t)sq * a.block * a.kin * sizeof(T);
   // block row i = blockIdx.y; this thread's 8 consecutive elements of the
   // row's logits and of its residual row (16-byte copies when both rows are
   // 16-byte aligned, element by element otherwise)
@@ -504,23 +529,23 @@ __global__ void synth_target_kernel(SynthArgs a) {
 cudaError_t launch_embed_block(int dtype, const void* embed, int H, int vocab, RoundState* rs,
                                int mask_id, int rows, void* x, const RingState* ring,
                                const double* inv_freq, int half, int tab_rows, float2* rope,
-                               int anchor_host, long long expect_pos, cudaStream_t st) {
-  const int grid = rows > tab_rows ? rows : tab_rows;
+                               int anchor_host, long long expect_pos, cudaStream_t st, int nseq) {
+  const int grid = (rows > tab_rows ? rows : tab_rows) * nseq;
   if (dtype)
     launch_pdl(embed_block_kernel<bf16>, dim3(grid), dim3(256), 0, st, (const bf16*)embed, H, vocab, rs, mask_id,
                                                    rows, (bf16*)x, ring, inv_freq, half,
-                                                   tab_rows, rope, anchor_host, expect_pos);
+                                                   tab_rows, rope, anchor_host, expect_pos, nseq);
   else
     launch_pdl(embed_block_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)embed, H, vocab, rs, mask_id,
                                                     rows, (float*)x, ring, inv_freq, half,
-                                                    tab_rows, rope, anchor_host, expect_pos);
+                                                    tab_rows, rope, anchor_host, expect_pos, nseq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(const double* inv_freq, int half, const RingState* ring,
-                              long long pos0, int rows, float2* rope, cudaStream_t st) {
+                              long long pos0, int rows, float2* rope, cudaStream_t st, int nseq) {
   if (rows <= 0) return cudaSuccess;
-  launch_pdl(rope_table_kernel, dim3(rows), dim3(64), 0, st, inv_freq, half, ring, pos0, rows, rope);
+  launch_pdl(rope_table_kernel, dim3(rows * nseq), dim3(64), 0, st, inv_freq, half, ring, pos0, rows, rope);
   return cudaGetLastError();
 }
 
@@ -574,7 +599,7 @@ cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int n
                               const void* kg, float eps, const float2* rope, int neox,
                               void* ring_k, void* ring_v, long long cap, int append_only,
                               RingState* ring, int use_dev, long long pos_host,
-                              cudaStream_t st) {
+                              cudaStream_t st, int rows_per_seq, long long seq_kv) {
   const int items = rows * nkv;
   if (items <= 0) return cudaSuccess;
   const int grid = (items + 3) / 4;
@@ -582,36 +607,37 @@ cudaError_t launch_kv_to_ring(int dtype, const void* kv, int ld, int rows, int n
     launch_pdl(kv_to_ring_kernel<bf16>, dim3(grid), dim3(128), 0, st, (const bf16*)kv, ld, rows, nkv, hd,
                                                   (const bf16*)kg, eps, rope, neox,
                                                   (bf16*)ring_k, (bf16*)ring_v, cap,
-                                                  append_only, ring, use_dev, pos_host);
+                                                  append_only, ring, use_dev, pos_host, rows_per_seq, seq_kv);
   else
     launch_pdl(kv_to_ring_kernel<float>, dim3(grid), dim3(128), 0, st, (const float*)kv, ld, rows, nkv, hd,
                                                    (const float*)kg, eps, rope, neox,
                                                    (float*)ring_k, (float*)ring_v, cap,
-                                                   append_only, ring, use_dev, pos_host);
+                                                   append_only, ring, use_dev, pos_host, rows_per_seq, seq_kv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nkv,
                                   const void* const* kgain, float eps, const float2* rope, int neox,
                                   void* ring_k, void* ring_v, long long cap, int append_only,
-                                  RingState* ring, cudaStream_t st, KTrace tr) {
+                                  RingState* ring, cudaStream_t st, KTrace tr, int rows_per_seq,
+                                  long long seq_kv) {
   (void)tr;
   const int items = rows * L * nkv;
   if (items <= 0) return cudaSuccess;
-  if (ldacc % 4) return cudaErrorInvalidValue;
+  if (ldacc % 4 || rows_per_seq < 1) return cudaErrorInvalidValue;
   launch_pdl(kv_acc_to_ring_kernel, dim3((items + 3) / 4), dim3(128), 0, st, acc, ldacc, rows, L, nkv, kgain,
-             eps, rope, neox, (bf16*)ring_k, (bf16*)ring_v, cap, append_only, ring);
+             eps, rope, neox, (bf16*)ring_k, (bf16*)ring_v, cap, append_only, ring, rows_per_seq, seq_kv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_commit(RoundState* rs, RingState* ring, int block, int keep,
-                          cudaStream_t st) {
-  launch_pdl(commit_kernel, dim3(1), dim3(1), 0, st, rs, ring, block, keep);
+                          cudaStream_t st, int nseq) {
+  launch_pdl(commit_kernel, dim3(1), dim3(nseq), 0, st, rs, ring, block, keep);
   return cudaGetLastError();
 }
 
-cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st) {
-  launch_pdl(ring_advance_kernel, dim3(1), dim3(1), 0, st, ring, d, mode);
+cudaError_t launch_ring_advance(RingState* ring, int d, int mode, cudaStream_t st, int nseq) {
+  launch_pdl(ring_advance_kernel, dim3(1), dim3(nseq), 0, st, ring, d, mode);
   return cudaGetLastError();
 }
 
@@ -668,7 +694,8 @@ cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st) 
   b.vec = (a.V * esz) % 16 == 0 && (a.kin * esz) % 16 == 0 && al16(a.logit_pool) && al16(a.resid_pool) &&
           al16(a.logits_out) && al16(a.resid_out);
   const int n = a.V > a.kin ? a.V : a.kin;
-  const dim3 grid((n + 8 * 256 - 1) / (8 * 256), a.block);
+  if (b.nseq < 1) b.nseq = 1;
+  const dim3 grid((n + 8 * 256 - 1) / (8 * 256), a.block, b.nseq);
   if (dtype) launch_pdl(synth_target_kernel<bf16>, grid, dim3(256), 0, st, b);
   else launch_pdl(synth_target_kernel<float>, grid, dim3(256), 0, st, b);
   return cudaGetLastError();

@@ -175,6 +175,37 @@ int dflash_ctx_create(const dflash_config* cfg, const dflash_weights* w,
                       void* stream, dflash_ctx** out);
 void dflash_ctx_destroy(dflash_ctx* ctx);
 
+/* ---- batched rounds ------------------------------------------------------------ */
+
+/* A context for n_seq sequences drafted, verified and committed together,
+ * the batched mode the Muse page leaves out ["Muse Glimmer DFlash assistant
+ * drafter on the round loop", "Not in this PR": batched (B > 1) windows
+ * decline through supports_batched()]. The sequences share the drafter's
+ * forward: every linear layer streams its weights once for the n_seq * block
+ * rows of a round. Each sequence has its own ring (window + slack rows),
+ * anchor, position and counters. The round calls keep their meaning with
+ * sequence-major tensors: dflash_draft_block writes draft_ids [n_seq][block-1]
+ * (anchor and anchor_pos must be -1: each sequence drafts from its device
+ * anchor), dflash_verify_accept takes target_logits [n_seq][block][V] and
+ * draft_ids [n_seq][block-1] and writes tokens [n_seq][block] and n
+ * [n_seq], dflash_append_block takes resid [n_seq][block][k*target_hidden],
+ * dflash_commit(ctx, -1) keeps each sequence's own n (a keep >= 0 applies to
+ * all), dflash_sync_round and dflash_synth_target are per sequence in the same
+ * layout (the stand-in target draws pool entry round * n_seq + s for sequence
+ * s). Sequences are ingested one by one (dflash_ingest_context_seq); a draft
+ * needs all of them. Needs 1 <= n_seq <= 64, n_seq * max_block <= 1024, a
+ * sliding window (window > 0) and no Markov head (EINVAL / ERANGE
+ * otherwise); the sampled verify and the Markov chain take one sequence.
+ * dflash_ctx_create is dflash_ctx_create_batched with n_seq = 1. */
+int dflash_ctx_create_batched(const dflash_config* cfg, const dflash_weights* w, int32_t n_seq,
+                              void* stream, dflash_ctx** out);
+/* Sequences per round of the context (1 for dflash_ctx_create). */
+int dflash_batch_size(const dflash_ctx* ctx);
+/* dflash_ingest_context for sequence seq (0 <= seq < n_seq; ERANGE
+ * otherwise); dflash_ingest_context is seq 0. */
+int dflash_ingest_context_seq(dflash_ctx* ctx, int32_t seq, const void* resid, int64_t rows,
+                              int64_t first_pos, int32_t anchor);
+
 /* Text of the last error on this context (or of the last failed create when
  * ctx is NULL). Never NULL. */
 const char* dflash_last_error(const dflash_ctx* ctx);
@@ -317,11 +348,18 @@ int dflash_get_draft_max_logit(dflash_ctx* ctx, float* out);
 /* Copies the lm_head argmax ids of the last draft's read-out rows (before
  * any Markov chain) [block - 1] (int32, device). */
 int dflash_get_backbone_ids(dflash_ctx* ctx, int32_t* out);
+/* State and counters of sequence 0 (syncs); the _seq forms take any
+ * sequence of a batch (ERANGE outside [0, n_seq)). dflash_reset_stats clears
+ * the counters of every sequence. */
 int dflash_get_state(dflash_ctx* ctx, dflash_round_state* out_host);
 int dflash_get_stats(dflash_ctx* ctx, dflash_stats* out_host);
+int dflash_get_state_seq(dflash_ctx* ctx, int32_t seq, dflash_round_state* out_host);
+int dflash_get_stats_seq(dflash_ctx* ctx, int32_t seq, dflash_stats* out_host);
 int dflash_reset_stats(dflash_ctx* ctx);
-/* The context's ring (borrowed; owned and destroyed by the context). */
+/* The context's ring, or sequence seq's ring of a batch (borrowed; owned and
+ * destroyed by the context). */
 int dflash_ring(dflash_ctx* ctx, ring_cache** out);
+int dflash_ring_seq(dflash_ctx* ctx, int32_t seq, ring_cache** out);
 
 /* ---- CUDA graphs of whole rounds -------------------------------------------- */
 

@@ -99,3 +99,21 @@ def test_null_context_calls_return_einval(B):
     assert B.lib.dflash_commit(None, -1) == B.EINVAL
     assert B.lib.ring_cache_trim(None, 1) == B.EINVAL
     B.lib.dflash_ctx_destroy(None)
+
+
+def test_batched_create_checks_before_cuda(B):
+    """n_seq outside [1, 64], a batch without a sliding window or with a Markov
+    head, and n_seq * max_block > 1024 are refused before any GPU work."""
+    from block_speculative_decoding_dflash_gb300 import synth
+    w = B.Weights()
+    h = ctypes.c_void_p()
+    c = B.make_config(synth.config("tiny"))
+    assert B.lib.dflash_ctx_create_batched(ctypes.byref(c), ctypes.byref(w), 0, None, ctypes.byref(h)) == B.ERANGE
+    assert B.lib.dflash_ctx_create_batched(ctypes.byref(c), ctypes.byref(w), 65, None, ctypes.byref(h)) == B.ERANGE
+    c2 = B.make_config(dict(synth.config("tiny"), window=0, max_context=64))
+    assert B.lib.dflash_ctx_create_batched(ctypes.byref(c2), ctypes.byref(w), 2, None, ctypes.byref(h)) == B.EINVAL
+    c3 = B.make_config(dict(synth.config("tiny"), max_block=600))
+    assert B.lib.dflash_ctx_create_batched(ctypes.byref(c3), ctypes.byref(w), 2, None, ctypes.byref(h)) == B.ERANGE
+    assert "1024" in B.last_error()
+    assert h.value is None
+    assert B.lib.dflash_batch_size(None) == 0
