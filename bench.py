@@ -321,37 +321,27 @@ def lm_head_bytes(cfg, rows):
     return cfg["vocab"] * cfg["hidden"] * 2 + rows * cfg["hidden"] * 2 + rows * 8
 
 
-def draft_bytes(cfg, rows, nctx):
-    """Algorithmic HBM bytes of one persistent draft-kernel launch: every
-    drafter weight once (5 layers of Wq Wk Wv Wo Wg Wu Wd, the lm_head), the
-    window's K and V of every layer, the block's embedding rows, and the
-    argmax outputs."""
-    H, I, hd = cfg["hidden"], cfg["intermediate"], cfg["head_dim"]
-    qdim, kvdim = cfg["n_q_heads"] * hd, cfg["n_kv_heads"] * hd
-    layer = (H * (qdim + 2 * kvdim) + qdim * H + 3 * H * I + 4 * H) * 2
-    kv = 2 * nctx * kvdim * 2
-    return cfg["n_layers"] * (layer + kv) + lm_head_bytes(cfg, rows - 1) + rows * H * 2
-
-
-def round_bytes(cfg, block, nctx):
+def round_bytes(cfg, block, nctx, n_seq=1):
     """Algorithmic HBM bytes of one round at verify width `block` with `nctx`
     visible context rows: every drafter weight once (5 layers of Wq Wk Wv Wo
     Wg Wu Wd and their norm gains, the lm_head), the window's K and V of every
     layer, the block's embedding rows, the target's block logits, the captured
     residual rows and encoder.fc plus every layer's Wk and Wv for the append,
-    and the ring rows it writes."""
+    and the ring rows it writes. A batch of n_seq sequences streams the
+    weights once and everything else once per sequence."""
     H, I, hd, L = cfg["hidden"], cfg["intermediate"], cfg["head_dim"], cfg["n_layers"]
     V, kin = cfg["vocab"], cfg["k_target_layers"] * cfg["target_hidden"]
     qdim, kvdim = cfg["n_q_heads"] * hd, cfg["n_kv_heads"] * hd
     rows = block - 1 if cfg.get("kind") == "dspark" else block
     layer_w = (H * (qdim + 2 * kvdim) + qdim * H + 3 * H * I + 2 * H + 2 * hd) * 2
-    draft = L * (layer_w + 2 * nctx * kvdim * 2) + 2 * H * 2 + V * H * 2 + (H * 2 if rows else 0)
+    shared = L * layer_w + 2 * H * 2 + V * H * 2 + H * kin * 2 + 2 * H * 2 + L * 2 * kvdim * H * 2
+    per_seq = L * 2 * nctx * kvdim * 2 + (H * 2 if rows else 0) + block * V * 2 \
+        + block * kin * 2 + L * 2 * block * kvdim * 2
     if cfg.get("markov_rank", 0):
         r = cfg["markov_rank"]
-        draft += r * V * 2 + (block - 1) * r * 2
-    verify = block * V * 2
-    append = block * kin * 2 + H * kin * 2 + 2 * H * 2 + L * 2 * kvdim * H * 2 + L * 2 * block * kvdim * 2
-    return draft + verify + append
+        shared += r * V * 2
+        per_seq += (block - 1) * r * 2
+    return shared + n_seq * per_seq
 
 
 # bytes each traced kernel class must move per launch (Muse shape)
@@ -458,8 +448,9 @@ def side_configs(job, args, peak, device):
     on the context's stream through captured round graphs: the DSpark drafter
     (widths 8 and 10, rank-256 Markov chain, append-only cache), the
     long-context slab stress (16384-row slab, window drop, width 16, keep ~
-    U{0..16}) and the Muse block-width sweep (widths 4..129 x planting
-    probability 0.3 / 0.7 / 0.95)."""
+    U{0..16}), the Muse block-width sweep (widths 4..129 x planting
+    probability 0.3 / 0.7 / 0.95) and batched rounds (2 to 8 sequences at
+    widths 4 and 16)."""
     import torch
     B, synth = job.B, job.synth
     R = args.config_rounds
@@ -562,6 +553,60 @@ def side_configs(job, args, peak, device):
                           "rounds_timed_per_point": R, "by_width_then_p": sweep,
                           "setup_s": round(time.time() - t0, 1)}
     ctx.close()
+    # -- batched rounds --------------------------------------------------------------------
+    t0 = time.time()
+    kin = cfg["k_target_layers"] * cfg["target_hidden"]
+    batched = {}
+    for S, w in ((2, 4), (4, 4), (8, 4), (2, 16), (4, 16)):
+        bcfg = dict(cfg, max_block=w)
+        ctx = B.DFlashContext(bcfg, job.wd, n_seq=S)
+        for sq in range(S):
+            ctx.ingest_context_seq(sq, job.resid, 2048, 0, 77 + sq)
+        ts = synth.make_target_stream(bcfg, S * (R + 8), w, seed=40 + S + w, logit_pool=4, resid_pool=8)
+        pools = _pools(B, ts, device)
+        ids = torch.zeros(S, w - 1, dtype=torch.int32, device=device)
+        tok = torch.zeros(S, w, dtype=torch.int32, device=device)
+        n = torch.zeros(S, dtype=torch.int32, device=device)
+        Lb = torch.zeros(S, w, cfg["vocab"], dtype=torch.bfloat16, device=device)
+        Rb = torch.zeros(S, w, kin, dtype=torch.bfloat16, device=device)
+
+        def one():
+            ctx.draft_block(w, ids)
+            ctx.synth_target(*pools, w, ids, Lb, Rb)
+            ctx.verify_accept(Lb, w, ids, tok, n)
+            ctx.append_block(Rb, w)
+            ctx.commit(-1)
+
+        one()
+        ctx.capture_begin()
+        one()
+        ctx.capture_end(1)
+        for _ in range(4):
+            ctx.graph_launch(1)
+        st0 = [ctx.stats(sq) for sq in range(S)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        for _ in range(R):
+            ctx.graph_launch(1)
+        e1.record(ctx.stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        st1 = [ctx.stats(sq) for sq in range(S)]
+        acc = sum(st1[sq]["accepted"] - st0[sq]["accepted"] for sq in range(S)) / (R * S)
+        us = ms * 1e3 / R
+        batched[f"{S}x{w}"] = {
+            "n_seq": S, "width": w, "rounds_per_s": round(R / (ms / 1e3), 1),
+            "sequence_rounds_per_s": round(S * R / (ms / 1e3), 1),
+            "draft_tok_s": round(S * R * (w - 1) / (ms / 1e3), 1),
+            "accepted_per_sequence_round": round(acc, 3), "round_us": round(us, 1),
+            "round_frac": round(round_bytes(bcfg, w, 2048, S) / (us * 1e-6) / 1e9 / peak, 3)}
+        ctx.close()
+        del pools, Lb, Rb
+    out["batched"] = {"workload": "muse_bf16_ctx2048_w2048_vocab202048_batched_nseq2to8_block4and16",
+                      "rounds_timed_per_point": R, "by_nseq_x_width": batched,
+                      "note": "one round drafts, verifies and commits every sequence of the batch; "
+                              "the weights stream once per round for all of them",
+                      "setup_s": round(time.time() - t0, 1)}
     return out
 
 
