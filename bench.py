@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -374,7 +375,9 @@ def kernel_breakdown(job, peak):
             c.graph_launch(60)
         c.sync()
         tr = c.kernel_trace_read()
-        main = [t for t in tr if not any(t[0].endswith(x) for x in (".1", ".2", ".3"))]
+        # the attention's split merge is its own kernel (slot .1 of the attention)
+        main = [(t[0].replace("attn.1", "attn_merge"),) + tuple(t[1:]) for t in tr
+                if t[0].endswith("attn.1") or not re.search(r"\.\d+$", t[0])]
         t0 = min(t[1] for t in main)
         t1 = max(t[3] for t in main)
         by = {}

@@ -351,8 +351,33 @@ void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMa
   a.nseg = i;
 }
 
+// More than 32 rows (wide verify blocks, batches): the finish-free GEMMs
+// (kEpiRed, kEpiRedPair) and the lm_head argmax run once per group of 32
+// rows, each launch streaming the weights again; b_map must then have been
+// encoded with 32-row boxes (bn_of of the whole row count).
 cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
-  return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
+  if (a.M <= 32) return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
+  if (a.epi != kEpiRed && a.epi != kEpiRedPair && a.epi != kEpiArgmax) return cudaErrorInvalidValue;
+  for (int r0 = 0; r0 < a.M; r0 += 32) {
+    TcGemmArgs g = a;
+    g.M = a.M - r0 < 32 ? a.M - r0 : 32;
+    g.b_row0 = a.b_row0 + r0;
+    if (g.acc) g.acc += (size_t)r0 * a.ldacc;
+    if (g.ids) g.ids += r0;
+    if (g.ids2) g.ids2 += r0;
+    if (g.maxv) g.maxv += r0;
+    if (a.epi == kEpiArgmax) g.whole_tiles = g.M > 8;
+    const cudaError_t e = launch_tc_gemm(g, 32, c->num_sms, true, c->stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The tensor-core path for `rows` block rows: up to 32 rows every GEMM of
+// the round; more in groups of 32, which needs the finish-free QKV of the
+// head_dim-128 attention.
+bool tc_rows(const dflash_ctx* c, int rows) {
+  return c->use_tc && (rows <= 32 || attention_mma_ok(c->dt, c->hd));
 }
 
 // Context rows -> ring: fc -> hidden_norm -> per layer [Wk | Wv] -> k-norm +
@@ -369,7 +394,7 @@ int context_rows_to_ring(dflash_ctx* c, const void* resid, int rows, void* f, vo
   const int sq = use_dev ? 0 : c->seq_cur;
   RingState* rst = c->ring->st + sq;
   CK(c->err, launch_rope_table(c->inv_freq, c->half, use_dev ? rst : nullptr, pos_host, rps, rope, st, ns));
-  const bool tc = c->use_tc && rows <= 32 && cn == c->app_c;
+  const bool tc = tc_rows(c, rows) && cn == c->app_c;
   if (tc) {
     // encoder.fc adds its fp32 sums into c->acc; hidden_norm rounds them
     // (f = rnd(acc)) and normalises
@@ -522,7 +547,7 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   cudaStream_t st = c->stream;
   const float eps = c->cfg.rms_eps;
   const std::string ln = "L" + std::to_string(l) + ".";
-  const bool tc = c->use_tc && rows <= 32;
+  const bool tc = tc_rows(c, rows);
   // The residual GEMMs (O, down) of the tensor-core path add their fp32 sums
   // into c->acc and leave the residual add to the RMSNorm that follows them:
   // x = rnd(x + rnd(acc)), then the norm of x.
@@ -533,13 +558,11 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st,
                               ktrace_slot(c, ln + "in_norm")));
   const int bi = bn_index(rows);
-  // q/k head norm + RoPE: applied by the tensor-core attention kernels as they
-  // load q and the block's k rows (the QKV GEMM then just stores, so its
-  // split tiles finish sooner), else by their own kernel
-  const bool attn_norm = tc && attention_mma_ok(dt, c->hd);
   // With the tensor-core attention the QKV GEMM adds its fp32 sums into
-  // c->qkv_acc and the attention rounds them as it loads q, k and v.
-  const bool qkv_red = tc && attn_norm;
+  // c->qkv_acc and one finishing kernel rounds them and applies the q/k head
+  // norm + RoPE (before it lets the attention launch: see launch_qkv_finish);
+  // otherwise the GEMM stores and two head-norm kernels follow.
+  const bool qkv_red = tc && attention_mma_ok(dt, c->hd);
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->qkv_n, c->H, qkv_red ? kEpiRed : kEpiStore);
     tc_segments(t, {{&c->lmaps[l].wq, c->qdim}, {&c->lmaps[l].wk, c->kvdim}, {&c->lmaps[l].wv, c->kvdim}});
@@ -556,7 +579,11 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     q.w[2] = LW(c, l, kWv); q.seg_end[2] = c->qkv_n;
     CK(c->err, launch_linear_rows(dt, q, st));
   }
-  if (!attn_norm) {
+  if (qkv_red) {
+    CK(c->err, launch_qkv_finish(c->qkv_acc, c->qkv_n, c->qkv, c->qkv_n, rows, c->nq, c->nkv, LW(c, l, kQNorm),
+                                 LW(c, l, kKNorm), eps, c->rope, c->cfg.rope_neox, st,
+                                 ktrace_slot(c, ln + "qkv_finish")));
+  } else {
     CK(c->err, launch_head_norm_rope(dt, c->qkv, c->qkv_n, rows, c->nq, c->hd, LW(c, l, kQNorm), eps,
                                      c->rope, c->cfg.rope_neox, st));
     CK(c->err, launch_head_norm_rope(dt, static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz,
@@ -568,14 +595,6 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.kb = static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz;
   at.vb = static_cast<char*>(c->qkv) + (size_t)(c->qdim + c->kvdim) * c->esz;
   at.ldkv = c->qkv_n;
-  if (qkv_red) {
-    at.q = c->qkv_acc;
-    at.kb = c->qkv_acc + c->qdim;
-    at.vb = c->qkv_acc + c->qdim + c->kvdim;
-    at.qkv_f32 = 1;
-    at.zero_acc = c->qkv_acc;
-    at.zero_n = rows * c->qkv_n;
-  }
   const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
   at.ring_k = static_cast<char*>(c->ring->k) + lay;
   at.ring_v = static_cast<char*>(c->ring->v) + lay;
@@ -588,11 +607,8 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
   at.err = c->tc_err;
-  at.trace = ktrace_slot(c, ln + "attn", 2);
-  if (attn_norm) {
-    at.qn = LW(c, l, kQNorm); at.kn = LW(c, l, kKNorm);
-    at.rope = c->rope; at.neox = c->cfg.rope_neox; at.eps = eps;
-  }
+  at.trace = ktrace_slot(c, ln + "attn", 5);
+  at.early_ctx = qkv_red ? 1 : 0;                // launch_qkv_finish precedes it
   CK(c->err, launch_attention(dt, at, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiRed);
@@ -1027,7 +1043,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
     int rc = layer_forward(c, l, rows);
     if (rc) return rc;
   }
-  if (c->use_tc && rows <= 32)   // the last down GEMM's sums are still in c->acc
+  if (tc_rows(c, rows))   // the last down GEMM's sums are still in c->acc
     CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, c->final_norm, c->xf, c->H, rows, c->H,
                                     c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
   else
@@ -1052,7 +1068,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_
   lm.counter = c->counters + 0;
   lm.grid = c->lm_grid;
   if (c->lm_timing) CK(c->err, cudaEventRecordWithFlags(c->lm_ev[0], st, c->capturing ? cudaEventRecordExternal : 0));
-  if (c->use_tc && lm_rows <= 32 && lm.logits == nullptr) {
+  if (tc_rows(c, lm_rows) && lm.logits == nullptr) {
     TcGemmArgs t = tc_args(c, lm_rows, c->V, c->H, kEpiArgmax);
     tc_segments(t, {{&c->lm_map, c->V}});
     t.b_map = c->xf_map[batch ? 0 : read0][bn_index(lm_rows)];
@@ -1216,7 +1232,7 @@ int dflash_lm_head_argmax(dflash_ctx* c, const void* x, int32_t rows, int32_t* i
   if (!x || !ids || !maxv) return fail(c->err, DFLASH_EINVAL, "an lm_head operand is NULL");
   if (rows < 1 || rows > c->cfg.max_block) return fail(c->err, DFLASH_ERANGE, "rows outside [1, max_block]");
   if (!aligned16(x)) return fail(c->err, DFLASH_EINVAL, "x must be 16-byte aligned");
-  if (c->use_tc && rows <= 32) {
+  if (c->use_tc) {
     TcGemmArgs t = tc_args(c, rows, c->V, c->H, kEpiArgmax);
     tc_segments(t, {{&c->lm_map, c->V}});
     if (!tc_encode_map(&t.b_map, x, c->H, rows, (uint64_t)c->H * 2, 64, bn_of(rows)))

@@ -43,6 +43,38 @@ __device__ __forceinline__ void f32x8_to_smem(void* dst, const float* src, bool 
   *reinterpret_cast<uint4*>(dst) = pk;
 }
 
+// Items e = threadIdx.x, threadIdx.x + blockDim.x, ... < n of 8 fp32 sums each
+// (item(e, &dst, &src) gives the 16 shared bytes and the 8 floats; src NULL:
+// zeros), rounded to bf16: four items a thread in flight, so the loads of a
+// thread's items cost one round trip to L2 instead of one each.
+template <class Item>
+__device__ __forceinline__ void f32x8_items_to_smem(int n, Item item) {
+  for (int e0 = threadIdx.x; e0 < n; e0 += 4 * blockDim.x) {
+    float4 lo[4], hi[4];
+    void* dst[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i * blockDim.x;
+      const float* src = nullptr;
+      dst[i] = nullptr;
+      if (e < n) item(e, dst[i], src);
+      lo[i] = src ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      hi[i] = src ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (dst[i])
+        *reinterpret_cast<uint4*>(dst[i]) = make_uint4(pack_bf16(lo[i].x, lo[i].y), pack_bf16(lo[i].z, lo[i].w),
+                                                       pack_bf16(hi[i].x, hi[i].y), pack_bf16(hi[i].z, hi[i].w));
+  }
+}
+
+// Phase marks of the kernel trace (last CTA through each phase): slot + 2
+// (k 1, 2) and slot + 3 (k 1, 2); slot + 1 is the merge kernel's.
+__device__ __forceinline__ void attn_phase(const KTrace& t, int n) {
+  if (t.p && threadIdx.x == 0) ktrace_mark(KTrace{t.p, t.slot + 2 + (n >> 1)}, 1 + (n & 1));
+}
+
 struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
   bf16 v[kKeys][kHd + kPad];
@@ -52,18 +84,26 @@ struct MmaSmem {
   bf16 pl[16][kKeys + kPad];               //                 low bf16 part
   float rm[16];                            // per query row: maximum score
   float rl[16];                            //                sum of P
+  bf16 gq[kHd], gk[kHd];                   // q and k head-norm gains
 };
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
   attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
-  // (Measured: 3 us per draft faster at 4 block rows; the tensor-core kernel
-  // used at 16 gained nothing from the same hint and does not issue it.)
-  attn_prefetch_context(a, blockIdx.x, blockIdx.y);
-  pdl_enter();
-  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
+  // the head-norm gains are weights: staged before the dependency resolves
+  if (a.qn && threadIdx.x < 2 * (kHd / 8)) {
+    const int ch = threadIdx.x & 15;
+    if (threadIdx.x < 16) cp_async16(&S.gq[ch * 8], reinterpret_cast<const bf16*>(a.qn) + ch * 8, true);
+    else cp_async16(&S.gk[ch * 8], reinterpret_cast<const bf16*>(a.kn) + ch * 8, true);
+  }
+  if (!a.early_ctx) {
+    // (Measured: 3 us per draft faster at 4 block rows.)
+    attn_prefetch_context(a, blockIdx.x, blockIdx.y);
+    pdl_enter();
+    if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  }
   const int s = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
@@ -86,41 +126,61 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
 
   const float* qf = reinterpret_cast<const float*>(a.q);
   auto load_q = [&](int q0) {
+    const int rows = Qn - q0 < kQChunk ? Qn - q0 : kQChunk;
+    if (a.qkv_f32) {
+      f32x8_items_to_smem(kQChunk * (kHd / 8), [&](int e, void*& dst, const float*& src) {
+        const int r = e >> 4, ch = e & 15, qi = q0 + r;
+        dst = &S.q[r][ch * 8];
+        if (r < rows) src = qf + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
+      });
+      return;
+    }
     for (int e = threadIdx.x; e < kQChunk * (kHd / 8); e += blockDim.x) {
       const int r = e >> 4, ch = e & 15;
       const int qi = q0 + r;
-      const bool valid = qi < Qn;
+      const bool valid = r < rows;
       const size_t off = valid ? (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8 : 0;
-      if (a.qkv_f32) f32x8_to_smem(&S.q[r][ch * 8], qf + off, valid);
-      else cp_async16(&S.q[r][ch * 8], qg + off, valid);
+      cp_async16(&S.q[r][ch * 8], qg + off, valid);
     }
   };
+  // K and V tiles: 128 keys x 16 chunks of 16 bytes each; the context rows
+  // (and zeros past the keys) first, before the dependency resolves when the
+  // ring may be read then (a.early_ctx), the block's own rows after it.
   if (j0 < nk) {
-    // K and V tiles: 128 keys x 16 chunks of 16 bytes each.
     for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
       const int j = e >> 4, ch = e & 15;
       const int kj = j0 + j;
-      const bf16* ks = kb;
-      const bf16* vs = vb;
-      bool valid = kj < nk;
-      if (kj < nctx) {
-        int slot = slot0 + kj;                     // = ring_slot(kstart + kj, cap)
-        if (slot >= cap) slot -= cap;
-        ks = rk + (size_t)slot * kHd + ch * 8;
-        vs = rv + (size_t)slot * kHd + ch * 8;
-      } else if (valid) {
-        const size_t off = (size_t)(kj - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
-        if (a.qkv_f32) {
-          f32x8_to_smem(&S.k[j][ch * 8], reinterpret_cast<const float*>(a.kb) + off, true);
-          f32x8_to_smem(&S.v[j][ch * 8], reinterpret_cast<const float*>(a.vb) + off, true);
-          continue;
-        }
-        ks = kb + off;
-        vs = vb + off;
-      }
-      cp_async16(&S.k[j][ch * 8], ks, valid);
-      cp_async16(&S.v[j][ch * 8], vs, valid);
+      if (kj >= nctx && kj < nk) continue;
+      const bool valid = kj < nctx;
+      int slot = slot0 + kj;                       // = ring_slot(kstart + kj, cap)
+      if (slot >= cap) slot -= cap;
+      const size_t off = valid ? (size_t)slot * kHd + ch * 8 : 0;
+      cp_async16(&S.k[j][ch * 8], rk + off, valid);
+      cp_async16(&S.v[j][ch * 8], rv + off, valid);
     }
+  }
+  if (a.early_ctx) {
+    pdl_enter();
+    if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  }
+  if (j0 < nk) {
+    const int kb0 = nctx > j0 ? nctx - j0 : 0;
+    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
+    if (!a.qkv_f32)
+      for (int e = threadIdx.x; e < (kb1 - kb0) * (kHd / 8); e += blockDim.x) {
+        const int j = kb0 + (e >> 4), ch = e & 15;
+        const size_t off = (size_t)(j0 + j - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
+        cp_async16(&S.k[j][ch * 8], kb + off, true);
+        cp_async16(&S.v[j][ch * 8], vb + off, true);
+      }
+    // the block's own keys and values from the QKV GEMM's fp32 sums
+    if (a.qkv_f32 && kb1 > kb0)
+      f32x8_items_to_smem((kb1 - kb0) * 2 * (kHd / 8), [&](int e, void*& dst, const float*& src) {
+        const int j = kb0 + (e >> 5), isv = (e >> 4) & 1, ch = e & 15;
+        const size_t off = (size_t)(j0 + j - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
+        dst = isv ? (void*)&S.v[j][ch * 8] : (void*)&S.k[j][ch * 8];
+        src = reinterpret_cast<const float*>(isv ? a.vb : a.kb) + off;
+      });
   }
   // Raw projections (a.qn set): per-head RMSNorm + RoPE of the loaded query
   // rows and of the block's own keys in this split, four threads a row.
@@ -130,8 +190,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
     if (r >= kQChunk || qi >= Qn) return;
     qk_norm_rope_quad([&](int d) { return __bfloat162float(S.q[r][d]); },
                       [&](int d, float v) { S.q[r][d] = __float2bfloat16_rn(v); },
-                      reinterpret_cast<const bf16*>(a.qn), a.eps, a.rope + (size_t)(qi / G) * (kHd / 2),
-                      a.neox, t);
+                      S.gq, a.eps, a.rope + (size_t)(qi / G) * (kHd / 2), a.neox, t);
   };
   const bool norm = a.qn != nullptr;
   load_q(0);
@@ -139,17 +198,22 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   __syncthreads();
   if (norm) {
     norm_q(0);
+    // the block's keys on the threads the queries leave free (whole quads)
     const int kb0 = nctx > j0 ? nctx - j0 : 0;
     const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
-    for (int e = threadIdx.x; e < (kb1 - kb0) * 4; e += blockDim.x) {
+    const int qthr = (Qn < kQChunk ? Qn : kQChunk) * 4;
+    const int kthr0 = qthr < static_cast<int>(blockDim.x) ? qthr : 0;
+    for (int e = static_cast<int>(threadIdx.x) - kthr0; e >= 0 && e < (kb1 - kb0) * 4;
+         e += blockDim.x - kthr0) {
       const int j = kb0 + (e >> 2);
       qk_norm_rope_quad([&](int d) { return __bfloat162float(S.k[j][d]); },
                         [&](int d, float v) { S.k[j][d] = __float2bfloat16_rn(v); },
-                        reinterpret_cast<const bf16*>(a.kn), a.eps,
+                        S.gk, a.eps,
                         a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, e & 3);
     }
     __syncthreads();
   }
+  attn_phase(a.trace, 0);                          // K, V, q loaded (and normalised)
 
   const int grp = lane >> 2, tig = lane & 3;
   const float scale = rsqrtf(static_cast<float>(kHd));
@@ -201,6 +265,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       }
     }
     __syncthreads();
+    if (qt == 0) attn_phase(a.trace, 1);            // first tile scored
     // Softmax rows: warp w takes query rows 2w and 2w + 1, four keys a lane;
     // P is kept as a high and a low bf16 part (about 16 significant bits).
 #pragma unroll
@@ -223,6 +288,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       if (lane == 0) { S.rm[r] = mx; S.rl[r] = l; }
     }
     __syncthreads();
+    if (qt == 0) attn_phase(a.trace, 2);            // first tile's softmax
     // O = P V: warp w owns output dims 16w .. 16w + 15 over all keys of the
     // split (eight 16-key steps, high and low parts of P)
     float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -275,6 +341,10 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
     attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, it / Qn, it % Qn,
                       reinterpret_cast<bf16*>(a.out), a.ldo, lane);
   }
+  if (tr.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(KTrace{tr.p, tr.slot + 3}, 1);   // merged
+  }
   // every attention CTA is done with the QKV GEMM's fp32 sums: clear them
   if (zero_acc)
     for (int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4; e < zero_n; e += gridDim.x * blockDim.x * 4)
@@ -322,8 +392,10 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
 __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
   attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
-  pdl_enter();
-  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  if (!a.early_ctx) {
+    pdl_enter();
+    if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
@@ -351,6 +423,26 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   const bf16* vb = reinterpret_cast<const bf16*>(a.vb) + (size_t)g * kHd;
   const bf16* qg = reinterpret_cast<const bf16*>(a.q) + (size_t)g * G * kHd;
 
+  // K into its tile, V into padded staging rows: the context rows and zeros
+  // past the keys first (before the dependency resolves with a.early_ctx),
+  // the block's own rows after it
+  if (j0 < nk) {
+    for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
+      const int j = e >> 4, ch = e & 15;
+      const int kj = j0 + j;
+      if (kj >= nctx && kj < nk) continue;
+      const bool valid = kj < nctx;
+      int slot = slot0 + kj;
+      if (slot >= cap) slot -= cap;
+      const size_t off = valid ? (size_t)slot * kHd + ch * 8 : 0;
+      cp_async16(sm + kTcK + tc_sw128(j, ch * 8), rk + off, valid);
+      cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, rv + off, valid);
+    }
+  }
+  if (a.early_ctx) {
+    pdl_enter();
+    if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  }
   if (j0 >= nk) {
     // a split past the keys: an empty partial (weight 0 in the merge)
     for (int e = threadIdx.x; e < Qn * kPartStride; e += blockDim.x) {
@@ -366,45 +458,55 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_holder, 256);
-
-  // K into its tile, V into padded staging rows (keys past nk zero-filled),
-  // each query into rows r and r + 64
-  for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
-    const int j = e >> 4, ch = e & 15;
-    const int kj = j0 + j;
-    const bf16* ks = kb;
-    const bf16* vs = vb;
-    const bool valid = kj < nk;
-    if (kj < nctx) {
-      int slot = slot0 + kj;
-      if (slot >= cap) slot -= cap;
-      ks = rk + (size_t)slot * kHd + ch * 8;
-      vs = rv + (size_t)slot * kHd + ch * 8;
-    } else if (valid) {
-      const size_t off = (size_t)(kj - nctx) * ldkv + ch * 8;
-      if (a.qkv_f32) {
-        f32x8_to_smem(sm + kTcK + tc_sw128(j, ch * 8), reinterpret_cast<const float*>(a.kb) + g * kHd + off, true);
-        f32x8_to_smem(sm + kTcVs + j * kTcVsRow + ch * 16, reinterpret_cast<const float*>(a.vb) + g * kHd + off,
-                      true);
-        continue;
-      }
-      ks = kb + off;
-      vs = vb + off;
-    }
-    cp_async16(sm + kTcK + tc_sw128(j, ch * 8), ks, valid);
-    cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, vs, valid);
+  __shared__ __align__(16) bf16 gq[kHd], gk[kHd];
+  if (a.qn && threadIdx.x < 2 * (kHd / 8)) {
+    const int ch = threadIdx.x & 15;
+    if (threadIdx.x < 16) cp_async16(&gq[ch * 8], reinterpret_cast<const bf16*>(a.qn) + ch * 8, true);
+    else cp_async16(&gk[ch * 8], reinterpret_cast<const bf16*>(a.kn) + ch * 8, true);
   }
-  // raw projections: each query into row r only, then normalised into r and r + 64
+
+  // the block's own keys and values (bf16), each query into rows r and r + 64
+  if (!a.qkv_f32) {
+    const int kb0 = nctx > j0 ? nctx - j0 : 0;
+    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
+    for (int e = threadIdx.x; e < (kb1 - kb0) * (kHd / 8); e += blockDim.x) {
+      const int j = kb0 + (e >> 4), ch = e & 15;
+      const size_t off = (size_t)(j0 + j - nctx) * ldkv + ch * 8;
+      cp_async16(sm + kTcK + tc_sw128(j, ch * 8), kb + off, true);
+      cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, vb + off, true);
+    }
+  }
   const bool norm = a.qn != nullptr;
-  for (int e = threadIdx.x; e < (norm ? 1 : 2) * kTileQ * (kHd / 8); e += blockDim.x) {
-    const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
-    const bool valid = qr < Qn;
-    const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
-    if (a.qkv_f32)
-      f32x8_to_smem(sm + kTcQ + tc_sw128(r, ch * 8), reinterpret_cast<const float*>(a.q) + (size_t)g * G * kHd + off,
-                    valid);
-    else
+  if (a.qkv_f32) {
+    // the block's own keys and values, then the queries, from the QKV GEMM's fp32 sums
+    const int kb0 = nctx > j0 ? nctx - j0 : 0;
+    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
+    const float* kf = reinterpret_cast<const float*>(a.kb) + g * kHd;
+    const float* vf = reinterpret_cast<const float*>(a.vb) + g * kHd;
+    const float* qf = reinterpret_cast<const float*>(a.q) + (size_t)g * G * kHd;
+    const int nkv_items = kb1 > kb0 ? (kb1 - kb0) * 2 * (kHd / 8) : 0;
+    f32x8_items_to_smem(nkv_items + (norm ? 1 : 2) * kTileQ * (kHd / 8),
+                        [&](int e, void*& dst, const float*& src) {
+      if (e < nkv_items) {
+        const int j = kb0 + (e >> 5), isv = (e >> 4) & 1, ch = e & 15;
+        const size_t off = (size_t)(j0 + j - nctx) * ldkv + ch * 8;
+        dst = isv ? (void*)(sm + kTcVs + j * kTcVsRow + ch * 16) : (void*)(sm + kTcK + tc_sw128(j, ch * 8));
+        src = (isv ? vf : kf) + off;
+        return;
+      }
+      e -= nkv_items;
+      const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
+      dst = sm + kTcQ + tc_sw128(r, ch * 8);
+      if (qr < Qn) src = qf + (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8;
+    });
+  } else {
+    // raw projections: each query into row r only, then normalised into r and r + 64
+    for (int e = threadIdx.x; e < (norm ? 1 : 2) * kTileQ * (kHd / 8); e += blockDim.x) {
+      const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
+      const bool valid = qr < Qn;
+      const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
       cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
+    }
   }
   cp_async_wait_all();
   if (norm) {
@@ -423,7 +525,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
               q0[tc_sw128(r, d) >> 1] = b;
               q0[tc_sw128(r + kTileQ, d) >> 1] = b;
             },
-            reinterpret_cast<const bf16*>(a.qn), a.eps, a.rope + (size_t)(r / G) * (kHd / 2), a.neox, t);
+            gq, a.eps, a.rope + (size_t)(r / G) * (kHd / 2), a.neox, t);
       }
     }
     const int kb0 = nctx > j0 ? nctx - j0 : 0;           // first block key of this split
@@ -433,7 +535,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       bf16* k0 = reinterpret_cast<bf16*>(sm + kTcK);
       qk_norm_rope_quad([&](int d) { return __bfloat162float(k0[tc_sw128(j, d) >> 1]); },
                         [&](int d, float v) { k0[tc_sw128(j, d) >> 1] = __float2bfloat16_rn(v); },
-                        reinterpret_cast<const bf16*>(a.kn), a.eps,
+                        gk, a.eps,
                         a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, t);
     }
   }
@@ -441,6 +543,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  attn_phase(a.trace, 0);                          // K, V, q loaded and normalised
   const uint32_t tmem = *tmem_holder;
   constexpr uint32_t idesc = idesc_bf16(128, 128);
   const uint32_t sbase = smem_u32(sm);
@@ -496,6 +599,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   }
   red_m[grp][qi] = mrow;
   __syncthreads();
+  attn_phase(a.trace, 1);                          // S read back
+
   const float M = fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
   float l = 0.f;
   uint32_t pk[16], pr[16];
@@ -526,6 +631,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  attn_phase(a.trace, 2);                          // P written
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int kc = 0; kc < 2; ++kc)
@@ -556,6 +662,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       *reinterpret_cast<float4*>(ost + 4 * i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
   }
   __syncthreads();
+  attn_phase(a.trace, 3);                          // O read back
   if (rh == 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {

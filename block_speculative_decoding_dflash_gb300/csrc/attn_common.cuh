@@ -33,6 +33,10 @@ __host__ __device__ __forceinline__ int attn_splits(long long n) {
 template <class Ld, class St>
 __device__ __forceinline__ void qk_norm_rope_quad(Ld ld, St st, const bf16* g, float eps,
                                                   const float2* rope_row, int neox, int t) {
+  // the row's rotations first: the global loads then overlap the reads below
+  float2 cs[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) cs[j] = rope_row[16 * t + j];
   float x[16], y[16];
   float ss = 0.f;
 #pragma unroll
@@ -54,9 +58,8 @@ __device__ __forceinline__ void qk_norm_rope_quad(Ld ld, St st, const bf16* g, f
     const int ia = neox ? i : 2 * i, ib = neox ? i + kAttnHd / 2 : 2 * i + 1;
     const float a = x[j] * inv * __bfloat162float(g[ia]);
     const float b = y[j] * inv * __bfloat162float(g[ib]);
-    const float2 cs = rope_row[i];
-    st(ia, a * cs.x - b * cs.y);
-    st(ib, a * cs.y + b * cs.x);
+    st(ia, a * cs[j].x - b * cs[j].y);
+    st(ib, a * cs[j].y + b * cs[j].x);
   }
 }
 

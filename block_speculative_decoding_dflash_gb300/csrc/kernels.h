@@ -50,6 +50,7 @@ struct TcGemmArgs {
   CUtensorMap a_map[kTcMaxSeg];    // weight segments, box {64, 128}
   CUtensorMap a2_map;              // up weight of kEpiSwiglu, box {64, 128}
   CUtensorMap b_map;               // X, box {64, BN}
+  int b_row0;                      // first row of X this launch reads (TMA row coordinate)
   int seg_tiles[kTcMaxSeg];
   int nseg;
   int M, N, K, tiles, kchunks, epi;
@@ -151,6 +152,13 @@ cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nk
                                   void* ring_k, void* ring_v, long long cap, int append_only,
                                   RingState* ring, cudaStream_t st, KTrace trace, int rows_per_seq,
                                   long long seq_kv);
+// bf16, head_dim 128: finishes a kEpiRed QKV GEMM (acc [rows][ldacc] fp32,
+// nq q heads, nkv k heads, nkv v heads): out = the rounded values, q and k
+// heads with the per-head RMSNorm (gains qn, kn) + RoPE (rope[r][64]); the
+// sums cleared. Waits for the GEMM before it lets the next kernel launch.
+cudaError_t launch_qkv_finish(float* acc, int ldacc, void* out, int ldo, int rows, int nq, int nkv,
+                              const void* qn, const void* kn, float eps, const float2* rope, int neox,
+                              cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
 // In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
 cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
                                   int heads, int hd, const void* g, float eps,
@@ -181,6 +189,8 @@ struct AttnArgs {
   void* out; int ldo;          // [rows, nq, hd]
   int* err;                    // bounded-wait timeouts are reported here (bit 32)
   KTrace trace;                // attention kernel; the separate merge kernel uses slot + 1
+                               // (its phase mark slot + 4), the attention's phase marks
+                               // slots + 2 and + 3
   // When qn is set (tensor-core path only), q and the block's k rows are the
   // raw projections: the kernel applies the per-head RMSNorm (gains qn / kn,
   // [hd]) and RoPE (rope[m * hd/2 + i] for block row m) as it loads them.
@@ -200,6 +210,11 @@ struct AttnArgs {
   // partials.
   int nseq;
   long long seq_kv;
+  // The kernel before the attention waited for its own dependency before it
+  // let the attention launch (launch_qkv_finish), so every kernel before that
+  // one is complete: the ring's context rows (and the ring state) may be read
+  // before the attention's own dependency resolves.
+  int early_ctx;
 };
 // Points a's per-sequence operands at sequence s: q, kb, vb hold elements of
 // qkv_esz bytes, the ring and out of esz bytes; partial rows are part_stride

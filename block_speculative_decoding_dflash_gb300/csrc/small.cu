@@ -390,6 +390,62 @@ __global__ void __launch_bounds__(128) kv_acc_to_ring_kernel(float* acc, int lda
   }
 }
 
+// Finish of the QKV GEMM's fp32 sums (bf16, head_dim 128): one warp per
+// (row, head) of the nq + 2 nkv heads, four dims a lane; every value rounded
+// (the GEMM's output rounding); q and k heads then the per-head RMSNorm (gains
+// qn / kn) and RoPE (rope[r][64]), rounded once more; the sums cleared. It
+// waits for the GEMM before it lets the attention launch, so everything
+// before the GEMM is complete once the attention runs: the attention may read
+// the ring's context rows before its own dependency resolves.
+__global__ void __launch_bounds__(128) qkv_finish_kernel(float* acc, int ldacc, bf16* out, int ldo, int rows,
+                                                        int nq, int nkv, const bf16* qn, const bf16* kn,
+                                                        float eps, const float2* rope, int neox, KTrace tr) {
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
+  __shared__ float sm[4][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = nq + 2 * nkv;
+  const int item = blockIdx.x * 4 + warp;
+  if (item < rows * heads) {
+    const int r = item / heads, h = item % heads;
+    float* src = acc + (size_t)r * ldacc + (size_t)h * 128;
+    const float4 v4 = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+    reinterpret_cast<float4*>(src)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float x[4] = {rnd<bf16>(v4.x), rnd<bf16>(v4.y), rnd<bf16>(v4.z), rnd<bf16>(v4.w)};
+    bf16* dst = out + (size_t)r * ldo + (size_t)h * 128;
+    if (h >= nq + nkv) {                               // V: rounded
+      uint2 pk;
+      pk.x = pack_bf2(x[0], x[1]);
+      pk.y = pack_bf2(x[2], x[3]);
+      reinterpret_cast<uint2*>(dst)[lane] = pk;
+    } else {                                           // q or k: head RMSNorm, gain, RoPE
+      const bf16* g = h < nq ? qn : kn;
+      float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / 128.0f + eps);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm[warp][lane * 4 + e] = x[e] * inv * __bfloat162float(g[lane * 4 + e]);
+      __syncwarp();
+      const float2* rr = rope + (size_t)r * 64;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int i = lane + 32 * q;                   // rotation pair i of 64
+        const int ia = neox ? i : 2 * i, ib = neox ? i + 64 : 2 * i + 1;
+        const float2 cs = rr[i];
+        const float a = sm[warp][ia], b = sm[warp][ib];
+        dst[ia] = __float2bfloat16_rn(a * cs.x - b * cs.y);
+        dst[ib] = __float2bfloat16_rn(a * cs.y + b * cs.x);
+      }
+    }
+  }
+  if (tr.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(tr, 2);
+  }
+}
+
 // ---- ring bookkeeping ------------------------------------------------------------
 __global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
   pdl_enter();
@@ -627,6 +683,17 @@ cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nk
   if (ldacc % 4 || rows_per_seq < 1) return cudaErrorInvalidValue;
   launch_pdl(kv_acc_to_ring_kernel, dim3((items + 3) / 4), dim3(128), 0, st, acc, ldacc, rows, L, nkv, kgain,
              eps, rope, neox, (bf16*)ring_k, (bf16*)ring_v, cap, append_only, ring, rows_per_seq, seq_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_finish(float* acc, int ldacc, void* out, int ldo, int rows, int nq, int nkv,
+                              const void* qn, const void* kn, float eps, const float2* rope, int neox,
+                              cudaStream_t st, KTrace tr) {
+  const int items = rows * (nq + 2 * nkv);
+  if (items <= 0) return cudaSuccess;
+  if (ldacc % 4 || ldo % 4) return cudaErrorInvalidValue;
+  launch_pdl(qkv_finish_kernel, dim3((items + 3) / 4), dim3(128), 0, st, acc, ldacc, (bf16*)out, ldo, rows, nq,
+             nkv, (const bf16*)qn, (const bf16*)kn, eps, rope, neox, tr);
   return cudaGetLastError();
 }
 

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       auto issue_b = [&](int st, unsigned u, int nc) {
         const int c = static_cast<int>(u % KC);
         uint8_t* sb = smem + (size_t)st * C::kStage + C::kBOff;
-        for (int k = 0; k < nc; ++k) tma_load_2d(sb + k * BN * 128, &a.b_map, (c + k) * 64, 0, &full[st]);
+        for (int k = 0; k < nc; ++k) tma_load_2d(sb + k * BN * 128, &a.b_map, (c + k) * 64, a.b_row0, &full[st]);
       };
       auto width = [&](unsigned u) {
         return (P == 2 && u + 1 < u1 && (u % KC) + 1 < KC) ? 2 : 1;

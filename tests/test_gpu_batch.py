@@ -161,10 +161,11 @@ def muse(H):
     return cfg, w, B.weights_to_device(w, "bf16"), H.f64_weights(w, "bf16", lazy_embed=True)
 
 
-@pytest.mark.parametrize("n_seq,block", [(4, 4), (2, 16)])
+@pytest.mark.parametrize("n_seq,block", [(4, 4), (2, 16), (4, 16)])
 def test_muse_batched_rounds(H, muse, n_seq, block):
     """16 rows (four sequences of 4) and 32 rows (two of 16) on the tensor-core
-    path: the weights stream once for the whole batch."""
+    path: the weights stream once for the whole batch; 64 rows (four of 16):
+    the GEMMs in two groups of 32 rows."""
     cfg, w, wd, w64 = muse
     b = Batch(H, dict(cfg, max_block=block), n_seq, w=w, w64=w64, wd=wd, ctx_rows=2048)
     for r in range(3):
