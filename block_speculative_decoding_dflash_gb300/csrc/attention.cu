@@ -24,7 +24,7 @@ constexpr int kWarps = 8;
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(AttnArgs a, int nsplit) {
   pdl_enter();
-  attn_select_seq(a, blockIdx.z, nsplit, sizeof(T), sizeof(T), a.hd + 2);
+  attn_select_seq(a, blockIdx.z, nsplit, sizeof(T), a.hd + 2);
   extern __shared__ float smem[];
   const int hd = a.hd, hdp = hd + 1;
   float* Ks = smem;                       // [kKS][hd+1]
@@ -131,7 +131,7 @@ __global__ void attn_combine_kernel(AttnArgs a, int nsplit) {
   const int Qn = a.rows * G;
   int item = blockIdx.x * (blockDim.x >> 5) + warp;         // over nseq * nkv * Qn
   if (item >= (a.nseq > 1 ? a.nseq : 1) * a.nkv * Qn) return;
-  attn_select_seq(a, item / (a.nkv * Qn), nsplit, sizeof(T), sizeof(T), a.hd + 2);
+  attn_select_seq(a, item / (a.nkv * Qn), nsplit, sizeof(T), a.hd + 2);
   item %= a.nkv * Qn;
   const int g = item / Qn, qi = item % Qn;
   const int r = qi / G, h = g * G + qi % G;

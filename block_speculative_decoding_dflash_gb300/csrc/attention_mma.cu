@@ -31,44 +31,6 @@ constexpr int kPad = 8;                    // bf16 elements of row padding (conf
 constexpr int kPartStride = kAttnPartStride;
 constexpr int kQChunk = 64;
 
-// 8 consecutive fp32 sums of a kEpiRed GEMM, rounded to bf16, into 16 bytes
-// of shared memory (zeros when !valid).
-__device__ __forceinline__ void f32x8_to_smem(void* dst, const float* src, bool valid) {
-  uint4 pk = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) {
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
-    pk = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
-  }
-  *reinterpret_cast<uint4*>(dst) = pk;
-}
-
-// Items e = threadIdx.x, threadIdx.x + blockDim.x, ... < n of 8 fp32 sums each
-// (item(e, &dst, &src) gives the 16 shared bytes and the 8 floats; src NULL:
-// zeros), rounded to bf16: four items a thread in flight, so the loads of a
-// thread's items cost one round trip to L2 instead of one each.
-template <class Item>
-__device__ __forceinline__ void f32x8_items_to_smem(int n, Item item) {
-  for (int e0 = threadIdx.x; e0 < n; e0 += 4 * blockDim.x) {
-    float4 lo[4], hi[4];
-    void* dst[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = e0 + i * blockDim.x;
-      const float* src = nullptr;
-      dst[i] = nullptr;
-      if (e < n) item(e, dst[i], src);
-      lo[i] = src ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      hi[i] = src ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (dst[i])
-        *reinterpret_cast<uint4*>(dst[i]) = make_uint4(pack_bf16(lo[i].x, lo[i].y), pack_bf16(lo[i].z, lo[i].w),
-                                                       pack_bf16(hi[i].x, hi[i].y), pack_bf16(hi[i].z, hi[i].w));
-  }
-}
-
 // Phase marks of the kernel trace (last CTA through each phase): slot + 2
 // (k 1, 2) and slot + 3 (k 1, 2); slot + 1 is the merge kernel's.
 __device__ __forceinline__ void attn_phase(const KTrace& t, int n) {
@@ -84,20 +46,13 @@ struct MmaSmem {
   bf16 pl[16][kKeys + kPad];               //                 low bf16 part
   float rm[16];                            // per query row: maximum score
   float rl[16];                            //                sum of P
-  bf16 gq[kHd], gk[kHd];                   // q and k head-norm gains
 };
 
 __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int nsplit) {
-  attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
+  attn_select_seq(a, blockIdx.z, nsplit, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
-  // the head-norm gains are weights: staged before the dependency resolves
-  if (a.qn && threadIdx.x < 2 * (kHd / 8)) {
-    const int ch = threadIdx.x & 15;
-    if (threadIdx.x < 16) cp_async16(&S.gq[ch * 8], reinterpret_cast<const bf16*>(a.qn) + ch * 8, true);
-    else cp_async16(&S.gk[ch * 8], reinterpret_cast<const bf16*>(a.kn) + ch * 8, true);
-  }
   if (!a.early_ctx) {
     // (Measured: 3 us per draft faster at 4 block rows.)
     attn_prefetch_context(a, blockIdx.x, blockIdx.y);
@@ -124,17 +79,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   const bf16* vb = reinterpret_cast<const bf16*>(a.vb);
   const bf16* qg = reinterpret_cast<const bf16*>(a.q);
 
-  const float* qf = reinterpret_cast<const float*>(a.q);
   auto load_q = [&](int q0) {
     const int rows = Qn - q0 < kQChunk ? Qn - q0 : kQChunk;
-    if (a.qkv_f32) {
-      f32x8_items_to_smem(kQChunk * (kHd / 8), [&](int e, void*& dst, const float*& src) {
-        const int r = e >> 4, ch = e & 15, qi = q0 + r;
-        dst = &S.q[r][ch * 8];
-        if (r < rows) src = qf + (size_t)(qi / G) * a.ldq + (size_t)(g * G + qi % G) * kHd + ch * 8;
-      });
-      return;
-    }
     for (int e = threadIdx.x; e < kQChunk * (kHd / 8); e += blockDim.x) {
       const int r = e >> 4, ch = e & 15;
       const int qi = q0 + r;
@@ -166,54 +112,17 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   if (j0 < nk) {
     const int kb0 = nctx > j0 ? nctx - j0 : 0;
     const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
-    if (!a.qkv_f32)
-      for (int e = threadIdx.x; e < (kb1 - kb0) * (kHd / 8); e += blockDim.x) {
-        const int j = kb0 + (e >> 4), ch = e & 15;
-        const size_t off = (size_t)(j0 + j - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
-        cp_async16(&S.k[j][ch * 8], kb + off, true);
-        cp_async16(&S.v[j][ch * 8], vb + off, true);
-      }
-    // the block's own keys and values from the QKV GEMM's fp32 sums
-    if (a.qkv_f32 && kb1 > kb0)
-      f32x8_items_to_smem((kb1 - kb0) * 2 * (kHd / 8), [&](int e, void*& dst, const float*& src) {
-        const int j = kb0 + (e >> 5), isv = (e >> 4) & 1, ch = e & 15;
-        const size_t off = (size_t)(j0 + j - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
-        dst = isv ? (void*)&S.v[j][ch * 8] : (void*)&S.k[j][ch * 8];
-        src = reinterpret_cast<const float*>(isv ? a.vb : a.kb) + off;
-      });
+    for (int e = threadIdx.x; e < (kb1 - kb0) * (kHd / 8); e += blockDim.x) {
+      const int j = kb0 + (e >> 4), ch = e & 15;
+      const size_t off = (size_t)(j0 + j - nctx) * a.ldkv + (size_t)g * kHd + ch * 8;
+      cp_async16(&S.k[j][ch * 8], kb + off, true);
+      cp_async16(&S.v[j][ch * 8], vb + off, true);
+    }
   }
-  // Raw projections (a.qn set): per-head RMSNorm + RoPE of the loaded query
-  // rows and of the block's own keys in this split, four threads a row.
-  auto norm_q = [&](int q0) {
-    const int r = threadIdx.x >> 2, t = threadIdx.x & 3;
-    const int qi = q0 + r;
-    if (r >= kQChunk || qi >= Qn) return;
-    qk_norm_rope_quad([&](int d) { return __bfloat162float(S.q[r][d]); },
-                      [&](int d, float v) { S.q[r][d] = __float2bfloat16_rn(v); },
-                      S.gq, a.eps, a.rope + (size_t)(qi / G) * (kHd / 2), a.neox, t);
-  };
-  const bool norm = a.qn != nullptr;
   load_q(0);
   cp_async_wait_all();
   __syncthreads();
-  if (norm) {
-    norm_q(0);
-    // the block's keys on the threads the queries leave free (whole quads)
-    const int kb0 = nctx > j0 ? nctx - j0 : 0;
-    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
-    const int qthr = (Qn < kQChunk ? Qn : kQChunk) * 4;
-    const int kthr0 = qthr < static_cast<int>(blockDim.x) ? qthr : 0;
-    for (int e = static_cast<int>(threadIdx.x) - kthr0; e >= 0 && e < (kb1 - kb0) * 4;
-         e += blockDim.x - kthr0) {
-      const int j = kb0 + (e >> 2);
-      qk_norm_rope_quad([&](int d) { return __bfloat162float(S.k[j][d]); },
-                        [&](int d, float v) { S.k[j][d] = __float2bfloat16_rn(v); },
-                        S.gk, a.eps,
-                        a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, e & 3);
-    }
-    __syncthreads();
-  }
-  attn_phase(a.trace, 0);                          // K, V, q loaded (and normalised)
+  attn_phase(a.trace, 0);                          // K, V, q loaded
 
   const int grp = lane >> 2, tig = lane & 3;
   const float scale = rsqrtf(static_cast<float>(kHd));
@@ -223,10 +132,6 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
       load_q(qt * 16);
       cp_async_wait_all();
       __syncthreads();
-      if (norm) {
-        norm_q(qt * 16);
-        __syncthreads();
-      }
     }
     // S = Q K^T: warp w scores the 16 queries of this tile against its 16
     // keys (two 8-key n-tiles), masks |q - k| <= W by absolute positions and
@@ -333,10 +238,8 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
   const int Qn = a.rows * G;
   const int ns = a.nseq > 1 ? a.nseq : 1;
   const int item = blockIdx.x * 4 + warp;
-  float* zero_acc = a.zero_acc;
-  const int zero_n = a.zero_n;
   if (item < ns * a.nkv * Qn) {
-    attn_select_seq(a, item / (a.nkv * Qn), nsplit, 2, 2, kPartStride);
+    attn_select_seq(a, item / (a.nkv * Qn), nsplit, 2, kPartStride);
     const int it = item % (a.nkv * Qn);
     attn_combine_warp(a.partial, nsplit, nsplit, Qn, G, it / Qn, it % Qn,
                       reinterpret_cast<bf16*>(a.out), a.ldo, lane);
@@ -345,11 +248,7 @@ __global__ void __launch_bounds__(128) attn_mma_combine_kernel(AttnArgs a, int n
     __syncthreads();
     if (threadIdx.x == 0) ktrace_mark(KTrace{tr.p, tr.slot + 3}, 1);   // merged
   }
-  // every attention CTA is done with the QKV GEMM's fp32 sums: clear them
-  if (zero_acc)
-    for (int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4; e < zero_n; e += gridDim.x * blockDim.x * 4)
-      *reinterpret_cast<float4*>(zero_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (tr.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(tr, 2); }
+  if (tr.p && threadIdx.x == 0) ktrace_mark(tr, 2);
 }
 
 constexpr int kTileQ = 64;                 // queries per kv head of the tensor-core kernel
@@ -390,7 +289,7 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
 }
 
 __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
-  attn_select_seq(a, blockIdx.z, nsplit, a.qkv_f32 ? 4 : 2, 2, kPartStride);
+  attn_select_seq(a, blockIdx.z, nsplit, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   if (!a.early_ctx) {
     pdl_enter();
@@ -458,15 +357,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_holder, 256);
-  __shared__ __align__(16) bf16 gq[kHd], gk[kHd];
-  if (a.qn && threadIdx.x < 2 * (kHd / 8)) {
-    const int ch = threadIdx.x & 15;
-    if (threadIdx.x < 16) cp_async16(&gq[ch * 8], reinterpret_cast<const bf16*>(a.qn) + ch * 8, true);
-    else cp_async16(&gk[ch * 8], reinterpret_cast<const bf16*>(a.kn) + ch * 8, true);
-  }
 
-  // the block's own keys and values (bf16), each query into rows r and r + 64
-  if (!a.qkv_f32) {
+  // the block's own keys and values, each query into rows r and r + 64
+  {
     const int kb0 = nctx > j0 ? nctx - j0 : 0;
     const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
     for (int e = threadIdx.x; e < (kb1 - kb0) * (kHd / 8); e += blockDim.x) {
@@ -476,74 +369,18 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       cp_async16(sm + kTcVs + j * kTcVsRow + ch * 16, vb + off, true);
     }
   }
-  const bool norm = a.qn != nullptr;
-  if (a.qkv_f32) {
-    // the block's own keys and values, then the queries, from the QKV GEMM's fp32 sums
-    const int kb0 = nctx > j0 ? nctx - j0 : 0;
-    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
-    const float* kf = reinterpret_cast<const float*>(a.kb) + g * kHd;
-    const float* vf = reinterpret_cast<const float*>(a.vb) + g * kHd;
-    const float* qf = reinterpret_cast<const float*>(a.q) + (size_t)g * G * kHd;
-    const int nkv_items = kb1 > kb0 ? (kb1 - kb0) * 2 * (kHd / 8) : 0;
-    f32x8_items_to_smem(nkv_items + (norm ? 1 : 2) * kTileQ * (kHd / 8),
-                        [&](int e, void*& dst, const float*& src) {
-      if (e < nkv_items) {
-        const int j = kb0 + (e >> 5), isv = (e >> 4) & 1, ch = e & 15;
-        const size_t off = (size_t)(j0 + j - nctx) * ldkv + ch * 8;
-        dst = isv ? (void*)(sm + kTcVs + j * kTcVsRow + ch * 16) : (void*)(sm + kTcK + tc_sw128(j, ch * 8));
-        src = (isv ? vf : kf) + off;
-        return;
-      }
-      e -= nkv_items;
-      const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
-      dst = sm + kTcQ + tc_sw128(r, ch * 8);
-      if (qr < Qn) src = qf + (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8;
-    });
-  } else {
-    // raw projections: each query into row r only, then normalised into r and r + 64
-    for (int e = threadIdx.x; e < (norm ? 1 : 2) * kTileQ * (kHd / 8); e += blockDim.x) {
-      const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
-      const bool valid = qr < Qn;
-      const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
-      cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
-    }
+  for (int e = threadIdx.x; e < 2 * kTileQ * (kHd / 8); e += blockDim.x) {
+    const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
+    const bool valid = qr < Qn;
+    const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
+    cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
   }
   cp_async_wait_all();
-  if (norm) {
-    __syncthreads();
-    // per-head RMSNorm + RoPE of the queries (four threads a row) and of the
-    // block's own keys in this split (the ring's keys are stored normalised)
-    const int t = threadIdx.x & 3;
-    {
-      const int r = threadIdx.x >> 2;
-      if (r < Qn) {
-        bf16* q0 = reinterpret_cast<bf16*>(sm + kTcQ);
-        qk_norm_rope_quad(
-            [&](int d) { return __bfloat162float(q0[tc_sw128(r, d) >> 1]); },
-            [&](int d, float v) {
-              const bf16 b = __float2bfloat16_rn(v);
-              q0[tc_sw128(r, d) >> 1] = b;
-              q0[tc_sw128(r + kTileQ, d) >> 1] = b;
-            },
-            gq, a.eps, a.rope + (size_t)(r / G) * (kHd / 2), a.neox, t);
-      }
-    }
-    const int kb0 = nctx > j0 ? nctx - j0 : 0;           // first block key of this split
-    const int kb1 = nk - j0 < kKeys ? nk - j0 : kKeys;
-    for (int e = threadIdx.x; e < (kb1 - kb0) * 4; e += blockDim.x) {
-      const int j = kb0 + (e >> 2);
-      bf16* k0 = reinterpret_cast<bf16*>(sm + kTcK);
-      qk_norm_rope_quad([&](int d) { return __bfloat162float(k0[tc_sw128(j, d) >> 1]); },
-                        [&](int d, float v) { k0[tc_sw128(j, d) >> 1] = __float2bfloat16_rn(v); },
-                        gk, a.eps,
-                        a.rope + (size_t)(j0 + j - nctx) * (kHd / 2), a.neox, t);
-    }
-  }
   fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  attn_phase(a.trace, 0);                          // K, V, q loaded and normalised
+  attn_phase(a.trace, 0);                          // K, V, q loaded
   const uint32_t tmem = *tmem_holder;
   constexpr uint32_t idesc = idesc_bf16(128, 128);
   const uint32_t sbase = smem_u32(sm);
@@ -705,11 +542,18 @@ size_t attention_mma_scratch_floats(int rows, int nq, int nkv, int max_ctx) {
 bool attention_mma_ok(int dtype, int hd) { return dtype == 1 && hd == kHd; }
 
 cudaError_t init_attention_mma_attrs() {
+  // the largest shared-memory carveout, as the GEMMs around them
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kTcAttnSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(MmaSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(MmaSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {

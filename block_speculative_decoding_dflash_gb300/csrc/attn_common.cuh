@@ -23,46 +23,6 @@ __host__ __device__ __forceinline__ int attn_splits(long long n) {
   return static_cast<int>((n + kAttnKeys - 1) / kAttnKeys);
 }
 
-// Per-head RMSNorm (gain g over kAttnHd dims) followed by RoPE of one q or k
-// row held by four consecutive lanes: lane t = lane & 3 takes the rotation
-// pairs 16t .. 16t + 15 (dims (i, i + 64) in the half-split layout, (2i,
-// 2i + 1) in the interleaved one). ld(d) reads dim d, st(d, v) writes it; the
-// result is rounded once, as the standalone head-norm kernel does. Only the
-// four lanes of the row's quad take part in its shuffles, so callers may skip
-// whole quads (rows past the end), never single lanes of one.
-template <class Ld, class St>
-__device__ __forceinline__ void qk_norm_rope_quad(Ld ld, St st, const bf16* g, float eps,
-                                                  const float2* rope_row, int neox, int t) {
-  // the row's rotations first: the global loads then overlap the reads below
-  float2 cs[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) cs[j] = rope_row[16 * t + j];
-  float x[16], y[16];
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int i = 16 * t + j;
-    const int ia = neox ? i : 2 * i, ib = neox ? i + kAttnHd / 2 : 2 * i + 1;
-    x[j] = ld(ia);
-    y[j] = ld(ib);
-    ss = fmaf(x[j], x[j], ss);
-    ss = fmaf(y[j], y[j], ss);
-  }
-  const unsigned quad = 0xFu << (threadIdx.x & 28);
-  ss += __shfl_xor_sync(quad, ss, 1);
-  ss += __shfl_xor_sync(quad, ss, 2);
-  const float inv = rsqrtf(ss / static_cast<float>(kAttnHd) + eps);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int i = 16 * t + j;
-    const int ia = neox ? i : 2 * i, ib = neox ? i + kAttnHd / 2 : 2 * i + 1;
-    const float a = x[j] * inv * __bfloat162float(g[ia]);
-    const float b = y[j] * inv * __bfloat162float(g[ib]);
-    st(ia, a * cs[j].x - b * cs[j].y);
-    st(ib, a * cs[j].y + b * cs[j].x);
-  }
-}
-
 // Before a kernel waits on the ones still running: asks L2 for the context
 // keys (thread 0) and values (thread 1) of key split s of kv head g. The ring
 // state read here may be older than the one the kernel then uses (a round

@@ -191,19 +191,6 @@ struct AttnArgs {
   KTrace trace;                // attention kernel; the separate merge kernel uses slot + 1
                                // (its phase mark slot + 4), the attention's phase marks
                                // slots + 2 and + 3
-  // When qn is set (tensor-core path only), q and the block's k rows are the
-  // raw projections: the kernel applies the per-head RMSNorm (gains qn / kn,
-  // [hd]) and RoPE (rope[m * hd/2 + i] for block row m) as it loads them.
-  const void* qn; const void* kn;
-  const float2* rope;
-  int neox;
-  float eps;
-  // Tensor-core kernels only: q, kb and vb point into the fp32 sums of a
-  // kEpiRed QKV GEMM ([rows][ldq] floats, ldkv == ldq); each value is rounded
-  // to bf16 as it is loaded (the GEMM's output rounding). The split-merge
-  // kernel then clears those sums: zero_acc [zero_n] floats.
-  int qkv_f32;
-  float* zero_acc; int zero_n;
   // Batch of nseq sequences (0 or 1: one): sequence s (blockIdx.z) has its
   // own ring state ring[s], ring rows seq_kv elements after sequence s - 1's,
   // its rows s * rows .. of q, kb, vb, out and the RoPE table, and its own
@@ -216,21 +203,18 @@ struct AttnArgs {
   // before the attention's own dependency resolves.
   int early_ctx;
 };
-// Points a's per-sequence operands at sequence s: q, kb, vb hold elements of
-// qkv_esz bytes, the ring and out of esz bytes; partial rows are part_stride
-// floats per query.
-__device__ __forceinline__ void attn_select_seq(AttnArgs& a, int s, int nsplit, int qkv_esz, int esz,
-                                                int part_stride) {
+// Points a's per-sequence operands at sequence s: q, kb, vb, the ring and out
+// hold elements of esz bytes; partial rows are part_stride floats per query.
+__device__ __forceinline__ void attn_select_seq(AttnArgs& a, int s, int nsplit, int esz, int part_stride) {
   if (s == 0) return;
   const int Qn = a.rows * (a.nq / a.nkv);
   a.ring += s;
-  a.q = static_cast<const char*>(a.q) + (size_t)s * a.rows * a.ldq * qkv_esz;
-  a.kb = static_cast<const char*>(a.kb) + (size_t)s * a.rows * a.ldkv * qkv_esz;
-  a.vb = static_cast<const char*>(a.vb) + (size_t)s * a.rows * a.ldkv * qkv_esz;
+  a.q = static_cast<const char*>(a.q) + (size_t)s * a.rows * a.ldq * esz;
+  a.kb = static_cast<const char*>(a.kb) + (size_t)s * a.rows * a.ldkv * esz;
+  a.vb = static_cast<const char*>(a.vb) + (size_t)s * a.rows * a.ldkv * esz;
   a.ring_k = static_cast<const char*>(a.ring_k) + (size_t)s * a.seq_kv * esz;
   a.ring_v = static_cast<const char*>(a.ring_v) + (size_t)s * a.seq_kv * esz;
   a.out = static_cast<char*>(a.out) + (size_t)s * a.rows * a.ldo * esz;
-  if (a.rope) a.rope += (size_t)s * a.rows * (a.hd / 2);
   a.partial += (size_t)s * a.nkv * nsplit * Qn * part_stride;
 }
 cudaError_t launch_attention(int dtype, const AttnArgs& a, cudaStream_t st);

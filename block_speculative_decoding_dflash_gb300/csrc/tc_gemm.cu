@@ -560,13 +560,20 @@ cudaError_t launch_tc(const TcGemmArgs& a, int grid, bool pdl, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI, S, P>, a);
 }
 
+// Every tensor-core kernel asks for the largest shared-memory carveout, so
+// that an SM moving from one of them to the next (the GEMMs of a layer take
+// 131 to 197 KB) never has to drain to reconfigure its L1 / shared split.
 template <int BN, int EPI>
 cudaError_t attr_tc() {
   constexpr int S = stages_for<BN, EPI>();
   constexpr int P = pairs_for<BN, EPI>();
   constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
-  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<BN, NV, S, P>::kSmem);
+  const cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S, P>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Cfg<BN, NV, S, P>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, S, P>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
 }
 
 // ---------------------------------------------------------------------------
@@ -842,6 +849,8 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess) return e;
   return attr_tc<32, kEpiArgmax>();
 }
 
