@@ -150,6 +150,62 @@ def make_weights(cfg: dict, seed: int = 0) -> dict:
 LAYER_KEYS = ("in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo",
               "post_norm", "wg", "wu", "wd")
 
+# Synthetic targets for the verify forward: Qwen3-shaped causal decoders whose
+# width is the drafter's target_hidden and whose captured layers feed its
+# encoder.fc (k_target_layers of them); sliding layers with the drafter's
+# window except the last, which sees its whole history.
+TARGETS = {
+    "tiny": dict(
+        n_layers=6, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16,
+        intermediate=128, vocab=1024, window=16, full_layers=(5,),
+        capture=(1, 2, 3, 4, 5), rope_neox=True, rope_theta=1e6, rms_eps=1e-6,
+        dtype="f32", max_block=16, max_context=512, weight_std=0.05,
+    ),
+    "muse": dict(
+        n_layers=6, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        intermediate=6144, vocab=202048, window=2048, full_layers=(5,),
+        capture=(1, 2, 3, 4, 5), rope_neox=True, rope_theta=1e6, rms_eps=1e-6,
+        dtype="bf16", max_block=32, max_context=8192, weight_std=0.02,
+    ),
+}
+
+
+def target_config(name: str, **overrides) -> dict:
+    cfg = copy.deepcopy(TARGETS[name])
+    cfg.update(overrides)
+    return cfg
+
+
+def make_target_weights(tcfg: dict, drafter_weights: dict, seed: int = 1) -> dict:
+    """Target weights: its own layers (N(0, weight_std), gains 1.0) and final
+    norm; the raw embedding table and the untied lm_head are the drafter's
+    (the drafter binds the target's)."""
+    dt, std = tcfg["dtype"], tcfg["weight_std"]
+    H, nq, nkv, hd, I = (tcfg[k] for k in ("hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate"))
+    w = {"embed": drafter_weights["embed"], "lm_head": drafter_weights["lm_head"],
+         "final_norm": ones((H,), dt), "layers": []}
+    for l in range(tcfg["n_layers"]):
+        p = f"target{l}."
+        w["layers"].append({
+            "in_norm": ones((H,), dt),
+            "wq": normal(seed, p + "wq", (nq * hd, H), std, dt),
+            "wk": normal(seed, p + "wk", (nkv * hd, H), std, dt),
+            "wv": normal(seed, p + "wv", (nkv * hd, H), std, dt),
+            "q_norm": ones((hd,), dt),
+            "k_norm": ones((hd,), dt),
+            "wo": normal(seed, p + "wo", (H, nq * hd), std, dt),
+            "post_norm": ones((H,), dt),
+            "wg": normal(seed, p + "wg", (I, H), std, dt),
+            "wu": normal(seed, p + "wu", (I, H), std, dt),
+            "wd": normal(seed, p + "wd", (H, I), std, dt),
+        })
+    return w
+
+
+def make_prompt(tcfg: dict, rows: int, seed: int = 0) -> np.ndarray:
+    """Prompt token ids, uniform over the vocabulary."""
+    return _stream(seed, "prompt").integers(0, tcfg["vocab"], rows).astype(np.int32)
+
 
 def make_context(cfg: dict, rows: int, seed: int = 0, name: str = "context") -> np.ndarray:
     """Captured target residual rows [rows, k * target_hidden], N(0, 1)."""

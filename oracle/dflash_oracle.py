@@ -51,6 +51,20 @@ Readings of points the pages leave open:
      sampling rule accepts d with probability p(d); the bonus after a
      rejection comes from p with d removed; uniforms are inputs and the
      inverse CDF runs in vocabulary order.
+ R14 The synthetic target is a Qwen3-shaped causal decoder with the drafter's
+     layer layout (R1, R2, R3, R12). Its sliding layers see key j from query
+     i iff 0 <= pos_i - pos_j <= W; its full layers iff pos_j <= pos_i. It
+     shares the raw embedding table and the untied lm_head with the drafter.
+ R15 The captured residual rows are the residual stream after each capture
+     layer, concatenated in capture order; the last capture layer may be the
+     last layer, whose output is the final norm's input.
+ R16 The target's logits are fp32 lm_head outputs of the final-normed rows,
+     without softcap (the greedy verify is unchanged by it; the sampled
+     verify applies it), rounded to the storage type as the GEMM stores them.
+ R17 A verify forward appends the block's K/V to every layer's cache; the
+     trim after the verify drops the last B - n rows of every layer (the
+     sliding layers' rings with the drafter's slack rule, the full layers'
+     caches append-only).
 
 Parity status: every function here has a named pin. The slack rule, the ring
 restore, accept = prefix + 1, the mask, attention, RoPE, RMSNorm, linear,
@@ -65,7 +79,13 @@ V row by hand, RoPE at the absolute position, no input norm), the draft's
 read-out rows through the final norm, lm_head and softcap, and the session's
 history against the ring model. The pages print no numbers for the layer
 layout itself (readings R1, R2, R4, R6, R12): those pins fix the reading
-taken, not a value from the pages.
+taken, not a value from the pages. The synthetic target (R14-R17) is pinned
+by ``tests/test_oracle_target.py``: the causal mask against triangle / band
+constructions and brute force, the masked attention against torch's
+scaled-dot-product attention, identity layers (raw-embedding streams, plain
+logits), the capture order, uniform attention (the causal mean of the
+visible values), one pass against prefill-then-verify, and a trim against
+never having appended the dropped rows.
 """
 
 from __future__ import annotations
@@ -83,6 +103,8 @@ __all__ = [
     "lm_head_argmax", "draft_block", "markov_chain",
     "verify_accept", "sampled_probs", "verify_sampled", "short_conv_block",
     "short_conv_rollback", "RingModel", "OracleSession", "stats_ratios",
+    "causal_mask", "causal_attention", "target_layer", "layer_window",
+    "target_forward", "TargetSession",
 ]
 
 
@@ -579,6 +601,141 @@ def stats_ratios(rounds: int, proposed: int, accepted: int) -> dict:
         "acceptance": accepted / proposed,
         "emitted": accepted + rounds,
     }
+
+
+# ---------------------------------------------------------------------------
+# The synthetic target: causal verify forward, residual capture, cache trim
+# ---------------------------------------------------------------------------
+
+def causal_mask(q_pos, k_pos, window: int) -> np.ndarray:
+    """Reading R14 (Muse page, "What changed", Muse target: sliding and full
+    caches): key j visible to query i iff pos_j <= pos_i, and for a sliding
+    layer (window > 0) also pos_i - pos_j <= window."""
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    k_pos = np.asarray(k_pos, dtype=np.int64)
+    d = q_pos[:, None] - k_pos[None, :]
+    vis = d >= 0
+    if window > 0:
+        vis &= d <= window
+    return vis
+
+
+def causal_attention(q, k, v, q_pos, k_pos, window: int) -> np.ndarray:
+    """Grouped-query attention under the causal (sliding or full) mask; the
+    same explicit score matrix and fp64 softmax as ``attention``."""
+    bq, nq, hd = q.shape
+    group = nq // k.shape[1]
+    mask = causal_mask(q_pos, k_pos, window)
+    out = np.zeros((bq, nq, hd), dtype=np.float64)
+    for h in range(nq):
+        g = h // group
+        sc = (q[:, h, :] @ k[:, g, :].T) / math.sqrt(hd)
+        sc = np.where(mask, sc, -np.inf)
+        sc = sc - sc.max(axis=1, keepdims=True)
+        pr = np.exp(sc)
+        pr = pr / pr.sum(axis=1, keepdims=True)
+        out[:, h, :] = pr @ v[:, g, :]
+    return out
+
+
+def target_layer(tcfg, lw, x, pos, hist_k, hist_v, hist_pos, window):
+    """One target decoder layer over rows x at positions pos (reading R14):
+    the drafter's layer with a causal mask, attending to the layer's cache
+    (hist_*) followed by the rows themselves. Returns the layer output and the
+    rows' K and V (normed + rotated K, rounded V), which join the cache."""
+    rnd = rounder(tcfg["dtype"])
+    eps = tcfg["rms_eps"]
+    nq, nkv, hd = tcfg["n_q_heads"], tcfg["n_kv_heads"], tcfg["head_dim"]
+    rows = x.shape[0]
+    xn = rnd(rmsnorm(x, lw["in_norm"], eps))
+    q = rnd(linear(xn, lw["wq"])).reshape(rows, nq, hd)
+    k = rnd(linear(xn, lw["wk"])).reshape(rows, nkv, hd)
+    v = rnd(linear(xn, lw["wv"])).reshape(rows, nkv, hd)
+    q = rnd(rope(head_rmsnorm(q, lw["q_norm"], eps), pos, tcfg["rope_theta"], tcfg["rope_neox"]))
+    k = rnd(rope(head_rmsnorm(k, lw["k_norm"], eps), pos, tcfg["rope_theta"], tcfg["rope_neox"]))
+    keys = np.concatenate([hist_k, k], axis=0)
+    vals = np.concatenate([hist_v, v], axis=0)
+    kpos = np.concatenate([hist_pos, pos])
+    a = rnd(causal_attention(q, keys, vals, pos, kpos, window))
+    o = rnd(linear(a.reshape(rows, nq * hd), lw["wo"]))
+    h = rnd(x + o)
+    hn = rnd(rmsnorm(h, lw["post_norm"], eps))
+    g = rnd(linear(hn, lw["wg"]))
+    u = rnd(linear(hn, lw["wu"]))
+    sw = rnd(silu(g) * u)
+    d = rnd(linear(sw, lw["wd"]))
+    return rnd(h + d), k, v
+
+
+def layer_window(tcfg, layer: int) -> int:
+    """A full layer attends to its whole history (window 0), a sliding one
+    through the target's window."""
+    return 0 if layer in tuple(tcfg["full_layers"]) else tcfg["window"]
+
+
+def target_forward(tcfg, tw, tokens, pos0, hist):
+    """The target's forward over ``tokens`` at positions pos0.. (readings
+    R14-R16). ``hist`` holds per layer (K, V, positions) of the rows already
+    in its cache. Returns the logits [rows, V] (storage-rounded fp32, no
+    softcap), the captured residual rows [rows, len(capture) * H] and the
+    rows' per-layer K and V."""
+    rnd = rounder(tcfg["dtype"])
+    toks = np.asarray(tokens, dtype=np.int64)
+    pos = pos0 + np.arange(toks.size, dtype=np.int64)
+    x = rnd(tw["embed"][toks])
+    streams, new_k, new_v = {}, [], []
+    for li, lw in enumerate(tw["layers"]):
+        hk, hv, hp = hist[li]
+        x, k, v = target_layer(tcfg, lw, x, pos, hk, hv, hp, layer_window(tcfg, li))
+        streams[li] = x
+        new_k.append(k)
+        new_v.append(v)
+    captured = np.concatenate([streams[l] for l in tcfg["capture"]], axis=1)
+    xf = rnd(rmsnorm(x, tw["final_norm"], tcfg["rms_eps"]))
+    logits = rnd(linear(xf, tw["lm_head"]).astype(np.float32).astype(np.float64))
+    return {"logits": logits, "captured": captured, "k": new_k, "v": new_v, "positions": pos}
+
+
+@dataclass
+class TargetSession:
+    """The target's caches as dense per-layer histories keyed by absolute
+    position (reading R17): a forward appends its rows, ``commit`` keeps the
+    first n rows of the last forward and drops the rest."""
+
+    tcfg: dict
+    tw: dict
+    pos: int = 0
+    hist: list = field(default_factory=list)
+    last_rows: int = 0
+
+    def __post_init__(self):
+        nkv, hd = self.tcfg["n_kv_heads"], self.tcfg["head_dim"]
+        if not self.hist:
+            self.hist = [(np.zeros((0, nkv, hd)), np.zeros((0, nkv, hd)), np.zeros(0, dtype=np.int64))
+                         for _ in self.tw["layers"]]
+
+    def forward(self, tokens) -> dict:
+        out = target_forward(self.tcfg, self.tw, tokens, self.pos, self.hist)
+        for li in range(len(self.hist)):
+            hk, hv, hp = self.hist[li]
+            self.hist[li] = (np.concatenate([hk, out["k"][li]]), np.concatenate([hv, out["v"][li]]),
+                             np.concatenate([hp, out["positions"]]))
+        self.last_rows = len(tokens)
+        self.pos += len(tokens)
+        return out
+
+    def commit(self, n: int) -> None:
+        """Trim the last forward's rows past the first n (trim(rows - n))."""
+        drop = self.last_rows - n
+        if not 0 <= drop <= self.last_rows:
+            raise ValueError("short rewind")
+        if drop:
+            self.hist = [(k[:-drop], v[:-drop], p[:-drop]) for k, v, p in self.hist]
+            self.pos -= drop
+        self.last_rows = 0
+
+    def cache(self, layer: int):
+        return self.hist[layer]
 
 
 # ---------------------------------------------------------------------------
