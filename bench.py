@@ -452,8 +452,8 @@ def side_configs(job, args, peak, device):
     (widths 8 and 10, rank-256 Markov chain, append-only cache), the
     long-context slab stress (16384-row slab, window drop, width 16, keep ~
     U{0..16}), the Muse block-width sweep (widths 4..129 x planting
-    probability 0.3 / 0.7 / 0.95) and batched rounds (2 to 8 sequences at
-    widths 4 and 16)."""
+    probability 0.3 / 0.7 / 0.95), batched rounds (2 to 8 sequences at
+    widths 4 and 16) and rounds with the synthetic target's verify forward."""
     import torch
     B, synth = job.B, job.synth
     R = args.config_rounds
@@ -610,7 +610,106 @@ def side_configs(job, args, peak, device):
                       "note": "one round drafts, verifies and commits every sequence of the batch; "
                               "the weights stream once per round for all of them",
                       "setup_s": round(time.time() - t0, 1)}
+    out["target_verify"] = target_rounds(job, R, peak, device)
     return out
+
+
+def target_bytes(tcfg, block, pos):
+    """Algorithmic HBM bytes of one verify forward of the synthetic target at
+    committed length pos: its layer weights, the cache rows its layers read
+    (window rows for a sliding layer, the whole history for a full one), the
+    lm_head, the block's logits and captured rows written, its K/V rows."""
+    H, I, hd, L = tcfg["hidden"], tcfg["intermediate"], tcfg["head_dim"], tcfg["n_layers"]
+    qdim, kvdim, V = tcfg["n_q_heads"] * hd, tcfg["n_kv_heads"] * hd, tcfg["vocab"]
+    layer_w = (H * (qdim + 2 * kvdim) + qdim * H + 3 * H * I + 2 * H + 2 * hd) * 2
+    full = set(tcfg["full_layers"])
+    kv = sum(2 * (pos if l in full else min(pos, tcfg["window"])) * kvdim * 2 for l in range(L))
+    return (L * layer_w + kv + V * H * 2 + H * 2 + block * V * 2
+            + block * len(tcfg["capture"]) * H * 2 + L * 2 * block * kvdim * 2)
+
+
+def target_rounds(job, R, peak, device):
+    """Rounds with the synthetic target's real verify forward in place of the
+    stand-in logits: a 2048-token prompt prefilled through the target (its
+    captured rows are the drafter's context), then rounds of draft -> target
+    verify forward -> accept -> append the captured rows -> both commits, one
+    CUDA graph per width, timed with CUDA events on the shared stream."""
+    import torch
+    B, synth = job.B, job.synth
+    t0 = time.time()
+    cfg = job.cfg
+    tcfg = synth.target_config("muse")
+    tw = synth.make_target_weights(tcfg, job.w)
+    twd = {"embed": job.wd["embed"], "lm_head": job.wd["lm_head"],
+           "final_norm": B.to_device(tw["final_norm"], "bf16", device),
+           "layers": [{k: B.to_device(v, "bf16", device) for k, v in lw.items()} for lw in tw["layers"]]}
+    stream = torch.cuda.Stream()
+    target = B.TargetContext(tcfg, twd, stream=stream)
+    drafter = B.DFlashContext(cfg, job.wd, stream=stream)
+    P, mb, kin, V = 2048, tcfg["max_block"], len(tcfg["capture"]) * tcfg["hidden"], tcfg["vocab"]
+    prompt = torch.tensor(synth.make_prompt(tcfg, P, seed=21), device=device)
+    cap = torch.empty(P, kin, dtype=torch.bfloat16, device=device)
+    last = torch.empty(1, V, dtype=torch.bfloat16, device=device)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for r0 in range(0, P, mb):
+        rows = min(mb, P - r0)
+        fin = r0 + rows == P
+        target.forward(prompt[r0:], rows, 1 if fin else 0, last if fin else None, cap[r0:])
+    p1.record(stream)
+    p1.synchronize()
+    prefill_ms = p0.elapsed_time(p1)
+    drafter.ingest_context(cap, P, 0, int(last.float().argmax().item()))
+    wmax = 16
+    ids = torch.zeros(wmax, dtype=torch.int32, device=device)
+    tok = torch.zeros(wmax, dtype=torch.int32, device=device)
+    n = torch.zeros(1, dtype=torch.int32, device=device)
+    logits = torch.empty(wmax, V, dtype=torch.bfloat16, device=device)
+    capb = torch.empty(wmax, kin, dtype=torch.bfloat16, device=device)
+
+    def one(w):
+        target._capturing = drafter._capturing
+        drafter.draft_block(w, ids)
+        target.verify(drafter, w, ids, logits, capb)
+        drafter.verify_accept(logits, w, ids, tok, n)
+        drafter.append_block(capb, w)
+        drafter.commit(-1)
+        target.commit(n, w)
+
+    res = {}
+    for w in (4, 16):
+        one(w)
+        drafter.capture_begin()
+        one(w)
+        drafter.capture_end(w)
+        target._capturing = False
+        for _ in range(4):
+            drafter.graph_launch(w)
+        st0 = drafter.stats()
+        pos0 = drafter.state()["position"]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(R):
+            drafter.graph_launch(w)
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        st1 = drafter.stats()
+        us = ms * 1e3 / R
+        nb = round_bytes(cfg, w, cfg["window"]) + target_bytes(tcfg, w, pos0)
+        assert target.state()["error"] == 0 and drafter.state()["error"] == 0
+        res[str(w)] = {"rounds_per_s": round(R / (ms / 1e3), 1),
+                       "emitted_tok_s": round((st1["emitted"] - st0["emitted"]) / (ms / 1e3), 1),
+                       "accepted_per_round": round((st1["accepted"] - st0["accepted"]) / R, 3),
+                       "round_us": round(us, 1), "round_bytes": nb,
+                       "round_frac": round(nb / (us * 1e-6) / 1e9 / peak, 3)}
+    drafter.close()
+    target.close()
+    return {"workload": "muse_bf16_target6L_w2048_full1_prompt2048_block4and16",
+            "prefill_ms": round(prefill_ms, 3), "rounds_timed_per_width": R, "by_width": res,
+            "note": "random-weight target and drafter: acceptance is what two unrelated random models "
+                    "give; the round time is the measurement",
+            "setup_s": round(time.time() - t0, 1)}
 
 
 def cpu_baseline(job, n_rounds, mix):

@@ -52,6 +52,19 @@ class Weights(ctypes.Structure):
         ("layers", ctypes.POINTER(ctypes.c_void_p))]
 
 
+class TargetConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "vocab", "window")] + [
+        ("full_layers", ctypes.c_uint64), ("n_capture", ctypes.c_int32), ("capture", ctypes.c_int32 * 8)] + [
+        (n, ctypes.c_int32) for n in ("rope_neox", "max_block", "dtype", "max_context")] + [
+        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+class TargetWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("embed", "final_norm", "lm_head")] + [
+        ("layers", ctypes.POINTER(ctypes.c_void_p))]
+
+
 class Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("rounds", "draft_n", "accepted", "emitted")]
 
@@ -124,6 +137,12 @@ _sig("dflash_ingest_gemm_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float),
 _sig("dflash_lm_head_elapsed_ms", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_float))
 _sig("dflash_synth_target", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
      _vp, _vp, _vp)
+_sig("dflash_target_create", ctypes.c_int, ctypes.POINTER(TargetConfig), ctypes.POINTER(TargetWeights), _vp,
+     ctypes.POINTER(_vp))
+_sig("dflash_target_forward", ctypes.c_int, _vp, _vp, _i32, _i32, _vp, _vp)
+_sig("dflash_target_verify", ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp)
+_sig("dflash_target_commit", ctypes.c_int, _vp, _vp, _i32)
+_sig("dflash_target_full_ring", ctypes.c_int, _vp, ctypes.POINTER(_vp))
 _sig("ring_cache_create", ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
      ctypes.POINTER(_vp))
 _sig("ring_cache_create_ex", ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
@@ -495,3 +514,71 @@ def short_conv_rollback(prev_state, bx, n_dev, layers, lcache, channels, block, 
                                         BF16 if dtype == "bf16" else F32, _ptr(state_out), st)
     if rc:
         raise DFlashError(rc, last_error(None))
+
+
+def make_target_config(tcfg: dict) -> TargetConfig:
+    """C target config from a config dict (the keys of ``synth.TARGETS``)."""
+    c = TargetConfig()
+    for k in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "vocab", "window",
+              "max_block", "max_context"):
+        setattr(c, k, int(tcfg[k]))
+    c.full_layers = sum(1 << int(l) for l in tcfg.get("full_layers", ()))
+    cap = tuple(int(l) for l in tcfg["capture"])
+    c.n_capture = len(cap)
+    for i, l in enumerate(cap):
+        c.capture[i] = l
+    c.rope_neox = 1 if tcfg.get("rope_neox", True) else 0
+    c.dtype = BF16 if tcfg["dtype"] == "bf16" else F32
+    c.rope_theta = float(tcfg.get("rope_theta", 1e6))
+    c.rms_eps = float(tcfg.get("rms_eps", 1e-6))
+    return c
+
+
+class TargetContext(DFlashContext):
+    """The synthetic target (C: dflash_target_create): the verify forward,
+    residual capture and cache trim. State, rings, graphs and close come from
+    DFlashContext."""
+
+    def __init__(self, tcfg: dict, weights: dict, stream: torch.cuda.Stream | None = None):
+        self.cfg = dict(tcfg)
+        self.n_seq = 1
+        self.ccfg = make_target_config(tcfg)
+        self.weights = weights
+        self.stream = stream or torch.cuda.Stream()
+        layer_ptrs = []
+        for lw in weights["layers"]:
+            layer_ptrs += [lw[k].data_ptr() for k in LAYER_KEYS]
+        self._layers = (ctypes.c_void_p * len(layer_ptrs))(*layer_ptrs)
+        w = TargetWeights()
+        w.embed = weights["embed"].data_ptr()
+        w.final_norm = weights["final_norm"].data_ptr()
+        w.lm_head = weights["lm_head"].data_ptr()
+        w.layers = ctypes.cast(self._layers, ctypes.POINTER(ctypes.c_void_p))
+        h = _vp()
+        rc = lib.dflash_target_create(ctypes.byref(self.ccfg), ctypes.byref(w), self.stream.cuda_stream,
+                                      ctypes.byref(h))
+        if rc:
+            raise DFlashError(rc, last_error(None))
+        self.h = h.value
+        self._capturing = False
+
+    def forward(self, tokens, rows, logit_rows=0, logits=None, captured=None):
+        self._prep()
+        self._check(lib.dflash_target_forward(self.h, _ptr(tokens), rows, logit_rows, _ptr(logits),
+                                              _ptr(captured)))
+
+    def verify(self, drafter, block, draft_ids, logits, captured=None):
+        self._prep()
+        self._check(lib.dflash_target_verify(self.h, drafter.h, block, _ptr(draft_ids), _ptr(logits),
+                                             _ptr(captured)))
+
+    def commit(self, n, block):
+        """Trim block - n rows of every layer's cache; n is a DEVICE int32
+        tensor (the verify's n)."""
+        self._prep()
+        self._check(lib.dflash_target_commit(self.h, _ptr(n), block))
+
+    def full_ring(self) -> RingCache | None:
+        h = _vp()
+        self._check(lib.dflash_target_full_ring(self.h, ctypes.byref(h)))
+        return RingCache(handle=h.value, owner=self) if h.value else None

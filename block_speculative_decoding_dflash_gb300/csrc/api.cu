@@ -182,6 +182,15 @@ struct dflash_ctx {
   int* ids_all = nullptr;                      // [R] read-out ids of every block row (batch)
   float* maxv_all = nullptr;                   // [R]
   unsigned* vf_ctr = nullptr;                  // [nseq] verify tickets
+  // the synthetic target (dflash_target_create): causal layers, the full
+  // layers' append-only cache beside the sliding ring, residual capture
+  bool is_target = false;
+  ring_cache* ring_full = nullptr;
+  std::vector<int> full_idx;                   // per layer: its index in ring_full, -1 if it slides
+  std::vector<int> capture;                    // captured layers, in order
+  void* cap_out = nullptr;                     // the forward being enqueued: its captured rows
+  int* tok = nullptr;                          // [max_block] the verify block's tokens
+  void* fc_unused = nullptr;                   // a zeroed stand-in for the drafter-only encoder.fc
   float* acc = nullptr;                        // [R][H] fp32 sums of the kEpiRed GEMMs, zero between uses
   float* qkv_acc = nullptr;                    // [R][qkv_n] fp32 sums of the QKV GEMM, zero between uses
   float* gu_acc = nullptr;                     // [R][2 I] fp32 gate / up sums, zero between uses
@@ -542,6 +551,18 @@ int context_rows_wide(dflash_ctx* c, const void* resid, int rows, void* f, void*
   return DFLASH_OK;
 }
 
+// A target forward's residual capture: the stream after `layer` (now in
+// c->x) into every capture slot that names it.
+int capture_stream(dflash_ctx* c, int layer, int rows) {
+  if (!c->is_target || !c->cap_out) return DFLASH_OK;
+  const size_t row = (size_t)c->H * c->esz, pitch = c->capture.size() * row;
+  for (size_t j = 0; j < c->capture.size(); ++j)
+    if (c->capture[j] == layer)
+      CK(c->err, cudaMemcpy2DAsync(static_cast<char*>(c->cap_out) + j * row, pitch, c->x, row, row, rows,
+                                   cudaMemcpyDeviceToDevice, c->stream));
+  return DFLASH_OK;
+}
+
 int layer_forward(dflash_ctx* c, int l, int rows) {
   const int dt = c->dt;
   cudaStream_t st = c->stream;
@@ -551,10 +572,12 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   // The residual GEMMs (O, down) of the tensor-core path add their fp32 sums
   // into c->acc and leave the residual add to the RMSNorm that follows them:
   // x = rnd(x + rnd(acc)), then the norm of x.
-  if (tc && l > 0)
+  if (tc && l > 0) {
     CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H,
                                     eps, st, ktrace_slot(c, ln + "in_norm")));
-  else
+    int rc = capture_stream(c, l - 1, rows);   // x now holds layer l - 1's output
+    if (rc) return rc;
+  } else
     CK(c->err, launch_rmsnorm(dt, c->x, c->H, LW(c, l, kInNorm), c->xn, c->H, rows, c->H, eps, st,
                               ktrace_slot(c, ln + "in_norm")));
   const int bi = bn_index(rows);
@@ -595,21 +618,31 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
   at.kb = static_cast<char*>(c->qkv) + (size_t)c->qdim * c->esz;
   at.vb = static_cast<char*>(c->qkv) + (size_t)(c->qdim + c->kvdim) * c->esz;
   at.ldkv = c->qkv_n;
-  const size_t lay = (size_t)l * c->nkv * c->ring->cap * c->hd * c->esz;
-  at.ring_k = static_cast<char*>(c->ring->k) + lay;
-  at.ring_v = static_cast<char*>(c->ring->v) + lay;
-  at.cap = c->ring->cap;
-  at.ring = c->ring->st;
-  at.window = c->cfg.window;
+  // a target's full layer attends over its append-only cache, causally
+  const bool full = c->is_target && c->full_idx[l] >= 0;
+  ring_cache* rg = full ? c->ring_full : c->ring;
+  const size_t lay = (size_t)(full ? c->full_idx[l] : l) * c->nkv * rg->cap * c->hd * c->esz;
+  at.ring_k = static_cast<char*>(rg->k) + lay;
+  at.ring_v = static_cast<char*>(rg->v) + lay;
+  at.cap = rg->cap;
+  at.ring = rg->st;
+  at.window = full ? 0 : c->cfg.window;
+  at.causal = c->is_target ? 1 : 0;
   at.rows = rows / c->nseq; at.nq = c->nq; at.nkv = c->nkv; at.hd = c->hd;
   at.nseq = c->nseq; at.seq_kv = (long long)seq_kv_elems(c);
-  at.max_ctx = c->max_ctx;
+  at.max_ctx = full ? static_cast<int>(rg->cap) : c->cfg.window > 0 ? c->cfg.window : c->max_ctx;
   at.partial = c->attn_part;
   at.out = c->attn; at.ldo = c->qdim;
   at.err = c->tc_err;
   at.trace = ktrace_slot(c, ln + "attn", 5);
   at.early_ctx = qkv_red ? 1 : 0;                // launch_qkv_finish precedes it
   CK(c->err, launch_attention(dt, at, st));
+  // a target's block rows join its cache (positions offset .., advanced once
+  // the whole forward is enqueued)
+  if (c->is_target)
+    CK(c->err, launch_kv_rows_to_ring(dt, c->qkv, c->qkv_n, c->qdim, c->qdim + c->kvdim, rows, c->nkv, c->hd,
+                                      static_cast<char*>(rg->k) + lay, static_cast<char*>(rg->v) + lay, rg->cap,
+                                      rg->append_only, rg->st, st));
   if (tc) {
     TcGemmArgs t = tc_args(c, rows, c->H, c->qdim, kEpiRed);
     tc_segments(t, {{&c->lmaps[l].wo, c->H}});
@@ -651,14 +684,16 @@ int layer_forward(dflash_ctx* c, int l, int rows) {
     LinearArgs d = lin_args(c->sbuf, c->I, c->x, c->H, rows, c->H, c->I);
     d.w[0] = LW(c, l, kWd); d.epi = kEpiResid; d.r = c->x; d.ldr = c->H;
     CK(c->err, launch_linear_rows(dt, d, st));
+    int rc = capture_stream(c, l, rows);
+    if (rc) return rc;
   }
   return DFLASH_OK;
 }
 
 // Append-only rings: make sure `rows` more rows fit (syncs only when the
 // conservative host bound says they might not, and never while capturing).
-int ensure_room(dflash_ctx* c, int rows) {
-  ring_cache* r = c->ring;
+int ensure_room(dflash_ctx* c, int rows, ring_cache* r = nullptr) {
+  if (!r) r = c->ring;
   if (!r->append_only) return DFLASH_OK;
   if (r->pos_hi + rows - r->host_base <= r->cap) return DFLASH_OK;
   if (c->capturing)
@@ -757,6 +792,9 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
     if (g) cudaGraphExecDestroy(g);
   for (ring_cache* v : ctx->views) ring_free(v);
   ring_free(ctx->ring);
+  ring_free(ctx->ring_full);
+  cudaFree(ctx->tok);
+  cudaFree(ctx->fc_unused);
   cudaFree(ctx->arena);
   cudaFree(ctx->ktr);
   for (auto& ev : ctx->ing_ev)
@@ -766,8 +804,18 @@ void dflash_ctx_destroy(dflash_ctx* ctx) {
   delete ctx;
 }
 
+int ctx_create_impl(const dflash_config* cfg, const dflash_weights* w, int32_t n_seq, void* stream,
+                    dflash_ctx** out, int max_ctx_floor);
+
 int dflash_ctx_create_batched(const dflash_config* cfg, const dflash_weights* w, int32_t n_seq,
                               void* stream, dflash_ctx** out) {
+  return ctx_create_impl(cfg, w, n_seq, stream, out, 0);
+}
+
+// max_ctx_floor: context rows the attention scratch must cover at least (the
+// target's full layers see more than its window).
+int ctx_create_impl(const dflash_config* cfg, const dflash_weights* w, int32_t n_seq, void* stream,
+                    dflash_ctx** out, int max_ctx_floor) {
   std::string& err = g_create_err;
   if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
   *out = nullptr;
@@ -816,6 +864,7 @@ int dflash_ctx_create_batched(const dflash_config* cfg, const dflash_weights* w,
   c->nseq = n_seq;
   c->rows_max = n_seq * cfg->max_block;
   c->max_ctx = cfg->window > 0 ? cfg->window : cfg->max_context;
+  if (c->max_ctx < max_ctx_floor) c->max_ctx = max_ctx_floor;
 
   rc = ring_create_impl(cfg->n_layers, c->nkv, c->hd, cfg->window, cfg->max_block, cfg->dtype,
                         cfg->max_context, 0, c->stream, &c->ring, err, n_seq);
@@ -953,6 +1002,7 @@ int dflash_ingest_context(dflash_ctx* c, const void* resid, int64_t rows, int64_
 int dflash_ingest_context_seq(dflash_ctx* c, int32_t seq, const void* resid, int64_t rows, int64_t first_pos,
                               int32_t anchor) {
   if (!c) return DFLASH_EINVAL;
+  if (c->is_target) return fail(c->err, DFLASH_EINVAL, "a target context takes the dflash_target_* calls");
   if (seq < 0 || seq >= c->nseq) return fail(c->err, DFLASH_ERANGE, "seq %d outside [0, %d)", seq, c->nseq);
   c->seq_cur = seq;
   if (rows <= 0) return fail(c->err, DFLASH_EEMPTY, "empty context (rows = %lld)", (long long)rows);
@@ -1014,6 +1064,7 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
 int dflash_draft_block(dflash_ctx* c, int32_t anchor, int64_t anchor_pos, int32_t block,
                        int32_t* draft_ids) {
   if (!c) return DFLASH_EINVAL;
+  if (c->is_target) return fail(c->err, DFLASH_EINVAL, "a target context takes the dflash_target_* calls");
   if (!draft_ids) return fail(c->err, DFLASH_EINVAL, "draft_ids is NULL");
   if (block < 2 || block > c->cfg.max_block)
     return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
@@ -1150,6 +1201,7 @@ int dflash_sync_round(dflash_ctx* c, int32_t* tokens_host, int32_t* n_host) {
 
 int dflash_append_block(dflash_ctx* c, const void* resid, int32_t block) {
   if (!c) return DFLASH_EINVAL;
+  if (c->is_target) return fail(c->err, DFLASH_EINVAL, "a target context takes the dflash_target_* calls");
   if (!resid || !aligned16(resid)) return fail(c->err, DFLASH_EINVAL, "resid is NULL or misaligned");
   if (block < 1 || block > c->cfg.max_block)
     return fail(c->err, DFLASH_ERANGE, "block %d outside [1, max_block=%d]", block, c->cfg.max_block);
@@ -1636,5 +1688,163 @@ int ring_cache_gather(ring_cache* r, int64_t pos0, int32_t count, void* k_out, v
 }
 
 const char* ring_cache_last_error(const ring_cache* r) { return r ? r->err.c_str() : g_create_err.c_str(); }
+
+// ---- the synthetic target ------------------------------------------------------
+
+int dflash_target_create(const dflash_target_config* tc, const dflash_target_weights* tw, void* stream,
+                         dflash_ctx** out) {
+  std::string& err = g_create_err;
+  if (!out) return fail(err, DFLASH_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!tc || !tw || !tw->embed || !tw->final_norm || !tw->lm_head || !tw->layers)
+    return fail(err, DFLASH_EINVAL, "a target config or weight pointer is NULL");
+  if (tc->n_layers < 1 || tc->n_layers > 64) return fail(err, DFLASH_ERANGE, "n_layers outside [1, 64]");
+  if (tc->window <= 0) return fail(err, DFLASH_EINVAL, "the sliding layers need a window > 0");
+  if (tc->max_block < 2 || tc->max_block > 32) return fail(err, DFLASH_ERANGE, "max_block outside [2, 32]");
+  if (tc->n_capture < 1 || tc->n_capture > 8) return fail(err, DFLASH_ERANGE, "n_capture outside [1, 8]");
+  for (int j = 0; j < tc->n_capture; ++j)
+    if (tc->capture[j] < 0 || tc->capture[j] >= tc->n_layers)
+      return fail(err, DFLASH_ERANGE, "capture layer %d outside [0, %d)", tc->capture[j], tc->n_layers);
+  if (tc->n_layers < 64 && (tc->full_layers >> tc->n_layers))
+    return fail(err, DFLASH_ERANGE, "full_layers names a layer past n_layers");
+  const int n_full = __builtin_popcountll(tc->full_layers);
+  if (n_full && tc->max_context < tc->max_block)
+    return fail(err, DFLASH_ERANGE, "max_context must hold at least max_block rows");
+  // the drafter's context machinery with a zeroed stand-in for its encoder.fc
+  // (a target never ingests residual rows)
+  dflash_config cfg{};
+  cfg.n_layers = tc->n_layers; cfg.hidden = tc->hidden; cfg.n_q_heads = tc->n_q_heads;
+  cfg.n_kv_heads = tc->n_kv_heads; cfg.head_dim = tc->head_dim; cfg.intermediate = tc->intermediate;
+  cfg.vocab = tc->vocab; cfg.window = tc->window; cfg.k_target_layers = 1; cfg.target_hidden = 64;
+  cfg.mask_token_id = 0; cfg.rope_neox = tc->rope_neox; cfg.max_block = tc->max_block;
+  cfg.kind = DFLASH_KIND_DFLASH; cfg.dtype = tc->dtype; cfg.max_context = tc->max_context;
+  cfg.rope_theta = tc->rope_theta; cfg.rms_eps = tc->rms_eps;
+  const size_t esz = tc->dtype == DFLASH_BF16 ? 2 : 4;
+  void* fc = nullptr;
+  cudaError_t e = cudaMalloc(&fc, (size_t)tc->hidden * 64 * esz);
+  if (e != cudaSuccess) return cuda_fail(err, e, "target allocation");
+  if ((e = cudaMemset(fc, 0, (size_t)tc->hidden * 64 * esz)) != cudaSuccess) {
+    cudaFree(fc);
+    return cuda_fail(err, e, "target allocation");
+  }
+  dflash_weights w{};
+  w.embed = tw->embed; w.fc = fc; w.hidden_norm = tw->final_norm; w.final_norm = tw->final_norm;
+  w.lm_head = tw->lm_head; w.layers = tw->layers;
+  dflash_ctx* c = nullptr;
+  int rc = ctx_create_impl(&cfg, &w, 1, stream, &c, n_full ? tc->max_context : 0);
+  if (rc) { cudaFree(fc); return rc; }
+  c->fc_unused = fc;
+  c->is_target = true;
+  c->full_idx.assign(tc->n_layers, -1);
+  for (int l = 0, k = 0; l < tc->n_layers; ++l)
+    if ((tc->full_layers >> l) & 1) c->full_idx[l] = k++;
+  c->capture.assign(tc->capture, tc->capture + tc->n_capture);
+  if (n_full) {
+    rc = ring_create_impl(n_full, c->nkv, c->hd, 0, tc->max_block, tc->dtype, tc->max_context, 0, c->stream,
+                          &c->ring_full, err);
+    if (rc) { dflash_ctx_destroy(c); return rc; }
+  }
+  if ((e = cudaMalloc(&c->tok, sizeof(int) * tc->max_block)) != cudaSuccess) {
+    dflash_ctx_destroy(c);
+    return cuda_fail(err, e, "target allocation");
+  }
+  c->has_context = true;
+  *out = c;
+  return DFLASH_OK;
+}
+
+int dflash_target_forward(dflash_ctx* c, const int32_t* tokens, int32_t rows, int32_t logit_rows, void* logits,
+                          void* captured) {
+  if (!c) return DFLASH_EINVAL;
+  if (!c->is_target) return fail(c->err, DFLASH_EINVAL, "not a target context (dflash_target_create)");
+  if (!tokens) return fail(c->err, DFLASH_EINVAL, "tokens is NULL");
+  if (rows < 1 || rows > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "rows %d outside [1, max_block=%d]", rows, c->cfg.max_block);
+  if (logit_rows < 0 || logit_rows > rows)
+    return fail(c->err, DFLASH_ERANGE, "logit_rows %d outside [0, rows=%d]", logit_rows, rows);
+  if ((logit_rows > 0) != (logits != nullptr))
+    return fail(c->err, DFLASH_EINVAL, "logits must be given exactly when logit_rows > 0");
+  if ((logits && !aligned16(logits)) || (captured && !aligned16(captured)))
+    return fail(c->err, DFLASH_EINVAL, "logits and captured must be 16-byte aligned");
+  if (c->ring_full) {
+    int rc = ensure_room(c, rows, c->ring_full);
+    if (rc) return rc;
+  }
+  const int dt = c->dt;
+  cudaStream_t st = c->stream;
+  CK(c->err, launch_rope_table(c->inv_freq, c->half, c->ring->st, 0, rows, c->rope, st));
+  CK(c->err, launch_embed_tokens(dt, c->embed, c->H, c->V, tokens, rows, c->x, c->rs, st));
+  c->cap_out = captured;
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    int rc = layer_forward(c, l, rows);
+    if (rc) { c->cap_out = nullptr; return rc; }
+  }
+  const bool tc = tc_rows(c, rows);
+  if (tc) {
+    CK(c->err, launch_resid_rmsnorm(c->x, c->H, c->acc, c->H, c->final_norm, c->xf, c->H, rows, c->H,
+                                    c->cfg.rms_eps, st, ktrace_slot(c, "final_norm")));
+    int rc = capture_stream(c, c->cfg.n_layers - 1, rows);
+    if (rc) { c->cap_out = nullptr; return rc; }
+  } else {
+    CK(c->err, launch_rmsnorm(dt, c->x, c->H, c->final_norm, c->xf, c->H, rows, c->H, c->cfg.rms_eps, st,
+                              ktrace_slot(c, "final_norm")));
+  }
+  c->cap_out = nullptr;
+  if (logit_rows > 0) {
+    const void* xf = static_cast<const char*>(c->xf) + (size_t)(rows - logit_rows) * c->H * c->esz;
+    if (tc) {
+      TcGemmArgs t = tc_args(c, logit_rows, c->V, c->H, kEpiStore);
+      tc_segments(t, {{&c->lm_map, c->V}});
+      if (!tc_encode_map(&t.b_map, xf, c->H, logit_rows, (uint64_t)c->H * 2, 64, bn_of(logit_rows)))
+        return fail(c->err, DFLASH_ECUDA, "cuTensorMapEncodeTiled failed for the final-normed rows");
+      t.y = logits; t.ldy = c->V;
+      t.trace = ktrace_slot(c, "target_logits", 4);
+      CK(c->err, tc_run(c, t));
+    } else {
+      LinearArgs a = lin_args(xf, c->H, logits, c->V, logit_rows, c->V, c->H);
+      a.w[0] = c->lm_head;
+      CK(c->err, launch_linear_rows(dt, a, st));
+    }
+  }
+  CK(c->err, launch_ring_advance(c->ring->st, rows, 0, st));
+  if (c->ring_full) {
+    CK(c->err, launch_ring_advance(c->ring_full->st, rows, 0, st));
+    c->ring_full->pos_hi += rows;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_target_verify(dflash_ctx* c, const dflash_ctx* drafter, int32_t block, const int32_t* draft_ids,
+                         void* logits, void* captured) {
+  if (!c || !drafter) return DFLASH_EINVAL;
+  if (!c->is_target || drafter->is_target)
+    return fail(c->err, DFLASH_EINVAL, "needs a target context and a drafter context");
+  if (drafter->nseq != 1) return fail(c->err, DFLASH_EINVAL, "the drafter must run one sequence");
+  if (drafter->stream != c->stream) return fail(c->err, DFLASH_EINVAL, "the drafter and the target must share a stream");
+  if (!draft_ids || !logits) return fail(c->err, DFLASH_EINVAL, "draft_ids or logits is NULL");
+  if (block < 2 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [2, max_block=%d]", block, c->cfg.max_block);
+  CK(c->err, launch_verify_tokens(drafter->rs, drafter->ring->st, draft_ids, block, c->tok, c->ring->st, c->rs,
+                                  c->stream));
+  return dflash_target_forward(c, c->tok, block, block, logits, captured);
+}
+
+int dflash_target_commit(dflash_ctx* c, const int32_t* n_dev, int32_t block) {
+  if (!c) return DFLASH_EINVAL;
+  if (!c->is_target) return fail(c->err, DFLASH_EINVAL, "not a target context (dflash_target_create)");
+  if (!n_dev) return fail(c->err, DFLASH_EINVAL, "n_dev is NULL");
+  if (block < 1 || block > c->cfg.max_block)
+    return fail(c->err, DFLASH_ERANGE, "block %d outside [1, max_block=%d]", block, c->cfg.max_block);
+  CK(c->err, launch_target_trim(c->ring->st, c->ring_full ? c->ring_full->st : nullptr, n_dev, block, c->rs,
+                                c->stream));
+  return DFLASH_OK;
+}
+
+int dflash_target_full_ring(dflash_ctx* c, ring_cache** out) {
+  if (!c || !out) return DFLASH_EINVAL;
+  if (!c->is_target) return fail(c->err, DFLASH_EINVAL, "not a target context (dflash_target_create)");
+  *out = c->ring_full;
+  return DFLASH_OK;
+}
 
 }  // extern "C"

@@ -1,4 +1,5 @@
-// Bidirectional sliding-window grouped-query attention of the drafter block
+// Sliding-window grouped-query attention of a block of rows (the drafter's
+// bidirectional mask, or a causal one for the target's verify forward)
 // over the ring cache plus the block's own K/V.
 //
 // Keys are addressed by absolute position: the ring holds position q in slot
@@ -91,8 +92,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(AttnArgs a, i
       float v = -INFINITY;
       if (kj < nk) {
         const long long kpos = kj < nctx ? kstart + kj : p + (kj - nctx);
-        const long long dist = qpos > kpos ? qpos - kpos : kpos - qpos;
-        if (a.window <= 0 || dist <= a.window) {
+        const long long dd = qpos - kpos;
+        const bool vis = a.causal ? (dd >= 0 && (a.window <= 0 || dd <= a.window))
+                                  : (a.window <= 0 || (dd < 0 ? -dd : dd) <= a.window);
+        if (vis) {
           float acc = 0.f;
           const float* kr = Ks + j * hdp;
           for (int d = 0; d < hd; ++d) acc = fmaf(q[d], kr[d], acc);

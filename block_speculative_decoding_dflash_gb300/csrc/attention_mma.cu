@@ -1,4 +1,5 @@
-// Bidirectional sliding-window GQA attention of the drafter block, bf16,
+// Sliding-window GQA attention of a block of rows (the drafter's
+// bidirectional mask, or a causal one for the target's verify forward), bf16,
 // head_dim 128, on tensor cores, one CTA per (split of kKeys = 128 keys, kv
 // head g); the queries of g are the block rows x its G query heads.
 //
@@ -160,10 +161,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
             const int kk = warp * 16 + nt * 8 + tig * 2 + c;
             const int kj = j0 + kk;
             bool vis = qi < Qn && kj < nk;
-            if (vis && a.window > 0) {
+            if (vis && (a.window > 0 || a.causal)) {
               const long long kpos = kj < nctx ? kstart + kj : p + (kj - nctx);
-              const long long d = qpos > kpos ? qpos - kpos : kpos - qpos;
-              vis = d <= a.window;
+              const long long d = qpos - kpos;
+              vis = a.causal ? (d >= 0 && (a.window <= 0 || d <= a.window)) : (d < 0 ? -d : d) <= a.window;
             }
             S.s[grp + hr * 8][kk] = vis ? sc[nt][hr * 2 + c] * scale : -INFINITY;
           }
@@ -415,10 +416,14 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   int lo = 0, hi = nk - 1;
   if (qi >= Qn) {
     lo = 1; hi = 0;
-  } else if (window > 0) {
+  } else {
     const long long rel = p + qi / G - kstart;           // query position - kstart
-    if (rel - window > lo) lo = static_cast<int>(rel - window);
-    if (rel + window < hi) hi = static_cast<int>(rel + window);
+    if (window > 0 && rel - window > lo) lo = static_cast<int>(rel - window);
+    if (a.causal) {
+      if (rel < hi) hi = static_cast<int>(rel);
+    } else if (window > 0 && rel + window < hi) {
+      hi = static_cast<int>(rel + window);
+    }
   }
   const float sl2 = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;   // scale * log2(e)
   bool ok = mbar_wait(&bar[0], 0);

@@ -39,6 +39,7 @@ struct RoundState {
 enum : int {
   kErrFull = 1,        // append-only ring overflow (rows skipped)
   kErrRange = 2,       // a token id outside the vocabulary reached a gather
+  kErrTrim = 16,       // a target trim longer than the rows appended since the last one
   kErrPos = 8,         // a draft's host-given anchor position was not the
                        // committed context length
 };

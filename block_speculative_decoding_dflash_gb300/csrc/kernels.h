@@ -159,6 +159,21 @@ cudaError_t launch_kv_acc_to_ring(float* acc, int ldacc, int rows, int L, int nk
 cudaError_t launch_qkv_finish(float* acc, int ldacc, void* out, int ldo, int rows, int nq, int nkv,
                               const void* qn, const void* kn, float eps, const float2* rope, int neox,
                               cudaStream_t st, KTrace trace = KTrace{nullptr, 0});
+// The synthetic target's verify forward: x[r] = embed[tokens[r]] (out-of-
+// range ids read row 0, kErrRange in rs); the verify block [drafter anchor,
+// d...] (kErrPos in trs unless the drafter's ring offset is the target's);
+// K / V rows of the finished QKV output into ring slots at ring->offset + r;
+// the trim of block - *n_dev rows on both ring states (kErrTrim in trs when
+// longer than the rows appended since the last trim).
+cudaError_t launch_embed_tokens(int dtype, const void* embed, int H, int vocab, const int* tokens, int rows,
+                                void* x, RoundState* rs, cudaStream_t st);
+cudaError_t launch_verify_tokens(const RoundState* drs, const RingState* dring, const int* d, int block,
+                                 int* tokens, const RingState* tring, RoundState* trs, cudaStream_t st);
+cudaError_t launch_kv_rows_to_ring(int dtype, const void* qkv, int ld, int kofs, int vofs, int rows, int nkv,
+                                   int hd, void* ring_k, void* ring_v, long long cap, int append_only,
+                                   RingState* ring, cudaStream_t st);
+cudaError_t launch_target_trim(RingState* a, RingState* b, const int* n_dev, int block, RoundState* trs,
+                               cudaStream_t st);
 // In place per-head RMSNorm + RoPE on buf[rows, heads, hd] (row stride ld).
 cudaError_t launch_head_norm_rope(int dtype, void* buf, int ld, int rows,
                                   int heads, int hd, const void* g, float eps,
@@ -183,6 +198,8 @@ struct AttnArgs {
   long long cap;
   const RingState* ring;       // offset = position of block row 0
   int window;                  // <= 0: unbounded
+  int causal;                  // 0: key visible iff |q - k| <= window (the drafter's bidirectional
+                               // sliding mask); 1: iff 0 <= q - k and (window <= 0 or q - k <= window)
   int rows, nq, nkv, hd;
   int max_ctx;                 // most context keys any round can see
   float* partial;              // scratch [nkv][nsplit][rows*G][hd + 2]

@@ -446,6 +446,76 @@ __global__ void __launch_bounds__(128) qkv_finish_kernel(float* acc, int ldacc, 
   }
 }
 
+// ---- the synthetic target's verify forward --------------------------------------
+// x[r] = E[tokens[r]]; a token outside the vocabulary reads row 0 and sets
+// kErrRange in rs.
+template <typename T>
+__global__ void embed_tokens_kernel(const T* E, int H, int vocab, const int* tokens, T* x, RoundState* rs) {
+  pdl_enter();
+  const int r = blockIdx.x;
+  int tok = tokens[r];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) atomicOr(&rs->error, kErrRange);
+    tok = 0;
+  }
+  const T* src = E + (size_t)tok * H;
+  T* dst = x + (size_t)r * H;
+  for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) copy8(src + i, dst + i);
+}
+
+// The verify block [anchor, d_1 .. d_{block-1}] from the drafter's round
+// state; the drafter's committed length must be the target's (kErrPos in trs
+// otherwise).
+__global__ void verify_tokens_kernel(const RoundState* drs, const RingState* dring, const int* d, int block,
+                                     int* tokens, const RingState* tring, RoundState* trs) {
+  pdl_enter();
+  for (int i = threadIdx.x; i < block; i += blockDim.x) tokens[i] = i == 0 ? drs->anchor : d[i - 1];
+  if (threadIdx.x == 0 && dring->offset != tring->offset) atomicOr(&trs->error, kErrPos);
+}
+
+// K and V of `rows` block rows (the finished QKV output: K at column kofs, V
+// at vofs of each row, nkv heads of hd) into the ring slots of positions
+// ring->offset + r; an append-only ring refuses rows past its capacity.
+template <typename T>
+__global__ void kv_rows_to_ring_kernel(const T* qkv, int ld, int kofs, int vofs, int rows, int nkv, int hd,
+                                       T* ring_k, T* ring_v, long long cap, int append_only, RingState* ring) {
+  pdl_enter();
+  const int chunks = hd / 8;
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= rows * nkv * chunks) return;
+  const int r = item / (nkv * chunks), h = (item / chunks) % nkv, c = item % chunks;
+  const long long pos = ring->offset + r;
+  if (append_only && pos - ring->base >= cap) {
+    if (c == 0) atomicOr(&ring->error, kErrFull);
+    return;
+  }
+  const long long slot = ring_slot(pos, cap);
+  const size_t src = (size_t)r * ld + (size_t)h * hd + c * 8;
+  const size_t dst = ((size_t)h * cap + slot) * hd + c * 8;
+  copy8(qkv + kofs + src, ring_k + dst);
+  copy8(qkv + vofs + src, ring_v + dst);
+}
+
+// The trim after a verify of `block` rows: every layer drops the last
+// block - n rows, n = *n_dev (the verify's accepted + 1); a and b are the
+// sliding and full layers' ring states (b may be NULL).
+__global__ void target_trim_kernel(RingState* a, RingState* b, const int* n_dev, int block, RoundState* trs) {
+  pdl_enter();
+  if (threadIdx.x != 0) return;
+  const int d = block - *n_dev;
+  RingState* rr[2] = {a, b};
+  for (int i = 0; i < 2; ++i) {
+    RingState* r = rr[i];
+    if (!r) continue;
+    if (d < 0 || d >= block || d > r->appended) {
+      atomicOr(&trs->error, kErrTrim);
+      continue;
+    }
+    r->offset -= d;
+    r->appended = 0;
+  }
+}
+
 // ---- ring bookkeeping ------------------------------------------------------------
 __global__ void ring_advance_kernel(RingState* ring, int d, int mode) {
   pdl_enter();
@@ -694,6 +764,46 @@ cudaError_t launch_qkv_finish(float* acc, int ldacc, void* out, int ldo, int row
   if (ldacc % 4 || ldo % 4) return cudaErrorInvalidValue;
   launch_pdl(qkv_finish_kernel, dim3((items + 3) / 4), dim3(128), 0, st, acc, ldacc, (bf16*)out, ldo, rows, nq,
              nkv, (const bf16*)qn, (const bf16*)kn, eps, rope, neox, tr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed_tokens(int dtype, const void* embed, int H, int vocab, const int* tokens, int rows,
+                                void* x, RoundState* rs, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (dtype)
+    launch_pdl(embed_tokens_kernel<bf16>, dim3(rows), dim3(256), 0, st, (const bf16*)embed, H, vocab, tokens,
+               (bf16*)x, rs);
+  else
+    launch_pdl(embed_tokens_kernel<float>, dim3(rows), dim3(256), 0, st, (const float*)embed, H, vocab, tokens,
+               (float*)x, rs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_tokens(const RoundState* drs, const RingState* dring, const int* d, int block,
+                                 int* tokens, const RingState* tring, RoundState* trs, cudaStream_t st) {
+  launch_pdl(verify_tokens_kernel, dim3(1), dim3(128), 0, st, drs, dring, d, block, tokens, tring, trs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_rows_to_ring(int dtype, const void* qkv, int ld, int kofs, int vofs, int rows, int nkv,
+                                   int hd, void* ring_k, void* ring_v, long long cap, int append_only,
+                                   RingState* ring, cudaStream_t st) {
+  const int items = rows * nkv * (hd / 8);
+  if (items <= 0) return cudaSuccess;
+  if (hd % 8 || ld % 8 || kofs % 8 || vofs % 8) return cudaErrorInvalidValue;
+  const dim3 grid((items + 127) / 128), blk(128);
+  if (dtype)
+    launch_pdl(kv_rows_to_ring_kernel<bf16>, grid, blk, 0, st, (const bf16*)qkv, ld, kofs, vofs, rows, nkv, hd,
+               (bf16*)ring_k, (bf16*)ring_v, cap, append_only, ring);
+  else
+    launch_pdl(kv_rows_to_ring_kernel<float>, grid, blk, 0, st, (const float*)qkv, ld, kofs, vofs, rows, nkv, hd,
+               (float*)ring_k, (float*)ring_v, cap, append_only, ring);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_target_trim(RingState* a, RingState* b, const int* n_dev, int block, RoundState* trs,
+                               cudaStream_t st) {
+  launch_pdl(target_trim_kernel, dim3(1), dim3(32), 0, st, a, b, n_dev, block, trs);
   return cudaGetLastError();
 }
 

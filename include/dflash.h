@@ -498,6 +498,80 @@ int dflash_short_conv_rollback(const void* prev_state, const void* bx, const int
                                int32_t layers, int32_t lcache, int32_t channels, int32_t block,
                                int32_t dtype, void* state_out, void* stream);
 
+/* ---- the synthetic target: a real verify forward ------------------------------ */
+
+/* A Qwen3-shaped causal decoder standing in for the target model [Muse "What
+ * changed", the Muse target: residual-stream capture before the final norm,
+ * trim rollback over the mixed sliding / full caches]. Layers have the
+ * drafter's layout (in_norm, Wq/Wk/Wv, per-head q/k norms + RoPE, Wo,
+ * post_norm, SwiGLU), with a causal mask: a sliding layer sees key j from
+ * query i iff 0 <= pos_i - pos_j <= window, a full layer iff pos_j <= pos_i.
+ * The sliding layers keep a ring of window + slack(max_block) rows, the full
+ * layers an append-only cache of max_context rows. */
+typedef struct dflash_target_config {
+  int32_t n_layers;        /* 1..64 */
+  int32_t hidden;          /* the drafter's target_hidden */
+  int32_t n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
+  int32_t window;          /* > 0: the sliding layers' window */
+  uint64_t full_layers;    /* bit l set: layer l is a full-attention layer */
+  int32_t n_capture;       /* 1..8: residual streams captured per row */
+  int32_t capture[8];      /* layer l: the residual stream after layer l, in
+                              this order (the drafter's k_target_layers
+                              streams) */
+  int32_t rope_neox;
+  int32_t max_block;       /* largest forward (2..32 rows) */
+  int32_t dtype;           /* DFLASH_F32 or DFLASH_BF16 */
+  int32_t max_context;     /* rows the full layers' caches hold */
+  float rope_theta;
+  float rms_eps;
+} dflash_target_config;
+
+typedef struct dflash_target_weights {
+  const void* embed;        /* [V, H] the raw embedding table (the drafter binds the same) */
+  const void* final_norm;   /* [H] */
+  const void* lm_head;      /* [V, H] untied (the drafter binds the same) */
+  const void* const* layers;/* HOST array of n_layers * DFLASH_LAYER_TENSORS device pointers */
+} dflash_target_weights;
+
+/* Creates a target (a dflash_ctx on which only the dflash_target_* calls,
+ * dflash_get_state, dflash_ctx_destroy, dflash_last_error and the ring
+ * accessors apply; drafting calls return EINVAL). Same conventions as
+ * dflash_ctx_create. EINVAL / ERANGE for a bad config (capture layers
+ * outside [0, n_layers), window <= 0, max_block outside [2, 32]). */
+int dflash_target_create(const dflash_target_config* cfg, const dflash_target_weights* w, void* stream,
+                         dflash_ctx** out);
+
+/* Forward of `rows` tokens (DEVICE int32 [rows]) at the positions after the
+ * target's committed length: appends their K/V to every layer's cache,
+ * writes the logits of the LAST logit_rows rows (DEVICE [logit_rows, V],
+ * storage dtype, no softcap; NULL when logit_rows == 0) and, when captured is
+ * not NULL, the captured residual rows (DEVICE [rows, n_capture * hidden],
+ * the streams in capture order). Used for the prompt prefill (chunks of up to
+ * max_block rows) and by dflash_target_verify. Enqueued only. EINVAL / ERANGE
+ * for bad arguments, EFULL when the full layers' caches may overflow. */
+int dflash_target_forward(dflash_ctx* target, const int32_t* tokens, int32_t rows, int32_t logit_rows,
+                          void* logits, void* captured);
+
+/* The verify forward of a round: the block [anchor, d_1 .. d_{block-1}] with
+ * the anchor read from the drafter's device state and draft_ids (DEVICE
+ * [block-1]); logits of every block row (DEVICE [block, V]) and the captured
+ * rows (DEVICE [block, n_capture * hidden]) that dflash_verify_accept and
+ * dflash_append_block then take. The drafter's committed length must equal
+ * the target's (device check: error bit 8 of the target's state). */
+int dflash_target_verify(dflash_ctx* target, const dflash_ctx* drafter, int32_t block,
+                         const int32_t* draft_ids, void* logits, void* captured);
+
+/* The trim after a verify of `block` rows: every layer's cache drops its
+ * last block - n rows, n = *n_dev (DEVICE int32: the verify's n = a + 1)
+ * [DSpark "Short-conv rollback": attention layers trim their KV cache]. A
+ * trim longer than the rows appended since the last one is refused on the
+ * device (error bit 16 of the target's state). Enqueued only. */
+int dflash_target_commit(dflash_ctx* target, const int32_t* n_dev, int32_t block);
+
+/* The full layers' cache (NULL when every layer slides); the sliding layers'
+ * ring is dflash_ring(target). */
+int dflash_target_full_ring(dflash_ctx* target, ring_cache** out);
+
 /* ---- ring KV cache (usable standalone) ---------------------------------------- */
 
 #define DFLASH_RING_UNFLOORED 1 /* test-only: size the slack by the unfloored

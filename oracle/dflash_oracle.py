@@ -673,12 +673,12 @@ def layer_window(tcfg, layer: int) -> int:
     return 0 if layer in tuple(tcfg["full_layers"]) else tcfg["window"]
 
 
-def target_forward(tcfg, tw, tokens, pos0, hist):
+def target_forward(tcfg, tw, tokens, pos0, hist, logit_rows=None):
     """The target's forward over ``tokens`` at positions pos0.. (readings
     R14-R16). ``hist`` holds per layer (K, V, positions) of the rows already
-    in its cache. Returns the logits [rows, V] (storage-rounded fp32, no
-    softcap), the captured residual rows [rows, len(capture) * H] and the
-    rows' per-layer K and V."""
+    in its cache. Returns the logits of the last ``logit_rows`` rows (all by
+    default) [.., V] (storage-rounded fp32, no softcap), the captured residual
+    rows [rows, len(capture) * H] and the rows' per-layer K and V."""
     rnd = rounder(tcfg["dtype"])
     toks = np.asarray(tokens, dtype=np.int64)
     pos = pos0 + np.arange(toks.size, dtype=np.int64)
@@ -692,6 +692,8 @@ def target_forward(tcfg, tw, tokens, pos0, hist):
         new_v.append(v)
     captured = np.concatenate([streams[l] for l in tcfg["capture"]], axis=1)
     xf = rnd(rmsnorm(x, tw["final_norm"], tcfg["rms_eps"]))
+    if logit_rows is not None:
+        xf = xf[xf.shape[0] - logit_rows:]
     logits = rnd(linear(xf, tw["lm_head"]).astype(np.float32).astype(np.float64))
     return {"logits": logits, "captured": captured, "k": new_k, "v": new_v, "positions": pos}
 
@@ -714,8 +716,8 @@ class TargetSession:
             self.hist = [(np.zeros((0, nkv, hd)), np.zeros((0, nkv, hd)), np.zeros(0, dtype=np.int64))
                          for _ in self.tw["layers"]]
 
-    def forward(self, tokens) -> dict:
-        out = target_forward(self.tcfg, self.tw, tokens, self.pos, self.hist)
+    def forward(self, tokens, logit_rows=None) -> dict:
+        out = target_forward(self.tcfg, self.tw, tokens, self.pos, self.hist, logit_rows)
         for li in range(len(self.hist)):
             hk, hv, hp = self.hist[li]
             self.hist[li] = (np.concatenate([hk, out["k"][li]]), np.concatenate([hv, out["v"][li]]),
