@@ -313,9 +313,9 @@ class Job:
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the lm_head
-# kernel at width 4 (ncu capture of this kernel version on this workload):
-# 831.16 MB read + 3.05 MB written.
-LMHEAD_TRAFFIC = 834_204_160
+# kernel at width 4 (ncu capture of this kernel version on this workload,
+# profiles/lmhead_argmax_muse_block4.md): 831.16 MB read + 3.24 MB written.
+LMHEAD_TRAFFIC = 834_399_488
 
 
 def lm_head_bytes(cfg, rows):
@@ -393,9 +393,25 @@ def kernel_breakdown(job, peak):
                 gbs = nb[cls] / (mean * 1e-6) / 1e9
                 e.update({"bytes": nb[cls], "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)})
             cl[cls] = e
-        out[str(w)] = {"traced_span_us": round((t1 - t0) / 1e3, 1), "classes": cl}
+        # the attention's phase marks (last CTA through each), after its
+        # dependency resolves, averaged over the layers
+        d = {name: (e, wr, x) for name, e, wr, x in tr}
+        ph = {"loaded": [], "scored": [], "softmax": [], "o_back": [], "exit": [], "merge_exit": []}
+        ok = lambda t: 0 < t < (1 << 63)
+        for name, _e, wr, x in tr:
+            if not name.endswith(".attn") or not ok(wr):
+                continue
+            s1, s2, s3 = d.get(name + ".1"), d.get(name + ".2"), d.get(name + ".3")
+            for key, t in (("loaded", s2[1]), ("scored", s2[2]), ("softmax", s3[1]), ("o_back", s3[2]),
+                           ("exit", x), ("merge_exit", s1[2])):
+                if ok(t):
+                    ph[key].append((t - wr) / 1e3)
+        out[str(w)] = {"traced_span_us": round((t1 - t0) / 1e3, 1), "classes": cl,
+                       "attn_phases_us": {k: round(statistics.mean(v), 2) for k, v in ph.items() if v}}
     return {"how": "kernel trace (globaltimer) of one captured round per width: per launch, "
-                   "dependency release to last CTA exit", "by_width": out}
+                   "dependency release to last CTA exit; attn_phases_us: the attention's last CTA "
+                   "through each phase, after its dependency resolves, mean over the layers",
+            "by_width": out}
 
 
 def _pools(B, ts, device):
