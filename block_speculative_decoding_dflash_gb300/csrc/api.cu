@@ -1058,6 +1058,7 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
   mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
   mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2;
   mk.grid = c->mk_grid;
+  mk.trace = ktrace_slot(c, "markov", mk.gamma);
   return launch_markov_chain(c->dt, mk, c->stream);
 }
 

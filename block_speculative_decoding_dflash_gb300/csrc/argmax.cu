@@ -259,17 +259,21 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
 }
 
 // ---- Markov chain step ---------------------------------------------------------------------
-// One launch per chain step (step j needs step j-1's argmax). A CTA takes
-// kMkCols vocabulary columns: its 256 threads are 64 groups of 8 columns x 4
-// quarters of the rank, so each thread issues r/4 independent 16-byte loads
-// of W2 (33.6 MB for the DSpark head, resident in L2 after the first step),
-// then the quarters are summed in shared memory. Each CTA folds its best
-// (value, column) into one 64-bit key per step with an atomic maximum (the
-// order-preserving value bits above the inverted column); the last CTA
-// decodes it into out[j] and clears it.
+// One launch per chain step (step j needs step j-1's argmax). A step reads
+// all of W2 (33.6 MB for the DSpark head, resident in L2 after the first
+// step) and is bound by how many of those bytes are in flight: a CTA takes
+// kMkCols vocabulary columns with 16 groups of 8 columns x kMkParts slices
+// of the rank, and each thread requests all of its slice's rows (16 at r =
+// 256) before it uses any, so about the whole matrix is requested at once
+// (512 CTAs at V = 65536). The slices are summed in shared memory in slice
+// order. Each CTA folds its best (value, column) into one 64-bit key per step
+// with an atomic maximum (the order-preserving value bits above the inverted
+// column); the last CTA decodes it into out[j] and clears it.
 constexpr int kMkThreads = 256;
-constexpr int kMkQuarters = 4;
-constexpr int kMkCols = (kMkThreads / kMkQuarters) * 8;
+constexpr int kMkParts = 16;
+constexpr int kMkGroups = kMkThreads / kMkParts;
+constexpr int kMkCols = kMkGroups * 8;
+constexpr int kMkBatch = 16;                  // W2 rows a thread has in flight at once
 
 __device__ __forceinline__ unsigned long long mk_key(float v, int i) {
   const uint32_t u = __float_as_uint(v + 0.0f);
@@ -279,11 +283,12 @@ __device__ __forceinline__ unsigned long long mk_key(float v, int i) {
 
 template <typename T>
 __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, int j) {
+  const KTrace tr{a.trace.p, a.trace.slot + j};
+  if (threadIdx.x == 0) ktrace_mark(tr, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(tr, 1);
   extern __shared__ float w1s[];               // [r]
-  __shared__ float part[kMkQuarters][kMkThreads / kMkQuarters][8];
-  __shared__ float sv[kMkThreads / 32];
-  __shared__ int si[kMkThreads / 32];
+  __shared__ float part[kMkParts][kMkGroups][8];
   int prev;
   if (j == 0) prev = a.anchor_host >= 0 ? a.anchor_host : a.rs->anchor;
   else prev = a.out[j - 1];
@@ -291,44 +296,69 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
   const T* w1 = reinterpret_cast<const T*>(a.w1) + (size_t)prev * a.r;
   for (int q = threadIdx.x; q < a.r; q += blockDim.x) w1s[q] = to_f(w1[q]);
   __syncthreads();
-  const int grp = threadIdx.x % (kMkThreads / kMkQuarters), qt = threadIdx.x / (kMkThreads / kMkQuarters);
+  const int grp = threadIdx.x % kMkGroups, pt = threadIdx.x / kMkGroups;
   const int c = blockIdx.x * kMkCols + grp * 8;
-  const int rq = (a.r + kMkQuarters - 1) / kMkQuarters;
-  const int q0 = qt * rq, q1 = min(a.r, q0 + rq);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (c < a.V) {
     const T* w2 = reinterpret_cast<const T*>(a.w2) + c;
-#pragma unroll 8
-    for (int q = q0; q < q1; ++q) {
-      float wv[8];
-      load8(w2 + (size_t)q * a.V, wv);
-      const float s = w1s[q];
+    // rows pt, pt + kMkParts, ...: kMkBatch of them requested before use
+    for (int q0 = pt; q0 < a.r; q0 += kMkBatch * kMkParts) {
+      if constexpr (sizeof(T) == 2) {
+        // kept as packed bf16 until used: 4 registers a row
+        uint4 raw[kMkBatch];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(s, wv[e], acc[e]);
+        for (int b = 0; b < kMkBatch; ++b) {
+          const int q = q0 + b * kMkParts;
+          raw[b] = q < a.r ? __ldg(reinterpret_cast<const uint4*>(w2 + (size_t)q * a.V)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int b = 0; b < kMkBatch; ++b) {
+          const int q = q0 + b * kMkParts;
+          const float sc = q < a.r ? w1s[q] : 0.f;
+          const bf16* e8 = reinterpret_cast<const bf16*>(&raw[b]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc, __bfloat162float(e8[e]), acc[e]);
+        }
+      } else {
+        float wv[kMkBatch / 2][8];
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int b = 0; b < kMkBatch / 2; ++b) {
+            const int q = q0 + (h * kMkBatch / 2 + b) * kMkParts;
+            if (q < a.r) load8(w2 + (size_t)q * a.V, wv[b]);
+          }
+#pragma unroll
+          for (int b = 0; b < kMkBatch / 2; ++b) {
+            const int q = q0 + (h * kMkBatch / 2 + b) * kMkParts;
+            if (q < a.r) {
+              const float sc = w1s[q];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc, wv[b][e], acc[e]);
+            }
+          }
+        }
+      }
     }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) part[qt][grp][e] = acc[e];
+  for (int e = 0; e < 8; ++e) part[pt][grp][e] = acc[e];
   __syncthreads();
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  if (qt == 0 && c < a.V) {
+  if (threadIdx.x < 32) {
+    // threads 0..15 sum their group's slices in slice order; the warp folds
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    const int cc = blockIdx.x * kMkCols + threadIdx.x * 8;
+    if (threadIdx.x < kMkGroups && cc < a.V) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float z = (part[0][grp][e] + part[1][grp][e]) + (part[2][grp][e] + part[3][grp][e]);
-      if (a.z) z = a.z[(size_t)j * a.ldz + c + e] + z;
-      if (better(z, c + e, bv, bi)) { bv = z; bi = c + e; }
+      for (int e = 0; e < 8; ++e) {
+        float z = 0.f;
+        for (int p = 0; p < kMkParts; ++p) z += part[p][threadIdx.x][e];
+        if (a.z) z = a.z[(size_t)j * a.ldz + cc + e] + z;
+        if (cc + e < a.V && better(z, cc + e, bv, bi)) { bv = z; bi = cc + e; }
+      }
     }
-  }
-  warp_argmax(bv, bi);
-  if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = bv; si[threadIdx.x >> 5] = bi; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    bv = sv[0];
-    bi = si[0];
-    for (int w = 1; w < kMkThreads / 32; ++w)
-      if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
-    atomicMax(a.key + j, mk_key(bv, bi));
+    warp_argmax(bv, bi);
+    if (threadIdx.x == 0) atomicMax(a.key + j, mk_key(bv, bi));
   }
   if (last_cta(a.counter, gridDim.x) && threadIdx.x == 0) {
     const unsigned long long key = atomicExch(a.key + j, 0ull);
@@ -336,6 +366,7 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
     a.out[j] = idx;
     if (a.out2) a.out2[j] = idx;
     *a.counter = 0u;
+    ktrace_mark(tr, 2);
   }
 }
 
@@ -398,6 +429,7 @@ cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st) {
+  if (a.V % 8) return cudaErrorInvalidValue;   // 8-column loads of W2 rows
   const size_t smem = sizeof(float) * a.r;
   for (int j = 0; j < a.gamma; ++j) {
     if (dtype) launch_pdl(markov_step_kernel<bf16>, dim3(a.grid), dim3(kMkThreads), smem, st, a, j);

@@ -333,6 +333,7 @@ struct MarkovArgs {
   unsigned long long* key;     // scratch [gamma] packed per-step maxima, zero between launches
   unsigned* counter;
   int grid;
+  KTrace trace;                // gamma slots: step j marks slot + j
 };
 cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st);
 int markov_grid(int V);
