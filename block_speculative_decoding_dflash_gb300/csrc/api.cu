@@ -169,7 +169,9 @@ struct dflash_ctx {
   float* mk_pv = nullptr;
   int* mk_pi = nullptr;
   int mk_grid = 0;
-  unsigned* counters = nullptr;  // [0] lm_head, [1] verify, [2] markov
+  unsigned* counters = nullptr;  // [0] lm_head, [1] verify, [2] markov, [4..5] markov grid barrier
+  bool mk_coop = false;          // the Markov chain in one cooperative launch (W2 fits shared memory)
+  int mk_coop_grid = 0;
   float* maxv = nullptr;
   int* backbone_ids = nullptr;
   float* zlog = nullptr;
@@ -888,6 +890,15 @@ int ctx_create_impl(const dflash_config* cfg, const dflash_weights* w, int32_t n
   c->lm_grid = lmhead_grid(c->V);
   c->vf_chunks = verify_chunks(c->V);
   c->mk_grid = markov_grid(c->V);
+  if (cfg->markov_rank > 0) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0 &&
+        markov_coop_ok(cfg->dtype, c->V, cfg->markov_rank, sms)) {
+      c->mk_coop = true;
+      c->mk_coop_grid = sms;
+    }
+  }
   size_t attn_floats = attention_scratch_floats(c->rows_max, c->nq, c->nkv, c->hd, c->max_ctx);
   const size_t attn_mma_floats = attention_mma_scratch_floats(c->rows_max, c->nq, c->nkv, c->max_ctx);
   if (attn_mma_floats > attn_floats) attn_floats = attn_mma_floats;
@@ -899,7 +910,7 @@ int ctx_create_impl(const dflash_config* cfg, const dflash_weights* w, int32_t n
       (size_t)c->ing_rows * c->H * E, (size_t)c->ing_rows * c->H * E,
       (size_t)c->ing_rows * 2 * c->kvdim * E * cfg->n_layers, (size_t)c->ing_rows * c->half * sizeof(float2),
       (size_t)c->lm_grid * R * 4, (size_t)c->lm_grid * R * 4, R * c->vf_chunks * 4,
-      R * c->vf_chunks * 4, R * 8, (size_t)c->mk_grid * 4, 4 * sizeof(unsigned),
+      R * c->vf_chunks * 4, R * 8, (size_t)c->mk_grid * 4, 8 * sizeof(unsigned),
       R * 4, R * 4, cfg->markov_add && cfg->markov_rank > 0 ? R * (size_t)c->V * 4 : 0,
       (size_t)kTcGrid * 2 * 2 * 32 * 128 * 4, (size_t)kTcTiles * 4, 64,
       (size_t)kTcGrid * 32 * 4, (size_t)kTcGrid * 32 * 4, 64,
@@ -1058,6 +1069,11 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
   mk.gamma = R; mk.out = draft_ids; mk.out2 = nullptr;
   mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2;
   mk.grid = c->mk_grid;
+  mk.bar = c->counters + 4; mk.err = c->tc_err;
+  if (c->mk_coop) {
+    mk.trace = ktrace_slot(c, "markov", 1);
+    return launch_markov_chain_coop(c->dt, mk, c->mk_coop_grid, c->stream);
+  }
   mk.trace = ktrace_slot(c, "markov", mk.gamma);
   return launch_markov_chain(c->dt, mk, c->stream);
 }
@@ -1318,7 +1334,9 @@ int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const floa
   mk.rs = c->rs; mk.anchor_host = anchor; mk.z = z; mk.ldz = c->V; mk.gamma = gamma;
   mk.out = out; mk.out2 = nullptr;
   mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2; mk.grid = c->mk_grid;
-  CK(c->err, launch_markov_chain(c->dt, mk, c->stream));
+  mk.bar = c->counters + 4; mk.err = c->tc_err;
+  if (c->mk_coop) CK(c->err, launch_markov_chain_coop(c->dt, mk, c->mk_coop_grid, c->stream));
+  else CK(c->err, launch_markov_chain(c->dt, mk, c->stream));
   return DFLASH_OK;
 }
 

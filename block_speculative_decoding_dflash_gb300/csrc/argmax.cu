@@ -10,6 +10,8 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "mma_sync.cuh"
+#include "ptx.cuh"
 #include "launch.cuh"
 
 namespace dfl {
@@ -370,7 +372,168 @@ __global__ void __launch_bounds__(kMkThreads) markov_step_kernel(MarkovArgs a, i
   }
 }
 
+// ---- the whole chain in one cooperative launch ------------------------------------------
+// CTA b holds W2's columns [b * cols, (b + 1) * cols) of every rank row in
+// shared memory (221 KB for the DSpark head on 152 SMs), loaded once before
+// the dependency resolves (W2 is a weight). Per step every CTA scores its
+// columns against W1[prev]: a warp takes 4 column groups of 8 x 8 slices of
+// the rank and sums the slices with shuffles (a fixed order); it folds its
+// best into key[j] with an atomic maximum; a grid barrier (all CTAs are
+// resident: cooperative launch; the wait is bounded and reports bit 64 in
+// err) makes the step's winner the next prev of every CTA.
+constexpr int kMkcThreads = 448;              // 14 warps x 4 groups = 56 groups of 8 columns
+constexpr int kMkcGroups = kMkcThreads / 32 * 4;
+constexpr int kMkcParts = 8;
+constexpr unsigned kMkcSpins = 1u << 22;
+
+__device__ __forceinline__ bool mkc_barrier(unsigned* count, unsigned* gen, unsigned nb, unsigned& g, int* err) {
+  __shared__ bool s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    const unsigned target = g + 1;
+    __threadfence();
+    if (atomicAdd(count, 1u) == nb - 1) {
+      atomicExch(count, 0u);
+      __threadfence();
+      atomicExch(gen, target);
+    } else {
+      unsigned spins = 0;
+      while (ld_acquire(gen) != target) {
+        if (++spins > kMkcSpins) { atomicOr(err, 64); ok = false; break; }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  g += 1;
+  __syncthreads();
+  return s_ok;
+}
+
+__global__ void __launch_bounds__(kMkcThreads, 1) markov_chain_coop_kernel(MarkovArgs a, int cols) {
+  extern __shared__ __align__(16) uint8_t mk_smem[];
+  bf16* w2s = reinterpret_cast<bf16*>(mk_smem);                         // [r][cols]
+  float* w1s = reinterpret_cast<float*>(mk_smem + (size_t)a.r * cols * 2);  // [r]
+  __shared__ float sv[kMkcThreads / 32];
+  __shared__ int si[kMkcThreads / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = blockIdx.x * cols;
+  const int ngran = cols / 8;
+  const bf16* w2 = reinterpret_cast<const bf16*>(a.w2);
+  for (int e = tid; e < a.r * ngran; e += blockDim.x) {
+    const int q = e / ngran, gcol = c0 + (e % ngran) * 8;
+    const bool valid = gcol < a.V;
+    cp_async16(w2s + (size_t)q * cols + (e % ngran) * 8, w2 + (size_t)q * a.V + (valid ? gcol : 0), valid);
+  }
+  unsigned g = ld_acquire(a.bar + 1);          // barrier generation at entry
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
+  pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
+  cp_async_wait_all();
+  // warp w: groups 4w .. 4w + 3; lane = group-in-warp + 4 * slice
+  const int gw = lane & 3, part = lane >> 2;
+  const int grp = warp * 4 + gw;
+  const int lc = grp * 8;                      // local column of this group
+  const bf16* w1 = reinterpret_cast<const bf16*>(a.w1);
+  int prev = a.anchor_host >= 0 ? a.anchor_host : a.rs->anchor;
+  for (int j = 0; j < a.gamma; ++j) {
+    if (prev < 0 || prev >= a.V) prev = 0;
+    for (int q = tid; q < a.r; q += blockDim.x) w1s[q] = __bfloat162float(w1[(size_t)prev * a.r + q]);
+    __syncthreads();
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (lc < cols) {
+      for (int q = part; q < a.r; q += kMkcParts) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(w2s + (size_t)q * cols + lc);
+        const bf16* e8 = reinterpret_cast<const bf16*>(&raw);
+        const float sc = w1s[q];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(sc, __bfloat162float(e8[e]), acc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 4);
+      acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 8);
+      acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+    }
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    const int cc = c0 + lc;
+    if (part == 0 && lc < cols) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (cc + e >= a.V) continue;
+        float z = acc[e];
+        if (a.z) z = a.z[(size_t)j * a.ldz + cc + e] + z;
+        if (better(z, cc + e, bv, bi)) { bv = z; bi = cc + e; }
+      }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+      bv = sv[0];
+      bi = si[0];
+      for (int w = 1; w < kMkcThreads / 32; ++w)
+        if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+      atomicMax(a.key + j, mk_key(bv, bi));
+    }
+    mkc_barrier(a.bar, a.bar + 1, gridDim.x, g, a.err);
+    const unsigned long long key = __ldcg(a.key + j);
+    prev = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+    if (blockIdx.x == 0 && tid == 0) {
+      a.out[j] = prev;
+      if (a.out2) a.out2[j] = prev;
+    }
+  }
+  // every CTA has read every key: clear them for the next chain
+  mkc_barrier(a.bar, a.bar + 1, gridDim.x, g, a.err);
+  if (blockIdx.x == 0)
+    for (int j = tid; j < a.gamma; j += blockDim.x) a.key[j] = 0ull;
+  if (blockIdx.x == 0 && tid == 0) ktrace_mark(a.trace, 2);
+}
+
 }  // namespace
+
+static int mkc_cols(int V, int grid) { return ((V + grid - 1) / grid + 7) / 8 * 8; }
+static size_t mkc_smem(int V, int r, int grid) { return (size_t)r * mkc_cols(V, grid) * 2 + (size_t)r * 4; }
+
+bool markov_coop_ok(int dtype, int V, int r, int grid) {
+  if (dtype != 1 || V % 8 || r < 1 || grid < 1) return false;
+  if (mkc_cols(V, grid) / 8 > kMkcGroups) return false;
+  const size_t smem = mkc_smem(V, r, grid);
+  if (smem > 227 * 1024) return false;
+  if (cudaFuncSetAttribute(markov_chain_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, markov_chain_coop_kernel, kMkcThreads, smem) !=
+      cudaSuccess)
+    return false;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return per_sm >= 1 && grid <= per_sm * sms;
+}
+
+cudaError_t launch_markov_chain_coop(int dtype, const MarkovArgs& a, int grid, cudaStream_t st) {
+  if (dtype != 1 || a.V % 8 || !a.bar || !a.err) return cudaErrorNotSupported;
+  const int cols = mkc_cols(a.V, grid);
+  if (cols / 8 > kMkcGroups) return cudaErrorNotSupported;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMkcThreads);
+  cfg.dynamicSmemBytes = mkc_smem(a.V, a.r, grid);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, markov_chain_coop_kernel, a, cols);
+}
 
 // Batch read-out: ids of every block row [nseq][rows] -> draft ids [nseq]
 // [rows - read0] (and the same for a second copy and the maxima).

@@ -334,8 +334,16 @@ struct MarkovArgs {
   unsigned* counter;
   int grid;
   KTrace trace;                // gamma slots: step j marks slot + j
+  unsigned* bar;               // [2] zeroed: grid barrier count and generation (one-launch chain)
+  int* err;                    // a barrier wait that gave up: bit 64
 };
 cudaError_t launch_markov_chain(int dtype, const MarkovArgs& a, cudaStream_t st);
+// The whole chain in one cooperative launch of `grid` CTAs (one per SM), W2
+// held in shared memory; cudaErrorNotSupported when W2 does not fit (the
+// caller then launches the chain step by step).
+cudaError_t launch_markov_chain_coop(int dtype, const MarkovArgs& a, int grid, cudaStream_t st);
+// Whether the one-launch chain fits this GPU for vocab V and rank r.
+bool markov_coop_ok(int dtype, int V, int r, int grid);
 int markov_grid(int V);
 
 struct SynthArgs {
