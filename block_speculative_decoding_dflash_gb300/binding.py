@@ -77,6 +77,7 @@ class RoundStateC(ctypes.Structure):
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 OPT_KERNEL_TRACE = 4
+OPT_MARKOV_STEPWISE = 8
 
 
 def _sig(name, res, *args):
@@ -442,6 +443,9 @@ class DFlashContext:
         o = _i64()
         self._check(lib.dflash_graph_kernel_count(self.h, slot, ctypes.byref(o)))
         return o.value
+
+    def set_option(self, option: int, value: int):
+        self._check(lib.dflash_set_option(self.h, option, value))
 
     def kernel_trace(self, enable: bool):
         """Stamp each launch of the per-operation draft (see kernel_trace_read)."""

@@ -171,6 +171,7 @@ struct dflash_ctx {
   int mk_grid = 0;
   unsigned* counters = nullptr;  // [0] lm_head, [1] verify, [2] markov, [4..5] markov grid barrier
   bool mk_coop = false;          // the Markov chain in one cooperative launch (W2 fits shared memory)
+  bool mk_stepwise = false;      // DFLASH_OPT_MARKOV_STEPWISE
   int mk_coop_grid = 0;
   float* maxv = nullptr;
   int* backbone_ids = nullptr;
@@ -1070,7 +1071,7 @@ cudaError_t draft_markov(dflash_ctx* c, int R, int32_t* draft_ids) {
   mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2;
   mk.grid = c->mk_grid;
   mk.bar = c->counters + 4; mk.err = c->tc_err;
-  if (c->mk_coop) {
+  if (c->mk_coop && !c->mk_stepwise) {
     mk.trace = ktrace_slot(c, "markov", 1);
     return launch_markov_chain_coop(c->dt, mk, c->mk_coop_grid, c->stream);
   }
@@ -1335,7 +1336,8 @@ int dflash_markov_chain(dflash_ctx* c, int32_t anchor, int32_t gamma, const floa
   mk.out = out; mk.out2 = nullptr;
   mk.key = reinterpret_cast<unsigned long long*>(c->mk_pv); mk.counter = c->counters + 2; mk.grid = c->mk_grid;
   mk.bar = c->counters + 4; mk.err = c->tc_err;
-  if (c->mk_coop) CK(c->err, launch_markov_chain_coop(c->dt, mk, c->mk_coop_grid, c->stream));
+  if (c->mk_coop && !c->mk_stepwise)
+    CK(c->err, launch_markov_chain_coop(c->dt, mk, c->mk_coop_grid, c->stream));
   else CK(c->err, launch_markov_chain(c->dt, mk, c->stream));
   return DFLASH_OK;
 }
@@ -1487,6 +1489,11 @@ int dflash_set_option(dflash_ctx* c, int32_t option, int64_t value) {
     c->ktr_on = value != 0;
     return DFLASH_OK;
   }
+  if (option == DFLASH_OPT_MARKOV_STEPWISE) {
+    if (value != 0 && value != 1) return fail(c->err, DFLASH_EINVAL, "option value %lld", (long long)value);
+    c->mk_stepwise = value != 0;
+    return DFLASH_OK;
+  }
   return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 
@@ -1514,6 +1521,7 @@ int dflash_get_option(dflash_ctx* c, int32_t option, int64_t* value) {
   if (!c) return DFLASH_EINVAL;
   if (!value) return fail(c->err, DFLASH_EINVAL, "value is NULL");
   if (option == DFLASH_OPT_KERNEL_TRACE) { *value = c->ktr_on ? 1 : 0; return DFLASH_OK; }
+  if (option == DFLASH_OPT_MARKOV_STEPWISE) { *value = c->mk_stepwise ? 1 : 0; return DFLASH_OK; }
   return fail(c->err, DFLASH_EINVAL, "unknown option %d", option);
 }
 

@@ -385,6 +385,11 @@ int dflash_graph_kernel_count(dflash_ctx* ctx, int32_t slot, int64_t* out_host);
  * latest CTA exit (allocates 6 KB on first use; 0 stops it). Read with
  * dflash_kernel_trace. */
 #define DFLASH_OPT_KERNEL_TRACE 4
+/* DFLASH_OPT_MARKOV_STEPWISE: 1 runs the DSpark Markov chain one launch per
+ * step instead of the one cooperative launch that holds W2 in shared memory
+ * (the fallback where W2 does not fit; same results); 0 (default) takes the
+ * cooperative launch where it fits. */
+#define DFLASH_OPT_MARKOV_STEPWISE 8
 /* EINVAL for an unknown option or value. Takes effect from the next call. */
 int dflash_set_option(dflash_ctx* ctx, int32_t option, int64_t value);
 int dflash_get_option(dflash_ctx* ctx, int32_t option, int64_t* value_host);

@@ -126,11 +126,15 @@ def test_muse_slab_stress_wraparound(H, muse):
 
 
 @pytest.mark.parametrize("add", [0, 1])
-def test_dspark_rounds(H, add):
+@pytest.mark.parametrize("stepwise", [0, 1])
+def test_dspark_rounds(H, add, stepwise):
+    """stepwise 1: the Markov chain one launch per step (the fallback of the
+    one cooperative launch)."""
     from block_speculative_decoding_dflash_gb300 import binding as B
     cfg = synth.config("dspark", markov_add=add, max_context=1024 + 4 * 10)
     w = synth.make_weights(cfg, 0)
     pair = H.Pair(cfg, weights=w, w64=H.f64_weights(w, "bf16"))
+    pair.ctx.set_option(B.OPT_MARKOV_STEPWISE, stepwise)
     pair.ingest(synth.make_context(cfg, 1024, seed=4), 0, anchor=999)
     stream = synth.make_target_stream(cfg, 4, 10, seed=4, logit_pool=2, resid_pool=4)
     for r, blk in enumerate((8, 10, 8, 10)):
