@@ -1173,6 +1173,7 @@ int dflash_verify_accept(dflash_ctx* c, const void* target_logits, int32_t block
   v.rs = c->rs; v.part_v = c->vf_pv; v.part_i = c->vf_pi; v.counter = c->vf_ctr;
   v.nseq = c->nseq;
   v.chunks = c->vf_chunks;
+  v.trace = ktrace_slot(c, "verify");
   CK(c->err, launch_verify(c->dt, v, c->stream));
   c->last_verify_block = block;
   c->last_tokens = tokens;
@@ -1577,6 +1578,7 @@ int dflash_synth_target(dflash_ctx* c, const void* logit_pool, const void* plant
   a.block_max = block_max; a.block = block; a.V = c->V; a.kin = c->kin;
   a.d = draft_ids; a.logits_out = logits_out; a.resid_out = resid_out; a.rs = c->rs;
   a.nseq = c->nseq;
+  a.trace = ktrace_slot(c, "synth_target");
   CK(c->err, launch_synth_target(c->dt, a, c->stream));
   return DFLASH_OK;
 }

@@ -174,7 +174,9 @@ constexpr int kMaxVerifyRows = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
   __shared__ float sv[8];
   __shared__ int si[8];
   __shared__ int t_s[kMaxVerifyRows];
@@ -256,6 +258,7 @@ __global__ void __launch_bounds__(256) verify_kernel(VerifyArgs a) {
       a.rs->a = acc;
       a.rs->bonus = t_s[acc];
       *a.counter = 0u;
+      ktrace_mark(a.trace, 2);
     }
   }
 }

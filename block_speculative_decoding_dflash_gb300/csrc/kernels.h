@@ -275,6 +275,7 @@ struct VerifyArgs {
   int nseq;                    // batch (0 or 1: one): sequence s at L + s [B, V], d + s [B-1],
                                // tokens + s [B], n + s, rs + s, partials + s [B * chunks],
                                // counter + s
+  KTrace trace;
 };
 cudaError_t launch_verify(int dtype, const VerifyArgs& a, cudaStream_t st);
 // Batch read-out: ids [nseq][rows - read0] = ids_all[s * rows + read0 + i]
@@ -356,6 +357,7 @@ struct SynthArgs {
   int vec;                     // set by the launcher: rows allow 16-byte copies
   int nseq;                    // batch: sequence s uses rs[s], d + s (block-1), outputs + s block
                                // rows, and pool entry (round * nseq + s)
+  KTrace trace;
 };
 cudaError_t launch_synth_target(int dtype, const SynthArgs& a, cudaStream_t st);
 

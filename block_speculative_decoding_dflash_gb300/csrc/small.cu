@@ -601,7 +601,9 @@ __global__ void ring_gather_kernel(const T* ring_k, const T* ring_v, int L,
 // ---- stand-in target -------------------------------------------------------------
 template <typename T>
 __global__ void synth_target_kernel(SynthArgs a) {
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   pdl_enter();
+  if (threadIdx.x == 0) ktrace_mark(a.trace, 1);
   // sequence blockIdx.z of a batch draws pool entry r * nseq + s
   const int sq = blockIdx.z;
   const long long r = a.rs[sq].rounds * a.nseq + sq;
@@ -647,6 +649,10 @@ __global__ void synth_target_kernel(SynthArgs a) {
     } else {
       for (int e = v; e < v + 8 && e < a.kin; ++e) Ro[e] = R[e];
     }
+  }
+  if (a.trace.p) {
+    __syncthreads();
+    if (threadIdx.x == 0) ktrace_mark(a.trace, 2);
   }
 }
 
