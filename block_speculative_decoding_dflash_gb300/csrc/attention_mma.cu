@@ -9,7 +9,8 @@
 // then takes two query rows' softmax over the split (P as a high and a low
 // bf16 part); each warp finally computes P V for 16 of the 128 output dims
 // over all the split's keys and writes them to the CTA's partial. Two to
-// four tiles: attn_tc_kernel (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
+// eight tiles: attn_tc_kernel (tcgen05.mma, below; more than eight: the
+// tile loop above). A combine kernel (one warp per (query, head)) then
 // merges the splits in split order and writes the bf16 output; nothing waits
 // on another CTA and the result is deterministic.
 //
@@ -282,6 +283,7 @@ constexpr int kTcBars = kTcVs + kKeys * kTcVsRow;
 constexpr size_t kTcAttnSmem = (size_t)kTcBars + 64 + 1024;
 constexpr int kTcOStride = kHd + 4;                  // O staging rows (floats), over K and V^T
 static_assert(kTileQ * kTcOStride * 4 <= 4 * kTcTileB, "O staging must fit in the K and V^T tiles");
+constexpr int kTileQWide = 128;            // queries per kv head of the wide variant
 
 // Byte offset of element (row, col) of a 128-row x 128-column bf16 operand
 // stored as two K-major 64-column tiles with 16-byte granules swizzled by row.
@@ -289,7 +291,14 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
   return (col >> 6) * kTcTileB + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2;
 }
 
+// WIDE: 65 to 128 queries, one operand row per query (row R = query R, P
+// rows over all 128 keys): warps w and w + 4 read the same TMEM lanes and
+// take keys 0-63 and 64-127 of those rows for the softmax; O needs no pair
+// sum and each thread stores its row's 64 dims of the partial directly.
+template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
+  constexpr int TQ = WIDE ? kTileQWide : kTileQ;     // queries held
+  constexpr int KPT = WIDE ? 64 : 32;                 // keys a thread takes in the softmax
   attn_select_seq(a, blockIdx.z, nsplit, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   if (!a.early_ctx) {
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kTcBars);     // [0] S ready, [1] O ready
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 2);
-  __shared__ float red_m[4][kTileQ], red_l[4][kTileQ];
+  __shared__ float red_m[4][TQ], red_l[4][TQ];
   const int s = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nq / a.nkv;
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     }
   }
   for (int e = threadIdx.x; e < 2 * kTileQ * (kHd / 8); e += blockDim.x) {
-    const int r = e >> 4, ch = e & 15, qr = r & (kTileQ - 1);
+    const int r = e >> 4, ch = e & 15, qr = WIDE ? r : (r & (kTileQ - 1));
     const bool valid = qr < Qn;
     const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
     cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
@@ -406,10 +415,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   }
 
   // thread: operand row R (TMEM lane), query qi = R mod 64, keys kc0 .. kc0 + 31
+  // (WIDE: query R, keys kc0 .. kc0 + 63)
   const int quad = warp & 3, half = warp >> 2;
-  const int R = quad * 32 + lane, qi = R & (kTileQ - 1), rh = R >> 6;
-  const int grp = rh * 2 + half;                       // which quarter of the keys
-  const int kc0 = grp * 32;
+  const int R = quad * 32 + lane, qi = WIDE ? R : (R & (kTileQ - 1)), rh = R >> 6;
+  const int grp = WIDE ? half : rh * 2 + half;         // which part of the keys
+  const int kc0 = grp * KPT;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   // visible keys of this query: kpos = kstart + kj within the window of its
   // position, kj < nk (0 <= lo, hi < nk)
@@ -428,13 +438,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   const float sl2 = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;   // scale * log2(e)
   bool ok = mbar_wait(&bar[0], 0);
   tc_fence_after();
-  float sv[32];
-  tmem_ld16(trow + kc0, &sv[0]);
-  tmem_ld16(trow + kc0 + 16, &sv[16]);
+  float sv[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT / 16; ++i) tmem_ld16(trow + kc0 + i * 16, &sv[i * 16]);
   tmem_ld_wait();
   float mrow = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
+  for (int c = 0; c < KPT; ++c) {
     const int kj = j0 + kc0 + c;
     sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sl2 : -INFINITY;
     mrow = fmaxf(mrow, sv[c]);
@@ -443,11 +453,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   __syncthreads();
   attn_phase(a.trace, 1);                          // S read back
 
-  const float M = fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
+  const float M = WIDE ? fmaxf(red_m[0][qi], red_m[1][qi])
+                       : fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
   float l = 0.f;
-  uint32_t pk[16], pr[16];
+  uint32_t pk[KPT / 2], pr[KPT / 2];
 #pragma unroll
-  for (int c = 0; c < 32; c += 2) {
+  for (int c = 0; c < KPT; c += 2) {
     const float p0 = (M == -INFINITY || sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - M);
     const float p1 = (M == -INFINITY || sv[c + 1] == -INFINITY) ? 0.f : exp2f(sv[c + 1] - M);
     l += p0 + p1;
@@ -457,17 +468,29 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   red_l[grp][qi] = l;
   // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
   // over the same granules of the other tile; the high bf16 part in Q's
-  // tiles, the low part in K's (K is no longer read once S is done)
+  // tiles, the low part in K's (K is no longer read once S is done). WIDE:
+  // its 64 keys, the whole of tile `half` in row R.
+  if (WIDE) {
 #pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    const int gg = half * 4 + gi;
-    const int at = R * 128 + ((gg ^ (R & 7)) << 4);
-    *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + at) =
-        make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
-    *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(sm + kTcK + rh * kTcTileB + at) =
-        make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
-    *reinterpret_cast<uint4*>(sm + kTcK + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+    for (int gg = 0; gg < 8; ++gg) {
+      const int at = R * 128 + ((gg ^ (R & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + kTcQ + half * kTcTileB + at) =
+          make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
+      *reinterpret_cast<uint4*>(sm + kTcK + half * kTcTileB + at) =
+          make_uint4(pr[4 * gg], pr[4 * gg + 1], pr[4 * gg + 2], pr[4 * gg + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const int gg = half * 4 + gi;
+      const int at = R * 128 + ((gg ^ (R & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + at) =
+          make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
+      *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sm + kTcK + rh * kTcTileB + at) =
+          make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
+      *reinterpret_cast<uint4*>(sm + kTcK + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   fence_proxy_async_shared();
   tc_fence_before();
@@ -497,6 +520,31 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
 #pragma unroll
   for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
   tmem_ld_wait();
+  if (WIDE) {
+    // row R is query R's whole sum: its 64 dims straight into the partial,
+    // with the row's maximum (natural-log units) and sum
+    if (qi < Qn) {
+      float* out = part + (size_t)qi * kPartStride;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float4*>(out + half * 64 + 4 * i) =
+            make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+      if (half == 0) {
+        out[kHd] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+        out[kHd + 1] = red_l[0][qi] + red_l[1][qi];
+      }
+    }
+    if (!ok && lane == 0) atomicOr(a.err, 32);
+    tc_fence_before();
+    __syncthreads();
+    attn_phase(a.trace, 3);                        // O read back
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 256);
+    }
+    if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
+    return;
+  }
   float* ost = reinterpret_cast<float*>(sm + kTcK) + qi * kTcOStride + half * 64;
   if (rh == 0) {
 #pragma unroll
@@ -548,10 +596,15 @@ bool attention_mma_ok(int dtype, int hd) { return dtype == 1 && hd == kHd; }
 
 cudaError_t init_attention_mma_attrs() {
   // the largest shared-memory carveout, as the GEMMs around them
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kTcAttnSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcAttnSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(MmaSmem));
@@ -568,10 +621,13 @@ cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
   const int Qn = a.rows * (a.nq / a.nkv);
   // Two to four 16-query tiles per kv head: the tensor-core kernel (A/B on
   // one GB300 at 64 queries per kv head: 16 us per draft faster than an
-  // mma.sync kernel with the split merge folded in). One tile: the 8-warp key
-  // split on mma.sync.
+  // mma.sync kernel with the split merge folded in); five to eight: its
+  // one-row-per-query variant. One tile, or more than eight: mma.sync.
   if (Qn > 16 && Qn <= kTileQ) {
-    cudaError_t e = launch_pdl(attn_tc_kernel, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
+    cudaError_t e = launch_pdl(attn_tc_kernel<false>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
+    if (e != cudaSuccess) return e;
+  } else if (Qn > kTileQ && Qn <= kTileQWide) {
+    cudaError_t e = launch_pdl(attn_tc_kernel<true>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = launch_pdl(attn_mma_kernel, grid, dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit);
