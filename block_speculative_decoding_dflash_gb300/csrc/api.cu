@@ -369,17 +369,21 @@ void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMa
 // encoded with 32-row boxes (bn_of of the whole row count).
 cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
   if (a.M <= 32) return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
+  // More rows: groups of up to 128 in one launch each (the weights stream
+  // once per group), X read as boxes of 32 rows (the map's box), so a last
+  // group of 32 rows or fewer runs at 32.
   if (a.epi != kEpiRed && a.epi != kEpiRedPair && a.epi != kEpiArgmax) return cudaErrorInvalidValue;
-  for (int r0 = 0; r0 < a.M; r0 += 32) {
+  for (int r0 = 0; r0 < a.M; r0 += 128) {
     TcGemmArgs g = a;
-    g.M = a.M - r0 < 32 ? a.M - r0 : 32;
+    g.M = a.M - r0 < 128 ? a.M - r0 : 128;
     g.b_row0 = a.b_row0 + r0;
     if (g.acc) g.acc += (size_t)r0 * a.ldacc;
     if (g.ids) g.ids += r0;
     if (g.ids2) g.ids2 += r0;
     if (g.maxv) g.maxv += r0;
     if (a.epi == kEpiArgmax) g.whole_tiles = g.M > 8;
-    const cudaError_t e = launch_tc_gemm(g, 32, c->num_sms, true, c->stream);
+    const int bn = g.M <= 32 ? 32 : g.M <= 64 ? 64 : 128;
+    const cudaError_t e = launch_tc_gemm(g, bn, c->num_sms, true, c->stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

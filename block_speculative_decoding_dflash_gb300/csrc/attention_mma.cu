@@ -8,9 +8,9 @@
 // K^T, mask |q - k| <= W by absolute positions) into shared memory; each warp
 // then takes two query rows' softmax over the split (P as a high and a low
 // bf16 part); each warp finally computes P V for 16 of the 128 output dims
-// over all the split's keys and writes them to the CTA's partial. Two to
-// eight tiles: attn_tc_kernel (tcgen05.mma, below; more than eight: the
-// tile loop above). A combine kernel (one warp per (query, head)) then
+// over all the split's keys and writes them to the CTA's partial (the tile
+// loop serves any number of tiles; it runs for one). Two or more tiles:
+// attn_tc_kernel (tcgen05.mma, below). A combine kernel (one warp per (query, head)) then
 // merges the splits in split order and writes the bf16 output; nothing waits
 // on another CTA and the result is deterministic.
 //
@@ -291,10 +291,11 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
   return (col >> 6) * kTcTileB + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2;
 }
 
-// WIDE: 65 to 128 queries, one operand row per query (row R = query R, P
-// rows over all 128 keys): warps w and w + 4 read the same TMEM lanes and
-// take keys 0-63 and 64-127 of those rows for the softmax; O needs no pair
-// sum and each thread stores its row's 64 dims of the partial directly.
+// WIDE: more than 64 queries, in chunks of 128 over the same K and V^T, one
+// operand row per query (row R = query R of the chunk, P rows over all 128
+// keys): warps w and w + 4 read the same TMEM lanes and take keys 0-63 and
+// 64-127 of those rows for the softmax; O needs no pair sum and each thread
+// stores its row's 64 dims of the partial directly.
 template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
   constexpr int TQ = WIDE ? kTileQWide : kTileQ;     // queries held
@@ -394,191 +395,218 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   const uint32_t tmem = *tmem_holder;
   constexpr uint32_t idesc = idesc_bf16(128, 128);
   const uint32_t sbase = smem_u32(sm);
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_bf16(tmem, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
-                    smem_desc_sw128(sbase + kTcK + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
-    tc_commit(&bar[0]);
-  }
-  // V^T while S is computed: the lanes of a warp take consecutive keys of one
-  // 8-dim granule, so each of its stores fills part of one row (fenced for
-  // the tensor cores with P below)
-  for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
-    const int j = e & (kKeys - 1), ch = e >> 7;
-    const uint4 u = *reinterpret_cast<const uint4*>(sm + kTcVs + j * kTcVsRow + ch * 16);
-    const bf16* h = reinterpret_cast<const bf16*>(&u);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) *reinterpret_cast<bf16*>(sm + kTcVt + tc_sw128(ch * 8 + t, j)) = h[t];
-  }
-
-  // thread: operand row R (TMEM lane), query qi = R mod 64, keys kc0 .. kc0 + 31
-  // (WIDE: query R, keys kc0 .. kc0 + 63)
+  // WIDE: the queries in chunks of 128 over the same K and V^T; P's low part
+  // then goes into V's staging rows (free once V^T is built) so that K stays
+  // for the next chunk's scores.
+  const int nqc = WIDE ? (Qn + kTileQWide - 1) / kTileQWide : 1;
+  const int plo = WIDE ? kTcVs : kTcK;
+  static_assert(2 * kTcTileB <= kTcBars - kTcVs, "P's low part must fit in V's staging rows");
   const int quad = warp & 3, half = warp >> 2;
-  const int R = quad * 32 + lane, qi = WIDE ? R : (R & (kTileQ - 1)), rh = R >> 6;
+  const int R = quad * 32 + lane, rh = R >> 6;
   const int grp = WIDE ? half : rh * 2 + half;         // which part of the keys
   const int kc0 = grp * KPT;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  // visible keys of this query: kpos = kstart + kj within the window of its
-  // position, kj < nk (0 <= lo, hi < nk)
-  int lo = 0, hi = nk - 1;
-  if (qi >= Qn) {
-    lo = 1; hi = 0;
-  } else {
-    const long long rel = p + qi / G - kstart;           // query position - kstart
-    if (window > 0 && rel - window > lo) lo = static_cast<int>(rel - window);
-    if (a.causal) {
-      if (rel < hi) hi = static_cast<int>(rel);
-    } else if (window > 0 && rel + window < hi) {
-      hi = static_cast<int>(rel + window);
-    }
-  }
   const float sl2 = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;   // scale * log2(e)
-  bool ok = mbar_wait(&bar[0], 0);
-  tc_fence_after();
-  float sv[KPT];
-#pragma unroll
-  for (int i = 0; i < KPT / 16; ++i) tmem_ld16(trow + kc0 + i * 16, &sv[i * 16]);
-  tmem_ld_wait();
-  float mrow = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < KPT; ++c) {
-    const int kj = j0 + kc0 + c;
-    sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sl2 : -INFINITY;
-    mrow = fmaxf(mrow, sv[c]);
-  }
-  red_m[grp][qi] = mrow;
-  __syncthreads();
-  attn_phase(a.trace, 1);                          // S read back
-
-  const float M = WIDE ? fmaxf(red_m[0][qi], red_m[1][qi])
-                       : fmaxf(fmaxf(red_m[0][qi], red_m[1][qi]), fmaxf(red_m[2][qi], red_m[3][qi]));
-  float l = 0.f;
-  uint32_t pk[KPT / 2], pr[KPT / 2];
-#pragma unroll
-  for (int c = 0; c < KPT; c += 2) {
-    const float p0 = (M == -INFINITY || sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - M);
-    const float p1 = (M == -INFINITY || sv[c + 1] == -INFINITY) ? 0.f : exp2f(sv[c + 1] - M);
-    l += p0 + p1;
-    pk[c >> 1] = pack_bf16(p0, p1);
-    pr[c >> 1] = pack_bf16_residue(p0, p1);
-  }
-  red_l[grp][qi] = l;
-  // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
-  // over the same granules of the other tile; the high bf16 part in Q's
-  // tiles, the low part in K's (K is no longer read once S is done). WIDE:
-  // its 64 keys, the whole of tile `half` in row R.
-  if (WIDE) {
-#pragma unroll
-    for (int gg = 0; gg < 8; ++gg) {
-      const int at = R * 128 + ((gg ^ (R & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + kTcQ + half * kTcTileB + at) =
-          make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
-      *reinterpret_cast<uint4*>(sm + kTcK + half * kTcTileB + at) =
-          make_uint4(pr[4 * gg], pr[4 * gg + 1], pr[4 * gg + 2], pr[4 * gg + 3]);
+  bool ok = true;
+  for (int qc = 0; qc < nqc; ++qc) {
+    if (qc > 0) {
+      // the next 128 queries into Q's tiles (the last P V is done with them)
+      for (int e = threadIdx.x; e < kTileQWide * (kHd / 8); e += blockDim.x) {
+        const int r = e >> 4, ch = e & 15, qr = qc * kTileQWide + r;
+        const bool valid = qr < Qn;
+        const size_t off = valid ? (size_t)(qr / G) * ldq + (size_t)(qr % G) * kHd + ch * 8 : 0;
+        cp_async16(sm + kTcQ + tc_sw128(r, ch * 8), qg + off, valid);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_shared();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
-  } else {
+    if (threadIdx.x == 0) {
 #pragma unroll
-    for (int gi = 0; gi < 4; ++gi) {
-      const int gg = half * 4 + gi;
-      const int at = R * 128 + ((gg ^ (R & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + at) =
-          make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
-      *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(sm + kTcK + rh * kTcTileB + at) =
-          make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
-      *reinterpret_cast<uint4*>(sm + kTcK + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tmem, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
+                      smem_desc_sw128(sbase + kTcK + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
+      tc_commit(&bar[0]);
     }
-  }
-  fence_proxy_async_shared();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  attn_phase(a.trace, 2);                          // P written
-  if (threadIdx.x == 0) {
+    if (qc == 0) {
+      // V^T while S is computed: the lanes of a warp take consecutive keys of
+      // one 8-dim granule, so each of its stores fills part of one row (fenced
+      // for the tensor cores with P below)
+      for (int e = threadIdx.x; e < kKeys * (kHd / 8); e += blockDim.x) {
+        const int j = e & (kKeys - 1), ch = e >> 7;
+        const uint4 u = *reinterpret_cast<const uint4*>(sm + kTcVs + j * kTcVsRow + ch * 16);
+        const bf16* h = reinterpret_cast<const bf16*>(&u);
 #pragma unroll
-    for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
-                    smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
-#pragma unroll
-    for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcK + kc * kTcTileB + kk * 32),
-                    smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, 1u);
-    tc_commit(&bar[1]);
-  }
-  // O: rows R and R + 64 hold the two halves of query qi's sum; each thread
-  // reads 64 dims of its row, the low rows store them, the high rows add
-  ok = mbar_wait(&bar[1], 0) && ok;
-  tc_fence_after();
-  float ov[64];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
-  tmem_ld_wait();
-  if (WIDE) {
-    // row R is query R's whole sum: its 64 dims straight into the partial,
-    // with the row's maximum (natural-log units) and sum
-    if (qi < Qn) {
-      float* out = part + (size_t)qi * kPartStride;
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<float4*>(out + half * 64 + 4 * i) =
-            make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-      if (half == 0) {
-        out[kHd] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
-        out[kHd + 1] = red_l[0][qi] + red_l[1][qi];
+        for (int t = 0; t < 8; ++t) *reinterpret_cast<bf16*>(sm + kTcVt + tc_sw128(ch * 8 + t, j)) = h[t];
       }
     }
-    if (!ok && lane == 0) atomicOr(a.err, 32);
+
+    // thread: operand row R (TMEM lane), query qi = R mod 64, keys kc0 .. kc0 + 31
+    // (WIDE: query qc * 128 + R, keys kc0 .. kc0 + 63)
+    const int qi = WIDE ? qc * kTileQWide + R : (R & (kTileQ - 1));
+    const int qs = WIDE ? R : qi;                        // its slot in red_m / red_l
+    // visible keys of this query: kpos = kstart + kj within the window of its
+    // position, kj < nk (0 <= lo, hi < nk)
+    int lo = 0, hi = nk - 1;
+    if (qi >= Qn) {
+      lo = 1; hi = 0;
+    } else {
+      const long long rel = p + qi / G - kstart;           // query position - kstart
+      if (window > 0 && rel - window > lo) lo = static_cast<int>(rel - window);
+      if (a.causal) {
+        if (rel < hi) hi = static_cast<int>(rel);
+      } else if (window > 0 && rel + window < hi) {
+        hi = static_cast<int>(rel + window);
+      }
+    }
+    ok = mbar_wait(&bar[0], static_cast<unsigned>(qc & 1)) && ok;
+    tc_fence_after();
+    float sv[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT / 16; ++i) tmem_ld16(trow + kc0 + i * 16, &sv[i * 16]);
+    tmem_ld_wait();
+    float mrow = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < KPT; ++c) {
+      const int kj = j0 + kc0 + c;
+      sv[c] = (kj >= lo && kj <= hi) ? sv[c] * sl2 : -INFINITY;
+      mrow = fmaxf(mrow, sv[c]);
+    }
+    red_m[grp][qs] = mrow;
+    __syncthreads();
+    if (qc == 0) attn_phase(a.trace, 1);             // S read back
+
+    const float M = WIDE ? fmaxf(red_m[0][qs], red_m[1][qs])
+                         : fmaxf(fmaxf(red_m[0][qs], red_m[1][qs]), fmaxf(red_m[2][qs], red_m[3][qs]));
+    float l = 0.f;
+    uint32_t pk[KPT / 2], pr[KPT / 2];
+#pragma unroll
+    for (int c = 0; c < KPT; c += 2) {
+      const float p0 = (M == -INFINITY || sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - M);
+      const float p1 = (M == -INFINITY || sv[c + 1] == -INFINITY) ? 0.f : exp2f(sv[c + 1] - M);
+      l += p0 + p1;
+      pk[c >> 1] = pack_bf16(p0, p1);
+      pr[c >> 1] = pack_bf16_residue(p0, p1);
+    }
+    red_l[grp][qs] = l;
+    // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
+    // over the same granules of the other tile; the high bf16 part in Q's
+    // tiles, the low part in K's (K is no longer read once S is done). WIDE:
+    // its 64 keys, the whole of tile `half` in row R; the low part in V's
+    // staging rows.
+    if (WIDE) {
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg) {
+        const int at = R * 128 + ((gg ^ (R & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + kTcQ + half * kTcTileB + at) =
+            make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
+        *reinterpret_cast<uint4*>(sm + plo + half * kTcTileB + at) =
+            make_uint4(pr[4 * gg], pr[4 * gg + 1], pr[4 * gg + 2], pr[4 * gg + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi) {
+        const int gg = half * 4 + gi;
+        const int at = R * 128 + ((gg ^ (R & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + kTcQ + rh * kTcTileB + at) =
+            make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
+        *reinterpret_cast<uint4*>(sm + kTcQ + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + plo + rh * kTcTileB + at) =
+            make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
+        *reinterpret_cast<uint4*>(sm + plo + (rh ^ 1) * kTcTileB + at) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async_shared();
     tc_fence_before();
     __syncthreads();
-    attn_phase(a.trace, 3);                        // O read back
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(tmem, 256);
+    tc_fence_after();
+    if (qc == 0) attn_phase(a.trace, 2);             // P written
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + kTcQ + kc * kTcTileB + kk * 32),
+                      smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, (kc | kk) ? 1u : 0u);
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tmem + 128, smem_desc_sw128(sbase + plo + kc * kTcTileB + kk * 32),
+                      smem_desc_sw128(sbase + kTcVt + kc * kTcTileB + kk * 32), idesc, 1u);
+      tc_commit(&bar[1]);
     }
-    if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
-    return;
-  }
-  float* ost = reinterpret_cast<float*>(sm + kTcK) + qi * kTcOStride + half * 64;
-  if (rh == 0) {
+    // O: rows R and R + 64 hold the two halves of query qi's sum; each thread
+    // reads 64 dims of its row, the low rows store them, the high rows add
+    // (WIDE: row R is query qi's whole sum)
+    ok = mbar_wait(&bar[1], static_cast<unsigned>(qc & 1)) && ok;
+    tc_fence_after();
+    float ov[64];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      *reinterpret_cast<float4*>(ost + 4 * i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-  }
-  __syncthreads();
-  attn_phase(a.trace, 3);                          // O read back
-  if (rh == 1) {
+    for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
+    tmem_ld_wait();
+    if (WIDE) {
+      // its 64 dims straight into the partial, with the row's maximum
+      // (natural-log units) and sum
+      if (qi < Qn) {
+        float* out = part + (size_t)qi * kPartStride;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float4 x = *reinterpret_cast<float4*>(ost + 4 * i);
-      x.x += ov[4 * i]; x.y += ov[4 * i + 1]; x.z += ov[4 * i + 2]; x.w += ov[4 * i + 3];
-      *reinterpret_cast<float4*>(ost + 4 * i) = x;
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float4*>(out + half * 64 + 4 * i) =
+              make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+        if (half == 0) {
+          out[kHd] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+          out[kHd + 1] = red_l[0][qs] + red_l[1][qs];
+        }
+      }
+      // S, O and Q's tiles, red_m and red_l free for the next chunk
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      continue;
+    }
+    float* ost = reinterpret_cast<float*>(sm + kTcK) + qi * kTcOStride + half * 64;
+    if (rh == 0) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float4*>(ost + 4 * i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+    }
+    __syncthreads();
+    attn_phase(a.trace, 3);                        // O read back
+    if (rh == 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float4 x = *reinterpret_cast<float4*>(ost + 4 * i);
+        x.x += ov[4 * i]; x.y += ov[4 * i + 1]; x.z += ov[4 * i + 2]; x.w += ov[4 * i + 3];
+        *reinterpret_cast<float4*>(ost + 4 * i) = x;
+      }
     }
   }
   if (!ok && lane == 0) atomicOr(a.err, 32);
   tc_fence_before();
   __syncthreads();
+  if (WIDE) attn_phase(a.trace, 3);                // O read back (every chunk)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
-  // the split's partial, one query row per warp pass (coalesced)
-  const float* osm = reinterpret_cast<const float*>(sm + kTcK);
-  for (int e = threadIdx.x; e < Qn * (kHd / 4); e += blockDim.x) {
-    const int q = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
-    float* out = part + (size_t)q * kPartStride;
-    *reinterpret_cast<float4*>(out + d4) = *reinterpret_cast<const float4*>(osm + q * kTcOStride + d4);
-    if (d4 == 0) {
-      // the row's maximum in natural-log units, as the merge expects
-      const float Mq = fmaxf(fmaxf(red_m[0][q], red_m[1][q]), fmaxf(red_m[2][q], red_m[3][q]));
-      out[kHd] = Mq == -INFINITY ? -INFINITY : Mq * 0.6931471805599453f;
-      out[kHd + 1] = (red_l[0][q] + red_l[1][q]) + (red_l[2][q] + red_l[3][q]);
+  if (!WIDE) {
+    // the split's partial, one query row per warp pass (coalesced)
+    const float* osm = reinterpret_cast<const float*>(sm + kTcK);
+    for (int e = threadIdx.x; e < Qn * (kHd / 4); e += blockDim.x) {
+      const int q = e / (kHd / 4), d4 = (e % (kHd / 4)) * 4;
+      float* out = part + (size_t)q * kPartStride;
+      *reinterpret_cast<float4*>(out + d4) = *reinterpret_cast<const float4*>(osm + q * kTcOStride + d4);
+      if (d4 == 0) {
+        // the row's maximum in natural-log units, as the merge expects
+        const float Mq = fmaxf(fmaxf(red_m[0][q], red_m[1][q]), fmaxf(red_m[2][q], red_m[3][q]));
+        out[kHd] = Mq == -INFINITY ? -INFINITY : Mq * 0.6931471805599453f;
+        out[kHd + 1] = (red_l[0][q] + red_l[1][q]) + (red_l[2][q] + red_l[3][q]);
+      }
     }
   }
   if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
@@ -621,12 +649,12 @@ cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
   const int Qn = a.rows * (a.nq / a.nkv);
   // Two to four 16-query tiles per kv head: the tensor-core kernel (A/B on
   // one GB300 at 64 queries per kv head: 16 us per draft faster than an
-  // mma.sync kernel with the split merge folded in); five to eight: its
-  // one-row-per-query variant. One tile, or more than eight: mma.sync.
+  // mma.sync kernel with the split merge folded in); five or more: its
+  // one-row-per-query variant, 128 queries at a time. One tile: mma.sync.
   if (Qn > 16 && Qn <= kTileQ) {
     cudaError_t e = launch_pdl(attn_tc_kernel<false>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
     if (e != cudaSuccess) return e;
-  } else if (Qn > kTileQ && Qn <= kTileQWide) {
+  } else if (Qn > kTileQ) {
     cudaError_t e = launch_pdl(attn_tc_kernel<true>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
     if (e != cudaSuccess) return e;
   } else {

@@ -37,7 +37,7 @@
 namespace dfl {
 namespace {
 
-constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+constexpr uint32_t tmem_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
 
 // A stage holds P consecutive K chunks of one tile (P = 2: each weight row
 // is read as 256 contiguous bytes per stage instead of 128, which lets HBM
@@ -53,10 +53,18 @@ struct Cfg {
 };
 
 
+// BN block rows: 16 or 32 for a draft block; 64 or 128 for more rows in one
+// launch (the fp32-sum and argmax epilogues only): the B tile is then loaded
+// as BN / 32 boxes of 32 rows, one MMA still covers all BN columns, and the
+// epilogue reads the accumulator 32 columns at a time.
 template <int BN, int EPI, int STAGES, int P>
 __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
   using C = Cfg<BN, NV, STAGES, P>;
+  constexpr int EC = BN < 32 ? BN : 32;           // block rows an epilogue pass takes (and a TMA box holds)
+  constexpr int NCH = BN / EC;
+  static_assert(NCH == 1 || EPI == kEpiRed || EPI == kEpiRedPair || EPI == kEpiArgmax,
+                "more than 32 block rows only for the fp32-sum and argmax epilogues");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
@@ -125,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       auto issue_b = [&](int st, unsigned u, int nc) {
         const int c = static_cast<int>(u % KC);
         uint8_t* sb = smem + (size_t)st * C::kStage + C::kBOff;
-        for (int k = 0; k < nc; ++k) tma_load_2d(sb + k * BN * 128, &a.b_map, (c + k) * 64, a.b_row0, &full[st]);
+        for (int k = 0; k < nc; ++k)
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch)
+            tma_load_2d(sb + k * BN * 128 + ch * EC * 128, &a.b_map, (c + k) * 64, a.b_row0 + ch * EC, &full[st]);
       };
       auto width = [&](unsigned u) {
         return (P == 2 && u + 1 < u1 && (u % KC) + 1 < KC) ? 2 : 1;
@@ -347,6 +358,65 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (NCH > 1) {
+        // 32 block rows at a time; every tile here is whole (the argmax) or
+        // needs no finish (the fp32 sums)
+        const int n = t * 128 + row;
+#pragma unroll 1
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int mo = ch * EC;
+          float acc[NV][EC];
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int j = 0; j < EC / 16; ++j)
+              tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * NV * BN + v * BN + mo + j * 16,
+                        &acc[v][j * 16]);
+          tmem_ld_wait();
+          if (ch == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+          }
+          if (EPI == kEpiRed || EPI == kEpiRedPair) {
+            if (n < a.N) {
+#pragma unroll
+              for (int v = 0; v < NV; ++v) {
+                float* dst = a.acc + (size_t)v * a.N + n;
+#pragma unroll
+                for (int m = 0; m < EC; ++m)
+                  if (mo + m < a.M) atomicAdd(dst + (size_t)(mo + m) * a.ldacc, acc[v][m]);
+              }
+            }
+          } else {
+            const bool valid = n < a.N;
+            const float cap = a.softcap;
+#pragma unroll
+            for (int m = 0; m < EC; ++m) {
+              if (mo + m >= a.M) continue;             // uniform
+              float z = acc[0][m];
+              if (cap > 0.f) z = cap * tanhf(z / cap);
+              float bv = valid ? z : -INFINITY;
+              int bi = valid ? n : 0x7fffffff;
+              warp_argmax(bv, bi);
+              if (lane == 0) { red_v[q][mo + m] = bv; red_i[q][mo + m] = bi; }
+            }
+            epi_sync();
+            if (threadIdx.x >= 64 && threadIdx.x < 64 + EC && mo + static_cast<int>(threadIdx.x) - 64 < a.M) {
+              const int m = mo + static_cast<int>(threadIdx.x) - 64;
+              float bv = best_v[m];
+              int bi = best_i[m];
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+                if (better(red_v[w][m], red_i[w][m], bv, bi)) { bv = red_v[w][m]; bi = red_i[w][m]; }
+              best_v[m] = bv;
+              best_i[m] = bi;
+            }
+            epi_sync();
+          }
+        }
+        u += c1 - c0;
+        continue;
+      }
       float acc[NV][BN];
 #pragma unroll
       for (int v = 0; v < NV; ++v)
@@ -417,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       }
     }
     if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 1}, 2);  // tiles published
+    // split tiles (one launch's block rows at most 32)
+    if constexpr (NCH == 1) {
     // Contributors whose partial loads are in flight at once: the long-K
     // GEMMs (residual, store) split a tile over about ten CTAs, the others
     // over two to four and need the registers for their epilogue.
@@ -486,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
         }
       }
     }
+    }
     if (a.trace.p && threadIdx.x == 64) ktrace_mark(KTrace{a.trace.p, a.trace.slot + 2}, 2);  // finished
     if (!ok) atomicOr(a.err, 4);
 
@@ -535,8 +608,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 // for the two-weight SwiGLU stages), which at up to 16 block rows holds most
 // of a CTA's weight range, requested before the programmatic dependency
 // resolves; the lm_head is long and takes a deeper ring.
+// With 64 or 128 block rows a stage's X sub-tiles grow to 8 or 16 KB: the
+// ring shrinks to what fits (48 / 64 KB stages, two weights: 80 / 96 KB).
 template <int BN, int EPI>
 constexpr int stages_for() {
+  if (BN == 64) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 4;
+  if (BN == 128) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 3;
   return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 3 : 4;
 }
 template <int BN, int EPI>
@@ -847,6 +924,12 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<32, kEpiRed>()) != cudaSuccess) return e;
   if ((e = attr_tc<16, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = attr_tc<32, kEpiRedPair>()) != cudaSuccess) return e;
+  if ((e = attr_tc<64, kEpiRed>()) != cudaSuccess) return e;
+  if ((e = attr_tc<64, kEpiRedPair>()) != cudaSuccess) return e;
+  if ((e = attr_tc<64, kEpiArgmax>()) != cudaSuccess) return e;
+  if ((e = attr_tc<128, kEpiRed>()) != cudaSuccess) return e;
+  if ((e = attr_tc<128, kEpiRedPair>()) != cudaSuccess) return e;
+  if ((e = attr_tc<128, kEpiArgmax>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -881,6 +964,19 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
   if (grid > want) grid = static_cast<int>(want);
   if (grid < 1) grid = 1;
   if (U * grid >= (1ll << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
+  if (bn == 64 || bn == 128) {
+    // more than 32 block rows: the fp32-sum and argmax epilogues, whole
+    // lm_head tiles
+    if (a.epi == kEpiArgmax && !a.whole_tiles) return cudaErrorInvalidValue;
+    switch (a.epi) {
+      case kEpiRed: return bn == 64 ? launch_tc<64, kEpiRed>(a, grid, pdl, st) : launch_tc<128, kEpiRed>(a, grid, pdl, st);
+      case kEpiRedPair:
+        return bn == 64 ? launch_tc<64, kEpiRedPair>(a, grid, pdl, st) : launch_tc<128, kEpiRedPair>(a, grid, pdl, st);
+      case kEpiArgmax:
+        return bn == 64 ? launch_tc<64, kEpiArgmax>(a, grid, pdl, st) : launch_tc<128, kEpiArgmax>(a, grid, pdl, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (bn == 16) {
     switch (a.epi) {
       case kEpiStore: return launch_tc<16, kEpiStore>(a, grid, pdl, st);
