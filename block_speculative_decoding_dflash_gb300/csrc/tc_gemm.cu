@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
   __shared__ int s_last;
   __shared__ float kv_ss[4][BN];
   __shared__ float kv_x[EPI == kEpiKVRing ? 128 * BN : 1];
+  // argmax over more than 32 block rows: each epilogue warp's 32 x 32 chunk
+  // of softcapped logits, transposed so that a lane scans one block row
+  __shared__ float tr_z[(EPI == kEpiArgmax && NCH > 1) ? 4 * 32 * 33 : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
@@ -388,18 +391,34 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
               }
             }
           } else {
+            // the warp's 32 vocabulary rows x 32 block rows through shared
+            // memory: lane m then scans block row mo + m over the 32 rows in
+            // index order (ties keep the lower index)
             const bool valid = n < a.N;
             const float cap = a.softcap;
+            float* tz = tr_z + q * 32 * 33;
 #pragma unroll
             for (int m = 0; m < EC; ++m) {
-              if (mo + m >= a.M) continue;             // uniform
               float z = acc[0][m];
               if (cap > 0.f) z = cap * tanhf(z / cap);
-              float bv = valid ? z : -INFINITY;
-              int bi = valid ? n : 0x7fffffff;
-              warp_argmax(bv, bi);
-              if (lane == 0) { red_v[q][mo + m] = bv; red_i[q][mo + m] = bi; }
+              tz[lane * 33 + m] = valid ? z : -INFINITY;
             }
+            __syncwarp();
+            {
+              float bv = -INFINITY;
+              int bi = 0x7fffffff;
+              const int n0 = t * 128 + q * 32;
+              if (mo + lane < a.M) {
+#pragma unroll 8
+                for (int l = 0; l < 32; ++l) {
+                  const float v = tz[l * 33 + lane];
+                  if (n0 + l < a.N && better(v, n0 + l, bv, bi)) { bv = v; bi = n0 + l; }
+                }
+              }
+              red_v[q][mo + lane] = bv;
+              red_i[q][mo + lane] = bi;
+            }
+            __syncwarp();
             epi_sync();
             if (threadIdx.x >= 64 && threadIdx.x < 64 + EC && mo + static_cast<int>(threadIdx.x) - 64 < a.M) {
               const int m = mo + static_cast<int>(threadIdx.x) - 64;
