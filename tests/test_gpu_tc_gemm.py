@@ -23,8 +23,8 @@ def B():
     return binding
 
 
-def _ctx(B, vocab, softcap=0.0, seed=0):
-    cfg = synth.config("muse", n_layers=1, vocab=vocab, mask_token_id=vocab - 1, max_block=32,
+def _ctx(B, vocab, softcap=0.0, seed=0, max_block=32):
+    cfg = synth.config("muse", n_layers=1, vocab=vocab, mask_token_id=vocab - 1, max_block=max_block,
                        softcap=softcap)
     w = synth.make_weights(cfg, seed)
     return B.DFlashContext(cfg, B.weights_to_device(w, "bf16")), w
@@ -99,9 +99,12 @@ def test_linear_residual_in_place(B):
 
 
 @pytest.mark.parametrize("vocab,rows,cap", [(202048, 3, 20.0), (202048, 15, 20.0), (65536, 9, 0.0),
-                                            (4096, 32, 0.0), (1000, 5, 20.0)])
+                                            (4096, 32, 0.0), (1000, 5, 20.0), (202048, 100, 20.0),
+                                            (65536, 64, 0.0), (4096, 129, 20.0)])
 def test_lm_head_argmax_matches_torch(B, vocab, rows, cap):
-    ctx, w = _ctx(B, vocab, softcap=cap)
+    """Up to 32 rows one launch of 16 or 32; 33-128 one launch of 64 or 128
+    rows (the accumulator read 32 columns at a time); 129 two launches."""
+    ctx, w = _ctx(B, vocab, softcap=cap, max_block=max(32, rows))
     lm = B.to_device(w["lm_head"], "bf16")
     g = torch.Generator(device="cuda").manual_seed(vocab + rows)
     x = torch.randn(rows, 2048, device="cuda", generator=g)
@@ -127,9 +130,10 @@ def test_lm_head_argmax_matches_torch(B, vocab, rows, cap):
     ctx.close()
 
 
-def test_lm_head_argmax_exact_ties_take_lowest_index(B):
-    vocab, rows = 202048, 4
-    cfg = synth.config("muse", n_layers=1, vocab=vocab, mask_token_id=vocab - 1, max_block=32)
+@pytest.mark.parametrize("rows", [4, 100])
+def test_lm_head_argmax_exact_ties_take_lowest_index(B, rows):
+    vocab = 202048
+    cfg = synth.config("muse", n_layers=1, vocab=vocab, mask_token_id=vocab - 1, max_block=max(32, rows))
     w = synth.make_weights(cfg, 1)
     ctx0 = B.DFlashContext(cfg, B.weights_to_device(w, "bf16"))
     g = torch.Generator(device="cuda").manual_seed(9)
@@ -141,11 +145,17 @@ def test_lm_head_argmax_exact_ties_take_lowest_index(B):
     first = ids.cpu().tolist()
     ctx0.close()
     lm = w["lm_head"].copy()
-    lows = []
+    lows, low_of, used = [], {}, set(first)
     for v in first:
-        lo = v // 3
-        lm[lo] = lm[v]               # an identical row at a lower index, in another tile
-        lows.append(lo)
+        if v not in low_of:
+            lo = v // 3
+            while lo in used:         # a lower index no other row's winner or copy uses
+                lo -= 1
+            assert lo >= 0
+            used.add(lo)
+            low_of[v] = lo
+            lm[lo] = lm[v]            # an identical row at a lower index, in another tile
+        lows.append(low_of[v])
     w2 = dict(w, lm_head=lm)
     ctx = B.DFlashContext(cfg, B.weights_to_device(w2, "bf16"))
     ctx.lm_head_argmax(x, rows, ids, mx)
