@@ -293,13 +293,13 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int col) {
 
 // WIDE: more than 64 queries, in chunks of 128 over the same K and V^T, one
 // operand row per query (row R = query R of the chunk, P rows over all 128
-// keys): warps w and w + 4 read the same TMEM lanes and take keys 0-63 and
-// 64-127 of those rows for the softmax; O needs no pair sum and each thread
-// stores its row's 64 dims of the partial directly.
+// keys), 16 warps: warps w, w + 4, w + 8, w + 12 read the same TMEM lanes and
+// take keys 0-31, ..., 96-127 of those rows for the softmax; O needs no pair
+// sum and each thread stores 32 dims of its row's partial directly.
 template <bool WIDE>
-__global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
+__global__ void __launch_bounds__((WIDE ? 2 : 1) * kWarps * 32) attn_tc_kernel(AttnArgs a, int nsplit) {
   constexpr int TQ = WIDE ? kTileQWide : kTileQ;     // queries held
-  constexpr int KPT = WIDE ? 64 : 32;                 // keys a thread takes in the softmax
+  constexpr int KPT = 32;                             // keys a thread takes in the softmax
   attn_select_seq(a, blockIdx.z, nsplit, 2, kPartStride);
   if (threadIdx.x == 0) ktrace_mark(a.trace, 0);
   if (!a.early_ctx) {
@@ -401,9 +401,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
   const int nqc = WIDE ? (Qn + kTileQWide - 1) / kTileQWide : 1;
   const int plo = WIDE ? kTcVs : kTcK;
   static_assert(2 * kTcTileB <= kTcBars - kTcVs, "P's low part must fit in V's staging rows");
-  const int quad = warp & 3, half = warp >> 2;
+  const int quad = warp & 3, half = warp >> 2;          // half: 0-1 (WIDE: 0-3)
   const int R = quad * 32 + lane, rh = R >> 6;
-  const int grp = WIDE ? half : rh * 2 + half;         // which part of the keys
+  const int grp = WIDE ? half : rh * 2 + half;         // which quarter of the keys
   const int kc0 = grp * KPT;
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const float sl2 = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;   // scale * log2(e)
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     }
 
     // thread: operand row R (TMEM lane), query qi = R mod 64, keys kc0 .. kc0 + 31
-    // (WIDE: query qc * 128 + R, keys kc0 .. kc0 + 63)
+    // (WIDE: query qc * 128 + R)
     const int qi = WIDE ? qc * kTileQWide + R : (R & (kTileQ - 1));
     const int qs = WIDE ? R : qi;                        // its slot in red_m / red_l
     // visible keys of this query: kpos = kstart + kj within the window of its
@@ -480,8 +480,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     __syncthreads();
     if (qc == 0) attn_phase(a.trace, 1);             // S read back
 
-    const float M = WIDE ? fmaxf(red_m[0][qs], red_m[1][qs])
-                         : fmaxf(fmaxf(red_m[0][qs], red_m[1][qs]), fmaxf(red_m[2][qs], red_m[3][qs]));
+    const float M = fmaxf(fmaxf(red_m[0][qs], red_m[1][qs]), fmaxf(red_m[2][qs], red_m[3][qs]));
     float l = 0.f;
     uint32_t pk[KPT / 2], pr[KPT / 2];
 #pragma unroll
@@ -496,16 +495,18 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     // P row R: this thread's 32 keys (tile rh, granules half*4 ..), and zeros
     // over the same granules of the other tile; the high bf16 part in Q's
     // tiles, the low part in K's (K is no longer read once S is done). WIDE:
-    // its 64 keys, the whole of tile `half` in row R; the low part in V's
-    // staging rows.
+    // only its own 32 keys (tile grp / 2, granules (grp % 2) * 4 ..) in row R,
+    // every key of the row being some thread's; the low part in V's staging
+    // rows.
     if (WIDE) {
 #pragma unroll
-      for (int gg = 0; gg < 8; ++gg) {
+      for (int gi = 0; gi < 4; ++gi) {
+        const int gg = (grp & 1) * 4 + gi;
         const int at = R * 128 + ((gg ^ (R & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm + kTcQ + half * kTcTileB + at) =
-            make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
-        *reinterpret_cast<uint4*>(sm + plo + half * kTcTileB + at) =
-            make_uint4(pr[4 * gg], pr[4 * gg + 1], pr[4 * gg + 2], pr[4 * gg + 3]);
+        *reinterpret_cast<uint4*>(sm + kTcQ + (grp >> 1) * kTcTileB + at) =
+            make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
+        *reinterpret_cast<uint4*>(sm + plo + (grp >> 1) * kTcTileB + at) =
+            make_uint4(pr[4 * gi], pr[4 * gi + 1], pr[4 * gi + 2], pr[4 * gi + 3]);
       }
     } else {
 #pragma unroll
@@ -546,21 +547,21 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
     ok = mbar_wait(&bar[1], static_cast<unsigned>(qc & 1)) && ok;
     tc_fence_after();
     float ov[64];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
-    tmem_ld_wait();
     if (WIDE) {
-      // its 64 dims straight into the partial, with the row's maximum
+      // its 32 dims straight into the partial, with the row's maximum
       // (natural-log units) and sum
+#pragma unroll
+      for (int i = 0; i < 2; ++i) tmem_ld16(trow + 128 + grp * 32 + i * 16, &ov[i * 16]);
+      tmem_ld_wait();
       if (qi < Qn) {
         float* out = part + (size_t)qi * kPartStride;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          *reinterpret_cast<float4*>(out + half * 64 + 4 * i) =
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(out + grp * 32 + 4 * i) =
               make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-        if (half == 0) {
+        if (grp == 0) {
           out[kHd] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
-          out[kHd + 1] = red_l[0][qs] + red_l[1][qs];
+          out[kHd + 1] = (red_l[0][qs] + red_l[1][qs]) + (red_l[2][qs] + red_l[3][qs]);
         }
       }
       // S, O and Q's tiles, red_m and red_l free for the next chunk
@@ -569,6 +570,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_tc_kernel(AttnArgs a, int ns
       tc_fence_after();
       continue;
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tmem_ld16(trow + 128 + half * 64 + i * 16, &ov[i * 16]);
+    tmem_ld_wait();
     float* ost = reinterpret_cast<float*>(sm + kTcK) + qi * kTcOStride + half * 64;
     if (rh == 0) {
 #pragma unroll
@@ -655,7 +659,7 @@ cudaError_t launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
     cudaError_t e = launch_pdl(attn_tc_kernel<false>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
     if (e != cudaSuccess) return e;
   } else if (Qn > kTileQ) {
-    cudaError_t e = launch_pdl(attn_tc_kernel<true>, grid, dim3(kWarps * 32), kTcAttnSmem, st, a, nsplit);
+    cudaError_t e = launch_pdl(attn_tc_kernel<true>, grid, dim3(2 * kWarps * 32), kTcAttnSmem, st, a, nsplit);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = launch_pdl(attn_mma_kernel, grid, dim3(kWarps * 32), sizeof(MmaSmem), st, a, nsplit);
