@@ -365,22 +365,24 @@ void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMa
 
 // More than 32 rows (wide verify blocks, batches): the finish-free GEMMs
 // (kEpiRed, kEpiRedPair) and the lm_head argmax run once per group of up to
-// 128 rows (64 or 128 block rows a launch), each launch streaming the
+// 128 rows (64 or 128 block rows a launch; 160 for kEpiRed), each launch streaming the
 // weights again; b_map must then have been encoded with 32-row boxes (bn_of
 // of the whole row count), which a last group of 32 rows or fewer also uses.
 cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
   if (a.M <= 32) return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
   if (a.epi != kEpiRed && a.epi != kEpiRedPair && a.epi != kEpiArgmax) return cudaErrorInvalidValue;
-  for (int r0 = 0; r0 < a.M; r0 += 128) {
+  // (one-weight fp32 sums: up to 160 rows in one launch)
+  const int group = a.epi == kEpiRed ? 160 : 128;
+  for (int r0 = 0; r0 < a.M; r0 += group) {
     TcGemmArgs g = a;
-    g.M = a.M - r0 < 128 ? a.M - r0 : 128;
+    g.M = a.M - r0 < group ? a.M - r0 : group;
     g.b_row0 = a.b_row0 + r0;
     if (g.acc) g.acc += (size_t)r0 * a.ldacc;
     if (g.ids) g.ids += r0;
     if (g.ids2) g.ids2 += r0;
     if (g.maxv) g.maxv += r0;
     if (a.epi == kEpiArgmax) g.whole_tiles = g.M > 8;
-    const int bn = g.M <= 32 ? 32 : g.M <= 64 ? 64 : 128;
+    const int bn = g.M <= 32 ? 32 : g.M <= 64 ? 64 : g.M <= 128 ? 128 : 160;
     const cudaError_t e = launch_tc_gemm(g, bn, c->num_sms, true, c->stream);
     if (e != cudaSuccess) return e;
   }

@@ -54,9 +54,10 @@ struct Cfg {
 
 
 // BN block rows: 16 or 32 for a draft block; 64 or 128 for more rows in one
-// launch (the fp32-sum and argmax epilogues only): the B tile is then loaded
-// as BN / 32 boxes of 32 rows, one MMA still covers all BN columns, and the
-// epilogue reads the accumulator 32 columns at a time.
+// launch (the fp32-sum and argmax epilogues only; 160 for the one-weight
+// fp32 sums): the B tile is then loaded as BN / 32 boxes of 32 rows, one MMA
+// still covers all BN columns, and the epilogue reads the accumulator 32
+// columns at a time.
 template <int BN, int EPI, int STAGES, int P>
 __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
@@ -633,6 +634,7 @@ template <int BN, int EPI>
 constexpr int stages_for() {
   if (BN == 64) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 4;
   if (BN == 128) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 3;
+  if (BN == 160) return 3;
   return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 3 : 4;
 }
 template <int BN, int EPI>
@@ -949,6 +951,7 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<128, kEpiRed>()) != cudaSuccess) return e;
   if ((e = attr_tc<128, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = attr_tc<128, kEpiArgmax>()) != cudaSuccess) return e;
+  if ((e = attr_tc<160, kEpiRed>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -983,6 +986,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
   if (grid > want) grid = static_cast<int>(want);
   if (grid < 1) grid = 1;
   if (U * grid >= (1ll << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
+  if (bn == 160) return a.epi == kEpiRed ? launch_tc<160, kEpiRed>(a, grid, pdl, st) : cudaErrorInvalidValue;
   if (bn == 64 || bn == 128) {
     // more than 32 block rows: the fp32-sum and argmax epilogues, whole
     // lm_head tiles
