@@ -365,14 +365,14 @@ void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMa
 
 // More than 32 rows (wide verify blocks, batches): the finish-free GEMMs
 // (kEpiRed, kEpiRedPair) and the lm_head argmax run once per group of up to
-// 128 rows (64 or 128 block rows a launch; 160 for kEpiRed), each launch streaming the
+// 128 rows (64 or 128 block rows a launch; 160 for the fp32 sums), each launch streaming the
 // weights again; b_map must then have been encoded with 32-row boxes (bn_of
 // of the whole row count), which a last group of 32 rows or fewer also uses.
 cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
   if (a.M <= 32) return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
   if (a.epi != kEpiRed && a.epi != kEpiRedPair && a.epi != kEpiArgmax) return cudaErrorInvalidValue;
-  // (one-weight fp32 sums: up to 160 rows in one launch)
-  const int group = a.epi == kEpiRed ? 160 : 128;
+  // (fp32 sums: up to 160 rows in one launch)
+  const int group = a.epi == kEpiArgmax ? 128 : 160;
   for (int r0 = 0; r0 < a.M; r0 += group) {
     TcGemmArgs g = a;
     g.M = a.M - r0 < group ? a.M - r0 : group;

@@ -48,16 +48,18 @@ struct Cfg {
   static constexpr int kSub = NV * kABytes;
   static constexpr int kBOff = P * kSub;
   static constexpr int kStage = P * (kSub + BN * 128);
-  static constexpr uint32_t kTmem = tmem_cols(2 * NV * BN);
+  // accumulator buffers in TMEM: two (the epilogue of one tile overlaps the
+  // next tile's MMAs) while they fit the 512 columns, else one
+  static constexpr int kBufs = 2 * NV * BN <= 512 ? 2 : 1;
+  static constexpr uint32_t kTmem = tmem_cols(kBufs * NV * BN);
   static constexpr size_t kSmem = (size_t)STAGES * kStage + 1024 + 512;
 };
 
 
 // BN block rows: 16 or 32 for a draft block; 64 or 128 for more rows in one
-// launch (the fp32-sum and argmax epilogues only; 160 for the one-weight
-// fp32 sums): the B tile is then loaded as BN / 32 boxes of 32 rows, one MMA
-// still covers all BN columns, and the epilogue reads the accumulator 32
-// columns at a time.
+// launch (the fp32-sum and argmax epilogues only; 160 for the fp32 sums):
+// the B tile is then loaded as BN / 32 boxes of 32 rows, one MMA still covers
+// all BN columns, and the epilogue reads the accumulator 32 columns at a time.
 template <int BN, int EPI, int STAGES, int P>
 __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   constexpr int NV = (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 1;
@@ -185,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       for (unsigned u = u0; u < u1 && ok; ++seg) {
         const int c0 = static_cast<int>(u % KC);
         const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
-        const int buf = seg & 1;
-        if (seg >= 2) ok = mbar_wait(&acc_empty[buf], static_cast<unsigned>((seg / 2 - 1) & 1));
+        const int buf = seg % C::kBufs;
+        if (seg >= C::kBufs) ok = mbar_wait(&acc_empty[buf], static_cast<unsigned>((seg / C::kBufs - 1) & 1));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * NV * BN;
@@ -355,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
       const int t = static_cast<int>(u / KC);
       const int c0 = static_cast<int>(u % KC);
       const int c1 = static_cast<int>(c0 + (u1 - u < KC - c0 ? u1 - u : KC - c0));
-      const int buf = seg & 1;
+      const int buf = seg % C::kBufs;
       const float gv = gain_of(t);
       float res[BN];
       resid_of(t, res);
-      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / 2) & 1));
+      ok = mbar_wait(&acc_full[buf], static_cast<unsigned>((seg / C::kBufs) & 1));
       if (!ok) break;
       tc_fence_after();
       if constexpr (NCH > 1) {
@@ -634,7 +636,7 @@ template <int BN, int EPI>
 constexpr int stages_for() {
   if (BN == 64) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 4;
   if (BN == 128) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 3;
-  if (BN == 160) return 3;
+  if (BN == 160) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 3;
   return EPI == kEpiArgmax ? (BN == 16 ? 6 : 5) : (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 3 : 4;
 }
 template <int BN, int EPI>
@@ -952,6 +954,7 @@ cudaError_t init_tc_attrs() {
   if ((e = attr_tc<128, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = attr_tc<128, kEpiArgmax>()) != cudaSuccess) return e;
   if ((e = attr_tc<160, kEpiRed>()) != cudaSuccess) return e;
+  if ((e = attr_tc<160, kEpiRedPair>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kWideSmem)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(tc_gemm_wide_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -986,7 +989,11 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, int bn, int grid, bool pdl, cuda
   if (grid > want) grid = static_cast<int>(want);
   if (grid < 1) grid = 1;
   if (U * grid >= (1ll << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
-  if (bn == 160) return a.epi == kEpiRed ? launch_tc<160, kEpiRed>(a, grid, pdl, st) : cudaErrorInvalidValue;
+  if (bn == 160) {
+    if (a.epi == kEpiRed) return launch_tc<160, kEpiRed>(a, grid, pdl, st);
+    if (a.epi == kEpiRedPair) return launch_tc<160, kEpiRedPair>(a, grid, pdl, st);
+    return cudaErrorInvalidValue;
+  }
   if (bn == 64 || bn == 128) {
     // more than 32 block rows: the fp32-sum and argmax epilogues, whole
     // lm_head tiles
