@@ -364,10 +364,11 @@ void tc_segments(TcGemmArgs& a, std::initializer_list<std::pair<const CUtensorMa
 }
 
 // More than 32 rows (wide verify blocks, batches): the finish-free GEMMs
-// (kEpiRed, kEpiRedPair) and the lm_head argmax run once per group of up to
-// 128 rows (64 or 128 block rows a launch; 160 for the fp32 sums), each launch streaming the
-// weights again; b_map must then have been encoded with 32-row boxes (bn_of
-// of the whole row count), which a last group of 32 rows or fewer also uses.
+// (kEpiRed, kEpiRedPair) run once per group of up to 160 rows and the lm_head
+// argmax once per group of up to 128 (64, 128 or 160 block rows a launch),
+// each launch streaming the weights again; b_map must then have been encoded
+// with 32-row boxes (bn_of of the whole row count), which a last group of 32
+// rows or fewer also uses.
 cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
   if (a.M <= 32) return launch_tc_gemm(a, bn_of(a.M), c->num_sms, true, c->stream);
   if (a.epi != kEpiRed && a.epi != kEpiRedPair && a.epi != kEpiArgmax) return cudaErrorInvalidValue;
@@ -390,8 +391,8 @@ cudaError_t tc_run(dflash_ctx* c, const TcGemmArgs& a) {
 }
 
 // The tensor-core path for `rows` block rows: up to 32 rows every GEMM of
-// the round; more in groups of up to 128, which needs the finish-free QKV of
-// the head_dim-128 attention.
+// the round; more in groups of up to 160 (128 for the argmax), which needs
+// the finish-free QKV of the head_dim-128 attention.
 bool tc_rows(const dflash_ctx* c, int rows) {
   return c->use_tc && (rows <= 32 || attention_mma_ok(c->dt, c->hd));
 }

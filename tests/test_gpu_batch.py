@@ -165,10 +165,23 @@ def muse(H):
 def test_muse_batched_rounds(H, muse, n_seq, block):
     """16 rows (four sequences of 4) and 32 rows (two of 16) on the tensor-core
     path: the weights stream once for the whole batch; 64 rows (four of 16):
-    the GEMMs in two groups of 32 rows."""
+    every GEMM in one launch of 64 block rows."""
     cfg, w, wd, w64 = muse
     b = Batch(H, dict(cfg, max_block=block), n_seq, w=w, w64=w64, wd=wd, ctx_rows=2048)
     for r in range(3):
         b.round(r, block)
+    b.check_rings(max_rows=32)
+    b.ctx.close()
+
+
+def test_muse_batched_rounds_past_one_launch(H, muse):
+    """176 rows (eleven sequences of 16): the fp32-sum GEMMs in groups of 160
+    and 16 block rows, the lm_head argmax in groups of 128 and 48, the
+    verify and the append over all 176 rows (a shorter context keeps the
+    eleven oracle sessions quick)."""
+    cfg, w, wd, w64 = muse
+    b = Batch(H, dict(cfg, max_block=16), 11, w=w, w64=w64, wd=wd, ctx_rows=256)
+    for r in range(2):
+        b.round(r, 16)
     b.check_rings(max_rows=32)
     b.ctx.close()
