@@ -39,6 +39,25 @@ __device__ __forceinline__ void attn_phase(const KTrace& t, int n) {
   if (t.p && threadIdx.x == 0) ktrace_mark(KTrace{t.p, t.slot + 2 + (n >> 1)}, 1 + (n & 1));
 }
 
+// This CTA's share of the two weights in a.l2_next (equal slices of their
+// concatenation, in 4 KB multiples), asked into L2 in pieces of at most 1 MB.
+__device__ __forceinline__ void attn_l2_prefetch_next(const AttnArgs& a) {
+  if (!a.l2_next[0] || threadIdx.x != 0) return;
+  const long long nct = (long long)gridDim.x * gridDim.y * gridDim.z;
+  const long long id = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+  const long long each = a.l2_next_bytes, total = 2 * each;
+  const long long per = ((total + nct - 1) / nct + 4095) & ~4095LL;
+  long long b0 = id * per;
+  const long long b1 = b0 + per < total ? b0 + per : total;
+  while (b0 < b1) {
+    const int w = b0 >= each ? 1 : 0;
+    const long long end = w ? b1 : (b1 < each ? b1 : each);
+    const long long n = end - b0 < (1 << 20) ? end - b0 : (1 << 20);
+    l2_prefetch_bulk(static_cast<const char*>(a.l2_next[w]) + (b0 - w * each), static_cast<uint32_t>(n));
+    b0 += n;
+  }
+}
+
 struct MmaSmem {
   bf16 k[kKeys][kHd + kPad];
   bf16 v[kKeys][kHd + kPad];
@@ -125,6 +144,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(AttnArgs a, int n
   cp_async_wait_all();
   __syncthreads();
   attn_phase(a.trace, 0);                          // K, V, q loaded
+  attn_l2_prefetch_next(a);
 
   const int grp = lane >> 2, tig = lane & 3;
   const float scale = rsqrtf(static_cast<float>(kHd));
@@ -359,6 +379,7 @@ __global__ void __launch_bounds__((WIDE ? 2 : 1) * kWarps * 32) attn_tc_kernel(A
       const int d = e % kPartStride;
       part[e] = d == kHd ? -INFINITY : 0.f;
     }
+    attn_l2_prefetch_next(a);
     if (a.trace.p) { __syncthreads(); if (threadIdx.x == 0) ktrace_mark(a.trace, 2); }
     return;
   }
@@ -392,6 +413,7 @@ __global__ void __launch_bounds__((WIDE ? 2 : 1) * kWarps * 32) attn_tc_kernel(A
   __syncthreads();
   tc_fence_after();
   attn_phase(a.trace, 0);                          // K, V, q loaded
+  attn_l2_prefetch_next(a);
   const uint32_t tmem = *tmem_holder;
   constexpr uint32_t idesc = idesc_bf16(128, 128);
   const uint32_t sbase = smem_u32(sm);

@@ -219,6 +219,12 @@ struct AttnArgs {
   // one is complete: the ring's context rows (and the ring state) may be read
   // before the attention's own dependency resolves.
   int early_ctx;
+  // The layer's gate and up weights (l2_next_bytes each, or null): every CTA
+  // asks L2 for its share of them once its own operands have landed, since
+  // HBM otherwise idles through the attention and its merge, and the gate/up
+  // GEMM two kernels later then streams them from L2.
+  const void* l2_next[2];
+  long long l2_next_bytes;
 };
 // Points a's per-sequence operands at sequence s: q, kb, vb, the ring and out
 // hold elements of esz bytes; partial rows are part_stride floats per query.
