@@ -56,8 +56,8 @@ struct Cfg {
 };
 
 
-// BN block rows: 16 or 32 for a draft block; 64 or 128 for more rows in one
-// launch (the fp32-sum and argmax epilogues only; 160 for the fp32 sums):
+// BN block rows: 16 or 32 for a draft block; 64, 128 or 160 for more rows in
+// one launch (the fp32-sum and argmax epilogues only; 160 for the sums):
 // the B tile is then loaded as BN / 32 boxes of 32 rows, one MMA still covers
 // all BN columns, and the epilogue reads the accumulator 32 columns at a time.
 template <int BN, int EPI, int STAGES, int P>
@@ -630,8 +630,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gemm_kernel(const __grid_const
 // for the two-weight SwiGLU stages), which at up to 16 block rows holds most
 // of a CTA's weight range, requested before the programmatic dependency
 // resolves; the lm_head is long and takes a deeper ring.
-// With 64 or 128 block rows a stage's X sub-tiles grow to 8 or 16 KB: the
-// ring shrinks to what fits (48 / 64 KB stages, two weights: 80 / 96 KB).
+// With 64, 128 or 160 block rows a stage's X sub-tiles grow to 8, 16 or
+// 20 KB: the ring shrinks to what fits (48 / 64 / 72 KB stages; two weights:
+// 80 / 96 / 104 KB). Single-chunk stages with deeper rings measured no
+// faster for the layer GEMMs and slower for the lm_head.
 template <int BN, int EPI>
 constexpr int stages_for() {
   if (BN == 64) return (EPI == kEpiSwiglu || EPI == kEpiRedPair) ? 2 : 4;
