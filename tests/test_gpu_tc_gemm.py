@@ -100,10 +100,11 @@ def test_linear_residual_in_place(B):
 
 @pytest.mark.parametrize("vocab,rows,cap", [(202048, 3, 20.0), (202048, 15, 20.0), (65536, 9, 0.0),
                                             (4096, 32, 0.0), (1000, 5, 20.0), (202048, 100, 20.0),
-                                            (65536, 64, 0.0), (4096, 129, 20.0)])
+                                            (65536, 64, 0.0), (4096, 129, 20.0), (65536, 300, 20.0)])
 def test_lm_head_argmax_matches_torch(B, vocab, rows, cap):
     """Up to 32 rows one launch of 16 or 32; 33-128 one launch of 64 or 128
-    rows (the accumulator read 32 columns at a time); 129 two launches."""
+    rows (the accumulator read 32 columns at a time); 129 two launches; 300
+    three (128, 128 and 44 rows, each writing its own rows' results)."""
     ctx, w = _ctx(B, vocab, softcap=cap, max_block=max(32, rows))
     lm = B.to_device(w["lm_head"], "bf16")
     g = torch.Generator(device="cuda").manual_seed(vocab + rows)
